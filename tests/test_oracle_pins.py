@@ -1,0 +1,373 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself:
+numbers the pages print, closed forms, invariants, special cases that reduce
+to a textbook result, and library routines on small shapes.  No GPU."""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name):
+    with open(os.path.join(GOLDEN, name)) as fh:
+        return [list(map(int, l.split())) for l in fh if l.strip() and not l.startswith("#")]
+
+
+# ---------------------------------------------------------------- sharding
+
+def test_shard_size_matches_pages_printed_sizes():
+    # block 368 MB -> DP2 shard 184 MB; Super 124 GB over DP4 -> 31 GB/rank
+    for total, dp, shard in _rows("overlap_analysis.txt"):
+        assert oracle.shard_numel(total, dp) == shard
+
+
+def test_shard_size_is_smallest_equal_split():
+    # Equal-size shards (all_gather_into_tensor needs them) with the least
+    # padding: s*S >= N and (S-1)*s < N.
+    for n in range(0, 200):
+        for s in range(1, 9):
+            S = oracle.shard_numel(n, s)
+            assert S * s >= n
+            assert n == 0 or (S - 1) * s < n
+
+
+@pytest.mark.parametrize("esize", [1, 2, 4])
+def test_shard_reassemble_brute_force(esize):
+    rng = np.random.default_rng(1)
+    for n in range(1, 65):
+        for s in range(1, 9):
+            flat = rng.integers(1, 256, size=n * esize, dtype=np.uint8)  # no zero bytes
+            shards = oracle.shard(flat, n, esize, s)
+            S = oracle.shard_numel(n, s)
+            assert all(len(x) == S * esize for x in shards)
+            gathered = oracle.reassemble(shards, S, esize)
+            # rank-order concatenation reproduces the flat buffer ...
+            assert np.array_equal(gathered[: n * esize], flat)
+            # ... and everything past it is zero padding
+            assert not gathered[n * esize:].any()
+            # shard r is exactly the r-th window of the concatenation
+            for r, x in enumerate(shards):
+                assert np.array_equal(x, gathered[r * S * esize:(r + 1) * S * esize])
+
+
+def test_shard_of_nonmultiple_pads_last_shard_only():
+    # 10 elements over 3 shards -> 4,4,4 with two zeros at the end of shard 2
+    flat = np.arange(1, 11, dtype=np.uint8)
+    sh = oracle.shard(flat, 10, 1, 3)
+    assert [list(x) for x in sh] == [[1, 2, 3, 4], [5, 6, 7, 8], [9, 10, 0, 0]]
+
+
+def test_flatten_groups_by_dtype_in_registration_order():
+    # params of two dtype codes interleaved; each group keeps registration order
+    a = np.array([1, 2], np.uint16).view(np.uint8)
+    b = np.array([3.0], np.float32).view(np.uint8)
+    c = np.array([4, 5, 6], np.uint16).view(np.uint8)
+    params = [(b, 1, 1), (a, 2, 0), (c, 3, 0)]
+    g0 = oracle.flatten_group(params, 0, 2).view(np.uint16)
+    g1 = oracle.flatten_group(params, 1, 4).view(np.float32)
+    assert list(g0) == [1, 2, 4, 5, 6]
+    assert list(g1) == [3.0]
+
+
+# closed forms of the shard lengths of the workloads: S_g = ceil(N_g / s)
+# with N_bf16 = 12 d^2 (d = hidden, f = 4d) and N_f32 = 8 d.
+@pytest.mark.parametrize("d,s,S_bf16,S_f32", [
+    (256, 2, 393_216, 1_024),
+    (1024, 3, 4_194_304, 2_731),
+    (3840, 4, 44_236_800, 7_680),
+    (6144, 2, 226_492_416, 24_576),
+])
+def test_workload_shard_lengths(d, s, S_bf16, S_f32):
+    assert oracle.shard_numel(12 * d * d, s) == S_bf16
+    assert oracle.shard_numel(8 * d, s) == S_f32
+
+
+def test_odd_workload_shards_are_misaligned_to_16_bytes():
+    # 3 shards of 2731 f32: 10924 bytes, 12 mod 16 -> shard 1 and 2 land at
+    # non-16-byte-aligned offsets of the gathered buffer.
+    S = oracle.shard_numel(8 * 1024, 3)
+    assert S * 3 - 8 * 1024 == 1
+    assert (S * 4) % 16 == 12
+
+
+def test_slot_layout_bases_and_sizes():
+    from layerwise_weight_offload_gb300 import workloads as W
+    w = W.CONFIGS["odd"]
+    descs = W.block_param_descs(w)
+    numels = [int(np.prod(sh)) for _, sh, _ in descs]
+    dtypes = [c for _, _, c in descs]
+    esizes = [W.ESIZE[c] for c in dtypes]
+    gdt, gbase, used = oracle.slot_layout(numels, dtypes, esizes, w.shards, 256)
+    # groups in order of first appearance: f32 (norm1.weight comes first), bf16
+    assert gdt == [W.F32, W.BF16]
+    assert gbase[0] == 0
+    f32_bytes = 3 * 2731 * 4
+    assert gbase[1] == (f32_bytes + 255) // 256 * 256
+    assert used == gbase[1] + 3 * 4_194_304 * 2
+    assert all(b % 256 == 0 for b in gbase)
+
+
+def test_slot_image_round_trip_small():
+    rng = np.random.default_rng(7)
+    numels = [5, 7, 3, 11]
+    dtypes = [1, 0, 1, 0]
+    esizes = [4, 2, 4, 2]
+    raw = [rng.integers(1, 256, size=n * e, dtype=np.uint8) for n, e in zip(numels, esizes)]
+    for s in range(1, 6):
+        image, gdt, gbase, used = oracle.slot_image(raw, numels, dtypes, esizes, s, 16)
+        # group 1 (code 1, f32) holds params 0 and 2 back to back
+        f32 = np.concatenate([raw[0], raw[2]])
+        assert np.array_equal(image[gbase[0]:gbase[0] + len(f32)], f32)
+        bf = np.concatenate([raw[1], raw[3]])
+        assert np.array_equal(image[gbase[1]:gbase[1] + len(bf)], bf)
+
+
+# ---------------------------------------------------------------- schedule
+
+def test_schedule_matches_hand_derived_golden():
+    got = oracle.schedule(3, 2)[:, :6].tolist()
+    assert got == _rows("schedule_n3_steps2.txt")
+
+
+@pytest.mark.parametrize("n", range(1, 10))
+@pytest.mark.parametrize("steps", range(1, 5))
+def test_schedule_closed_form_and_invariants(n, steps):
+    ev = oracle.schedule(n, steps)
+    for row in ev:
+        k, blk, rs, pb, ps, waits, viol = row.tolist()
+        assert blk == k % n
+        assert rs == k % 2                 # i%2 plus correction == global parity
+        assert ps == 1 - rs                # only two slots, never the one read
+        assert pb == (blk + 1) % n         # circular tail -> head prefetch
+        assert waits == (k - 1 if k > 0 else -1)
+        assert viol == 0
+
+
+@pytest.mark.parametrize("n", [3, 5, 7, 9])
+def test_odd_count_collides_without_correction(n):
+    # The pages: without _prefetched_slot tracking, the circular tail->head
+    # prefetch collides with the head's read slot for odd block counts.
+    ev = oracle.schedule(n, 2, use_correction=False)
+    assert (ev[:n, 6] == 0).all()          # first pass: i%2 alone is right
+    assert (ev[n:, 6] != 0).any()          # second pass: collision
+
+
+@pytest.mark.parametrize("n", [2, 4, 8])
+def test_even_count_needs_no_correction(n):
+    a = oracle.schedule(n, 3, use_correction=False)
+    b = oracle.schedule(n, 3, use_correction=True)
+    assert np.array_equal(a, b)
+    assert (a[:, 6] == 0).all()
+
+
+def test_at_most_two_blocks_resident():
+    for n in range(1, 10):
+        ev = oracle.schedule(n, 3)
+        holds = {0: 0, 1: None}
+        for row in ev:
+            _, blk, rs, pb, ps, _, _ = row.tolist()
+            assert holds[rs] == blk
+            holds[ps] = pb
+            assert len([v for v in holds.values() if v is not None]) <= 2
+
+
+# ---------------------------------------------------------------- block math
+
+def test_gelu_tanh_close_to_erf_gelu_and_odd_identity():
+    for z in np.linspace(-8, 8, 1601):
+        exact = 0.5 * z * (1 + math.erf(z / math.sqrt(2)))
+        g = oracle.gelu_tanh(z)
+        assert abs(g - exact) < 5e-4           # published accuracy of the tanh form
+        # tanh is odd, so gelu(z) - gelu(-z) = z exactly (up to rounding)
+        assert abs(g - oracle.gelu_tanh(-z) - z) < 1e-12 * max(1, abs(z))
+    assert oracle.gelu_tanh(0.0) == 0.0
+
+
+def test_rmsnorm_closed_forms():
+    d = 7
+    one = np.ones(d, np.float32)
+    zero = np.zeros(d, np.float32)
+    x = np.full((1, d), 3.0)
+    h = oracle.rmsnorm_mod(x, one, zero, zero, eps=1e-6)
+    assert np.allclose(h, 3.0 / math.sqrt(9.0 + 1e-6), rtol=0, atol=1e-15)
+    # scale = -1 or gain = 0 leaves only the shift
+    shift = np.arange(d, dtype=np.float32)
+    rng = np.random.default_rng(0)
+    xr = rng.standard_normal((4, d))
+    assert np.array_equal(oracle.rmsnorm_mod(xr, one, shift, -one), np.tile(shift, (4, 1)))
+    assert np.array_equal(oracle.rmsnorm_mod(xr, zero, shift, zero), np.tile(shift, (4, 1)))
+    # eps = 0: invariant to scaling the row; unit mean square
+    h1 = oracle.rmsnorm_mod(xr, one, zero, zero, eps=0.0)
+    h2 = oracle.rmsnorm_mod(5.0 * xr, one, zero, zero, eps=0.0)
+    assert np.allclose(h1, h2, atol=1e-13)
+    assert np.allclose((h1 ** 2).mean(axis=1), 1.0, atol=1e-13)
+    # scale doubles the normalised row: (1 + 1)
+    h3 = oracle.rmsnorm_mod(xr, one, zero, one, eps=0.0)
+    assert np.allclose(h3, 2 * h1, atol=1e-13)
+
+
+@pytest.mark.parametrize("rows,k,n", [(1, 1, 1), (3, 5, 7), (17, 33, 9), (64, 48, 80)])
+def test_linear_against_numpy_matmul(rows, k, n):
+    rng = np.random.default_rng(rows * 100 + n)
+    a = rng.standard_normal((rows, k))
+    w = rng.standard_normal((n, k)).astype(np.float32)
+    y = oracle.linear(a, w, threads=3)
+    assert np.allclose(y, a @ w.astype(np.float64).T, rtol=1e-12, atol=1e-12)
+
+
+def _qkv(rng, b, t, d):
+    return rng.standard_normal((b * t, 3 * d))
+
+
+def test_attention_zero_queries_average_values():
+    rng = np.random.default_rng(3)
+    b, t, d, h = 2, 9, 8, 2
+    qkv = _qkv(rng, b, t, d)
+    qkv[:, :d] = 0.0
+    o = oracle.attention(qkv, b, t, d, h)
+    v = qkv[:, 2 * d:].reshape(b, t, d)
+    assert np.allclose(o.reshape(b, t, d), v.mean(axis=1, keepdims=True).repeat(t, 1), atol=1e-14)
+
+
+def test_attention_single_token_returns_value():
+    rng = np.random.default_rng(4)
+    qkv = _qkv(rng, 3, 1, 16)
+    o = oracle.attention(qkv, 3, 1, 16, 4)
+    assert np.allclose(o, qkv[:, 32:], atol=0)
+
+
+def test_attention_two_tokens_sigmoid_closed_form():
+    # one head of dim 4 -> scale 1/2; softmax over two scores = sigmoid(s0-s1)
+    d = 4
+    qkv = np.zeros((2, 3 * d))
+    qkv[0, :d] = [1, 0, 0, 0]
+    qkv[1, :d] = [0, 2, 0, 0]
+    qkv[0, d:2 * d] = [3, 1, 0, 0]         # k0
+    qkv[1, d:2 * d] = [-1, 2, 0, 0]        # k1
+    qkv[0, 2 * d:] = [1, 2, 3, 4]          # v0
+    qkv[1, 2 * d:] = [-4, 0, 1, 2]         # v1
+    o = oracle.attention(qkv, 1, 2, d, 1)
+    for t, (s0, s1) in enumerate([(3 * 0.5, -1 * 0.5), (2 * 0.5, 4 * 0.5)]):
+        p0 = 1.0 / (1.0 + math.exp(-(s0 - s1)))
+        expect = p0 * qkv[0, 2 * d:] + (1 - p0) * qkv[1, 2 * d:]
+        assert np.allclose(o[t], expect, atol=1e-14)
+
+
+def test_attention_permutations_and_head_independence():
+    rng = np.random.default_rng(5)
+    b, t, d, h = 1, 12, 16, 4
+    qkv = _qkv(rng, b, t, d)
+    o = oracle.attention(qkv, b, t, d, h)
+    perm = rng.permutation(t)
+    # permuting tokens permutes the output rows (no positions, non-causal)
+    op = oracle.attention(qkv[perm], b, t, d, h)
+    assert np.allclose(op, o[perm], atol=1e-13)
+    # changing head 1's q, k and v leaves the other heads' columns unchanged
+    hd = d // h
+    q2 = qkv.copy()
+    for base in (0, d, 2 * d):
+        q2[:, base + hd:base + 2 * hd] = rng.standard_normal((t, hd))
+    o2 = oracle.attention(q2, b, t, d, h)
+    keep = [c for c in range(d) if not hd <= c < 2 * hd]
+    assert np.allclose(o2[:, keep], o[:, keep], atol=0)
+    assert not np.allclose(o2[:, hd:2 * hd], o[:, hd:2 * hd])
+
+
+def test_attention_batch_items_are_independent():
+    rng = np.random.default_rng(6)
+    t, d = 5, 8
+    qkv = _qkv(rng, 2, t, d)
+    o = oracle.attention(qkv, 2, t, d, 2)
+    o0 = oracle.attention(qkv[:t], 1, t, d, 2)
+    assert np.allclose(o[:t], o0, atol=0)
+
+
+def _params(rng, d, f):
+    p = {}
+    for name in oracle.PARAM_ORDER:
+        if name.startswith("norm"):
+            p[name] = np.ones(d, np.float32)
+        elif name.startswith("ada"):
+            p[name] = (0.1 * rng.standard_normal(d)).astype(np.float32)
+    p["attn.qkv.weight"] = (0.02 * rng.standard_normal((3 * d, d))).astype(np.float32)
+    p["attn.out.weight"] = (0.02 * rng.standard_normal((d, d))).astype(np.float32)
+    p["mlp.fc1.weight"] = (0.02 * rng.standard_normal((f, d))).astype(np.float32)
+    p["mlp.fc2.weight"] = (0.02 * rng.standard_normal((d, f))).astype(np.float32)
+    return p
+
+
+def test_block_zero_gates_is_identity():
+    rng = np.random.default_rng(8)
+    d, f, t = 16, 64, 6
+    p = _params(rng, d, f)
+    p["ada1.gate"][:] = 0
+    p["ada2.gate"][:] = 0
+    x = rng.standard_normal((t, d)).astype(np.float32)
+    y = oracle.block_forward(x, p, 1, t, d, 4, f)
+    assert np.array_equal(y, x.astype(np.float64))
+
+
+def _perm_matrix(perm):
+    m = np.zeros((len(perm), len(perm)), np.float32)
+    m[np.arange(len(perm)), perm] = 1.0
+    return m
+
+
+def test_block_attention_branch_closed_form():
+    # Wq = Wk = 0 -> uniform attention; Wv, Wo permutations; MLP gated off.
+    rng = np.random.default_rng(9)
+    d, f, t, heads = 12, 48, 5, 3
+    p = _params(rng, d, f)
+    pv, po = rng.permutation(d), rng.permutation(d)
+    w = np.zeros((3 * d, d), np.float32)
+    w[2 * d:] = _perm_matrix(pv)
+    p["attn.qkv.weight"] = w
+    p["attn.out.weight"] = _perm_matrix(po)
+    p["ada2.gate"][:] = 0
+    x = rng.standard_normal((t, d)).astype(np.float32)
+    y = oracle.block_forward(x, p, 1, t, d, heads, f)
+    h = oracle.rmsnorm_mod(x.astype(np.float64), p["norm1.weight"], p["ada1.shift"], p["ada1.scale"])
+    v = h[:, pv]                                # y = h W^T with W a permutation
+    o = np.tile(v.mean(axis=0), (t, 1))         # uniform attention
+    expect = x + p["ada1.gate"] * o[:, po]
+    assert np.allclose(y, expect, atol=1e-13)
+
+
+def test_block_mlp_branch_closed_form():
+    # attention gated off; W1's first d rows a permutation, rest zero;
+    # W2's first d columns a permutation, rest zero.
+    rng = np.random.default_rng(10)
+    d, f, t = 8, 32, 4
+    p = _params(rng, d, f)
+    p["ada1.gate"][:] = 0
+    p1, p2 = rng.permutation(d), rng.permutation(d)
+    w1 = np.zeros((f, d), np.float32)
+    w1[:d] = _perm_matrix(p1)
+    w2 = np.zeros((d, f), np.float32)
+    w2[:, :d] = _perm_matrix(p2)
+    p["mlp.fc1.weight"], p["mlp.fc2.weight"] = w1, w2
+    x = (3 * rng.standard_normal((t, d))).astype(np.float32)
+    y = oracle.block_forward(x, p, 1, t, d, 2, f)
+    h2 = oracle.rmsnorm_mod(x.astype(np.float64), p["norm2.weight"], p["ada2.shift"], p["ada2.scale"])
+    u = np.vectorize(oracle.gelu_tanh)(h2[:, p1])
+    expect = x + p["ada2.gate"] * u[:, p2]
+    assert np.allclose(y, expect, atol=1e-13)
+
+
+def test_block_token_permutation_equivariance_and_batch():
+    rng = np.random.default_rng(11)
+    d, f, t = 16, 64, 7
+    p = _params(rng, d, f)
+    x = rng.standard_normal((2 * t, d)).astype(np.float32)
+    y = oracle.block_forward(x, p, 2, t, d, 4, f)
+    perm = rng.permutation(t)
+    xp = x.copy()
+    xp[:t] = x[:t][perm]
+    yp = oracle.block_forward(xp, p, 2, t, d, 4, f)
+    assert np.allclose(yp[:t], y[:t][perm], atol=1e-12)
+    assert np.allclose(yp[t:], y[t:], atol=0)
