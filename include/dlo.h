@@ -1,0 +1,338 @@
+/*
+ * dlo.h — C ABI of the GB300 per-block weight stream of Distributed
+ * Layerwise Offload (DLO).
+ *
+ * Sources, cited by page title and section:
+ *   [B1] "Distributed Layerwise Offload" (vLLM blog preview, 2026-07-30):
+ *        "Weight Sharding + AllGather", "Double-Buffer Memory Bound",
+ *        "Slot Tracking: i%2 + Dynamic Correction", "Fail-Closed Design".
+ *   [B2] "Distributed Layerwise Offload: Scaling Toward 200B+ DiT Models
+ *        Efficiently in vLLM-Omni" (vLLM blog, 2026-08-17):
+ *        "2. Weight Sharding with AllGather Reconstruction",
+ *        "3. Double-Buffered Prefetch with H2D + AllGather Overlap".
+ *   [D5] vLLM-Omni design doc "Distributed Layerwise Offload":
+ *        "AllGather path", "Rank-local path without DLO AllGather".
+ *
+ * What the library does.  Each block's parameters are flattened by dtype and
+ * split into n_shards equal, zero-padded shards that live in pinned host
+ * memory.  Two device slots, each large enough for the largest block, hold
+ * the block being computed and the block being prefetched.  A prefetch copies
+ * every shard host->device and reassembles the shards, in rank order, into
+ * the slot (on one GPU the n_shards host regions stand in for the ranks of an
+ * all_gather_into_tensor).  Parameters are zero-copy pointers into the slot.
+ * The block forward runs on a compute stream that waits for the slot's ready
+ * event; the next block's prefetch runs on a copy stream that waits for the
+ * free event of the forward that last read the target slot.
+ *
+ * Conventions.
+ *   - Every call returns a dlo_status.  Out-parameters are written only on
+ *     DLO_OK.  On failure dlo_last_error() returns a message (per thread).
+ *     Nothing throws across the ABI.  Calls fail closed ([B1] "Fail-Closed
+ *     Design"): a call that would read a slot that does not hold the
+ *     requested block, or write a slot that is still being read without a
+ *     wait, returns an error instead.
+ *   - Streams are passed as `void*` holding a cudaStream_t; device and host
+ *     buffers as plain pointers.  The header needs no CUDA include.
+ *   - bf16 tensors are passed as uint16_t (raw bits).
+ *   - The library never allocates device memory or pins host memory: the
+ *     caller owns slots, activations, scratch, shard buffers and streams.
+ *     The library owns plans, engines, their CUDA events and logs.
+ */
+#ifndef DLO_H_
+#define DLO_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DLO_OK = 0,
+  DLO_ERR_INVALID = 1,  /* bad argument: null, size, alignment, unknown name */
+  DLO_ERR_CUDA = 2,     /* a CUDA runtime/driver call failed (text in dlo_last_error) */
+  DLO_ERR_TIMEOUT = 3,  /* a bounded wait ran out (host poll or device-side wait) */
+  DLO_ERR_STATE = 4,    /* call not valid in the current state (e.g. block not resident) */
+  DLO_ERR_NOMEM = 5     /* a caller-provided buffer is too small */
+} dlo_status;
+
+typedef enum { DLO_BF16 = 0, DLO_F32 = 1 } dlo_dtype;
+
+/* How a prefetch moves the shards host->device.
+ *   DMA:    one cudaMemcpyAsync per (dtype group, shard) on the copy stream,
+ *           straight to the shard's final offset in the slot (copy engines,
+ *           no SMs).
+ *   KERNEL: one launch of a copy-and-reassemble kernel that reads the mapped
+ *           pinned host shards with 16-byte loads and writes them to their
+ *           final slot offsets (SMs read over the host link).
+ *   AUTO:   the first prefetches alternate between the two under the real
+ *           workload, timed with events; the faster per byte is then kept. */
+typedef enum { DLO_COPY_AUTO = 0, DLO_COPY_DMA = 1, DLO_COPY_KERNEL = 2 } dlo_copy_mode;
+
+/* ------------------------------------------------------------------------
+ * Plan: the per-block layout ([B1] "Weight Sharding + AllGather"; [B2] §2).
+ * ------------------------------------------------------------------------ */
+
+typedef struct {
+  const char* name;     /* parameter name, copied by dlo_plan_create */
+  int32_t ndim;         /* 1..4 */
+  int64_t shape[4];     /* row-major; shape[ndim-1] is contiguous */
+  int32_t dtype;        /* dlo_dtype */
+} dlo_param_desc;
+
+typedef struct dlo_plan dlo_plan;
+
+typedef struct {
+  int32_t n_params;
+  int32_t n_groups;     /* distinct dtypes, in order of first appearance */
+  int32_t n_shards;
+  int32_t has_dit_roles;/* 1 if the names match the synthetic DiT block */
+  int64_t slot_bytes;   /* bytes a slot needs for this block */
+  int64_t group_align;  /* byte alignment of each group's base in a slot (256) */
+} dlo_plan_info;
+
+typedef struct {
+  int32_t dtype;
+  int32_t esize;            /* bytes per element */
+  int64_t numel;            /* N_g: elements of all params of this dtype */
+  int64_t shard_numel;      /* S_g = ceil(N_g / n_shards)  ([B2] §2) */
+  int64_t shard_bytes;      /* S_g * esize: bytes each shard contributes */
+  int64_t shard_alloc_bytes;/* shard_bytes rounded up to 16: required size of
+                               every host shard buffer of this group */
+  int64_t base;             /* byte offset of the gathered group in a slot */
+} dlo_group_info;
+
+typedef struct {
+  int32_t group;            /* index into the plan's groups */
+  int32_t dtype;
+  int64_t numel;
+  int64_t group_offset;     /* element offset inside the flat group */
+  int64_t slot_offset;      /* byte offset inside a slot (base + offset*esize) */
+} dlo_param_info;
+
+/* Builds the layout of one block.  Parameters of one dtype are concatenated
+ * in the given (registration) order with no gap; each dtype group is split
+ * into n_shards shards of S_g = ceil(N_g / n_shards) elements, the last
+ * zero-padded ([B2] §2); in a slot, groups follow in order of first
+ * appearance, each at a 256-byte aligned base, each occupying
+ * n_shards * S_g elements (the gathered buffer, padding included).
+ * n_shards >= 1 (1 is the rank-local path of [D5]).  *out is owned by the
+ * caller and released with dlo_plan_destroy.
+ * Errors: DLO_ERR_INVALID on null pointers, n_params < 1, ndim outside 1..4,
+ * a non-positive extent, an unknown dtype, or n_shards < 1. */
+dlo_status dlo_plan_create(const dlo_param_desc* params, int32_t n_params,
+                           int32_t n_shards, dlo_plan** out);
+dlo_status dlo_plan_query(const dlo_plan* plan, dlo_plan_info* out);
+dlo_status dlo_plan_group(const dlo_plan* plan, int32_t group, dlo_group_info* out);
+dlo_status dlo_plan_param(const dlo_plan* plan, int32_t param, dlo_param_info* out);
+
+/* CPU flatten / pad / split ([B2] §2, the rank-r copy window).
+ * param_src[p]: host pointer to parameter p's contiguous data (n_params
+ *   entries, in plan order).
+ * shard_dst[g * n_shards + r]: host buffer of at least shard_alloc_bytes for
+ *   group g, shard r (pinned memory for the stream to use it; any memory is
+ *   accepted here).  Each is fully written: the shard's elements, then zeros.
+ * Errors: DLO_ERR_INVALID on null pointers. */
+dlo_status dlo_shard_host(const dlo_plan* plan, const void* const* param_src,
+                          void* const* shard_dst);
+void dlo_plan_destroy(dlo_plan* plan);
+
+/* ------------------------------------------------------------------------
+ * One-shot reassembly ([B1] "Weight Sharding + AllGather" steps 1-2; [D5]
+ * "AllGather path"): copies every shard of a block host->device into `dst`
+ * laid out as a slot, on `stream`, with the given mode (AUTO means DMA here).
+ * shard_ptrs: as in dlo_shard_host; each must be 16-byte aligned and hold
+ *   shard_alloc_bytes (the kernel path reads whole 16-byte words).  The
+ *   kernel path needs page-locked, device-mapped memory (cudaHostAlloc or
+ *   cudaHostRegister with mapping); DLO_ERR_INVALID otherwise.
+ * dst: device buffer of at least plan slot_bytes; 256-byte aligned.
+ * Asynchronous; the shard memory must stay valid until the stream passes. */
+dlo_status dlo_reassemble(const dlo_plan* plan, const void* const* shard_ptrs,
+                          void* dst, int32_t mode, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Synthetic DiT block (the block the stream feeds; the pages do not define
+ * one).  x is the fp32 residual [batch*tokens, hidden], updated in place:
+ *   h  = RMSNorm(x) * g1 * (1 + scale1) + shift1          (bf16)
+ *   qkv = h Wqkv^T                                         (bf16, [.., 3d])
+ *   o  = softmax(q k^T / sqrt(hd)) v per head, non-causal  (bf16)
+ *   x += gate1 * (o Wo^T)
+ *   h2 = RMSNorm(x) * g2 * (1 + scale2) + shift2
+ *   x += gate2 * (GELU_tanh(h2 W1^T) W2^T)
+ * Linear weights are [out, in] (nn.Linear layout), bf16; norm gains and
+ * adaLN vectors are fp32 [hidden].  Accumulation is fp32.
+ * ------------------------------------------------------------------------ */
+
+typedef struct {
+  int32_t batch;
+  int32_t tokens;
+  int32_t hidden;   /* multiple of 64 */
+  int32_t heads;    /* hidden / heads must be 64 or 128 */
+  int32_t mlp;      /* multiple of 64 */
+  float eps;        /* RMSNorm epsilon */
+} dlo_dit_cfg;
+
+/* Bytes of device scratch one block forward needs (bf16 h, qkv, o, u). */
+size_t dlo_forward_scratch_bytes(const dlo_dit_cfg* cfg);
+
+/* One block forward with weights at `block_base`, laid out as a slot of
+ * `plan` (the plan's parameter names must be the DiT block's: norm1.weight,
+ * ada1.shift, ada1.scale, ada1.gate, attn.qkv.weight, attn.out.weight,
+ * norm2.weight, ada2.shift, ada2.scale, ada2.gate, mlp.fc1.weight,
+ * mlp.fc2.weight).  Used for the all-resident reference run; the streamed
+ * path calls the same kernels through dlo_block_forward.
+ * x: device fp32 [batch*tokens*hidden], 16-byte aligned, updated in place.
+ * scratch: device, >= dlo_forward_scratch_bytes, 256-byte aligned.
+ * Errors: DLO_ERR_INVALID on shapes the kernels do not support, a plan
+ * without DiT roles or with mismatched shapes; DLO_ERR_NOMEM if scratch is
+ * too small. */
+dlo_status dlo_forward(const dlo_dit_cfg* cfg, const dlo_plan* plan,
+                       const void* block_base, float* x, void* scratch,
+                       size_t scratch_bytes, void* stream);
+
+/* Single steps of the block, for per-kernel checks (device pointers):
+ *   rmsnorm_mod: h = bf16(x / sqrt(mean(x^2)+eps) * g * (1+scale) + shift)
+ *   linear:      out = epilogue(a W^T), a bf16 [M,K], W bf16 [N,K];
+ *                epilogue 0: out bf16 [M,N] = acc
+ *                         1: out bf16 [M,N] = GELU_tanh(acc)
+ *                         2: out fp32 [M,N] += gate[N] * acc  (in place)
+ *                K and N multiples of 8; pointers 16-byte aligned.
+ *   attention:   o bf16 [batch*tokens, d] from qkv bf16 [batch*tokens, 3d] */
+dlo_status dlo_op_rmsnorm_mod(const float* x, int64_t rows, int64_t d,
+                              const float* g, const float* shift,
+                              const float* scale, float eps, uint16_t* h,
+                              void* stream);
+dlo_status dlo_op_linear(const uint16_t* a, int64_t M, int64_t K,
+                         const uint16_t* w, int64_t N, int32_t epilogue,
+                         void* out, const float* gate, void* stream);
+dlo_status dlo_op_attention(const uint16_t* qkv, int64_t batch, int64_t tokens,
+                            int64_t d, int64_t heads, uint16_t* o, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Engine: two slots, the hook schedule, events ([B1] "Double-Buffer Memory
+ * Bound", "Slot Tracking: i%2 + Dynamic Correction"; [B2] §3; [D5]
+ * "AllGather path").
+ * ------------------------------------------------------------------------ */
+
+typedef struct dlo_engine dlo_engine;
+
+typedef struct {
+  int32_t n_blocks;       /* blocks per pass (hooks), >= 1 */
+  void* slot[2];          /* device buffers, 256-byte aligned, caller-owned */
+  int64_t slot_bytes;     /* capacity of each slot */
+  void* compute_stream;   /* cudaStream_t for block forwards */
+  void* copy_stream;      /* cudaStream_t for prefetches (must differ) */
+  int32_t copy_mode;      /* dlo_copy_mode */
+  int32_t copy_ctas;      /* CTAs of the copy kernel; 0 = default (152) */
+  int32_t timing;         /* 1: bracket every prefetch with timing events */
+} dlo_engine_desc;
+
+typedef struct {
+  int32_t k;                  /* global forward index */
+  int32_t block;
+  int32_t read_slot;
+  int32_t prefetch_block;
+  int32_t prefetch_slot;
+  int32_t waits_on_free_of_k; /* forward whose free event the prefetch waited on; -1: none */
+  int32_t copy_mode;          /* mode used for the prefetch */
+} dlo_sched_event;
+
+/* Creates an engine.  Each hook i starts with current_slot = i % 2 and no
+ * prefetched slot; hook 0's predecessor is hook n_blocks-1 (circular).
+ * Errors: DLO_ERR_INVALID on null/misaligned slots, equal streams,
+ * n_blocks < 1; DLO_ERR_CUDA if events cannot be created. */
+dlo_status dlo_engine_create(const dlo_engine_desc* desc, dlo_engine** out);
+
+/* Registers block `block` (0 <= block < n_blocks) with its plan and shard
+ * pointers (shard_ptrs[g * n_shards + r], host, pinned, 16-byte aligned,
+ * shard_alloc_bytes each; borrowed until dlo_engine_destroy).  The plan is
+ * borrowed too.  Several blocks may share one plan and one set of shards.
+ * Errors: DLO_ERR_INVALID (range, plan larger than a slot, pointer not
+ * pinned/mapped or misaligned), DLO_ERR_STATE (already registered). */
+dlo_status dlo_register_block(dlo_engine* e, int32_t block, const dlo_plan* plan,
+                              const void* const* shard_ptrs);
+
+/* Enqueues a prefetch of `block` into `slot` on the copy stream: the copy
+ * stream waits for the free event of the forward that last read `slot`,
+ * copies and reassembles, then records the slot's ready event.  This is the
+ * setup prefetch (block 0 into slot 0) before the first forward; the hook
+ * issues all later prefetches itself.
+ * Errors: DLO_ERR_INVALID (range), DLO_ERR_STATE (block unregistered). */
+dlo_status dlo_prefetch(dlo_engine* e, int32_t block, int32_t slot);
+
+/* Makes the compute stream wait for the ready event of the slot holding
+ * `block` (non-blocking on the host).  DLO_ERR_STATE if no slot holds it. */
+dlo_status dlo_wait(dlo_engine* e, int32_t block);
+
+/* Host-side poll of the same event, bounded by timeout_ms; DLO_ERR_TIMEOUT
+ * when it runs out.  Never spins on the device. */
+dlo_status dlo_wait_host(dlo_engine* e, int32_t block, int32_t timeout_ms);
+
+/* Device pointer of parameter `param` of resident `block` (a view into the
+ * slot, no copy; [B1] "Weight Sharding + AllGather" step 3).
+ * DLO_ERR_STATE if no slot holds the block. */
+dlo_status dlo_param_view(const dlo_engine* e, int32_t block, int32_t param,
+                          void** dev_ptr);
+
+/* The pre-forward hook of block `block`, which must be the next block of
+ * the pass (global forward k -> block k mod n_blocks):
+ *   1. adopt the previous hook's prefetched slot, if it has one;
+ *   2. make the compute stream wait for that slot's ready event;
+ *   3. prefetch block (block+1) mod n_blocks into the other slot (circular
+ *      tail->head wrap), after the free event of that slot's last reader;
+ *   4. record the prefetched slot.
+ * Writes the slot the forward must read to *slot_out (may be null).
+ * Errors: DLO_ERR_STATE if `block` is not the next block, if the slot does
+ * not hold it, or if a post_forward is missing. */
+dlo_status dlo_pre_forward(dlo_engine* e, int32_t block, int32_t* slot_out);
+
+/* Records the free event of the slot just read, on the compute stream. */
+dlo_status dlo_post_forward(dlo_engine* e, int32_t block);
+
+/* pre_forward + dlo_forward on the slot + post_forward. */
+dlo_status dlo_block_forward(dlo_engine* e, int32_t block, const dlo_dit_cfg* cfg,
+                             float* x, void* scratch, size_t scratch_bytes);
+
+/* Copies up to `cap` entries of the schedule log (one per forward). */
+dlo_status dlo_schedule_log(const dlo_engine* e, dlo_sched_event* buf,
+                            int32_t cap, int32_t* n_out);
+
+/* Engine counters.  copy_ms[i] / copy_bytes[i]: elapsed time and bytes of
+ * the i-th timed prefetch (only with desc.timing = 1; synchronises on the
+ * events it reads).  chosen_mode: the mode AUTO settled on (or the fixed
+ * mode); dma_ns_per_mb / kernel_ns_per_mb: AUTO's measured rates (0 if not
+ * measured). */
+typedef struct {
+  int32_t chosen_mode;
+  int32_t n_forwards;
+  int32_t n_prefetches;
+  double dma_ns_per_mb;
+  double kernel_ns_per_mb;
+} dlo_engine_stats;
+dlo_status dlo_engine_query(dlo_engine* e, dlo_engine_stats* out);
+dlo_status dlo_engine_copy_times(dlo_engine* e, float* copy_ms, int64_t* copy_bytes,
+                                 int32_t cap, int32_t* n_out);
+
+/* Waits (host side, bounded by timeout_ms) for both streams' enqueued
+ * engine work, then releases the engine's events.  The caller's buffers are
+ * untouched.  Returns DLO_ERR_TIMEOUT (and keeps the engine) if the work
+ * does not finish in time.  A null engine is accepted. */
+dlo_status dlo_engine_destroy(dlo_engine* e, int32_t timeout_ms);
+
+/* Device-side status of the library's kernels: every spin-wait inside a
+ * kernel is bounded; a wait that runs out records a code here and the
+ * kernel returns early.  Reads and clears the word (synchronises the
+ * device).  *code = 0 means no wait ran out. */
+dlo_status dlo_kernel_status(int32_t* code);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* dlo_last_error(void);
+
+/* Library version, for diagnostics. */
+const char* dlo_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DLO_H_ */

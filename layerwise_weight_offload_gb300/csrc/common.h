@@ -1,0 +1,121 @@
+// common.h — internal helpers shared by the library's translation units:
+// status/error reporting, CUDA checks, the plan's in-memory form and the
+// launchers each kernel file exports to the host-side orchestration.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <string>
+#include <vector>
+
+#include "../../include/dlo.h"
+
+namespace dlo {
+
+// Thread-local message behind dlo_last_error().
+void set_error(const char* fmt, ...);
+void clear_error();
+
+#define DLO_FAIL(code, ...)          \
+  do {                               \
+    ::dlo::set_error(__VA_ARGS__);   \
+    return (code);                   \
+  } while (0)
+
+#define DLO_CUDA(call)                                                     \
+  do {                                                                     \
+    cudaError_t err_ = (call);                                             \
+    if (err_ != cudaSuccess)                                               \
+      DLO_FAIL(DLO_ERR_CUDA, "%s failed: %s (%s:%d)", #call,               \
+               cudaGetErrorString(err_), __FILE__, __LINE__);              \
+  } while (0)
+
+#define DLO_TRY(expr)                         \
+  do {                                        \
+    dlo_status st_ = (expr);                  \
+    if (st_ != DLO_OK) return st_;            \
+  } while (0)
+
+constexpr int64_t kGroupAlign = 256;
+constexpr int kMaxSegments = 64;   // (dtype group, shard) pairs per prefetch
+
+inline int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
+
+// Roles of the synthetic DiT block's parameters.
+enum Role {
+  R_G1 = 0, R_SHIFT1, R_SCALE1, R_GATE1, R_WQKV, R_WO,
+  R_G2, R_SHIFT2, R_SCALE2, R_GATE2, R_W1, R_W2, R_COUNT
+};
+extern const char* const kRoleNames[R_COUNT];
+
+}  // namespace dlo
+
+struct dlo_plan {
+  struct Param {
+    std::string name;
+    int32_t ndim;
+    int64_t shape[4];
+    int32_t dtype;
+    int64_t numel;
+    int32_t group;
+    int64_t group_offset;   // elements
+    int64_t slot_offset;    // bytes
+  };
+  struct Group {
+    int32_t dtype;
+    int32_t esize;
+    int64_t numel;
+    int64_t shard_numel;
+    int64_t shard_bytes;
+    int64_t shard_alloc_bytes;
+    int64_t base;
+  };
+  std::vector<Param> params;
+  std::vector<Group> groups;
+  int32_t n_shards = 1;
+  int64_t slot_bytes = 0;
+  int32_t role[dlo::R_COUNT];   // param index per role, -1 if absent
+  bool has_dit_roles = false;
+};
+
+namespace dlo {
+
+// One host->device piece of a prefetch: a shard and its final place.
+struct Segment {
+  const void* src;    // device-accessible address of the pinned host shard
+  void* dst;          // slot + base_g + r * shard_bytes
+  int64_t bytes;      // shard_bytes
+};
+
+struct SegmentTable {
+  int32_t n;
+  Segment seg[kMaxSegments];
+};
+
+// copy_kernel.cu
+dlo_status launch_copy_reassemble(const SegmentTable& t, int ctas,
+                                  cudaStream_t stream);
+
+// norm.cu
+dlo_status launch_rmsnorm_mod(const float* x, int64_t rows, int64_t d,
+                              const float* g, const float* shift,
+                              const float* scale, float eps, uint16_t* h,
+                              cudaStream_t stream);
+
+// gemm.cu
+enum Epilogue { EPI_BF16 = 0, EPI_GELU_BF16 = 1, EPI_RESID_F32 = 2 };
+dlo_status launch_linear(const uint16_t* a, int64_t M, int64_t K,
+                         const uint16_t* w, int64_t N, int epilogue, void* out,
+                         const float* gate, cudaStream_t stream);
+
+// attention.cu
+dlo_status launch_attention(const uint16_t* qkv, int64_t batch,
+                            int64_t tokens, int64_t d, int64_t heads,
+                            uint16_t* o, cudaStream_t stream);
+
+// status.cu: device-side error word written by bounded waits
+int* device_error_word();  // device address (cached per device)
+
+}  // namespace dlo

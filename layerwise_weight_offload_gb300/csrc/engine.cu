@@ -1,0 +1,552 @@
+// engine.cu — two device slots, the per-block hook schedule, and the
+// prefetch (host->device copy plus reassembly) on a dedicated copy stream.
+//
+// "Distributed Layerwise Offload" (vLLM blog preview, 2026-07-30):
+//   "Weight Sharding + AllGather": H2D of each shard on copy_stream, gather
+//     of the full block, re-pointing of parameters, forward on a compute
+//     stream that waits for the gather event; block N+1's preparation
+//     overlaps block N's forward.
+//   "Double-Buffer Memory Bound": exactly two blocks on the device.
+//   "Slot Tracking: i%2 + Dynamic Correction": hook i starts at slot i % 2;
+//     when the previous hook has prefetched, the hook takes that slot, which
+//     keeps the circular tail->head prefetch of an odd block count from
+//     landing in the slot the head reads.
+// "Distributed Layerwise Offload: Scaling Toward 200B+ DiT Models
+// Efficiently in vLLM-Omni", "3. Double-Buffered Prefetch with H2D +
+// AllGather Overlap": two buffers sized to the largest block, shared by all
+// blocks, event-based synchronisation between streams.
+//
+// Beyond the pages: the prefetch into a slot also waits for the free event
+// recorded after the last forward that read that slot (the pages draw only
+// the compute-waits-for-gather arrow; reusing two buffers needs the reverse
+// write-after-read wait too).
+#include <chrono>
+#include <new>
+#include <thread>
+
+#include "common.h"
+
+namespace dlo {
+dlo_status forward_impl(const dlo_dit_cfg* cfg, const dlo_plan* plan, const void* block_base,
+                        float* x, void* scratch, size_t scratch_bytes, cudaStream_t stream);
+}
+
+struct dlo_engine {
+  struct Block {
+    const dlo_plan* plan = nullptr;
+    std::vector<const void*> host;   // [g * n_shards + r]
+    std::vector<const void*> dev;    // device-accessible addresses (null: DMA only)
+    int64_t bytes = 0;               // bytes one prefetch moves
+  };
+  struct Hook {
+    int32_t current_slot;
+    int32_t prefetched_slot;         // -1: none yet
+  };
+  struct Timed {
+    cudaEvent_t a, b;
+    int64_t bytes;
+    int32_t mode;
+  };
+
+  int32_t n_blocks = 0;
+  uint8_t* slot[2] = {nullptr, nullptr};
+  int64_t slot_bytes = 0;
+  cudaStream_t compute = nullptr, copy = nullptr;
+  int32_t mode = DLO_COPY_AUTO;
+  int32_t copy_ctas = 0;
+  bool timing = false;
+  std::vector<Block> blocks;
+  std::vector<Hook> hooks;
+  cudaEvent_t ready[2] = {nullptr, nullptr};
+  cudaEvent_t freed[2] = {nullptr, nullptr};
+  int32_t slot_holds[2] = {-1, -1};
+  int32_t last_reader[2] = {-1, -1};
+  int64_t k = 0;                     // next global forward index
+  bool in_forward = false;
+  int32_t cur_block = -1, cur_slot = -1;
+  std::vector<dlo_sched_event> log;
+  std::vector<Timed> timed;          // with timing = 1: every prefetch
+  // AUTO: the first prefetches alternate modes and are timed
+  std::vector<Timed> race;
+  int32_t chosen = -1;               // DLO_COPY_DMA / DLO_COPY_KERNEL once decided
+  double dma_ns_per_mb = 0, kernel_ns_per_mb = 0;
+  int64_t n_prefetches = 0;
+};
+
+namespace dlo {
+namespace {
+
+constexpr int kRaceRounds = 3;   // timed prefetches per mode before AUTO decides
+
+dlo_status build_segments(const dlo_engine::Block& b, uint8_t* dst, SegmentTable* t) {
+  const dlo_plan* p = b.plan;
+  const int32_t s = p->n_shards;
+  t->n = 0;
+  for (size_t g = 0; g < p->groups.size(); ++g) {
+    const auto& grp = p->groups[g];
+    for (int32_t r = 0; r < s; ++r) {
+      if (t->n >= kMaxSegments)
+        DLO_FAIL(DLO_ERR_INVALID, "prefetch: more than %d (group, shard) pieces", kMaxSegments);
+      Segment& sg = t->seg[t->n++];
+      sg.src = b.dev[g * s + r];
+      sg.dst = dst + grp.base + static_cast<int64_t>(r) * grp.shard_bytes;
+      sg.bytes = grp.shard_bytes;
+    }
+  }
+  return DLO_OK;
+}
+
+dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, int ctas,
+                      cudaStream_t stream) {
+  const dlo_plan* p = b.plan;
+  const int32_t s = p->n_shards;
+  if (mode == DLO_COPY_KERNEL) {
+    for (const void* q : b.dev)
+      if (!q) DLO_FAIL(DLO_ERR_INVALID, "prefetch: a shard is not device-mapped pinned memory");
+    SegmentTable t;
+    DLO_TRY(build_segments(b, dst, &t));
+    return launch_copy_reassemble(t, ctas, stream);
+  }
+  for (size_t g = 0; g < p->groups.size(); ++g) {
+    const auto& grp = p->groups[g];
+    for (int32_t r = 0; r < s; ++r)
+      DLO_CUDA(cudaMemcpyAsync(dst + grp.base + static_cast<int64_t>(r) * grp.shard_bytes,
+                               b.host[g * s + r], static_cast<size_t>(grp.shard_bytes),
+                               cudaMemcpyHostToDevice, stream));
+  }
+  return DLO_OK;
+}
+
+bool all_mapped(const dlo_engine::Block& b) {
+  for (const void* q : b.dev)
+    if (!q) return false;
+  return true;
+}
+
+// AUTO: decide once every raced prefetch has completed (non-blocking query).
+void try_decide(dlo_engine* e) {
+  if (e->chosen >= 0 || static_cast<int>(e->race.size()) < 2 * kRaceRounds) return;
+  for (const auto& t : e->race)
+    if (cudaEventQuery(t.b) != cudaSuccess) return;
+  double ms[3] = {0, 0, 0}, mb[3] = {0, 0, 0};
+  for (const auto& t : e->race) {
+    float v = 0;
+    cudaEventElapsedTime(&v, t.a, t.b);
+    ms[t.mode] += v;
+    mb[t.mode] += t.bytes / 1e6;
+  }
+  e->dma_ns_per_mb = mb[DLO_COPY_DMA] > 0 ? ms[DLO_COPY_DMA] * 1e6 / mb[DLO_COPY_DMA] : 0;
+  e->kernel_ns_per_mb =
+      mb[DLO_COPY_KERNEL] > 0 ? ms[DLO_COPY_KERNEL] * 1e6 / mb[DLO_COPY_KERNEL] : 0;
+  e->chosen = (e->kernel_ns_per_mb > 0 && e->kernel_ns_per_mb < e->dma_ns_per_mb)
+                  ? DLO_COPY_KERNEL
+                  : DLO_COPY_DMA;
+  for (auto& t : e->race) {
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
+  e->race.clear();
+}
+
+dlo_status make_timed(dlo_engine::Timed* t) {
+  DLO_CUDA(cudaEventCreate(&t->a));
+  if (cudaEventCreate(&t->b) != cudaSuccess) {
+    cudaEventDestroy(t->a);
+    DLO_FAIL(DLO_ERR_CUDA, "cudaEventCreate failed");
+  }
+  return DLO_OK;
+}
+
+// Enqueues the prefetch of `block` into `slot` on the copy stream.
+dlo_status enqueue_prefetch(dlo_engine* e, int32_t block, int32_t slot) {
+  const dlo_engine::Block& b = e->blocks[block];
+  int32_t mode = e->mode;
+  bool racing = false;
+  if (mode == DLO_COPY_AUTO) {
+    try_decide(e);
+    if (e->chosen >= 0) {
+      mode = e->chosen;
+    } else if (!all_mapped(b)) {
+      mode = DLO_COPY_DMA;
+    } else if (static_cast<int>(e->race.size()) < 2 * kRaceRounds) {
+      mode = (e->race.size() % 2 == 0) ? DLO_COPY_DMA : DLO_COPY_KERNEL;
+      racing = true;
+    } else {
+      mode = DLO_COPY_DMA;   // raced prefetches still in flight
+    }
+  }
+  DLO_CUDA(cudaStreamWaitEvent(e->copy, e->freed[slot], 0));
+  dlo_engine::Timed t{};
+  const bool timed = racing || e->timing;
+  if (timed) {
+    DLO_TRY(make_timed(&t));
+    t.bytes = b.bytes;
+    t.mode = mode;
+    DLO_CUDA(cudaEventRecord(t.a, e->copy));
+  }
+  DLO_TRY(copy_block(b, e->slot[slot], mode, e->copy_ctas, e->copy));
+  if (timed) {
+    DLO_CUDA(cudaEventRecord(t.b, e->copy));
+    if (racing)
+      e->race.push_back(t);    // AUTO's measurement; not listed in the timing log
+    else
+      e->timed.push_back(t);
+  }
+  DLO_CUDA(cudaEventRecord(e->ready[slot], e->copy));
+  e->slot_holds[slot] = block;
+  e->n_prefetches++;
+  return DLO_OK;
+}
+
+dlo_status check_engine(const dlo_engine* e) {
+  if (!e) DLO_FAIL(DLO_ERR_INVALID, "null engine");
+  return DLO_OK;
+}
+
+int32_t slot_of(const dlo_engine* e, int32_t block) {
+  if (e->slot_holds[0] == block) return 0;
+  if (e->slot_holds[1] == block) return 1;
+  return -1;
+}
+
+}  // namespace
+}  // namespace dlo
+
+extern "C" {
+
+dlo_status dlo_engine_create(const dlo_engine_desc* d, dlo_engine** out) {
+  using namespace dlo;
+  if (!d || !out) DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: null argument");
+  if (d->n_blocks < 1) DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: n_blocks must be >= 1");
+  if (!d->slot[0] || !d->slot[1] || d->slot[0] == d->slot[1])
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: two distinct slots are required");
+  if ((reinterpret_cast<uintptr_t>(d->slot[0]) | reinterpret_cast<uintptr_t>(d->slot[1])) & 255u)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: slots must be 256-byte aligned");
+  if (d->slot_bytes <= 0) DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: slot_bytes must be > 0");
+  if (d->compute_stream == d->copy_stream)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: compute and copy streams must differ");
+  if (d->copy_mode < DLO_COPY_AUTO || d->copy_mode > DLO_COPY_KERNEL)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: unknown copy mode %d", d->copy_mode);
+  dlo_engine* e = new (std::nothrow) dlo_engine();
+  if (!e) DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: out of host memory");
+  e->n_blocks = d->n_blocks;
+  e->slot[0] = static_cast<uint8_t*>(d->slot[0]);
+  e->slot[1] = static_cast<uint8_t*>(d->slot[1]);
+  e->slot_bytes = d->slot_bytes;
+  e->compute = static_cast<cudaStream_t>(d->compute_stream);
+  e->copy = static_cast<cudaStream_t>(d->copy_stream);
+  e->mode = d->copy_mode;
+  e->copy_ctas = d->copy_ctas;
+  e->timing = d->timing != 0;
+  e->blocks.resize(d->n_blocks);
+  e->hooks.resize(d->n_blocks);
+  for (int32_t i = 0; i < d->n_blocks; ++i) e->hooks[i] = {i % 2, -1};
+  if (d->copy_mode != DLO_COPY_AUTO) e->chosen = d->copy_mode;
+  for (int s = 0; s < 2; ++s) {
+    if (cudaEventCreateWithFlags(&e->ready[s], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&e->freed[s], cudaEventDisableTiming) != cudaSuccess) {
+      for (int q = 0; q < 2; ++q) {
+        if (e->ready[q]) cudaEventDestroy(e->ready[q]);
+        if (e->freed[q]) cudaEventDestroy(e->freed[q]);
+      }
+      delete e;
+      DLO_FAIL(DLO_ERR_CUDA, "dlo_engine_create: cudaEventCreate failed");
+    }
+  }
+  *out = e;
+  return DLO_OK;
+}
+
+dlo_status dlo_register_block(dlo_engine* e, int32_t block, const dlo_plan* plan,
+                              const void* const* shard_ptrs) {
+  using namespace dlo;
+  DLO_TRY(check_engine(e));
+  if (block < 0 || block >= e->n_blocks)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block: block %d out of range", block);
+  if (!plan || !shard_ptrs) DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block: null argument");
+  if (e->blocks[block].plan)
+    DLO_FAIL(DLO_ERR_STATE, "dlo_register_block: block %d already registered", block);
+  if (plan->slot_bytes > e->slot_bytes)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block: block needs %lld bytes, slots hold %lld",
+             (long long)plan->slot_bytes, (long long)e->slot_bytes);
+  const size_t n = plan->groups.size() * static_cast<size_t>(plan->n_shards);
+  if (n > static_cast<size_t>(kMaxSegments))
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block: %zu (group, shard) pieces, at most %d", n,
+             kMaxSegments);
+  dlo_engine::Block b;
+  b.plan = plan;
+  b.host.assign(shard_ptrs, shard_ptrs + n);
+  b.dev.assign(n, nullptr);
+  for (size_t i = 0; i < n; ++i) {
+    const void* q = shard_ptrs[i];
+    if (!q || (reinterpret_cast<uintptr_t>(q) & 15u))
+      DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block: shard %zu is null or not 16-byte aligned",
+               i);
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, q) != cudaSuccess || a.type != cudaMemoryTypeHost) {
+      cudaGetLastError();
+      DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block: shard %zu is not page-locked host memory",
+               i);
+    }
+    b.dev[i] = a.devicePointer;
+  }
+  for (const auto& g : plan->groups) b.bytes += g.shard_bytes * plan->n_shards;
+  if (e->mode == DLO_COPY_KERNEL && !all_mapped(b))
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block: kernel copies need device-mapped shards");
+  e->blocks[block] = std::move(b);
+  return DLO_OK;
+}
+
+dlo_status dlo_prefetch(dlo_engine* e, int32_t block, int32_t slot) {
+  using namespace dlo;
+  DLO_TRY(check_engine(e));
+  if (block < 0 || block >= e->n_blocks || slot < 0 || slot > 1)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_prefetch: block %d / slot %d out of range", block, slot);
+  if (!e->blocks[block].plan)
+    DLO_FAIL(DLO_ERR_STATE, "dlo_prefetch: block %d is not registered", block);
+  if (e->in_forward && e->cur_slot == slot)
+    DLO_FAIL(DLO_ERR_STATE, "dlo_prefetch: slot %d is being read by block %d", slot,
+             e->cur_block);
+  return enqueue_prefetch(e, block, slot);
+}
+
+dlo_status dlo_wait(dlo_engine* e, int32_t block) {
+  using namespace dlo;
+  DLO_TRY(check_engine(e));
+  const int32_t s = slot_of(e, block);
+  if (s < 0) DLO_FAIL(DLO_ERR_STATE, "dlo_wait: block %d is in no slot", block);
+  DLO_CUDA(cudaStreamWaitEvent(e->compute, e->ready[s], 0));
+  return DLO_OK;
+}
+
+dlo_status dlo_wait_host(dlo_engine* e, int32_t block, int32_t timeout_ms) {
+  using namespace dlo;
+  DLO_TRY(check_engine(e));
+  const int32_t s = slot_of(e, block);
+  if (s < 0) DLO_FAIL(DLO_ERR_STATE, "dlo_wait_host: block %d is in no slot", block);
+  const auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    const cudaError_t q = cudaEventQuery(e->ready[s]);
+    if (q == cudaSuccess) return DLO_OK;
+    if (q != cudaErrorNotReady) DLO_CUDA(q);
+    const auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(
+                        std::chrono::steady_clock::now() - t0)
+                        .count();
+    if (ms >= timeout_ms)
+      DLO_FAIL(DLO_ERR_TIMEOUT, "dlo_wait_host: block %d not ready after %d ms", block,
+               timeout_ms);
+    std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+}
+
+dlo_status dlo_param_view(const dlo_engine* e, int32_t block, int32_t param, void** dev_ptr) {
+  using namespace dlo;
+  DLO_TRY(check_engine(e));
+  if (!dev_ptr) DLO_FAIL(DLO_ERR_INVALID, "dlo_param_view: null argument");
+  if (block < 0 || block >= e->n_blocks || !e->blocks[block].plan)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_param_view: block %d not registered", block);
+  const dlo_plan* p = e->blocks[block].plan;
+  if (param < 0 || param >= static_cast<int32_t>(p->params.size()))
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_param_view: param %d out of range", param);
+  const int32_t s = slot_of(e, block);
+  if (s < 0) DLO_FAIL(DLO_ERR_STATE, "dlo_param_view: block %d is in no slot", block);
+  *dev_ptr = e->slot[s] + p->params[param].slot_offset;
+  return DLO_OK;
+}
+
+dlo_status dlo_pre_forward(dlo_engine* e, int32_t block, int32_t* slot_out) {
+  using namespace dlo;
+  DLO_TRY(check_engine(e));
+  if (e->in_forward)
+    DLO_FAIL(DLO_ERR_STATE, "dlo_pre_forward: block %d has no post_forward yet", e->cur_block);
+  const int32_t n = e->n_blocks;
+  const int32_t expect = static_cast<int32_t>(e->k % n);
+  if (block != expect)
+    DLO_FAIL(DLO_ERR_STATE, "dlo_pre_forward: forward %lld must run block %d, not %d",
+             (long long)e->k, expect, block);
+  const int32_t next = (block + 1) % n;
+  if (!e->blocks[block].plan || !e->blocks[next].plan)
+    DLO_FAIL(DLO_ERR_STATE, "dlo_pre_forward: block %d or %d is not registered", block, next);
+  dlo_engine::Hook& h = e->hooks[block];
+  const dlo_engine::Hook& prev = e->hooks[(block + n - 1) % n];
+  int32_t slot = h.current_slot;
+  if (prev.prefetched_slot >= 0) slot = prev.prefetched_slot;
+  if (e->slot_holds[slot] != block)
+    DLO_FAIL(DLO_ERR_STATE, "dlo_pre_forward: slot %d holds block %d, not %d", slot,
+             e->slot_holds[slot], block);
+  DLO_CUDA(cudaStreamWaitEvent(e->compute, e->ready[slot], 0));
+  const int32_t ps = 1 - slot;
+  const int32_t waits = e->last_reader[ps];
+  DLO_TRY(enqueue_prefetch(e, next, ps));
+  h.current_slot = slot;
+  h.prefetched_slot = ps;
+  e->last_reader[slot] = static_cast<int32_t>(e->k);
+  dlo_sched_event ev;
+  ev.k = static_cast<int32_t>(e->k);
+  ev.block = block;
+  ev.read_slot = slot;
+  ev.prefetch_block = next;
+  ev.prefetch_slot = ps;
+  ev.waits_on_free_of_k = waits;
+  ev.copy_mode = e->chosen >= 0 ? e->chosen : DLO_COPY_AUTO;
+  e->log.push_back(ev);
+  e->in_forward = true;
+  e->cur_block = block;
+  e->cur_slot = slot;
+  if (slot_out) *slot_out = slot;
+  return DLO_OK;
+}
+
+dlo_status dlo_post_forward(dlo_engine* e, int32_t block) {
+  using namespace dlo;
+  DLO_TRY(check_engine(e));
+  if (!e->in_forward || block != e->cur_block)
+    DLO_FAIL(DLO_ERR_STATE, "dlo_post_forward: block %d is not the block in flight", block);
+  DLO_CUDA(cudaEventRecord(e->freed[e->cur_slot], e->compute));
+  e->in_forward = false;
+  e->k++;
+  return DLO_OK;
+}
+
+dlo_status dlo_block_forward(dlo_engine* e, int32_t block, const dlo_dit_cfg* cfg, float* x,
+                             void* scratch, size_t scratch_bytes) {
+  using namespace dlo;
+  DLO_TRY(check_engine(e));
+  int32_t slot = -1;
+  DLO_TRY(dlo_pre_forward(e, block, &slot));
+  const dlo_status st = forward_impl(cfg, e->blocks[block].plan, e->slot[slot], x, scratch,
+                                     scratch_bytes, e->compute);
+  // the free event is recorded even if a launch was refused, so that the
+  // schedule stays consistent; the error is still returned
+  const dlo_status st2 = dlo_post_forward(e, block);
+  return st != DLO_OK ? st : st2;
+}
+
+dlo_status dlo_schedule_log(const dlo_engine* e, dlo_sched_event* buf, int32_t cap,
+                            int32_t* n_out) {
+  using namespace dlo;
+  DLO_TRY(check_engine(e));
+  if (!n_out || (cap > 0 && !buf)) DLO_FAIL(DLO_ERR_INVALID, "dlo_schedule_log: null argument");
+  const int32_t n = static_cast<int32_t>(e->log.size());
+  const int32_t m = n < cap ? n : cap;
+  for (int32_t i = 0; i < m; ++i) buf[i] = e->log[i];
+  *n_out = n;
+  return DLO_OK;
+}
+
+dlo_status dlo_engine_query(dlo_engine* e, dlo_engine_stats* out) {
+  using namespace dlo;
+  DLO_TRY(check_engine(e));
+  if (!out) DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_query: null argument");
+  try_decide(e);
+  out->chosen_mode = e->chosen >= 0 ? e->chosen : DLO_COPY_AUTO;
+  out->n_forwards = static_cast<int32_t>(e->k);
+  out->n_prefetches = static_cast<int32_t>(e->n_prefetches);
+  out->dma_ns_per_mb = e->dma_ns_per_mb;
+  out->kernel_ns_per_mb = e->kernel_ns_per_mb;
+  return DLO_OK;
+}
+
+dlo_status dlo_engine_copy_times(dlo_engine* e, float* copy_ms, int64_t* copy_bytes, int32_t cap,
+                                 int32_t* n_out) {
+  using namespace dlo;
+  DLO_TRY(check_engine(e));
+  if (!n_out || (cap > 0 && (!copy_ms || !copy_bytes)))
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_copy_times: null argument");
+  int32_t n = 0;
+  for (const auto& t : e->timed) {
+    if (n < cap) {
+      DLO_CUDA(cudaEventSynchronize(t.b));
+      float ms = 0;
+      DLO_CUDA(cudaEventElapsedTime(&ms, t.a, t.b));
+      copy_ms[n] = ms;
+      copy_bytes[n] = t.bytes;
+    }
+    ++n;
+  }
+  *n_out = n;
+  return DLO_OK;
+}
+
+dlo_status dlo_engine_destroy(dlo_engine* e, int32_t timeout_ms) {
+  using namespace dlo;
+  if (!e) return DLO_OK;
+  // drain both streams (bounded): mark their current tails and poll
+  cudaEvent_t tail[2] = {nullptr, nullptr};
+  cudaStream_t st[2] = {e->copy, e->compute};
+  for (int i = 0; i < 2; ++i) {
+    DLO_CUDA(cudaEventCreateWithFlags(&tail[i], cudaEventDisableTiming));
+    DLO_CUDA(cudaEventRecord(tail[i], st[i]));
+  }
+  const auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    const cudaError_t q0 = cudaEventQuery(tail[0]);
+    const cudaError_t q1 = cudaEventQuery(tail[1]);
+    if (q0 == cudaSuccess && q1 == cudaSuccess) break;
+    if ((q0 != cudaSuccess && q0 != cudaErrorNotReady) ||
+        (q1 != cudaSuccess && q1 != cudaErrorNotReady)) {
+      cudaEventDestroy(tail[0]);
+      cudaEventDestroy(tail[1]);
+      DLO_FAIL(DLO_ERR_CUDA, "dlo_engine_destroy: stream error while draining");
+    }
+    const auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(
+                        std::chrono::steady_clock::now() - t0)
+                        .count();
+    if (ms >= timeout_ms) {
+      cudaEventDestroy(tail[0]);
+      cudaEventDestroy(tail[1]);
+      DLO_FAIL(DLO_ERR_TIMEOUT, "dlo_engine_destroy: streams not drained after %d ms",
+               timeout_ms);
+    }
+    std::this_thread::sleep_for(std::chrono::microseconds(100));
+  }
+  cudaEventDestroy(tail[0]);
+  cudaEventDestroy(tail[1]);
+  for (int s = 0; s < 2; ++s) {
+    cudaEventDestroy(e->ready[s]);
+    cudaEventDestroy(e->freed[s]);
+  }
+  for (auto& t : e->timed) {
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
+  for (auto& t : e->race) {
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
+  delete e;
+  return DLO_OK;
+}
+
+dlo_status dlo_reassemble(const dlo_plan* plan, const void* const* shard_ptrs, void* dst,
+                          int32_t mode, void* stream) {
+  using namespace dlo;
+  if (!plan || !shard_ptrs || !dst) DLO_FAIL(DLO_ERR_INVALID, "dlo_reassemble: null argument");
+  if (reinterpret_cast<uintptr_t>(dst) & 255u)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_reassemble: dst must be 256-byte aligned");
+  const size_t n = plan->groups.size() * static_cast<size_t>(plan->n_shards);
+  if (n > static_cast<size_t>(kMaxSegments))
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_reassemble: too many (group, shard) pieces");
+  dlo_engine::Block b;
+  b.plan = plan;
+  b.host.assign(shard_ptrs, shard_ptrs + n);
+  b.dev.assign(n, nullptr);
+  for (size_t i = 0; i < n; ++i) {
+    const void* q = shard_ptrs[i];
+    if (!q || (reinterpret_cast<uintptr_t>(q) & 15u))
+      DLO_FAIL(DLO_ERR_INVALID, "dlo_reassemble: shard %zu null or not 16-byte aligned", i);
+    if (mode == DLO_COPY_KERNEL) {
+      cudaPointerAttributes a{};
+      if (cudaPointerGetAttributes(&a, q) != cudaSuccess || a.type != cudaMemoryTypeHost ||
+          !a.devicePointer) {
+        cudaGetLastError();
+        DLO_FAIL(DLO_ERR_INVALID, "dlo_reassemble: shard %zu is not mapped pinned memory", i);
+      }
+      b.dev[i] = a.devicePointer;
+    }
+  }
+  const int32_t m = mode == DLO_COPY_KERNEL ? DLO_COPY_KERNEL : DLO_COPY_DMA;
+  return copy_block(b, static_cast<uint8_t*>(dst), m, 0, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,145 @@
+// forward.cu — the synthetic DiT block forward over weights laid out as a
+// slot, and the single-step entry points used by the per-kernel checks.
+//
+// The pages run the block forward on a compute stream that waits for the
+// gather event ("Distributed Layerwise Offload" (vLLM blog preview,
+// 2026-07-30), "Weight Sharding + AllGather", step 4) with parameters
+// re-pointed into the gathered buffer (step 3).  Here the re-pointing is the
+// plan's slot offsets added to the slot's base; the forward is seven
+// launches on one stream:
+//   rmsnorm_mod -> linear(qkv, bf16) -> attention -> linear(out, gated
+//   residual) -> rmsnorm_mod -> linear(fc1, GELU) -> linear(fc2, gated
+//   residual).
+#include "common.h"
+
+namespace dlo {
+namespace {
+
+struct ScratchLayout {
+  size_t h, qkv, o, u, total;
+};
+
+ScratchLayout scratch_layout(const dlo_dit_cfg& c) {
+  const size_t M = static_cast<size_t>(c.batch) * c.tokens;
+  const size_t d = c.hidden, f = c.mlp;
+  auto r = [](size_t v) { return (v + 255) / 256 * 256; };
+  ScratchLayout s;
+  s.h = 0;
+  s.qkv = r(s.h + M * d * 2);
+  s.o = r(s.qkv + M * 3 * d * 2);
+  s.u = r(s.o + M * d * 2);
+  s.total = r(s.u + M * f * 2);
+  return s;
+}
+
+dlo_status check_cfg(const dlo_dit_cfg* c) {
+  if (!c) DLO_FAIL(DLO_ERR_INVALID, "forward: null config");
+  if (c->batch < 1 || c->tokens < 1 || c->hidden < 64 || c->heads < 1 || c->mlp < 64)
+    DLO_FAIL(DLO_ERR_INVALID, "forward: batch/tokens/hidden/heads/mlp out of range");
+  if (c->hidden % 64 != 0 || c->mlp % 64 != 0)
+    DLO_FAIL(DLO_ERR_INVALID, "forward: hidden (%d) and mlp (%d) must be multiples of 64",
+             c->hidden, c->mlp);
+  if (c->hidden % c->heads != 0 ||
+      (c->hidden / c->heads != 64 && c->hidden / c->heads != 128))
+    DLO_FAIL(DLO_ERR_INVALID, "forward: head dim %d x %d not supported (64 or 128)",
+             c->hidden, c->heads);
+  if (!(c->eps >= 0.f)) DLO_FAIL(DLO_ERR_INVALID, "forward: eps must be >= 0");
+  return DLO_OK;
+}
+
+dlo_status check_plan(const dlo_dit_cfg& c, const dlo_plan* plan) {
+  if (!plan) DLO_FAIL(DLO_ERR_INVALID, "forward: null plan");
+  if (!plan->has_dit_roles)
+    DLO_FAIL(DLO_ERR_INVALID, "forward: the plan's parameter names are not the DiT block's");
+  const int64_t d = c.hidden, f = c.mlp;
+  struct Want { int role; int32_t dtype; int64_t a, b; };
+  const Want want[] = {
+      {R_G1, DLO_F32, d, 0},      {R_SHIFT1, DLO_F32, d, 0}, {R_SCALE1, DLO_F32, d, 0},
+      {R_GATE1, DLO_F32, d, 0},   {R_WQKV, DLO_BF16, 3 * d, d}, {R_WO, DLO_BF16, d, d},
+      {R_G2, DLO_F32, d, 0},      {R_SHIFT2, DLO_F32, d, 0}, {R_SCALE2, DLO_F32, d, 0},
+      {R_GATE2, DLO_F32, d, 0},   {R_W1, DLO_BF16, f, d},    {R_W2, DLO_BF16, d, f}};
+  for (const Want& w : want) {
+    const auto& p = plan->params[plan->role[w.role]];
+    const bool ok = p.dtype == w.dtype &&
+                    (w.b == 0 ? (p.ndim == 1 && p.shape[0] == w.a)
+                              : (p.ndim == 2 && p.shape[0] == w.a && p.shape[1] == w.b));
+    if (!ok) DLO_FAIL(DLO_ERR_INVALID, "forward: parameter %s has the wrong shape or dtype",
+                      kRoleNames[w.role]);
+    if (p.slot_offset % 16 != 0)
+      DLO_FAIL(DLO_ERR_INVALID, "forward: parameter %s is not 16-byte aligned in the slot",
+               kRoleNames[w.role]);
+  }
+  return DLO_OK;
+}
+
+}  // namespace
+
+dlo_status forward_impl(const dlo_dit_cfg* cfg, const dlo_plan* plan, const void* block_base,
+                        float* x, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
+  DLO_TRY(check_cfg(cfg));
+  DLO_TRY(check_plan(*cfg, plan));
+  const ScratchLayout sl = scratch_layout(*cfg);
+  if (!block_base || !x || !scratch) DLO_FAIL(DLO_ERR_INVALID, "forward: null pointer");
+  if (reinterpret_cast<uintptr_t>(block_base) & 255u)
+    DLO_FAIL(DLO_ERR_INVALID, "forward: block base must be 256-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(scratch) & 255u))
+    DLO_FAIL(DLO_ERR_INVALID, "forward: x must be 16-byte and scratch 256-byte aligned");
+  if (scratch_bytes < sl.total)
+    DLO_FAIL(DLO_ERR_NOMEM, "forward: scratch holds %zu bytes, needs %zu", scratch_bytes,
+             sl.total);
+  const uint8_t* base = static_cast<const uint8_t*>(block_base);
+  auto W = [&](int role) { return base + plan->params[plan->role[role]].slot_offset; };
+  auto F = [&](int role) { return reinterpret_cast<const float*>(W(role)); };
+  auto H = [&](int role) { return reinterpret_cast<const uint16_t*>(W(role)); };
+  uint8_t* s = static_cast<uint8_t*>(scratch);
+  uint16_t* h = reinterpret_cast<uint16_t*>(s + sl.h);
+  uint16_t* qkv = reinterpret_cast<uint16_t*>(s + sl.qkv);
+  uint16_t* o = reinterpret_cast<uint16_t*>(s + sl.o);
+  uint16_t* u = reinterpret_cast<uint16_t*>(s + sl.u);
+  const int64_t M = static_cast<int64_t>(cfg->batch) * cfg->tokens;
+  const int64_t d = cfg->hidden, f = cfg->mlp;
+  DLO_TRY(launch_rmsnorm_mod(x, M, d, F(R_G1), F(R_SHIFT1), F(R_SCALE1), cfg->eps, h, stream));
+  DLO_TRY(launch_linear(h, M, d, H(R_WQKV), 3 * d, EPI_BF16, qkv, nullptr, stream));
+  DLO_TRY(launch_attention(qkv, cfg->batch, cfg->tokens, d, cfg->heads, o, stream));
+  DLO_TRY(launch_linear(o, M, d, H(R_WO), d, EPI_RESID_F32, x, F(R_GATE1), stream));
+  DLO_TRY(launch_rmsnorm_mod(x, M, d, F(R_G2), F(R_SHIFT2), F(R_SCALE2), cfg->eps, h, stream));
+  DLO_TRY(launch_linear(h, M, d, H(R_W1), f, EPI_GELU_BF16, u, nullptr, stream));
+  DLO_TRY(launch_linear(u, M, f, H(R_W2), d, EPI_RESID_F32, x, F(R_GATE2), stream));
+  return DLO_OK;
+}
+
+}  // namespace dlo
+
+extern "C" {
+
+size_t dlo_forward_scratch_bytes(const dlo_dit_cfg* cfg) {
+  if (dlo::check_cfg(cfg) != DLO_OK) return 0;
+  return dlo::scratch_layout(*cfg).total;
+}
+
+dlo_status dlo_forward(const dlo_dit_cfg* cfg, const dlo_plan* plan, const void* block_base,
+                       float* x, void* scratch, size_t scratch_bytes, void* stream) {
+  return dlo::forward_impl(cfg, plan, block_base, x, scratch, scratch_bytes,
+                           static_cast<cudaStream_t>(stream));
+}
+
+dlo_status dlo_op_rmsnorm_mod(const float* x, int64_t rows, int64_t d, const float* g,
+                              const float* shift, const float* scale, float eps, uint16_t* h,
+                              void* stream) {
+  return dlo::launch_rmsnorm_mod(x, rows, d, g, shift, scale, eps, h,
+                                 static_cast<cudaStream_t>(stream));
+}
+
+dlo_status dlo_op_linear(const uint16_t* a, int64_t M, int64_t K, const uint16_t* w, int64_t N,
+                         int32_t epilogue, void* out, const float* gate, void* stream) {
+  return dlo::launch_linear(a, M, K, w, N, epilogue, out, gate,
+                            static_cast<cudaStream_t>(stream));
+}
+
+dlo_status dlo_op_attention(const uint16_t* qkv, int64_t batch, int64_t tokens, int64_t d,
+                            int64_t heads, uint16_t* o, void* stream) {
+  return dlo::launch_attention(qkv, batch, tokens, d, heads, o,
+                               static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

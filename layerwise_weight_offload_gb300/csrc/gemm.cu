@@ -1,0 +1,370 @@
+// gemm.cu — the block's linears on the 5th-generation tensor cores.
+//
+// out = epilogue(A W^T): A bf16 [M, K] (activations, K contiguous), W bf16
+// [N, K] (a weight view inside a slot, nn.Linear layout, K contiguous), fp32
+// accumulation in tensor memory.  Epilogues: store bf16; GELU-tanh then
+// store bf16; gated residual x[M, N] += gate[N] * acc in fp32.
+//
+// Structure (one CTA per SM, persistent over 128 x 256 output tiles):
+//   warp 0     TMA producer: 128x64 A box and 256x64 W box per stage,
+//              128-byte swizzled, 4-stage ring guarded by full/empty
+//              mbarriers;
+//   warp 1     allocates 512 TMEM columns (two 256-column fp32
+//              accumulators) and one thread issues tcgen05.mma
+//              (M=128, N=256, K=16, kind::f16) and tcgen05.commit;
+//   warps 2-5  epilogue: tcgen05.ld of their 32-lane quarter, the fused
+//              epilogue, stores to global; they release the accumulator so
+//              the next tile's MMAs overlap this tile's epilogue.
+// Ragged M, N and K are covered by TMA zero fill and epilogue masks.  No
+// split-K and no atomics: every output element is produced by one thread in
+// a fixed order, so results do not depend on addresses or scheduling.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "common.h"
+#include "ptx.cuh"
+
+namespace dlo {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int B_BYTES = BN * BK * 2;          // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+
+__device__ __forceinline__ void record_failure(int* err, volatile int* abort, int code) {
+  atomicCAS(err, 0, code);
+  *abort = 1;
+}
+
+__device__ __forceinline__ float gelu_tanh(float z) {
+  const float k0 = 0.7978845608028654f;   // sqrt(2/pi)
+  const float k1 = 0.044715f;
+  return 0.5f * z * (1.f + tanhf(k0 * (z + k1 * z * z * z)));
+}
+
+template <int EPI>
+__device__ __forceinline__ void epilogue_store(const uint32_t (&r)[32], int64_t row, int64_t n0,
+                                               int64_t N, void* out, const float* gate) {
+  if (EPI == EPI_RESID_F32) {
+    float* xr = static_cast<float*>(out) + row * N + n0;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      if (n0 + 4 * g + 4 <= N) {
+        float4 xv = *reinterpret_cast<float4*>(xr + 4 * g);
+        const float4 gv = __ldg(reinterpret_cast<const float4*>(gate + n0 + 4 * g));
+        xv.x += gv.x * __uint_as_float(r[4 * g + 0]);
+        xv.y += gv.y * __uint_as_float(r[4 * g + 1]);
+        xv.z += gv.z * __uint_as_float(r[4 * g + 2]);
+        xv.w += gv.w * __uint_as_float(r[4 * g + 3]);
+        *reinterpret_cast<float4*>(xr + 4 * g) = xv;
+      }
+    }
+  } else {
+    uint32_t pk[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      float a = __uint_as_float(r[2 * j]), b = __uint_as_float(r[2 * j + 1]);
+      if (EPI == EPI_GELU_BF16) {
+        a = gelu_tanh(a);
+        b = gelu_tanh(b);
+      }
+      __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
+      pk[j] = *reinterpret_cast<uint32_t*>(&p);
+    }
+    uint16_t* orow = static_cast<uint16_t*>(out) + row * N + n0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (n0 + 8 * g + 8 <= N)
+        *reinterpret_cast<uint4*>(orow + 8 * g) =
+            make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
+                    const __grid_constant__ CUtensorMap tma_b, int M, int N, int K, void* out,
+                    const float* gate, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tma_a);
+    tma_prefetch_desc(&tma_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_m = (M + BM - 1) / BM;
+  const int num_n = (N + BN - 1) / BN;
+  const int num_tiles = num_m * num_n;
+  const int num_k = (K + BK - 1) / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int m_idx = tile % num_m, n_idx = tile / num_m;
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort)) {
+            record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_PRODUCER);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          tma_load_2d(sA + stage * A_BYTES, &tma_a, &full[stage], kb * BK, m_idx * BM);
+          tma_load_2d(sB + stage * B_BYTES, &tma_b, &full[stage], kb * BK, n_idx * BN);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // let the loads already issued land before the CTA's shared memory
+        // can be handed to another CTA (bounded; no abort check)
+        volatile int never = 0;
+        for (int back = 1; back <= STAGES && back <= issued; ++back) {
+          int s = stage - back;
+          uint32_t ph = phase;
+          if (s < 0) {
+            s += STAGES;
+            ph ^= 1u;
+          }
+          mbar_wait_bounded(&full[s], ph, &never);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort)) {
+          record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_MMA_EMPTY);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait_bounded(&full[stage], phase, abort)) {
+            record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_MMA_FULL);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * A_BYTES);
+          const uint32_t b_addr = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16(d_tmem, sdesc_k_sw128(a_addr + kk * 32), sdesc_k_sw128(b_addr + kk * 32),
+                      idesc, (kb | kk) != 0 ? 1u : 0u);
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        // wait (bounded) for every MMA already issued before TMEM is freed
+        volatile int never = 0;
+        umma_commit(drain);
+        mbar_wait_bounded(drain, 0, &never);
+      }
+    }
+  } else {
+    const int quad = warp & 3;   // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int m_idx = tile % num_m, n_idx = tile / num_m;
+      if (!mbar_wait_bounded(&tfull[acc], acc_phase, abort)) {
+        if (lane == 0) record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_EPILOGUE);
+        break;
+      }
+      tc_fence_after();
+      const int64_t row = static_cast<int64_t>(m_idx) * BM + quad * 32 + lane;
+      const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) +
+                             (static_cast<uint32_t>(quad * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int64_t n0 = static_cast<int64_t>(n_idx) * BN + c * 32;
+        if (n0 >= N) break;
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + c * 32, r);
+        tmem_ld_wait();
+        if (row < M) epilogue_store<EPI>(r, row, n0, N, out, gate);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] (cols contiguous) as TMA boxes of
+// box_rows x 64 with 128-byte swizzle; out-of-range elements read as zero.
+dlo_status make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols,
+                    uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) DLO_FAIL(DLO_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    DLO_FAIL(DLO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %lld x %lld at %p", (int)r,
+             (long long)rows, (long long)cols, ptr);
+  return DLO_OK;
+}
+
+int sm_count() {
+  static int n = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 152;
+  });
+  return n;
+}
+
+template <int EPI>
+dlo_status launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int K,
+                      void* out, const float* gate, int* err, cudaStream_t stream) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_tcgen05_kernel<EPI>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  });
+  DLO_CUDA(attr_err);
+  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int grid = tiles < sm_count() ? tiles : sm_count();
+  gemm_tcgen05_kernel<EPI><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ma, mb, M, N, K, out, gate,
+                                                                      err);
+  DLO_CUDA(cudaGetLastError());
+  return DLO_OK;
+}
+
+}  // namespace
+
+dlo_status launch_linear(const uint16_t* a, int64_t M, int64_t K, const uint16_t* w, int64_t N,
+                         int epilogue, void* out, const float* gate, cudaStream_t stream) {
+  if (M == 0) return DLO_OK;
+  if (!a || !w || !out || M < 0 || K <= 0 || N <= 0)
+    DLO_FAIL(DLO_ERR_INVALID, "linear: bad arguments (M %lld, K %lld, N %lld)", (long long)M,
+             (long long)K, (long long)N);
+  if (K % 8 != 0 || N % 8 != 0)
+    DLO_FAIL(DLO_ERR_INVALID, "linear: K (%lld) and N (%lld) must be multiples of 8",
+             (long long)K, (long long)N);
+  if (M > (1LL << 31) - 1 || N > (1LL << 31) - 1 || K > (1LL << 31) - 1)
+    DLO_FAIL(DLO_ERR_INVALID, "linear: extent too large");
+  if ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(w) |
+       reinterpret_cast<uintptr_t>(out)) & 15u)
+    DLO_FAIL(DLO_ERR_INVALID, "linear: a, w and out must be 16-byte aligned");
+  if (epilogue == EPI_RESID_F32 && (!gate || (reinterpret_cast<uintptr_t>(gate) & 15u)))
+    DLO_FAIL(DLO_ERR_INVALID, "linear: the residual epilogue needs a 16-byte aligned gate");
+  int* err = device_error_word();
+  if (!err) DLO_FAIL(DLO_ERR_CUDA, "linear: cannot resolve the device error word");
+  CUtensorMap ma, mb;
+  DLO_TRY(make_map(&ma, a, M, K, BM));
+  DLO_TRY(make_map(&mb, w, N, K, BN));
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  switch (epilogue) {
+    case EPI_BF16: return launch_epi<EPI_BF16>(ma, mb, m, n, k, out, gate, err, stream);
+    case EPI_GELU_BF16: return launch_epi<EPI_GELU_BF16>(ma, mb, m, n, k, out, gate, err, stream);
+    case EPI_RESID_F32: return launch_epi<EPI_RESID_F32>(ma, mb, m, n, k, out, gate, err, stream);
+    default: DLO_FAIL(DLO_ERR_INVALID, "linear: unknown epilogue %d", epilogue);
+  }
+}
+
+}  // namespace dlo

@@ -1,0 +1,353 @@
+"""ctypes binding of ``libdlo.so`` (include/dlo.h): argument marshalling only.
+
+Every function keeps the C name without the ``dlo_`` prefix, takes plain
+integers (device or host addresses, e.g. ``tensor.data_ptr()``) or objects
+with ``data_ptr()``, and raises :class:`DLOError` when the C call returns a
+non-zero status.  All computation happens in the library's CUDA kernels; if
+the library cannot be loaded this module raises at import of the library,
+there is no fallback.
+"""
+import ctypes
+import os
+import re
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libdlo.so")
+
+OK, ERR_INVALID, ERR_CUDA, ERR_TIMEOUT, ERR_STATE, ERR_NOMEM = range(6)
+BF16, F32 = 0, 1
+COPY_AUTO, COPY_DMA, COPY_KERNEL = 0, 1, 2
+EPI_BF16, EPI_GELU_BF16, EPI_RESID_F32 = 0, 1, 2
+COPY_MODE_NAMES = {COPY_AUTO: "auto", COPY_DMA: "dma", COPY_KERNEL: "kernel"}
+
+
+class DLOError(RuntimeError):
+    def __init__(self, status, where, message):
+        super().__init__("%s failed with status %d: %s" % (where, status, message))
+        self.status = status
+
+
+c_i32, c_i64, c_vp, c_sz, c_f32 = (ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p,
+                                   ctypes.c_size_t, ctypes.c_float)
+
+
+class ParamDesc(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("ndim", c_i32), ("shape", c_i64 * 4),
+                ("dtype", c_i32)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("n_params", c_i32), ("n_groups", c_i32), ("n_shards", c_i32),
+                ("has_dit_roles", c_i32), ("slot_bytes", c_i64), ("group_align", c_i64)]
+
+
+class GroupInfo(ctypes.Structure):
+    _fields_ = [("dtype", c_i32), ("esize", c_i32), ("numel", c_i64), ("shard_numel", c_i64),
+                ("shard_bytes", c_i64), ("shard_alloc_bytes", c_i64), ("base", c_i64)]
+
+
+class ParamInfo(ctypes.Structure):
+    _fields_ = [("group", c_i32), ("dtype", c_i32), ("numel", c_i64), ("group_offset", c_i64),
+                ("slot_offset", c_i64)]
+
+
+class DitCfg(ctypes.Structure):
+    _fields_ = [("batch", c_i32), ("tokens", c_i32), ("hidden", c_i32), ("heads", c_i32),
+                ("mlp", c_i32), ("eps", c_f32)]
+
+
+class EngineDesc(ctypes.Structure):
+    _fields_ = [("n_blocks", c_i32), ("slot", c_vp * 2), ("slot_bytes", c_i64),
+                ("compute_stream", c_vp), ("copy_stream", c_vp), ("copy_mode", c_i32),
+                ("copy_ctas", c_i32), ("timing", c_i32)]
+
+
+class SchedEvent(ctypes.Structure):
+    _fields_ = [("k", c_i32), ("block", c_i32), ("read_slot", c_i32), ("prefetch_block", c_i32),
+                ("prefetch_slot", c_i32), ("waits_on_free_of_k", c_i32), ("copy_mode", c_i32)]
+
+
+class EngineStats(ctypes.Structure):
+    _fields_ = [("chosen_mode", c_i32), ("n_forwards", c_i32), ("n_prefetches", c_i32),
+                ("dma_ns_per_mb", ctypes.c_double), ("kernel_ns_per_mb", ctypes.c_double)]
+
+
+_P = ctypes.POINTER
+_SIGS = {
+    "dlo_plan_create": (c_i32, [_P(ParamDesc), c_i32, c_i32, _P(c_vp)]),
+    "dlo_plan_query": (c_i32, [c_vp, _P(PlanInfo)]),
+    "dlo_plan_group": (c_i32, [c_vp, c_i32, _P(GroupInfo)]),
+    "dlo_plan_param": (c_i32, [c_vp, c_i32, _P(ParamInfo)]),
+    "dlo_shard_host": (c_i32, [c_vp, _P(c_vp), _P(c_vp)]),
+    "dlo_plan_destroy": (None, [c_vp]),
+    "dlo_reassemble": (c_i32, [c_vp, _P(c_vp), c_vp, c_i32, c_vp]),
+    "dlo_forward_scratch_bytes": (c_sz, [_P(DitCfg)]),
+    "dlo_forward": (c_i32, [_P(DitCfg), c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "dlo_op_rmsnorm_mod": (c_i32, [c_vp, c_i64, c_i64, c_vp, c_vp, c_vp, c_f32, c_vp, c_vp]),
+    "dlo_op_linear": (c_i32, [c_vp, c_i64, c_i64, c_vp, c_i64, c_i32, c_vp, c_vp, c_vp]),
+    "dlo_op_attention": (c_i32, [c_vp, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp]),
+    "dlo_engine_create": (c_i32, [_P(EngineDesc), _P(c_vp)]),
+    "dlo_register_block": (c_i32, [c_vp, c_i32, c_vp, _P(c_vp)]),
+    "dlo_prefetch": (c_i32, [c_vp, c_i32, c_i32]),
+    "dlo_wait": (c_i32, [c_vp, c_i32]),
+    "dlo_wait_host": (c_i32, [c_vp, c_i32, c_i32]),
+    "dlo_param_view": (c_i32, [c_vp, c_i32, c_i32, _P(c_vp)]),
+    "dlo_pre_forward": (c_i32, [c_vp, c_i32, _P(c_i32)]),
+    "dlo_post_forward": (c_i32, [c_vp, c_i32]),
+    "dlo_block_forward": (c_i32, [c_vp, c_i32, _P(DitCfg), c_vp, c_vp, c_sz]),
+    "dlo_schedule_log": (c_i32, [c_vp, _P(SchedEvent), c_i32, _P(c_i32)]),
+    "dlo_engine_query": (c_i32, [c_vp, _P(EngineStats)]),
+    "dlo_engine_copy_times": (c_i32, [c_vp, _P(c_f32), _P(c_i64), c_i32, _P(c_i32)]),
+    "dlo_engine_destroy": (c_i32, [c_vp, c_i32]),
+    "dlo_kernel_status": (c_i32, [_P(c_i32)]),
+    "dlo_last_error": (ctypes.c_char_p, []),
+    "dlo_version": (ctypes.c_char_p, []),
+}
+
+_lib = None
+
+
+def lib():
+    """Loads libdlo.so (built by ``layerwise_weight_offload_gb300.build``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError("libdlo.so is not built (run __graft_entry__.build() or "
+                              "python -m layerwise_weight_offload_gb300.build); "
+                              "there is no fallback path")
+        L = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def header_symbols(path=None):
+    """Names of the functions include/dlo.h declares."""
+    path = path or os.path.join(os.path.dirname(_PKG), "include", "dlo.h")
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dlo_[a-z_0-9]+)\s*\(", text)))
+
+
+def _check(status, where):
+    if status != OK:
+        msg = lib().dlo_last_error()
+        raise DLOError(status, where, msg.decode() if msg else "")
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
+    raise TypeError("cannot take the address of %r" % type(x))
+
+
+def _ptrs(xs):
+    return (c_vp * len(xs))(*[_ptr(x) for x in xs])
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def last_error():
+    return lib().dlo_last_error().decode()
+
+
+def version():
+    return lib().dlo_version().decode()
+
+
+# ---- plan ------------------------------------------------------------------
+
+class Plan:
+    def __init__(self, descs, n_shards):
+        """descs: sequence of (name, shape, dtype code) in registration order."""
+        self._names = [d[0].encode() for d in descs]
+        arr = (ParamDesc * len(descs))()
+        for i, (name, shape, code) in enumerate(descs):
+            arr[i].name = self._names[i]
+            arr[i].ndim = len(shape)
+            for j, v in enumerate(shape):
+                arr[i].shape[j] = int(v)
+            arr[i].dtype = int(code)
+        h = c_vp()
+        _check(lib().dlo_plan_create(arr, len(descs), int(n_shards), ctypes.byref(h)),
+               "dlo_plan_create")
+        self.handle = h.value
+        self.n_shards = int(n_shards)
+
+    def info(self):
+        out = PlanInfo()
+        _check(lib().dlo_plan_query(self.handle, ctypes.byref(out)), "dlo_plan_query")
+        return out
+
+    def group(self, g):
+        out = GroupInfo()
+        _check(lib().dlo_plan_group(self.handle, g, ctypes.byref(out)), "dlo_plan_group")
+        return out
+
+    def param(self, p):
+        out = ParamInfo()
+        _check(lib().dlo_plan_param(self.handle, p, ctypes.byref(out)), "dlo_plan_param")
+        return out
+
+    def groups(self):
+        return [self.group(g) for g in range(self.info().n_groups)]
+
+    def shard_host(self, param_srcs, shard_dsts):
+        _check(lib().dlo_shard_host(self.handle, _ptrs(param_srcs), _ptrs(shard_dsts)),
+               "dlo_shard_host")
+
+    def destroy(self):
+        if self.handle:
+            lib().dlo_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def plan_create(descs, n_shards):
+    return Plan(descs, n_shards)
+
+
+def reassemble(plan, shard_ptrs, dst, mode=COPY_DMA, stream=None):
+    _check(lib().dlo_reassemble(plan.handle, _ptrs(shard_ptrs), _ptr(dst), int(mode),
+                                _stream(stream)), "dlo_reassemble")
+
+
+# ---- block forward -----------------------------------------------------------
+
+def dit_cfg(batch, tokens, hidden, heads, mlp, eps=1e-6):
+    return DitCfg(int(batch), int(tokens), int(hidden), int(heads), int(mlp), float(eps))
+
+
+def forward_scratch_bytes(cfg):
+    return int(lib().dlo_forward_scratch_bytes(ctypes.byref(cfg)))
+
+
+def forward(cfg, plan, block_base, x, scratch, scratch_bytes, stream=None):
+    _check(lib().dlo_forward(ctypes.byref(cfg), plan.handle, _ptr(block_base), _ptr(x),
+                             _ptr(scratch), int(scratch_bytes), _stream(stream)), "dlo_forward")
+
+
+def op_rmsnorm_mod(x, rows, d, g, shift, scale, eps, h, stream=None):
+    _check(lib().dlo_op_rmsnorm_mod(_ptr(x), rows, d, _ptr(g), _ptr(shift), _ptr(scale),
+                                    float(eps), _ptr(h), _stream(stream)), "dlo_op_rmsnorm_mod")
+
+
+def op_linear(a, M, K, w, N, epilogue, out, gate=None, stream=None):
+    _check(lib().dlo_op_linear(_ptr(a), M, K, _ptr(w), N, int(epilogue), _ptr(out), _ptr(gate),
+                               _stream(stream)), "dlo_op_linear")
+
+
+def op_attention(qkv, batch, tokens, d, heads, o, stream=None):
+    _check(lib().dlo_op_attention(_ptr(qkv), batch, tokens, d, heads, _ptr(o), _stream(stream)),
+           "dlo_op_attention")
+
+
+def kernel_status():
+    v = c_i32()
+    _check(lib().dlo_kernel_status(ctypes.byref(v)), "dlo_kernel_status")
+    return v.value
+
+
+# ---- engine ------------------------------------------------------------------
+
+class Engine:
+    def __init__(self, n_blocks, slot0, slot1, slot_bytes, compute_stream, copy_stream,
+                 copy_mode=COPY_AUTO, copy_ctas=0, timing=False):
+        d = EngineDesc()
+        d.n_blocks = int(n_blocks)
+        d.slot[0] = _ptr(slot0)
+        d.slot[1] = _ptr(slot1)
+        d.slot_bytes = int(slot_bytes)
+        d.compute_stream = _stream(compute_stream)
+        d.copy_stream = _stream(copy_stream)
+        d.copy_mode = int(copy_mode)
+        d.copy_ctas = int(copy_ctas)
+        d.timing = 1 if timing else 0
+        h = c_vp()
+        _check(lib().dlo_engine_create(ctypes.byref(d), ctypes.byref(h)), "dlo_engine_create")
+        self.handle = h.value
+        self.n_blocks = int(n_blocks)
+
+    def register_block(self, block, plan, shard_ptrs):
+        _check(lib().dlo_register_block(self.handle, block, plan.handle, _ptrs(shard_ptrs)),
+               "dlo_register_block")
+
+    def prefetch(self, block, slot):
+        _check(lib().dlo_prefetch(self.handle, block, slot), "dlo_prefetch")
+
+    def wait(self, block):
+        _check(lib().dlo_wait(self.handle, block), "dlo_wait")
+
+    def wait_host(self, block, timeout_ms):
+        _check(lib().dlo_wait_host(self.handle, block, int(timeout_ms)), "dlo_wait_host")
+
+    def param_view(self, block, param):
+        out = c_vp()
+        _check(lib().dlo_param_view(self.handle, block, param, ctypes.byref(out)),
+               "dlo_param_view")
+        return out.value
+
+    def pre_forward(self, block):
+        s = c_i32()
+        _check(lib().dlo_pre_forward(self.handle, block, ctypes.byref(s)), "dlo_pre_forward")
+        return s.value
+
+    def post_forward(self, block):
+        _check(lib().dlo_post_forward(self.handle, block), "dlo_post_forward")
+
+    def block_forward(self, block, cfg, x, scratch, scratch_bytes):
+        _check(lib().dlo_block_forward(self.handle, block, ctypes.byref(cfg), _ptr(x),
+                                       _ptr(scratch), int(scratch_bytes)), "dlo_block_forward")
+
+    def schedule_log(self):
+        n = c_i32()
+        _check(lib().dlo_schedule_log(self.handle, None, 0, ctypes.byref(n)), "dlo_schedule_log")
+        buf = (SchedEvent * max(1, n.value))()
+        _check(lib().dlo_schedule_log(self.handle, buf, n.value, ctypes.byref(n)),
+               "dlo_schedule_log")
+        return [(e.k, e.block, e.read_slot, e.prefetch_block, e.prefetch_slot,
+                 e.waits_on_free_of_k, e.copy_mode) for e in buf[:n.value]]
+
+    def query(self):
+        s = EngineStats()
+        _check(lib().dlo_engine_query(self.handle, ctypes.byref(s)), "dlo_engine_query")
+        return s
+
+    def copy_times(self):
+        n = c_i32()
+        _check(lib().dlo_engine_copy_times(self.handle, None, None, 0, ctypes.byref(n)),
+               "dlo_engine_copy_times")
+        ms = (c_f32 * max(1, n.value))()
+        by = (c_i64 * max(1, n.value))()
+        _check(lib().dlo_engine_copy_times(self.handle, ms, by, n.value, ctypes.byref(n)),
+               "dlo_engine_copy_times")
+        return list(ms[:n.value]), list(by[:n.value])
+
+    def destroy(self, timeout_ms=60000):
+        if self.handle:
+            _check(lib().dlo_engine_destroy(self.handle, int(timeout_ms)), "dlo_engine_destroy")
+            self.handle = None
+
+
+def engine_create(*args, **kw):
+    return Engine(*args, **kw)

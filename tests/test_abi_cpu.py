@@ -1,0 +1,132 @@
+"""C-ABI checks that need no GPU: the library loads and exports every symbol
+the header declares; the plan's layout and the host sharding agree with the
+oracle byte for byte; bad arguments fail closed with a status."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+from tests._util import build_lib
+from layerwise_weight_offload_gb300 import dlo, workloads as W
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build_lib()
+
+
+def test_library_exports_every_header_symbol():
+    names = dlo.header_symbols()
+    assert len(names) >= 25
+    L = dlo.lib()
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+    # every declared function has a binding signature
+    assert set(names) <= set(dlo._SIGS), set(names) - set(dlo._SIGS)
+    assert "sm_103a" in dlo.version()
+
+
+def _descs_random(rng, n_params):
+    descs = []
+    for i in range(n_params):
+        code = int(rng.integers(0, 2))
+        ndim = int(rng.integers(1, 3))
+        shape = tuple(int(v) for v in rng.integers(1, 9, size=ndim))
+        descs.append(("p%d" % i, shape, code))
+    return descs
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_plan_layout_and_shards_match_oracle(seed):
+    rng = np.random.default_rng(seed)
+    descs = _descs_random(rng, int(rng.integers(1, 7)))
+    s = int(rng.integers(1, 9))
+    plan = dlo.Plan(descs, s)
+    info = plan.info()
+    numels = [int(np.prod(sh)) for _, sh, _ in descs]
+    codes = [c for _, _, c in descs]
+    esizes = [W.ESIZE[c] for c in codes]
+    raw = [rng.integers(0, 256, size=n * e, dtype=np.uint8) for n, e in zip(numels, esizes)]
+    image, gdt, gbase, used = oracle.slot_image(raw, numels, codes, esizes, s, 256)
+    assert info.slot_bytes == used
+    assert info.n_groups == len(gdt)
+    shards = []
+    for gi, g in enumerate(plan.groups()):
+        assert g.dtype == gdt[gi] and g.base == gbase[gi]
+        assert g.shard_numel == oracle.shard_numel(g.numel, s)
+        assert g.shard_alloc_bytes % 16 == 0 and g.shard_alloc_bytes >= g.shard_bytes
+        shards += [np.full(g.shard_alloc_bytes, 0xEE, np.uint8) for _ in range(s)]
+    plan.shard_host([r.ctypes.data for r in raw], [x.ctypes.data for x in shards])
+    # each host shard equals the oracle's shard, then zeros to the 16-byte end
+    for gi, g in enumerate(plan.groups()):
+        flat = oracle.flatten_group(list(zip(raw, numels, codes)), g.dtype, g.esize)
+        ref = oracle.shard(flat, g.numel, g.esize, s)
+        for r in range(s):
+            got = shards[gi * s + r]
+            assert np.array_equal(got[:g.shard_bytes], ref[r])
+            assert not got[g.shard_bytes:].any()
+    # the parameter views: offsets inside the oracle's slot image
+    for p in range(len(descs)):
+        pi = plan.param(p)
+        n = numels[p] * esizes[p]
+        assert np.array_equal(image[pi.slot_offset:pi.slot_offset + n], raw[p])
+
+
+@pytest.mark.parametrize("name", ["tiny", "odd", "nano", "super", "sweep-d1664-t256-s8"])
+def test_workload_plans(name):
+    w = W.CONFIGS[name]
+    plan = dlo.Plan(W.block_param_descs(w), w.shards)
+    info = plan.info()
+    assert info.has_dit_roles == 1
+    bf = [g for g in plan.groups() if g.dtype == W.BF16][0]
+    f32 = [g for g in plan.groups() if g.dtype == W.F32][0]
+    assert bf.numel == 12 * w.hidden ** 2 and f32.numel == 8 * w.hidden
+    assert bf.shard_numel == oracle.shard_numel(bf.numel, w.shards)
+    assert f32.shard_numel == oracle.shard_numel(f32.numel, w.shards)
+    for p in range(info.n_params):
+        assert plan.param(p).slot_offset % 16 == 0
+
+
+def test_bad_arguments_fail_closed():
+    L = dlo.lib()
+    out = ctypes.c_void_p()
+    assert L.dlo_plan_create(None, 1, 1, ctypes.byref(out)) == dlo.ERR_INVALID
+    assert "null" in dlo.last_error()
+    arr = (dlo.ParamDesc * 1)()
+    arr[0].name = b"x"
+    arr[0].ndim = 1
+    arr[0].shape[0] = 4
+    arr[0].dtype = 7
+    assert L.dlo_plan_create(arr, 1, 2, ctypes.byref(out)) == dlo.ERR_INVALID
+    arr[0].dtype = 0
+    assert L.dlo_plan_create(arr, 1, 0, ctypes.byref(out)) == dlo.ERR_INVALID
+    arr[0].shape[0] = 0
+    assert L.dlo_plan_create(arr, 1, 1, ctypes.byref(out)) == dlo.ERR_INVALID
+    with pytest.raises(dlo.DLOError):
+        dlo.Plan([("a", (3,), 0)], 2).group(5)
+    # engine: rejects equal streams, null slots, misalignment before any CUDA call
+    d = dlo.EngineDesc()
+    d.n_blocks = 2
+    assert L.dlo_engine_create(ctypes.byref(d), ctypes.byref(out)) == dlo.ERR_INVALID
+    d.slot[0], d.slot[1] = 4096, 4096 * 3
+    d.slot_bytes = 100
+    d.compute_stream = d.copy_stream = 8
+    assert L.dlo_engine_create(ctypes.byref(d), ctypes.byref(out)) == dlo.ERR_INVALID
+    d.copy_stream = 16
+    d.slot[1] = 4096 * 3 + 8
+    assert L.dlo_engine_create(ctypes.byref(d), ctypes.byref(out)) == dlo.ERR_INVALID
+    # forward config checks
+    assert dlo.forward_scratch_bytes(dlo.dit_cfg(1, 16, 96, 1, 256)) == 0     # hidden % 64
+    assert dlo.forward_scratch_bytes(dlo.dit_cfg(1, 16, 256, 8, 1024)) == 0   # head dim 32
+    assert dlo.forward_scratch_bytes(dlo.dit_cfg(1, 16, 256, 4, 1024)) > 0
+    # engine calls on a null engine
+    assert L.dlo_prefetch(None, 0, 0) == dlo.ERR_INVALID
+    assert L.dlo_engine_destroy(None, 10) == dlo.OK
+
+
+def test_scratch_bytes_cover_the_buffers():
+    w = W.CONFIGS["odd"]
+    cfg = dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp)
+    M, d, f = w.tokens, w.hidden, w.mlp
+    assert dlo.forward_scratch_bytes(cfg) >= 2 * M * (d + 3 * d + d + f)

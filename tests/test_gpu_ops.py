@@ -1,0 +1,133 @@
+"""Each kernel of the block forward against the oracle's step, on the same
+seeded inputs: RMSNorm+adaLN, the tcgen05 linear with its three epilogues
+(ragged M, N and K included), and attention (head dims 64 and 128, ragged
+token counts, two batch items)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests._util import build_lib, assert_oracle_close
+from layerwise_weight_offload_gb300 import dlo
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build_lib()
+
+
+def _gen(seed):
+    g = torch.Generator().manual_seed(seed)
+    return lambda *shape, std=1.0: std * torch.randn(*shape, generator=g)
+
+
+def _status_clean():
+    torch.cuda.synchronize()
+    assert dlo.kernel_status() == 0
+
+
+@pytest.mark.parametrize("rows,d", [(1, 64), (7, 256), (200, 1024), (33, 3840)])
+def test_rmsnorm_mod(rows, d):
+    r = _gen(rows * 7 + d)
+    x = r(rows, d)
+    g = 1.0 + r(d, std=0.1)
+    shift, scale = r(d, std=0.1), r(d, std=0.1)
+    xd, gd, sd, cd = (t.cuda() for t in (x, g, shift, scale))
+    h = torch.empty(rows, d, dtype=torch.bfloat16, device="cuda")
+    dlo.op_rmsnorm_mod(xd, rows, d, gd, sd, cd, 1e-6, h)
+    _status_clean()
+    ref = oracle.rmsnorm_mod(x.numpy(), g.numpy(), shift.numpy(), scale.numpy(), 1e-6)
+    got = h.float().cpu().numpy()
+    # bf16 output: each element within one bf16 rounding of the exact value
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6)
+
+
+LIN_SHAPES = [
+    (128, 64, 256),      # one tile
+    (256, 1024, 3072),   # several tiles in M, N and K
+    (200, 320, 264),     # ragged M, N (vs 256) and K (vs 64)
+    (1, 64, 8),          # degenerate
+    (1000, 1024, 1024),
+    (77, 4096, 1024),    # long K
+]
+
+
+@pytest.mark.parametrize("M,K,N", LIN_SHAPES)
+@pytest.mark.parametrize("epi", [dlo.EPI_BF16, dlo.EPI_GELU_BF16, dlo.EPI_RESID_F32])
+def test_linear(M, K, N, epi):
+    r = _gen(M * 131 + K * 7 + N + epi)
+    a = r(M, K).to(torch.bfloat16)
+    w = r(N, K, std=0.05).to(torch.bfloat16)
+    ad, wd = a.cuda(), w.cuda()
+    ref = oracle.linear(a.float().numpy(), w.float().numpy())
+    if epi == dlo.EPI_RESID_F32:
+        x = r(M, N)
+        gate = r(N, std=0.1)
+        xd, gd = x.cuda(), gate.cuda()
+        dlo.op_linear(ad, M, K, wd, N, epi, xd, gd)
+        _status_clean()
+        got = xd.cpu().numpy()
+        exp = x.numpy().astype(np.float64) + gate.numpy().astype(np.float64) * ref
+        # fp32 accumulation against fp64: |err| << 1e-4 for these magnitudes
+        assert np.abs(got - exp).max() <= 1e-4 * max(1.0, np.abs(exp).max())
+        delta_got = got - x.numpy()
+        assert_oracle_close(delta_got, exp - x.numpy(), "resid delta", 1e-3, 1e-4)
+    else:
+        out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        dlo.op_linear(ad, M, K, wd, N, epi, out)
+        _status_clean()
+        got = out.float().cpu().numpy()
+        if epi == dlo.EPI_GELU_BF16:
+            ref = np.vectorize(oracle.gelu_tanh)(ref)
+        tol = 2.0 ** -8 * np.abs(ref) + 1e-5 * np.sqrt(K) * np.abs(ref).max()
+        assert np.all(np.abs(got - ref) <= tol), np.abs(got - ref).max()
+
+
+ATT_SHAPES = [
+    (1, 64, 256, 4),     # hd 64, one KV tile
+    (1, 200, 256, 4),    # ragged tokens
+    (2, 130, 512, 4),    # hd 128, two batch items, ragged
+    (1, 1, 128, 1),      # single token: output = v
+    (1, 1024, 1024, 16),
+    (1, 333, 384, 3),
+]
+
+
+@pytest.mark.parametrize("B,T,d,H", ATT_SHAPES)
+def test_attention(B, T, d, H):
+    r = _gen(B * 1000 + T + d + H)
+    qkv = r(B * T, 3 * d).to(torch.bfloat16)
+    o = torch.full((B * T, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dlo.op_attention(qkv.cuda(), B, T, d, H, o)
+    _status_clean()
+    ref = oracle.attention(qkv.float().numpy(), B, T, d, H)
+    got = o.float().cpu().numpy()
+    assert_oracle_close(got, ref, "attention", 1e-2, 4e-3)
+    if T == 1:
+        assert np.array_equal(got, qkv[:, 2 * d:].float().numpy())
+
+
+def test_attention_scale_is_checked_by_two_tokens():
+    # two tokens, one head of 64: output is a sigmoid-weighted mix of v0, v1
+    d = 64
+    qkv = torch.zeros(2, 3 * d)
+    qkv[:, :d] = torch.randn(2, d, generator=torch.Generator().manual_seed(0))
+    qkv[:, d:2 * d] = torch.randn(2, d, generator=torch.Generator().manual_seed(1))
+    qkv[:, 2 * d:] = torch.randn(2, d, generator=torch.Generator().manual_seed(2))
+    qkv = qkv.to(torch.bfloat16)
+    o = torch.empty(2, d, dtype=torch.bfloat16, device="cuda")
+    dlo.op_attention(qkv.cuda(), 1, 2, d, 1, o)
+    _status_clean()
+    ref = oracle.attention(qkv.float().numpy(), 1, 2, d, 1)
+    assert_oracle_close(o.float().cpu().numpy(), ref, "two tokens", 1e-2, 4e-3)
+
+
+def test_rejects_unsupported_shapes():
+    a = torch.zeros(4, 12, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(dlo.DLOError):
+        dlo.op_linear(a, 4, 12, a, 4, dlo.EPI_BF16, a)            # K, N not multiples of 8
+    q = torch.zeros(4, 96 * 3, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(dlo.DLOError):
+        dlo.op_attention(q, 1, 4, 96, 3, q)                        # head dim 32

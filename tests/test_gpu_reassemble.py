@@ -1,0 +1,95 @@
+"""The prefetch's bytes: a slot reassembled on the GPU (DMA and the copy
+kernel) equals the oracle's slot image byte for byte."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests._util import build_lib, raw_bytes
+from layerwise_weight_offload_gb300 import dlo, workloads as W
+from layerwise_weight_offload_gb300.stack import HostBlocks, PinnedBuffer
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build_lib()
+
+
+def _expected_image(host, hb):
+    w = host.w
+    p = host.params[hb]
+    numels = [int(np.prod(sh)) for _, sh, _ in host.descs]
+    codes = [c for _, _, c in host.descs]
+    esizes = [W.ESIZE[c] for c in codes]
+    raw = [raw_bytes(p[name]) for name, _, _ in host.descs]
+    image, _, _, used = oracle.slot_image(raw, numels, codes, esizes, w.shards, 256)
+    return image
+
+
+@pytest.mark.parametrize("mode", [dlo.COPY_DMA, dlo.COPY_KERNEL])
+@pytest.mark.parametrize("name", ["tiny", "odd"])
+def test_workload_slot_bit_exact(name, mode):
+    w = W.CONFIGS[name]
+    w = W.Workload(**{**w.__dict__, "distinct": 2, "n_blocks": 2})
+    host = HostBlocks(w, seed=3, keep_params=True)
+    info = host.plan.info()
+    dst = torch.full((info.slot_bytes + 512,), 0xA5, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    for hb in range(2):
+        dlo.reassemble(host.plan, host.shard_ptrs(hb), dst, mode, s)
+        s.synchronize()
+        got = dst.cpu().numpy()
+        exp = _expected_image(host, hb)
+        # compare every group's gathered range (gaps between groups untouched)
+        for g in host.plan.groups():
+            n = w.shards * g.shard_bytes
+            assert np.array_equal(got[g.base:g.base + n], exp[g.base:g.base + n]), (hb, g.dtype)
+        assert (got[info.slot_bytes:] == 0xA5).all()     # nothing written past the slot
+    host.close()
+
+
+def _custom_plan_case(rng, s):
+    """Random parameter sets whose shard byte lengths are not multiples of 16."""
+    descs = []
+    for i in range(int(rng.integers(1, 6))):
+        code = int(rng.integers(0, 2))
+        n = int(rng.integers(1, 5000))
+        descs.append(("p%d" % i, (n,), code))
+    return descs
+
+
+@pytest.mark.parametrize("mode", [dlo.COPY_DMA, dlo.COPY_KERNEL])
+def test_misaligned_shards_bit_exact(mode):
+    rng = np.random.default_rng(11)
+    s_stream = torch.cuda.Stream()
+    n_cases = 0
+    for trial in range(40):
+        s = int(rng.integers(1, 9))
+        descs = _custom_plan_case(rng, s)
+        plan = dlo.Plan(descs, s)
+        groups = plan.groups()
+        numels = [d[1][0] for d in descs]
+        codes = [d[2] for d in descs]
+        esizes = [W.ESIZE[c] for c in codes]
+        raw = [rng.integers(0, 256, size=n * e, dtype=np.uint8) for n, e in zip(numels, esizes)]
+        sizes = [g.shard_alloc_bytes for g in groups for _ in range(s)]
+        offs = np.cumsum([0] + [(x + 255) // 256 * 256 for x in sizes])
+        buf = PinnedBuffer(int(offs[-1]))
+        ptrs = [buf.ptr + int(o) for o in offs[:-1]]
+        plan.shard_host([r.ctypes.data for r in raw], ptrs)
+        info = plan.info()
+        dst = torch.full((info.slot_bytes + 256,), 0x5A, dtype=torch.uint8, device="cuda")
+        dlo.reassemble(plan, ptrs, dst, mode, s_stream)
+        s_stream.synchronize()
+        got = dst.cpu().numpy()
+        exp, _, gbase, used = oracle.slot_image(raw, numels, codes, esizes, s, 256)
+        for g in groups:
+            n = s * g.shard_bytes
+            assert np.array_equal(got[g.base:g.base + n], exp[g.base:g.base + n]), (trial, s)
+            if g.shard_bytes % 16:
+                n_cases += 1
+        assert (got[info.slot_bytes:] == 0x5A).all()
+        buf.close()
+    assert n_cases > 10        # the misaligned paths were exercised

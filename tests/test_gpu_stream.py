@@ -1,0 +1,221 @@
+"""The streamed stack on the GPU against the oracle:
+- the engine's slot/event schedule equals the oracle's literal hook
+  simulation, entry for entry;
+- at every forward the slot the compute stream reads holds exactly the
+  oracle's reassembled image of that block (the stream's read-after-write
+  and write-after-read ordering);
+- the streamed forward is bit-identical to the all-resident forward;
+- the block forward matches the oracle within the acceptance bar, step by
+  step (teacher-forced: the oracle's input at step s is the GPU's output of
+  step s-1)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests._util import build_lib, raw_bytes, params_f32, assert_oracle_close
+from layerwise_weight_offload_gb300 import dlo, workloads as W
+from layerwise_weight_offload_gb300.stack import HostBlocks, StreamedStack, ResidentStack
+
+pytestmark = pytest.mark.gpu
+
+MODES = [dlo.COPY_DMA, dlo.COPY_KERNEL, dlo.COPY_AUTO]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build_lib()
+
+
+def _slot_image(host, hb):
+    p = host.params[hb]
+    numels = [int(np.prod(sh)) for _, sh, _ in host.descs]
+    codes = [c for _, _, c in host.descs]
+    esizes = [W.ESIZE[c] for c in codes]
+    raw = [raw_bytes(p[name]) for name, _, _ in host.descs]
+    image, _, _, _ = oracle.slot_image(raw, numels, codes, esizes, host.w.shards, 256)
+    return image
+
+
+def _small(name, **kw):
+    base = W.CONFIGS[name].__dict__.copy()
+    base.update(kw)
+    return W.Workload(**base)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("n_blocks,steps", [(1, 3), (2, 2), (3, 2), (9, 3), (8, 1)])
+def test_schedule_and_slot_contents(n_blocks, steps, mode):
+    # small blocks so that every slot can be snapshotted
+    w = W.custom("sched", n_blocks=n_blocks, hidden=256, heads=4, mlp=1024, tokens=64,
+                 shards=3, steps=steps, distinct=min(n_blocks, 3))
+    host = HostBlocks(w, seed=5, keep_params=True)
+    st = StreamedStack(host, copy_mode=mode)
+    images = [_slot_image(host, hb) for hb in range(w.distinct)]
+    st.prime()
+    snaps = []
+    groups = host.plan.groups()
+    for k in range(n_blocks * steps):
+        i = k % n_blocks
+        slot = st.engine.pre_forward(i)
+        snap = torch.empty_like(st.slots[slot])
+        with torch.cuda.stream(st.compute):
+            snap.copy_(st.slots[slot])        # read on the compute stream, like a forward
+        snaps.append((i, snap))
+        st.engine.post_forward(i)
+    torch.cuda.synchronize()
+    log = st.engine.schedule_log()
+    ref = oracle.schedule(n_blocks, steps)
+    assert [tuple(e[:6]) for e in log] == [tuple(int(v) for v in r[:6]) for r in ref]
+    for i, snap in snaps:
+        got = snap.cpu().numpy()
+        exp = images[i % w.distinct]
+        for g in groups:
+            n = w.shards * g.shard_bytes
+            assert np.array_equal(got[g.base:g.base + n], exp[g.base:g.base + n]), (i, g.dtype)
+    stats = st.engine.query()
+    assert stats.n_forwards == n_blocks * steps
+    assert stats.n_prefetches == n_blocks * steps + 1
+    st.close()
+    host.close()
+
+
+def test_fail_closed_states():
+    w = W.custom("fc", n_blocks=3, hidden=256, heads=4, mlp=1024, tokens=64, shards=2)
+    host = HostBlocks(w, seed=1)
+    st = StreamedStack(host, copy_mode=dlo.COPY_DMA)
+    e = st.engine
+    with pytest.raises(dlo.DLOError) as ei:
+        e.pre_forward(0)                       # nothing prefetched yet
+    assert ei.value.status == dlo.ERR_STATE
+    with pytest.raises(dlo.DLOError):
+        e.param_view(0, 0)                     # not resident
+    st.prime()
+    with pytest.raises(dlo.DLOError) as ei:
+        e.pre_forward(1)                       # out of order
+    assert ei.value.status == dlo.ERR_STATE
+    slot = e.pre_forward(0)
+    with pytest.raises(dlo.DLOError):
+        e.prefetch(2, slot)                    # slot being read
+    with pytest.raises(dlo.DLOError):
+        e.pre_forward(1)                       # post_forward missing
+    with pytest.raises(dlo.DLOError):
+        e.register_block(0, host.plan, host.shard_ptrs(0))   # twice
+    v = e.param_view(0, 4)
+    assert v == st.slots[slot].data_ptr() + host.plan.param(4).slot_offset
+    e.post_forward(0)
+    e.wait_host(1, 10000)
+    torch.cuda.synchronize()
+    st.close()
+    host.close()
+
+
+def test_register_rejects_pageable_and_oversized():
+    w = W.custom("rj", n_blocks=2, hidden=256, heads=4, mlp=1024, tokens=64, shards=2)
+    host = HostBlocks(w, seed=1)
+    st = StreamedStack(host, copy_mode=dlo.COPY_KERNEL)
+    pageable = [torch.empty(g.shard_alloc_bytes, dtype=torch.uint8) for g in host.plan.groups()
+                for _ in range(w.shards)]
+    e2 = dlo.Engine(2, st.slots[0], st.slots[1], st.slot_bytes, st.compute, st.copy,
+                    dlo.COPY_KERNEL)
+    with pytest.raises(dlo.DLOError) as ei:
+        e2.register_block(0, host.plan, [t.data_ptr() for t in pageable])
+    assert ei.value.status == dlo.ERR_INVALID
+    e3 = dlo.Engine(2, st.slots[0], st.slots[1], 1024, st.compute, st.copy, dlo.COPY_DMA)
+    with pytest.raises(dlo.DLOError):
+        e3.register_block(0, host.plan, host.shard_ptrs(0))
+    e2.destroy()
+    e3.destroy()
+    st.close()
+    host.close()
+
+
+def _run_streamed(host, x0, steps, mode):
+    st = StreamedStack(host, copy_mode=mode)
+    x = x0.clone().cuda()
+    outs = []
+    for _ in range(steps):
+        st.compute.wait_stream(torch.cuda.current_stream())
+        st.step(x)
+        torch.cuda.current_stream().wait_stream(st.compute)
+        outs.append(x.clone())
+    torch.cuda.synchronize()
+    st.close()
+    return outs
+
+
+def _run_resident(host, x0, steps):
+    rs = ResidentStack(host)
+    x = x0.clone().cuda()
+    outs = []
+    per_block = []
+    for _ in range(steps):
+        rs.stream.wait_stream(torch.cuda.current_stream())
+        for i in range(host.w.n_blocks):
+            xin = x.clone()
+            rs.block(i, x)
+            torch.cuda.current_stream().wait_stream(rs.stream)
+            per_block.append((i, xin, x.clone()))
+        outs.append(x.clone())
+    torch.cuda.synchronize()
+    return outs, per_block
+
+
+def _check_against_oracle(host, per_block, which):
+    w = host.w
+    for idx in which:
+        i, xin, xout = per_block[idx]
+        p = params_f32(host.params[i % w.distinct])
+        xin_np = xin.cpu().numpy()
+        ref = oracle.block_forward(xin_np, p, w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps)
+        got = xout.cpu().numpy()
+        assert_oracle_close(got, ref, "block %d output" % idx)
+        # the branch updates alone, which the residual would otherwise mask
+        assert_oracle_close(got - xin_np, ref - xin_np, "block %d update" % idx, 2e-2, 1e-2)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_tiny_streamed_vs_resident_vs_oracle(mode):
+    w = W.CONFIGS["tiny"]
+    host = HostBlocks(w, seed=0, keep_params=True)
+    x0 = W.gen_x(w, seed=0)
+    res, per_block = _run_resident(host, x0, w.steps)
+    stm = _run_streamed(host, x0, w.steps, mode)
+    for a, b in zip(res, stm):
+        assert torch.equal(a, b)            # bit-identical
+    _check_against_oracle(host, per_block, range(len(per_block)))
+    assert dlo.kernel_status() == 0
+    host.close()
+
+
+def test_odd_streamed_vs_resident_vs_oracle():
+    w = W.CONFIGS["odd"]
+    host = HostBlocks(w, seed=0, keep_params=True)
+    x0 = W.gen_x(w, seed=0)
+    res, per_block = _run_resident(host, x0, w.steps)
+    for mode in (dlo.COPY_AUTO, dlo.COPY_KERNEL):
+        stm = _run_streamed(host, x0, w.steps, mode)
+        for a, b in zip(res, stm):
+            assert torch.equal(a, b)
+    n = w.n_blocks
+    # sampled, teacher-forced: blocks 0, 1, n-1 of step 0, block 0 of the last step
+    _check_against_oracle(host, per_block, [0, 1, n - 1, (w.steps - 1) * n])
+    assert dlo.kernel_status() == 0
+    host.close()
+
+
+@pytest.mark.parametrize("cfg", [
+    dict(n_blocks=3, hidden=320, heads=5, mlp=1280, tokens=200, shards=3),   # ragged tiles
+    dict(n_blocks=2, hidden=256, heads=2, mlp=1024, tokens=1, shards=2),     # one token
+    dict(n_blocks=3, hidden=384, heads=3, mlp=1536, tokens=77, shards=5, batch=2),
+])
+def test_ragged_streamed_vs_resident_vs_oracle(cfg):
+    w = W.custom("ragged", steps=2, **cfg)
+    host = HostBlocks(w, seed=9, keep_params=True)
+    x0 = W.gen_x(w, seed=9)
+    res, per_block = _run_resident(host, x0, w.steps)
+    stm = _run_streamed(host, x0, w.steps, dlo.COPY_AUTO)
+    for a, b in zip(res, stm):
+        assert torch.equal(a, b)
+    _check_against_oracle(host, per_block, range(len(per_block)))
+    host.close()
