@@ -1,0 +1,483 @@
+"""Benchmark of the streamed per-block weight stream on GB300.
+
+One bench step is one denoising step of the workload: every block once,
+each block's weights streamed host->device into a slot (prefetch of block
+i+1 overlapping block i's forward) and the block forward run on them.
+
+Prints one JSON line:
+  value       streamed block forwards per second (whole job, all ranks),
+              inputs (pinned host shards, x on the device) in place before
+              the timed region;
+  e2e         the same, with x copied from pinned host memory and the result
+              read back every step inside the timed region;
+  h2d_gbs     bytes moved host->device / copy-stream busy time;
+  exposed_transfer_ms_per_step  streamed minus all-resident step time;
+  roofline    the dominant operation (the host->device copy) against the
+              measured pinned cudaMemcpyAsync ceiling of this machine;
+  roofline_compute  the largest linear against the measured bf16 peak;
+  cpu_baseline the CPU oracle on a bounded sample of the same workload.
+
+--impl reference times the CPU oracle (the reference arm of this build):
+each step is one oracle block forward of the same workload on the host
+cores; under torchrun only rank 0 runs it.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "streamed block-fwd/s; H2D GB/s vs roofline; exposed transfer ms/step (1×GB300)"
+UNIT = "block-fwd/s"
+DEFAULT_CONFIG = "odd"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--copy-mode", default="auto", choices=["auto", "dma", "kernel"])
+    ap.add_argument("--copy-ctas", type=int, default=0)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--gen-device", default=None, help="cpu or cuda (default: by size)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", default=None,
+                    choices=["linear", "attention", "norm", "copy", "forward"],
+                    help="run one kernel of the workload's block `--reps` times (for ncu)")
+    ap.add_argument("--reps", type=int, default=3)
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(v, ws):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(v)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while a region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), d.get("hbm_gbs"), "measured"
+    except (OSError, ValueError):
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def oracle_block_rate(w, seconds, seed=0):
+    """CPU oracle block forwards per second on a bounded sample: host block
+    0 of the workload, repeated until `seconds` have passed (at least once)."""
+    import numpy as np
+    import oracle
+    from layerwise_weight_offload_gb300 import workloads as W
+    p = {k: v.float().numpy() for k, v in W.gen_block(w, 0, seed).items()}
+    x = W.gen_x(w, seed).numpy()
+    threads = oracle.default_threads()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.block_forward(x, p, w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
+                             threads=threads)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return n / el, n, el, threads
+
+
+def run_reference(args, ws, rank):
+    """The oracle as the reference arm: K timed steps of one oracle block
+    forward each (after W untimed), on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+    from layerwise_weight_offload_gb300 import workloads as W
+    w = W.CONFIGS[args.config]
+    p = {k: v.float().numpy() for k, v in W.gen_block(w, 0, args.seed).items()}
+    x = W.gen_x(w, args.seed).numpy()
+    threads = oracle.default_threads()
+    for _ in range(args.warmup):
+        oracle.block_forward(x, p, w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
+                             threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.block_forward(x, p, w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
+                             threads=threads)
+    el = time.perf_counter() - t0
+    v = args.steps / el
+    sample = ("%d oracle block forwards (fp64, naive loops) of host block 0 of workload %s"
+              % (args.steps, args.config))
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w, args),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, args):
+    return {"workload": "%s: %d blocks/step (%d distinct host blocks), hidden %d, %d heads, "
+                        "mlp %d, %d tokens, batch %d, %d shards per dtype group, %d denoising "
+                        "steps in the workload" % (w.name, w.n_blocks, w.distinct, w.hidden,
+                                                   w.heads, w.mlp, w.tokens, w.batch, w.shards,
+                                                   w.steps),
+            "name": w.name, "copy_mode": args.copy_mode}
+
+
+def h2d_ceiling_gbs(torch, nbytes=1 << 30, reps=10):
+    """Pinned host -> device cudaMemcpyAsync ceiling of this machine (best of reps)."""
+    from layerwise_weight_offload_gb300.stack import PinnedBuffer
+    buf = PinnedBuffer(nbytes)
+    src = buf.view(0, nbytes)
+    src.fill_(1)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    best = float("inf")
+    with torch.cuda.stream(s):
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            dst.copy_(src, non_blocking=True)
+            b.record(s)
+            b.synchronize()
+            best = min(best, a.elapsed_time(b))
+    s.synchronize()
+    del dst
+    buf.close()
+    return nbytes / best / 1e6
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+    from layerwise_weight_offload_gb300 import build as B
+    B.build()
+    from layerwise_weight_offload_gb300 import dlo, workloads as W
+    from layerwise_weight_offload_gb300.stack import HostBlocks, StreamedStack, ResidentStack
+
+    torch.cuda.set_device(local)
+    w = W.CONFIGS[args.config]
+    mode = {"auto": dlo.COPY_AUTO, "dma": dlo.COPY_DMA, "kernel": dlo.COPY_KERNEL}[args.copy_mode]
+    bf16_peak, bf16_sust, hbm_peak, peak_src = measured_peaks()
+    ceiling = h2d_ceiling_gbs(torch)
+
+    gen_dev = args.gen_device or ("cuda" if w.distinct * w.bf16_numel() > 2e9 else "cpu")
+    host = HostBlocks(w, seed=args.seed, gen_device=gen_dev)
+    bytes_per_block = sum(g.shard_bytes * w.shards for g in host.plan.groups())
+    st = StreamedStack(host, copy_mode=mode, copy_ctas=args.copy_ctas, timing=True)
+    x0 = W.gen_x(w, args.seed, device="cuda")
+    x = x0.clone()
+    cur = torch.cuda.current_stream()
+
+    def run_steps(n):
+        st.compute.wait_stream(cur)
+        for _ in range(n):
+            st.step(x)
+        cur.wait_stream(st.compute)
+
+    run_steps(args.warmup)
+    torch.cuda.synchronize()
+    n_copies_before = len(st.engine.copy_times()[0])
+    stats0 = st.engine.query()
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(st.compute)
+    for _ in range(args.steps):
+        st.step(x)
+    ev1.record(st.compute)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(ws)
+    ms = max_over_ranks(ev0.elapsed_time(ev1), ws)
+    stats1 = st.engine.query()
+    copy_ms, copy_bytes = st.engine.copy_times()
+    copy_ms, copy_bytes = copy_ms[n_copies_before:], copy_bytes[n_copies_before:]
+    # the prefetches enqueued by the timed forwards (the last one prefetches
+    # block 0 of the next step); the setup and warm-up ones are excluded
+    n_fwd = w.n_blocks * args.steps
+    copy_ms, copy_bytes = copy_ms[:n_fwd], copy_bytes[:n_fwd]
+    busy_ms = sum(copy_ms)
+    h2d = sum(copy_bytes) / (busy_ms * 1e6) if busy_ms > 0 else None
+    value = ws * n_fwd / (ms / 1e3)
+    ms_step = ms / args.steps
+    chosen = dlo.COPY_MODE_NAMES[stats1.chosen_mode]
+    kernel_launches_copy = stats1.n_kernel_prefetches - stats0.n_kernel_prefetches
+    gpu_launches = 7 * n_fwd + kernel_launches_copy
+
+    # all-resident reference run: same kernels, no transfer
+    rs = ResidentStack(host)
+    xr = x0.clone()
+    rs.stream.wait_stream(cur)
+    for _ in range(args.warmup):
+        rs.step(xr)
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record(rs.stream)
+    for _ in range(args.steps):
+        rs.step(xr)
+    r1.record(rs.stream)
+    torch.cuda.synchronize()
+    res_ms_step = r0.elapsed_time(r1) / args.steps
+    exposed = ms_step - res_ms_step
+    copy_per_step = busy_ms / args.steps
+    overlap = 1.0 - exposed / copy_per_step if copy_per_step > 0 else None
+
+    # block roofline: max(bytes / link ceiling, flops / bf16 peak)
+    flops = w.flops_per_block()
+    t_link = bytes_per_block / (ceiling * 1e9)
+    t_comp = flops / (bf16_sust * 1e12)
+    t_roof = max(t_link, t_comp)
+    roof_frac = (w.n_blocks * t_roof * 1e3) / ms_step
+
+    # largest linear alone (fc1: T x d -> f), event-timed on its stream
+    M, K, N = w.batch * w.tokens, w.hidden, w.mlp
+    a = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+    wt = (0.02 * torch.randn(N, K, device="cuda")).to(torch.bfloat16)
+    out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    ls = torch.cuda.Stream()
+    ls.wait_stream(cur)
+    for _ in range(3):
+        dlo.op_linear(a, M, K, wt, N, dlo.EPI_GELU_BF16, out, None, ls)
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 20
+    l0.record(ls)
+    for _ in range(reps):
+        dlo.op_linear(a, M, K, wt, N, dlo.EPI_GELU_BF16, out, None, ls)
+    l1.record(ls)
+    torch.cuda.synchronize()
+    lin_ms = l0.elapsed_time(l1) / reps
+    lin_tflops = 2.0 * M * K * N / (lin_ms * 1e-3) / 1e12
+
+    # end to end through the public API: x in from pinned host, result out
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.empty_like(x0, device="cpu").pin_memory()
+        xh.copy_(x0.cpu())
+        yh = torch.empty_like(xh).pin_memory()
+        st.compute.wait_stream(cur)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0.record(st.compute)
+        for _ in range(args.steps):
+            with torch.cuda.stream(st.compute):
+                x.copy_(xh, non_blocking=True)
+            st.step(x)
+            with torch.cuda.stream(st.compute):
+                yh.copy_(x, non_blocking=True)
+        e1.record(st.compute)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(e0.elapsed_time(e1), ws)
+        xb = x.numel() * x.element_size()
+        e2e = {"value": ws * n_fwd / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": xb + w.n_blocks * bytes_per_block,
+               "d2h_bytes_per_step": xb,
+               "note": "h2d counts x plus every streamed weight shard of the step"}
+
+    status = dlo.kernel_status()
+    if status != 0:
+        raise RuntimeError("a kernel wait timed out (device status %d)" % status)
+    st.close()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v, n, el, threads = oracle_block_rate(w, args.cpu_seconds, args.seed)
+        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": "%d fp64 oracle block forward(s) of host block 0 of %s in %.1f s; "
+                         "the oracle's reassembly is not included" % (n, w.name, el)}
+
+    copy_name = "copy_reassemble_kernel" if chosen == "kernel" else "cudaMemcpyAsync (copy engines)"
+    achieved = (sum(copy_bytes) / len(copy_bytes)) / (statistics.mean(copy_ms) * 1e6) \
+        if copy_ms else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded torch.randn, bf16 linear weights ~N(0,0.02), f32 adaLN "
+                "~N(0,0.1), norm gains 1, x ~N(0,1)",
+        "config": dict(workload_config(w, args), chosen_copy_mode=chosen,
+                       l2="streamed weights %.0f MB per step > 129 MB L2"
+                          % (w.n_blocks * bytes_per_block / 1e6),
+                       parallelism="replicas" if ws > 1 else "single GPU"),
+        "h2d_gbs": h2d, "h2d_ceiling_gbs": ceiling,
+        "h2d_nominal_pcie5_x16_gbs": 63.0,
+        "exposed_transfer_ms_per_step": exposed, "resident_ms_per_step": res_ms_step,
+        "copy_busy_ms_per_step": copy_per_step, "overlap_fraction": overlap,
+        "block_roofline_fraction": roof_frac,
+        "block_roofline": {"bytes_per_block": bytes_per_block, "flops_per_block": flops,
+                           "t_link_ms": t_link * 1e3, "t_compute_ms": t_comp * 1e3,
+                           "bound": "h2d" if t_link >= t_comp else "tensor"},
+        "auto_race_us_per_forward": {"dma": stats1.race_dma_us, "kernel": stats1.race_kernel_us},
+        "roofline": {"name": copy_name, "bound": "h2d", "achieved": achieved,
+                     "peak": ceiling, "unit": "GB/s",
+                     "frac": achieved / ceiling if achieved else None, "traffic": None,
+                     "peak_source": "pinned cudaMemcpyAsync 1 GiB ceiling measured in this run",
+                     "bytes_per_launch": bytes_per_block},
+        "roofline_compute": {"name": "gemm_tcgen05_kernel (fc1, GELU epilogue)",
+                             "bound": "tensor", "achieved": lin_tflops, "peak": bf16_peak,
+                             "unit": "TFLOP/s", "frac": lin_tflops / bf16_peak,
+                             "traffic": None, "peak_source": peak_src + " burst bf16",
+                             "shape": [M, K, N], "ms": lin_ms},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_only(args):
+    """One kernel of the workload's block, `reps` event-timed launches on one
+    stream; prints the mean time.  Sized by the workload, one host block."""
+    import torch
+    from layerwise_weight_offload_gb300 import build as B
+    B.build()
+    from layerwise_weight_offload_gb300 import dlo, workloads as W
+    from layerwise_weight_offload_gb300.stack import HostBlocks, ResidentStack
+    w = W.CONFIGS[args.config]
+    w = W.Workload(**{**w.__dict__, "distinct": 1, "n_blocks": 1})
+    M, d, f, H = w.batch * w.tokens, w.hidden, w.mlp, w.heads
+    s = torch.cuda.Stream()
+    dev = "cuda"
+    if args.only == "linear":
+        a = torch.randn(M, d, device=dev).to(torch.bfloat16)
+        wt = (0.02 * torch.randn(f, d, device=dev)).to(torch.bfloat16)
+        out = torch.empty(M, f, dtype=torch.bfloat16, device=dev)
+        fn = lambda: dlo.op_linear(a, M, d, wt, f, dlo.EPI_GELU_BF16, out, None, s)
+    elif args.only == "attention":
+        qkv = torch.randn(M, 3 * d, device=dev).to(torch.bfloat16)
+        o = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+        fn = lambda: dlo.op_attention(qkv, w.batch, w.tokens, d, H, o, s)
+    elif args.only == "norm":
+        x = torch.randn(M, d, device=dev)
+        g = torch.ones(d, device=dev)
+        z = torch.zeros(d, device=dev)
+        h = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+        fn = lambda: dlo.op_rmsnorm_mod(x, M, d, g, z, z, 1e-6, h, s)
+    else:
+        host = HostBlocks(w, seed=args.seed, gen_device="cuda")
+        if args.only == "copy":
+            dst = torch.empty(host.plan.info().slot_bytes, dtype=torch.uint8, device=dev)
+            ptrs = host.shard_ptrs(0)
+            mode = dlo.COPY_DMA if args.copy_mode == "dma" else dlo.COPY_KERNEL
+            fn = lambda: dlo.reassemble(host.plan, ptrs, dst, mode, s)
+        else:
+            rs = ResidentStack(host, stream=s)
+            x = W.gen_x(w, args.seed, device=dev)
+            fn = lambda: rs.block(0, x)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(args.reps):
+        fn()
+    e1.record(s)
+    torch.cuda.synchronize()
+    assert dlo.kernel_status() == 0
+    print(json.dumps({"only": args.only, "config": args.config, "reps": args.reps,
+                      "ms_per_rep": e0.elapsed_time(e1) / args.reps}), flush=True)
+
+
+def main():
+    args = parse()
+    if args.only:
+        run_only(args)
+        return
+    ws, rank, local = dist_env()
+    if args.warmup < 3:
+        args.warmup = 3
+    if ws > 1:
+        import torch.distributed as dist
+        if args.impl == "reference":
+            if rank != 0:
+                return
+        else:
+            import torch
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1 and args.impl != "reference":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

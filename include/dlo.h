@@ -171,7 +171,13 @@ typedef struct {
   int32_t heads;    /* hidden / heads must be 64 or 128 */
   int32_t mlp;      /* multiple of 64 */
   float eps;        /* RMSNorm epsilon */
+  int32_t flags;    /* DLO_FWD_GRAPH: launch the seven kernels as one cached
+                       CUDA graph (captured on first use for this config,
+                       plan, weight base, x and scratch); results are the
+                       same bits as direct launches */
 } dlo_dit_cfg;
+
+enum { DLO_FWD_GRAPH = 1 };
 
 /* Bytes of device scratch one block forward needs (bf16 h, qkv, o, u). */
 size_t dlo_forward_scratch_bytes(const dlo_dit_cfg* cfg);
@@ -226,6 +232,12 @@ typedef struct {
   int32_t copy_mode;      /* dlo_copy_mode */
   int32_t copy_ctas;      /* CTAs of the copy kernel; 0 = default (152) */
   int32_t timing;         /* 1: bracket every prefetch with timing events */
+  int32_t dma_streams;    /* DMA fan-out: the (group, shard) copies of one
+                             prefetch are spread over this many library-owned
+                             streams forked from the copy stream and joined
+                             back before the ready event; 0 = default (1:
+                             every copy on the copy stream, which measured
+                             faster on GB300 than spreading them) */
 } dlo_engine_desc;
 
 typedef struct {
@@ -301,14 +313,21 @@ dlo_status dlo_schedule_log(const dlo_engine* e, dlo_sched_event* buf,
 /* Engine counters.  copy_ms[i] / copy_bytes[i]: elapsed time and bytes of
  * the i-th timed prefetch (only with desc.timing = 1; synchronises on the
  * events it reads).  chosen_mode: the mode AUTO settled on (or the fixed
- * mode); dma_ns_per_mb / kernel_ns_per_mb: AUTO's measured rates (0 if not
- * measured). */
+ * mode; DLO_COPY_AUTO while undecided); n_kernel_prefetches counts
+ * copy-kernel launches.  AUTO races the two modes on the quantity that
+ * matters, the compute stream's time per block forward while the next
+ * block streams in.  With n = n_blocks, the prefetches issued by forwards
+ * n+2 .. n+6 use DMA and those issued by forwards n+7 .. n+11 the copy
+ * kernel (after one full pass, so first-touch costs are excluded);
+ * race_dma_us / race_kernel_us are the mean intervals between consecutive
+ * free events inside each window (0 until measured). */
 typedef struct {
   int32_t chosen_mode;
   int32_t n_forwards;
   int32_t n_prefetches;
-  double dma_ns_per_mb;
-  double kernel_ns_per_mb;
+  int32_t n_kernel_prefetches;
+  double race_dma_us;
+  double race_kernel_us;
 } dlo_engine_stats;
 dlo_status dlo_engine_query(dlo_engine* e, dlo_engine_stats* out);
 dlo_status dlo_engine_copy_times(dlo_engine* e, float* copy_ms, int64_t* copy_bytes,

@@ -244,16 +244,29 @@ attention_kernel(const uint16_t* __restrict__ qkv, int64_t tokens, int64_t d, in
 }
 
 template <int HD>
+constexpr int att_smem() { return 5 * 64 * HD * 2; }   // Q + 2 K + 2 V tiles
+
+cudaError_t g_att_err = cudaSuccess;
+std::once_flag g_att_once;
+
+void set_att_attrs() {
+  std::call_once(g_att_once, [] {
+    cudaError_t e0 = cudaFuncSetAttribute(attention_kernel<64>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          att_smem<64>());
+    cudaError_t e1 = cudaFuncSetAttribute(attention_kernel<128>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          att_smem<128>());
+    g_att_err = e0 != cudaSuccess ? e0 : e1;
+  });
+}
+
+template <int HD>
 dlo_status launch_hd(const uint16_t* qkv, int64_t batch, int64_t tokens, int64_t d,
                      int64_t heads, uint16_t* o, cudaStream_t stream) {
-  constexpr int SMEM = 5 * 64 * HD * 2;   // Q + 2 K + 2 V tiles
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attention_kernel<HD>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-  });
-  DLO_CUDA(attr_err);
+  constexpr int SMEM = att_smem<HD>();
+  set_att_attrs();
+  DLO_CUDA(g_att_err);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
   dim3 grid(static_cast<unsigned>((tokens + BQ - 1) / BQ), static_cast<unsigned>(heads),
             static_cast<unsigned>(batch));
@@ -265,6 +278,12 @@ dlo_status launch_hd(const uint16_t* qkv, int64_t batch, int64_t tokens, int64_t
 }
 
 }  // namespace
+
+dlo_status attention_preload() {
+  set_att_attrs();
+  DLO_CUDA(g_att_err);
+  return DLO_OK;
+}
 
 dlo_status launch_attention(const uint16_t* qkv, int64_t batch, int64_t tokens, int64_t d,
                             int64_t heads, uint16_t* o, cudaStream_t stream) {

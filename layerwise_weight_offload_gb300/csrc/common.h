@@ -78,6 +78,7 @@ struct dlo_plan {
   int64_t slot_bytes = 0;
   int32_t role[dlo::R_COUNT];   // param index per role, -1 if absent
   bool has_dit_roles = false;
+  uint64_t id = 0;              // unique per plan (keys cached graphs)
 };
 
 namespace dlo {
@@ -117,5 +118,12 @@ dlo_status launch_attention(const uint16_t* qkv, int64_t batch,
 
 // status.cu: device-side error word written by bounded waits
 int* device_error_word();  // device address (cached per device)
+
+// One-time per-process preparation of each kernel (function attributes,
+// module loading), so that no first-launch cost lands in a timed window or
+// inside a graph capture.
+dlo_status gemm_preload();
+dlo_status attention_preload();
+dlo_status copy_preload();
 
 }  // namespace dlo

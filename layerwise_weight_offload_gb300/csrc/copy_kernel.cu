@@ -112,6 +112,12 @@ copy_reassemble_kernel(const __grid_constant__ SegmentTable t) {
 
 }  // namespace
 
+dlo_status copy_preload() {
+  cudaFuncAttributes attr;
+  DLO_CUDA(cudaFuncGetAttributes(&attr, copy_reassemble_kernel));
+  return DLO_OK;
+}
+
 dlo_status launch_copy_reassemble(const SegmentTable& t, int ctas, cudaStream_t stream) {
   if (t.n <= 0) return DLO_OK;
   if (ctas <= 0) ctas = 152;

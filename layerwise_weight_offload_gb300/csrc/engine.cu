@@ -20,6 +20,7 @@
 // recorded after the last forward that read that slot (the pages draw only
 // the compute-waits-for-gather arrow; reusing two buffers needs the reverse
 // write-after-read wait too).
+#include <algorithm>
 #include <chrono>
 #include <new>
 #include <thread>
@@ -47,6 +48,7 @@ struct dlo_engine {
     int64_t bytes;
     int32_t mode;
   };
+  static constexpr int kMaxFan = 8;
 
   int32_t n_blocks = 0;
   uint8_t* slot[2] = {nullptr, nullptr};
@@ -66,17 +68,35 @@ struct dlo_engine {
   int32_t cur_block = -1, cur_slot = -1;
   std::vector<dlo_sched_event> log;
   std::vector<Timed> timed;          // with timing = 1: every prefetch
-  // AUTO: the first prefetches alternate modes and are timed
-  std::vector<Timed> race;
+  // DMA fan-out (library-owned streams forked from / joined to `copy`)
+  int32_t fan = 1;
+  cudaStream_t aux[kMaxFan] = {};
+  cudaEvent_t fork_ev = nullptr;
+  cudaEvent_t join_ev[kMaxFan] = {};
+  // AUTO race: timing events on the compute stream at the window edges
+  cudaEvent_t race_ev[4] = {};
+  bool race_rec[4] = {false, false, false, false};
   int32_t chosen = -1;               // DLO_COPY_DMA / DLO_COPY_KERNEL once decided
-  double dma_ns_per_mb = 0, kernel_ns_per_mb = 0;
+  double race_dma_us = 0, race_kernel_us = 0;
   int64_t n_prefetches = 0;
+  int64_t n_kernel_prefetches = 0;
 };
 
 namespace dlo {
+dlo_status preload_kernels();
 namespace {
 
-constexpr int kRaceRounds = 3;   // timed prefetches per mode before AUTO decides
+// AUTO races DMA against the copy kernel on the compute stream's time per
+// forward: prefetches issued by forwards [s, s + W) use DMA, those issued by
+// the next W forwards use the copy kernel, s = race_start(n_blocks).
+// Forward k+1 reads what the prefetch issued at forward k brought in and
+// overlaps the prefetch issued at k+1, so the free-event intervals of
+// forwards s+1 .. s+W-1 see only DMA, and the next W-1 only the kernel.
+// The race starts after one full pass over the blocks plus two forwards,
+// so that one-time costs (module loading, first launches, the first
+// device access to each pinned host page) stay out of both windows.
+constexpr int64_t kRaceWindow = 5;
+inline int64_t race_start(int32_t n_blocks) { return static_cast<int64_t>(n_blocks) + 2; }
 
 dlo_status build_segments(const dlo_engine::Block& b, uint8_t* dst, SegmentTable* t) {
   const dlo_plan* p = b.plan;
@@ -96,56 +116,91 @@ dlo_status build_segments(const dlo_engine::Block& b, uint8_t* dst, SegmentTable
   return DLO_OK;
 }
 
-dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, int ctas,
-                      cudaStream_t stream) {
-  const dlo_plan* p = b.plan;
-  const int32_t s = p->n_shards;
-  if (mode == DLO_COPY_KERNEL) {
-    for (const void* q : b.dev)
-      if (!q) DLO_FAIL(DLO_ERR_INVALID, "prefetch: a shard is not device-mapped pinned memory");
-    SegmentTable t;
-    DLO_TRY(build_segments(b, dst, &t));
-    return launch_copy_reassemble(t, ctas, stream);
-  }
-  for (size_t g = 0; g < p->groups.size(); ++g) {
-    const auto& grp = p->groups[g];
-    for (int32_t r = 0; r < s; ++r)
-      DLO_CUDA(cudaMemcpyAsync(dst + grp.base + static_cast<int64_t>(r) * grp.shard_bytes,
-                               b.host[g * s + r], static_cast<size_t>(grp.shard_bytes),
-                               cudaMemcpyHostToDevice, stream));
-  }
-  return DLO_OK;
-}
-
 bool all_mapped(const dlo_engine::Block& b) {
   for (const void* q : b.dev)
     if (!q) return false;
   return true;
 }
 
-// AUTO: decide once every raced prefetch has completed (non-blocking query).
+// One prefetch's bytes: the copy kernel (one launch), or DMA — one
+// cudaMemcpyAsync per (group, shard) to its final slot offset, dealt to up
+// to `fan` streams (largest first, each to the least-loaded stream) that
+// fork from `stream` and join back into it.
+dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, int ctas,
+                      cudaStream_t stream, int fan, cudaStream_t* aux, cudaEvent_t fork_ev,
+                      cudaEvent_t* join_ev) {
+  const dlo_plan* p = b.plan;
+  const int32_t s = p->n_shards;
+  if (mode == DLO_COPY_KERNEL) {
+    if (!all_mapped(b))
+      DLO_FAIL(DLO_ERR_INVALID, "prefetch: a shard is not device-mapped pinned memory");
+    SegmentTable t;
+    DLO_TRY(build_segments(b, dst, &t));
+    return launch_copy_reassemble(t, ctas, stream);
+  }
+  struct Piece { uint8_t* dst; const void* src; int64_t bytes; };
+  std::vector<Piece> pieces;
+  for (size_t g = 0; g < p->groups.size(); ++g) {
+    const auto& grp = p->groups[g];
+    for (int32_t r = 0; r < s; ++r)
+      pieces.push_back({dst + grp.base + static_cast<int64_t>(r) * grp.shard_bytes,
+                        b.host[g * s + r], grp.shard_bytes});
+  }
+  const int used = static_cast<int>(std::min<size_t>(fan, pieces.size()));
+  if (used <= 1) {
+    for (const Piece& q : pieces)
+      DLO_CUDA(cudaMemcpyAsync(q.dst, q.src, static_cast<size_t>(q.bytes),
+                               cudaMemcpyHostToDevice, stream));
+    return DLO_OK;
+  }
+  std::stable_sort(pieces.begin(), pieces.end(),
+                   [](const Piece& a, const Piece& c) { return a.bytes > c.bytes; });
+  std::vector<int64_t> load(used, 0);
+  DLO_CUDA(cudaEventRecord(fork_ev, stream));
+  for (int j = 0; j < used; ++j) DLO_CUDA(cudaStreamWaitEvent(aux[j], fork_ev, 0));
+  for (const Piece& q : pieces) {
+    int j = 0;
+    for (int c = 1; c < used; ++c)
+      if (load[c] < load[j]) j = c;
+    load[j] += q.bytes;
+    DLO_CUDA(cudaMemcpyAsync(q.dst, q.src, static_cast<size_t>(q.bytes),
+                             cudaMemcpyHostToDevice, aux[j]));
+  }
+  for (int j = 0; j < used; ++j) {
+    DLO_CUDA(cudaEventRecord(join_ev[j], aux[j]));
+    DLO_CUDA(cudaStreamWaitEvent(stream, join_ev[j], 0));
+  }
+  return DLO_OK;
+}
+
+// AUTO: decide once the four window-edge events have completed
+// (non-blocking).
 void try_decide(dlo_engine* e) {
-  if (e->chosen >= 0 || static_cast<int>(e->race.size()) < 2 * kRaceRounds) return;
-  for (const auto& t : e->race)
-    if (cudaEventQuery(t.b) != cudaSuccess) return;
-  double ms[3] = {0, 0, 0}, mb[3] = {0, 0, 0};
-  for (const auto& t : e->race) {
-    float v = 0;
-    cudaEventElapsedTime(&v, t.a, t.b);
-    ms[t.mode] += v;
-    mb[t.mode] += t.bytes / 1e6;
+  if (e->chosen >= 0) return;
+  for (int i = 0; i < 4; ++i)
+    if (!e->race_rec[i] || cudaEventQuery(e->race_ev[i]) != cudaSuccess) return;
+  float d = 0, kk = 0;
+  cudaEventElapsedTime(&d, e->race_ev[0], e->race_ev[1]);
+  cudaEventElapsedTime(&kk, e->race_ev[2], e->race_ev[3]);
+  e->race_dma_us = 1e3 * d / (kRaceWindow - 1);
+  e->race_kernel_us = 1e3 * kk / (kRaceWindow - 1);
+  e->chosen = e->race_kernel_us < e->race_dma_us ? DLO_COPY_KERNEL : DLO_COPY_DMA;
+}
+
+// Mode of a prefetch issued by forward k (k < 0: outside the hook).
+int32_t mode_for(dlo_engine* e, int64_t k, const dlo_engine::Block& b) {
+  if (e->mode != DLO_COPY_AUTO) return e->mode;
+  try_decide(e);
+  if (e->chosen >= 0) return e->chosen;
+  const int64_t s0 = race_start(e->n_blocks);
+  if (k >= s0 + kRaceWindow && k < s0 + 2 * kRaceWindow) {
+    if (!all_mapped(b)) {   // the kernel cannot read this block: no race
+      e->chosen = DLO_COPY_DMA;
+      return DLO_COPY_DMA;
+    }
+    return DLO_COPY_KERNEL;
   }
-  e->dma_ns_per_mb = mb[DLO_COPY_DMA] > 0 ? ms[DLO_COPY_DMA] * 1e6 / mb[DLO_COPY_DMA] : 0;
-  e->kernel_ns_per_mb =
-      mb[DLO_COPY_KERNEL] > 0 ? ms[DLO_COPY_KERNEL] * 1e6 / mb[DLO_COPY_KERNEL] : 0;
-  e->chosen = (e->kernel_ns_per_mb > 0 && e->kernel_ns_per_mb < e->dma_ns_per_mb)
-                  ? DLO_COPY_KERNEL
-                  : DLO_COPY_DMA;
-  for (auto& t : e->race) {
-    cudaEventDestroy(t.a);
-    cudaEventDestroy(t.b);
-  }
-  e->race.clear();
+  return DLO_COPY_DMA;
 }
 
 dlo_status make_timed(dlo_engine::Timed* t) {
@@ -158,43 +213,27 @@ dlo_status make_timed(dlo_engine::Timed* t) {
 }
 
 // Enqueues the prefetch of `block` into `slot` on the copy stream.
-dlo_status enqueue_prefetch(dlo_engine* e, int32_t block, int32_t slot) {
+dlo_status enqueue_prefetch(dlo_engine* e, int32_t block, int32_t slot, int64_t issued_by_k,
+                            int32_t* used_mode = nullptr) {
   const dlo_engine::Block& b = e->blocks[block];
-  int32_t mode = e->mode;
-  bool racing = false;
-  if (mode == DLO_COPY_AUTO) {
-    try_decide(e);
-    if (e->chosen >= 0) {
-      mode = e->chosen;
-    } else if (!all_mapped(b)) {
-      mode = DLO_COPY_DMA;
-    } else if (static_cast<int>(e->race.size()) < 2 * kRaceRounds) {
-      mode = (e->race.size() % 2 == 0) ? DLO_COPY_DMA : DLO_COPY_KERNEL;
-      racing = true;
-    } else {
-      mode = DLO_COPY_DMA;   // raced prefetches still in flight
-    }
-  }
+  const int32_t mode = mode_for(e, issued_by_k, b);
+  if (used_mode) *used_mode = mode;
   DLO_CUDA(cudaStreamWaitEvent(e->copy, e->freed[slot], 0));
   dlo_engine::Timed t{};
-  const bool timed = racing || e->timing;
-  if (timed) {
+  if (e->timing) {
     DLO_TRY(make_timed(&t));
     t.bytes = b.bytes;
     t.mode = mode;
+    e->timed.push_back(t);
     DLO_CUDA(cudaEventRecord(t.a, e->copy));
   }
-  DLO_TRY(copy_block(b, e->slot[slot], mode, e->copy_ctas, e->copy));
-  if (timed) {
-    DLO_CUDA(cudaEventRecord(t.b, e->copy));
-    if (racing)
-      e->race.push_back(t);    // AUTO's measurement; not listed in the timing log
-    else
-      e->timed.push_back(t);
-  }
+  DLO_TRY(copy_block(b, e->slot[slot], mode, e->copy_ctas, e->copy, e->fan, e->aux, e->fork_ev,
+                     e->join_ev));
+  if (e->timing) DLO_CUDA(cudaEventRecord(t.b, e->copy));
   DLO_CUDA(cudaEventRecord(e->ready[slot], e->copy));
   e->slot_holds[slot] = block;
   e->n_prefetches++;
+  if (mode == DLO_COPY_KERNEL) e->n_kernel_prefetches++;
   return DLO_OK;
 }
 
@@ -207,6 +246,25 @@ int32_t slot_of(const dlo_engine* e, int32_t block) {
   if (e->slot_holds[0] == block) return 0;
   if (e->slot_holds[1] == block) return 1;
   return -1;
+}
+
+void release(dlo_engine* e) {
+  for (int s = 0; s < 2; ++s) {
+    if (e->ready[s]) cudaEventDestroy(e->ready[s]);
+    if (e->freed[s]) cudaEventDestroy(e->freed[s]);
+  }
+  for (auto& t : e->timed) {
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
+  for (int i = 0; i < 4; ++i)
+    if (e->race_ev[i]) cudaEventDestroy(e->race_ev[i]);
+  if (e->fork_ev) cudaEventDestroy(e->fork_ev);
+  for (int j = 0; j < dlo_engine::kMaxFan; ++j) {
+    if (e->join_ev[j]) cudaEventDestroy(e->join_ev[j]);
+    if (e->aux[j]) cudaStreamDestroy(e->aux[j]);
+  }
+  delete e;
 }
 
 }  // namespace
@@ -227,6 +285,10 @@ dlo_status dlo_engine_create(const dlo_engine_desc* d, dlo_engine** out) {
     DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: compute and copy streams must differ");
   if (d->copy_mode < DLO_COPY_AUTO || d->copy_mode > DLO_COPY_KERNEL)
     DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: unknown copy mode %d", d->copy_mode);
+  if (d->dma_streams < 0 || d->dma_streams > dlo_engine::kMaxFan)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: dma_streams must be 0..%d",
+             dlo_engine::kMaxFan);
+  DLO_TRY(preload_kernels());
   dlo_engine* e = new (std::nothrow) dlo_engine();
   if (!e) DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: out of host memory");
   e->n_blocks = d->n_blocks;
@@ -238,20 +300,26 @@ dlo_status dlo_engine_create(const dlo_engine_desc* d, dlo_engine** out) {
   e->mode = d->copy_mode;
   e->copy_ctas = d->copy_ctas;
   e->timing = d->timing != 0;
+  e->fan = d->dma_streams == 0 ? 1 : d->dma_streams;
   e->blocks.resize(d->n_blocks);
   e->hooks.resize(d->n_blocks);
   for (int32_t i = 0; i < d->n_blocks; ++i) e->hooks[i] = {i % 2, -1};
   if (d->copy_mode != DLO_COPY_AUTO) e->chosen = d->copy_mode;
-  for (int s = 0; s < 2; ++s) {
-    if (cudaEventCreateWithFlags(&e->ready[s], cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&e->freed[s], cudaEventDisableTiming) != cudaSuccess) {
-      for (int q = 0; q < 2; ++q) {
-        if (e->ready[q]) cudaEventDestroy(e->ready[q]);
-        if (e->freed[q]) cudaEventDestroy(e->freed[q]);
-      }
-      delete e;
-      DLO_FAIL(DLO_ERR_CUDA, "dlo_engine_create: cudaEventCreate failed");
-    }
+  bool ok = true;
+  for (int s = 0; s < 2; ++s)
+    ok = ok && cudaEventCreateWithFlags(&e->ready[s], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&e->freed[s], cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; i < 4; ++i) ok = ok && cudaEventCreate(&e->race_ev[i]) == cudaSuccess;
+  if (e->fan > 1) {
+    ok = ok && cudaEventCreateWithFlags(&e->fork_ev, cudaEventDisableTiming) == cudaSuccess;
+    for (int j = 0; j < e->fan; ++j)
+      ok = ok && cudaStreamCreateWithFlags(&e->aux[j], cudaStreamNonBlocking) == cudaSuccess &&
+           cudaEventCreateWithFlags(&e->join_ev[j], cudaEventDisableTiming) == cudaSuccess;
+  }
+  if (!ok) {
+    cudaGetLastError();
+    release(e);
+    DLO_FAIL(DLO_ERR_CUDA, "dlo_engine_create: cannot create the engine's events/streams");
   }
   *out = e;
   return DLO_OK;
@@ -307,7 +375,7 @@ dlo_status dlo_prefetch(dlo_engine* e, int32_t block, int32_t slot) {
   if (e->in_forward && e->cur_slot == slot)
     DLO_FAIL(DLO_ERR_STATE, "dlo_prefetch: slot %d is being read by block %d", slot,
              e->cur_block);
-  return enqueue_prefetch(e, block, slot);
+  return enqueue_prefetch(e, block, slot, -1);
 }
 
 dlo_status dlo_wait(dlo_engine* e, int32_t block) {
@@ -377,7 +445,8 @@ dlo_status dlo_pre_forward(dlo_engine* e, int32_t block, int32_t* slot_out) {
   DLO_CUDA(cudaStreamWaitEvent(e->compute, e->ready[slot], 0));
   const int32_t ps = 1 - slot;
   const int32_t waits = e->last_reader[ps];
-  DLO_TRY(enqueue_prefetch(e, next, ps));
+  int32_t used_mode = DLO_COPY_DMA;
+  DLO_TRY(enqueue_prefetch(e, next, ps, e->k, &used_mode));
   h.current_slot = slot;
   h.prefetched_slot = ps;
   e->last_reader[slot] = static_cast<int32_t>(e->k);
@@ -388,7 +457,7 @@ dlo_status dlo_pre_forward(dlo_engine* e, int32_t block, int32_t* slot_out) {
   ev.prefetch_block = next;
   ev.prefetch_slot = ps;
   ev.waits_on_free_of_k = waits;
-  ev.copy_mode = e->chosen >= 0 ? e->chosen : DLO_COPY_AUTO;
+  ev.copy_mode = used_mode;
   e->log.push_back(ev);
   e->in_forward = true;
   e->cur_block = block;
@@ -403,6 +472,15 @@ dlo_status dlo_post_forward(dlo_engine* e, int32_t block) {
   if (!e->in_forward || block != e->cur_block)
     DLO_FAIL(DLO_ERR_STATE, "dlo_post_forward: block %d is not the block in flight", block);
   DLO_CUDA(cudaEventRecord(e->freed[e->cur_slot], e->compute));
+  if (e->chosen < 0) {
+    const int64_t s0 = race_start(e->n_blocks), w = kRaceWindow;
+    const int64_t edge[4] = {s0, s0 + w - 1, s0 + w, s0 + 2 * w - 1};
+    for (int i = 0; i < 4; ++i)
+      if (e->k == edge[i]) {
+        DLO_CUDA(cudaEventRecord(e->race_ev[i], e->compute));
+        e->race_rec[i] = true;
+      }
+  }
   e->in_forward = false;
   e->k++;
   return DLO_OK;
@@ -442,8 +520,9 @@ dlo_status dlo_engine_query(dlo_engine* e, dlo_engine_stats* out) {
   out->chosen_mode = e->chosen >= 0 ? e->chosen : DLO_COPY_AUTO;
   out->n_forwards = static_cast<int32_t>(e->k);
   out->n_prefetches = static_cast<int32_t>(e->n_prefetches);
-  out->dma_ns_per_mb = e->dma_ns_per_mb;
-  out->kernel_ns_per_mb = e->kernel_ns_per_mb;
+  out->n_kernel_prefetches = static_cast<int32_t>(e->n_kernel_prefetches);
+  out->race_dma_us = e->race_dma_us;
+  out->race_kernel_us = e->race_kernel_us;
   return DLO_OK;
 }
 
@@ -502,19 +581,7 @@ dlo_status dlo_engine_destroy(dlo_engine* e, int32_t timeout_ms) {
   }
   cudaEventDestroy(tail[0]);
   cudaEventDestroy(tail[1]);
-  for (int s = 0; s < 2; ++s) {
-    cudaEventDestroy(e->ready[s]);
-    cudaEventDestroy(e->freed[s]);
-  }
-  for (auto& t : e->timed) {
-    cudaEventDestroy(t.a);
-    cudaEventDestroy(t.b);
-  }
-  for (auto& t : e->race) {
-    cudaEventDestroy(t.a);
-    cudaEventDestroy(t.b);
-  }
-  delete e;
+  release(e);
   return DLO_OK;
 }
 
@@ -546,7 +613,8 @@ dlo_status dlo_reassemble(const dlo_plan* plan, const void* const* shard_ptrs, v
     }
   }
   const int32_t m = mode == DLO_COPY_KERNEL ? DLO_COPY_KERNEL : DLO_COPY_DMA;
-  return copy_block(b, static_cast<uint8_t*>(dst), m, 0, static_cast<cudaStream_t>(stream));
+  return copy_block(b, static_cast<uint8_t*>(dst), m, 0, static_cast<cudaStream_t>(stream), 1,
+                    nullptr, nullptr, nullptr);
 }
 
 }  // extern "C"

@@ -10,6 +10,9 @@
 //   rmsnorm_mod -> linear(qkv, bf16) -> attention -> linear(out, gated
 //   residual) -> rmsnorm_mod -> linear(fc1, GELU) -> linear(fc2, gated
 //   residual).
+#include <mutex>
+#include <utility>
+
 #include "common.h"
 
 namespace dlo {
@@ -72,21 +75,8 @@ dlo_status check_plan(const dlo_dit_cfg& c, const dlo_plan* plan) {
   return DLO_OK;
 }
 
-}  // namespace
-
-dlo_status forward_impl(const dlo_dit_cfg* cfg, const dlo_plan* plan, const void* block_base,
-                        float* x, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
-  DLO_TRY(check_cfg(cfg));
-  DLO_TRY(check_plan(*cfg, plan));
-  const ScratchLayout sl = scratch_layout(*cfg);
-  if (!block_base || !x || !scratch) DLO_FAIL(DLO_ERR_INVALID, "forward: null pointer");
-  if (reinterpret_cast<uintptr_t>(block_base) & 255u)
-    DLO_FAIL(DLO_ERR_INVALID, "forward: block base must be 256-byte aligned");
-  if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(scratch) & 255u))
-    DLO_FAIL(DLO_ERR_INVALID, "forward: x must be 16-byte and scratch 256-byte aligned");
-  if (scratch_bytes < sl.total)
-    DLO_FAIL(DLO_ERR_NOMEM, "forward: scratch holds %zu bytes, needs %zu", scratch_bytes,
-             sl.total);
+dlo_status launch_all(const dlo_dit_cfg* cfg, const dlo_plan* plan, const ScratchLayout& sl,
+                      const void* block_base, float* x, void* scratch, cudaStream_t stream) {
   const uint8_t* base = static_cast<const uint8_t*>(block_base);
   auto W = [&](int role) { return base + plan->params[plan->role[role]].slot_offset; };
   auto F = [&](int role) { return reinterpret_cast<const float*>(W(role)); };
@@ -106,6 +96,111 @@ dlo_status forward_impl(const dlo_dit_cfg* cfg, const dlo_plan* plan, const void
   DLO_TRY(launch_linear(h, M, d, H(R_W1), f, EPI_GELU_BF16, u, nullptr, stream));
   DLO_TRY(launch_linear(u, M, f, H(R_W2), d, EPI_RESID_F32, x, F(R_GATE2), stream));
   return DLO_OK;
+}
+
+// Cached CUDA graphs of the seven launches.  A graph bakes in every kernel
+// argument (tensor maps included), so its key is everything those depend
+// on: the shape, the plan (by id: addresses of freed plans can be reused),
+// the weight base, x, scratch and the device.
+struct GraphKey {
+  int32_t batch, tokens, hidden, heads, mlp;
+  float eps;
+  uint64_t plan_id;
+  const void* base;
+  const float* x;
+  const void* scratch;
+  int device;
+  bool operator==(const GraphKey& o) const {
+    return batch == o.batch && tokens == o.tokens && hidden == o.hidden && heads == o.heads &&
+           mlp == o.mlp && eps == o.eps && plan_id == o.plan_id && base == o.base &&
+           x == o.x && scratch == o.scratch && device == o.device;
+  }
+};
+
+constexpr size_t kMaxGraphs = 1024;
+std::mutex g_graph_mu;
+std::vector<std::pair<GraphKey, cudaGraphExec_t>> g_graphs;
+cudaStream_t g_capture[64] = {};
+
+dlo_status forward_graph(const dlo_dit_cfg* cfg, const dlo_plan* plan, const ScratchLayout& sl,
+                         const void* block_base, float* x, void* scratch,
+                         cudaStream_t stream) {
+  int dev = 0;
+  DLO_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) DLO_FAIL(DLO_ERR_INVALID, "forward: device %d out of range", dev);
+  const GraphKey key{cfg->batch, cfg->tokens, cfg->hidden, cfg->heads, cfg->mlp, cfg->eps,
+                     plan->id, block_base, x, scratch, dev};
+  cudaGraphExec_t exec = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_graph_mu);
+    for (auto& kv : g_graphs)
+      if (kv.first == key) {
+        exec = kv.second;
+        break;
+      }
+    if (!exec) {
+      if (!g_capture[dev]) DLO_CUDA(cudaStreamCreateWithFlags(&g_capture[dev],
+                                                              cudaStreamNonBlocking));
+      cudaStream_t cap = g_capture[dev];
+      DLO_CUDA(cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal));
+      const dlo_status st = launch_all(cfg, plan, sl, block_base, x, scratch, cap);
+      cudaGraph_t graph = nullptr;
+      const cudaError_t ce = cudaStreamEndCapture(cap, &graph);
+      if (st != DLO_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return st;
+      }
+      DLO_CUDA(ce);
+      const cudaError_t ie = cudaGraphInstantiate(&exec, graph, 0);
+      cudaGraphDestroy(graph);
+      DLO_CUDA(ie);
+      if (g_graphs.size() >= kMaxGraphs) {
+        // evict the oldest half; wait for the device so none is in flight
+        DLO_CUDA(cudaDeviceSynchronize());
+        for (size_t i = 0; i < kMaxGraphs / 2; ++i) cudaGraphExecDestroy(g_graphs[i].second);
+        g_graphs.erase(g_graphs.begin(), g_graphs.begin() + kMaxGraphs / 2);
+      }
+      g_graphs.emplace_back(key, exec);
+    }
+  }
+  DLO_CUDA(cudaGraphLaunch(exec, stream));
+  return DLO_OK;
+}
+
+}  // namespace
+
+dlo_status preload_kernels() {
+  static std::once_flag once;
+  static dlo_status st = DLO_OK;
+  std::call_once(once, [] {
+    st = gemm_preload();
+    if (st == DLO_OK) st = attention_preload();
+    if (st == DLO_OK) st = copy_preload();
+    if (st == DLO_OK && !device_error_word()) {
+      set_error("cannot resolve the device error word");
+      st = DLO_ERR_CUDA;
+    }
+  });
+  return st;
+}
+
+dlo_status forward_impl(const dlo_dit_cfg* cfg, const dlo_plan* plan, const void* block_base,
+                        float* x, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
+  DLO_TRY(check_cfg(cfg));
+  DLO_TRY(check_plan(*cfg, plan));
+  const ScratchLayout sl = scratch_layout(*cfg);
+  if (!block_base || !x || !scratch) DLO_FAIL(DLO_ERR_INVALID, "forward: null pointer");
+  if (reinterpret_cast<uintptr_t>(block_base) & 255u)
+    DLO_FAIL(DLO_ERR_INVALID, "forward: block base must be 256-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(scratch) & 255u))
+    DLO_FAIL(DLO_ERR_INVALID, "forward: x must be 16-byte and scratch 256-byte aligned");
+  if (scratch_bytes < sl.total)
+    DLO_FAIL(DLO_ERR_NOMEM, "forward: scratch holds %zu bytes, needs %zu", scratch_bytes,
+             sl.total);
+  DLO_TRY(preload_kernels());
+  if (cfg->flags & DLO_FWD_GRAPH)
+    return forward_graph(cfg, plan, sl, block_base, x, scratch, stream);
+  return launch_all(cfg, plan, sl, block_base, x, scratch, stream);
 }
 
 }  // namespace dlo

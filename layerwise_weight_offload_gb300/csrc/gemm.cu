@@ -318,15 +318,27 @@ int sm_count() {
 }
 
 template <int EPI>
+cudaError_t set_attr() {
+  return cudaFuncSetAttribute(gemm_tcgen05_kernel<EPI>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+}
+
+cudaError_t g_attr_err = cudaSuccess;
+std::once_flag g_attr_once;
+
+void set_all_attrs() {
+  std::call_once(g_attr_once, [] {
+    cudaError_t e0 = set_attr<EPI_BF16>(), e1 = set_attr<EPI_GELU_BF16>(),
+                e2 = set_attr<EPI_RESID_F32>();
+    g_attr_err = e0 != cudaSuccess ? e0 : (e1 != cudaSuccess ? e1 : e2);
+  });
+}
+
+template <int EPI>
 dlo_status launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int K,
                       void* out, const float* gate, int* err, cudaStream_t stream) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_tcgen05_kernel<EPI>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  });
-  DLO_CUDA(attr_err);
+  set_all_attrs();
+  DLO_CUDA(g_attr_err);
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
   gemm_tcgen05_kernel<EPI><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ma, mb, M, N, K, out, gate,
@@ -336,6 +348,14 @@ dlo_status launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N
 }
 
 }  // namespace
+
+dlo_status gemm_preload() {
+  set_all_attrs();
+  DLO_CUDA(g_attr_err);
+  if (!encode_fn()) DLO_FAIL(DLO_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  sm_count();
+  return DLO_OK;
+}
 
 dlo_status launch_linear(const uint16_t* a, int64_t M, int64_t K, const uint16_t* w, int64_t N,
                          int epilogue, void* out, const float* gate, cudaStream_t stream) {

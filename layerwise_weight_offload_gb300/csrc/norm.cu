@@ -1,7 +1,8 @@
 // norm.cu — RMSNorm fused with the adaLN modulation of the synthetic DiT
 // block: h = bf16( x / sqrt(mean(x^2) + eps) * g * (1 + scale) + shift ).
-// One CTA per row; the row is read twice (the second read hits L1/L2), the
-// mean square is reduced in a fixed tree order, so results are deterministic.
+// One warp per row; the row is read twice (the second read hits L1/L2), the
+// mean square is reduced in a fixed shuffle-tree order, so results are
+// deterministic.
 #include <cuda_bf16.h>
 
 #include "common.h"
@@ -9,37 +10,31 @@
 namespace dlo {
 namespace {
 
-constexpr int kNormThreads = 256;
+constexpr int kNormThreads = 256;            // 8 warps, one row per warp
+constexpr int kRowsPerCta = kNormThreads / 32;
 
 __global__ void __launch_bounds__(kNormThreads)
-rmsnorm_mod_kernel(const float* __restrict__ x, int64_t d, const float* __restrict__ g,
-                   const float* __restrict__ shift, const float* __restrict__ scale, float eps,
-                   uint16_t* __restrict__ h) {
-  const int64_t row = blockIdx.x;
+rmsnorm_mod_kernel(const float* __restrict__ x, int64_t rows, int64_t d,
+                   const float* __restrict__ g, const float* __restrict__ shift,
+                   const float* __restrict__ scale, float eps, uint16_t* __restrict__ h) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5);
+  if (row >= rows) return;
   const float4* xr = reinterpret_cast<const float4*>(x + row * d);
   const int64_t n4 = d / 4;
   float ss = 0.f;
-  for (int64_t i = threadIdx.x; i < n4; i += kNormThreads) {
+  for (int64_t i = lane; i < n4; i += 32) {
     const float4 v = xr[i];
     ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
-  __shared__ float red[kNormThreads / 32];
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float v = threadIdx.x < kNormThreads / 32 ? red[threadIdx.x] : 0.f;
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (threadIdx.x == 0) red[0] = v;
-  }
-  __syncthreads();
-  const float inv = rsqrtf(red[0] / static_cast<float>(d) + eps);
+  const float inv = rsqrtf(ss / static_cast<float>(d) + eps);
   const float4* g4 = reinterpret_cast<const float4*>(g);
   const float4* s4 = reinterpret_cast<const float4*>(scale);
   const float4* b4 = reinterpret_cast<const float4*>(shift);
   uint2* hr = reinterpret_cast<uint2*>(h + row * d);
-  for (int64_t i = threadIdx.x; i < n4; i += kNormThreads) {
-    const float4 v = xr[i], gg = g4[i], sc = s4[i], sh = b4[i];
+  for (int64_t i = lane; i < n4; i += 32) {
+    const float4 v = xr[i], gg = __ldg(g4 + i), sc = __ldg(s4 + i), sh = __ldg(b4 + i);
     const float o0 = v.x * inv * gg.x * (1.f + sc.x) + sh.x;
     const float o1 = v.y * inv * gg.y * (1.f + sc.y) + sh.y;
     const float o2 = v.z * inv * gg.z * (1.f + sc.z) + sh.z;
@@ -66,9 +61,10 @@ dlo_status launch_rmsnorm_mod(const float* x, int64_t rows, int64_t d, const flo
        reinterpret_cast<uintptr_t>(shift) | reinterpret_cast<uintptr_t>(scale)) & 15u ||
       reinterpret_cast<uintptr_t>(h) & 7u)
     DLO_FAIL(DLO_ERR_INVALID, "rmsnorm_mod: pointers must be 16-byte (h: 8-byte) aligned");
-  if (rows > 0x7fffffffLL) DLO_FAIL(DLO_ERR_INVALID, "rmsnorm_mod: too many rows");
-  rmsnorm_mod_kernel<<<static_cast<unsigned>(rows), kNormThreads, 0, stream>>>(x, d, g, shift,
-                                                                               scale, eps, h);
+  const int64_t ctas = (rows + kRowsPerCta - 1) / kRowsPerCta;
+  if (ctas > 0x7fffffffLL) DLO_FAIL(DLO_ERR_INVALID, "rmsnorm_mod: too many rows");
+  rmsnorm_mod_kernel<<<static_cast<unsigned>(ctas), kNormThreads, 0, stream>>>(
+      x, rows, d, g, shift, scale, eps, h);
   DLO_CUDA(cudaGetLastError());
   return DLO_OK;
 }

@@ -14,6 +14,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstring>
+#include <atomic>
 #include <new>
 
 #include "common.h"
@@ -66,6 +67,8 @@ dlo_status dlo_plan_create(const dlo_param_desc* params, int32_t n_params,
   dlo_plan* plan = new (std::nothrow) dlo_plan();
   if (!plan) DLO_FAIL(DLO_ERR_INVALID, "dlo_plan_create: out of host memory");
   plan->n_shards = n_shards;
+  static std::atomic<uint64_t> next_id{1};
+  plan->id = next_id.fetch_add(1);
   for (int32_t p = 0; p < n_params; ++p) {
     const dlo_param_desc& d = params[p];
     if (d.ndim < 1 || d.ndim > 4 || esize_of(d.dtype) == 0) {

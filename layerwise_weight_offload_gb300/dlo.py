@@ -53,13 +53,13 @@ class ParamInfo(ctypes.Structure):
 
 class DitCfg(ctypes.Structure):
     _fields_ = [("batch", c_i32), ("tokens", c_i32), ("hidden", c_i32), ("heads", c_i32),
-                ("mlp", c_i32), ("eps", c_f32)]
+                ("mlp", c_i32), ("eps", c_f32), ("flags", c_i32)]
 
 
 class EngineDesc(ctypes.Structure):
     _fields_ = [("n_blocks", c_i32), ("slot", c_vp * 2), ("slot_bytes", c_i64),
                 ("compute_stream", c_vp), ("copy_stream", c_vp), ("copy_mode", c_i32),
-                ("copy_ctas", c_i32), ("timing", c_i32)]
+                ("copy_ctas", c_i32), ("timing", c_i32), ("dma_streams", c_i32)]
 
 
 class SchedEvent(ctypes.Structure):
@@ -69,7 +69,8 @@ class SchedEvent(ctypes.Structure):
 
 class EngineStats(ctypes.Structure):
     _fields_ = [("chosen_mode", c_i32), ("n_forwards", c_i32), ("n_prefetches", c_i32),
-                ("dma_ns_per_mb", ctypes.c_double), ("kernel_ns_per_mb", ctypes.c_double)]
+                ("n_kernel_prefetches", c_i32), ("race_dma_us", ctypes.c_double),
+                ("race_kernel_us", ctypes.c_double)]
 
 
 _P = ctypes.POINTER
@@ -234,8 +235,12 @@ def reassemble(plan, shard_ptrs, dst, mode=COPY_DMA, stream=None):
 
 # ---- block forward -----------------------------------------------------------
 
-def dit_cfg(batch, tokens, hidden, heads, mlp, eps=1e-6):
-    return DitCfg(int(batch), int(tokens), int(hidden), int(heads), int(mlp), float(eps))
+FWD_GRAPH = 1
+
+
+def dit_cfg(batch, tokens, hidden, heads, mlp, eps=1e-6, graph=True):
+    return DitCfg(int(batch), int(tokens), int(hidden), int(heads), int(mlp), float(eps),
+                  FWD_GRAPH if graph else 0)
 
 
 def forward_scratch_bytes(cfg):
@@ -272,7 +277,7 @@ def kernel_status():
 
 class Engine:
     def __init__(self, n_blocks, slot0, slot1, slot_bytes, compute_stream, copy_stream,
-                 copy_mode=COPY_AUTO, copy_ctas=0, timing=False):
+                 copy_mode=COPY_AUTO, copy_ctas=0, timing=False, dma_streams=0):
         d = EngineDesc()
         d.n_blocks = int(n_blocks)
         d.slot[0] = _ptr(slot0)
@@ -283,6 +288,7 @@ class Engine:
         d.copy_mode = int(copy_mode)
         d.copy_ctas = int(copy_ctas)
         d.timing = 1 if timing else 0
+        d.dma_streams = int(dma_streams)
         h = c_vp()
         _check(lib().dlo_engine_create(ctypes.byref(d), ctypes.byref(h)), "dlo_engine_create")
         self.handle = h.value

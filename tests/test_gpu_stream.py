@@ -219,3 +219,74 @@ def test_ragged_streamed_vs_resident_vs_oracle(cfg):
         assert torch.equal(a, b)
     _check_against_oracle(host, per_block, range(len(per_block)))
     host.close()
+
+
+def test_graph_replay_equals_direct_launches():
+    w = W.custom("graph", n_blocks=2, hidden=256, heads=4, mlp=1024, tokens=130, shards=2)
+    host = HostBlocks(w, seed=4)
+    rs = ResidentStack(host)
+    x0 = W.gen_x(w, seed=4, device="cuda")
+    outs = []
+    for graph in (False, True, True):        # second graph call replays the cached graph
+        rs.cfg = dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps, graph=graph)
+        x = x0.clone()
+        rs.stream.wait_stream(torch.cuda.current_stream())
+        rs.step(x)
+        torch.cuda.current_stream().wait_stream(rs.stream)
+        outs.append(x)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    host.close()
+
+
+@pytest.mark.parametrize("dma_streams", [1, 2, 8])
+def test_dma_fan_out_bytes(dma_streams):
+    w = W.custom("fan", n_blocks=3, hidden=256, heads=4, mlp=1024, tokens=64, shards=5,
+                 distinct=3)
+    host = HostBlocks(w, seed=2, keep_params=True)
+    st = StreamedStack(host, copy_mode=dlo.COPY_DMA)
+    st.engine.destroy()
+    st.engine = dlo.Engine(w.n_blocks, st.slots[0], st.slots[1], st.slot_bytes, st.compute,
+                           st.copy, dlo.COPY_DMA, 0, False, dma_streams)
+    for i in range(w.n_blocks):
+        st.engine.register_block(i, host.plan, host.shard_ptrs(i))
+    st.prime()
+    for k in range(2 * w.n_blocks):
+        i = k % w.n_blocks
+        slot = st.engine.pre_forward(i)
+        snap = torch.empty_like(st.slots[slot])
+        with torch.cuda.stream(st.compute):
+            snap.copy_(st.slots[slot])
+        st.engine.post_forward(i)
+        torch.cuda.synchronize()
+        exp = _slot_image(host, i)
+        got = snap.cpu().numpy()
+        for g in host.plan.groups():
+            n = w.shards * g.shard_bytes
+            assert np.array_equal(got[g.base:g.base + n], exp[g.base:g.base + n])
+    st.close()
+    host.close()
+
+
+def test_auto_races_on_forward_time():
+    w = W.custom("race", n_blocks=5, hidden=512, heads=4, mlp=2048, tokens=256, shards=2,
+                 steps=4, distinct=5)
+    host = HostBlocks(w, seed=3)
+    st = StreamedStack(host, copy_mode=dlo.COPY_AUTO)
+    x = W.gen_x(w, seed=3, device="cuda")
+    st.compute.wait_stream(torch.cuda.current_stream())
+    for _ in range(w.steps):
+        st.step(x)
+    torch.cuda.synchronize()
+    s = st.engine.query()
+    assert s.race_dma_us > 0 and s.race_kernel_us > 0
+    assert s.chosen_mode in (dlo.COPY_DMA, dlo.COPY_KERNEL)
+    assert s.chosen_mode == (dlo.COPY_KERNEL if s.race_kernel_us < s.race_dma_us
+                             else dlo.COPY_DMA)
+    modes = [e[6] for e in st.engine.schedule_log()]
+    s0 = w.n_blocks + 2
+    assert modes[s0:s0 + 5] == [dlo.COPY_DMA] * 5
+    assert modes[s0 + 5:s0 + 10] == [dlo.COPY_KERNEL] * 5
+    assert s.n_kernel_prefetches >= 5
+    st.close()
+    host.close()
