@@ -197,6 +197,30 @@ dlo_status dlo_forward(const dlo_dit_cfg* cfg, const dlo_plan* plan,
                        const void* block_base, float* x, void* scratch,
                        size_t scratch_bytes, void* stream);
 
+/* dlo_forward without a caller scratch buffer, for callers that cannot
+ * allocate device memory: code running while a stream is captured into a
+ * CUDA graph (cudaMalloc is refused or breaks the capture there), serving
+ * loops that must not allocate after warm-up (cudaMalloc/cudaFree can
+ * synchronise the device and stall every stream), and hosts whose device
+ * memory belongs to another allocator with a fixed budget.  The pages have
+ * no counterpart of this call; it is an addition of this library.
+ * Scratch comes from a 32 MiB array in the library's own device memory
+ * (a file-scope __device__ array, held by every GPU that loads the library
+ * until the process exits).  A shape whose scratch
+ * (dlo_forward_scratch_bytes) exceeds 32 MiB is rejected with
+ * DLO_ERR_NOMEM.  The call allocates nothing: no cudaMalloc/cudaFree, no
+ * graph instantiation (the seven kernels are launched directly, whatever
+ * cfg->flags says).
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call on a device shares the one array,
+ * which keeps the last call's contents (the forward needs none of it to
+ * start at zero): calls whose work overlaps on the GPU (other streams, or
+ * other threads) race on it and must be serialised by the caller.
+ * Arguments and errors are those of dlo_forward. */
+dlo_status dlo_forward_noalloc(const dlo_dit_cfg* cfg, const dlo_plan* plan,
+                               const void* block_base, float* x, void* stream);
+
 /* Single steps of the block, for per-kernel checks (device pointers):
  *   rmsnorm_mod: h = bf16(x / sqrt(mean(x^2)+eps) * g * (1+scale) + shift)
  *   linear:      out = epilogue(a W^T), a bf16 [M,K], W bf16 [N,K];

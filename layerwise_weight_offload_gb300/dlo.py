@@ -84,6 +84,7 @@ _SIGS = {
     "dlo_reassemble": (c_i32, [c_vp, _P(c_vp), c_vp, c_i32, c_vp]),
     "dlo_forward_scratch_bytes": (c_sz, [_P(DitCfg)]),
     "dlo_forward": (c_i32, [_P(DitCfg), c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
+    "dlo_forward_noalloc": (c_i32, [_P(DitCfg), c_vp, c_vp, c_vp, c_vp]),
     "dlo_op_rmsnorm_mod": (c_i32, [c_vp, c_i64, c_i64, c_vp, c_vp, c_vp, c_f32, c_vp, c_vp]),
     "dlo_op_linear": (c_i32, [c_vp, c_i64, c_i64, c_vp, c_i64, c_i32, c_vp, c_vp, c_vp]),
     "dlo_op_attention": (c_i32, [c_vp, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp]),
@@ -250,6 +251,12 @@ def forward_scratch_bytes(cfg):
 def forward(cfg, plan, block_base, x, scratch, scratch_bytes, stream=None):
     _check(lib().dlo_forward(ctypes.byref(cfg), plan.handle, _ptr(block_base), _ptr(x),
                              _ptr(scratch), int(scratch_bytes), _stream(stream)), "dlo_forward")
+
+
+def forward_noalloc(cfg, plan, block_base, x, stream=None):
+    """dlo_forward with the library's static scratch (allocates nothing)."""
+    _check(lib().dlo_forward_noalloc(ctypes.byref(cfg), plan.handle, _ptr(block_base), _ptr(x),
+                                     _stream(stream)), "dlo_forward_noalloc")
 
 
 def op_rmsnorm_mod(x, rows, d, g, shift, scale, eps, h, stream=None):
