@@ -423,7 +423,9 @@ def run_only(args):
     elif args.only == "attention":
         qkv = torch.randn(M, 3 * d, device=dev).to(torch.bfloat16)
         o = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
-        fn = lambda: dlo.op_attention(qkv, w.batch, w.tokens, d, H, o, s)
+        nb = dlo.op_attention_scratch_bytes(w.batch, w.tokens, d)
+        sc = torch.empty(nb, dtype=torch.uint8, device=dev)
+        fn = lambda: dlo.op_attention(qkv, w.batch, w.tokens, d, H, o, sc, nb, s)
     elif args.only == "norm":
         x = torch.randn(M, d, device=dev)
         g = torch.ones(d, device=dev)

@@ -179,7 +179,8 @@ typedef struct {
 
 enum { DLO_FWD_GRAPH = 1 };
 
-/* Bytes of device scratch one block forward needs (bf16 h, qkv, o, u). */
+/* Bytes of device scratch one block forward needs (bf16 h, qkv, V
+ * transposed, o, u). */
 size_t dlo_forward_scratch_bytes(const dlo_dit_cfg* cfg);
 
 /* One block forward with weights at `block_base`, laid out as a slot of
@@ -228,7 +229,11 @@ dlo_status dlo_forward_noalloc(const dlo_dit_cfg* cfg, const dlo_plan* plan,
  *                         1: out bf16 [M,N] = GELU_tanh(acc)
  *                         2: out fp32 [M,N] += gate[N] * acc  (in place)
  *                K and N multiples of 8; pointers 16-byte aligned.
- *   attention:   o bf16 [batch*tokens, d] from qkv bf16 [batch*tokens, 3d] */
+ *   attention:   o bf16 [batch*tokens, d] from qkv bf16 [batch*tokens, 3d];
+ *                scratch (device, 16-byte aligned) holds V transposed,
+ *                dlo_op_attention_scratch_bytes(batch, tokens, d) bytes
+ *                (inside dlo_forward the QKV linear writes that layout
+ *                directly). */
 dlo_status dlo_op_rmsnorm_mod(const float* x, int64_t rows, int64_t d,
                               const float* g, const float* shift,
                               const float* scale, float eps, uint16_t* h,
@@ -236,8 +241,10 @@ dlo_status dlo_op_rmsnorm_mod(const float* x, int64_t rows, int64_t d,
 dlo_status dlo_op_linear(const uint16_t* a, int64_t M, int64_t K,
                          const uint16_t* w, int64_t N, int32_t epilogue,
                          void* out, const float* gate, void* stream);
+size_t dlo_op_attention_scratch_bytes(int64_t batch, int64_t tokens, int64_t d);
 dlo_status dlo_op_attention(const uint16_t* qkv, int64_t batch, int64_t tokens,
-                            int64_t d, int64_t heads, uint16_t* o, void* stream);
+                            int64_t d, int64_t heads, uint16_t* o, void* scratch,
+                            size_t scratch_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * Engine: two slots, the hook schedule, events ([B1] "Double-Buffer Memory

@@ -3,6 +3,7 @@
 // launchers each kernel file exports to the host-side orchestration.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -106,15 +107,38 @@ dlo_status launch_rmsnorm_mod(const float* x, int64_t rows, int64_t d,
                               cudaStream_t stream);
 
 // gemm.cu
-enum Epilogue { EPI_BF16 = 0, EPI_GELU_BF16 = 1, EPI_RESID_F32 = 2 };
+// EPI_QKV: columns [0, 2d) stored bf16 like EPI_BF16, columns [2d, 3d)
+// (the V block) stored transposed into vt[b*d + c, t] (row stride vt_ld).
+enum Epilogue { EPI_BF16 = 0, EPI_GELU_BF16 = 1, EPI_RESID_F32 = 2, EPI_QKV = 3 };
+struct EpiArgs {
+  void* out;            // bf16 [M, N], or fp32 x [M, N] for the residual
+  const float* gate;    // [N], residual epilogue
+  uint16_t* vt;         // EPI_QKV: V transposed
+  int64_t vt_ld;        // EPI_QKV: row stride of vt (>= tokens)
+  int tokens;           // EPI_QKV: rows per batch item
+  int v_col0;           // EPI_QKV: first V column (2d)
+};
 dlo_status launch_linear(const uint16_t* a, int64_t M, int64_t K,
                          const uint16_t* w, int64_t N, int epilogue, void* out,
                          const float* gate, cudaStream_t stream);
+dlo_status launch_linear_ex(const uint16_t* a, int64_t M, int64_t K, const uint16_t* w,
+                            int64_t N, int epilogue, const EpiArgs& ea, cudaStream_t stream);
 
 // attention.cu
-dlo_status launch_attention(const uint16_t* qkv, int64_t batch,
-                            int64_t tokens, int64_t d, int64_t heads,
-                            uint16_t* o, cudaStream_t stream);
+int64_t vt_ld_for(int64_t tokens);   // row stride of vt: tokens rounded up to 8
+dlo_status launch_attention_vt(const uint16_t* qkv, const uint16_t* vt, int64_t vt_ld,
+                               int64_t batch, int64_t tokens, int64_t d, int64_t heads,
+                               uint16_t* o, cudaStream_t stream);
+dlo_status launch_transpose_v(const uint16_t* qkv, int64_t batch, int64_t tokens, int64_t d,
+                              uint16_t* vt, int64_t vt_ld, cudaStream_t stream);
+
+// tmap.cu: TMA descriptors and device facts
+// Row-major bf16 matrix [rows, cols] with a row stride of `ld` elements as
+// TMA boxes of box_rows x box_cols (box_cols * 2 = 128 bytes with the
+// 128-byte swizzle); out-of-range elements read as zero.
+dlo_status make_tmap_2d(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols,
+                        int64_t ld, uint32_t box_rows, uint32_t box_cols);
+int sm_count();
 
 // status.cu: device-side error word written by bounded waits
 int* device_error_word();  // device address (cached per device)

@@ -19,17 +19,22 @@ namespace dlo {
 namespace {
 
 struct ScratchLayout {
-  size_t h, qkv, o, u, total;
+  size_t h, qkv, vt, o, u, total;
+  int64_t vt_ld;
 };
 
+// bf16 scratch of one forward: h [M, d] (both norms), qkv [M, 3d] (Q and K
+// used), vt [batch*d, vt_ld] (V transposed), o [M, d], u [M, f].
 ScratchLayout scratch_layout(const dlo_dit_cfg& c) {
   const size_t M = static_cast<size_t>(c.batch) * c.tokens;
   const size_t d = c.hidden, f = c.mlp;
   auto r = [](size_t v) { return (v + 255) / 256 * 256; };
   ScratchLayout s;
+  s.vt_ld = vt_ld_for(c.tokens);
   s.h = 0;
   s.qkv = r(s.h + M * d * 2);
-  s.o = r(s.qkv + M * 3 * d * 2);
+  s.vt = r(s.qkv + M * 3 * d * 2);
+  s.o = r(s.vt + static_cast<size_t>(c.batch) * d * static_cast<size_t>(s.vt_ld) * 2);
   s.u = r(s.o + M * d * 2);
   s.total = r(s.u + M * f * 2);
   return s;
@@ -84,13 +89,21 @@ dlo_status launch_all(const dlo_dit_cfg* cfg, const dlo_plan* plan, const Scratc
   uint8_t* s = static_cast<uint8_t*>(scratch);
   uint16_t* h = reinterpret_cast<uint16_t*>(s + sl.h);
   uint16_t* qkv = reinterpret_cast<uint16_t*>(s + sl.qkv);
+  uint16_t* vt = reinterpret_cast<uint16_t*>(s + sl.vt);
   uint16_t* o = reinterpret_cast<uint16_t*>(s + sl.o);
   uint16_t* u = reinterpret_cast<uint16_t*>(s + sl.u);
   const int64_t M = static_cast<int64_t>(cfg->batch) * cfg->tokens;
   const int64_t d = cfg->hidden, f = cfg->mlp;
   DLO_TRY(launch_rmsnorm_mod(x, M, d, F(R_G1), F(R_SHIFT1), F(R_SCALE1), cfg->eps, h, stream));
-  DLO_TRY(launch_linear(h, M, d, H(R_WQKV), 3 * d, EPI_BF16, qkv, nullptr, stream));
-  DLO_TRY(launch_attention(qkv, cfg->batch, cfg->tokens, d, cfg->heads, o, stream));
+  EpiArgs qa{};
+  qa.out = qkv;
+  qa.vt = vt;
+  qa.vt_ld = sl.vt_ld;
+  qa.tokens = cfg->tokens;
+  qa.v_col0 = static_cast<int>(2 * d);
+  DLO_TRY(launch_linear_ex(h, M, d, H(R_WQKV), 3 * d, EPI_QKV, qa, stream));
+  DLO_TRY(launch_attention_vt(qkv, vt, sl.vt_ld, cfg->batch, cfg->tokens, d, cfg->heads, o,
+                              stream));
   DLO_TRY(launch_linear(o, M, d, H(R_WO), d, EPI_RESID_F32, x, F(R_GATE1), stream));
   DLO_TRY(launch_rmsnorm_mod(x, M, d, F(R_G2), F(R_SHIFT2), F(R_SCALE2), cfg->eps, h, stream));
   DLO_TRY(launch_linear(h, M, d, H(R_W1), f, EPI_GELU_BF16, u, nullptr, stream));
@@ -231,10 +244,28 @@ dlo_status dlo_op_linear(const uint16_t* a, int64_t M, int64_t K, const uint16_t
                             static_cast<cudaStream_t>(stream));
 }
 
+size_t dlo_op_attention_scratch_bytes(int64_t batch, int64_t tokens, int64_t d) {
+  if (batch <= 0 || tokens <= 0 || d <= 0) return 0;
+  return static_cast<size_t>(batch * d * dlo::vt_ld_for(tokens) * 2);
+}
+
 dlo_status dlo_op_attention(const uint16_t* qkv, int64_t batch, int64_t tokens, int64_t d,
-                            int64_t heads, uint16_t* o, void* stream) {
-  return dlo::launch_attention(qkv, batch, tokens, d, heads, o,
-                               static_cast<cudaStream_t>(stream));
+                            int64_t heads, uint16_t* o, void* scratch, size_t scratch_bytes,
+                            void* stream) {
+  using namespace dlo;
+  if (batch == 0 || tokens == 0) return DLO_OK;
+  const size_t need = dlo_op_attention_scratch_bytes(batch, tokens, d);
+  if (!scratch || (reinterpret_cast<uintptr_t>(scratch) & 15u))
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_op_attention: scratch must be 16-byte aligned");
+  if (scratch_bytes < need)
+    DLO_FAIL(DLO_ERR_NOMEM, "dlo_op_attention: scratch holds %zu bytes, needs %zu",
+             scratch_bytes, need);
+  DLO_TRY(preload_kernels());
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint16_t* vt = static_cast<uint16_t*>(scratch);
+  const int64_t vt_ld = vt_ld_for(tokens);
+  DLO_TRY(launch_transpose_v(qkv, batch, tokens, d, vt, vt_ld, st));
+  return launch_attention_vt(qkv, vt, vt_ld, batch, tokens, d, heads, o, st);
 }
 
 }  // extern "C"

@@ -50,7 +50,23 @@ __device__ __forceinline__ float gelu_tanh(float z) {
 
 template <int EPI>
 __device__ __forceinline__ void epilogue_store(const uint32_t (&r)[32], int64_t row, int64_t n0,
-                                               int64_t N, void* out, const float* gate) {
+                                               int64_t N, const EpiArgs& ea) {
+  void* out = ea.out;
+  const float* gate = ea.gate;
+  if (EPI == EPI_QKV && n0 >= ea.v_col0) {
+    // V columns: transposed store, vt[b*d + c, t]; the 32 lanes of a warp
+    // hold 32 consecutive rows, so each store instruction writes 64
+    // contiguous bytes of one vt row
+    const int64_t b = row / ea.tokens, t = row - b * ea.tokens;
+    const int64_t d = ea.v_col0 / 2;
+    uint16_t* dst = ea.vt + (b * d + (n0 - ea.v_col0)) * ea.vt_ld + t;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      __nv_bfloat16 v = __float2bfloat16_rn(__uint_as_float(r[i]));
+      dst[static_cast<int64_t>(i) * ea.vt_ld] = *reinterpret_cast<uint16_t*>(&v);
+    }
+    return;
+  }
   if (EPI == EPI_RESID_F32) {
     float* xr = static_cast<float*>(out) + row * N + n0;
 #pragma unroll
@@ -89,8 +105,8 @@ __device__ __forceinline__ void epilogue_store(const uint32_t (&r)[32], int64_t 
 template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
-                    const __grid_constant__ CUtensorMap tma_b, int M, int N, int K, void* out,
-                    const float* gate, int* err) {
+                    const __grid_constant__ CUtensorMap tma_b, int M, int N, int K,
+                    const EpiArgs ea, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -232,7 +248,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int m_idx = tile % num_m, n_idx = tile / num_m;
-      if (!mbar_wait_bounded(&tfull[acc], acc_phase, abort)) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tfull[acc], acc_phase, abort))) {
         if (lane == 0) record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_EPILOGUE);
         break;
       }
@@ -247,7 +263,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
         tmem_ld_wait();
-        if (row < M) epilogue_store<EPI>(r, row, n0, N, out, gate);
+        if (row < M) epilogue_store<EPI>(r, row, n0, N, ea);
       }
       tc_fence_before();
       __syncwarp();
@@ -267,56 +283,6 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
   }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-// Row-major bf16 matrix [rows, cols] (cols contiguous) as TMA boxes of
-// box_rows x 64 with 128-byte swizzle; out-of-range elements read as zero.
-dlo_status make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols,
-                    uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) DLO_FAIL(DLO_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    DLO_FAIL(DLO_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %lld x %lld at %p", (int)r,
-             (long long)rows, (long long)cols, ptr);
-  return DLO_OK;
-}
-
-int sm_count() {
-  static int n = 0;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 152;
-  });
-  return n;
-}
-
 template <int EPI>
 cudaError_t set_attr() {
   return cudaFuncSetAttribute(gemm_tcgen05_kernel<EPI>,
@@ -329,20 +295,19 @@ std::once_flag g_attr_once;
 void set_all_attrs() {
   std::call_once(g_attr_once, [] {
     cudaError_t e0 = set_attr<EPI_BF16>(), e1 = set_attr<EPI_GELU_BF16>(),
-                e2 = set_attr<EPI_RESID_F32>();
-    g_attr_err = e0 != cudaSuccess ? e0 : (e1 != cudaSuccess ? e1 : e2);
+                e2 = set_attr<EPI_RESID_F32>(), e3 = set_attr<EPI_QKV>();
+    g_attr_err = e0 != cudaSuccess ? e0 : (e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3));
   });
 }
 
 template <int EPI>
 dlo_status launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int K,
-                      void* out, const float* gate, int* err, cudaStream_t stream) {
+                      const EpiArgs& ea, int* err, cudaStream_t stream) {
   set_all_attrs();
   DLO_CUDA(g_attr_err);
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
-  gemm_tcgen05_kernel<EPI><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ma, mb, M, N, K, out, gate,
-                                                                      err);
+  gemm_tcgen05_kernel<EPI><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ma, mb, M, N, K, ea, err);
   DLO_CUDA(cudaGetLastError());
   return DLO_OK;
 }
@@ -352,15 +317,14 @@ dlo_status launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N
 dlo_status gemm_preload() {
   set_all_attrs();
   DLO_CUDA(g_attr_err);
-  if (!encode_fn()) DLO_FAIL(DLO_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   sm_count();
   return DLO_OK;
 }
 
-dlo_status launch_linear(const uint16_t* a, int64_t M, int64_t K, const uint16_t* w, int64_t N,
-                         int epilogue, void* out, const float* gate, cudaStream_t stream) {
+dlo_status launch_linear_ex(const uint16_t* a, int64_t M, int64_t K, const uint16_t* w,
+                            int64_t N, int epilogue, const EpiArgs& ea, cudaStream_t stream) {
   if (M == 0) return DLO_OK;
-  if (!a || !w || !out || M < 0 || K <= 0 || N <= 0)
+  if (!a || !w || !ea.out || M < 0 || K <= 0 || N <= 0)
     DLO_FAIL(DLO_ERR_INVALID, "linear: bad arguments (M %lld, K %lld, N %lld)", (long long)M,
              (long long)K, (long long)N);
   if (K % 8 != 0 || N % 8 != 0)
@@ -369,22 +333,36 @@ dlo_status launch_linear(const uint16_t* a, int64_t M, int64_t K, const uint16_t
   if (M > (1LL << 31) - 1 || N > (1LL << 31) - 1 || K > (1LL << 31) - 1)
     DLO_FAIL(DLO_ERR_INVALID, "linear: extent too large");
   if ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(w) |
-       reinterpret_cast<uintptr_t>(out)) & 15u)
+       reinterpret_cast<uintptr_t>(ea.out)) & 15u)
     DLO_FAIL(DLO_ERR_INVALID, "linear: a, w and out must be 16-byte aligned");
-  if (epilogue == EPI_RESID_F32 && (!gate || (reinterpret_cast<uintptr_t>(gate) & 15u)))
+  if (epilogue == EPI_RESID_F32 && (!ea.gate || (reinterpret_cast<uintptr_t>(ea.gate) & 15u)))
     DLO_FAIL(DLO_ERR_INVALID, "linear: the residual epilogue needs a 16-byte aligned gate");
+  if (epilogue == EPI_QKV &&
+      (!ea.vt || ea.tokens <= 0 || ea.v_col0 <= 0 || ea.v_col0 % 64 != 0 || ea.vt_ld < ea.tokens ||
+       N != ea.v_col0 / 2 * 3))
+    DLO_FAIL(DLO_ERR_INVALID, "linear: bad arguments for the QKV epilogue");
   int* err = device_error_word();
   if (!err) DLO_FAIL(DLO_ERR_CUDA, "linear: cannot resolve the device error word");
   CUtensorMap ma, mb;
-  DLO_TRY(make_map(&ma, a, M, K, BM));
-  DLO_TRY(make_map(&mb, w, N, K, BN));
+  DLO_TRY(make_tmap_2d(&ma, a, M, K, K, BM, BK));
+  DLO_TRY(make_tmap_2d(&mb, w, N, K, K, BN, BK));
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   switch (epilogue) {
-    case EPI_BF16: return launch_epi<EPI_BF16>(ma, mb, m, n, k, out, gate, err, stream);
-    case EPI_GELU_BF16: return launch_epi<EPI_GELU_BF16>(ma, mb, m, n, k, out, gate, err, stream);
-    case EPI_RESID_F32: return launch_epi<EPI_RESID_F32>(ma, mb, m, n, k, out, gate, err, stream);
+    case EPI_BF16: return launch_epi<EPI_BF16>(ma, mb, m, n, k, ea, err, stream);
+    case EPI_GELU_BF16: return launch_epi<EPI_GELU_BF16>(ma, mb, m, n, k, ea, err, stream);
+    case EPI_RESID_F32: return launch_epi<EPI_RESID_F32>(ma, mb, m, n, k, ea, err, stream);
+    case EPI_QKV: return launch_epi<EPI_QKV>(ma, mb, m, n, k, ea, err, stream);
     default: DLO_FAIL(DLO_ERR_INVALID, "linear: unknown epilogue %d", epilogue);
   }
+}
+
+dlo_status launch_linear(const uint16_t* a, int64_t M, int64_t K, const uint16_t* w, int64_t N,
+                         int epilogue, void* out, const float* gate, cudaStream_t stream) {
+  if (epilogue == EPI_QKV) DLO_FAIL(DLO_ERR_INVALID, "linear: the QKV epilogue is internal");
+  EpiArgs ea{};
+  ea.out = out;
+  ea.gate = gate;
+  return launch_linear_ex(a, M, K, w, N, epilogue, ea, stream);
 }
 
 }  // namespace dlo

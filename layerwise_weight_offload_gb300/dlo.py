@@ -87,7 +87,8 @@ _SIGS = {
     "dlo_forward_noalloc": (c_i32, [_P(DitCfg), c_vp, c_vp, c_vp, c_vp]),
     "dlo_op_rmsnorm_mod": (c_i32, [c_vp, c_i64, c_i64, c_vp, c_vp, c_vp, c_f32, c_vp, c_vp]),
     "dlo_op_linear": (c_i32, [c_vp, c_i64, c_i64, c_vp, c_i64, c_i32, c_vp, c_vp, c_vp]),
-    "dlo_op_attention": (c_i32, [c_vp, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp]),
+    "dlo_op_attention_scratch_bytes": (c_sz, [c_i64, c_i64, c_i64]),
+    "dlo_op_attention": (c_i32, [c_vp, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp, c_sz, c_vp]),
     "dlo_engine_create": (c_i32, [_P(EngineDesc), _P(c_vp)]),
     "dlo_register_block": (c_i32, [c_vp, c_i32, c_vp, _P(c_vp)]),
     "dlo_prefetch": (c_i32, [c_vp, c_i32, c_i32]),
@@ -269,9 +270,13 @@ def op_linear(a, M, K, w, N, epilogue, out, gate=None, stream=None):
                                _stream(stream)), "dlo_op_linear")
 
 
-def op_attention(qkv, batch, tokens, d, heads, o, stream=None):
-    _check(lib().dlo_op_attention(_ptr(qkv), batch, tokens, d, heads, _ptr(o), _stream(stream)),
-           "dlo_op_attention")
+def op_attention_scratch_bytes(batch, tokens, d):
+    return int(lib().dlo_op_attention_scratch_bytes(batch, tokens, d))
+
+
+def op_attention(qkv, batch, tokens, d, heads, o, scratch, scratch_bytes, stream=None):
+    _check(lib().dlo_op_attention(_ptr(qkv), batch, tokens, d, heads, _ptr(o), _ptr(scratch),
+                                  int(scratch_bytes), _stream(stream)), "dlo_op_attention")
 
 
 def kernel_status():

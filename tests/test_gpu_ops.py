@@ -85,6 +85,12 @@ def test_linear(M, K, N, epi):
         assert np.all(np.abs(got - ref) <= tol), np.abs(got - ref).max()
 
 
+def _attention(qkv, B, T, d, H, o):
+    n = dlo.op_attention_scratch_bytes(B, T, d)
+    scratch = torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda")   # NaN-filled
+    dlo.op_attention(qkv, B, T, d, H, o, scratch, n)
+
+
 ATT_SHAPES = [
     (1, 64, 256, 4),     # hd 64, one KV tile
     (1, 200, 256, 4),    # ragged tokens
@@ -92,6 +98,8 @@ ATT_SHAPES = [
     (1, 1, 128, 1),      # single token: output = v
     (1, 1024, 1024, 16),
     (1, 333, 384, 3),
+    (1, 2500, 256, 2),   # many KV tiles: rescaling path, hd 128
+    (3, 129, 128, 2),    # three batch items, one key past a tile
 ]
 
 
@@ -100,7 +108,7 @@ def test_attention(B, T, d, H):
     r = _gen(B * 1000 + T + d + H)
     qkv = r(B * T, 3 * d).to(torch.bfloat16)
     o = torch.full((B * T, d), float("nan"), dtype=torch.bfloat16, device="cuda")
-    dlo.op_attention(qkv.cuda(), B, T, d, H, o)
+    _attention(qkv.cuda(), B, T, d, H, o)
     _status_clean()
     ref = oracle.attention(qkv.float().numpy(), B, T, d, H)
     got = o.float().cpu().numpy()
@@ -118,7 +126,7 @@ def test_attention_scale_is_checked_by_two_tokens():
     qkv[:, 2 * d:] = torch.randn(2, d, generator=torch.Generator().manual_seed(2))
     qkv = qkv.to(torch.bfloat16)
     o = torch.empty(2, d, dtype=torch.bfloat16, device="cuda")
-    dlo.op_attention(qkv.cuda(), 1, 2, d, 1, o)
+    _attention(qkv.cuda(), 1, 2, d, 1, o)
     _status_clean()
     ref = oracle.attention(qkv.float().numpy(), 1, 2, d, 1)
     assert_oracle_close(o.float().cpu().numpy(), ref, "two tokens", 1e-2, 4e-3)
@@ -130,4 +138,4 @@ def test_rejects_unsupported_shapes():
         dlo.op_linear(a, 4, 12, a, 4, dlo.EPI_BF16, a)            # K, N not multiples of 8
     q = torch.zeros(4, 96 * 3, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(dlo.DLOError):
-        dlo.op_attention(q, 1, 4, 96, 3, q)                        # head dim 32
+        _attention(q, 1, 4, 96, 3, q)                              # head dim 32
