@@ -443,6 +443,8 @@ def run_only(args):
             rs = ResidentStack(host, stream=s)
             x = W.gen_x(w, args.seed, device=dev)
             fn = lambda: rs.block(0, x)
+    for _ in range(2):          # first calls: module loading, attributes, graph capture
+        fn()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s)

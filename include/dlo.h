@@ -60,9 +60,11 @@ typedef enum {
 typedef enum { DLO_BF16 = 0, DLO_F32 = 1 } dlo_dtype;
 
 /* How a prefetch moves the shards host->device.
- *   DMA:    one cudaMemcpyAsync per (dtype group, shard) on the copy stream,
- *           straight to the shard's final offset in the slot (copy engines,
- *           no SMs).
+ *   DMA:    copy engines, no SMs: per dtype group one cudaMemcpy2DAsync
+ *           when the group's host shards sit at a constant stride (rows =
+ *           shards, destination pitch = shard bytes, i.e. the gathered
+ *           layout), else one cudaMemcpyAsync per shard, each straight to
+ *           the shard's final offset in the slot.
  *   KERNEL: one launch of a copy-and-reassemble kernel that reads the mapped
  *           pinned host shards with 16-byte loads and writes them to their
  *           final slot offsets (SMs read over the host link).
@@ -180,7 +182,8 @@ typedef struct {
 enum { DLO_FWD_GRAPH = 1 };
 
 /* Bytes of device scratch one block forward needs (bf16 h, qkv, V
- * transposed, o, u). */
+ * transposed, o, u, and the fp32 split-K workspace of its narrow linears).
+ * The split choice depends on the device's SM count. */
 size_t dlo_forward_scratch_bytes(const dlo_dit_cfg* cfg);
 
 /* One block forward with weights at `block_base`, laid out as a slot of
@@ -229,6 +232,14 @@ dlo_status dlo_forward_noalloc(const dlo_dit_cfg* cfg, const dlo_plan* plan,
  *                         1: out bf16 [M,N] = GELU_tanh(acc)
  *                         2: out fp32 [M,N] += gate[N] * acc  (in place)
  *                K and N multiples of 8; pointers 16-byte aligned.
+ *                workspace (device, may be null): when the output has too
+ *                few 128x256 tiles to fill the GPU, K is split into slices
+ *                computed in parallel into fp32 partials in the workspace,
+ *                then summed in slice order (deterministic) by a second
+ *                kernel that applies the epilogue; this needs
+ *                dlo_op_linear_workspace_bytes(M, N, K, epilogue) bytes
+ *                (0: the shape does not split).  Without enough workspace
+ *                the linear runs unsplit.
  *   attention:   o bf16 [batch*tokens, d] from qkv bf16 [batch*tokens, 3d];
  *                scratch (device, 16-byte aligned) holds V transposed,
  *                dlo_op_attention_scratch_bytes(batch, tokens, d) bytes
@@ -238,9 +249,11 @@ dlo_status dlo_op_rmsnorm_mod(const float* x, int64_t rows, int64_t d,
                               const float* g, const float* shift,
                               const float* scale, float eps, uint16_t* h,
                               void* stream);
+size_t dlo_op_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t epilogue);
 dlo_status dlo_op_linear(const uint16_t* a, int64_t M, int64_t K,
                          const uint16_t* w, int64_t N, int32_t epilogue,
-                         void* out, const float* gate, void* stream);
+                         void* out, const float* gate, void* workspace,
+                         size_t workspace_bytes, void* stream);
 size_t dlo_op_attention_scratch_bytes(int64_t batch, int64_t tokens, int64_t d);
 dlo_status dlo_op_attention(const uint16_t* qkv, int64_t batch, int64_t tokens,
                             int64_t d, int64_t heads, uint16_t* o, void* scratch,
@@ -347,11 +360,12 @@ dlo_status dlo_schedule_log(const dlo_engine* e, dlo_sched_event* buf,
  * mode; DLO_COPY_AUTO while undecided); n_kernel_prefetches counts
  * copy-kernel launches.  AUTO races the two modes on the quantity that
  * matters, the compute stream's time per block forward while the next
- * block streams in.  With n = n_blocks, the prefetches issued by forwards
- * n+2 .. n+6 use DMA and those issued by forwards n+7 .. n+11 the copy
- * kernel (after one full pass, so first-touch costs are excluded);
- * race_dma_us / race_kernel_us are the mean intervals between consecutive
- * free events inside each window (0 until measured). */
+ * block streams in.  With n = n_blocks, four windows of 6 forwards start at
+ * forward n+2 (after one full pass, so first-touch costs are excluded):
+ * the prefetches issued in windows 1 and 3 use DMA, in windows 2 and 4 the
+ * copy kernel; race_dma_us / race_kernel_us are each mode's better
+ * window's mean interval between consecutive free events (0 until
+ * measured). */
 typedef struct {
   int32_t chosen_mode;
   int32_t n_forwards;

@@ -7,25 +7,30 @@
 // c, u] (keys contiguous), which the QKV linear's epilogue writes directly,
 // so that both products below take K-major operands.
 //
-// One CTA = 128 queries of one (batch, head), 6 warps:
-//   warp 0     TMA: the Q tile once, then K and V^T tiles of 128 keys into a
-//              2-stage ring (full/empty mbarriers);
-//   warp 1     allocates 512 TMEM columns and issues tcgen05.mma:
-//              S_j = Q K_j^T (M=128, N=128) into one of two TMEM S buffers,
-//              then O += P_{j-1} V_{j-1} (M=128, N=hd) into the TMEM O
-//              accumulator, so the next S overlaps the softmax of the
-//              previous tile;
-//   warps 2-5  one thread per query row (its TMEM lane): tcgen05.ld of the
-//              S row, mask of keys past the end, running maximum and sum in
-//              the exp2 domain, P = exp2(s - m) written as bf16 into a
-//              128-byte-swizzled shared tile for the next MMA; at the end
-//              O / l is stored as bf16.
-// The running maximum is allowed to go stale by up to 2^8 (in the exp2
-// domain): O in TMEM is rescaled (tcgen05.ld, multiply, tcgen05.st) only
-// when a row's maximum grows by more than 8, which keeps every P <= 256.
-// Keys past the end are -inf in S and zero in V (TMA zero fill).  All waits
-// are bounded; a wait that runs out records a code in the device error
-// word and the kernel returns early.
+// One CTA = 128 queries of one (batch, head), 11 warps:
+//   warp 0     TMA: the Q tile once, then K tiles of 128 keys into a 2-stage
+//              ring (a stage is released as soon as its S product is done);
+//   warp 10    TMA: V^T tiles of 128 keys into a 2-stage ring (released after
+//              the PV product), so a V reload never delays the next K;
+//   warp 1     allocates 512 TMEM columns and issues tcgen05.mma: S_j =
+//              Q K_j^T (M=128, N=128) into S buffer j%2, and O_{j%2} +=
+//              P_j V_j (M=128, N=hd); S_{j+2} is issued right after PV_j;
+//   warps 2-5  softmax set 0: even KV tiles; warps 6-9: set 1, odd tiles.
+//              One thread per query row (its TMEM lane): tcgen05.ld of the S
+//              row, mask of keys past the end, running maximum and sum in
+//              the exp2 domain, P = exp2(s - m) as bf16 into the set's
+//              128-byte-swizzled P tile.  Two sets put two warps on every
+//              scheduler, so one set's latencies hide behind the other's
+//              work.  Each set keeps its own (m, l, O); at the end the two
+//              are merged, O = (O_0 2^(m_0-m) + O_1 2^(m_1-m)) / l, and each
+//              set stores half of the head dimension as bf16.
+// A set's running maximum may go stale by up to 2^8 (exp2 domain): its O is
+// rescaled in TMEM (tcgen05.ld, multiply, tcgen05.st) only when a row's
+// maximum grows by more than 8, so every P <= 256.  S_{j+2} is issued after
+// PV_j, so when a set sees S of its next tile, its previous PV is complete
+// and both its O and its P tile are free.  Keys past the end are -inf in S
+// and zero in V (TMA zero fill).  All waits are bounded; a wait that runs
+// out records a code in the device error word and the kernel returns early.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -36,7 +41,7 @@
 namespace dlo {
 namespace {
 
-constexpr int BQ = 128, BKV = 128, ATT_THREADS = 192;
+constexpr int BQ = 128, BKV = 128, ATT_THREADS = 352;
 constexpr uint32_t ATT_TMEM_COLS = 512;
 constexpr float kRescaleThreshold = 8.f;   // log2 units
 
@@ -61,6 +66,14 @@ __device__ __forceinline__ void att_fail(int* err, volatile int* abort, int code
   *abort = 1;
 }
 
+// 2^x by the hardware approximation (MUFU.EX2 through the PTX instruction;
+// denormal results flush to zero, 2^-inf = 0).  Inputs here are <= 8.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);
@@ -82,14 +95,15 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* q_full = bar + 0;
   uint64_t* k_full = bar + 1;     // [2]
-  uint64_t* v_full = bar + 3;     // [2]
-  uint64_t* kv_empty = bar + 5;   // [2]
-  uint64_t* s_full = bar + 7;     // [2]
-  uint64_t* s_empty = bar + 9;    // [2]
-  uint64_t* p_full = bar + 11;    // [2]
-  uint64_t* pv_done = bar + 13;
-  uint64_t* drain = bar + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 15);
+  uint64_t* k_empty = bar + 3;    // [2]
+  uint64_t* v_full = bar + 5;     // [2]
+  uint64_t* v_empty = bar + 7;    // [2]
+  uint64_t* s_full = bar + 9;     // [2]  per softmax set
+  uint64_t* s_empty = bar + 11;   // [2]
+  uint64_t* p_full = bar + 13;    // [2]
+  uint64_t* pv_done = bar + 15;   // [2]
+  uint64_t* drain = bar + 17;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 18);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -101,13 +115,14 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
     mbar_init(q_full, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
       mbar_init(&s_full[s], 1);
       mbar_init(&s_empty[s], 4);
       mbar_init(&p_full[s], 4);
+      mbar_init(&pv_done[s], 1);
     }
-    mbar_init(pv_done, 1);
     mbar_init(drain, 1);
     *abort = 0;
     fence_mbar_init();
@@ -124,44 +139,47 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;             // two buffers of 128 columns
-  const uint32_t tO = tmem + 256;       // HD columns
+  const uint32_t tS = tmem;             // S of set x at column 128 x
+  const uint32_t tO = tmem + 256;       // O of set x at column 256 + HD x
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 10) {
     if (lane == 0) {
-      const int row_q = b * tokens + q0;
-      mbar_arrive_expect_tx(q_full, L::Q_BYTES);
-      for (int c = 0; c < HD / 64; ++c)
-        tma_load_2d(sQ + c * (BQ * 128), &tm_qk, q_full, head * HD + 64 * c, row_q);
+      const bool is_k = warp == 0;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      if (is_k) {
+        mbar_arrive_expect_tx(q_full, L::Q_BYTES);
+        for (int c = 0; c < HD / 64; ++c)
+          tma_load_2d(sQ + c * (BQ * 128), &tm_qk, q_full, head * HD + 64 * c, b * tokens + q0);
+      }
       int issued = 0;
-      bool ok = true;
       for (int j = 0; j < n_kv; ++j) {
         const int s = j & 1;
         const uint32_t n = static_cast<uint32_t>(j >> 1);
-        if (!mbar_wait_bounded(&kv_empty[s], (n & 1u) ^ 1u, abort)) {
+        const int kv0 = j * BKV;
+        if (!mbar_wait_bounded(&empty[s], (n & 1u) ^ 1u, abort)) {
           att_fail(err, abort, DEV_TIMEOUT_PRODUCER);
-          ok = false;
           break;
         }
-        const int kv0 = j * BKV;
-        mbar_arrive_expect_tx(&k_full[s], L::K_BYTES);
-        for (int c = 0; c < HD / 64; ++c)
-          tma_load_2d(sK + s * L::K_BYTES + c * (BKV * 128), &tm_qk, &k_full[s],
-                      d + head * HD + 64 * c, b * tokens + kv0);
-        mbar_arrive_expect_tx(&v_full[s], L::V_BYTES);
-        for (int c = 0; c < 2; ++c)
-          tma_load_2d(sV + s * L::V_BYTES + c * L::V_CHUNK, &tm_vt, &v_full[s], kv0 + 64 * c,
-                      (b * heads + head) * HD);
+        if (is_k) {
+          mbar_arrive_expect_tx(&full[s], L::K_BYTES);
+          for (int c = 0; c < HD / 64; ++c)
+            tma_load_2d(sK + s * L::K_BYTES + c * (BKV * 128), &tm_qk, &full[s],
+                        d + head * HD + 64 * c, b * tokens + kv0);
+        } else {
+          mbar_arrive_expect_tx(&full[s], L::V_BYTES);
+          for (int c = 0; c < 2; ++c)
+            tma_load_2d(sV + s * L::V_BYTES + c * L::V_CHUNK, &tm_vt, &full[s], kv0 + 64 * c,
+                        (b * heads + head) * HD);
+        }
         ++issued;
       }
-      if (!ok) {
+      if (*abort) {
         // let the copies already issued land before the CTA can exit
         volatile int never = 0;
-        mbar_wait_bounded(q_full, 0, &never);
-        for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j) {
-          mbar_wait_bounded(&k_full[j & 1], static_cast<uint32_t>((j >> 1) & 1), &never);
-          mbar_wait_bounded(&v_full[j & 1], static_cast<uint32_t>((j >> 1) & 1), &never);
-        }
+        if (is_k) mbar_wait_bounded(q_full, 0, &never);
+        for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
+          mbar_wait_bounded(&full[j & 1], static_cast<uint32_t>((j >> 1) & 1), &never);
       }
     }
   } else if (warp == 1) {
@@ -171,169 +189,210 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
       bool ok = mbar_wait_bounded(q_full, 0, abort);
       if (!ok) att_fail(err, abort, DEV_TIMEOUT_MMA_FULL);
       const uint32_t q_addr = smem_u32(sQ);
-      for (int j = 0; ok && j <= n_kv; ++j) {
-        if (j < n_kv) {
-          const int s = j & 1;
-          const uint32_t n = static_cast<uint32_t>(j >> 1);
-          if (!mbar_wait_bounded(&k_full[s], n & 1u, abort) ||
-              !mbar_wait_bounded(&s_empty[s], (n & 1u) ^ 1u, abort)) {
-            att_fail(err, abort, DEV_TIMEOUT_MMA_FULL);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t k_addr = smem_u32(sK + s * L::K_BYTES);
+      // S_j = Q K_j^T into S buffer j%2
+      auto issue_s = [&](int j) -> bool {
+        const int x = j & 1;
+        const uint32_t n = static_cast<uint32_t>(j >> 1);
+        if (!mbar_wait_bounded(&k_full[x], n & 1u, abort) ||
+            !mbar_wait_bounded(&s_empty[x], (n & 1u) ^ 1u, abort))
+          return false;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sK + x * L::K_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-            umma_bf16(tS + s * BKV, sdesc_k_sw128(q_addr + off), sdesc_k_sw128(k_addr + off),
-                      idesc_s, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(&s_full[s]);
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
+          umma_bf16(tS + x * BKV, sdesc_k_sw128(q_addr + off), sdesc_k_sw128(k_addr + off),
+                    idesc_s, kk > 0 ? 1u : 0u);
         }
-        if (j >= 1) {
-          const int jj = j - 1;
-          const int s = jj & 1;
-          const uint32_t n = static_cast<uint32_t>(jj >> 1);
-          if (!mbar_wait_bounded(&p_full[s], n & 1u, abort) ||
-              !mbar_wait_bounded(&v_full[s], n & 1u, abort)) {
-            att_fail(err, abort, DEV_TIMEOUT_MMA_FULL);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t p_addr = smem_u32(sP + s * L::P_BYTES);
-          const uint32_t v_addr = smem_u32(sV + s * L::V_BYTES);
+        umma_commit(&k_empty[x]);
+        umma_commit(&s_full[x]);
+        return true;
+      };
+      for (int j = 0; ok && j < 2 && j < n_kv; ++j) ok = issue_s(j);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int x = j & 1;
+        const uint32_t n = static_cast<uint32_t>(j >> 1);
+        if (!mbar_wait_bounded(&p_full[x], n & 1u, abort) ||
+            !mbar_wait_bounded(&v_full[x], n & 1u, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t p_addr = smem_u32(sP + x * L::P_BYTES);
+        const uint32_t v_addr = smem_u32(sV + x * L::V_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BKV / 16; ++kk) {
-            umma_bf16(tO, sdesc_k_sw128(p_addr + (kk >> 2) * L::P_CHUNK + (kk & 3) * 32),
-                      sdesc_k_sw128(v_addr + (kk >> 2) * L::V_CHUNK + (kk & 3) * 32), idesc_o,
-                      (jj > 0 || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(&kv_empty[s]);
-          umma_commit(pv_done);
-        }
+        for (int kk = 0; kk < BKV / 16; ++kk)
+          umma_bf16(tO + x * HD, sdesc_k_sw128(p_addr + (kk >> 2) * L::P_CHUNK + (kk & 3) * 32),
+                    sdesc_k_sw128(v_addr + (kk >> 2) * L::V_CHUNK + (kk & 3) * 32), idesc_o,
+                    (j >= 2 || kk > 0) ? 1u : 0u);
+        umma_commit(&v_empty[x]);
+        umma_commit(&pv_done[x]);
+        if (j + 2 < n_kv) ok = issue_s(j + 2);
       }
       if (!ok) {
+        att_fail(err, abort, DEV_TIMEOUT_MMA_FULL);
         volatile int never = 0;
         umma_commit(drain);
         mbar_wait_bounded(drain, 0, &never);
       }
     }
   } else {
+    const int x = (warp - 2) >> 2;             // softmax set: 0 even tiles, 1 odd tiles
     const int quad = warp & 3;
     const int row = quad * 32 + lane;          // query row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tSx = tS + x * BKV, tOx = tO + x * HD;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      const int s = j & 1;
+    int last = -1;                             // last tile this set processed
+    for (int j = x; j < n_kv; j += 2) {
       const uint32_t n = static_cast<uint32_t>(j >> 1);
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&s_full[s], n & 1u, abort))) {
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&s_full[x], n & 1u, abort))) {
         if (lane == 0) att_fail(err, abort, DEV_TIMEOUT_EPILOGUE);
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sr[4][32];
+      const int valid = tokens - j * BKV;      // keys of this tile that exist
+      // pass 1: row maximum of the raw scores (S is read twice from TMEM so
+      // that only 64 of its 128 values are in registers at a time)
+      float mx[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tS + s * BKV + c * 32 + lane_off, sr[c]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[s]);
-      const int kv0 = j * BKV;
-      const int valid = tokens - kv0;          // keys of this tile that exist
-      float mt = -INFINITY;
+      for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int cp = 0; cp < 2; ++cp) {
+        uint32_t ra[32], rb[32];
+        tmem_ld_32x32b_x32(tSx + (2 * cp) * 32 + lane_off, ra);
+        tmem_ld_32x32b_x32(tSx + (2 * cp + 1) * 32 + lane_off, rb);
+        tmem_ld_wait();
+        if (valid < BKV) {                     // only the last tile has missing keys
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (cp * 64 + i >= valid) ra[i] = __float_as_uint(-INFINITY);
+            if (cp * 64 + 32 + i >= valid) rb[i] = __float_as_uint(-INFINITY);
+          }
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          float x = __uint_as_float(sr[c][i]) * scale_log2;
-          if (c * 32 + i >= valid) x = -INFINITY;
-          sr[c][i] = __float_as_uint(x);
-          mt = fmaxf(mt, x);
+          mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(ra[i]));
+          mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(rb[i]));
         }
-      if (j == 0) {
+      }
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+                       scale_log2;
+      if (last < 0) {
         m = mt;
       } else {
         const bool need = mt > m + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
-          // O must hold every product up to tile j-1 before it is scaled
-          if (!__all_sync(0xffffffffu,
-                          mbar_wait_bounded(pv_done, static_cast<uint32_t>((j - 1) & 1), abort))) {
-            if (lane == 0) att_fail(err, abort, DEV_TIMEOUT_EPILOGUE);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+          // this set's previous PV completed before its S_j was issued
           float corr = 1.f;
           if (need) {
-            corr = exp2f(m - mt);
+            corr = ex2_approx(m - mt);
             m = mt;
             l *= corr;
           }
 #pragma unroll 1
           for (int c = 0; c < HD / 32; ++c) {
             uint32_t orr[32];
-            tmem_ld_32x32b_x32(tO + c * 32 + lane_off, orr);
+            tmem_ld_32x32b_x32(tOx + c * 32 + lane_off, orr);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               orr[i] = __float_as_uint(__uint_as_float(orr[i]) * corr);
-            tmem_st_32x32b_x32(tO + c * 32 + lane_off, orr);
+            tmem_st_32x32b_x32(tOx + c * 32 + lane_off, orr);
           }
           tmem_st_wait();
         }
       }
-      // P = exp2(s - m) as bf16 into the swizzled P tile of this stage
-      uint8_t* prow = sP + s * L::P_BYTES + row * 128;
+      // pass 2: P = exp2(s * scale - m) as bf16 into this set's swizzled P
+      // tile; the row sum runs in eight independent partial sums
+      uint8_t* prow = sP + x * L::P_BYTES + row * 128;
+      const float neg_m = -m;
+      float ls[8];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        float p[8];
+      for (int e = 0; e < 8; ++e) ls[e] = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p[e] = exp2f(__uint_as_float(sr[c >> 2][(c & 3) * 8 + e]) - m);
-          l += p[e];
-        }
-        const uint4 v = make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]),
-                                   pack_bf16(p[4], p[5]), pack_bf16(p[6], p[7]));
-        const int cc = c & 7;
-        *reinterpret_cast<uint4*>(prow + (c >> 3) * L::P_CHUNK + ((cc ^ (row & 7)) << 4)) = v;
+      for (int cp = 0; cp < 2; ++cp) {
+        uint32_t rr[2][32];
+        tmem_ld_32x32b_x32(tSx + (2 * cp) * 32 + lane_off, rr[0]);
+        tmem_ld_32x32b_x32(tSx + (2 * cp + 1) * 32 + lane_off, rr[1]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {        // 8 keys: chunk c of the 16 in a row
+            const int c = cp * 8 + h * 4 + q;
+            float p[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              float v = ex2_approx(fmaf(__uint_as_float(rr[h][q * 8 + e]), scale_log2, neg_m));
+              if (valid < BKV && c * 8 + e >= valid) v = 0.f;
+              p[e] = v;
+              ls[e] += v;
+            }
+            const uint4 pk = make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]),
+                                        pack_bf16(p[4], p[5]), pack_bf16(p[6], p[7]));
+            const int cc = c & 7;
+            *reinterpret_cast<uint4*>(prow + (c >> 3) * L::P_CHUNK + ((cc ^ (row & 7)) << 4)) = pk;
+          }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[x]);
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[s]);
+      if (lane == 0) mbar_arrive(&p_full[x]);
+      last = j;
     }
-    if (ok) {
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait_bounded(pv_done, static_cast<uint32_t>((n_kv - 1) & 1), abort))) {
-        if (lane == 0) att_fail(err, abort, DEV_TIMEOUT_EPILOGUE);
-      } else {
-        tc_fence_after();
-        const float inv = 1.f / l;
-        const int t = q0 + row;
-        uint16_t* orow = o + (static_cast<int64_t>(b) * tokens + t) * d + head * HD;
+    // this set's last product, then the merge of the two sets through the
+    // (now idle) P tiles
+    if (ok && last >= 0 &&
+        !__all_sync(0xffffffffu,
+                    mbar_wait_bounded(&pv_done[x], static_cast<uint32_t>((last >> 1) & 1),
+                                      abort))) {
+      if (lane == 0) att_fail(err, abort, DEV_TIMEOUT_EPILOGUE);
+      ok = false;
+    }
+    // both sets must be past their last product before any P tile is reused
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    float* xch = reinterpret_cast<float*>(sP);  // [set][row] m, then l
+    xch[x * 256 + row] = m;
+    xch[x * 256 + 128 + row] = l;
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    const float m0 = xch[row], l0 = xch[128 + row];
+    const float m1 = xch[256 + row], l1 = xch[384 + row];
+    const float mm = fmaxf(m0, m1);
+    const float c0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - mm);
+    const float c1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - mm);
+    const float inv = 1.f / (l0 * c0 + l1 * c1);
+    if (ok && !*abort) {
+      tc_fence_after();
+      const int t = q0 + row;
+      uint16_t* orow = o + (static_cast<int64_t>(b) * tokens + t) * d + head * HD;
 #pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t orr[32];
-          tmem_ld_32x32b_x32(tO + c * 32 + lane_off, orr);
-          tmem_ld_wait();
-          if (t < tokens) {
+      for (int c = x * (HD / 64); c < (x + 1) * (HD / 64); ++c) {
+        uint32_t oa[32], ob[32];
+        tmem_ld_32x32b_x32(tO + c * 32 + lane_off, oa);
+        tmem_ld_32x32b_x32(tO + HD + c * 32 + lane_off, ob);
+        tmem_ld_wait();
+        if (t < tokens) {
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              const uint4 v = make_uint4(
-                  pack_bf16(__uint_as_float(orr[8 * g + 0]) * inv,
-                            __uint_as_float(orr[8 * g + 1]) * inv),
-                  pack_bf16(__uint_as_float(orr[8 * g + 2]) * inv,
-                            __uint_as_float(orr[8 * g + 3]) * inv),
-                  pack_bf16(__uint_as_float(orr[8 * g + 4]) * inv,
-                            __uint_as_float(orr[8 * g + 5]) * inv),
-                  pack_bf16(__uint_as_float(orr[8 * g + 6]) * inv,
-                            __uint_as_float(orr[8 * g + 7]) * inv));
-              *reinterpret_cast<uint4*>(orow + c * 32 + 8 * g) = v;
+          for (int g = 0; g < 4; ++g) {
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              // a set without tiles never wrote its O: leave it out entirely
+              const float va = c0 == 0.f ? 0.f : __uint_as_float(oa[8 * g + e]) * c0;
+              const float vb = c1 == 0.f ? 0.f : __uint_as_float(ob[8 * g + e]) * c1;
+              v[e] = (va + vb) * inv;
             }
+            *reinterpret_cast<uint4*>(orow + c * 32 + 8 * g) =
+                make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
+                           pack_bf16(v[6], v[7]));
           }
         }
       }

@@ -109,7 +109,10 @@ dlo_status launch_rmsnorm_mod(const float* x, int64_t rows, int64_t d,
 // gemm.cu
 // EPI_QKV: columns [0, 2d) stored bf16 like EPI_BF16, columns [2d, 3d)
 // (the V block) stored transposed into vt[b*d + c, t] (row stride vt_ld).
-enum Epilogue { EPI_BF16 = 0, EPI_GELU_BF16 = 1, EPI_RESID_F32 = 2, EPI_QKV = 3 };
+// EPI_PARTIAL (internal): fp32 partial sums of one K slice into ws.
+enum Epilogue {
+  EPI_BF16 = 0, EPI_GELU_BF16 = 1, EPI_RESID_F32 = 2, EPI_QKV = 3, EPI_PARTIAL = 4
+};
 struct EpiArgs {
   void* out;            // bf16 [M, N], or fp32 x [M, N] for the residual
   const float* gate;    // [N], residual epilogue
@@ -117,10 +120,17 @@ struct EpiArgs {
   int64_t vt_ld;        // EPI_QKV: row stride of vt (>= tokens)
   int tokens;           // EPI_QKV: rows per batch item
   int v_col0;           // EPI_QKV: first V column (2d)
+  float* ws;            // split-K workspace [splits, M, N] fp32 (null: no split)
+  size_t ws_bytes;
+  int64_t ws_rows;      // M, set for the partial epilogue
 };
+// K slices a linear of this shape is split into (1: no split; the QKV
+// epilogue never splits) and the fp32 workspace that needs.
+int linear_splits(int64_t M, int64_t N, int64_t K, int epilogue);
+size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int epilogue);
 dlo_status launch_linear(const uint16_t* a, int64_t M, int64_t K,
                          const uint16_t* w, int64_t N, int epilogue, void* out,
-                         const float* gate, cudaStream_t stream);
+                         const float* gate, float* ws, size_t ws_bytes, cudaStream_t stream);
 dlo_status launch_linear_ex(const uint16_t* a, int64_t M, int64_t K, const uint16_t* w,
                             int64_t N, int epilogue, const EpiArgs& ea, cudaStream_t stream);
 

@@ -37,6 +37,7 @@ struct dlo_engine {
     const dlo_plan* plan = nullptr;
     std::vector<const void*> host;   // [g * n_shards + r]
     std::vector<const void*> dev;    // device-accessible addresses (null: DMA only)
+    std::vector<int64_t> pitch;      // [g]: constant host stride between shards, 0 if none
     int64_t bytes = 0;               // bytes one prefetch moves
   };
   struct Hook {
@@ -74,8 +75,9 @@ struct dlo_engine {
   cudaEvent_t fork_ev = nullptr;
   cudaEvent_t join_ev[kMaxFan] = {};
   // AUTO race: timing events on the compute stream at the window edges
-  cudaEvent_t race_ev[4] = {};
-  bool race_rec[4] = {false, false, false, false};
+  // (windows DMA, kernel, DMA, kernel; two events each)
+  cudaEvent_t race_ev[8] = {};
+  bool race_rec[8] = {false, false, false, false, false, false, false, false};
   int32_t chosen = -1;               // DLO_COPY_DMA / DLO_COPY_KERNEL once decided
   double race_dma_us = 0, race_kernel_us = 0;
   int64_t n_prefetches = 0;
@@ -87,15 +89,17 @@ dlo_status preload_kernels();
 namespace {
 
 // AUTO races DMA against the copy kernel on the compute stream's time per
-// forward: prefetches issued by forwards [s, s + W) use DMA, those issued by
-// the next W forwards use the copy kernel, s = race_start(n_blocks).
-// Forward k+1 reads what the prefetch issued at forward k brought in and
-// overlaps the prefetch issued at k+1, so the free-event intervals of
-// forwards s+1 .. s+W-1 see only DMA, and the next W-1 only the kernel.
+// forward.  Four windows of W forwards follow s = race_start(n_blocks):
+// the prefetches issued by the forwards of windows 0 and 2 use DMA, those
+// of windows 1 and 3 the copy kernel.  Forward k+1 reads what the prefetch
+// issued at forward k brought in and overlaps the prefetch issued at k+1,
+// so the free-event intervals inside a window see only that window's mode.
+// Each mode keeps its better window, which discounts a one-off stall.
 // The race starts after one full pass over the blocks plus two forwards,
 // so that one-time costs (module loading, first launches, the first
-// device access to each pinned host page) stay out of both windows.
-constexpr int64_t kRaceWindow = 5;
+// device access to each pinned host page) stay out of every window.
+constexpr int64_t kRaceWindow = 6;
+constexpr int kRaceWindows = 4;
 inline int64_t race_start(int32_t n_blocks) { return static_cast<int64_t>(n_blocks) + 2; }
 
 dlo_status build_segments(const dlo_engine::Block& b, uint8_t* dst, SegmentTable* t) {
@@ -114,6 +118,25 @@ dlo_status build_segments(const dlo_engine::Block& b, uint8_t* dst, SegmentTable
     }
   }
   return DLO_OK;
+}
+
+// A group whose shards sit at a constant host stride (>= the shard bytes)
+// can move as one 2-D DMA: rows = shards, row width = shard bytes, source
+// pitch = the stride, destination pitch = the shard bytes (the gathered
+// layout).  Returns that stride, or 0.
+void compute_pitches(dlo_engine::Block* b) {
+  const dlo_plan* p = b->plan;
+  const int32_t s = p->n_shards;
+  b->pitch.assign(p->groups.size(), 0);
+  for (size_t g = 0; g < p->groups.size(); ++g) {
+    if (s < 2) continue;
+    const char* h0 = static_cast<const char*>(b->host[g * s]);
+    const int64_t stride = static_cast<const char*>(b->host[g * s + 1]) - h0;
+    bool ok = stride >= p->groups[g].shard_bytes;
+    for (int32_t r = 2; ok && r < s; ++r)
+      ok = static_cast<const char*>(b->host[g * s + r]) - h0 == stride * r;
+    if (ok) b->pitch[g] = stride;
+  }
 }
 
 bool all_mapped(const dlo_engine::Block& b) {
@@ -142,10 +165,19 @@ dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, in
   std::vector<Piece> pieces;
   for (size_t g = 0; g < p->groups.size(); ++g) {
     const auto& grp = p->groups[g];
+    if (fan <= 1 && !b.pitch.empty() && b.pitch[g] > 0) {
+      // all shards of the group in one 2-D copy
+      DLO_CUDA(cudaMemcpy2DAsync(dst + grp.base, static_cast<size_t>(grp.shard_bytes),
+                                 b.host[g * s], static_cast<size_t>(b.pitch[g]),
+                                 static_cast<size_t>(grp.shard_bytes), static_cast<size_t>(s),
+                                 cudaMemcpyHostToDevice, stream));
+      continue;
+    }
     for (int32_t r = 0; r < s; ++r)
       pieces.push_back({dst + grp.base + static_cast<int64_t>(r) * grp.shard_bytes,
                         b.host[g * s + r], grp.shard_bytes});
   }
+  if (pieces.empty()) return DLO_OK;
   const int used = static_cast<int>(std::min<size_t>(fan, pieces.size()));
   if (used <= 1) {
     for (const Piece& q : pieces)
@@ -177,13 +209,17 @@ dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, in
 // (non-blocking).
 void try_decide(dlo_engine* e) {
   if (e->chosen >= 0) return;
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 2 * kRaceWindows; ++i)
     if (!e->race_rec[i] || cudaEventQuery(e->race_ev[i]) != cudaSuccess) return;
-  float d = 0, kk = 0;
-  cudaEventElapsedTime(&d, e->race_ev[0], e->race_ev[1]);
-  cudaEventElapsedTime(&kk, e->race_ev[2], e->race_ev[3]);
-  e->race_dma_us = 1e3 * d / (kRaceWindow - 1);
-  e->race_kernel_us = 1e3 * kk / (kRaceWindow - 1);
+  double best[2] = {1e30, 1e30};   // [0] DMA, [1] kernel
+  for (int w = 0; w < kRaceWindows; ++w) {
+    float ms = 0;
+    cudaEventElapsedTime(&ms, e->race_ev[2 * w], e->race_ev[2 * w + 1]);
+    const double us = 1e3 * ms / (kRaceWindow - 1);
+    best[w & 1] = std::min(best[w & 1], us);
+  }
+  e->race_dma_us = best[0];
+  e->race_kernel_us = best[1];
   e->chosen = e->race_kernel_us < e->race_dma_us ? DLO_COPY_KERNEL : DLO_COPY_DMA;
 }
 
@@ -193,7 +229,8 @@ int32_t mode_for(dlo_engine* e, int64_t k, const dlo_engine::Block& b) {
   try_decide(e);
   if (e->chosen >= 0) return e->chosen;
   const int64_t s0 = race_start(e->n_blocks);
-  if (k >= s0 + kRaceWindow && k < s0 + 2 * kRaceWindow) {
+  const int64_t w = k >= s0 ? (k - s0) / kRaceWindow : -1;
+  if (w >= 0 && w < kRaceWindows && (w & 1)) {
     if (!all_mapped(b)) {   // the kernel cannot read this block: no race
       e->chosen = DLO_COPY_DMA;
       return DLO_COPY_DMA;
@@ -257,7 +294,7 @@ void release(dlo_engine* e) {
     cudaEventDestroy(t.a);
     cudaEventDestroy(t.b);
   }
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
     if (e->race_ev[i]) cudaEventDestroy(e->race_ev[i]);
   if (e->fork_ev) cudaEventDestroy(e->fork_ev);
   for (int j = 0; j < dlo_engine::kMaxFan; ++j) {
@@ -309,7 +346,8 @@ dlo_status dlo_engine_create(const dlo_engine_desc* d, dlo_engine** out) {
   for (int s = 0; s < 2; ++s)
     ok = ok && cudaEventCreateWithFlags(&e->ready[s], cudaEventDisableTiming) == cudaSuccess &&
          cudaEventCreateWithFlags(&e->freed[s], cudaEventDisableTiming) == cudaSuccess;
-  for (int i = 0; i < 4; ++i) ok = ok && cudaEventCreate(&e->race_ev[i]) == cudaSuccess;
+  for (int i = 0; i < 2 * kRaceWindows; ++i)
+    ok = ok && cudaEventCreate(&e->race_ev[i]) == cudaSuccess;
   if (e->fan > 1) {
     ok = ok && cudaEventCreateWithFlags(&e->fork_ev, cudaEventDisableTiming) == cudaSuccess;
     for (int j = 0; j < e->fan; ++j)
@@ -359,6 +397,7 @@ dlo_status dlo_register_block(dlo_engine* e, int32_t block, const dlo_plan* plan
     b.dev[i] = a.devicePointer;
   }
   for (const auto& g : plan->groups) b.bytes += g.shard_bytes * plan->n_shards;
+  compute_pitches(&b);
   if (e->mode == DLO_COPY_KERNEL && !all_mapped(b))
     DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block: kernel copies need device-mapped shards");
   e->blocks[block] = std::move(b);
@@ -473,13 +512,15 @@ dlo_status dlo_post_forward(dlo_engine* e, int32_t block) {
     DLO_FAIL(DLO_ERR_STATE, "dlo_post_forward: block %d is not the block in flight", block);
   DLO_CUDA(cudaEventRecord(e->freed[e->cur_slot], e->compute));
   if (e->chosen < 0) {
-    const int64_t s0 = race_start(e->n_blocks), w = kRaceWindow;
-    const int64_t edge[4] = {s0, s0 + w - 1, s0 + w, s0 + 2 * w - 1};
-    for (int i = 0; i < 4; ++i)
-      if (e->k == edge[i]) {
+    const int64_t s0 = race_start(e->n_blocks);
+    for (int w = 0; w < kRaceWindows; ++w) {
+      const int64_t first = s0 + w * kRaceWindow, lastk = first + kRaceWindow - 1;
+      if (e->k == first || e->k == lastk) {
+        const int i = 2 * w + (e->k == lastk ? 1 : 0);
         DLO_CUDA(cudaEventRecord(e->race_ev[i], e->compute));
         e->race_rec[i] = true;
       }
+    }
   }
   e->in_forward = false;
   e->k++;
@@ -613,6 +654,7 @@ dlo_status dlo_reassemble(const dlo_plan* plan, const void* const* shard_ptrs, v
     }
   }
   const int32_t m = mode == DLO_COPY_KERNEL ? DLO_COPY_KERNEL : DLO_COPY_DMA;
+  compute_pitches(&b);
   return copy_block(b, static_cast<uint8_t*>(dst), m, 0, static_cast<cudaStream_t>(stream), 1,
                     nullptr, nullptr, nullptr);
 }

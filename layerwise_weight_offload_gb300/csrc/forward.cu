@@ -10,6 +10,7 @@
 //   rmsnorm_mod -> linear(qkv, bf16) -> attention -> linear(out, gated
 //   residual) -> rmsnorm_mod -> linear(fc1, GELU) -> linear(fc2, gated
 //   residual).
+#include <algorithm>
 #include <mutex>
 #include <utility>
 
@@ -19,12 +20,13 @@ namespace dlo {
 namespace {
 
 struct ScratchLayout {
-  size_t h, qkv, vt, o, u, total;
+  size_t h, qkv, vt, o, u, ws, ws_bytes, total;
   int64_t vt_ld;
 };
 
-// bf16 scratch of one forward: h [M, d] (both norms), qkv [M, 3d] (Q and K
-// used), vt [batch*d, vt_ld] (V transposed), o [M, d], u [M, f].
+// Scratch of one forward: bf16 h [M, d] (both norms), qkv [M, 3d] (Q and K
+// used), vt [batch*d, vt_ld] (V transposed), o [M, d], u [M, f], and the
+// fp32 split-K workspace of the largest split linear (0 if none splits).
 ScratchLayout scratch_layout(const dlo_dit_cfg& c) {
   const size_t M = static_cast<size_t>(c.batch) * c.tokens;
   const size_t d = c.hidden, f = c.mlp;
@@ -36,7 +38,13 @@ ScratchLayout scratch_layout(const dlo_dit_cfg& c) {
   s.vt = r(s.qkv + M * 3 * d * 2);
   s.o = r(s.vt + static_cast<size_t>(c.batch) * d * static_cast<size_t>(s.vt_ld) * 2);
   s.u = r(s.o + M * d * 2);
-  s.total = r(s.u + M * f * 2);
+  s.ws = r(s.u + M * f * 2);
+  const int64_t Mi = static_cast<int64_t>(M), di = c.hidden, fi = c.mlp;
+  size_t w = linear_workspace_bytes(Mi, di, di, EPI_RESID_F32);
+  w = std::max(w, linear_workspace_bytes(Mi, fi, di, EPI_GELU_BF16));
+  w = std::max(w, linear_workspace_bytes(Mi, di, fi, EPI_RESID_F32));
+  s.ws_bytes = w;
+  s.total = r(s.ws + w);
   return s;
 }
 
@@ -92,6 +100,7 @@ dlo_status launch_all(const dlo_dit_cfg* cfg, const dlo_plan* plan, const Scratc
   uint16_t* vt = reinterpret_cast<uint16_t*>(s + sl.vt);
   uint16_t* o = reinterpret_cast<uint16_t*>(s + sl.o);
   uint16_t* u = reinterpret_cast<uint16_t*>(s + sl.u);
+  float* ws = sl.ws_bytes ? reinterpret_cast<float*>(s + sl.ws) : nullptr;
   const int64_t M = static_cast<int64_t>(cfg->batch) * cfg->tokens;
   const int64_t d = cfg->hidden, f = cfg->mlp;
   DLO_TRY(launch_rmsnorm_mod(x, M, d, F(R_G1), F(R_SHIFT1), F(R_SCALE1), cfg->eps, h, stream));
@@ -104,10 +113,12 @@ dlo_status launch_all(const dlo_dit_cfg* cfg, const dlo_plan* plan, const Scratc
   DLO_TRY(launch_linear_ex(h, M, d, H(R_WQKV), 3 * d, EPI_QKV, qa, stream));
   DLO_TRY(launch_attention_vt(qkv, vt, sl.vt_ld, cfg->batch, cfg->tokens, d, cfg->heads, o,
                               stream));
-  DLO_TRY(launch_linear(o, M, d, H(R_WO), d, EPI_RESID_F32, x, F(R_GATE1), stream));
+  DLO_TRY(launch_linear(o, M, d, H(R_WO), d, EPI_RESID_F32, x, F(R_GATE1), ws, sl.ws_bytes,
+                        stream));
   DLO_TRY(launch_rmsnorm_mod(x, M, d, F(R_G2), F(R_SHIFT2), F(R_SCALE2), cfg->eps, h, stream));
-  DLO_TRY(launch_linear(h, M, d, H(R_W1), f, EPI_GELU_BF16, u, nullptr, stream));
-  DLO_TRY(launch_linear(u, M, f, H(R_W2), d, EPI_RESID_F32, x, F(R_GATE2), stream));
+  DLO_TRY(launch_linear(h, M, d, H(R_W1), f, EPI_GELU_BF16, u, nullptr, ws, sl.ws_bytes, stream));
+  DLO_TRY(launch_linear(u, M, f, H(R_W2), d, EPI_RESID_F32, x, F(R_GATE2), ws, sl.ws_bytes,
+                        stream));
   return DLO_OK;
 }
 
@@ -238,10 +249,17 @@ dlo_status dlo_op_rmsnorm_mod(const float* x, int64_t rows, int64_t d, const flo
                                  static_cast<cudaStream_t>(stream));
 }
 
+size_t dlo_op_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t epilogue) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  return dlo::linear_workspace_bytes(M, N, K, epilogue);
+}
+
 dlo_status dlo_op_linear(const uint16_t* a, int64_t M, int64_t K, const uint16_t* w, int64_t N,
-                         int32_t epilogue, void* out, const float* gate, void* stream) {
-  return dlo::launch_linear(a, M, K, w, N, epilogue, out, gate,
-                            static_cast<cudaStream_t>(stream));
+                         int32_t epilogue, void* out, const float* gate, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  DLO_TRY(dlo::preload_kernels());
+  return dlo::launch_linear(a, M, K, w, N, epilogue, out, gate, static_cast<float*>(workspace),
+                            workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 size_t dlo_op_attention_scratch_bytes(int64_t batch, int64_t tokens, int64_t d) {

@@ -27,7 +27,8 @@ dlo_status forward_impl(const dlo_dit_cfg* cfg, const dlo_plan* plan, const void
 namespace {
 
 // 32 MiB: enough for the scratch of, for example, a 1024-token block of
-// hidden size 1024 with a 4096-wide MLP.
+// hidden size 512 with a 2048-wide MLP (dlo_forward_scratch_bytes gives the
+// exact need of a shape).
 constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(32) << 20;
 
 __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];

@@ -50,9 +50,20 @@ __device__ __forceinline__ float gelu_tanh(float z) {
 
 template <int EPI>
 __device__ __forceinline__ void epilogue_store(const uint32_t (&r)[32], int64_t row, int64_t n0,
-                                               int64_t N, const EpiArgs& ea) {
+                                               int64_t N, int ks, const EpiArgs& ea) {
   void* out = ea.out;
   const float* gate = ea.gate;
+  if (EPI == EPI_PARTIAL) {
+    // fp32 partial sum of one K slice: ws[ks][row][n0..n0+31]
+    float* pr = ea.ws + (static_cast<int64_t>(ks) * ea.ws_rows + row) * N + n0;
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+      if (n0 + 4 * g + 4 <= N)
+        *reinterpret_cast<float4*>(pr + 4 * g) =
+            make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                        __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+    return;
+  }
   if (EPI == EPI_QKV && n0 >= ea.v_col0) {
     // V columns: transposed store, vt[b*d + c, t]; the 32 lanes of a warp
     // hold 32 consecutive rows, so each store instruction writes 64
@@ -106,7 +117,7 @@ template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
                     const __grid_constant__ CUtensorMap tma_b, int M, int N, int K,
-                    const EpiArgs ea, int* err) {
+                    int splits, const EpiArgs ea, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -153,6 +164,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
   const int num_n = (N + BN - 1) / BN;
   const int num_tiles = num_m * num_n;
   const int num_k = (K + BK - 1) / BK;
+  // work unit u = (tile, K slice); slice ks covers k-blocks [kb0, kb1)
+  const int num_units = num_tiles * splits;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -160,9 +173,12 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        const int tile = u / splits, ks = u - tile * splits;
+        const int kb0 = static_cast<int>(static_cast<int64_t>(ks) * num_k / splits);
+        const int kb1 = static_cast<int>(static_cast<int64_t>(ks + 1) * num_k / splits);
         const int m_idx = tile % num_m, n_idx = tile / num_m;
-        for (int kb = 0; kb < num_k; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort)) {
             record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_PRODUCER);
             ok = false;
@@ -201,7 +217,10 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        const int ks = u % splits;
+        const int kb0 = static_cast<int>(static_cast<int64_t>(ks) * num_k / splits);
+        const int kb1 = static_cast<int>(static_cast<int64_t>(ks + 1) * num_k / splits);
         if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort)) {
           record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_MMA_EMPTY);
           ok = false;
@@ -209,7 +228,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < num_k; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_bounded(&full[stage], phase, abort)) {
             record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_MMA_FULL);
             ok = false;
@@ -221,7 +240,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             umma_bf16(d_tmem, sdesc_k_sw128(a_addr + kk * 32), sdesc_k_sw128(b_addr + kk * 32),
-                      idesc, (kb | kk) != 0 ? 1u : 0u);
+                      idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
@@ -246,7 +265,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
     const int quad = warp & 3;   // TMEM lane quarter this warp may access
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+      const int tile = u / splits, ks = u - tile * splits;
       const int m_idx = tile % num_m, n_idx = tile / num_m;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tfull[acc], acc_phase, abort))) {
         if (lane == 0) record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_EPILOGUE);
@@ -263,7 +283,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
         tmem_ld_wait();
-        if (row < M) epilogue_store<EPI>(r, row, n0, N, ea);
+        if (row < M) epilogue_store<EPI>(r, row, n0, N, ks, ea);
       }
       tc_fence_before();
       __syncwarp();
@@ -295,23 +315,103 @@ std::once_flag g_attr_once;
 void set_all_attrs() {
   std::call_once(g_attr_once, [] {
     cudaError_t e0 = set_attr<EPI_BF16>(), e1 = set_attr<EPI_GELU_BF16>(),
-                e2 = set_attr<EPI_RESID_F32>(), e3 = set_attr<EPI_QKV>();
-    g_attr_err = e0 != cudaSuccess ? e0 : (e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3));
+                e2 = set_attr<EPI_RESID_F32>(), e3 = set_attr<EPI_QKV>(),
+                e4 = set_attr<EPI_PARTIAL>();
+    const cudaError_t all[5] = {e0, e1, e2, e3, e4};
+    g_attr_err = cudaSuccess;
+    for (cudaError_t e : all)
+      if (e != cudaSuccess) g_attr_err = e;
   });
 }
 
 template <int EPI>
 dlo_status launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int K,
-                      const EpiArgs& ea, int* err, cudaStream_t stream) {
+                      int splits, const EpiArgs& ea, int* err, cudaStream_t stream) {
   set_all_attrs();
   DLO_CUDA(g_attr_err);
-  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const int grid = tiles < sm_count() ? tiles : sm_count();
-  gemm_tcgen05_kernel<EPI><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ma, mb, M, N, K, ea, err);
+  const int units = ((M + BM - 1) / BM) * ((N + BN - 1) / BN) * splits;
+  const int grid = units < sm_count() ? units : sm_count();
+  gemm_tcgen05_kernel<EPI><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ma, mb, M, N, K, splits, ea,
+                                                                      err);
   DLO_CUDA(cudaGetLastError());
   return DLO_OK;
 }
 
+// Sums the K slices of a split linear in slice order and applies the
+// final epilogue (bf16 store, GELU-tanh, or gated residual).
+template <int EPI>
+__global__ void __launch_bounds__(256)
+splitk_reduce_kernel(const float* __restrict__ ws, int splits, int64_t M, int64_t N,
+                     const EpiArgs ea) {
+  const int64_t n4 = N / 4, total = M * n4;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = i / n4, c = (i - row * n4) * 4;
+    float4 acc = *reinterpret_cast<const float4*>(ws + row * N + c);
+    for (int s = 1; s < splits; ++s) {
+      const float4 v = *reinterpret_cast<const float4*>(ws + (s * M + row) * N + c);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    if (EPI == EPI_RESID_F32) {
+      float4* xp = reinterpret_cast<float4*>(static_cast<float*>(ea.out) + row * N + c);
+      const float4 gv = __ldg(reinterpret_cast<const float4*>(ea.gate + c));
+      float4 xv = *xp;
+      xv.x += gv.x * acc.x;
+      xv.y += gv.y * acc.y;
+      xv.z += gv.z * acc.z;
+      xv.w += gv.w * acc.w;
+      *xp = xv;
+    } else {
+      if (EPI == EPI_GELU_BF16) {
+        acc.x = gelu_tanh(acc.x);
+        acc.y = gelu_tanh(acc.y);
+        acc.z = gelu_tanh(acc.z);
+        acc.w = gelu_tanh(acc.w);
+      }
+      __nv_bfloat162 p0 = __floats2bfloat162_rn(acc.x, acc.y);
+      __nv_bfloat162 p1 = __floats2bfloat162_rn(acc.z, acc.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&p0);
+      pk.y = *reinterpret_cast<uint32_t*>(&p1);
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(ea.out) + row * N + c) = pk;
+    }
+  }
+}
+
+template <int EPI>
+dlo_status launch_reduce(const float* ws, int splits, int64_t M, int64_t N, const EpiArgs& ea,
+                         cudaStream_t stream) {
+  const int64_t total = M * (N / 4);
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  splitk_reduce_kernel<EPI><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ws, splits, M, N,
+                                                                               ea);
+  DLO_CUDA(cudaGetLastError());
+  return DLO_OK;
+}
+
+}  // namespace
+
+int linear_splits(int64_t M, int64_t N, int64_t K, int epilogue) {
+  if (epilogue == EPI_QKV) return 1;
+  const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int64_t num_k = (K + BK - 1) / BK;
+  int64_t s = sm_count() / (tiles > 0 ? tiles : 1);
+  if (s > num_k / 4) s = num_k / 4;      // every slice keeps at least 4 k-blocks
+  if (s > 8) s = 8;
+  return s < 2 ? 1 : static_cast<int>(s);
+}
+
+size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int epilogue) {
+  const int s = linear_splits(M, N, K, epilogue);
+  return s > 1 ? static_cast<size_t>(s) * M * N * 4 : 0;
+}
+
+namespace {
 }  // namespace
 
 dlo_status gemm_preload() {
@@ -347,21 +447,40 @@ dlo_status launch_linear_ex(const uint16_t* a, int64_t M, int64_t K, const uint1
   DLO_TRY(make_tmap_2d(&ma, a, M, K, K, BM, BK));
   DLO_TRY(make_tmap_2d(&mb, w, N, K, K, BN, BK));
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  const int splits = linear_splits(M, N, K, epilogue);
+  const size_t ws_need = splits > 1 ? static_cast<size_t>(splits) * M * N * 4 : 0;
+  if (splits > 1 && ea.ws && ea.ws_bytes >= ws_need &&
+      !(reinterpret_cast<uintptr_t>(ea.ws) & 15u)) {
+    // K split across CTAs: fp32 partials, then an ordered reduction with
+    // the epilogue (deterministic: the slice order is fixed)
+    EpiArgs pa = ea;
+    pa.ws_rows = M;
+    DLO_TRY(launch_epi<EPI_PARTIAL>(ma, mb, m, n, k, splits, pa, err, stream));
+    switch (epilogue) {
+      case EPI_BF16: return launch_reduce<EPI_BF16>(ea.ws, splits, M, N, ea, stream);
+      case EPI_GELU_BF16: return launch_reduce<EPI_GELU_BF16>(ea.ws, splits, M, N, ea, stream);
+      case EPI_RESID_F32: return launch_reduce<EPI_RESID_F32>(ea.ws, splits, M, N, ea, stream);
+      default: DLO_FAIL(DLO_ERR_INVALID, "linear: unknown epilogue %d", epilogue);
+    }
+  }
   switch (epilogue) {
-    case EPI_BF16: return launch_epi<EPI_BF16>(ma, mb, m, n, k, ea, err, stream);
-    case EPI_GELU_BF16: return launch_epi<EPI_GELU_BF16>(ma, mb, m, n, k, ea, err, stream);
-    case EPI_RESID_F32: return launch_epi<EPI_RESID_F32>(ma, mb, m, n, k, ea, err, stream);
-    case EPI_QKV: return launch_epi<EPI_QKV>(ma, mb, m, n, k, ea, err, stream);
+    case EPI_BF16: return launch_epi<EPI_BF16>(ma, mb, m, n, k, 1, ea, err, stream);
+    case EPI_GELU_BF16: return launch_epi<EPI_GELU_BF16>(ma, mb, m, n, k, 1, ea, err, stream);
+    case EPI_RESID_F32: return launch_epi<EPI_RESID_F32>(ma, mb, m, n, k, 1, ea, err, stream);
+    case EPI_QKV: return launch_epi<EPI_QKV>(ma, mb, m, n, k, 1, ea, err, stream);
     default: DLO_FAIL(DLO_ERR_INVALID, "linear: unknown epilogue %d", epilogue);
   }
 }
 
 dlo_status launch_linear(const uint16_t* a, int64_t M, int64_t K, const uint16_t* w, int64_t N,
-                         int epilogue, void* out, const float* gate, cudaStream_t stream) {
+                         int epilogue, void* out, const float* gate, float* ws, size_t ws_bytes,
+                         cudaStream_t stream) {
   if (epilogue == EPI_QKV) DLO_FAIL(DLO_ERR_INVALID, "linear: the QKV epilogue is internal");
   EpiArgs ea{};
   ea.out = out;
   ea.gate = gate;
+  ea.ws = ws;
+  ea.ws_bytes = ws_bytes;
   return launch_linear_ex(a, M, K, w, N, epilogue, ea, stream);
 }
 

@@ -86,7 +86,9 @@ _SIGS = {
     "dlo_forward": (c_i32, [_P(DitCfg), c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "dlo_forward_noalloc": (c_i32, [_P(DitCfg), c_vp, c_vp, c_vp, c_vp]),
     "dlo_op_rmsnorm_mod": (c_i32, [c_vp, c_i64, c_i64, c_vp, c_vp, c_vp, c_f32, c_vp, c_vp]),
-    "dlo_op_linear": (c_i32, [c_vp, c_i64, c_i64, c_vp, c_i64, c_i32, c_vp, c_vp, c_vp]),
+    "dlo_op_linear_workspace_bytes": (c_sz, [c_i64, c_i64, c_i64, c_i32]),
+    "dlo_op_linear": (c_i32, [c_vp, c_i64, c_i64, c_vp, c_i64, c_i32, c_vp, c_vp, c_vp, c_sz,
+                              c_vp]),
     "dlo_op_attention_scratch_bytes": (c_sz, [c_i64, c_i64, c_i64]),
     "dlo_op_attention": (c_i32, [c_vp, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp, c_sz, c_vp]),
     "dlo_engine_create": (c_i32, [_P(EngineDesc), _P(c_vp)]),
@@ -265,9 +267,15 @@ def op_rmsnorm_mod(x, rows, d, g, shift, scale, eps, h, stream=None):
                                     float(eps), _ptr(h), _stream(stream)), "dlo_op_rmsnorm_mod")
 
 
-def op_linear(a, M, K, w, N, epilogue, out, gate=None, stream=None):
+def op_linear_workspace_bytes(M, N, K, epilogue):
+    return int(lib().dlo_op_linear_workspace_bytes(M, N, K, int(epilogue)))
+
+
+def op_linear(a, M, K, w, N, epilogue, out, gate=None, stream=None, workspace=None,
+              workspace_bytes=0):
     _check(lib().dlo_op_linear(_ptr(a), M, K, _ptr(w), N, int(epilogue), _ptr(out), _ptr(gate),
-                               _stream(stream)), "dlo_op_linear")
+                               _ptr(workspace), int(workspace_bytes), _stream(stream)),
+           "dlo_op_linear")
 
 
 def op_attention_scratch_bytes(batch, tokens, d):

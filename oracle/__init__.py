@@ -43,6 +43,9 @@ def lib():
         L.oracle_attention.argtypes = [vp, i64, i64, i64, i64, vp, i32]
         L.oracle_block_forward.restype = None
         L.oracle_block_forward.argtypes = [vp, i64, i64, i64, i64, i64, dbl, vp, vp, i32]
+        L.oracle_block_forward_rows.restype = None
+        L.oracle_block_forward_rows.argtypes = [vp, i64, i64, i64, i64, i64, dbl, vp, vp, i64,
+                                                vp, i32]
         _lib = L
     return _lib
 
@@ -188,4 +191,16 @@ def block_forward(x, params, batch, tokens, d, heads, f, eps=1e-6, threads=None)
     out = np.zeros((batch * tokens, d), dtype=np.float64)
     lib().oracle_block_forward(_ptr(x), batch, tokens, d, heads, f, eps,
                                _ptr_array(arrs), _ptr(out), threads or default_threads())
+    return out
+
+
+def block_forward_rows(x, params, rows, batch, tokens, d, heads, f, eps=1e-6, threads=None):
+    """Block output for the listed query rows only (K and V from all tokens)."""
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(batch * tokens, d)
+    arrs = [np.ascontiguousarray(params[n], dtype=np.float32) for n in PARAM_ORDER]
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.zeros((len(rows), d), dtype=np.float64)
+    lib().oracle_block_forward_rows(_ptr(x), batch, tokens, d, heads, f, eps, _ptr_array(arrs),
+                                    _ptr(rows), len(rows), _ptr(out),
+                                    threads or default_threads())
     return out

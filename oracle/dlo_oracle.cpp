@@ -324,4 +324,67 @@ void oracle_block_forward(const float* x_in, int64_t batch, int64_t tokens,
   std::memcpy(x_out, x.data(), sizeof(double) * M * d);
 }
 
+
+// The same block forward, evaluated only for the query rows listed in
+// `rows` (indices into [0, batch*tokens)): every token still contributes
+// its K and V to attention, but the out-projection, the residuals and the
+// MLP run for the listed rows only.  For a listed row each value is formed
+// by exactly the operations, in the same order, as oracle_block_forward.
+// Output: x_out[i, :] is the block output of row rows[i].
+void oracle_block_forward_rows(const float* x_in, int64_t batch, int64_t tokens, int64_t d,
+                               int64_t heads, int64_t f, double eps, const float* const* p,
+                               const int64_t* rows, int64_t n_rows, double* x_out,
+                               int32_t threads) {
+  const int64_t M = batch * tokens;
+  const int64_t hd = d / heads;
+  const double scale = 1.0 / std::sqrt(static_cast<double>(hd));
+  std::vector<double> x(M * d), h(M * d), kv(M * 2 * d);
+  for (int64_t e = 0; e < M * d; ++e) x[e] = static_cast<double>(x_in[e]);
+  oracle_rmsnorm_mod(x.data(), M, d, p[0], p[1], p[2], eps, h.data());
+  // K and V of every token: rows d..3d of Wqkv
+  oracle_linear(h.data(), M, d, p[4] + d * d, 2 * d, kv.data(), threads);
+  std::vector<double> xs(n_rows * d), hs(n_rows * d), q(n_rows * d), o(n_rows * d),
+      y(n_rows * d), u(n_rows * f);
+  for (int64_t i = 0; i < n_rows; ++i)
+    for (int64_t c = 0; c < d; ++c) {
+      xs[i * d + c] = x[rows[i] * d + c];
+      hs[i * d + c] = h[rows[i] * d + c];
+    }
+  oracle_linear(hs.data(), n_rows, d, p[4], d, q.data(), threads);   // Q rows 0..d
+  run_rows(n_rows * heads, threads, [&](int64_t lo, int64_t hi) {
+    std::vector<double> s(tokens);
+    for (int64_t job = lo; job < hi; ++job) {
+      const int64_t i = job / heads, j = job % heads;
+      const int64_t b = rows[i] / tokens;
+      const double* qr = q.data() + i * d + j * hd;
+      double m = -INFINITY;
+      for (int64_t t = 0; t < tokens; ++t) {
+        const double* kk = kv.data() + (b * tokens + t) * 2 * d + j * hd;
+        double dot = 0.0;
+        for (int64_t c = 0; c < hd; ++c) dot += qr[c] * kk[c];
+        s[t] = dot * scale;
+        m = std::max(m, s[t]);
+      }
+      double denom = 0.0;
+      for (int64_t t = 0; t < tokens; ++t) { s[t] = std::exp(s[t] - m); denom += s[t]; }
+      for (int64_t c = 0; c < hd; ++c) {
+        double acc = 0.0;
+        for (int64_t t = 0; t < tokens; ++t)
+          acc += s[t] * kv[(b * tokens + t) * 2 * d + d + j * hd + c];
+        o[i * d + j * hd + c] = acc / denom;
+      }
+    }
+  });
+  oracle_linear(o.data(), n_rows, d, p[5], d, y.data(), threads);
+  for (int64_t i = 0; i < n_rows; ++i)
+    for (int64_t c = 0; c < d; ++c) xs[i * d + c] += static_cast<double>(p[3][c]) * y[i * d + c];
+  oracle_rmsnorm_mod(xs.data(), n_rows, d, p[6], p[7], p[8], eps, hs.data());
+  oracle_linear(hs.data(), n_rows, d, p[10], f, u.data(), threads);
+  for (int64_t e = 0; e < n_rows * f; ++e) u[e] = oracle_gelu_tanh(u[e]);
+  oracle_linear(u.data(), n_rows, f, p[11], d, y.data(), threads);
+  for (int64_t i = 0; i < n_rows; ++i)
+    for (int64_t c = 0; c < d; ++c) xs[i * d + c] += static_cast<double>(p[9][c]) * y[i * d + c];
+  std::memcpy(x_out, xs.data(), sizeof(double) * n_rows * d);
+}
+
 }  // extern "C"

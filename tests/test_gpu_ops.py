@@ -50,23 +50,29 @@ LIN_SHAPES = [
     (200, 320, 264),     # ragged M, N (vs 256) and K (vs 64)
     (1, 64, 8),          # degenerate
     (1000, 1024, 1024),
-    (77, 4096, 1024),    # long K
+    (77, 4096, 1024),    # long K: splits 8 ways when a workspace is given
+    (1024, 4096, 1024),  # the odd workload's fc2 shape
 ]
 
 
+@pytest.mark.parametrize("split", [False, True])
 @pytest.mark.parametrize("M,K,N", LIN_SHAPES)
 @pytest.mark.parametrize("epi", [dlo.EPI_BF16, dlo.EPI_GELU_BF16, dlo.EPI_RESID_F32])
-def test_linear(M, K, N, epi):
+def test_linear(M, K, N, epi, split):
     r = _gen(M * 131 + K * 7 + N + epi)
     a = r(M, K).to(torch.bfloat16)
     w = r(N, K, std=0.05).to(torch.bfloat16)
     ad, wd = a.cuda(), w.cuda()
+    nws = dlo.op_linear_workspace_bytes(M, N, K, epi) if split else 0
+    if split and nws == 0:
+        pytest.skip("this shape does not split")
+    ws = torch.full((max(nws, 16) // 4,), float("nan"), device="cuda") if split else None
     ref = oracle.linear(a.float().numpy(), w.float().numpy())
     if epi == dlo.EPI_RESID_F32:
         x = r(M, N)
         gate = r(N, std=0.1)
         xd, gd = x.cuda(), gate.cuda()
-        dlo.op_linear(ad, M, K, wd, N, epi, xd, gd)
+        dlo.op_linear(ad, M, K, wd, N, epi, xd, gd, None, ws, nws)
         _status_clean()
         got = xd.cpu().numpy()
         exp = x.numpy().astype(np.float64) + gate.numpy().astype(np.float64) * ref
@@ -76,7 +82,7 @@ def test_linear(M, K, N, epi):
         assert_oracle_close(delta_got, exp - x.numpy(), "resid delta", 1e-3, 1e-4)
     else:
         out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-        dlo.op_linear(ad, M, K, wd, N, epi, out)
+        dlo.op_linear(ad, M, K, wd, N, epi, out, None, None, ws, nws)
         _status_clean()
         got = out.float().cpu().numpy()
         if epi == dlo.EPI_GELU_BF16:

@@ -371,3 +371,15 @@ def test_block_token_permutation_equivariance_and_batch():
     yp = oracle.block_forward(xp, p, 2, t, d, 4, f)
     assert np.allclose(yp[:t], y[:t][perm], atol=1e-12)
     assert np.allclose(yp[t:], y[t:], atol=0)
+
+
+def test_block_rows_equals_full_block_on_listed_rows():
+    # the sampled-rows form must reproduce the full forward's rows exactly
+    rng = np.random.default_rng(12)
+    d, f, t = 16, 64, 9
+    p = _params(rng, d, f)
+    x = rng.standard_normal((2 * t, d)).astype(np.float32)
+    full = oracle.block_forward(x, p, 2, t, d, 4, f, threads=3)
+    rows = [0, 5, 8, 9, 17]
+    part = oracle.block_forward_rows(x, p, rows, 2, t, d, 4, f, threads=3)
+    assert np.array_equal(part, full[rows])
