@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--pretouch", type=int, default=1,
+                    help="1: read every pinned host block once from the GPU before timing")
     ap.add_argument("--only", default=None,
                     choices=["linear", "attention", "norm", "copy", "forward"],
                     help="run one kernel of the workload's block `--reps` times (for ncu)")
@@ -239,6 +241,12 @@ def run_ours(args, ws, rank, local):
     gen_dev = args.gen_device or ("cuda" if w.distinct * w.bf16_numel() > 2e9 else "cpu")
     host = HostBlocks(w, seed=args.seed, gen_device=gen_dev)
     bytes_per_block = sum(g.shard_bytes * w.shards for g in host.plan.groups())
+    pretouch_s = None
+    if args.pretouch:
+        # setup, untimed: one device-side pass over every pinned host block
+        t0 = time.perf_counter()
+        host.pretouch()
+        pretouch_s = time.perf_counter() - t0
     st = StreamedStack(host, copy_mode=mode, copy_ctas=args.copy_ctas, timing=True)
     x0 = W.gen_x(w, args.seed, device="cuda")
     x = x0.clone()
@@ -276,6 +284,9 @@ def run_ours(args, ws, rank, local):
     copy_ms, copy_bytes = copy_ms[:n_fwd], copy_bytes[:n_fwd]
     busy_ms = sum(copy_ms)
     h2d = sum(copy_bytes) / (busy_ms * 1e6) if busy_ms > 0 else None
+    qs = sorted(copy_ms)
+    copy_dist = {"min": qs[0], "median": qs[len(qs) // 2], "max": qs[-1],
+                 "first": copy_ms[:3], "last": copy_ms[-3:]} if qs else None
     value = ws * n_fwd / (ms / 1e3)
     ms_step = ms / args.steps
     chosen = dlo.COPY_MODE_NAMES[stats1.chosen_mode]
@@ -385,6 +396,8 @@ def run_ours(args, ws, rank, local):
                            "t_link_ms": t_link * 1e3, "t_compute_ms": t_comp * 1e3,
                            "bound": "h2d" if t_link >= t_comp else "tensor"},
         "auto_race_us_per_forward": {"dma": stats1.race_dma_us, "kernel": stats1.race_kernel_us},
+        "copy_ms_distribution": copy_dist, "pretouch_s": pretouch_s,
+        "host_huge_page_fraction": host.buf.huge_fraction(),
         "roofline": {"name": copy_name, "bound": "h2d", "achieved": achieved,
                      "peak": ceiling, "unit": "GB/s",
                      "frac": achieved / ceiling if achieved else None, "traffic": None,

@@ -4,6 +4,9 @@ two-slot engine, and an all-resident reference over the same kernels.
 PyTorch provides device memory, pinned host memory and streams only; every
 step of the method runs in the library (``dlo``).
 """
+import ctypes
+import mmap
+
 import torch
 
 from . import dlo
@@ -14,19 +17,50 @@ def _round_up(v, a):
     return (v + a - 1) // a * a
 
 
-class PinnedBuffer:
-    """Page-locked, device-mapped host bytes of an exact size.
+_MADV_COLLAPSE = 25
 
-    Allocated as ordinary host memory and registered with the CUDA driver
-    (cudaHostRegister, portable | mapped), so the size is not rounded the way
-    a caching pinned allocator rounds it."""
+
+def _collapse(ptr, nbytes):
+    """Asks the kernel to back [ptr, ptr+nbytes) with huge pages now
+    (MADV_COLLAPSE, Linux 6.1+); ignored where unsupported."""
+    try:
+        libc = ctypes.CDLL(None, use_errno=True)
+        libc.madvise.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int]
+        libc.madvise(ctypes.c_void_p(ptr), ctypes.c_size_t(nbytes), _MADV_COLLAPSE)
+    except (OSError, AttributeError):
+        pass
+
+
+class PinnedBuffer:
+    """Page-locked, device-mapped host bytes of an exact size, backed by
+    transparent huge pages.
+
+    The bytes come from an anonymous mapping aligned to 512 MiB and marked
+    MADV_HUGEPAGE, touched once, then registered with the CUDA driver
+    (cudaHostRegister, portable | mapped).  On the GB300 (NVLink-C2C, 64 KiB
+    base pages) the GPU's sustained host->device rate from pinned memory
+    built of small pages falls far below the link rate once the footprint
+    is several GB (address translations no longer fit the GPU's caches);
+    from huge-page memory it stays at the link rate.  Unlike a caching
+    pinned allocator, the size is not rounded to a power of two."""
+
+    ALIGN = 512 << 20
 
     def __init__(self, nbytes):
         self.nbytes = int(nbytes)
-        self._t = torch.empty(self.nbytes + 4096, dtype=torch.uint8)
-        base = self._t.data_ptr()
-        self.ptr = _round_up(base, 4096)
+        size = self.nbytes + self.ALIGN
+        self._map = mmap.mmap(-1, size, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+        try:
+            self._map.madvise(mmap.MADV_HUGEPAGE)
+        except (AttributeError, OSError, ValueError):
+            pass
+        self._cbuf = (ctypes.c_uint8 * size).from_buffer(self._map)
+        base = ctypes.addressof(self._cbuf)
+        self.ptr = _round_up(base, self.ALIGN)
         self.offset = self.ptr - base
+        ctypes.memset(self.ptr, 0, self.nbytes)       # first touch: huge pages
+        _collapse(self.ptr, self.nbytes)
+        self._t = torch.frombuffer(self._map, dtype=torch.uint8)
         rt = torch.cuda.cudart()
         err = rt.cudaHostRegister(self.ptr, self.nbytes, 1 | 2)   # portable | mapped
         code = err.value if hasattr(err, "value") else int(err)
@@ -37,10 +71,40 @@ class PinnedBuffer:
     def view(self, offset, nbytes):
         return self._t[self.offset + offset:self.offset + offset + nbytes]
 
+    def huge_fraction(self):
+        """Fraction of the buffer's resident bytes backed by huge pages
+        (from /proc/self/smaps), or None where that is not readable."""
+        try:
+            with open("/proc/self/smaps") as fh:
+                lines = fh.read().splitlines()
+        except OSError:
+            return None
+        lo, hi = self.ptr, self.ptr + self.nbytes
+        rss = huge = 0
+        inside = False
+        for line in lines:
+            head = line.split(" ", 1)[0]
+            if "-" in head and ":" not in head:
+                a, b = (int(v, 16) for v in head.split("-"))
+                inside = a < hi and b > lo
+            elif inside and line.startswith("Rss:"):
+                rss += int(line.split()[1])
+            elif inside and line.startswith("AnonHugePages:"):
+                huge += int(line.split()[1])
+        return huge / rss if rss else None
+
     def close(self):
         if self.registered:
             torch.cuda.cudart().cudaHostUnregister(self.ptr)
             self.registered = False
+        if self._map is not None:
+            self._t = None
+            self._cbuf = None
+            try:
+                self._map.close()
+            except BufferError:
+                pass            # a view still exports the buffer; freed with it
+            self._map = None
 
     def __del__(self):
         try:
@@ -77,6 +141,18 @@ class HostBlocks:
             if keep_params:
                 self.params.append(p)
             del p
+
+    def pretouch(self, stream=None):
+        """Reads every host block once from the GPU (a copy-kernel pass, then
+        a DMA pass, into a scratch slot) so that first-access costs of the
+        pinned pages are paid at setup rather than in the first forwards."""
+        dst = torch.empty(self.plan.info().slot_bytes, dtype=torch.uint8, device="cuda")
+        s = stream or torch.cuda.Stream()
+        for mode in (dlo.COPY_KERNEL, dlo.COPY_DMA):
+            for hb in range(self.w.distinct):
+                dlo.reassemble(self.plan, self.shard_ptrs(hb), dst, mode, s)
+        s.synchronize()
+        del dst
 
     def shard_ptrs(self, hb):
         base = self.buf.ptr + hb * self.block_bytes
