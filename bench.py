@@ -52,6 +52,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true",
+                    help="do not sample nvidia-smi during the timed region (diagnostics)")
+    ap.add_argument("--dump-copies", action="store_true",
+                    help="add every timed prefetch's duration to the JSON line")
     ap.add_argument("--pretouch", type=int, default=1,
                     help="1: read every pinned host block once from the GPU before timing")
     ap.add_argument("--only", default=None,
@@ -265,7 +269,8 @@ def run_ours(args, ws, rank, local):
     barrier(ws)
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
-    clocks.start()
+    if not args.no_clocks:
+        clocks.start()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(st.compute)
     for _ in range(args.steps):
@@ -398,6 +403,8 @@ def run_ours(args, ws, rank, local):
         "auto_race_us_per_forward": {"dma": stats1.race_dma_us, "kernel": stats1.race_kernel_us},
         "copy_ms_distribution": copy_dist, "pretouch_s": pretouch_s,
         "host_huge_page_fraction": host.buf.huge_fraction(),
+        "host_huge_ranges_used_fraction": host.buf.good_fraction(),
+        "copy_ms_all": copy_ms if args.dump_copies else None,
         "roofline": {"name": copy_name, "bound": "h2d", "achieved": achieved,
                      "peak": ceiling, "unit": "GB/s",
                      "frac": achieved / ceiling if achieved else None, "traffic": None,

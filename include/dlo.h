@@ -64,7 +64,10 @@ typedef enum { DLO_BF16 = 0, DLO_F32 = 1 } dlo_dtype;
  *           when the group's host shards sit at a constant stride (rows =
  *           shards, destination pitch = shard bytes, i.e. the gathered
  *           layout), else one cudaMemcpyAsync per shard, each straight to
- *           the shard's final offset in the slot.
+ *           the shard's final offset in the slot.  In the engine, a group
+ *           under 1 MiB (when the block has another, larger group and its
+ *           shards are device-mapped) moves by a one-CTA copy-kernel launch
+ *           on a library-owned side stream while the DMA runs.
  *   KERNEL: one launch of a copy-and-reassemble kernel that reads the mapped
  *           pinned host shards with 16-byte loads and writes them to their
  *           final slot offsets (SMs read over the host link).

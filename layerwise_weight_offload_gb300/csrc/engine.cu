@@ -74,6 +74,10 @@ struct dlo_engine {
   cudaStream_t aux[kMaxFan] = {};
   cudaEvent_t fork_ev = nullptr;
   cudaEvent_t join_ev[kMaxFan] = {};
+  // DMA mode: dtype groups smaller than kSmallGroupBytes move by a one-CTA
+  // copy-kernel launch on this side stream, concurrent with the large DMA
+  cudaStream_t side = nullptr;
+  cudaEvent_t side_fork = nullptr, side_join = nullptr;
   // AUTO race: timing events on the compute stream at the window edges
   // (windows DMA, kernel, DMA, kernel; two events each)
   cudaEvent_t race_ev[8] = {};
@@ -149,9 +153,15 @@ bool all_mapped(const dlo_engine::Block& b) {
 // cudaMemcpyAsync per (group, shard) to its final slot offset, dealt to up
 // to `fan` streams (largest first, each to the least-loaded stream) that
 // fork from `stream` and join back into it.
+// Small groups (the f32 norm/adaLN vectors: a few tens of KB) pay more for
+// a DMA's setup than for their bytes; they go by copy kernel on a side
+// stream while the large group's DMA runs.
+constexpr int64_t kSmallGroupBytes = 1 << 20;
+
 dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, int ctas,
                       cudaStream_t stream, int fan, cudaStream_t* aux, cudaEvent_t fork_ev,
-                      cudaEvent_t* join_ev) {
+                      cudaEvent_t* join_ev, cudaStream_t side = nullptr,
+                      cudaEvent_t side_fork = nullptr, cudaEvent_t side_join = nullptr) {
   const dlo_plan* p = b.plan;
   const int32_t s = p->n_shards;
   if (mode == DLO_COPY_KERNEL) {
@@ -161,10 +171,34 @@ dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, in
     DLO_TRY(build_segments(b, dst, &t));
     return launch_copy_reassemble(t, ctas, stream);
   }
+  std::vector<char> by_kernel(p->groups.size(), 0);
+  if (side && all_mapped(b) && p->groups.size() > 1) {
+    SegmentTable t;
+    t.n = 0;
+    for (size_t g = 0; g < p->groups.size(); ++g) {
+      const auto& grp = p->groups[g];
+      if (grp.shard_bytes * s >= kSmallGroupBytes || t.n + s > kMaxSegments) continue;
+      by_kernel[g] = 1;
+      for (int32_t r = 0; r < s; ++r) {
+        Segment& sg = t.seg[t.n++];
+        sg.src = b.dev[g * s + r];
+        sg.dst = dst + grp.base + static_cast<int64_t>(r) * grp.shard_bytes;
+        sg.bytes = grp.shard_bytes;
+      }
+    }
+    if (t.n > 0) {
+      DLO_CUDA(cudaEventRecord(side_fork, stream));
+      DLO_CUDA(cudaStreamWaitEvent(side, side_fork, 0));
+      DLO_TRY(launch_copy_reassemble(t, 1, side));
+      DLO_CUDA(cudaEventRecord(side_join, side));
+    }
+  }
   struct Piece { uint8_t* dst; const void* src; int64_t bytes; };
   std::vector<Piece> pieces;
+  bool joined = false;
   for (size_t g = 0; g < p->groups.size(); ++g) {
     const auto& grp = p->groups[g];
+    if (by_kernel[g]) continue;
     if (fan <= 1 && !b.pitch.empty() && b.pitch[g] > 0) {
       // all shards of the group in one 2-D copy
       DLO_CUDA(cudaMemcpy2DAsync(dst + grp.base, static_cast<size_t>(grp.shard_bytes),
@@ -177,13 +211,22 @@ dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, in
       pieces.push_back({dst + grp.base + static_cast<int64_t>(r) * grp.shard_bytes,
                         b.host[g * s + r], grp.shard_bytes});
   }
-  if (pieces.empty()) return DLO_OK;
+  auto join_side = [&]() -> dlo_status {
+    for (size_t g = 0; g < by_kernel.size(); ++g)
+      if (by_kernel[g]) {
+        DLO_CUDA(cudaStreamWaitEvent(stream, side_join, 0));
+        break;
+      }
+    return DLO_OK;
+  };
+  (void)joined;
+  if (pieces.empty()) return join_side();
   const int used = static_cast<int>(std::min<size_t>(fan, pieces.size()));
   if (used <= 1) {
     for (const Piece& q : pieces)
       DLO_CUDA(cudaMemcpyAsync(q.dst, q.src, static_cast<size_t>(q.bytes),
                                cudaMemcpyHostToDevice, stream));
-    return DLO_OK;
+    return join_side();
   }
   std::stable_sort(pieces.begin(), pieces.end(),
                    [](const Piece& a, const Piece& c) { return a.bytes > c.bytes; });
@@ -202,7 +245,7 @@ dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, in
     DLO_CUDA(cudaEventRecord(join_ev[j], aux[j]));
     DLO_CUDA(cudaStreamWaitEvent(stream, join_ev[j], 0));
   }
-  return DLO_OK;
+  return join_side();
 }
 
 // AUTO: decide once the four window-edge events have completed
@@ -265,7 +308,7 @@ dlo_status enqueue_prefetch(dlo_engine* e, int32_t block, int32_t slot, int64_t 
     DLO_CUDA(cudaEventRecord(t.a, e->copy));
   }
   DLO_TRY(copy_block(b, e->slot[slot], mode, e->copy_ctas, e->copy, e->fan, e->aux, e->fork_ev,
-                     e->join_ev));
+                     e->join_ev, e->side, e->side_fork, e->side_join));
   if (e->timing) DLO_CUDA(cudaEventRecord(t.b, e->copy));
   DLO_CUDA(cudaEventRecord(e->ready[slot], e->copy));
   e->slot_holds[slot] = block;
@@ -297,6 +340,9 @@ void release(dlo_engine* e) {
   for (int i = 0; i < 8; ++i)
     if (e->race_ev[i]) cudaEventDestroy(e->race_ev[i]);
   if (e->fork_ev) cudaEventDestroy(e->fork_ev);
+  if (e->side_fork) cudaEventDestroy(e->side_fork);
+  if (e->side_join) cudaEventDestroy(e->side_join);
+  if (e->side) cudaStreamDestroy(e->side);
   for (int j = 0; j < dlo_engine::kMaxFan; ++j) {
     if (e->join_ev[j]) cudaEventDestroy(e->join_ev[j]);
     if (e->aux[j]) cudaStreamDestroy(e->aux[j]);
@@ -348,6 +394,9 @@ dlo_status dlo_engine_create(const dlo_engine_desc* d, dlo_engine** out) {
          cudaEventCreateWithFlags(&e->freed[s], cudaEventDisableTiming) == cudaSuccess;
   for (int i = 0; i < 2 * kRaceWindows; ++i)
     ok = ok && cudaEventCreate(&e->race_ev[i]) == cudaSuccess;
+  ok = ok && cudaStreamCreateWithFlags(&e->side, cudaStreamNonBlocking) == cudaSuccess &&
+       cudaEventCreateWithFlags(&e->side_fork, cudaEventDisableTiming) == cudaSuccess &&
+       cudaEventCreateWithFlags(&e->side_join, cudaEventDisableTiming) == cudaSuccess;
   if (e->fan > 1) {
     ok = ok && cudaEventCreateWithFlags(&e->fork_ev, cudaEventDisableTiming) == cudaSuccess;
     for (int j = 0; j < e->fan; ++j)

@@ -18,68 +18,173 @@ def _round_up(v, a):
 
 
 _MADV_COLLAPSE = 25
+_HUGE = 512 << 20        # PMD size of a 64 KiB-page kernel; also a multiple of 2 MiB
 
 
 def _collapse(ptr, nbytes):
     """Asks the kernel to back [ptr, ptr+nbytes) with huge pages now
-    (MADV_COLLAPSE, Linux 6.1+); ignored where unsupported."""
+    (MADV_COLLAPSE, Linux 6.1+).  True if it reports success."""
     try:
         libc = ctypes.CDLL(None, use_errno=True)
         libc.madvise.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int]
-        libc.madvise(ctypes.c_void_p(ptr), ctypes.c_size_t(nbytes), _MADV_COLLAPSE)
+        return libc.madvise(ctypes.c_void_p(ptr), ctypes.c_size_t(nbytes), _MADV_COLLAPSE) == 0
     except (OSError, AttributeError):
-        pass
+        return False
 
 
 class PinnedBuffer:
-    """Page-locked, device-mapped host bytes of an exact size, backed by
-    transparent huge pages.
+    """Page-locked, device-mapped host bytes backed by transparent huge
+    pages, with an allocator that only hands out huge-page ranges.
 
-    The bytes come from an anonymous mapping aligned to 512 MiB and marked
-    MADV_HUGEPAGE, touched once, then registered with the CUDA driver
-    (cudaHostRegister, portable | mapped).  On the GB300 (NVLink-C2C, 64 KiB
-    base pages) the GPU's sustained host->device rate from pinned memory
-    built of small pages falls far below the link rate once the footprint
-    is several GB (address translations no longer fit the GPU's caches);
-    from huge-page memory it stays at the link rate.  Unlike a caching
-    pinned allocator, the size is not rounded to a power of two."""
+    The mapping is anonymous, aligned to 512 MiB and marked MADV_HUGEPAGE.
+    Ranges of 512 MiB are prepared as the allocator reaches them: touched,
+    then collapsed (MADV_COLLAPSE); a range the kernel could not back with a
+    huge page is skipped.  The prepared prefix is then registered with the
+    CUDA driver (cudaHostRegister, portable | mapped).
 
-    ALIGN = 512 << 20
+    Why: on the GB300 (NVLink-C2C, 64 KiB base pages) the GPU's sustained
+    host->device rate from pinned memory made of small pages falls far
+    below the link rate once the footprint is several GB (17-150 GB/s
+    measured, against 211 GB/s from huge-page memory), and a block that
+    lands even partly in small pages takes 10-40x longer to stream.
 
-    def __init__(self, nbytes):
+    With defer=False (default) `nbytes` are placed and registered at once
+    and `ptr` points at them; with defer=True the caller place()s its pieces
+    and then calls register()."""
+
+    SMALL = 256 << 20     # below this the footprint is too small to matter
+
+    def __init__(self, nbytes, spare=0.25, tries=3, defer=False):
         self.nbytes = int(nbytes)
-        size = self.nbytes + self.ALIGN
-        self._map = mmap.mmap(-1, size, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
-        try:
-            self._map.madvise(mmap.MADV_HUGEPAGE)
-        except (AttributeError, OSError, ValueError):
-            pass
-        self._cbuf = (ctypes.c_uint8 * size).from_buffer(self._map)
+        self.small = self.nbytes < self.SMALL
+        n_ranges = max(1, -(-self.nbytes // _HUGE))
+        self.capacity = (_round_up(self.nbytes, 1 << 16) if self.small
+                         else (n_ranges + int(n_ranges * spare) + 2) * _HUGE)
+        self.tries = tries
+        self._map = mmap.mmap(-1, self.capacity + _HUGE,
+                              flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+        if not self.small:
+            try:
+                self._map.madvise(mmap.MADV_HUGEPAGE)
+            except (AttributeError, OSError, ValueError):
+                pass
+        self._cbuf = (ctypes.c_uint8 * (self.capacity + _HUGE)).from_buffer(self._map)
         base = ctypes.addressof(self._cbuf)
-        self.ptr = _round_up(base, self.ALIGN)
+        self.ptr = _round_up(base, _HUGE)
         self.offset = self.ptr - base
-        ctypes.memset(self.ptr, 0, self.nbytes)       # first touch: huge pages
-        _collapse(self.ptr, self.nbytes)
-        self._t = torch.frombuffer(self._map, dtype=torch.uint8)
+        self.good = []                  # per prepared 512 MiB range
+        self._cursor = 0
+        self._t = None
+        self.registered = False
+        self.registered_bytes = 0
+        if not defer:
+            self.base_offset = self.place([self.nbytes], 256 if self.small else _HUGE)[0]
+            self.register()
+            self.ptr += self.base_offset
+            self.offset += self.base_offset
+
+    def _prepare(self, upto):
+        if self.small:
+            if not self.good:
+                ctypes.memset(self.ptr, 0, self.capacity)
+                self.good = [False]
+            return
+        while len(self.good) < upto:
+            r = len(self.good)
+            if (r + 1) * _HUGE > self.capacity:
+                raise MemoryError("PinnedBuffer: capacity exhausted")
+            ctypes.memset(self.ptr + r * _HUGE, 0, _HUGE)      # first touch
+            ok = False
+            for _ in range(self.tries):
+                if _collapse(self.ptr + r * _HUGE, _HUGE):
+                    ok = True
+                    break
+            self.good.append(ok)
+
+    def place(self, sizes, align=256):
+        """Offsets (from .ptr) for pieces of the given sizes, in order.
+        Pieces go into runs of huge-page ranges first (a piece never covers
+        a range the kernel could not back with a huge page); pieces that
+        find no such run once the spare room is used up take the remaining
+        space, small pages included."""
+        if self.registered:
+            raise RuntimeError("PinnedBuffer: place after register")
+        if self.small:
+            self._prepare(1)
+            offs = []
+            for n in sizes:
+                pos = _round_up(self._cursor, align)
+                if pos + int(n) > self.capacity:
+                    raise MemoryError("PinnedBuffer: %d bytes do not fit" % int(n))
+                offs.append(pos)
+                self._cursor = pos + int(n)
+            return offs
+        offs = [None] * len(sizes)
+        cursor = self._cursor
+        for i, n in enumerate(sizes):
+            n = int(n)
+            pos = _round_up(cursor, align)
+            while True:
+                first, last = pos // _HUGE, (pos + n - 1) // _HUGE
+                if (last + 1) * _HUGE > self.capacity:
+                    break
+                self._prepare(last + 1)
+                bad = [r for r in range(first, last + 1) if not self.good[r]]
+                if not bad:
+                    offs[i] = pos
+                    cursor = pos + n
+                    break
+                pos = (bad[-1] + 1) * _HUGE
+        self._cursor = max(cursor, self._cursor)
+        # leftovers: first fit into the space no piece uses
+        for i, n in enumerate(sizes):
+            if offs[i] is not None:
+                continue
+            used = sorted((o, o + int(sizes[j])) for j, o in enumerate(offs) if o is not None)
+            pos, n = 0, int(n)
+            for a, b in used + [(self.capacity, self.capacity)]:
+                pos = _round_up(pos, align)
+                if pos + n <= a:
+                    break
+                pos = max(pos, b)
+            if pos + n > self.capacity:
+                raise MemoryError("PinnedBuffer: %d bytes do not fit" % n)
+            self._prepare((pos + n - 1) // _HUGE + 1)
+            offs[i] = pos
+            self._cursor = max(self._cursor, pos + n)
+        return offs
+
+    def register(self):
+        nbytes = self.capacity if self.small else len(self.good) * _HUGE
         rt = torch.cuda.cudart()
-        err = rt.cudaHostRegister(self.ptr, self.nbytes, 1 | 2)   # portable | mapped
+        self._reg_ptr = self.ptr
+        err = rt.cudaHostRegister(self.ptr, nbytes, 1 | 2)   # portable | mapped
         code = err.value if hasattr(err, "value") else int(err)
         if code != 0:
-            raise RuntimeError("cudaHostRegister of %d bytes failed (%d)" % (self.nbytes, code))
+            raise RuntimeError("cudaHostRegister of %d bytes failed (%d)" % (nbytes, code))
         self.registered = True
+        self.registered_bytes = nbytes
+        self._t = torch.frombuffer(self._map, dtype=torch.uint8)
 
     def view(self, offset, nbytes):
         return self._t[self.offset + offset:self.offset + offset + nbytes]
 
+    def good_fraction(self):
+        """Fraction of the prepared 512 MiB ranges backed by a huge page
+        (None for a small buffer, which uses base pages)."""
+        if self.small or not self.good:
+            return None
+        return sum(self.good) / len(self.good)
+
     def huge_fraction(self):
-        """Fraction of the buffer's resident bytes backed by huge pages
+        """Fraction of the mapping's resident bytes backed by huge pages
         (from /proc/self/smaps), or None where that is not readable."""
         try:
             with open("/proc/self/smaps") as fh:
                 lines = fh.read().splitlines()
         except OSError:
             return None
-        lo, hi = self.ptr, self.ptr + self.nbytes
+        lo, hi = self.ptr, self.ptr + self.capacity
         rss = huge = 0
         inside = False
         for line in lines:
@@ -95,7 +200,7 @@ class PinnedBuffer:
 
     def close(self):
         if self.registered:
-            torch.cuda.cudart().cudaHostUnregister(self.ptr)
+            torch.cuda.cudart().cudaHostUnregister(self._reg_ptr)
             self.registered = False
         if self._map is not None:
             self._t = None
@@ -114,9 +219,10 @@ class PinnedBuffer:
 
 
 class HostBlocks:
-    """The pinned shards of `w.distinct` host blocks: per block, for every
-    dtype group g and shard r, shard_alloc_bytes at a 256-byte aligned offset
-    of one registered buffer."""
+    """The pinned shards of `w.distinct` host blocks.  For every host block
+    and dtype group g, the group's shards sit at a constant stride (the
+    shard bytes rounded up to 256) inside one huge-page-backed piece, so a
+    prefetch can move each group as one 2-D DMA."""
 
     def __init__(self, w: W.Workload, seed=0, gen_device="cpu", keep_params=False):
         self.w = w
@@ -124,14 +230,19 @@ class HostBlocks:
         self.plan = dlo.Plan(self.descs, w.shards)
         self.groups = self.plan.groups()
         s = w.shards
-        self.offsets = []
-        off = 0
-        for g in self.groups:
-            for _ in range(s):
-                self.offsets.append(off)
-                off += _round_up(g.shard_alloc_bytes, 256)
-        self.block_bytes = off
-        self.buf = PinnedBuffer(self.block_bytes * w.distinct)
+        self.strides = [_round_up(g.shard_alloc_bytes, 256) for g in self.groups]
+        piece = [s * st for st in self.strides]
+        self.buf = PinnedBuffer(w.distinct * sum(_round_up(p, 256) for p in piece), defer=True)
+        where = self.buf.place([piece[g] for _ in range(w.distinct)
+                                for g in range(len(self.groups))])
+        self.offsets = []                  # [hb][g * s + r] offsets from buf.ptr
+        for hb in range(w.distinct):
+            offs = []
+            for g, st in enumerate(self.strides):
+                o = where[hb * len(self.groups) + g]
+                offs += [o + r * st for r in range(s)]
+            self.offsets.append(offs)
+        self.buf.register()
         self.params = [] if keep_params else None
         for hb in range(w.distinct):
             p = W.gen_block(w, hb, seed, device=gen_device)
@@ -155,15 +266,14 @@ class HostBlocks:
         del dst
 
     def shard_ptrs(self, hb):
-        base = self.buf.ptr + hb * self.block_bytes
-        return [base + o for o in self.offsets]
+        return [self.buf.ptr + o for o in self.offsets[hb]]
 
     def shard_views(self, hb):
         """uint8 tensors over the shards of host block hb, [g * s + r]."""
         out = []
-        for i, o in enumerate(self.offsets):
+        for i, o in enumerate(self.offsets[hb]):
             g = self.groups[i // self.w.shards]
-            out.append(self.buf.view(hb * self.block_bytes + o, g.shard_alloc_bytes))
+            out.append(self.buf.view(o, g.shard_alloc_bytes))
         return out
 
     def close(self):
