@@ -59,9 +59,14 @@ def parse():
     ap.add_argument("--pretouch", type=int, default=1,
                     help="1: read every pinned host block once from the GPU before timing")
     ap.add_argument("--only", default=None,
-                    choices=["linear", "attention", "norm", "copy", "forward"],
+                    choices=["linear", "fc2", "attention", "norm", "copy", "forward"],
                     help="run one kernel of the workload's block `--reps` times (for ncu)")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--sweep", action="store_true",
+                    help="run the transfer-vs-compute sweep (36 cells), one JSON line per cell")
+    ap.add_argument("--sweep-d", default="1664,3328,6656")
+    ap.add_argument("--sweep-t", default="256,4096,16384")
+    ap.add_argument("--sweep-s", default="1,2,4,8")
     return ap.parse_args()
 
 
@@ -440,6 +445,14 @@ def run_only(args):
         wt = (0.02 * torch.randn(f, d, device=dev)).to(torch.bfloat16)
         out = torch.empty(M, f, dtype=torch.bfloat16, device=dev)
         fn = lambda: dlo.op_linear(a, M, d, wt, f, dlo.EPI_GELU_BF16, out, None, s)
+    elif args.only == "fc2":
+        a = torch.randn(M, f, device=dev).to(torch.bfloat16)
+        wt = (0.02 * torch.randn(d, f, device=dev)).to(torch.bfloat16)
+        x = torch.randn(M, d, device=dev)
+        gate = 0.1 * torch.randn(d, device=dev)
+        nws = dlo.op_linear_workspace_bytes(M, d, f, dlo.EPI_RESID_F32)
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+        fn = lambda: dlo.op_linear(a, M, f, wt, d, dlo.EPI_RESID_F32, x, gate, s, ws, nws)
     elif args.only == "attention":
         qkv = torch.randn(M, 3 * d, device=dev).to(torch.bfloat16)
         o = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
@@ -477,10 +490,98 @@ def run_only(args):
                       "ms_per_rep": e0.elapsed_time(e1) / args.reps}), flush=True)
 
 
+def run_sweep(args):
+    """The transfer-vs-compute sweep: for every (hidden d, tokens T, shards s)
+    cell, 16 blocks per step streamed through the engine (AUTO copy mode)
+    and the same blocks all resident; prints one JSON line per cell with the
+    streamed and resident step times, exposed transfer, overlap and the
+    block-roofline fraction.  Weights are drawn once per d and re-sharded
+    per s; one set of pinned shards serves all T."""
+    import torch
+    from layerwise_weight_offload_gb300 import build as B
+    B.build()
+    from layerwise_weight_offload_gb300 import dlo, workloads as W
+    from layerwise_weight_offload_gb300.stack import HostBlocks, StreamedStack, ResidentStack
+    bf16_peak, bf16_sust, _, _ = measured_peaks()
+    ceiling = h2d_ceiling_gbs(torch)
+    for d in [int(v) for v in args.sweep_d.split(",")]:
+        base = W.CONFIGS["sweep-d%d-t256-s1" % d]
+        params = []
+        for hb in range(base.distinct):
+            p = W.gen_block(base, hb, args.seed, device="cuda")
+            params.append({k: v.cpu().contiguous() for k, v in p.items()})
+        torch.cuda.empty_cache()
+        for s in [int(v) for v in args.sweep_s.split(",")]:
+            w0 = W.CONFIGS["sweep-d%d-t256-s%d" % (d, s)]
+            host = HostBlocks(w0, params=params)
+            host.pretouch()
+            for T in [int(v) for v in args.sweep_t.split(",")]:
+                w = W.CONFIGS["sweep-d%d-t%d-s%d" % (d, T, s)]
+                host.w = w
+                st = StreamedStack(host, copy_mode=dlo.COPY_AUTO, timing=True)
+                x = W.gen_x(w, args.seed, device="cuda")
+                cur = torch.cuda.current_stream()
+                steps = 3 if T < 16384 else 2
+                warm = 3
+                st.compute.wait_stream(cur)
+                for _ in range(warm):
+                    st.step(x)
+                torch.cuda.synchronize()
+                n_before = len(st.engine.copy_times()[0])
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st.compute)
+                for _ in range(steps):
+                    st.step(x)
+                e1.record(st.compute)
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / steps
+                cms, cby = st.engine.copy_times()
+                cms = cms[n_before:n_before + w.n_blocks * steps]
+                cby = cby[n_before:n_before + w.n_blocks * steps]
+                chosen = dlo.COPY_MODE_NAMES[st.engine.query().chosen_mode]
+                st.close()
+                rs = ResidentStack(host)
+                xr = W.gen_x(w, args.seed, device="cuda")
+                rs.stream.wait_stream(cur)
+                rs.step(xr)
+                r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                r0.record(rs.stream)
+                for _ in range(steps):
+                    rs.step(xr)
+                r1.record(rs.stream)
+                torch.cuda.synchronize()
+                res = r0.elapsed_time(r1) / steps
+                del rs
+                bytes_block = sum(g.shard_bytes * s for g in host.plan.groups())
+                t_roof = max(bytes_block / (ceiling * 1e9), w.flops_per_block() / (bf16_sust * 1e12))
+                copy_step = sum(cms) / steps
+                exposed = ms - res
+                print(json.dumps({
+                    "cell": w.name, "hidden": d, "tokens": T, "shards": s, "blocks": w.n_blocks,
+                    "streamed_ms_per_step": ms, "resident_ms_per_step": res,
+                    "exposed_transfer_ms_per_step": exposed,
+                    "copy_ms_per_step": copy_step,
+                    "h2d_gbs": sum(cby) / (sum(cms) * 1e6) if cms else None,
+                    "overlap_fraction": 1 - exposed / copy_step if copy_step > 0 else None,
+                    "block_fwd_per_s": w.n_blocks / (ms / 1e3),
+                    "block_roofline_fraction": w.n_blocks * t_roof * 1e3 / ms,
+                    "bound": "h2d" if bytes_block / (ceiling * 1e9) >= w.flops_per_block() / (bf16_sust * 1e12) else "tensor",
+                    "copy_mode": chosen}), flush=True)
+                del x, xr
+                torch.cuda.empty_cache()
+            host.close()
+            del host
+    if dlo.kernel_status() != 0:
+        raise RuntimeError("a kernel wait timed out")
+
+
 def main():
     args = parse()
     if args.only:
         run_only(args)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
     ws, rank, local = dist_env()
     if args.warmup < 3:

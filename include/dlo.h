@@ -63,7 +63,8 @@ typedef enum { DLO_BF16 = 0, DLO_F32 = 1 } dlo_dtype;
  *   DMA:    copy engines, no SMs: per dtype group one cudaMemcpy2DAsync
  *           when the group's host shards sit at a constant stride (rows =
  *           shards, destination pitch = shard bytes, i.e. the gathered
- *           layout), else one cudaMemcpyAsync per shard, each straight to
+ *           layout; one cudaMemcpyAsync when that stride equals the shard
+ *           bytes), else one cudaMemcpyAsync per shard, each straight to
  *           the shard's final offset in the slot.  In the engine, a group
  *           under 1 MiB (when the block has another, larger group and its
  *           shards are device-mapped) moves by a one-CTA copy-kernel launch

@@ -200,11 +200,18 @@ dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, in
     const auto& grp = p->groups[g];
     if (by_kernel[g]) continue;
     if (fan <= 1 && !b.pitch.empty() && b.pitch[g] > 0) {
-      // all shards of the group in one 2-D copy
-      DLO_CUDA(cudaMemcpy2DAsync(dst + grp.base, static_cast<size_t>(grp.shard_bytes),
-                                 b.host[g * s], static_cast<size_t>(b.pitch[g]),
-                                 static_cast<size_t>(grp.shard_bytes), static_cast<size_t>(s),
+      if (b.pitch[g] == grp.shard_bytes) {
+        // the shards are back to back in host memory: one linear copy
+        DLO_CUDA(cudaMemcpyAsync(dst + grp.base, b.host[g * s],
+                                 static_cast<size_t>(grp.shard_bytes) * s,
                                  cudaMemcpyHostToDevice, stream));
+      } else {
+        // all shards of the group in one 2-D copy
+        DLO_CUDA(cudaMemcpy2DAsync(dst + grp.base, static_cast<size_t>(grp.shard_bytes),
+                                   b.host[g * s], static_cast<size_t>(b.pitch[g]),
+                                   static_cast<size_t>(grp.shard_bytes), static_cast<size_t>(s),
+                                   cudaMemcpyHostToDevice, stream));
+      }
       continue;
     }
     for (int32_t r = 0; r < s; ++r)

@@ -224,7 +224,7 @@ class HostBlocks:
     shard bytes rounded up to 256) inside one huge-page-backed piece, so a
     prefetch can move each group as one 2-D DMA."""
 
-    def __init__(self, w: W.Workload, seed=0, gen_device="cpu", keep_params=False):
+    def __init__(self, w: W.Workload, seed=0, gen_device="cpu", keep_params=False, params=None):
         self.w = w
         self.descs = W.block_param_descs(w)
         self.plan = dlo.Plan(self.descs, w.shards)
@@ -245,8 +245,11 @@ class HostBlocks:
         self.buf.register()
         self.params = [] if keep_params else None
         for hb in range(w.distinct):
-            p = W.gen_block(w, hb, seed, device=gen_device)
-            p = {k: v.cpu().contiguous() for k, v in p.items()}
+            if params is not None:
+                p = params[hb]
+            else:
+                p = W.gen_block(w, hb, seed, device=gen_device)
+                p = {k: v.cpu().contiguous() for k, v in p.items()}
             srcs = [p[name].data_ptr() for name, _, _ in self.descs]
             self.plan.shard_host(srcs, self.shard_ptrs(hb))
             if keep_params:
