@@ -7,30 +7,31 @@
 // c, u] (keys contiguous), which the QKV linear's epilogue writes directly,
 // so that both products below take K-major operands.
 //
-// One CTA = 128 queries of one (batch, head), 11 warps:
-//   warp 0     TMA: the Q tile once, then K tiles of 128 keys into a 2-stage
-//              ring (a stage is released as soon as its S product is done);
-//   warp 10    TMA: V^T tiles of 128 keys into a 2-stage ring (released after
-//              the PV product), so a V reload never delays the next K;
-//   warp 1     allocates 512 TMEM columns and issues tcgen05.mma: S_j =
-//              Q K_j^T (M=128, N=128) into S buffer j%2, and O_{j%2} +=
-//              P_j V_j (M=128, N=hd); S_{j+2} is issued right after PV_j;
-//   warps 2-5  softmax set 0: even KV tiles; warps 6-9: set 1, odd tiles.
-//              One thread per query row (its TMEM lane): tcgen05.ld of the S
-//              row, mask of keys past the end, running maximum and sum in
-//              the exp2 domain, P = exp2(s - m) as bf16 into the set's
-//              128-byte-swizzled P tile.  Two sets put two warps on every
-//              scheduler, so one set's latencies hide behind the other's
-//              work.  Each set keeps its own (m, l, O); at the end the two
-//              are merged, O = (O_0 2^(m_0-m) + O_1 2^(m_1-m)) / l, and each
-//              set stores half of the head dimension as bf16.
-// A set's running maximum may go stale by up to 2^8 (exp2 domain): its O is
-// rescaled in TMEM (tcgen05.ld, multiply, tcgen05.st) only when a row's
-// maximum grows by more than 8, so every P <= 256.  S_{j+2} is issued after
-// PV_j, so when a set sees S of its next tile, its previous PV is complete
-// and both its O and its P tile are free.  Keys past the end are -inf in S
-// and zero in V (TMA zero fill).  All waits are bounded; a wait that runs
-// out records a code in the device error word and the kernel returns early.
+// One CTA = 128 queries of one (batch, head), three warpgroups:
+//   WG0, WG1   softmax sets 0 and 1 (even / odd KV tiles), one thread per
+//              query row (its TMEM lane);
+//   WG2        warp 8: TMA of the Q tile once, then K tiles of 128 keys into
+//              a 2-stage ring; warp 9: TMEM allocation (512 columns) and the
+//              tcgen05.mma issue; warp 10: TMA of V^T tiles into a 2-stage
+//              ring.
+// The producer/MMA warpgroup gives registers back (setmaxnreg.dec to 56) so
+// the softmax warpgroups can hold a whole 128-score row in registers
+// (setmaxnreg.inc to 224; 128*56 + 256*224 equals the launch's 384*168).
+// Per KV tile j of set x = j%2:
+//   MMA:     S_j = Q K_j^T (M=128, N=128) into TMEM S buffer x; PV_j:
+//            O_x += P_j V_j (M=128, N=hd).  S_{j+2} is issued as soon as set
+//            x has copied S_j out of TMEM, before PV_j, so the next scores
+//            are ready when the set finishes the current tile.
+//   softmax: tcgen05.ld of the S row into registers, release of the S
+//            buffer, row maximum (the set's first tile fixes m; later tiles
+//            keep it unless a row's maximum grows by more than 2^64, which
+//            rescales O_x and l), then — after PV_{j-2} has finished with
+//            this set's P tile and O — P = exp2(s - m) as bf16 into the P
+//            tile (128-byte swizzle) and the row sum.
+// At the end O = (O_0 2^(m_0-m) + O_1 2^(m_1-m)) / l, each set storing half
+// of the head dimension as bf16.  Keys past the end are -inf in S and zero
+// in V (TMA zero fill).  All waits are bounded; a wait that runs out records
+// a code in the device error word and the kernel returns early.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -41,9 +42,13 @@
 namespace dlo {
 namespace {
 
-constexpr int BQ = 128, BKV = 128, ATT_THREADS = 352;
+constexpr int BQ = 128, BKV = 128, ATT_THREADS = 384;
 constexpr uint32_t ATT_TMEM_COLS = 512;
-constexpr float kRescaleThreshold = 8.f;   // log2 units
+// A set keeps the maximum of its first tile until a row's scores exceed it
+// by more than this (log2 units): P then stays below 2^64, far from the
+// fp32 and bf16 range limits (without loss of relative precision), and O
+// needs no rescaling in the common case.
+constexpr float kGrowLimit = 64.f;
 
 template <int HD>
 struct AttLayout {
@@ -107,6 +112,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wg = warp >> 2;
   const int q0 = blockIdx.x * BQ;
   const int head = blockIdx.y, b = blockIdx.z;
   const int n_kv = (tokens + BKV - 1) / BKV;
@@ -127,11 +133,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
     *abort = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tm_qk);
     tma_prefetch_desc(&tm_vt);
   }
-  if (warp == 1) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, ATT_TMEM_COLS);
     tmem_relinquish();
   }
@@ -142,9 +148,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
   const uint32_t tS = tmem;             // S of set x at column 128 x
   const uint32_t tO = tmem + 256;       // O of set x at column 256 + HD x
 
-  if (warp == 0 || warp == 10) {
-    if (lane == 0) {
-      const bool is_k = warp == 0;
+  if (wg == 2) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    if ((warp == 8 || warp == 10) && lane == 0) {
+      const bool is_k = warp == 8;
       uint64_t* full = is_k ? k_full : v_full;
       uint64_t* empty = is_k ? k_empty : v_empty;
       if (is_k) {
@@ -181,15 +188,12 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
         for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
           mbar_wait_bounded(&full[j & 1], static_cast<uint32_t>((j >> 1) & 1), &never);
       }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
+    } else if (warp == 9 && lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(BQ, BKV);
       constexpr uint32_t idesc_o = idesc_bf16_f32(BQ, HD);
       bool ok = mbar_wait_bounded(q_full, 0, abort);
-      if (!ok) att_fail(err, abort, DEV_TIMEOUT_MMA_FULL);
       const uint32_t q_addr = smem_u32(sQ);
-      // S_j = Q K_j^T into S buffer j%2
+      // S_j = Q K_j^T into S buffer j%2 once the set has copied S_{j-2} out
       auto issue_s = [&](int j) -> bool {
         const int x = j & 1;
         const uint32_t n = static_cast<uint32_t>(j >> 1);
@@ -212,6 +216,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
       for (int j = 0; ok && j < n_kv; ++j) {
         const int x = j & 1;
         const uint32_t n = static_cast<uint32_t>(j >> 1);
+        if (j + 2 < n_kv && !(ok = issue_s(j + 2))) break;
         if (!mbar_wait_bounded(&p_full[x], n & 1u, abort) ||
             !mbar_wait_bounded(&v_full[x], n & 1u, abort)) {
           ok = false;
@@ -227,7 +232,6 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
                     (j >= 2 || kk > 0) ? 1u : 0u);
         umma_commit(&v_empty[x]);
         umma_commit(&pv_done[x]);
-        if (j + 2 < n_kv) ok = issue_s(j + 2);
       }
       if (!ok) {
         att_fail(err, abort, DEV_TIMEOUT_MMA_FULL);
@@ -237,11 +241,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
       }
     }
   } else {
-    const int x = (warp - 2) >> 2;             // softmax set: 0 even tiles, 1 odd tiles
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
+    const int x = wg;                          // softmax set: 0 even tiles, 1 odd tiles
     const int quad = warp & 3;
     const int row = quad * 32 + lane;          // query row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tSx = tS + x * BKV, tOx = tO + x * HD;
+    uint8_t* prow = sP + x * L::P_BYTES + row * 128;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     int last = -1;                             // last tile this set processed
@@ -253,40 +259,48 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
         break;
       }
       tc_fence_after();
+      // the whole S row into registers, then the S buffer is free for S_{j+2}
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tSx + c * 32 + lane_off, sr[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[x]);
       const int valid = tokens - j * BKV;      // keys of this tile that exist
-      // pass 1: row maximum of the raw scores (S is read twice from TMEM so
-      // that only 64 of its 128 values are in registers at a time)
+      if (valid < BKV) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i >= valid) sr[c][i] = __float_as_uint(-INFINITY);
+      }
       float mx[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
 #pragma unroll
-      for (int cp = 0; cp < 2; ++cp) {
-        uint32_t ra[32], rb[32];
-        tmem_ld_32x32b_x32(tSx + (2 * cp) * 32 + lane_off, ra);
-        tmem_ld_32x32b_x32(tSx + (2 * cp + 1) * 32 + lane_off, rb);
-        tmem_ld_wait();
-        if (valid < BKV) {                     // only the last tile has missing keys
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (cp * 64 + i >= valid) ra[i] = __float_as_uint(-INFINITY);
-            if (cp * 64 + 32 + i >= valid) rb[i] = __float_as_uint(-INFINITY);
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(ra[i]));
-          mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(rb[i]));
-        }
-      }
+        for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(sr[c][i]));
       const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
                        scale_log2;
+      // PV_{j-2} must be done with this set's P tile (and O) before either
+      // is touched
+      if (last >= 0 &&
+          !__all_sync(0xffffffffu,
+                      mbar_wait_bounded(&pv_done[x], static_cast<uint32_t>((last >> 1) & 1),
+                                        abort))) {
+        if (lane == 0) att_fail(err, abort, DEV_TIMEOUT_EPILOGUE);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
       if (last < 0) {
-        m = mt;
+        m = mt;                                // the set's first tile fixes m
       } else {
-        const bool need = mt > m + kRescaleThreshold;
+        const bool need = mt > m + kGrowLimit;
         if (__any_sync(0xffffffffu, need)) {
-          // this set's previous PV completed before its S_j was issued
           float corr = 1.f;
           if (need) {
             corr = ex2_approx(m - mt);
@@ -306,41 +320,25 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
           tmem_st_wait();
         }
       }
-      // pass 2: P = exp2(s * scale - m) as bf16 into this set's swizzled P
-      // tile; the row sum runs in eight independent partial sums
-      uint8_t* prow = sP + x * L::P_BYTES + row * 128;
+      // P = exp2(s * scale - m) as bf16 into the swizzled P tile; row sum in
+      // eight independent partial sums
       const float neg_m = -m;
       float ls[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) ls[e] = 0.f;
 #pragma unroll
-      for (int cp = 0; cp < 2; ++cp) {
-        uint32_t rr[2][32];
-        tmem_ld_32x32b_x32(tSx + (2 * cp) * 32 + lane_off, rr[0]);
-        tmem_ld_32x32b_x32(tSx + (2 * cp + 1) * 32 + lane_off, rr[1]);
-        tmem_ld_wait();
+      for (int c = 0; c < 16; ++c) {
+        float p[8];
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {        // 8 keys: chunk c of the 16 in a row
-            const int c = cp * 8 + h * 4 + q;
-            float p[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              float v = ex2_approx(fmaf(__uint_as_float(rr[h][q * 8 + e]), scale_log2, neg_m));
-              if (valid < BKV && c * 8 + e >= valid) v = 0.f;
-              p[e] = v;
-              ls[e] += v;
-            }
-            const uint4 pk = make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]),
-                                        pack_bf16(p[4], p[5]), pack_bf16(p[6], p[7]));
-            const int cc = c & 7;
-            *reinterpret_cast<uint4*>(prow + (c >> 3) * L::P_CHUNK + ((cc ^ (row & 7)) << 4)) = pk;
-          }
+        for (int e = 0; e < 8; ++e) {
+          p[e] = ex2_approx(fmaf(__uint_as_float(sr[c >> 2][(c & 3) * 8 + e]), scale_log2, neg_m));
+          ls[e] += p[e];
+        }
+        const uint4 pk = make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]),
+                                    pack_bf16(p[4], p[5]), pack_bf16(p[6], p[7]));
+        const int cc = c & 7;
+        *reinterpret_cast<uint4*>(prow + (c >> 3) * L::P_CHUNK + ((cc ^ (row & 7)) << 4)) = pk;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[x]);
       l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       fence_proxy_async_smem();
       tc_fence_before();
@@ -357,7 +355,6 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
       if (lane == 0) att_fail(err, abort, DEV_TIMEOUT_EPILOGUE);
       ok = false;
     }
-    // both sets must be past their last product before any P tile is reused
     asm volatile("bar.sync 1, 256;" ::: "memory");
     float* xch = reinterpret_cast<float*>(sP);  // [set][row] m, then l
     xch[x * 256 + row] = m;
@@ -401,7 +398,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, ATT_TMEM_COLS);
   }
@@ -430,7 +427,16 @@ transpose_v_kernel(const uint16_t* __restrict__ qkv, int tokens, int d, uint16_t
 }
 
 cudaError_t g_att_err = cudaSuccess;
+bool g_att_regs_ok = false;
 std::once_flag g_att_once;
+
+// The register split of the kernel (setmaxnreg: 128 threads down to 56,
+// 256 threads up to 224) needs the launch to hold 128*56 + 256*224 = 64512
+// registers, i.e. exactly 168 per thread for 384 threads; a smaller launch
+// allocation would leave setmaxnreg.inc waiting.  The launcher checks the
+// compiled count and refuses to launch otherwise.
+constexpr int kAttRegsPerThread = 168;
+static_assert(128 * 56 + 256 * 224 == ATT_THREADS * kAttRegsPerThread, "register split");
 
 void set_att_attrs() {
   std::call_once(g_att_once, [] {
@@ -441,6 +447,11 @@ void set_att_attrs() {
                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           AttLayout<128>::SMEM);
     g_att_err = e0 != cudaSuccess ? e0 : e1;
+    cudaFuncAttributes a64{}, a128{};
+    if (g_att_err == cudaSuccess) g_att_err = cudaFuncGetAttributes(&a64, attention_tc_kernel<64>);
+    if (g_att_err == cudaSuccess)
+      g_att_err = cudaFuncGetAttributes(&a128, attention_tc_kernel<128>);
+    g_att_regs_ok = a64.numRegs == kAttRegsPerThread && a128.numRegs == kAttRegsPerThread;
   });
 }
 
@@ -450,6 +461,9 @@ dlo_status launch_hd(const CUtensorMap& tm_qk, const CUtensorMap& tm_vt, int64_t
                      cudaStream_t stream) {
   set_att_attrs();
   DLO_CUDA(g_att_err);
+  if (!g_att_regs_ok)
+    DLO_FAIL(DLO_ERR_CUDA, "attention: kernel not compiled with %d registers per thread",
+             kAttRegsPerThread);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
   dim3 grid(static_cast<unsigned>((tokens + BQ - 1) / BQ), static_cast<unsigned>(heads),
             static_cast<unsigned>(batch));
@@ -467,6 +481,9 @@ int64_t vt_ld_for(int64_t tokens) { return (tokens + 7) / 8 * 8; }
 dlo_status attention_preload() {
   set_att_attrs();
   DLO_CUDA(g_att_err);
+  if (!g_att_regs_ok)
+    DLO_FAIL(DLO_ERR_CUDA, "attention: kernel not compiled with %d registers per thread",
+             kAttRegsPerThread);
   return DLO_OK;
 }
 

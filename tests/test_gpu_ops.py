@@ -145,3 +145,22 @@ def test_rejects_unsupported_shapes():
     q = torch.zeros(4, 96 * 3, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(dlo.DLOError):
         _attention(q, 1, 4, 96, 3, q)                              # head dim 32
+
+
+@pytest.mark.parametrize("d,H", [(256, 4), (256, 2)])
+def test_attention_scores_growing_across_tiles(d, H):
+    # scores rise with the key index, so later KV tiles have a much larger
+    # row maximum than the first one: exercises the rescale-and-redo path
+    T = 2048
+    hd = d // H
+    qkv = torch.zeros(T, 3 * d)
+    qkv[:, :d] = 1.0
+    ramp = torch.arange(T, dtype=torch.float32) / T
+    qkv[:, d:2 * d] = (ramp * 40.0 / hd ** 0.5)[:, None] * 8.0
+    qkv[:, 2 * d:] = torch.randn(T, d, generator=torch.Generator().manual_seed(5))
+    qkv = qkv.to(torch.bfloat16)
+    o = torch.full((T, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    _attention(qkv.cuda(), 1, T, d, H, o)
+    _status_clean()
+    ref = oracle.attention(qkv.float().numpy(), 1, T, d, H)
+    assert_oracle_close(o.float().cpu().numpy(), ref, "growing scores", 1e-2, 4e-3)
