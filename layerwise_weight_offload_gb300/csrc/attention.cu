@@ -7,31 +7,33 @@
 // c, u] (keys contiguous), which the QKV linear's epilogue writes directly,
 // so that both products below take K-major operands.
 //
-// One CTA = 128 queries of one (batch, head), three warpgroups:
-//   WG0, WG1   softmax sets 0 and 1 (even / odd KV tiles), one thread per
-//              query row (its TMEM lane);
-//   WG2        warp 8: TMA of the Q tile once, then K tiles of 128 keys into
-//              a 2-stage ring; warp 9: TMEM allocation (512 columns) and the
-//              tcgen05.mma issue; warp 10: TMA of V^T tiles into a 2-stage
-//              ring.
-// The producer/MMA warpgroup gives registers back (setmaxnreg.dec to 56) so
-// the softmax warpgroups can hold a whole 128-score row in registers
-// (setmaxnreg.inc to 224; 128*56 + 256*224 equals the launch's 384*168).
-// Per KV tile j of set x = j%2:
-//   MMA:     S_j = Q K_j^T (M=128, N=128) into TMEM S buffer x; PV_j:
-//            O_x += P_j V_j (M=128, N=hd).  S_{j+2} is issued as soon as set
-//            x has copied S_j out of TMEM, before PV_j, so the next scores
-//            are ready when the set finishes the current tile.
-//   softmax: tcgen05.ld of the S row into registers, release of the S
-//            buffer, row maximum (the set's first tile fixes m; later tiles
-//            keep it unless a row's maximum grows by more than 2^64, which
-//            rescales O_x and l), then — after PV_{j-2} has finished with
-//            this set's P tile and O — P = exp2(s - m) as bf16 into the P
-//            tile (128-byte swizzle) and the row sum.
-// At the end O = (O_0 2^(m_0-m) + O_1 2^(m_1-m)) / l, each set storing half
-// of the head dimension as bf16.  Keys past the end are -inf in S and zero
-// in V (TMA zero fill).  All waits are bounded; a wait that runs out records
-// a code in the device error word and the kernel returns early.
+// One CTA = two 128-query tiles (Q_0, Q_1) of one (batch, head) that share
+// every K and V tile: KV tiles of 128 keys stream once through shared memory
+// for 256 queries.  (Grids that would then have fewer CTAs than SMs run one
+// query tile per CTA instead; WG1 then idles.)  Three warpgroups:
+//   WG0, WG1   softmax of Q_0 and Q_1, one thread per query row (its TMEM
+//              lane); each finally writes its tile of o;
+//   WG2        warp 8: TMA of the two Q tiles, then K_0, V_0, K_1, V_1, ...
+//              into one NS-stage ring (NS = 5 for hd 128, 12 for hd 64);
+//              warp 9: TMEM allocation (512 columns) and the tcgen05.mma
+//              issue.
+// TMEM: S_t at column 128 t (fp32, 128 keys); P_t (bf16, two per column)
+// overwrites the first 64 columns of S_t; O_t at column 256 + hd t.
+// MMA order: S_0(0) S_1(0), then per KV tile j
+//   PV_0(j)  O_0 += P_0(j) V_j   (A = P_0 from TMEM, B = V_j^T in smem)
+//   S_0(j+1) = Q_0 K_{j+1}^T     (after PV_0(j) in issue order, so P_0(j)
+//                                 is read before S_0(j+1) overwrites it)
+//   PV_1(j), S_1(j+1).
+// While softmax t turns S_t(j+1) into P_t(j+1) the tensor pipe runs the
+// other tile's PV and S.  The commit that signals S_t(j+1) also covers
+// PV_t(j), so softmax t may then rescale O_t and overwrite P_t.
+// Softmax per tile: tcgen05.ld of the 128 scores, row maximum (a tile's
+// first KV tile fixes m; later ones keep it unless a row's scaled maximum
+// exceeds m by more than kGrowLimit, which rescales O_t and l), P =
+// 2^(s*scale - m) as bf16 into TMEM with tcgen05.st, row sum l.  At the end
+// o = O_t / l.  Keys past the end are -inf in S and zero in V (TMA zero
+// fill).  All waits are bounded; a wait that runs out records a code in the
+// device error word and the kernel returns early.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -52,18 +54,15 @@ constexpr float kGrowLimit = 64.f;
 
 template <int HD>
 struct AttLayout {
-  static constexpr int Q_BYTES = BQ * HD * 2;          // HD/64 chunks of 128 rows x 128 B
-  static constexpr int K_BYTES = BKV * HD * 2;
+  static constexpr int NS = HD == 128 ? 5 : 12;        // K/V ring stages
+  static constexpr int Q_TILE = BQ * HD * 2;           // HD/64 chunks of 128 rows x 128 B
+  static constexpr int K_CHUNK = BKV * 128;            // 128 keys x 64 dims
   static constexpr int V_CHUNK = HD * 128;             // HD rows x 64 keys
-  static constexpr int V_BYTES = 2 * V_CHUNK;          // 128 keys
-  static constexpr int P_CHUNK = BQ * 128;             // 128 rows x 64 keys
-  static constexpr int P_BYTES = 2 * P_CHUNK;
+  static constexpr int KV_BYTES = BKV * HD * 2;        // one K or V^T tile
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + 2 * K_BYTES;
-  static constexpr int OFF_P = OFF_V + 2 * V_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;    // barriers + alignment slack
+  static constexpr int OFF_KV = OFF_Q + 2 * Q_TILE;
+  static constexpr int OFF_BAR = OFF_KV + NS * KV_BYTES;
+  static constexpr int SMEM = OFF_BAR + 512 + 1024;    // barriers + alignment slack
 };
 
 __device__ __forceinline__ void att_fail(int* err, volatile int* abort, int code) {
@@ -72,7 +71,8 @@ __device__ __forceinline__ void att_fail(int* err, volatile int* abort, int code
 }
 
 // 2^x by the hardware approximation (MUFU.EX2 through the PTX instruction;
-// denormal results flush to zero, 2^-inf = 0).  Inputs here are <= 8.
+// denormal results flush to zero, 2^-inf = 0).  Inputs here are at most
+// kGrowLimit.
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -84,50 +84,83 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
+// Maximum of the first n (clamped to 0..32) of 32 fp32 scores; -inf if none.
+__device__ __forceinline__ float masked_max(const uint32_t (&sr)[32], int n) {
+  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (i < n) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(sr[i]));
+  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+// Multiplies this warp's 32 lanes x (32 * CHUNKS) fp32 columns from taddr by
+// each lane's corr.
+template <int CHUNKS>
+__device__ __forceinline__ void rescale_tmem_f32(uint32_t taddr, float corr) {
+#pragma unroll 1
+  for (int c = 0; c < CHUNKS; ++c) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(taddr + c * 32, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+    tmem_st_32x32b_x32(taddr + c * 32, r);
+  }
+}
+
+// Multiplies 16 columns of bf16 pairs from taddr by each lane's corr.
+__device__ __forceinline__ void rescale_tmem_bf16x2(uint32_t taddr, float corr) {
+  uint32_t r[32];
+  tmem_ld_32x32b_x32(taddr, r);              // columns taddr..taddr+31; the
+  tmem_ld_wait();                            // first 16 are the P chunk
+  uint32_t q[16];
+#pragma unroll
+  for (int h = 0; h < 16; ++h) {
+    const float lo = __uint_as_float(r[h] << 16), hi = __uint_as_float(r[h] & 0xFFFF0000u);
+    q[h] = pack_bf16(lo * corr, hi * corr);
+  }
+  tmem_st_32x32b_x16(taddr, q);
+}
+
 template <int HD>
 __global__ void __launch_bounds__(ATT_THREADS, 1)
 attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
                     const __grid_constant__ CUtensorMap tm_vt, int tokens, int d, int heads,
-                    uint16_t* __restrict__ o, float scale_log2, int* err) {
+                    uint16_t* __restrict__ o, float scale_log2, int nt, int* err) {
   using L = AttLayout<HD>;
+  constexpr int NS = L::NS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem + L::OFF_Q;
-  uint8_t* sK = smem + L::OFF_K;
-  uint8_t* sV = smem + L::OFF_V;
-  uint8_t* sP = smem + L::OFF_P;
+  uint8_t* sKV = smem + L::OFF_KV;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
-  uint64_t* q_full = bar + 0;
-  uint64_t* k_full = bar + 1;     // [2]
-  uint64_t* k_empty = bar + 3;    // [2]
-  uint64_t* v_full = bar + 5;     // [2]
-  uint64_t* v_empty = bar + 7;    // [2]
-  uint64_t* s_full = bar + 9;     // [2]  per softmax set
-  uint64_t* s_empty = bar + 11;   // [2]
-  uint64_t* p_full = bar + 13;    // [2]
-  uint64_t* pv_done = bar + 15;   // [2]
-  uint64_t* drain = bar + 17;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 18);
+  uint64_t* q_full = bar;
+  uint64_t* full = bar + 1;                  // [NS]
+  uint64_t* empty = full + NS;               // [NS]
+  uint64_t* s_full = empty + NS;             // [2]  per query tile
+  uint64_t* p_full = s_full + 2;             // [2]
+  uint64_t* o_done = p_full + 2;             // [2]
+  uint64_t* drain = o_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wg = warp >> 2;
-  const int q0 = blockIdx.x * BQ;
+  const int q0 = blockIdx.x * nt * BQ;       // nt: query tiles of this CTA (1 or 2)
   const int head = blockIdx.y, b = blockIdx.z;
   const int n_kv = (tokens + BKV - 1) / BKV;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
-      mbar_init(&s_full[s], 1);
-      mbar_init(&s_empty[s], 4);
-      mbar_init(&p_full[s], 4);
-      mbar_init(&pv_done[s], 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 4);
+      mbar_init(&o_done[t], 1);
     }
     mbar_init(drain, 1);
     *abort = 0;
@@ -145,38 +178,35 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;             // S of set x at column 128 x
-  const uint32_t tO = tmem + 256;       // O of set x at column 256 + HD x
+  const uint32_t tS = tmem;             // S_t (and P_t) at column 128 t
+  const uint32_t tO = tmem + 256;       // O_t at column 256 + HD t
 
   if (wg == 2) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
-    if ((warp == 8 || warp == 10) && lane == 0) {
-      const bool is_k = warp == 8;
-      uint64_t* full = is_k ? k_full : v_full;
-      uint64_t* empty = is_k ? k_empty : v_empty;
-      if (is_k) {
-        mbar_arrive_expect_tx(q_full, L::Q_BYTES);
+    if (warp == 8 && lane == 0) {
+      // load i = 2j is K_j, i = 2j+1 is V_j; stage i % NS, use i / NS
+      mbar_arrive_expect_tx(q_full, nt * L::Q_TILE);
+      for (int t = 0; t < nt; ++t)
         for (int c = 0; c < HD / 64; ++c)
-          tma_load_2d(sQ + c * (BQ * 128), &tm_qk, q_full, head * HD + 64 * c, b * tokens + q0);
-      }
+          tma_load_2d(sQ + t * L::Q_TILE + c * (BQ * 128), &tm_qk, q_full, head * HD + 64 * c,
+                      b * tokens + q0 + t * BQ);
       int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j & 1;
-        const uint32_t n = static_cast<uint32_t>(j >> 1);
-        const int kv0 = j * BKV;
-        if (!mbar_wait_bounded(&empty[s], (n & 1u) ^ 1u, abort)) {
+      for (int i = 0; i < 2 * n_kv; ++i) {
+        const int s = i % NS;
+        const uint32_t use = static_cast<uint32_t>(i / NS);
+        const int kv0 = (i >> 1) * BKV;
+        if (!mbar_wait_bounded(&empty[s], (use & 1u) ^ 1u, abort)) {
           att_fail(err, abort, DEV_TIMEOUT_PRODUCER);
           break;
         }
-        if (is_k) {
-          mbar_arrive_expect_tx(&full[s], L::K_BYTES);
+        mbar_arrive_expect_tx(&full[s], L::KV_BYTES);
+        uint8_t* dst = sKV + s * L::KV_BYTES;
+        if ((i & 1) == 0) {
           for (int c = 0; c < HD / 64; ++c)
-            tma_load_2d(sK + s * L::K_BYTES + c * (BKV * 128), &tm_qk, &full[s],
-                        d + head * HD + 64 * c, b * tokens + kv0);
+            tma_load_2d(dst + c * L::K_CHUNK, &tm_qk, &full[s], d + head * HD + 64 * c,
+                        b * tokens + kv0);
         } else {
-          mbar_arrive_expect_tx(&full[s], L::V_BYTES);
           for (int c = 0; c < 2; ++c)
-            tma_load_2d(sV + s * L::V_BYTES + c * L::V_CHUNK, &tm_vt, &full[s], kv0 + 64 * c,
+            tma_load_2d(dst + c * L::V_CHUNK, &tm_vt, &full[s], kv0 + 64 * c,
                         (b * heads + head) * HD);
         }
         ++issued;
@@ -184,54 +214,93 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
       if (*abort) {
         // let the copies already issued land before the CTA can exit
         volatile int never = 0;
-        if (is_k) mbar_wait_bounded(q_full, 0, &never);
-        for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
-          mbar_wait_bounded(&full[j & 1], static_cast<uint32_t>((j >> 1) & 1), &never);
+        mbar_wait_bounded(q_full, 0, &never);
+        for (int i = issued - NS < 0 ? 0 : issued - NS; i < issued; ++i)
+          mbar_wait_bounded(&full[i % NS], static_cast<uint32_t>((i / NS) & 1), &never);
       }
     } else if (warp == 9 && lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(BQ, BKV);
       constexpr uint32_t idesc_o = idesc_bf16_f32(BQ, HD);
-      bool ok = mbar_wait_bounded(q_full, 0, abort);
-      const uint32_t q_addr = smem_u32(sQ);
-      // S_j = Q K_j^T into S buffer j%2 once the set has copied S_{j-2} out
-      auto issue_s = [&](int j) -> bool {
-        const int x = j & 1;
-        const uint32_t n = static_cast<uint32_t>(j >> 1);
-        if (!mbar_wait_bounded(&k_full[x], n & 1u, abort) ||
-            !mbar_wait_bounded(&s_empty[x], (n & 1u) ^ 1u, abort))
-          return false;
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(sK + x * L::K_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (BQ * 128) + (kk & 3) * 32;
-          umma_bf16(tS + x * BKV, sdesc_k_sw128(q_addr + off), sdesc_k_sw128(k_addr + off),
-                    idesc_s, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&k_empty[x]);
-        umma_commit(&s_full[x]);
-        return true;
+      // Each tcgen05.mma occupies the issuing thread for about as long as
+      // the tensor pipe needs to execute it, so everything between two MMAs
+      // costs tensor time: descriptors are formed once and advanced by
+      // constant offsets (the 14-bit start-address field never carries, as
+      // shared-memory addresses are below 256 KB), and the groups are fully
+      // unrolled.
+      const uint64_t dq = sdesc_k_sw128(smem_u32(sQ));
+      const uint64_t dkv = sdesc_k_sw128(smem_u32(sKV));
+      auto wait_load = [&](int i) {
+        return mbar_wait_bounded(&full[i % NS], static_cast<uint32_t>((i / NS) & 1), abort);
       };
-      for (int j = 0; ok && j < 2 && j < n_kv; ++j) ok = issue_s(j);
+      // S_t = Q_t K^T with K in stage s
+      auto mma_s = [&](int t, int s) {
+        const uint64_t a = dq + static_cast<uint64_t>((t * L::Q_TILE) >> 4);
+        const uint64_t b = dkv + static_cast<uint64_t>((s * L::KV_BYTES) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16(tS + t * BKV, a + (((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4),
+                    b + (((kk >> 2) * L::K_CHUNK + (kk & 3) * 32) >> 4), idesc_s,
+                    kk > 0 ? 1u : 0u);
+      };
+      // O_t += P_t V with V^T in stage s
+      auto mma_pv = [&](int t, int s, bool acc) {
+        const uint64_t b = dkv + static_cast<uint64_t>((s * L::KV_BYTES) >> 4);
+        const uint32_t first = acc ? 1u : 0u;
+#pragma unroll
+        for (int kk = 0; kk < BKV / 16; ++kk)
+          umma_bf16_tmem_a(tO + t * HD, tS + t * BKV + kk * 8,
+                           b + (((kk >> 2) * L::V_CHUNK + (kk & 3) * 32) >> 4), idesc_o,
+                           kk > 0 ? 1u : first);
+      };
+      bool ok = mbar_wait_bounded(q_full, 0, abort) && wait_load(0);
+      if (ok) {
+        tc_fence_after();
+        mma_s(0, 0);
+        umma_commit(&s_full[0]);
+        if (nt == 2) {
+          mma_s(1, 0);
+          umma_commit(&s_full[1]);
+        }
+        umma_commit(&empty[0]);
+      }
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int x = j & 1;
-        const uint32_t n = static_cast<uint32_t>(j >> 1);
-        if (j + 2 < n_kv && !(ok = issue_s(j + 2))) break;
-        if (!mbar_wait_bounded(&p_full[x], n & 1u, abort) ||
-            !mbar_wait_bounded(&v_full[x], n & 1u, abort)) {
+        const uint32_t par = static_cast<uint32_t>(j & 1);
+        const int iv = 2 * j + 1, ik = 2 * j + 2;
+        const bool more = j + 1 < n_kv;
+        if (!mbar_wait_bounded(&p_full[0], par, abort) || !wait_load(iv)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t p_addr = smem_u32(sP + x * L::P_BYTES);
-        const uint32_t v_addr = smem_u32(sV + x * L::V_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk)
-          umma_bf16(tO + x * HD, sdesc_k_sw128(p_addr + (kk >> 2) * L::P_CHUNK + (kk & 3) * 32),
-                    sdesc_k_sw128(v_addr + (kk >> 2) * L::V_CHUNK + (kk & 3) * 32), idesc_o,
-                    (j >= 2 || kk > 0) ? 1u : 0u);
-        umma_commit(&v_empty[x]);
-        umma_commit(&pv_done[x]);
+        mma_pv(0, iv % NS, j > 0);
+        if (nt == 1) umma_commit(&empty[iv % NS]);
+        if (more) {
+          if (!wait_load(ik)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_s(0, ik % NS);
+          umma_commit(&s_full[0]);
+          if (nt == 1) umma_commit(&empty[ik % NS]);
+        } else {
+          umma_commit(&o_done[0]);
+        }
+        if (nt == 1) continue;
+        if (!mbar_wait_bounded(&p_full[1], par, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        mma_pv(1, iv % NS, j > 0);
+        umma_commit(&empty[iv % NS]);
+        if (more) {
+          mma_s(1, ik % NS);
+          umma_commit(&empty[ik % NS]);
+          umma_commit(&s_full[1]);
+        } else {
+          umma_commit(&o_done[1]);
+        }
       }
       if (!ok) {
         att_fail(err, abort, DEV_TIMEOUT_MMA_FULL);
@@ -240,153 +309,111 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
         mbar_wait_bounded(drain, 0, &never);
       }
     }
-  } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
-    const int x = wg;                          // softmax set: 0 even tiles, 1 odd tiles
+  } else if (wg < nt) {
+    const int t = wg;                          // query tile of this warpgroup
     const int quad = warp & 3;
     const int row = quad * 32 + lane;          // query row in the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tSx = tS + x * BKV, tOx = tO + x * HD;
-    uint8_t* prow = sP + x * L::P_BYTES + row * 128;
+    const uint32_t tSt = tS + t * BKV + lane_off, tOt = tO + t * HD + lane_off;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    int last = -1;                             // last tile this set processed
-    for (int j = x; j < n_kv; j += 2) {
-      const uint32_t n = static_cast<uint32_t>(j >> 1);
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&s_full[x], n & 1u, abort))) {
+    for (int j = 0; j < n_kv; ++j) {
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait_bounded(&s_full[t], static_cast<uint32_t>(j & 1), abort))) {
         if (lane == 0) att_fail(err, abort, DEV_TIMEOUT_EPILOGUE);
         ok = false;
         break;
       }
       tc_fence_after();
-      // the whole S row into registers, then the S buffer is free for S_{j+2}
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tSx + c * 32 + lane_off, sr[c]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[x]);
       const int valid = tokens - j * BKV;      // keys of this tile that exist
-      if (valid < BKV) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i >= valid) sr[c][i] = __float_as_uint(-INFINITY);
-      }
-      float mx[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(sr[c][i]));
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
-                       scale_log2;
-      // PV_{j-2} must be done with this set's P tile (and O) before either
-      // is touched
-      if (last >= 0 &&
-          !__all_sync(0xffffffffu,
-                      mbar_wait_bounded(&pv_done[x], static_cast<uint32_t>((last >> 1) & 1),
-                                        abort))) {
-        if (lane == 0) att_fail(err, abort, DEV_TIMEOUT_EPILOGUE);
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (last < 0) {
-        m = mt;                                // the set's first tile fixes m
-      } else {
-        const bool need = mt > m + kGrowLimit;
-        if (__any_sync(0xffffffffu, need)) {
-          float corr = 1.f;
-          if (need) {
-            corr = ex2_approx(m - mt);
-            m = mt;
-            l *= corr;
-          }
+      if (j == 0) {
+        // the first KV tile fixes m: its row maximum, read chunk by chunk
+        float mx = -INFINITY;
 #pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t orr[32];
-            tmem_ld_32x32b_x32(tOx + c * 32 + lane_off, orr);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              orr[i] = __float_as_uint(__uint_as_float(orr[i]) * corr);
-            tmem_st_32x32b_x32(tOx + c * 32 + lane_off, orr);
-          }
-          tmem_st_wait();
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sr[32];
+          tmem_ld_32x32b_x32(tSt + c * 32, sr);
+          tmem_ld_wait();
+          mx = fmaxf(mx, masked_max(sr, valid - c * 32));
         }
+        m = mx * scale_log2;
       }
-      // P = exp2(s * scale - m) as bf16 into the swizzled P tile; row sum in
-      // eight independent partial sums
-      const float neg_m = -m;
+      // P = exp2(s * scale - m) as bf16 pairs over the first 64 columns of
+      // S_t, 32 scores at a time (chunk c of P lands on columns 16c..16c+15,
+      // which chunk c/2 of S, already read, occupied); the row sum in eight
+      // independent partial sums
       float ls[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) ls[e] = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32];
+        tmem_ld_32x32b_x32(tSt + c * 32, sr);
+        tmem_ld_wait();
+        const int vc = valid - c * 32;
+        if (vc < 32) {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        float p[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          p[e] = ex2_approx(fmaf(__uint_as_float(sr[c >> 2][(c & 3) * 8 + e]), scale_log2, neg_m));
-          ls[e] += p[e];
+          for (int i = 0; i < 32; ++i)
+            if (i >= vc) sr[i] = __float_as_uint(-INFINITY);
         }
-        const uint4 pk = make_uint4(pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]),
-                                    pack_bf16(p[4], p[5]), pack_bf16(p[6], p[7]));
-        const int cc = c & 7;
-        *reinterpret_cast<uint4*>(prow + (c >> 3) * L::P_CHUNK + ((cc ^ (row & 7)) << 4)) = pk;
+        if (j > 0) {
+          // a row whose scores outgrow m by more than kGrowLimit moves m up:
+          // O_t (PV_t(j-1) has completed: it precedes S_t(j) in issue
+          // order), l, this tile's partial sums and its P chunks so far are
+          // scaled by 2^(m_old - m_new)
+          const float cm = masked_max(sr, 32) * scale_log2;
+          const bool need = cm > m + kGrowLimit;
+          if (__any_sync(0xffffffffu, need)) {
+            tmem_st_wait();                    // P chunks so far are in TMEM
+            const float corr = need ? ex2_approx(m - cm) : 1.f;
+            if (need) m = cm;
+            l *= corr;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ls[e] *= corr;
+            rescale_tmem_f32<HD / 32>(tOt, corr);
+#pragma unroll 1
+            for (int pc = 0; pc < c; ++pc) rescale_tmem_bf16x2(tSt + pc * 16, corr);
+            tmem_st_wait();
+          }
+        }
+        const float neg_m = -m;
+        uint32_t pk[16];
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * h]), scale_log2, neg_m));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * h + 1]), scale_log2, neg_m));
+          ls[(2 * h) & 7] += p0;
+          ls[(2 * h + 1) & 7] += p1;
+          pk[h] = pack_bf16(p0, p1);
+        }
+        tmem_st_32x32b_x16(tSt + c * 16, pk);
       }
       l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[x]);
-      last = j;
+      if (lane == 0) mbar_arrive(&p_full[t]);
     }
-    // this set's last product, then the merge of the two sets through the
-    // (now idle) P tiles
-    if (ok && last >= 0 &&
-        !__all_sync(0xffffffffu,
-                    mbar_wait_bounded(&pv_done[x], static_cast<uint32_t>((last >> 1) & 1),
-                                      abort))) {
+    if (ok && !__all_sync(0xffffffffu, mbar_wait_bounded(&o_done[t], 0, abort))) {
       if (lane == 0) att_fail(err, abort, DEV_TIMEOUT_EPILOGUE);
       ok = false;
     }
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    float* xch = reinterpret_cast<float*>(sP);  // [set][row] m, then l
-    xch[x * 256 + row] = m;
-    xch[x * 256 + 128 + row] = l;
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    const float m0 = xch[row], l0 = xch[128 + row];
-    const float m1 = xch[256 + row], l1 = xch[384 + row];
-    const float mm = fmaxf(m0, m1);
-    const float c0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - mm);
-    const float c1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - mm);
-    const float inv = 1.f / (l0 * c0 + l1 * c1);
     if (ok && !*abort) {
       tc_fence_after();
-      const int t = q0 + row;
-      uint16_t* orow = o + (static_cast<int64_t>(b) * tokens + t) * d + head * HD;
+      const float inv = 1.f / l;
+      const int q = q0 + t * BQ + row;
+      uint16_t* orow = o + (static_cast<int64_t>(b) * tokens + q) * d + head * HD;
 #pragma unroll 1
-      for (int c = x * (HD / 64); c < (x + 1) * (HD / 64); ++c) {
-        uint32_t oa[32], ob[32];
-        tmem_ld_32x32b_x32(tO + c * 32 + lane_off, oa);
-        tmem_ld_32x32b_x32(tO + HD + c * 32 + lane_off, ob);
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t oa[32];
+        tmem_ld_32x32b_x32(tOt + c * 32, oa);
         tmem_ld_wait();
-        if (t < tokens) {
+        if (q < tokens) {
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             float v[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              // a set without tiles never wrote its O: leave it out entirely
-              const float va = c0 == 0.f ? 0.f : __uint_as_float(oa[8 * g + e]) * c0;
-              const float vb = c1 == 0.f ? 0.f : __uint_as_float(ob[8 * g + e]) * c1;
-              v[e] = (va + vb) * inv;
-            }
+            for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(oa[8 * g + e]) * inv;
             *reinterpret_cast<uint4*>(orow + c * 32 + 8 * g) =
                 make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
                            pack_bf16(v[6], v[7]));
@@ -427,16 +454,7 @@ transpose_v_kernel(const uint16_t* __restrict__ qkv, int tokens, int d, uint16_t
 }
 
 cudaError_t g_att_err = cudaSuccess;
-bool g_att_regs_ok = false;
 std::once_flag g_att_once;
-
-// The register split of the kernel (setmaxnreg: 128 threads down to 56,
-// 256 threads up to 224) needs the launch to hold 128*56 + 256*224 = 64512
-// registers, i.e. exactly 168 per thread for 384 threads; a smaller launch
-// allocation would leave setmaxnreg.inc waiting.  The launcher checks the
-// compiled count and refuses to launch otherwise.
-constexpr int kAttRegsPerThread = 168;
-static_assert(128 * 56 + 256 * 224 == ATT_THREADS * kAttRegsPerThread, "register split");
 
 void set_att_attrs() {
   std::call_once(g_att_once, [] {
@@ -447,11 +465,6 @@ void set_att_attrs() {
                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           AttLayout<128>::SMEM);
     g_att_err = e0 != cudaSuccess ? e0 : e1;
-    cudaFuncAttributes a64{}, a128{};
-    if (g_att_err == cudaSuccess) g_att_err = cudaFuncGetAttributes(&a64, attention_tc_kernel<64>);
-    if (g_att_err == cudaSuccess)
-      g_att_err = cudaFuncGetAttributes(&a128, attention_tc_kernel<128>);
-    g_att_regs_ok = a64.numRegs == kAttRegsPerThread && a128.numRegs == kAttRegsPerThread;
   });
 }
 
@@ -461,15 +474,16 @@ dlo_status launch_hd(const CUtensorMap& tm_qk, const CUtensorMap& tm_vt, int64_t
                      cudaStream_t stream) {
   set_att_attrs();
   DLO_CUDA(g_att_err);
-  if (!g_att_regs_ok)
-    DLO_FAIL(DLO_ERR_CUDA, "attention: kernel not compiled with %d registers per thread",
-             kAttRegsPerThread);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
-  dim3 grid(static_cast<unsigned>((tokens + BQ - 1) / BQ), static_cast<unsigned>(heads),
-            static_cast<unsigned>(batch));
+  // Two query tiles per CTA halve the K/V traffic per query; when that
+  // leaves SMs idle (fewer CTAs than SMs), one tile per CTA doubles the CTAs.
+  const int64_t pairs = (tokens + 2 * BQ - 1) / (2 * BQ);
+  const int nt = pairs * heads * batch >= sm_count() ? 2 : 1;
+  dim3 grid(static_cast<unsigned>((tokens + nt * BQ - 1) / (nt * BQ)),
+            static_cast<unsigned>(heads), static_cast<unsigned>(batch));
   attention_tc_kernel<HD><<<grid, ATT_THREADS, AttLayout<HD>::SMEM, stream>>>(
       tm_qk, tm_vt, static_cast<int>(tokens), static_cast<int>(d), static_cast<int>(heads), o,
-      scale_log2, err);
+      scale_log2, nt, err);
   DLO_CUDA(cudaGetLastError());
   return DLO_OK;
 }
@@ -481,9 +495,6 @@ int64_t vt_ld_for(int64_t tokens) { return (tokens + 7) / 8 * 8; }
 dlo_status attention_preload() {
   set_att_attrs();
   DLO_CUDA(g_att_err);
-  if (!g_att_regs_ok)
-    DLO_FAIL(DLO_ERR_CUDA, "attention: kernel not compiled with %d registers per thread",
-             kAttRegsPerThread);
   return DLO_OK;
 }
 

@@ -106,6 +106,9 @@ ATT_SHAPES = [
     (1, 333, 384, 3),
     (1, 2500, 256, 2),   # many KV tiles: rescaling path, hd 128
     (3, 129, 128, 2),    # three batch items, one key past a tile
+    # grids of at least one CTA per SM take two query tiles per CTA
+    (2, 1100, 2048, 16),  # hd 128, ragged last pair, second batch item
+    (1, 2000, 1216, 19),  # hd 64, last CTA's second tile partly past the end
 ]
 
 
