@@ -29,7 +29,8 @@
 // PV_t(j), so softmax t may then rescale O_t and overwrite P_t.
 // Softmax per tile: tcgen05.ld of the 128 scores, row maximum (a tile's
 // first KV tile fixes m; later ones keep it unless a row's scaled maximum
-// exceeds m by more than kGrowLimit, which rescales O_t and l), P =
+// exceeds m by more than kGrowLimit, which moves m up and rescales O_t, l
+// and the P chunks already written), P =
 // 2^(s*scale - m) as bf16 into TMEM with tcgen05.st, row sum l.  At the end
 // o = O_t / l.  Keys past the end are -inf in S and zero in V (TMA zero
 // fill).  All waits are bounded; a wait that runs out records a code in the
@@ -46,11 +47,18 @@ namespace {
 
 constexpr int BQ = 128, BKV = 128, ATT_THREADS = 384;
 constexpr uint32_t ATT_TMEM_COLS = 512;
-// A set keeps the maximum of its first tile until a row's scores exceed it
-// by more than this (log2 units): P then stays below 2^64, far from the
-// fp32 and bf16 range limits (without loss of relative precision), and O
-// needs no rescaling in the common case.
+// A query tile keeps the row maximum m of its first KV tile until a row's
+// scaled scores exceed it by more than this (log2 units): P then stays below
+// 2^64, far from the fp32 and bf16 range limits (without loss of relative
+// precision), and O needs no rescaling in the common case.
 constexpr float kGrowLimit = 64.f;
+// Of every 8 score pairs, this many take 2^x from the polynomial on the FMA
+// pipes and the rest from the MUFU: the MUFU alone (16 per clock per SM)
+// would take about as long as the tensor products of a tile.
+#ifndef ATT_POLY_PAIRS
+#define ATT_POLY_PAIRS 0
+#endif
+constexpr int kPolyPairs = ATT_POLY_PAIRS;
 
 template <int HD>
 struct AttLayout {
@@ -71,8 +79,7 @@ __device__ __forceinline__ void att_fail(int* err, volatile int* abort, int code
 }
 
 // 2^x by the hardware approximation (MUFU.EX2 through the PTX instruction;
-// denormal results flush to zero, 2^-inf = 0).  Inputs here are at most
-// kGrowLimit.
+// denormal results flush to zero, 2^-inf = 0).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -82,6 +89,61 @@ __device__ __forceinline__ float ex2_approx(float x) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// Packed pairs of fp32 (Blackwell's paired FMA/add pipes): lane 0 in the
+// low 32 bits.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float f2_hi(uint64_t v) {
+  return __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// 2^x for a pair on the FMA pipes instead of the MUFU: x = n + f with
+// n = round(x) (adding and removing 1.5 * 2^23 leaves round(x) in the low
+// mantissa bits), 2^f from a cubic in f on [-1/2, 1/2] whose coefficients
+// minimise the largest relative error (7.5e-5 in fp32 evaluation, well under
+// the bf16 half-ulp of P; exp2_poly.py beside this file derives them), and n
+// added to the exponent field.  x is first clamped to >= -126 so that the
+// exponent field cannot wrap below zero (the result for anything smaller is
+// at most 2^-126, a stand-in for 0 next to the row's maximum of 1); callers
+// keep x <= 64.
+__device__ __forceinline__ uint64_t exp2_poly_pair(uint64_t x) {
+  x = f2(fmaxf(f2_lo(x), -126.f), fmaxf(f2_hi(x), -126.f));
+  const uint64_t magic = 0x4B4000004B400000ull;      // 1.5 * 2^23, both lanes
+  const uint64_t t = f2_add(x, magic);
+  const uint64_t f = f2_sub(x, f2_sub(t, magic));
+  uint64_t p = f2_fma(f2(5.517166853e-02f, 5.517166853e-02f), f,
+                      f2(2.426111251e-01f, 2.426111251e-01f));
+  p = f2_fma(p, f, f2(6.932609677e-01f, 6.932609677e-01f));
+  p = f2_fma(p, f, f2(9.999280572e-01f, 9.999280572e-01f));
+  const uint32_t lo = static_cast<uint32_t>(p) + (static_cast<uint32_t>(t) << 23);
+  const uint32_t hi = static_cast<uint32_t>(p >> 32) + (static_cast<uint32_t>(t >> 32) << 23);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
 // Maximum of the first n (clamped to 0..32) of 32 fp32 scores; -inf if none.
@@ -340,11 +402,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
       }
       // P = exp2(s * scale - m) as bf16 pairs over the first 64 columns of
       // S_t, 32 scores at a time (chunk c of P lands on columns 16c..16c+15,
-      // which chunk c/2 of S, already read, occupied); the row sum in eight
-      // independent partial sums
-      float ls[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ls[e] = 0.f;
+      // which chunk c/2 of S, already read, occupied); the row sum in four
+      // packed pairs of partial sums
+      uint64_t ls[4] = {0, 0, 0, 0};
+      const uint64_t sc2 = f2(scale_log2, scale_log2);
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t sr[32];
@@ -368,27 +429,33 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
             const float corr = need ? ex2_approx(m - cm) : 1.f;
             if (need) m = cm;
             l *= corr;
+            const uint64_t corr2 = f2(corr, corr);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ls[e] *= corr;
+            for (int e = 0; e < 4; ++e) ls[e] = f2_mul(ls[e], corr2);
             rescale_tmem_f32<HD / 32>(tOt, corr);
 #pragma unroll 1
             for (int pc = 0; pc < c; ++pc) rescale_tmem_bf16x2(tSt + pc * 16, corr);
             tmem_st_wait();
           }
         }
-        const float neg_m = -m;
+        const uint64_t nm2 = f2(-m, -m);
         uint32_t pk[16];
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * h]), scale_log2, neg_m));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * h + 1]), scale_log2, neg_m));
-          ls[(2 * h) & 7] += p0;
-          ls[(2 * h + 1) & 7] += p1;
-          pk[h] = pack_bf16(p0, p1);
+          const uint64_t x = f2_fma(f2(__uint_as_float(sr[2 * h]), __uint_as_float(sr[2 * h + 1])),
+                                    sc2, nm2);
+          uint64_t pp;
+          if ((h & 7) < kPolyPairs)
+            pp = exp2_poly_pair(x);
+          else
+            pp = f2(ex2_approx(f2_lo(x)), ex2_approx(f2_hi(x)));
+          ls[h & 3] = f2_add(ls[h & 3], pp);
+          pk[h] = pack_bf16(f2_lo(pp), f2_hi(pp));
         }
         tmem_st_32x32b_x16(tSt + c * 16, pk);
       }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      const uint64_t l2 = f2_add(f2_add(ls[0], ls[1]), f2_add(ls[2], ls[3]));
+      l += f2_lo(l2) + f2_hi(l2);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();

@@ -65,18 +65,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete yet is
+// suspended until it completes or about hint_ns pass, so that waiting warps
+// leave the issue slots of their SM sub-partition to the warps that work.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of `bar` with the given parity to complete.  Returns
-// false if *abort becomes non-zero or the wait exceeds kWaitTimeoutNs.
+// false if *abort becomes non-zero or the wait exceeds kWaitTimeoutNs.  The
+// waiting thread sleeps in 20-microsecond slices (the hardware wakes it when
+// the phase completes), so a role that sets *abort is seen within one slice.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
-    }
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
   }
 }
 
