@@ -409,6 +409,7 @@ def run_ours(args, ws, rank, local):
         "copy_ms_distribution": copy_dist, "pretouch_s": pretouch_s,
         "host_huge_page_fraction": host.buf.huge_fraction(),
         "host_huge_ranges_used_fraction": host.buf.good_fraction(),
+        "host_range_survey": host.buf.survey_summary(),
         "copy_ms_all": copy_ms if args.dump_copies else None,
         "roofline": {"name": copy_name, "bound": "h2d", "achieved": achieved,
                      "peak": ceiling, "unit": "GB/s",

@@ -73,6 +73,9 @@ class PinnedBuffer:
         self.ptr = _round_up(base, _HUGE)
         self.offset = self.ptr - base
         self.good = []                  # per prepared 512 MiB range
+        self.rate = []                  # per range: surveyed H2D GB/s, or None
+        self.fast = []                  # per range: None (not surveyed) or bool
+        self.segments = []              # registered [first, end) range spans
         self._cursor = 0
         self._t = None
         self.registered = False
@@ -100,6 +103,8 @@ class PinnedBuffer:
                     ok = True
                     break
             self.good.append(ok)
+            self.rate.append(None)
+            self.fast.append(None)
 
     def place(self, sizes, align=256):
         """Offsets (from .ptr) for pieces of the given sizes, in order.
@@ -155,19 +160,143 @@ class PinnedBuffer:
         return offs
 
     def register(self):
-        nbytes = self.capacity if self.small else len(self.good) * _HUGE
+        """Registers the prepared ranges not registered yet (all of them on the
+        first call) with the CUDA driver as one segment."""
         rt = torch.cuda.cudart()
-        self._reg_ptr = self.ptr
-        err = rt.cudaHostRegister(self.ptr, nbytes, 1 | 2)   # portable | mapped
+        if self.small:
+            start, nbytes = 0, self.capacity
+        else:
+            first = self.segments[-1][1] if self.segments else 0
+            start, nbytes = first * _HUGE, (len(self.good) - first) * _HUGE
+            if nbytes <= 0:
+                return
+        err = rt.cudaHostRegister(self.ptr + start, nbytes, 1 | 2)   # portable | mapped
         code = err.value if hasattr(err, "value") else int(err)
         if code != 0:
             raise RuntimeError("cudaHostRegister of %d bytes failed (%d)" % (nbytes, code))
+        if not self.small:
+            self.segments.append((start // _HUGE, len(self.good)))
+        self._reg_ptrs = getattr(self, "_reg_ptrs", []) + [self.ptr + start]
         self.registered = True
-        self.registered_bytes = nbytes
-        self._t = torch.frombuffer(self._map, dtype=torch.uint8)
+        self.registered_bytes += nbytes
+        if self._t is None:
+            self._t = torch.frombuffer(self._map, dtype=torch.uint8)
+
+    def survey(self, min_frac=0.6, device="cuda"):
+        """Times a 512 MiB host->device copy of every registered huge-page
+        range not surveyed yet, on the second of two passes over all of them
+        (so every range is timed after the others' copies, as in a streaming
+        loop, and after its own first-access costs), and marks as slow the
+        ranges below min_frac of the median rate.
+
+        Why: on some GB300 hosts a part of the huge-page ranges streams to the
+        GPU at a few GB/s in steady state while the rest reaches the link
+        rate (211 GB/s), though all are physically contiguous and in the same
+        memory zone; a block placed there stalls every step it is read in."""
+        todo = [r for seg in self.segments for r in range(*seg)
+                if self.good[r] and self.fast[r] is None]
+        if not todo:
+            return
+        dst = torch.empty(_HUGE, dtype=torch.uint8, device=device)
+        s = torch.cuda.Stream(device=device)
+        for rep in range(2):
+            evs = []
+            with torch.cuda.stream(s):
+                for r in todo:
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(s)
+                    dst.copy_(self.view(r * _HUGE, _HUGE), non_blocking=True)
+                    e1.record(s)
+                    evs.append((r, e0, e1))
+            s.synchronize()
+        for r, e0, e1 in evs:
+            self.rate[r] = _HUGE / (e0.elapsed_time(e1) * 1e6)
+        rates = sorted(x for x in self.rate if x is not None)
+        ref = rates[len(rates) // 2]
+        for r in todo:
+            self.fast[r] = self.rate[r] >= min_frac * ref
+        del dst
+
+    def place_surveyed(self, sizes, align=256, min_frac=0.6):
+        """Offsets (from .ptr) for pieces of the given sizes, placed only in
+        runs of huge-page ranges that streamed at the link rate in a survey
+        (see survey()) and never across a registration segment.  Ranges are
+        prepared, registered and surveyed in rounds until the fast ones hold
+        every piece; if the reservation runs out first, the remaining pieces
+        go to any registered space.  Registers as it goes (no register()
+        afterwards)."""
+        if self.small:
+            offs = self.place(sizes, align)
+            self.register()
+            return offs
+        sizes = [int(n) for n in sizes]
+        need = sum(_round_up(n, align) for n in sizes)
+        want = -(-need // _HUGE) + len(sizes) // 16 + 2
+        n_ranges = self.capacity // _HUGE
+        while True:
+            usable = sum(1 for r, f in enumerate(self.fast) if f and self.good[r])
+            short = want - usable
+            if short > 0 and len(self.good) < n_ranges:
+                self._prepare(min(n_ranges, len(self.good) + short))
+                self.register()
+                self.survey(min_frac)
+                continue
+            offs = self._fit(sizes, align)
+            if offs is not None or len(self.good) >= n_ranges:
+                break
+            want += max(2, want // 8)
+        if offs is None:
+            offs = self._fit(sizes, align, any_range=True)
+        if offs is None:
+            raise MemoryError("PinnedBuffer: the pieces do not fit")
+        return offs
+
+    def _fit(self, sizes, align, any_range=False):
+        """First-fit of the pieces into runs of usable ranges inside one
+        registration segment each; None if some piece finds no room."""
+        def usable(r):
+            return any_range or (self.good[r] and self.fast[r])
+        offs = []
+        taken = []                          # (start, end) byte spans handed out
+        for n in sizes:
+            found = None
+            for a, b in self.segments:
+                pos = a * _HUGE
+                while pos + n <= b * _HUGE:
+                    pos = _round_up(pos, align)
+                    first, last = pos // _HUGE, (pos + n - 1) // _HUGE
+                    if last >= b:
+                        break
+                    bad = [r for r in range(first, last + 1) if not usable(r)]
+                    if bad:
+                        pos = (bad[-1] + 1) * _HUGE
+                        continue
+                    clash = [e for s, e in taken if s < pos + n and e > pos]
+                    if clash:
+                        pos = max(clash)
+                        continue
+                    found = pos
+                    break
+                if found is not None:
+                    break
+            if found is None:
+                return None
+            offs.append(found)
+            taken.append((found, found + n))
+        return offs
 
     def view(self, offset, nbytes):
         return self._t[self.offset + offset:self.offset + offset + nbytes]
+
+    def survey_summary(self):
+        """Counts and rates of the surveyed ranges (None if none were)."""
+        rates = [x for x in self.rate if x is not None]
+        if not rates:
+            return None
+        rates.sort()
+        return {"ranges": len(rates), "slow": sum(1 for f in self.fast if f is False),
+                "median_gbs": rates[len(rates) // 2], "min_gbs": rates[0]}
 
     def good_fraction(self):
         """Fraction of the prepared 512 MiB ranges backed by a huge page
@@ -200,7 +329,9 @@ class PinnedBuffer:
 
     def close(self):
         if self.registered:
-            torch.cuda.cudart().cudaHostUnregister(self._reg_ptr)
+            for p in getattr(self, "_reg_ptrs", []):
+                torch.cuda.cudart().cudaHostUnregister(p)
+            self._reg_ptrs = []
             self.registered = False
         if self._map is not None:
             self._t = None
@@ -232,9 +363,10 @@ class HostBlocks:
         s = w.shards
         self.strides = [_round_up(g.shard_alloc_bytes, 256) for g in self.groups]
         piece = [s * st for st in self.strides]
-        self.buf = PinnedBuffer(w.distinct * sum(_round_up(p, 256) for p in piece), defer=True)
-        where = self.buf.place([piece[g] for _ in range(w.distinct)
-                                for g in range(len(self.groups))])
+        self.buf = PinnedBuffer(w.distinct * sum(_round_up(p, 256) for p in piece), spare=0.5,
+                                defer=True)
+        where = self.buf.place_surveyed([piece[g] for _ in range(w.distinct)
+                                         for g in range(len(self.groups))])
         self.offsets = []                  # [hb][g * s + r] offsets from buf.ptr
         for hb in range(w.distinct):
             offs = []
@@ -242,7 +374,6 @@ class HostBlocks:
                 o = where[hb * len(self.groups) + g]
                 offs += [o + r * st for r in range(s)]
             self.offsets.append(offs)
-        self.buf.register()
         self.params = [] if keep_params else None
         for hb in range(w.distinct):
             if params is not None:
