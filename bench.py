@@ -62,6 +62,8 @@ def parse():
                     choices=["linear", "fc2", "attention", "norm", "copy", "forward"],
                     help="run one kernel of the workload's block `--reps` times (for ncu)")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--layout", default="dit", choices=["dit", "mxfp8", "int8"],
+                    help="with --only copy: the block's linears as bf16 (dit) or in a 1-byte layout")
     ap.add_argument("--sweep", action="store_true",
                     help="run the transfer-vs-compute sweep (36 cells), one JSON line per cell")
     ap.add_argument("--sweep-d", default="1664,3328,6656")
@@ -466,6 +468,8 @@ def run_only(args):
         z = torch.zeros(d, device=dev)
         h = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
         fn = lambda: dlo.op_rmsnorm_mod(x, M, d, g, z, z, 1e-6, h, s)
+    elif args.only == "copy" and args.layout != "dit":
+        return run_copy_layout(args, w)
     else:
         host = HostBlocks(w, seed=args.seed, gen_device="cuda")
         if args.only == "copy":
@@ -489,6 +493,55 @@ def run_only(args):
     assert dlo.kernel_status() == 0
     print(json.dumps({"only": args.only, "config": args.config, "reps": args.reps,
                       "ms_per_rep": e0.elapsed_time(e1) / args.reps}), flush=True)
+
+
+def run_copy_layout(args, w):
+    """Reassembly of one block whose linears are in a 1-byte layout (fp8 +
+    e8m0 block scales, or int8 + fp32 row scales; some weights transposed
+    views): random bytes in surveyed pinned shards, both copy modes timed
+    over `reps` prefetch-sized reassemblies each."""
+    import numpy as np
+    import torch
+    from layerwise_weight_offload_gb300 import dlo, workloads as W
+    from layerwise_weight_offload_gb300.stack import PinnedBuffer
+    descs = W.block_param_descs_quantized(w, args.layout)
+    plan = dlo.Plan(descs, w.shards)
+    groups = plan.groups()
+    sizes = [g.shard_alloc_bytes for g in groups for _ in range(w.shards)]
+    buf = PinnedBuffer(sum(-(-n // 256) * 256 for n in sizes), spare=0.5, defer=True)
+    offs = buf.place_surveyed(sizes)
+    ptrs = [buf.ptr + o for o in offs]
+    rng = np.random.default_rng(args.seed)
+    srcs = []
+    for p in range(plan.info().n_params):
+        pi = plan.param(p)
+        srcs.append(rng.integers(0, 256, size=pi.storage_numel * dlo.ESIZE[pi.dtype],
+                                 dtype=np.uint8))
+    plan.shard_host([x.ctypes.data for x in srcs], ptrs)
+    nbytes = sum(g.shard_bytes * w.shards for g in groups)
+    dst = torch.empty(plan.info().slot_bytes, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    ceiling = h2d_ceiling_gbs(torch)
+    res = {}
+    for name, mode in (("dma", dlo.COPY_DMA), ("kernel", dlo.COPY_KERNEL)):
+        for _ in range(2):
+            dlo.reassemble(plan, ptrs, dst, mode, s)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(args.reps):
+            dlo.reassemble(plan, ptrs, dst, mode, s)
+        e1.record(s)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.reps
+        res[name] = {"ms_per_block": ms, "gbs": nbytes / (ms * 1e6),
+                     "frac_of_ceiling": nbytes / (ms * 1e6) / ceiling}
+    assert dlo.kernel_status() == 0
+    print(json.dumps({"only": "copy", "config": args.config, "layout": args.layout,
+                      "shards": w.shards, "bytes_per_block": nbytes,
+                      "groups": [(g.dtype, g.shard_bytes) for g in groups],
+                      "h2d_ceiling_gbs": ceiling, "reps": args.reps, **res}), flush=True)
+    buf.close()
 
 
 def run_sweep(args):

@@ -57,7 +57,22 @@ typedef enum {
   DLO_ERR_NOMEM = 5     /* a caller-provided buffer is too small */
 } dlo_status;
 
-typedef enum { DLO_BF16 = 0, DLO_F32 = 1 } dlo_dtype;
+/* Element types of parameters.  Every distinct code forms its own dtype
+ * group (its own flat buffer and shards), so an 8-bit weight and its 8-bit
+ * block scales travel as two groups.  The 1-byte codes cover the layouts the
+ * pages' online quantisation keeps ("Request and loading constraints": an
+ * int8 weight with an fp32 scale, an fp8 weight with an e8m0 block scale);
+ * the library moves their bytes and interprets none of them. */
+typedef enum {
+  DLO_BF16 = 0,
+  DLO_F32 = 1,
+  DLO_F16 = 2,
+  DLO_FP8_E4M3 = 3,
+  DLO_FP8_E5M2 = 4,
+  DLO_I8 = 5,
+  DLO_U8 = 6,
+  DLO_E8M0 = 7   /* 8-bit power-of-two block scale */
+} dlo_dtype;
 
 /* How a prefetch moves the shards host->device.
  *   DMA:    copy engines, no SMs: per dtype group one cudaMemcpy2DAsync
@@ -83,8 +98,17 @@ typedef enum { DLO_COPY_AUTO = 0, DLO_COPY_DMA = 1, DLO_COPY_KERNEL = 2 } dlo_co
 typedef struct {
   const char* name;     /* parameter name, copied by dlo_plan_create */
   int32_t ndim;         /* 1..4 */
-  int64_t shape[4];     /* row-major; shape[ndim-1] is contiguous */
+  int64_t shape[4];     /* logical extents */
   int32_t dtype;        /* dlo_dtype */
+  int64_t stride[4];    /* element strides of the view over its storage, each
+                           >= 0; all 0 means row-major contiguous.  A strided
+                           view (e.g. a transposed finalized weight) is packed
+                           in physical order: the plan moves its storage
+                           extent, 1 + sum_i (shape[i]-1)*stride[i] elements
+                           starting at element [0,..,0], and the device-side
+                           view is the same strides over the slot copy
+                           (reading of "physical-order packing", "Request and
+                           loading constraints") */
 } dlo_param_desc;
 
 typedef struct dlo_plan dlo_plan;
@@ -112,9 +136,13 @@ typedef struct {
 typedef struct {
   int32_t group;            /* index into the plan's groups */
   int32_t dtype;
-  int64_t numel;
+  int64_t numel;            /* logical elements (product of the extents) */
   int64_t group_offset;     /* element offset inside the flat group */
   int64_t slot_offset;      /* byte offset inside a slot (base + offset*esize) */
+  int64_t storage_numel;    /* elements packed for it (its storage extent;
+                               numel for a contiguous parameter) */
+  int64_t stride[4];        /* element strides of the device-side view
+                               (row-major ones for a contiguous parameter) */
 } dlo_param_info;
 
 /* Builds the layout of one block.  Parameters of one dtype are concatenated
@@ -124,9 +152,15 @@ typedef struct {
  * appearance, each at a 256-byte aligned base, each occupying
  * n_shards * S_g elements (the gathered buffer, padding included).
  * n_shards >= 1 (1 is the rank-local path of [D5]).  *out is owned by the
- * caller and released with dlo_plan_destroy.
+ * caller and released with dlo_plan_destroy.  Parameters of different
+ * blocks may differ in number, names, dtypes and sizes (heterogeneous
+ * blocks): each block has its own plan, and an engine's slots must hold the
+ * largest.  has_dit_roles is set when all twelve DiT parameter names are
+ * present with the dtypes the block forward reads (bf16 linears, f32
+ * vectors) and contiguous layouts.
  * Errors: DLO_ERR_INVALID on null pointers, n_params < 1, ndim outside 1..4,
- * a non-positive extent, an unknown dtype, or n_shards < 1. */
+ * a non-positive extent, a negative stride, an unknown dtype, or
+ * n_shards < 1. */
 dlo_status dlo_plan_create(const dlo_param_desc* params, int32_t n_params,
                            int32_t n_shards, dlo_plan** out);
 dlo_status dlo_plan_query(const dlo_plan* plan, dlo_plan_info* out);
@@ -134,7 +168,8 @@ dlo_status dlo_plan_group(const dlo_plan* plan, int32_t group, dlo_group_info* o
 dlo_status dlo_plan_param(const dlo_plan* plan, int32_t param, dlo_param_info* out);
 
 /* CPU flatten / pad / split ([B2] §2, the rank-r copy window).
- * param_src[p]: host pointer to parameter p's contiguous data (n_params
+ * param_src[p]: host pointer to parameter p's element [0,..,0]; its
+ *   storage_numel elements are read from there in memory order (n_params
  *   entries, in plan order).
  * shard_dst[g * n_shards + r]: host buffer of at least shard_alloc_bytes for
  *   group g, shard r (pinned memory for the stream to use it; any memory is

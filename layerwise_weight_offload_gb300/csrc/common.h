@@ -59,7 +59,10 @@ struct dlo_plan {
     int32_t ndim;
     int64_t shape[4];
     int32_t dtype;
-    int64_t numel;
+    int64_t numel;          // logical elements
+    int64_t stride[4];      // element strides of the view (row-major if contiguous)
+    bool contiguous;
+    int64_t storage_numel;  // elements packed: the view's storage extent
     int32_t group;
     int64_t group_offset;   // elements
     int64_t slot_offset;    // bytes

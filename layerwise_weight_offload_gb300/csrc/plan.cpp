@@ -46,8 +46,19 @@ static int32_t esize_of(int32_t dtype) {
   switch (dtype) {
     case DLO_BF16: return 2;
     case DLO_F32: return 4;
+    case DLO_F16: return 2;
+    case DLO_FP8_E4M3:
+    case DLO_FP8_E5M2:
+    case DLO_I8:
+    case DLO_U8:
+    case DLO_E8M0: return 1;
     default: return 0;
   }
+}
+
+// dtype the block forward reads for each DiT role
+static int32_t role_dtype(int r) {
+  return (r == R_WQKV || r == R_WO || r == R_W1 || r == R_W2) ? DLO_BF16 : DLO_F32;
 }
 
 }  // namespace dlo
@@ -82,13 +93,26 @@ dlo_status dlo_plan_create(const dlo_param_desc* params, int32_t n_params,
     q.dtype = d.dtype;
     q.numel = 1;
     for (int i = 0; i < 4; ++i) q.shape[i] = i < d.ndim ? d.shape[i] : 1;
+    bool given = false;
     for (int i = 0; i < d.ndim; ++i) {
-      if (d.shape[i] <= 0) {
+      if (d.shape[i] <= 0 || d.stride[i] < 0) {
         delete plan;
-        DLO_FAIL(DLO_ERR_INVALID, "dlo_plan_create: param %d has extent %lld", p,
-                 (long long)d.shape[i]);
+        DLO_FAIL(DLO_ERR_INVALID, "dlo_plan_create: param %d has extent %lld / stride %lld", p,
+                 (long long)d.shape[i], (long long)d.stride[i]);
       }
       q.numel *= d.shape[i];
+      given = given || d.stride[i] != 0;
+    }
+    // row-major strides of the logical shape
+    int64_t rm[4] = {0, 0, 0, 0};
+    for (int i = d.ndim - 1; i >= 0; --i) rm[i] = i == d.ndim - 1 ? 1 : rm[i + 1] * d.shape[i + 1];
+    q.contiguous = true;
+    q.storage_numel = 1;
+    for (int i = 0; i < 4; ++i) q.stride[i] = 0;
+    for (int i = 0; i < d.ndim; ++i) {
+      q.stride[i] = given ? d.stride[i] : rm[i];
+      q.storage_numel += (d.shape[i] - 1) * q.stride[i];
+      if (d.shape[i] > 1 && q.stride[i] != rm[i]) q.contiguous = false;
     }
     // group by dtype, in order of first appearance
     int32_t g = -1;
@@ -103,7 +127,7 @@ dlo_status dlo_plan_create(const dlo_param_desc* params, int32_t n_params,
     }
     q.group = g;
     q.group_offset = plan->groups[g].numel;
-    plan->groups[g].numel += q.numel;
+    plan->groups[g].numel += q.storage_numel;
     plan->params.push_back(q);
   }
   int64_t cursor = 0;
@@ -117,12 +141,16 @@ dlo_status dlo_plan_create(const dlo_param_desc* params, int32_t n_params,
   plan->slot_bytes = cursor;
   for (auto& q : plan->params)
     q.slot_offset = plan->groups[q.group].base + q.group_offset * plan->groups[q.group].esize;
-  // DiT roles, by name
+  // DiT roles, by name; a role counts only with the dtype and the contiguous
+  // layout the block forward reads
   bool all = true;
   for (int r = 0; r < R_COUNT; ++r) {
     plan->role[r] = -1;
-    for (size_t p = 0; p < plan->params.size(); ++p)
-      if (plan->params[p].name == kRoleNames[r]) plan->role[r] = static_cast<int32_t>(p);
+    for (size_t p = 0; p < plan->params.size(); ++p) {
+      const auto& q = plan->params[p];
+      if (q.name == kRoleNames[r] && q.dtype == role_dtype(r) && q.contiguous)
+        plan->role[r] = static_cast<int32_t>(p);
+    }
     if (plan->role[r] < 0) all = false;
   }
   plan->has_dit_roles = all;
@@ -167,6 +195,8 @@ dlo_status dlo_plan_param(const dlo_plan* plan, int32_t param, dlo_param_info* o
   out->numel = q.numel;
   out->group_offset = q.group_offset;
   out->slot_offset = q.slot_offset;
+  out->storage_numel = q.storage_numel;
+  for (int i = 0; i < 4; ++i) out->stride[i] = q.stride[i];
   return DLO_OK;
 }
 
@@ -192,7 +222,7 @@ dlo_status dlo_shard_host(const dlo_plan* plan, const void* const* param_src,
     const auto& grp = plan->groups[q.group];
     const uint8_t* src = static_cast<const uint8_t*>(param_src[&q - plan->params.data()]);
     int64_t flat = q.group_offset;         // element index in the flat group
-    int64_t left = q.numel;
+    int64_t left = q.storage_numel;        // storage extent, in memory order
     while (left > 0) {
       const int64_t r = flat / grp.shard_numel;
       const int64_t in_shard = flat - r * grp.shard_numel;

@@ -15,7 +15,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libdlo.so")
 
 OK, ERR_INVALID, ERR_CUDA, ERR_TIMEOUT, ERR_STATE, ERR_NOMEM = range(6)
-BF16, F32 = 0, 1
+BF16, F32, F16, FP8_E4M3, FP8_E5M2, I8, U8, E8M0 = 0, 1, 2, 3, 4, 5, 6, 7
+ESIZE = {BF16: 2, F32: 4, F16: 2, FP8_E4M3: 1, FP8_E5M2: 1, I8: 1, U8: 1, E8M0: 1}
 COPY_AUTO, COPY_DMA, COPY_KERNEL = 0, 1, 2
 EPI_BF16, EPI_GELU_BF16, EPI_RESID_F32 = 0, 1, 2
 COPY_MODE_NAMES = {COPY_AUTO: "auto", COPY_DMA: "dma", COPY_KERNEL: "kernel"}
@@ -33,7 +34,7 @@ c_i32, c_i64, c_vp, c_sz, c_f32 = (ctypes.c_int32, ctypes.c_int64, ctypes.c_void
 
 class ParamDesc(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char_p), ("ndim", c_i32), ("shape", c_i64 * 4),
-                ("dtype", c_i32)]
+                ("dtype", c_i32), ("stride", c_i64 * 4)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -48,7 +49,7 @@ class GroupInfo(ctypes.Structure):
 
 class ParamInfo(ctypes.Structure):
     _fields_ = [("group", c_i32), ("dtype", c_i32), ("numel", c_i64), ("group_offset", c_i64),
-                ("slot_offset", c_i64)]
+                ("slot_offset", c_i64), ("storage_numel", c_i64), ("stride", c_i64 * 4)]
 
 
 class DitCfg(ctypes.Structure):
@@ -179,14 +180,21 @@ def version():
 
 class Plan:
     def __init__(self, descs, n_shards):
-        """descs: sequence of (name, shape, dtype code) in registration order."""
+        """descs: sequence of (name, shape, dtype code) or (name, shape, dtype
+        code, element strides) in registration order; no strides (or all 0)
+        means row-major contiguous."""
         self._names = [d[0].encode() for d in descs]
         arr = (ParamDesc * len(descs))()
-        for i, (name, shape, code) in enumerate(descs):
+        for i, d in enumerate(descs):
+            name, shape, code = d[:3]
+            strides = d[3] if len(d) > 3 else None
             arr[i].name = self._names[i]
             arr[i].ndim = len(shape)
             for j, v in enumerate(shape):
                 arr[i].shape[j] = int(v)
+            if strides is not None:
+                for j, v in enumerate(strides):
+                    arr[i].stride[j] = int(v)
             arr[i].dtype = int(code)
         h = c_vp()
         _check(lib().dlo_plan_create(arr, len(descs), int(n_shards), ctypes.byref(h)),

@@ -22,6 +22,7 @@ from dataclasses import dataclass, replace
 import torch
 
 BF16, F32 = 0, 1          # dtype codes of the C ABI
+FP8_E4M3, I8, E8M0 = 3, 5, 7
 ESIZE = {BF16: 2, F32: 4}
 TORCH_DTYPE = {BF16: torch.bfloat16, F32: torch.float32}
 
@@ -100,6 +101,31 @@ def block_param_descs(w: Workload):
         ("ada2.scale", (d,), F32), ("ada2.gate", (d,), F32),
         ("mlp.fc1.weight", (f, d), BF16), ("mlp.fc2.weight", (d, f), BF16),
     ]
+
+
+def block_param_descs_quantized(w: Workload, kind: str):
+    """The same block with its four linears kept in a 1-byte layout, as
+    online quantisation finalizes them ([D5] "Request and loading
+    constraints"): kind "mxfp8" is an fp8 (e4m3) weight with one e8m0 scale
+    per 32 weights along the input dimension, "int8" an int8 weight with one
+    fp32 scale per output row.  The QKV and fc1 weights are given as
+    transposed views ([in, out] storage seen as [out, in]), the others
+    contiguous; the f32 vectors are unchanged.  Shapes only: these blocks are
+    moved and reassembled, not computed with."""
+    out = []
+    for name, shape, code in block_param_descs(w):
+        if code != BF16:
+            out.append((name, shape, code))
+            continue
+        o, i = shape
+        transposed = name in ("attn.qkv.weight", "mlp.fc1.weight")
+        wcode = FP8_E4M3 if kind == "mxfp8" else I8
+        out.append((name, shape, wcode, (1, o)) if transposed else (name, shape, wcode))
+        if kind == "mxfp8":
+            out.append((name + ".scale", (o, i // 32), E8M0))
+        else:
+            out.append((name + ".scale", (o,), F32))
+    return out
 
 
 def _generator(device, seed, block, index):

@@ -23,6 +23,8 @@ def lib():
         i32, i64, vp, dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_double
         L.oracle_shard_numel.restype = i64
         L.oracle_shard_numel.argtypes = [i64, i32]
+        L.oracle_storage_extent.restype = i64
+        L.oracle_storage_extent.argtypes = [i32, vp, vp]
         L.oracle_flatten_group.restype = i64
         L.oracle_flatten_group.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         L.oracle_shard.restype = None
@@ -69,6 +71,13 @@ def default_threads():
 
 def shard_numel(total_numel, dp_size):
     return int(lib().oracle_shard_numel(total_numel, dp_size))
+
+
+def storage_extent(shape, strides):
+    """Elements packed for a view of these extents and element strides."""
+    sh = np.asarray(shape, dtype=np.int64)
+    st = np.asarray(strides, dtype=np.int64)
+    return int(lib().oracle_storage_extent(len(sh), _ptr(sh), _ptr(st)))
 
 
 def flatten_group(params, dtype_code, esize):

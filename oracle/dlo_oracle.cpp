@@ -50,6 +50,19 @@ extern "C" {
 // rank r holding the flat window [r*S, (r+1)*S).
 // ---------------------------------------------------------------------------
 
+// Storage extent, in elements, of a view with the given extents and element
+// strides.  [D5] "Request and loading constraints": finalized 1-byte weights
+// and their scales may be contiguous or transposed views, and they are
+// packed in physical order.  Reading: the packed elements of a view are its
+// storage from element [0,..,0] through its last element in memory, i.e.
+// 1 + sum_i (shape_i - 1) * stride_i (strides >= 0); for row-major strides
+// that is the element count.
+int64_t oracle_storage_extent(int32_t ndim, const int64_t* shape, const int64_t* stride) {
+  int64_t last = 0;
+  for (int32_t i = 0; i < ndim; ++i) last += (shape[i] - 1) * stride[i];
+  return last + 1;
+}
+
 int64_t oracle_shard_numel(int64_t total_numel, int32_t dp_size) {
   if (dp_size <= 0 || total_numel < 0) return -1;
   return (total_numel + dp_size - 1) / dp_size;

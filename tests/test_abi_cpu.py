@@ -28,13 +28,34 @@ def test_library_exports_every_header_symbol():
 
 
 def _descs_random(rng, n_params):
+    """Parameters of every dtype code; some are strided views (transposed or
+    with gaps), given with their element strides."""
     descs = []
     for i in range(n_params):
-        code = int(rng.integers(0, 2))
-        ndim = int(rng.integers(1, 3))
+        code = int(rng.integers(0, 8))
+        ndim = int(rng.integers(1, 4))
         shape = tuple(int(v) for v in rng.integers(1, 9, size=ndim))
-        descs.append(("p%d" % i, shape, code))
+        kind = int(rng.integers(0, 3))
+        if kind == 0 or ndim == 1:
+            descs.append(("p%d" % i, shape, code))
+        elif kind == 1:                  # a row-major [.., b, a] tensor seen as [.., a, b]
+            a_, b_ = shape[-2], shape[-1]
+            st = [int(np.prod(shape[j + 1:])) for j in range(ndim)]
+            st[-2], st[-1] = 1, a_
+            descs.append(("p%d" % i, shape, code, tuple(st)))
+        else:                            # row-major with a padded leading stride
+            rm = [int(np.prod(shape[j + 1:])) for j in range(ndim)]
+            st = list(rm)
+            st[0] = rm[0] + int(rng.integers(1, 5))
+            descs.append(("p%d" % i, shape, code, tuple(st)))
     return descs
+
+
+def _storage(desc):
+    shape = desc[1]
+    if len(desc) > 3:
+        return oracle.storage_extent(shape, desc[3])
+    return int(np.prod(shape))
 
 
 @pytest.mark.parametrize("seed", range(40))
@@ -44,9 +65,9 @@ def test_plan_layout_and_shards_match_oracle(seed):
     s = int(rng.integers(1, 9))
     plan = dlo.Plan(descs, s)
     info = plan.info()
-    numels = [int(np.prod(sh)) for _, sh, _ in descs]
-    codes = [c for _, _, c in descs]
-    esizes = [W.ESIZE[c] for c in codes]
+    numels = [_storage(d) for d in descs]          # elements packed per parameter
+    codes = [d[2] for d in descs]
+    esizes = [dlo.ESIZE[c] for c in codes]
     raw = [rng.integers(0, 256, size=n * e, dtype=np.uint8) for n, e in zip(numels, esizes)]
     image, gdt, gbase, used = oracle.slot_image(raw, numels, codes, esizes, s, 256)
     assert info.slot_bytes == used
@@ -69,8 +90,27 @@ def test_plan_layout_and_shards_match_oracle(seed):
     # the parameter views: offsets inside the oracle's slot image
     for p in range(len(descs)):
         pi = plan.param(p)
+        assert pi.storage_numel == numels[p]
+        assert pi.numel == int(np.prod(descs[p][1]))
+        if len(descs[p]) > 3:
+            assert tuple(pi.stride[:len(descs[p][1])]) == tuple(descs[p][3])
         n = numels[p] * esizes[p]
         assert np.array_equal(image[pi.slot_offset:pi.slot_offset + n], raw[p])
+
+
+def test_role_contract_needs_dtype_and_layout():
+    w = W.CONFIGS["tiny"]
+    descs = W.block_param_descs(w)
+    assert dlo.Plan(descs, 2).info().has_dit_roles == 1
+    # a transposed fc1 weight, or an fp8 one, is moved but not a DiT role
+    i = [d[0] for d in descs].index("mlp.fc1.weight")
+    f, d = descs[i][1]
+    t = list(descs)
+    t[i] = (descs[i][0], (f, d), W.BF16, (1, f))
+    assert dlo.Plan(t, 2).info().has_dit_roles == 0
+    q = list(descs)
+    q[i] = (descs[i][0], (f, d), dlo.FP8_E4M3)
+    assert dlo.Plan(q, 2).info().has_dit_roles == 0
 
 
 @pytest.mark.parametrize("name", ["tiny", "odd", "nano", "super", "sweep-d1664-t256-s8"])
@@ -97,9 +137,12 @@ def test_bad_arguments_fail_closed():
     arr[0].name = b"x"
     arr[0].ndim = 1
     arr[0].shape[0] = 4
-    arr[0].dtype = 7
+    arr[0].dtype = 8                                   # no such dtype code
     assert L.dlo_plan_create(arr, 1, 2, ctypes.byref(out)) == dlo.ERR_INVALID
     arr[0].dtype = 0
+    arr[0].stride[0] = -1                              # negative stride
+    assert L.dlo_plan_create(arr, 1, 2, ctypes.byref(out)) == dlo.ERR_INVALID
+    arr[0].stride[0] = 0
     assert L.dlo_plan_create(arr, 1, 0, ctypes.byref(out)) == dlo.ERR_INVALID
     arr[0].shape[0] = 0
     assert L.dlo_plan_create(arr, 1, 1, ctypes.byref(out)) == dlo.ERR_INVALID

@@ -383,3 +383,53 @@ def test_block_rows_equals_full_block_on_listed_rows():
     rows = [0, 5, 8, 9, 17]
     part = oracle.block_forward_rows(x, p, rows, 2, t, d, 4, f, threads=3)
     assert np.array_equal(part, full[rows])
+
+
+# ---- strided views packed in physical order ([D5] "Request and loading
+# constraints") ------------------------------------------------------------
+
+def _random_view(rng):
+    ndim = int(rng.integers(1, 5))
+    shape = [int(v) for v in rng.integers(1, 6, size=ndim)]
+    strides = [int(v) for v in rng.integers(0, 40, size=ndim)]
+    return shape, strides
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_storage_extent_matches_numpy_byte_bounds(seed):
+    # independent pin: numpy's own bounds of an as_strided view over a buffer
+    rng = np.random.default_rng(seed)
+    shape, strides = _random_view(rng)
+    base = np.zeros(4096, dtype=np.uint8)
+    view = np.lib.stride_tricks.as_strided(base, shape=shape, strides=strides)
+    lo, hi = np.lib.array_utils.byte_bounds(view)
+    assert oracle.storage_extent(shape, strides) == hi - lo
+
+
+def test_storage_extent_of_contiguous_and_transposed():
+    assert oracle.storage_extent([7, 5], [5, 1]) == 35
+    assert oracle.storage_extent([5, 7], [1, 5]) == 35           # its transpose
+    assert oracle.storage_extent([3, 4, 2], [8, 2, 1]) == 24
+    assert oracle.storage_extent([6], [3]) == 16                  # every third
+    assert oracle.storage_extent([4, 3], [0, 1]) == 3             # broadcast rows
+
+
+@pytest.mark.parametrize("esize", [1, 2, 4])
+def test_transposed_view_survives_physical_order_packing(esize):
+    # pack the storage of a transposed view, shard and reassemble it, then the
+    # same strides over the gathered bytes give the view back
+    rng = np.random.default_rng(esize)
+    a = rng.integers(0, 256, size=(9, 13 * esize), dtype=np.uint8)    # [m, n] rows
+    m, n = 9, 13
+    t_shape, t_strides = (n, m), (1, n)                                 # elements
+    ext = oracle.storage_extent(t_shape, t_strides)
+    assert ext == m * n
+    flat = oracle.flatten_group([(a.reshape(-1), ext, 5)], 5, esize)
+    for s in (1, 2, 3, 5):
+        shards = oracle.shard(flat, ext, esize, s)
+        gathered = oracle.reassemble(shards, oracle.shard_numel(ext, s), esize)
+        back = np.lib.stride_tricks.as_strided(
+            gathered, shape=(n, m, esize),
+            strides=(t_strides[0] * esize, t_strides[1] * esize, 1))
+        want = a.reshape(m, n, esize).transpose(1, 0, 2)
+        assert np.array_equal(back, want)
