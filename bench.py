@@ -44,7 +44,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default=DEFAULT_CONFIG)
-    ap.add_argument("--copy-mode", default="auto", choices=["auto", "dma", "kernel"])
+    ap.add_argument("--copy-mode", default="auto", choices=["auto", "dma", "kernel", "staged"])
     ap.add_argument("--copy-ctas", type=int, default=0)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
@@ -245,7 +245,8 @@ def run_ours(args, ws, rank, local):
 
     torch.cuda.set_device(local)
     w = W.CONFIGS[args.config]
-    mode = {"auto": dlo.COPY_AUTO, "dma": dlo.COPY_DMA, "kernel": dlo.COPY_KERNEL}[args.copy_mode]
+    mode = {"auto": dlo.COPY_AUTO, "dma": dlo.COPY_DMA, "kernel": dlo.COPY_KERNEL,
+            "staged": dlo.COPY_STAGED}[args.copy_mode]
     bf16_peak, bf16_sust, hbm_peak, peak_src = measured_peaks()
     ceiling = h2d_ceiling_gbs(torch)
 
@@ -386,7 +387,9 @@ def run_ours(args, ws, rank, local):
                "sample": "%d fp64 oracle block forward(s) of host block 0 of %s in %.1f s; "
                          "the oracle's reassembly is not included" % (n, w.name, el)}
 
-    copy_name = "copy_reassemble_kernel" if chosen == "kernel" else "cudaMemcpyAsync (copy engines)"
+    copy_name = {"kernel": "copy_reassemble_kernel",
+                 "staged": "cudaMemcpyAsync into staging (copy engines), then a device gather"}.get(
+        chosen, "cudaMemcpyAsync (copy engines)")
     achieved = (sum(copy_bytes) / len(copy_bytes)) / (statistics.mean(copy_ms) * 1e6) \
         if copy_ms else None
     line = {

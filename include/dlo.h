@@ -88,8 +88,22 @@ typedef enum {
  *           pinned host shards with 16-byte loads and writes them to their
  *           final slot offsets (SMs read over the host link).
  *   AUTO:   the first prefetches alternate between the two under the real
- *           workload, timed with events; the faster per byte is then kept. */
-typedef enum { DLO_COPY_AUTO = 0, DLO_COPY_DMA = 1, DLO_COPY_KERNEL = 2 } dlo_copy_mode;
+ *           workload, timed with events; the faster per byte is then kept.
+ *   STAGED: the two-phase form of [B1] "Weight Sharding + AllGather" steps
+ *           1-2 ([B2] §3: H2D on copy_stream, AllGather on comm_stream): the
+ *           shards first land, by DMA, in a device staging buffer laid out
+ *           shard by shard (group g, shard r at stage_base_g + r *
+ *           shard_alloc_bytes); then a device-to-device copy-and-reassemble
+ *           kernel on a second ("gather") stream writes them to their slot
+ *           offsets, which is what all_gather_into_tensor produces.  Needs
+ *           the engine's staging buffers and gather stream.  Never chosen by
+ *           AUTO. */
+typedef enum {
+  DLO_COPY_AUTO = 0,
+  DLO_COPY_DMA = 1,
+  DLO_COPY_KERNEL = 2,
+  DLO_COPY_STAGED = 3
+} dlo_copy_mode;
 
 /* ------------------------------------------------------------------------
  * Plan: the per-block layout ([B1] "Weight Sharding + AllGather"; [B2] §2).
@@ -120,6 +134,9 @@ typedef struct {
   int32_t has_dit_roles;/* 1 if the names match the synthetic DiT block */
   int64_t slot_bytes;   /* bytes a slot needs for this block */
   int64_t group_align;  /* byte alignment of each group's base in a slot (256) */
+  int64_t staging_bytes;/* bytes a staging buffer needs for this block in
+                           DLO_COPY_STAGED (groups shard by shard, each shard
+                           at a 16-byte aligned offset) */
 } dlo_plan_info;
 
 typedef struct {
@@ -131,6 +148,9 @@ typedef struct {
   int64_t shard_alloc_bytes;/* shard_bytes rounded up to 16: required size of
                                every host shard buffer of this group */
   int64_t base;             /* byte offset of the gathered group in a slot */
+  int64_t stage_base;       /* byte offset of the group's first shard in a
+                               staging buffer (256-byte aligned); shard r at
+                               stage_base + r * shard_alloc_bytes */
 } dlo_group_info;
 
 typedef struct {
@@ -191,6 +211,21 @@ void dlo_plan_destroy(dlo_plan* plan);
  * Asynchronous; the shard memory must stay valid until the stream passes. */
 dlo_status dlo_reassemble(const dlo_plan* plan, const void* const* shard_ptrs,
                           void* dst, int32_t mode, void* stream);
+
+/* One-shot staged reassembly (the DLO_COPY_STAGED phases, [B2] §3): the
+ * shards move host->device into `staging` by DMA on copy_stream, then a
+ * device-to-device copy-and-reassemble kernel on gather_stream (which waits
+ * for the first phase through an event) writes `dst` laid out as a slot.
+ * shard_ptrs: as in dlo_reassemble (page-locked; mapping not needed).
+ * staging: device buffer of at least plan staging_bytes, 256-byte aligned.
+ * dst: device buffer of at least plan slot_bytes, 256-byte aligned.
+ * copy_stream and gather_stream may be the same stream.  Asynchronous; the
+ * shards and staging must stay valid until gather_stream passes.
+ * Errors: DLO_ERR_INVALID on null or misaligned pointers or a staging
+ * buffer smaller than staging_bytes; DLO_ERR_CUDA on a CUDA failure. */
+dlo_status dlo_reassemble_staged(const dlo_plan* plan, const void* const* shard_ptrs,
+                                 void* staging, int64_t staging_bytes, void* dst,
+                                 void* copy_stream, void* gather_stream);
 
 /* ------------------------------------------------------------------------
  * Synthetic DiT block (the block the stream feeds; the pages do not define
@@ -321,6 +356,17 @@ typedef struct {
                              back before the ready event; 0 = default (1:
                              every copy on the copy stream, which measured
                              faster on GB300 than spreading them) */
+  void* staging[2];       /* DLO_COPY_STAGED only: device staging buffers,
+                             256-byte aligned, caller-owned; staging[x] serves
+                             the prefetches into slot x.  Null otherwise. */
+  int64_t staging_bytes;  /* capacity of each staging buffer (>= every
+                             registered block's plan staging_bytes) */
+  void* gather_stream;    /* DLO_COPY_STAGED only: cudaStream_t of the
+                             device-to-device phase; differs from the other
+                             two streams.  The H2D into staging[x] waits only
+                             for the gather that last read staging[x]; the
+                             gather waits for the H2D and for the slot's free
+                             event, and records the slot's ready event. */
 } dlo_engine_desc;
 
 typedef struct {

@@ -75,11 +75,13 @@ struct dlo_plan {
     int64_t shard_bytes;
     int64_t shard_alloc_bytes;
     int64_t base;
+    int64_t stage_base;     // first shard's offset in a staging buffer
   };
   std::vector<Param> params;
   std::vector<Group> groups;
   int32_t n_shards = 1;
   int64_t slot_bytes = 0;
+  int64_t staging_bytes = 0;
   int32_t role[dlo::R_COUNT];   // param index per role, -1 if absent
   bool has_dit_roles = false;
   uint64_t id = 0;              // unique per plan (keys cached graphs)

@@ -83,6 +83,14 @@ struct dlo_engine {
   cudaEvent_t race_ev[8] = {};
   bool race_rec[8] = {false, false, false, false, false, false, false, false};
   int32_t chosen = -1;               // DLO_COPY_DMA / DLO_COPY_KERNEL once decided
+  // DLO_COPY_STAGED: caller-owned staging buffers (staging[x] serves slot x)
+  // and gather stream; staged[x] marks the H2D into staging[x] done,
+  // stage_free[x] the gather out of it
+  uint8_t* staging[2] = {nullptr, nullptr};
+  int64_t staging_bytes = 0;
+  cudaStream_t gather = nullptr;
+  cudaEvent_t staged[2] = {nullptr, nullptr};
+  cudaEvent_t stage_free[2] = {nullptr, nullptr};
   double race_dma_us = 0, race_kernel_us = 0;
   int64_t n_prefetches = 0;
   int64_t n_kernel_prefetches = 0;
@@ -255,6 +263,60 @@ dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, in
   return join_side();
 }
 
+// DLO_COPY_STAGED, phase 1 (the H2D of [B2] §3): every shard host->device
+// by DMA into the staging buffer, shard by shard — group g, shard r at
+// stage_base_g + r * shard_alloc_bytes (16-byte aligned).  A group whose
+// host shards sit at a constant stride moves as one 2-D copy (one linear
+// copy when that stride equals the staging stride).
+dlo_status stage_h2d(const dlo_engine::Block& b, uint8_t* staging, cudaStream_t stream) {
+  const dlo_plan* p = b.plan;
+  const int32_t s = p->n_shards;
+  for (size_t g = 0; g < p->groups.size(); ++g) {
+    const auto& grp = p->groups[g];
+    uint8_t* d0 = staging + grp.stage_base;
+    const int64_t sp = grp.shard_alloc_bytes;
+    const int64_t hp = b.pitch.empty() ? 0 : b.pitch[g];
+    if (hp == sp) {
+      DLO_CUDA(cudaMemcpyAsync(d0, b.host[g * s], static_cast<size_t>(sp) * s,
+                               cudaMemcpyHostToDevice, stream));
+    } else if (hp > 0) {
+      DLO_CUDA(cudaMemcpy2DAsync(d0, static_cast<size_t>(sp), b.host[g * s],
+                                 static_cast<size_t>(hp), static_cast<size_t>(grp.shard_bytes),
+                                 static_cast<size_t>(s), cudaMemcpyHostToDevice, stream));
+    } else {
+      for (int32_t r = 0; r < s; ++r)
+        DLO_CUDA(cudaMemcpyAsync(d0 + static_cast<int64_t>(r) * sp, b.host[g * s + r],
+                                 static_cast<size_t>(grp.shard_bytes), cudaMemcpyHostToDevice,
+                                 stream));
+    }
+  }
+  return DLO_OK;
+}
+
+// DLO_COPY_STAGED, phase 2 (the AllGather of [B2] §3 on one device): the
+// copy-and-reassemble kernel moves every staged shard to its slot offset
+// (group base + r * shard_bytes), i.e. the concatenation in rank order that
+// all_gather_into_tensor produces.
+dlo_status stage_gather(const dlo_plan* p, const uint8_t* staging, uint8_t* dst, int ctas,
+                        cudaStream_t stream) {
+  const int32_t s = p->n_shards;
+  SegmentTable t;
+  t.n = 0;
+  for (size_t g = 0; g < p->groups.size(); ++g) {
+    const auto& grp = p->groups[g];
+    for (int32_t r = 0; r < s; ++r) {
+      if (t.n >= kMaxSegments)
+        DLO_FAIL(DLO_ERR_INVALID, "staged gather: more than %d (group, shard) pieces",
+                 kMaxSegments);
+      Segment& sg = t.seg[t.n++];
+      sg.src = staging + grp.stage_base + static_cast<int64_t>(r) * grp.shard_alloc_bytes;
+      sg.dst = dst + grp.base + static_cast<int64_t>(r) * grp.shard_bytes;
+      sg.bytes = grp.shard_bytes;
+    }
+  }
+  return launch_copy_reassemble(t, ctas, stream);
+}
+
 // AUTO: decide once the four window-edge events have completed
 // (non-blocking).
 void try_decide(dlo_engine* e) {
@@ -305,6 +367,30 @@ dlo_status enqueue_prefetch(dlo_engine* e, int32_t block, int32_t slot, int64_t 
   const dlo_engine::Block& b = e->blocks[block];
   const int32_t mode = mode_for(e, issued_by_k, b);
   if (used_mode) *used_mode = mode;
+  if (mode == DLO_COPY_STAGED) {
+    // H2D into staging[slot] once the gather that last read it is done;
+    // the gather then waits for the H2D and for the slot's free event
+    DLO_CUDA(cudaStreamWaitEvent(e->copy, e->stage_free[slot], 0));
+    dlo_engine::Timed t{};
+    if (e->timing) {
+      DLO_TRY(make_timed(&t));
+      t.bytes = b.bytes;
+      t.mode = mode;
+      e->timed.push_back(t);
+      DLO_CUDA(cudaEventRecord(t.a, e->copy));
+    }
+    DLO_TRY(stage_h2d(b, e->staging[slot], e->copy));
+    if (e->timing) DLO_CUDA(cudaEventRecord(t.b, e->copy));
+    DLO_CUDA(cudaEventRecord(e->staged[slot], e->copy));
+    DLO_CUDA(cudaStreamWaitEvent(e->gather, e->staged[slot], 0));
+    DLO_CUDA(cudaStreamWaitEvent(e->gather, e->freed[slot], 0));
+    DLO_TRY(stage_gather(b.plan, e->staging[slot], e->slot[slot], e->copy_ctas, e->gather));
+    DLO_CUDA(cudaEventRecord(e->stage_free[slot], e->gather));
+    DLO_CUDA(cudaEventRecord(e->ready[slot], e->gather));
+    e->slot_holds[slot] = block;
+    e->n_prefetches++;
+    return DLO_OK;
+  }
   DLO_CUDA(cudaStreamWaitEvent(e->copy, e->freed[slot], 0));
   dlo_engine::Timed t{};
   if (e->timing) {
@@ -339,6 +425,8 @@ void release(dlo_engine* e) {
   for (int s = 0; s < 2; ++s) {
     if (e->ready[s]) cudaEventDestroy(e->ready[s]);
     if (e->freed[s]) cudaEventDestroy(e->freed[s]);
+    if (e->staged[s]) cudaEventDestroy(e->staged[s]);
+    if (e->stage_free[s]) cudaEventDestroy(e->stage_free[s]);
   }
   for (auto& t : e->timed) {
     cudaEventDestroy(t.a);
@@ -373,8 +461,20 @@ dlo_status dlo_engine_create(const dlo_engine_desc* d, dlo_engine** out) {
   if (d->slot_bytes <= 0) DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: slot_bytes must be > 0");
   if (d->compute_stream == d->copy_stream)
     DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: compute and copy streams must differ");
-  if (d->copy_mode < DLO_COPY_AUTO || d->copy_mode > DLO_COPY_KERNEL)
+  if (d->copy_mode < DLO_COPY_AUTO || d->copy_mode > DLO_COPY_STAGED)
     DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: unknown copy mode %d", d->copy_mode);
+  if (d->copy_mode == DLO_COPY_STAGED) {
+    if (!d->staging[0] || !d->staging[1] || d->staging[0] == d->staging[1] ||
+        d->staging_bytes <= 0)
+      DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: staged copies need two staging buffers");
+    if ((reinterpret_cast<uintptr_t>(d->staging[0]) |
+         reinterpret_cast<uintptr_t>(d->staging[1])) & 255u)
+      DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: staging buffers must be 256-byte aligned");
+    if (!d->gather_stream || d->gather_stream == d->copy_stream ||
+        d->gather_stream == d->compute_stream)
+      DLO_FAIL(DLO_ERR_INVALID,
+               "dlo_engine_create: staged copies need a gather stream of their own");
+  }
   if (d->dma_streams < 0 || d->dma_streams > dlo_engine::kMaxFan)
     DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: dma_streams must be 0..%d",
              dlo_engine::kMaxFan);
@@ -391,6 +491,12 @@ dlo_status dlo_engine_create(const dlo_engine_desc* d, dlo_engine** out) {
   e->copy_ctas = d->copy_ctas;
   e->timing = d->timing != 0;
   e->fan = d->dma_streams == 0 ? 1 : d->dma_streams;
+  if (d->copy_mode == DLO_COPY_STAGED) {
+    e->staging[0] = static_cast<uint8_t*>(d->staging[0]);
+    e->staging[1] = static_cast<uint8_t*>(d->staging[1]);
+    e->staging_bytes = d->staging_bytes;
+    e->gather = static_cast<cudaStream_t>(d->gather_stream);
+  }
   e->blocks.resize(d->n_blocks);
   e->hooks.resize(d->n_blocks);
   for (int32_t i = 0; i < d->n_blocks; ++i) e->hooks[i] = {i % 2, -1};
@@ -401,6 +507,11 @@ dlo_status dlo_engine_create(const dlo_engine_desc* d, dlo_engine** out) {
          cudaEventCreateWithFlags(&e->freed[s], cudaEventDisableTiming) == cudaSuccess;
   for (int i = 0; i < 2 * kRaceWindows; ++i)
     ok = ok && cudaEventCreate(&e->race_ev[i]) == cudaSuccess;
+  if (e->gather)
+    for (int s = 0; s < 2; ++s)
+      ok = ok &&
+           cudaEventCreateWithFlags(&e->staged[s], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&e->stage_free[s], cudaEventDisableTiming) == cudaSuccess;
   ok = ok && cudaStreamCreateWithFlags(&e->side, cudaStreamNonBlocking) == cudaSuccess &&
        cudaEventCreateWithFlags(&e->side_fork, cudaEventDisableTiming) == cudaSuccess &&
        cudaEventCreateWithFlags(&e->side_join, cudaEventDisableTiming) == cudaSuccess;
@@ -431,6 +542,10 @@ dlo_status dlo_register_block(dlo_engine* e, int32_t block, const dlo_plan* plan
   if (plan->slot_bytes > e->slot_bytes)
     DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block: block needs %lld bytes, slots hold %lld",
              (long long)plan->slot_bytes, (long long)e->slot_bytes);
+  if (e->gather && plan->staging_bytes > e->staging_bytes)
+    DLO_FAIL(DLO_ERR_INVALID,
+             "dlo_register_block: block needs %lld staging bytes, staging holds %lld",
+             (long long)plan->staging_bytes, (long long)e->staging_bytes);
   const size_t n = plan->groups.size() * static_cast<size_t>(plan->n_shards);
   if (n > static_cast<size_t>(kMaxSegments))
     DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block: %zu (group, shard) pieces, at most %d", n,
@@ -647,37 +762,45 @@ dlo_status dlo_engine_copy_times(dlo_engine* e, float* copy_ms, int64_t* copy_by
 dlo_status dlo_engine_destroy(dlo_engine* e, int32_t timeout_ms) {
   using namespace dlo;
   if (!e) return DLO_OK;
-  // drain both streams (bounded): mark their current tails and poll
-  cudaEvent_t tail[2] = {nullptr, nullptr};
-  cudaStream_t st[2] = {e->copy, e->compute};
-  for (int i = 0; i < 2; ++i) {
-    DLO_CUDA(cudaEventCreateWithFlags(&tail[i], cudaEventDisableTiming));
-    DLO_CUDA(cudaEventRecord(tail[i], st[i]));
+  // drain the streams (bounded): mark their current tails and poll
+  cudaEvent_t tail[3] = {nullptr, nullptr, nullptr};
+  cudaStream_t st[3] = {e->copy, e->compute, e->gather};
+  const int n = e->gather ? 3 : 2;
+  auto drop = [&]() {
+    for (int i = 0; i < n; ++i)
+      if (tail[i]) cudaEventDestroy(tail[i]);
+  };
+  for (int i = 0; i < n; ++i) {
+    if (cudaEventCreateWithFlags(&tail[i], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventRecord(tail[i], st[i]) != cudaSuccess) {
+      drop();
+      DLO_FAIL(DLO_ERR_CUDA, "dlo_engine_destroy: cannot mark the stream tails");
+    }
   }
   const auto t0 = std::chrono::steady_clock::now();
   for (;;) {
-    const cudaError_t q0 = cudaEventQuery(tail[0]);
-    const cudaError_t q1 = cudaEventQuery(tail[1]);
-    if (q0 == cudaSuccess && q1 == cudaSuccess) break;
-    if ((q0 != cudaSuccess && q0 != cudaErrorNotReady) ||
-        (q1 != cudaSuccess && q1 != cudaErrorNotReady)) {
-      cudaEventDestroy(tail[0]);
-      cudaEventDestroy(tail[1]);
-      DLO_FAIL(DLO_ERR_CUDA, "dlo_engine_destroy: stream error while draining");
+    bool done = true;
+    for (int i = 0; i < n; ++i) {
+      const cudaError_t q = cudaEventQuery(tail[i]);
+      if (q == cudaErrorNotReady) {
+        done = false;
+      } else if (q != cudaSuccess) {
+        drop();
+        DLO_FAIL(DLO_ERR_CUDA, "dlo_engine_destroy: stream error while draining");
+      }
     }
+    if (done) break;
     const auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(
                         std::chrono::steady_clock::now() - t0)
                         .count();
     if (ms >= timeout_ms) {
-      cudaEventDestroy(tail[0]);
-      cudaEventDestroy(tail[1]);
+      drop();
       DLO_FAIL(DLO_ERR_TIMEOUT, "dlo_engine_destroy: streams not drained after %d ms",
                timeout_ms);
     }
     std::this_thread::sleep_for(std::chrono::microseconds(100));
   }
-  cudaEventDestroy(tail[0]);
-  cudaEventDestroy(tail[1]);
+  drop();
   release(e);
   return DLO_OK;
 }
@@ -709,10 +832,49 @@ dlo_status dlo_reassemble(const dlo_plan* plan, const void* const* shard_ptrs, v
       b.dev[i] = a.devicePointer;
     }
   }
+  if (mode == DLO_COPY_STAGED)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_reassemble: staged copies go through dlo_reassemble_staged");
   const int32_t m = mode == DLO_COPY_KERNEL ? DLO_COPY_KERNEL : DLO_COPY_DMA;
   compute_pitches(&b);
   return copy_block(b, static_cast<uint8_t*>(dst), m, 0, static_cast<cudaStream_t>(stream), 1,
                     nullptr, nullptr, nullptr);
+}
+
+dlo_status dlo_reassemble_staged(const dlo_plan* plan, const void* const* shard_ptrs,
+                                 void* staging, int64_t staging_bytes, void* dst,
+                                 void* copy_stream, void* gather_stream) {
+  using namespace dlo;
+  if (!plan || !shard_ptrs || !staging || !dst)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_reassemble_staged: null argument");
+  if ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(staging)) & 255u)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_reassemble_staged: dst and staging must be 256-byte aligned");
+  if (staging_bytes < plan->staging_bytes)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_reassemble_staged: staging holds %lld bytes, needs %lld",
+             (long long)staging_bytes, (long long)plan->staging_bytes);
+  const size_t n = plan->groups.size() * static_cast<size_t>(plan->n_shards);
+  if (n > static_cast<size_t>(kMaxSegments))
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_reassemble_staged: too many (group, shard) pieces");
+  dlo_engine::Block b;
+  b.plan = plan;
+  b.host.assign(shard_ptrs, shard_ptrs + n);
+  for (size_t i = 0; i < n; ++i)
+    if (!shard_ptrs[i] || (reinterpret_cast<uintptr_t>(shard_ptrs[i]) & 15u))
+      DLO_FAIL(DLO_ERR_INVALID, "dlo_reassemble_staged: shard %zu null or not 16-byte aligned",
+               i);
+  compute_pitches(&b);
+  const cudaStream_t cs = static_cast<cudaStream_t>(copy_stream);
+  const cudaStream_t gs = static_cast<cudaStream_t>(gather_stream);
+  DLO_TRY(stage_h2d(b, static_cast<uint8_t*>(staging), cs));
+  if (gs != cs) {
+    cudaEvent_t ev = nullptr;
+    DLO_CUDA(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+    const cudaError_t e1 = cudaEventRecord(ev, cs);
+    const cudaError_t e2 = e1 == cudaSuccess ? cudaStreamWaitEvent(gs, ev, 0) : e1;
+    cudaEventDestroy(ev);   // released once the recorded work completes
+    DLO_CUDA(e2);
+  }
+  return stage_gather(plan, static_cast<const uint8_t*>(staging), static_cast<uint8_t*>(dst), 0,
+                      gs);
 }
 
 }  // extern "C"

@@ -130,15 +130,19 @@ dlo_status dlo_plan_create(const dlo_param_desc* params, int32_t n_params,
     plan->groups[g].numel += q.storage_numel;
     plan->params.push_back(q);
   }
-  int64_t cursor = 0;
+  int64_t cursor = 0, stage_cursor = 0;
   for (auto& grp : plan->groups) {
     grp.shard_numel = (grp.numel + n_shards - 1) / n_shards;
     grp.shard_bytes = grp.shard_numel * grp.esize;
     grp.shard_alloc_bytes = round_up(grp.shard_bytes, 16);
     grp.base = round_up(cursor, kGroupAlign);
     cursor = grp.base + static_cast<int64_t>(n_shards) * grp.shard_bytes;
+    // staging (DLO_COPY_STAGED): shard by shard, every shard 16-byte aligned
+    grp.stage_base = round_up(stage_cursor, kGroupAlign);
+    stage_cursor = grp.stage_base + static_cast<int64_t>(n_shards) * grp.shard_alloc_bytes;
   }
   plan->slot_bytes = cursor;
+  plan->staging_bytes = stage_cursor;
   for (auto& q : plan->params)
     q.slot_offset = plan->groups[q.group].base + q.group_offset * plan->groups[q.group].esize;
   // DiT roles, by name; a role counts only with the dtype and the contiguous
@@ -167,6 +171,7 @@ dlo_status dlo_plan_query(const dlo_plan* plan, dlo_plan_info* out) {
   out->has_dit_roles = plan->has_dit_roles ? 1 : 0;
   out->slot_bytes = plan->slot_bytes;
   out->group_align = dlo::kGroupAlign;
+  out->staging_bytes = plan->staging_bytes;
   return DLO_OK;
 }
 
@@ -182,6 +187,7 @@ dlo_status dlo_plan_group(const dlo_plan* plan, int32_t group, dlo_group_info* o
   out->shard_bytes = g.shard_bytes;
   out->shard_alloc_bytes = g.shard_alloc_bytes;
   out->base = g.base;
+  out->stage_base = g.stage_base;
   return DLO_OK;
 }
 

@@ -17,9 +17,10 @@ _LIB_PATH = os.path.join(_PKG, "libdlo.so")
 OK, ERR_INVALID, ERR_CUDA, ERR_TIMEOUT, ERR_STATE, ERR_NOMEM = range(6)
 BF16, F32, F16, FP8_E4M3, FP8_E5M2, I8, U8, E8M0 = 0, 1, 2, 3, 4, 5, 6, 7
 ESIZE = {BF16: 2, F32: 4, F16: 2, FP8_E4M3: 1, FP8_E5M2: 1, I8: 1, U8: 1, E8M0: 1}
-COPY_AUTO, COPY_DMA, COPY_KERNEL = 0, 1, 2
+COPY_AUTO, COPY_DMA, COPY_KERNEL, COPY_STAGED = 0, 1, 2, 3
 EPI_BF16, EPI_GELU_BF16, EPI_RESID_F32 = 0, 1, 2
-COPY_MODE_NAMES = {COPY_AUTO: "auto", COPY_DMA: "dma", COPY_KERNEL: "kernel"}
+COPY_MODE_NAMES = {COPY_AUTO: "auto", COPY_DMA: "dma", COPY_KERNEL: "kernel",
+                   COPY_STAGED: "staged"}
 
 
 class DLOError(RuntimeError):
@@ -39,12 +40,14 @@ class ParamDesc(ctypes.Structure):
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [("n_params", c_i32), ("n_groups", c_i32), ("n_shards", c_i32),
-                ("has_dit_roles", c_i32), ("slot_bytes", c_i64), ("group_align", c_i64)]
+                ("has_dit_roles", c_i32), ("slot_bytes", c_i64), ("group_align", c_i64),
+                ("staging_bytes", c_i64)]
 
 
 class GroupInfo(ctypes.Structure):
     _fields_ = [("dtype", c_i32), ("esize", c_i32), ("numel", c_i64), ("shard_numel", c_i64),
-                ("shard_bytes", c_i64), ("shard_alloc_bytes", c_i64), ("base", c_i64)]
+                ("shard_bytes", c_i64), ("shard_alloc_bytes", c_i64), ("base", c_i64),
+                ("stage_base", c_i64)]
 
 
 class ParamInfo(ctypes.Structure):
@@ -60,7 +63,8 @@ class DitCfg(ctypes.Structure):
 class EngineDesc(ctypes.Structure):
     _fields_ = [("n_blocks", c_i32), ("slot", c_vp * 2), ("slot_bytes", c_i64),
                 ("compute_stream", c_vp), ("copy_stream", c_vp), ("copy_mode", c_i32),
-                ("copy_ctas", c_i32), ("timing", c_i32), ("dma_streams", c_i32)]
+                ("copy_ctas", c_i32), ("timing", c_i32), ("dma_streams", c_i32),
+                ("staging", c_vp * 2), ("staging_bytes", c_i64), ("gather_stream", c_vp)]
 
 
 class SchedEvent(ctypes.Structure):
@@ -83,6 +87,7 @@ _SIGS = {
     "dlo_shard_host": (c_i32, [c_vp, _P(c_vp), _P(c_vp)]),
     "dlo_plan_destroy": (None, [c_vp]),
     "dlo_reassemble": (c_i32, [c_vp, _P(c_vp), c_vp, c_i32, c_vp]),
+    "dlo_reassemble_staged": (c_i32, [c_vp, _P(c_vp), c_vp, c_i64, c_vp, c_vp, c_vp]),
     "dlo_forward_scratch_bytes": (c_sz, [_P(DitCfg)]),
     "dlo_forward": (c_i32, [_P(DitCfg), c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "dlo_forward_noalloc": (c_i32, [_P(DitCfg), c_vp, c_vp, c_vp, c_vp]),
@@ -245,6 +250,13 @@ def reassemble(plan, shard_ptrs, dst, mode=COPY_DMA, stream=None):
                                 _stream(stream)), "dlo_reassemble")
 
 
+def reassemble_staged(plan, shard_ptrs, staging, staging_bytes, dst, copy_stream=None,
+                      gather_stream=None):
+    _check(lib().dlo_reassemble_staged(plan.handle, _ptrs(shard_ptrs), _ptr(staging),
+                                       int(staging_bytes), _ptr(dst), _stream(copy_stream),
+                                       _stream(gather_stream)), "dlo_reassemble_staged")
+
+
 # ---- block forward -----------------------------------------------------------
 
 FWD_GRAPH = 1
@@ -305,7 +317,9 @@ def kernel_status():
 
 class Engine:
     def __init__(self, n_blocks, slot0, slot1, slot_bytes, compute_stream, copy_stream,
-                 copy_mode=COPY_AUTO, copy_ctas=0, timing=False, dma_streams=0):
+                 copy_mode=COPY_AUTO, copy_ctas=0, timing=False, dma_streams=0,
+                 staging=None, staging_bytes=0, gather_stream=None):
+        """staging: two device buffers (and gather_stream) for COPY_STAGED."""
         d = EngineDesc()
         d.n_blocks = int(n_blocks)
         d.slot[0] = _ptr(slot0)
@@ -317,6 +331,11 @@ class Engine:
         d.copy_ctas = int(copy_ctas)
         d.timing = 1 if timing else 0
         d.dma_streams = int(dma_streams)
+        if staging is not None:
+            d.staging[0] = _ptr(staging[0])
+            d.staging[1] = _ptr(staging[1])
+        d.staging_bytes = int(staging_bytes)
+        d.gather_stream = _stream(gather_stream)
         h = c_vp()
         _check(lib().dlo_engine_create(ctypes.byref(d), ctypes.byref(h)), "dlo_engine_create")
         self.handle = h.value

@@ -426,8 +426,18 @@ class StreamedStack:
                       for _ in range(2)]
         self.compute = torch.cuda.Stream(device=device)
         self.copy = torch.cuda.Stream(device=device)
+        self.staging, self.gather, staging_bytes = None, None, 0
+        if copy_mode == dlo.COPY_STAGED:
+            # the two-phase form: H2D into device staging, then a
+            # device-to-device gather on a third stream
+            staging_bytes = _round_up(self.plan.info().staging_bytes, 256)
+            self.staging = [torch.empty(staging_bytes, dtype=torch.uint8, device=device)
+                            for _ in range(2)]
+            self.gather = torch.cuda.Stream(device=device)
         self.engine = dlo.Engine(w.n_blocks, self.slots[0], self.slots[1], self.slot_bytes,
-                                 self.compute, self.copy, copy_mode, copy_ctas, timing)
+                                 self.compute, self.copy, copy_mode, copy_ctas, timing,
+                                 staging=self.staging, staging_bytes=staging_bytes,
+                                 gather_stream=self.gather)
         for i in range(w.n_blocks):
             self.engine.register_block(i, self.plan, host.shard_ptrs(i % w.distinct))
         self.cfg = dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps)

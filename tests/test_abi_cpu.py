@@ -98,6 +98,44 @@ def test_plan_layout_and_shards_match_oracle(seed):
         assert np.array_equal(image[pi.slot_offset:pi.slot_offset + n], raw[p])
 
 
+@pytest.mark.parametrize("seed", range(10))
+def test_staging_layout(seed):
+    rng = np.random.default_rng(100 + seed)
+    descs = _descs_random(rng, int(rng.integers(1, 7)))
+    s = int(rng.integers(1, 9))
+    plan = dlo.Plan(descs, s)
+    info = plan.info()
+    end = 0
+    for g in plan.groups():
+        assert g.stage_base % 256 == 0 and g.stage_base >= end
+        assert g.shard_alloc_bytes % 16 == 0
+        end = g.stage_base + s * g.shard_alloc_bytes
+    assert info.staging_bytes == end
+
+
+def test_staged_engine_arguments_fail_closed():
+    L = dlo.lib()
+    out = ctypes.c_void_p()
+    d = dlo.EngineDesc()
+    d.n_blocks = 2
+    d.slot[0], d.slot[1] = 4096, 4096 * 3
+    d.slot_bytes = 100
+    d.compute_stream, d.copy_stream = 8, 16
+    d.copy_mode = dlo.COPY_STAGED
+    assert L.dlo_engine_create(ctypes.byref(d), ctypes.byref(out)) == dlo.ERR_INVALID  # no staging
+    d.staging[0], d.staging[1] = 4096 * 8, 4096 * 9
+    d.staging_bytes = 100
+    assert L.dlo_engine_create(ctypes.byref(d), ctypes.byref(out)) == dlo.ERR_INVALID  # no gather
+    d.gather_stream = 16
+    assert L.dlo_engine_create(ctypes.byref(d), ctypes.byref(out)) == dlo.ERR_INVALID  # = copy
+    d.gather_stream = 24
+    d.staging[1] = 4096 * 9 + 16
+    assert L.dlo_engine_create(ctypes.byref(d), ctypes.byref(out)) == dlo.ERR_INVALID  # misaligned
+    d.copy_mode = 4
+    assert L.dlo_engine_create(ctypes.byref(d), ctypes.byref(out)) == dlo.ERR_INVALID  # no mode 4
+    assert L.dlo_reassemble_staged(None, None, None, 0, None, None, None) == dlo.ERR_INVALID
+
+
 def test_role_contract_needs_dtype_and_layout():
     w = W.CONFIGS["tiny"]
     descs = W.block_param_descs(w)

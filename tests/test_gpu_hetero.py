@@ -16,7 +16,7 @@ from layerwise_weight_offload_gb300.stack import PinnedBuffer
 
 pytestmark = pytest.mark.gpu
 
-MODES = [dlo.COPY_DMA, dlo.COPY_KERNEL, dlo.COPY_AUTO]
+MODES = [dlo.COPY_DMA, dlo.COPY_KERNEL, dlo.COPY_AUTO, dlo.COPY_STAGED]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -76,7 +76,13 @@ def test_heterogeneous_blocks_stream_exact(mode, shards):
     slots = [torch.empty(slot_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
     compute, copy = torch.cuda.Stream(), torch.cuda.Stream()
     n_blocks, steps = 3, 3
-    e = dlo.Engine(n_blocks, slots[0], slots[1], slot_bytes, compute, copy, mode)
+    staging, gather, staging_bytes = None, None, 0
+    if mode == dlo.COPY_STAGED:
+        staging_bytes = -(-max(p.info().staging_bytes for p in plans) // 256) * 256
+        staging = [torch.empty(staging_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
+        gather = torch.cuda.Stream()
+    e = dlo.Engine(n_blocks, slots[0], slots[1], slot_bytes, compute, copy, mode,
+                   staging=staging, staging_bytes=staging_bytes, gather_stream=gather)
     for b in range(n_blocks):
         e.register_block(b, plans[b], ptrs[b])
     e.prefetch(0, 0)

@@ -93,3 +93,41 @@ def test_misaligned_shards_bit_exact(mode):
         assert (got[info.slot_bytes:] == 0x5A).all()
         buf.close()
     assert n_cases > 10        # the misaligned paths were exercised
+
+
+@pytest.mark.parametrize("same_stream", [False, True])
+@pytest.mark.parametrize("name", ["tiny", "odd"])
+def test_staged_reassembly_bit_exact(name, same_stream):
+    # the two-phase form: H2D into device staging, then the device gather
+    w = W.CONFIGS[name]
+    w = W.Workload(**{**w.__dict__, "distinct": 2, "n_blocks": 2})
+    host = HostBlocks(w, seed=4, keep_params=True)
+    info = host.plan.info()
+    dst = torch.full((info.slot_bytes + 512,), 0xA5, dtype=torch.uint8, device="cuda")
+    staging = torch.full((info.staging_bytes,), 0x5A, dtype=torch.uint8, device="cuda")
+    cs = torch.cuda.Stream()
+    gs = cs if same_stream else torch.cuda.Stream()
+    for hb in range(2):
+        dlo.reassemble_staged(host.plan, host.shard_ptrs(hb), staging, info.staging_bytes, dst,
+                              cs, gs)
+        torch.cuda.synchronize()
+        got = dst.cpu().numpy()
+        exp = _expected_image(host, hb)
+        for g in host.plan.groups():
+            n = w.shards * g.shard_bytes
+            assert np.array_equal(got[g.base:g.base + n], exp[g.base:g.base + n]), (hb, g.dtype)
+            # staging holds each host shard at its 16-byte aligned offset
+            st = staging.cpu().numpy()
+            views = host.shard_views(hb)
+            gi = [x.dtype for x in host.plan.groups()].index(g.dtype)
+            for r in range(w.shards):
+                off = g.stage_base + r * g.shard_alloc_bytes
+                assert np.array_equal(st[off:off + g.shard_bytes],
+                                      views[gi * w.shards + r][:g.shard_bytes].numpy())
+        assert (got[info.slot_bytes:] == 0xA5).all()
+    with pytest.raises(dlo.DLOError):
+        dlo.reassemble_staged(host.plan, host.shard_ptrs(0), staging, info.staging_bytes - 16,
+                              dst, cs, gs)
+    with pytest.raises(dlo.DLOError):
+        dlo.reassemble(host.plan, host.shard_ptrs(0), dst, dlo.COPY_STAGED, cs)
+    host.close()

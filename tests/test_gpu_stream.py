@@ -19,7 +19,7 @@ from layerwise_weight_offload_gb300.stack import HostBlocks, StreamedStack, Resi
 
 pytestmark = pytest.mark.gpu
 
-MODES = [dlo.COPY_DMA, dlo.COPY_KERNEL, dlo.COPY_AUTO]
+MODES = [dlo.COPY_DMA, dlo.COPY_KERNEL, dlo.COPY_AUTO, dlo.COPY_STAGED]
 
 
 @pytest.fixture(scope="module", autouse=True)
