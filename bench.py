@@ -62,6 +62,9 @@ def parse():
                     choices=["linear", "fc2", "attention", "norm", "copy", "forward"],
                     help="run one kernel of the workload's block `--reps` times (for ncu)")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--source", default="shards", choices=["shards", "pageable", "registered"],
+                    help="shards: pinned host shards (default); pageable / registered: the "
+                         "rank-local path with one shard, blocks by parameter address")
     ap.add_argument("--layout", default="dit", choices=["dit", "mxfp8", "int8"],
                     help="with --only copy: the block's linears as bf16 (dit) or in a 1-byte layout")
     ap.add_argument("--sweep", action="store_true",
@@ -210,7 +213,7 @@ def workload_config(w, args):
                         "steps in the workload" % (w.name, w.n_blocks, w.distinct, w.hidden,
                                                    w.heads, w.mlp, w.tokens, w.batch, w.shards,
                                                    w.steps),
-            "name": w.name, "copy_mode": args.copy_mode}
+            "name": w.name, "copy_mode": args.copy_mode, "host_source": args.source}
 
 
 def h2d_ceiling_gbs(torch, nbytes=1 << 30, reps=10):
@@ -251,7 +254,10 @@ def run_ours(args, ws, rank, local):
     ceiling = h2d_ceiling_gbs(torch)
 
     gen_dev = args.gen_device or ("cuda" if w.distinct * w.bf16_numel() > 2e9 else "cpu")
-    host = HostBlocks(w, seed=args.seed, gen_device=gen_dev)
+    if args.source != "shards":
+        w = W.Workload(**{**w.__dict__, "shards": 1})
+    host = HostBlocks(w, seed=args.seed, gen_device=gen_dev,
+                      keep_params=args.source != "shards")
     bytes_per_block = sum(g.shard_bytes * w.shards for g in host.plan.groups())
     pretouch_s = None
     if args.pretouch:
@@ -259,7 +265,11 @@ def run_ours(args, ws, rank, local):
         t0 = time.perf_counter()
         host.pretouch()
         pretouch_s = time.perf_counter() - t0
-    st = StreamedStack(host, copy_mode=mode, copy_ctas=args.copy_ctas, timing=True)
+    if args.source != "shards":
+        from layerwise_weight_offload_gb300.stack import SourceStack
+        st = SourceStack(host, transport=args.source, timing=True)
+    else:
+        st = StreamedStack(host, copy_mode=mode, copy_ctas=args.copy_ctas, timing=True)
     x0 = W.gen_x(w, args.seed, device="cuda")
     x = x0.clone()
     cur = torch.cuda.current_stream()
@@ -415,6 +425,12 @@ def run_ours(args, ws, rank, local):
         "host_huge_page_fraction": host.buf.huge_fraction(),
         "host_huge_ranges_used_fraction": host.buf.good_fraction(),
         "host_range_survey": host.buf.survey_summary(),
+        "source_path": ({"transport": args.source,
+                         "direct_prefetches": stats1.n_direct_prefetches,
+                         "packed_prefetches": stats1.n_packed_prefetches,
+                         "pack_ms_per_packed_block": (stats1.pack_ms - stats0.pack_ms) /
+                         max(1, stats1.n_packed_prefetches - stats0.n_packed_prefetches)}
+                        if args.source != "shards" else None),
         "copy_ms_all": copy_ms if args.dump_copies else None,
         "roofline": {"name": copy_name, "bound": "h2d", "achieved": achieved,
                      "peak": ceiling, "unit": "GB/s",

@@ -54,7 +54,11 @@ typedef enum {
   DLO_ERR_CUDA = 2,     /* a CUDA runtime/driver call failed (text in dlo_last_error) */
   DLO_ERR_TIMEOUT = 3,  /* a bounded wait ran out (host poll or device-side wait) */
   DLO_ERR_STATE = 4,    /* call not valid in the current state (e.g. block not resident) */
-  DLO_ERR_NOMEM = 5     /* a caller-provided buffer is too small */
+  DLO_ERR_NOMEM = 5,    /* a caller-provided buffer is too small */
+  DLO_ERR_PARTIAL = 6   /* a registration failed and could not be fully rolled
+                           back: some ranges are still registered, so their
+                           mappings must stay open (fatal for the caller's
+                           setup) */
 } dlo_status;
 
 /* Element types of parameters.  Every distinct code forms its own dtype
@@ -339,6 +343,41 @@ dlo_status dlo_op_attention(const uint16_t* qkv, int64_t batch, int64_t tokens,
  * "AllGather path").
  * ------------------------------------------------------------------------ */
 
+/* ------------------------------------------------------------------------
+ * Registered host ranges ([D5] "Registered mmap transport"): page-locks
+ * complete host ranges (for example a read-only checkpoint mapping) so that
+ * the rank-local path can copy tensor views straight from them into the
+ * slots, without the two host staging slots.
+ * ptrs[i], bytes[i]: n ranges; each is widened to whole pages, and ranges
+ *   that then share pages are merged (a page is registered once); the
+ *   merged ranges are registered in address order.
+ * flags: 1 = the ranges are read-only (cudaHostRegisterReadOnly).
+ * limit_bytes: > 0 caps the page-aligned total; over it nothing is
+ *   registered and DLO_ERR_NOMEM is returned (the caller keeps staging).
+ * All or nothing: on a failure the ranges registered by this call are
+ * unregistered again and the status is DLO_ERR_CUDA; if an unregistration
+ * fails too, DLO_ERR_PARTIAL (those mappings must not be closed).
+ * *registered_bytes (may be null) receives the page-aligned total on
+ * success.  Unregistering is the caller's, with dlo_host_unregister_ranges
+ * (same ptrs/bytes); it unregisters every range and reports the first
+ * failure (retryable). */
+dlo_status dlo_host_register_ranges(const void* const* ptrs, const int64_t* bytes, int32_t n,
+                                    int32_t flags, int64_t limit_bytes,
+                                    int64_t* registered_bytes);
+dlo_status dlo_host_unregister_ranges(const void* const* ptrs, const int64_t* bytes, int32_t n);
+
+/* Test hook: replaces the CUDA registration calls used by the two
+ * functions above with fakes (enable = 1): the fake register fails on its
+ * call number fail_register_at (0-based; -1: never), the fake unregister on
+ * call number fail_unregister_at.  Each fake call is logged; *n_calls and
+ * log[] (capacity cap) receive entries of +(i+1) for "register range i" and
+ * -(i+1) for "unregister range i" (i: index among the merged, address-ordered
+ * page ranges).  enable = 0 restores the real calls.
+ * Touches no GPU; for host-side tests of the all-or-nothing contract. */
+dlo_status dlo_debug_fake_host_register(int32_t enable, int32_t fail_register_at,
+                                        int32_t fail_unregister_at);
+dlo_status dlo_debug_fake_host_register_log(int32_t* log, int32_t cap, int32_t* n_calls);
+
 typedef struct dlo_engine dlo_engine;
 
 typedef struct {
@@ -367,6 +406,15 @@ typedef struct {
                              for the gather that last read staging[x]; the
                              gather waits for the H2D and for the slot's free
                              event, and records the slot's ready event. */
+  void* host_staging[2];  /* rank-local source blocks only (see
+                             dlo_register_block_source): two page-locked
+                             host buffers, caller-owned, into which CPU
+                             threads pack a block before its DMA; host
+                             staging x serves the prefetches into slot x.
+                             Null when unused. */
+  int64_t host_staging_bytes; /* capacity of each (>= a packed block's
+                             slot_bytes) */
+  int32_t pack_threads;   /* CPU threads that pack a block (0 = 4) */
 } dlo_engine_desc;
 
 typedef struct {
@@ -393,6 +441,26 @@ dlo_status dlo_engine_create(const dlo_engine_desc* desc, dlo_engine** out);
  * pinned/mapped or misaligned), DLO_ERR_STATE (already registered). */
 dlo_status dlo_register_block(dlo_engine* e, int32_t block, const dlo_plan* plan,
                               const void* const* shard_ptrs);
+
+/* Rank-local source blocks ([D5] "Rank-local path without DLO AllGather"):
+ * registers `block` by the host addresses of its parameters instead of by
+ * shards.  The plan must have n_shards = 1 (no sharding on this path).
+ * param_src[p]: parameter p's element [0,..,0] in any host memory (pageable
+ *   runtime tensors, a checkpoint mapping); storage_numel elements are read
+ *   in memory order.  Borrowed until the engine is destroyed.
+ * If every parameter lies in page-locked memory (for example ranges
+ * registered with dlo_host_register_ranges), each prefetch copies every
+ * parameter straight into its slot offset ("Registered mmap transport").
+ * Otherwise each prefetch into slot x first waits for the DMA that last read
+ * host staging x, packs the parameters there on pack_threads CPU threads (in
+ * the calling thread, which returns once the pack is done), then moves the
+ * packed block with one DMA ("two bounded pinned host staging slots");
+ * the engine's host staging buffers are then required.
+ * Errors: DLO_ERR_INVALID on bad arguments, n_shards != 1, a block too
+ * large for the slots or host staging, or no host staging for a pageable
+ * source; DLO_ERR_STATE if the block is registered already. */
+dlo_status dlo_register_block_source(dlo_engine* e, int32_t block, const dlo_plan* plan,
+                                     const void* const* param_src);
 
 /* Enqueues a prefetch of `block` into `slot` on the copy stream: the copy
  * stream waits for the free event of the forward that last read `slot`,
@@ -458,6 +526,10 @@ typedef struct {
   int32_t n_kernel_prefetches;
   double race_dma_us;
   double race_kernel_us;
+  int32_t n_direct_prefetches; /* source blocks copied straight from
+                                  page-locked parameters */
+  int32_t n_packed_prefetches; /* source blocks packed into host staging */
+  double pack_ms;              /* host time spent packing (waits included) */
 } dlo_engine_stats;
 dlo_status dlo_engine_query(dlo_engine* e, dlo_engine_stats* out);
 dlo_status dlo_engine_copy_times(dlo_engine* e, float* copy_ms, int64_t* copy_bytes,

@@ -22,6 +22,9 @@
 // write-after-read wait too).
 #include <algorithm>
 #include <chrono>
+#include <condition_variable>
+#include <cstring>
+#include <mutex>
 #include <new>
 #include <thread>
 
@@ -32,6 +35,80 @@ dlo_status forward_impl(const dlo_dit_cfg* cfg, const dlo_plan* plan, const void
                         float* x, void* scratch, size_t scratch_bytes, cudaStream_t stream);
 }
 
+namespace dlo {
+
+// CPU threads that pack a rank-local block: run() hands the copy tasks to
+// the pool's threads and the calling thread and returns once all are done.
+class PackPool {
+ public:
+  struct Task {
+    uint8_t* dst;
+    const uint8_t* src;
+    size_t n;
+  };
+  explicit PackPool(int threads) {
+    for (int i = 1; i < threads; ++i) th_.emplace_back([this] { loop(); });
+  }
+  ~PackPool() {
+    {
+      std::lock_guard<std::mutex> l(mu_);
+      stop_ = true;
+    }
+    cv_.notify_all();
+    for (auto& t : th_) t.join();
+  }
+  void run(const std::vector<Task>& tasks) {
+    {
+      std::lock_guard<std::mutex> l(mu_);
+      tasks_ = &tasks;
+      next_ = 0;
+      left_ = tasks.size();
+      ++gen_;
+    }
+    cv_.notify_all();
+    work();
+    std::unique_lock<std::mutex> l(mu_);
+    done_.wait(l, [this] { return left_ == 0; });
+    tasks_ = nullptr;
+  }
+
+ private:
+  void work() {
+    for (;;) {
+      const Task* t;
+      {
+        std::lock_guard<std::mutex> l(mu_);
+        if (!tasks_ || next_ >= tasks_->size()) return;
+        t = &(*tasks_)[next_++];
+      }
+      std::memcpy(t->dst, t->src, t->n);
+      std::lock_guard<std::mutex> l(mu_);
+      if (--left_ == 0) done_.notify_all();
+    }
+  }
+  void loop() {
+    uint64_t seen = 0;
+    for (;;) {
+      {
+        std::unique_lock<std::mutex> l(mu_);
+        cv_.wait(l, [&] { return stop_ || (gen_ != seen && tasks_ && next_ < tasks_->size()); });
+        if (stop_) return;
+        seen = gen_;
+      }
+      work();
+    }
+  }
+  std::vector<std::thread> th_;
+  std::mutex mu_;
+  std::condition_variable cv_, done_;
+  const std::vector<Task>* tasks_ = nullptr;
+  size_t next_ = 0, left_ = 0;
+  uint64_t gen_ = 0;
+  bool stop_ = false;
+};
+
+}  // namespace dlo
+
 struct dlo_engine {
   struct Block {
     const dlo_plan* plan = nullptr;
@@ -39,6 +116,16 @@ struct dlo_engine {
     std::vector<const void*> dev;    // device-accessible addresses (null: DMA only)
     std::vector<int64_t> pitch;      // [g]: constant host stride between shards, 0 if none
     int64_t bytes = 0;               // bytes one prefetch moves
+    // rank-local source block (dlo_register_block_source): parameters by
+    // address; direct = every one page-locked (copied straight into the slot)
+    struct Src {
+      const uint8_t* p;
+      int64_t bytes;
+      int64_t off;                   // byte offset in a slot
+    };
+    bool source = false;
+    bool direct = false;
+    std::vector<Src> src;
   };
   struct Hook {
     int32_t current_slot;
@@ -91,6 +178,16 @@ struct dlo_engine {
   cudaStream_t gather = nullptr;
   cudaEvent_t staged[2] = {nullptr, nullptr};
   cudaEvent_t stage_free[2] = {nullptr, nullptr};
+  // rank-local source blocks: caller-owned pinned host staging (host staging
+  // x serves slot x), the event of the last DMA out of each, the CPU pool
+  // that packs, and counters
+  uint8_t* host_staging[2] = {nullptr, nullptr};
+  int64_t host_staging_bytes = 0;
+  cudaEvent_t hs_read[2] = {nullptr, nullptr};
+  bool hs_pending[2] = {false, false};
+  dlo::PackPool* pool = nullptr;
+  int64_t n_direct = 0, n_packed = 0;
+  double pack_ms = 0;
   double race_dma_us = 0, race_kernel_us = 0;
   int64_t n_prefetches = 0;
   int64_t n_kernel_prefetches = 0;
@@ -361,10 +458,79 @@ dlo_status make_timed(dlo_engine::Timed* t) {
   return DLO_OK;
 }
 
+// Host-side bounded wait for an event (polls; false after timeout_ms).
+bool wait_event_host(cudaEvent_t ev, int timeout_ms) {
+  const auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    const cudaError_t q = cudaEventQuery(ev);
+    if (q == cudaSuccess) return true;
+    if (q != cudaErrorNotReady) return false;
+    if (std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(timeout_ms))
+      return false;
+    std::this_thread::sleep_for(std::chrono::microseconds(20));
+  }
+}
+
+constexpr int kHostStagingWaitMs = 60000;
+
+// Prefetch of a rank-local source block into `slot` ([D5] "Rank-local path
+// without DLO AllGather").  Direct: every parameter copied by DMA from its
+// page-locked source to its slot offset.  Packed: once the DMA that last
+// read host staging `slot` is done, CPU threads copy the parameters to
+// their slot offsets inside it, then one DMA moves the packed block.
+dlo_status prefetch_source(dlo_engine* e, int32_t block, int32_t slot) {
+  const dlo_engine::Block& b = e->blocks[block];
+  dlo_engine::Timed t{};
+  if (e->timing) {
+    DLO_TRY(make_timed(&t));
+    t.bytes = b.bytes;
+    t.mode = DLO_COPY_DMA;
+    e->timed.push_back(t);
+  }
+  if (b.direct) {
+    DLO_CUDA(cudaStreamWaitEvent(e->copy, e->freed[slot], 0));
+    if (e->timing) DLO_CUDA(cudaEventRecord(t.a, e->copy));
+    for (const auto& s : b.src)
+      DLO_CUDA(cudaMemcpyAsync(e->slot[slot] + s.off, s.p, static_cast<size_t>(s.bytes),
+                               cudaMemcpyHostToDevice, e->copy));
+    e->n_direct++;
+  } else {
+    const auto t0 = std::chrono::steady_clock::now();
+    if (e->hs_pending[slot] && !wait_event_host(e->hs_read[slot], kHostStagingWaitMs))
+      DLO_FAIL(DLO_ERR_TIMEOUT, "prefetch: host staging %d not released by its DMA", slot);
+    std::vector<PackPool::Task> tasks;
+    constexpr size_t kPiece = 4u << 20;
+    for (const auto& s : b.src)
+      for (int64_t o = 0; o < s.bytes; o += static_cast<int64_t>(kPiece))
+        tasks.push_back({e->host_staging[slot] + s.off + o, s.p + o,
+                         static_cast<size_t>(std::min<int64_t>(kPiece, s.bytes - o))});
+    e->pool->run(tasks);
+    e->pack_ms += std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0)
+                      .count();
+    DLO_CUDA(cudaStreamWaitEvent(e->copy, e->freed[slot], 0));
+    if (e->timing) DLO_CUDA(cudaEventRecord(t.a, e->copy));
+    DLO_CUDA(cudaMemcpyAsync(e->slot[slot], e->host_staging[slot],
+                             static_cast<size_t>(b.plan->slot_bytes), cudaMemcpyHostToDevice,
+                             e->copy));
+    DLO_CUDA(cudaEventRecord(e->hs_read[slot], e->copy));
+    e->hs_pending[slot] = true;
+    e->n_packed++;
+  }
+  if (e->timing) DLO_CUDA(cudaEventRecord(t.b, e->copy));
+  DLO_CUDA(cudaEventRecord(e->ready[slot], e->copy));
+  e->slot_holds[slot] = block;
+  e->n_prefetches++;
+  return DLO_OK;
+}
+
 // Enqueues the prefetch of `block` into `slot` on the copy stream.
 dlo_status enqueue_prefetch(dlo_engine* e, int32_t block, int32_t slot, int64_t issued_by_k,
                             int32_t* used_mode = nullptr) {
   const dlo_engine::Block& b = e->blocks[block];
+  if (b.source) {
+    if (used_mode) *used_mode = DLO_COPY_DMA;
+    return prefetch_source(e, block, slot);
+  }
   const int32_t mode = mode_for(e, issued_by_k, b);
   if (used_mode) *used_mode = mode;
   if (mode == DLO_COPY_STAGED) {
@@ -427,7 +593,9 @@ void release(dlo_engine* e) {
     if (e->freed[s]) cudaEventDestroy(e->freed[s]);
     if (e->staged[s]) cudaEventDestroy(e->staged[s]);
     if (e->stage_free[s]) cudaEventDestroy(e->stage_free[s]);
+    if (e->hs_read[s]) cudaEventDestroy(e->hs_read[s]);
   }
+  delete e->pool;
   for (auto& t : e->timed) {
     cudaEventDestroy(t.a);
     cudaEventDestroy(t.b);
@@ -475,10 +643,27 @@ dlo_status dlo_engine_create(const dlo_engine_desc* d, dlo_engine** out) {
       DLO_FAIL(DLO_ERR_INVALID,
                "dlo_engine_create: staged copies need a gather stream of their own");
   }
+  if (d->host_staging[0] || d->host_staging[1]) {
+    if (!d->host_staging[0] || !d->host_staging[1] || d->host_staging[0] == d->host_staging[1] ||
+        d->host_staging_bytes <= 0)
+      DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: host staging needs two distinct buffers");
+    if (d->pack_threads < 0 || d->pack_threads > 64)
+      DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: pack_threads must be 0..64");
+  }
   if (d->dma_streams < 0 || d->dma_streams > dlo_engine::kMaxFan)
     DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: dma_streams must be 0..%d",
              dlo_engine::kMaxFan);
   DLO_TRY(preload_kernels());
+  for (int s = 0; s < 2 && d->host_staging[0]; ++s) {
+    cudaPointerAttributes pa{};
+    const uint8_t* hs = static_cast<const uint8_t*>(d->host_staging[s]);
+    if (cudaPointerGetAttributes(&pa, hs) != cudaSuccess || pa.type != cudaMemoryTypeHost ||
+        cudaPointerGetAttributes(&pa, hs + d->host_staging_bytes - 1) != cudaSuccess ||
+        pa.type != cudaMemoryTypeHost) {
+      cudaGetLastError();
+      DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: host staging %d is not page-locked", s);
+    }
+  }
   dlo_engine* e = new (std::nothrow) dlo_engine();
   if (!e) DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: out of host memory");
   e->n_blocks = d->n_blocks;
@@ -507,6 +692,15 @@ dlo_status dlo_engine_create(const dlo_engine_desc* d, dlo_engine** out) {
          cudaEventCreateWithFlags(&e->freed[s], cudaEventDisableTiming) == cudaSuccess;
   for (int i = 0; i < 2 * kRaceWindows; ++i)
     ok = ok && cudaEventCreate(&e->race_ev[i]) == cudaSuccess;
+  if (d->host_staging[0]) {
+    e->host_staging[0] = static_cast<uint8_t*>(d->host_staging[0]);
+    e->host_staging[1] = static_cast<uint8_t*>(d->host_staging[1]);
+    e->host_staging_bytes = d->host_staging_bytes;
+    for (int s = 0; s < 2; ++s)
+      ok = ok && cudaEventCreateWithFlags(&e->hs_read[s], cudaEventDisableTiming) == cudaSuccess;
+  }
+  e->pool = new (std::nothrow) PackPool(d->pack_threads > 0 ? d->pack_threads : 4);
+  ok = ok && e->pool != nullptr;
   if (e->gather)
     for (int s = 0; s < 2; ++s)
       ok = ok &&
@@ -571,6 +765,47 @@ dlo_status dlo_register_block(dlo_engine* e, int32_t block, const dlo_plan* plan
   compute_pitches(&b);
   if (e->mode == DLO_COPY_KERNEL && !all_mapped(b))
     DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block: kernel copies need device-mapped shards");
+  e->blocks[block] = std::move(b);
+  return DLO_OK;
+}
+
+dlo_status dlo_register_block_source(dlo_engine* e, int32_t block, const dlo_plan* plan,
+                                     const void* const* param_src) {
+  using namespace dlo;
+  DLO_TRY(check_engine(e));
+  if (block < 0 || block >= e->n_blocks)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block_source: block %d out of range", block);
+  if (!plan || !param_src) DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block_source: null argument");
+  if (e->blocks[block].plan)
+    DLO_FAIL(DLO_ERR_STATE, "dlo_register_block_source: block %d already registered", block);
+  if (plan->n_shards != 1)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block_source: the rank-local path has 1 shard");
+  if (plan->slot_bytes > e->slot_bytes)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block_source: block needs %lld bytes, slots hold %lld",
+             (long long)plan->slot_bytes, (long long)e->slot_bytes);
+  dlo_engine::Block b;
+  b.plan = plan;
+  b.source = true;
+  b.direct = true;
+  for (size_t p = 0; p < plan->params.size(); ++p) {
+    const auto& q = plan->params[p];
+    const uint8_t* s = static_cast<const uint8_t*>(param_src[p]);
+    if (!s) DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block_source: param %zu is null", p);
+    const int64_t n = q.storage_numel * plan->groups[q.group].esize;
+    b.src.push_back({s, n, q.slot_offset});
+    b.bytes += n;
+    cudaPointerAttributes a0{}, a1{};
+    const bool locked = cudaPointerGetAttributes(&a0, s) == cudaSuccess &&
+                        a0.type == cudaMemoryTypeHost &&
+                        cudaPointerGetAttributes(&a1, s + n - 1) == cudaSuccess &&
+                        a1.type == cudaMemoryTypeHost;
+    cudaGetLastError();
+    b.direct = b.direct && locked;
+  }
+  if (!b.direct && (!e->host_staging[0] || e->host_staging_bytes < plan->slot_bytes))
+    DLO_FAIL(DLO_ERR_INVALID,
+             "dlo_register_block_source: pageable parameters need host staging of %lld bytes",
+             (long long)plan->slot_bytes);
   e->blocks[block] = std::move(b);
   return DLO_OK;
 }
@@ -735,6 +970,9 @@ dlo_status dlo_engine_query(dlo_engine* e, dlo_engine_stats* out) {
   out->n_kernel_prefetches = static_cast<int32_t>(e->n_kernel_prefetches);
   out->race_dma_us = e->race_dma_us;
   out->race_kernel_us = e->race_kernel_us;
+  out->n_direct_prefetches = static_cast<int32_t>(e->n_direct);
+  out->n_packed_prefetches = static_cast<int32_t>(e->n_packed);
+  out->pack_ms = e->pack_ms;
   return DLO_OK;
 }
 

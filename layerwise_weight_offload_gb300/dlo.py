@@ -14,7 +14,7 @@ import re
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libdlo.so")
 
-OK, ERR_INVALID, ERR_CUDA, ERR_TIMEOUT, ERR_STATE, ERR_NOMEM = range(6)
+OK, ERR_INVALID, ERR_CUDA, ERR_TIMEOUT, ERR_STATE, ERR_NOMEM, ERR_PARTIAL = range(7)
 BF16, F32, F16, FP8_E4M3, FP8_E5M2, I8, U8, E8M0 = 0, 1, 2, 3, 4, 5, 6, 7
 ESIZE = {BF16: 2, F32: 4, F16: 2, FP8_E4M3: 1, FP8_E5M2: 1, I8: 1, U8: 1, E8M0: 1}
 COPY_AUTO, COPY_DMA, COPY_KERNEL, COPY_STAGED = 0, 1, 2, 3
@@ -64,7 +64,9 @@ class EngineDesc(ctypes.Structure):
     _fields_ = [("n_blocks", c_i32), ("slot", c_vp * 2), ("slot_bytes", c_i64),
                 ("compute_stream", c_vp), ("copy_stream", c_vp), ("copy_mode", c_i32),
                 ("copy_ctas", c_i32), ("timing", c_i32), ("dma_streams", c_i32),
-                ("staging", c_vp * 2), ("staging_bytes", c_i64), ("gather_stream", c_vp)]
+                ("staging", c_vp * 2), ("staging_bytes", c_i64), ("gather_stream", c_vp),
+                ("host_staging", c_vp * 2), ("host_staging_bytes", c_i64),
+                ("pack_threads", c_i32)]
 
 
 class SchedEvent(ctypes.Structure):
@@ -75,7 +77,8 @@ class SchedEvent(ctypes.Structure):
 class EngineStats(ctypes.Structure):
     _fields_ = [("chosen_mode", c_i32), ("n_forwards", c_i32), ("n_prefetches", c_i32),
                 ("n_kernel_prefetches", c_i32), ("race_dma_us", ctypes.c_double),
-                ("race_kernel_us", ctypes.c_double)]
+                ("race_kernel_us", ctypes.c_double), ("n_direct_prefetches", c_i32),
+                ("n_packed_prefetches", c_i32), ("pack_ms", ctypes.c_double)]
 
 
 _P = ctypes.POINTER
@@ -99,6 +102,11 @@ _SIGS = {
     "dlo_op_attention": (c_i32, [c_vp, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp, c_sz, c_vp]),
     "dlo_engine_create": (c_i32, [_P(EngineDesc), _P(c_vp)]),
     "dlo_register_block": (c_i32, [c_vp, c_i32, c_vp, _P(c_vp)]),
+    "dlo_register_block_source": (c_i32, [c_vp, c_i32, c_vp, _P(c_vp)]),
+    "dlo_host_register_ranges": (c_i32, [_P(c_vp), _P(c_i64), c_i32, c_i32, c_i64, _P(c_i64)]),
+    "dlo_host_unregister_ranges": (c_i32, [_P(c_vp), _P(c_i64), c_i32]),
+    "dlo_debug_fake_host_register": (c_i32, [c_i32, c_i32, c_i32]),
+    "dlo_debug_fake_host_register_log": (c_i32, [_P(c_i32), c_i32, _P(c_i32)]),
     "dlo_prefetch": (c_i32, [c_vp, c_i32, c_i32]),
     "dlo_wait": (c_i32, [c_vp, c_i32]),
     "dlo_wait_host": (c_i32, [c_vp, c_i32, c_i32]),
@@ -307,6 +315,37 @@ def op_attention(qkv, batch, tokens, d, heads, o, scratch, scratch_bytes, stream
                                   int(scratch_bytes), _stream(stream)), "dlo_op_attention")
 
 
+def host_register_ranges(ptrs, sizes, read_only=False, limit_bytes=0):
+    """Page-locks the ranges, all or nothing; returns the registered bytes."""
+    n = len(ptrs)
+    arr = (c_i64 * max(n, 1))(*[int(s) for s in sizes])
+    out = c_i64(0)
+    _check(lib().dlo_host_register_ranges(_ptrs(ptrs), arr, n, 1 if read_only else 0,
+                                          int(limit_bytes), ctypes.byref(out)),
+           "dlo_host_register_ranges")
+    return out.value
+
+
+def host_unregister_ranges(ptrs, sizes):
+    n = len(ptrs)
+    arr = (c_i64 * max(n, 1))(*[int(s) for s in sizes])
+    _check(lib().dlo_host_unregister_ranges(_ptrs(ptrs), arr, n), "dlo_host_unregister_ranges")
+
+
+def debug_fake_host_register(enable, fail_register_at=-1, fail_unregister_at=-1):
+    _check(lib().dlo_debug_fake_host_register(int(enable), int(fail_register_at),
+                                              int(fail_unregister_at)),
+           "dlo_debug_fake_host_register")
+
+
+def debug_fake_host_register_log():
+    buf = (c_i32 * 256)()
+    n = c_i32(0)
+    _check(lib().dlo_debug_fake_host_register_log(buf, 256, ctypes.byref(n)),
+           "dlo_debug_fake_host_register_log")
+    return list(buf[:min(n.value, 256)])
+
+
 def kernel_status():
     v = c_i32()
     _check(lib().dlo_kernel_status(ctypes.byref(v)), "dlo_kernel_status")
@@ -318,8 +357,11 @@ def kernel_status():
 class Engine:
     def __init__(self, n_blocks, slot0, slot1, slot_bytes, compute_stream, copy_stream,
                  copy_mode=COPY_AUTO, copy_ctas=0, timing=False, dma_streams=0,
-                 staging=None, staging_bytes=0, gather_stream=None):
-        """staging: two device buffers (and gather_stream) for COPY_STAGED."""
+                 staging=None, staging_bytes=0, gather_stream=None, host_staging=None,
+                 host_staging_bytes=0, pack_threads=0):
+        """staging: two device buffers (and gather_stream) for COPY_STAGED;
+        host_staging: two page-locked host buffers for rank-local source
+        blocks whose parameters are pageable."""
         d = EngineDesc()
         d.n_blocks = int(n_blocks)
         d.slot[0] = _ptr(slot0)
@@ -336,6 +378,11 @@ class Engine:
             d.staging[1] = _ptr(staging[1])
         d.staging_bytes = int(staging_bytes)
         d.gather_stream = _stream(gather_stream)
+        if host_staging is not None:
+            d.host_staging[0] = _ptr(host_staging[0])
+            d.host_staging[1] = _ptr(host_staging[1])
+        d.host_staging_bytes = int(host_staging_bytes)
+        d.pack_threads = int(pack_threads)
         h = c_vp()
         _check(lib().dlo_engine_create(ctypes.byref(d), ctypes.byref(h)), "dlo_engine_create")
         self.handle = h.value
@@ -344,6 +391,10 @@ class Engine:
     def register_block(self, block, plan, shard_ptrs):
         _check(lib().dlo_register_block(self.handle, block, plan.handle, _ptrs(shard_ptrs)),
                "dlo_register_block")
+
+    def register_block_source(self, block, plan, param_srcs):
+        _check(lib().dlo_register_block_source(self.handle, block, plan.handle,
+                                               _ptrs(param_srcs)), "dlo_register_block_source")
 
     def prefetch(self, block, slot):
         _check(lib().dlo_prefetch(self.handle, block, slot), "dlo_prefetch")

@@ -464,6 +464,77 @@ class StreamedStack:
             self.engine = None
 
 
+class SourceStack:
+    """The rank-local path ([D5] "Rank-local path without DLO AllGather"):
+    one shard, blocks registered by the host addresses of their parameters
+    (host.params, ordinary pageable tensors).  transport "pageable": CPU
+    threads pack each block into one of two pinned host staging slots before
+    its DMA; "registered": the parameters' memory is page-locked (all or
+    nothing) and copied straight into the slots."""
+
+    def __init__(self, host: HostBlocks, transport="pageable", pack_threads=0, timing=False,
+                 device="cuda"):
+        w = host.w
+        if w.shards != 1 or host.params is None:
+            raise ValueError("SourceStack needs a one-shard HostBlocks with keep_params=True")
+        self.w, self.host, self.plan, self.transport = w, host, host.plan, transport
+        self.slot_bytes = _round_up(self.plan.info().slot_bytes, 256)
+        self.slots = [torch.empty(self.slot_bytes, dtype=torch.uint8, device=device)
+                      for _ in range(2)]
+        self.compute = torch.cuda.Stream(device=device)
+        self.copy = torch.cuda.Stream(device=device)
+        self.srcs = [[host.params[hb][name].data_ptr() for name, _, _ in host.descs]
+                     for hb in range(w.distinct)]
+        self.reg = None
+        self.hs = None
+        staging = None
+        if transport == "registered":
+            ptrs, sizes = [], []
+            for hb in range(w.distinct):
+                for name, _, _ in host.descs:
+                    t = host.params[hb][name]
+                    ptrs.append(t.data_ptr())
+                    sizes.append(t.numel() * t.element_size())
+            dlo.host_register_ranges(ptrs, sizes)
+            self.reg = (ptrs, sizes)
+        else:
+            self.hs = PinnedBuffer(2 * self.slot_bytes, defer=True)
+            offs = self.hs.place_surveyed([self.slot_bytes, self.slot_bytes])
+            staging = [self.hs.ptr + o for o in offs]
+        self.engine = dlo.Engine(w.n_blocks, self.slots[0], self.slots[1], self.slot_bytes,
+                                 self.compute, self.copy, dlo.COPY_DMA, 0, timing,
+                                 host_staging=staging,
+                                 host_staging_bytes=self.slot_bytes if staging else 0,
+                                 pack_threads=pack_threads)
+        for i in range(w.n_blocks):
+            self.engine.register_block_source(i, self.plan, self.srcs[i % w.distinct])
+        self.cfg = dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps)
+        self.scratch_bytes = dlo.forward_scratch_bytes(self.cfg)
+        self.scratch = torch.empty(self.scratch_bytes, dtype=torch.uint8, device=device)
+        self.primed = False
+
+    def prime(self):
+        self.engine.prefetch(0, 0)
+        self.primed = True
+
+    def step(self, x):
+        if not self.primed:
+            self.prime()
+        for i in range(self.w.n_blocks):
+            self.engine.block_forward(i, self.cfg, x, self.scratch, self.scratch_bytes)
+
+    def close(self):
+        if self.engine is not None:
+            self.engine.destroy()
+            self.engine = None
+        if self.reg is not None:
+            dlo.host_unregister_ranges(*self.reg)
+            self.reg = None
+        if self.hs is not None:
+            self.hs.close()
+            self.hs = None
+
+
 class ResidentStack:
     """Every distinct block reassembled once into its own device buffer (the
     same slot layout), then the same forward kernels: the reference run the
