@@ -313,8 +313,10 @@ def run_ours(args, ws, rank, local):
     value = ws * n_fwd / (ms / 1e3)
     ms_step = ms / args.steps
     chosen = dlo.COPY_MODE_NAMES[stats1.chosen_mode]
-    kernel_launches_copy = stats1.n_kernel_prefetches - stats0.n_kernel_prefetches
-    gpu_launches = 7 * n_fwd + kernel_launches_copy
+    # the library's own kernels in the timed region: every forward's launches
+    # plus the copy-kernel launches of the prefetches the timed forwards issued
+    gpu_launches = (n_fwd * dlo.forward_launches(st.cfg) +
+                    stats1.n_copy_kernel_launches - stats0.n_copy_kernel_launches)
 
     # all-resident reference run: same kernels, no transfer
     rs = ResidentStack(host)

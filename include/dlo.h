@@ -264,6 +264,14 @@ enum { DLO_FWD_GRAPH = 1 };
  * The split choice depends on the device's SM count. */
 size_t dlo_forward_scratch_bytes(const dlo_dit_cfg* cfg);
 
+/* Number of kernel launches one dlo_forward (or dlo_forward_noalloc) makes
+ * for this configuration — two norm launches, the QKV linear, attention,
+ * and for the out-projection, fc1 and fc2 one GEMM each plus one ordered
+ * reduction when the linear runs as K slices (the split depends on the
+ * current device's SM count; 152 when none is visible) — or 0 for an
+ * invalid configuration.  Launches nothing. */
+int32_t dlo_forward_launches(const dlo_dit_cfg* cfg);
+
 /* One block forward with weights at `block_base`, laid out as a slot of
  * `plan` (the plan's parameter names must be the DiT block's: norm1.weight,
  * ada1.shift, ada1.scale, ada1.gate, attn.qkv.weight, attn.out.weight,
@@ -530,6 +538,9 @@ typedef struct {
                                   page-locked parameters */
   int32_t n_packed_prefetches; /* source blocks packed into host staging */
   double pack_ms;              /* host time spent packing (waits included) */
+  int32_t n_copy_kernel_launches; /* copy-kernel launches of all prefetches:
+                                  KERNEL prefetches, DMA prefetches' small
+                                  groups, STAGED gathers */
 } dlo_engine_stats;
 dlo_status dlo_engine_query(dlo_engine* e, dlo_engine_stats* out);
 dlo_status dlo_engine_copy_times(dlo_engine* e, float* copy_ms, int64_t* copy_bytes,

@@ -187,6 +187,7 @@ struct dlo_engine {
   bool hs_pending[2] = {false, false};
   dlo::PackPool* pool = nullptr;
   int64_t n_direct = 0, n_packed = 0;
+  int64_t n_copy_launches = 0;
   double pack_ms = 0;
   double race_dma_us = 0, race_kernel_us = 0;
   int64_t n_prefetches = 0;
@@ -266,7 +267,8 @@ constexpr int64_t kSmallGroupBytes = 1 << 20;
 dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, int ctas,
                       cudaStream_t stream, int fan, cudaStream_t* aux, cudaEvent_t fork_ev,
                       cudaEvent_t* join_ev, cudaStream_t side = nullptr,
-                      cudaEvent_t side_fork = nullptr, cudaEvent_t side_join = nullptr) {
+                      cudaEvent_t side_fork = nullptr, cudaEvent_t side_join = nullptr,
+                      int64_t* launches = nullptr) {
   const dlo_plan* p = b.plan;
   const int32_t s = p->n_shards;
   if (mode == DLO_COPY_KERNEL) {
@@ -274,6 +276,7 @@ dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, in
       DLO_FAIL(DLO_ERR_INVALID, "prefetch: a shard is not device-mapped pinned memory");
     SegmentTable t;
     DLO_TRY(build_segments(b, dst, &t));
+    if (launches) ++*launches;
     return launch_copy_reassemble(t, ctas, stream);
   }
   std::vector<char> by_kernel(p->groups.size(), 0);
@@ -295,6 +298,7 @@ dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, in
       DLO_CUDA(cudaEventRecord(side_fork, stream));
       DLO_CUDA(cudaStreamWaitEvent(side, side_fork, 0));
       DLO_TRY(launch_copy_reassemble(t, 1, side));
+      if (launches) ++*launches;
       DLO_CUDA(cudaEventRecord(side_join, side));
     }
   }
@@ -551,6 +555,7 @@ dlo_status enqueue_prefetch(dlo_engine* e, int32_t block, int32_t slot, int64_t 
     DLO_CUDA(cudaStreamWaitEvent(e->gather, e->staged[slot], 0));
     DLO_CUDA(cudaStreamWaitEvent(e->gather, e->freed[slot], 0));
     DLO_TRY(stage_gather(b.plan, e->staging[slot], e->slot[slot], e->copy_ctas, e->gather));
+    e->n_copy_launches++;
     DLO_CUDA(cudaEventRecord(e->stage_free[slot], e->gather));
     DLO_CUDA(cudaEventRecord(e->ready[slot], e->gather));
     e->slot_holds[slot] = block;
@@ -567,7 +572,7 @@ dlo_status enqueue_prefetch(dlo_engine* e, int32_t block, int32_t slot, int64_t 
     DLO_CUDA(cudaEventRecord(t.a, e->copy));
   }
   DLO_TRY(copy_block(b, e->slot[slot], mode, e->copy_ctas, e->copy, e->fan, e->aux, e->fork_ev,
-                     e->join_ev, e->side, e->side_fork, e->side_join));
+                     e->join_ev, e->side, e->side_fork, e->side_join, &e->n_copy_launches));
   if (e->timing) DLO_CUDA(cudaEventRecord(t.b, e->copy));
   DLO_CUDA(cudaEventRecord(e->ready[slot], e->copy));
   e->slot_holds[slot] = block;
@@ -973,6 +978,7 @@ dlo_status dlo_engine_query(dlo_engine* e, dlo_engine_stats* out) {
   out->n_direct_prefetches = static_cast<int32_t>(e->n_direct);
   out->n_packed_prefetches = static_cast<int32_t>(e->n_packed);
   out->pack_ms = e->pack_ms;
+  out->n_copy_kernel_launches = static_cast<int32_t>(e->n_copy_launches);
   return DLO_OK;
 }
 

@@ -236,6 +236,20 @@ size_t dlo_forward_scratch_bytes(const dlo_dit_cfg* cfg) {
   return dlo::scratch_layout(*cfg).total;
 }
 
+int32_t dlo_forward_launches(const dlo_dit_cfg* cfg) {
+  using namespace dlo;
+  if (check_cfg(cfg) != DLO_OK) return 0;
+  const int64_t M = static_cast<int64_t>(cfg->batch) * cfg->tokens, d = cfg->hidden,
+                f = cfg->mlp;
+  // norm x2, QKV linear, attention; out-projection, fc1, fc2 (+ reduction each
+  // when split), as launch_all issues them
+  int32_t n = 4;
+  n += linear_splits(M, d, d, EPI_RESID_F32) > 1 ? 2 : 1;
+  n += linear_splits(M, f, d, EPI_GELU_BF16) > 1 ? 2 : 1;
+  n += linear_splits(M, d, f, EPI_RESID_F32) > 1 ? 2 : 1;
+  return n;
+}
+
 dlo_status dlo_forward(const dlo_dit_cfg* cfg, const dlo_plan* plan, const void* block_base,
                        float* x, void* scratch, size_t scratch_bytes, void* stream) {
   return dlo::forward_impl(cfg, plan, block_base, x, scratch, scratch_bytes,

@@ -78,7 +78,8 @@ class EngineStats(ctypes.Structure):
     _fields_ = [("chosen_mode", c_i32), ("n_forwards", c_i32), ("n_prefetches", c_i32),
                 ("n_kernel_prefetches", c_i32), ("race_dma_us", ctypes.c_double),
                 ("race_kernel_us", ctypes.c_double), ("n_direct_prefetches", c_i32),
-                ("n_packed_prefetches", c_i32), ("pack_ms", ctypes.c_double)]
+                ("n_packed_prefetches", c_i32), ("pack_ms", ctypes.c_double),
+                ("n_copy_kernel_launches", c_i32)]
 
 
 _P = ctypes.POINTER
@@ -92,6 +93,7 @@ _SIGS = {
     "dlo_reassemble": (c_i32, [c_vp, _P(c_vp), c_vp, c_i32, c_vp]),
     "dlo_reassemble_staged": (c_i32, [c_vp, _P(c_vp), c_vp, c_i64, c_vp, c_vp, c_vp]),
     "dlo_forward_scratch_bytes": (c_sz, [_P(DitCfg)]),
+    "dlo_forward_launches": (c_i32, [_P(DitCfg)]),
     "dlo_forward": (c_i32, [_P(DitCfg), c_vp, c_vp, c_vp, c_vp, c_sz, c_vp]),
     "dlo_forward_noalloc": (c_i32, [_P(DitCfg), c_vp, c_vp, c_vp, c_vp]),
     "dlo_op_rmsnorm_mod": (c_i32, [c_vp, c_i64, c_i64, c_vp, c_vp, c_vp, c_f32, c_vp, c_vp]),
@@ -273,6 +275,10 @@ FWD_GRAPH = 1
 def dit_cfg(batch, tokens, hidden, heads, mlp, eps=1e-6, graph=True):
     return DitCfg(int(batch), int(tokens), int(hidden), int(heads), int(mlp), float(eps),
                   FWD_GRAPH if graph else 0)
+
+
+def forward_launches(cfg):
+    return int(lib().dlo_forward_launches(ctypes.byref(cfg)))
 
 
 def forward_scratch_bytes(cfg):

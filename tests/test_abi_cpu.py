@@ -211,3 +211,13 @@ def test_scratch_bytes_cover_the_buffers():
     cfg = dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp)
     M, d, f = w.tokens, w.hidden, w.mlp
     assert dlo.forward_scratch_bytes(cfg) >= 2 * M * (d + 3 * d + d + f)
+
+
+def test_forward_launch_count():
+    # norms, QKV, attention, and the three other linears with a reduction each
+    # when split into K slices
+    for name in ("tiny", "odd", "nano", "super"):
+        w = W.CONFIGS[name]
+        n = dlo.forward_launches(dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp))
+        assert 7 <= n <= 10
+    assert dlo.forward_launches(dlo.dit_cfg(1, 16, 96, 1, 256)) == 0       # invalid config
