@@ -325,31 +325,48 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
         }
         umma_commit(&empty[0]);
       }
+      // The barriers a group needs are tested (non-blocking) while the
+      // previous group's MMAs issue and the result is used after them, so
+      // the shared-memory reads overlap MMA issue; only a barrier found not
+      // ready is waited on.  pre0 / pre1: PV_0 / PV_1's inputs known ready.
+      auto test_load = [&](int i) {
+        return mbar_test(&full[i % NS], static_cast<uint32_t>((i / NS) & 1));
+      };
+      bool pre0 = false, pre1 = false;
       for (int j = 0; ok && j < n_kv; ++j) {
         const uint32_t par = static_cast<uint32_t>(j & 1);
         const int iv = 2 * j + 1, ik = 2 * j + 2;
         const bool more = j + 1 < n_kv;
-        if (!mbar_wait_bounded(&p_full[0], par, abort) || !wait_load(iv)) {
+        if (!pre0 && (!mbar_wait_bounded(&p_full[0], par, abort) || !wait_load(iv))) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const bool k_ready = more && test_load(ik);
         mma_pv(0, iv % NS, j > 0);
         if (nt == 1) umma_commit(&empty[iv % NS]);
         if (more) {
-          if (!wait_load(ik)) {
+          if (!k_ready && !wait_load(ik)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          const bool nxt = nt == 2 ? mbar_test(&p_full[1], par)
+                                   : mbar_test(&p_full[0], par ^ 1u) && test_load(ik + 1);
           mma_s(0, ik % NS);
           umma_commit(&s_full[0]);
-          if (nt == 1) umma_commit(&empty[ik % NS]);
+          if (nt == 1) {
+            umma_commit(&empty[ik % NS]);
+            pre0 = nxt;
+            continue;
+          }
+          pre1 = nxt;
         } else {
           umma_commit(&o_done[0]);
+          if (nt == 1) continue;
+          pre1 = false;
         }
-        if (nt == 1) continue;
-        if (!mbar_wait_bounded(&p_full[1], par, abort)) {
+        if (!pre1 && !mbar_wait_bounded(&p_full[1], par, abort)) {
           ok = false;
           break;
         }
@@ -357,6 +374,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
         mma_pv(1, iv % NS, j > 0);
         umma_commit(&empty[iv % NS]);
         if (more) {
+          pre0 = mbar_test(&p_full[0], par ^ 1u) && test_load(ik + 1);
           mma_s(1, ik % NS);
           umma_commit(&empty[ik % NS]);
           umma_commit(&s_full[1]);

@@ -65,6 +65,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of a phase (mbarrier.test_wait): never suspends.  Its
+// result is meant to be consumed later, so that the shared-memory read
+// overlaps other issue (an MMA thread tests the next stage's barrier before
+// issuing the current stage's MMAs).
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // As mbar_try_wait, but a thread whose phase is not complete yet is
 // suspended until it completes or about hint_ns pass, so that waiting warps
 // leave the issue slots of their SM sub-partition to the warps that work.
