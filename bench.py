@@ -175,6 +175,42 @@ def oracle_block_rate(w, seconds, seed=0):
     return n / el, n, el, threads
 
 
+def oracle_extras(w, seed=0, seconds=3.0):
+    """The oracle's other two figures: its shard-reassembly throughput on the
+    bf16 group of one block of `w` (element-wise copies, one thread), and its
+    block-forward rate on one thread, taken on the tiny workload (a
+    one-thread forward of the larger ones takes minutes)."""
+    import numpy as np
+    import oracle
+    from layerwise_weight_offload_gb300 import workloads as W
+    rng = np.random.default_rng(seed)
+    n = w.bf16_numel()
+    flat = rng.integers(0, 256, size=2 * n, dtype=np.uint8)
+    shards = oracle.shard(flat, n, 2, w.shards)
+    S = oracle.shard_numel(n, w.shards)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.reassemble(shards, S, 2)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds / 2:
+            break
+    gbs = reps * w.shards * S * 2 / ((time.perf_counter() - t0) * 1e9)
+    t = W.CONFIGS["tiny"]
+    p = {k: v.float().numpy() for k, v in W.gen_block(t, 0, seed).items()}
+    x = W.gen_x(t, seed).numpy()
+    k, t0 = 0, time.perf_counter()
+    while True:
+        oracle.block_forward(x, p, t.batch, t.tokens, t.hidden, t.heads, t.mlp, t.eps, threads=1)
+        k += 1
+        if time.perf_counter() - t0 >= seconds / 2:
+            break
+    return {"oracle_reassemble_gbs": gbs,
+            "oracle_reassemble_sample": "%d reassemblies of the %s bf16 group (%d shards)"
+                                        % (reps, w.name, w.shards),
+            "one_thread_tiny_block_fwd_per_s": k / (time.perf_counter() - t0),
+            "one_thread_sample": "%d fp64 oracle forwards of a tiny block on 1 thread" % k}
+
+
 def run_reference(args, ws, rank):
     """The oracle as the reference arm: K timed steps of one oracle block
     forward each (after W untimed), on the host cores."""
@@ -397,7 +433,8 @@ def run_ours(args, ws, rank, local):
         v, n, el, threads = oracle_block_rate(w, args.cpu_seconds, args.seed)
         cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": "%d fp64 oracle block forward(s) of host block 0 of %s in %.1f s; "
-                         "the oracle's reassembly is not included" % (n, w.name, el)}
+                         "the oracle's reassembly is not included" % (n, w.name, el),
+               **oracle_extras(w, args.seed)}
 
     copy_name = {"kernel": "copy_reassemble_kernel",
                  "staged": "cudaMemcpyAsync into staging (copy engines), then a device gather"}.get(
