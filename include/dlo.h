@@ -423,6 +423,13 @@ typedef struct {
   int64_t host_staging_bytes; /* capacity of each (>= a packed block's
                              slot_bytes) */
   int32_t pack_threads;   /* CPU threads that pack a block (0 = 4) */
+  int32_t two_copy_streams;/* 0 (default): every prefetch on copy_stream,
+                             as the pages draw it; 1: prefetches into slot 1
+                             on a second, library-owned stream, so that the
+                             copies of consecutive blocks may overlap at their
+                             ends (each still waits for its slot's free
+                             event).  Measured on GB300 with one H2D link: no
+                             gain, the copy engines run them one at a time */
 } dlo_engine_desc;
 
 typedef struct {
@@ -544,6 +551,14 @@ typedef struct {
 } dlo_engine_stats;
 dlo_status dlo_engine_query(dlo_engine* e, dlo_engine_stats* out);
 dlo_status dlo_engine_copy_times(dlo_engine* e, float* copy_ms, int64_t* copy_bytes,
+                                 int32_t cap, int32_t* n_out);
+/* With timing = 1: each prefetch's start and end (ms) on one clock, counted
+ * from the first timed prefetch's start, for the first `cap` prefetches;
+ * *n_out = how many were timed.  Prefetches into the two slots may overlap
+ * (two copy streams), so the copy engines' busy time is the union of these
+ * intervals, not the sum of copy_times.  Blocks until the spans' end events
+ * have completed. */
+dlo_status dlo_engine_copy_spans(dlo_engine* e, float* start_ms, float* end_ms,
                                  int32_t cap, int32_t* n_out);
 
 /* Waits (host side, bounded by timeout_ms) for both streams' enqueued

@@ -142,6 +142,11 @@ struct dlo_engine {
   uint8_t* slot[2] = {nullptr, nullptr};
   int64_t slot_bytes = 0;
   cudaStream_t compute = nullptr, copy = nullptr;
+  // prefetches into slot x run on slot_copy[x]: the caller's copy stream,
+  // or for slot 1 a library-owned one with two_copy_streams, so that
+  // consecutive block copies may overlap at their ends
+  cudaStream_t slot_copy[2] = {nullptr, nullptr};
+  cudaStream_t own_copy = nullptr;
   int32_t mode = DLO_COPY_AUTO;
   int32_t copy_ctas = 0;
   bool timing = false;
@@ -484,6 +489,7 @@ constexpr int kHostStagingWaitMs = 60000;
 // their slot offsets inside it, then one DMA moves the packed block.
 dlo_status prefetch_source(dlo_engine* e, int32_t block, int32_t slot) {
   const dlo_engine::Block& b = e->blocks[block];
+  cudaStream_t cs = e->slot_copy[slot];
   dlo_engine::Timed t{};
   if (e->timing) {
     DLO_TRY(make_timed(&t));
@@ -492,11 +498,11 @@ dlo_status prefetch_source(dlo_engine* e, int32_t block, int32_t slot) {
     e->timed.push_back(t);
   }
   if (b.direct) {
-    DLO_CUDA(cudaStreamWaitEvent(e->copy, e->freed[slot], 0));
-    if (e->timing) DLO_CUDA(cudaEventRecord(t.a, e->copy));
+    DLO_CUDA(cudaStreamWaitEvent(cs, e->freed[slot], 0));
+    if (e->timing) DLO_CUDA(cudaEventRecord(t.a, cs));
     for (const auto& s : b.src)
       DLO_CUDA(cudaMemcpyAsync(e->slot[slot] + s.off, s.p, static_cast<size_t>(s.bytes),
-                               cudaMemcpyHostToDevice, e->copy));
+                               cudaMemcpyHostToDevice, cs));
     e->n_direct++;
   } else {
     const auto t0 = std::chrono::steady_clock::now();
@@ -511,17 +517,17 @@ dlo_status prefetch_source(dlo_engine* e, int32_t block, int32_t slot) {
     e->pool->run(tasks);
     e->pack_ms += std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0)
                       .count();
-    DLO_CUDA(cudaStreamWaitEvent(e->copy, e->freed[slot], 0));
-    if (e->timing) DLO_CUDA(cudaEventRecord(t.a, e->copy));
+    DLO_CUDA(cudaStreamWaitEvent(cs, e->freed[slot], 0));
+    if (e->timing) DLO_CUDA(cudaEventRecord(t.a, cs));
     DLO_CUDA(cudaMemcpyAsync(e->slot[slot], e->host_staging[slot],
                              static_cast<size_t>(b.plan->slot_bytes), cudaMemcpyHostToDevice,
-                             e->copy));
-    DLO_CUDA(cudaEventRecord(e->hs_read[slot], e->copy));
+                             cs));
+    DLO_CUDA(cudaEventRecord(e->hs_read[slot], cs));
     e->hs_pending[slot] = true;
     e->n_packed++;
   }
-  if (e->timing) DLO_CUDA(cudaEventRecord(t.b, e->copy));
-  DLO_CUDA(cudaEventRecord(e->ready[slot], e->copy));
+  if (e->timing) DLO_CUDA(cudaEventRecord(t.b, cs));
+  DLO_CUDA(cudaEventRecord(e->ready[slot], cs));
   e->slot_holds[slot] = block;
   e->n_prefetches++;
   return DLO_OK;
@@ -531,6 +537,7 @@ dlo_status prefetch_source(dlo_engine* e, int32_t block, int32_t slot) {
 dlo_status enqueue_prefetch(dlo_engine* e, int32_t block, int32_t slot, int64_t issued_by_k,
                             int32_t* used_mode = nullptr) {
   const dlo_engine::Block& b = e->blocks[block];
+  cudaStream_t cs = e->slot_copy[slot];
   if (b.source) {
     if (used_mode) *used_mode = DLO_COPY_DMA;
     return prefetch_source(e, block, slot);
@@ -540,18 +547,18 @@ dlo_status enqueue_prefetch(dlo_engine* e, int32_t block, int32_t slot, int64_t 
   if (mode == DLO_COPY_STAGED) {
     // H2D into staging[slot] once the gather that last read it is done;
     // the gather then waits for the H2D and for the slot's free event
-    DLO_CUDA(cudaStreamWaitEvent(e->copy, e->stage_free[slot], 0));
+    DLO_CUDA(cudaStreamWaitEvent(cs, e->stage_free[slot], 0));
     dlo_engine::Timed t{};
     if (e->timing) {
       DLO_TRY(make_timed(&t));
       t.bytes = b.bytes;
       t.mode = mode;
       e->timed.push_back(t);
-      DLO_CUDA(cudaEventRecord(t.a, e->copy));
+      DLO_CUDA(cudaEventRecord(t.a, cs));
     }
-    DLO_TRY(stage_h2d(b, e->staging[slot], e->copy));
-    if (e->timing) DLO_CUDA(cudaEventRecord(t.b, e->copy));
-    DLO_CUDA(cudaEventRecord(e->staged[slot], e->copy));
+    DLO_TRY(stage_h2d(b, e->staging[slot], cs));
+    if (e->timing) DLO_CUDA(cudaEventRecord(t.b, cs));
+    DLO_CUDA(cudaEventRecord(e->staged[slot], cs));
     DLO_CUDA(cudaStreamWaitEvent(e->gather, e->staged[slot], 0));
     DLO_CUDA(cudaStreamWaitEvent(e->gather, e->freed[slot], 0));
     DLO_TRY(stage_gather(b.plan, e->staging[slot], e->slot[slot], e->copy_ctas, e->gather));
@@ -562,19 +569,19 @@ dlo_status enqueue_prefetch(dlo_engine* e, int32_t block, int32_t slot, int64_t 
     e->n_prefetches++;
     return DLO_OK;
   }
-  DLO_CUDA(cudaStreamWaitEvent(e->copy, e->freed[slot], 0));
+  DLO_CUDA(cudaStreamWaitEvent(cs, e->freed[slot], 0));
   dlo_engine::Timed t{};
   if (e->timing) {
     DLO_TRY(make_timed(&t));
     t.bytes = b.bytes;
     t.mode = mode;
     e->timed.push_back(t);
-    DLO_CUDA(cudaEventRecord(t.a, e->copy));
+    DLO_CUDA(cudaEventRecord(t.a, cs));
   }
-  DLO_TRY(copy_block(b, e->slot[slot], mode, e->copy_ctas, e->copy, e->fan, e->aux, e->fork_ev,
+  DLO_TRY(copy_block(b, e->slot[slot], mode, e->copy_ctas, cs, e->fan, e->aux, e->fork_ev,
                      e->join_ev, e->side, e->side_fork, e->side_join, &e->n_copy_launches));
-  if (e->timing) DLO_CUDA(cudaEventRecord(t.b, e->copy));
-  DLO_CUDA(cudaEventRecord(e->ready[slot], e->copy));
+  if (e->timing) DLO_CUDA(cudaEventRecord(t.b, cs));
+  DLO_CUDA(cudaEventRecord(e->ready[slot], cs));
   e->slot_holds[slot] = block;
   e->n_prefetches++;
   if (mode == DLO_COPY_KERNEL) e->n_kernel_prefetches++;
@@ -601,6 +608,7 @@ void release(dlo_engine* e) {
     if (e->hs_read[s]) cudaEventDestroy(e->hs_read[s]);
   }
   delete e->pool;
+  if (e->own_copy) cudaStreamDestroy(e->own_copy);
   for (auto& t : e->timed) {
     cudaEventDestroy(t.a);
     cudaEventDestroy(t.b);
@@ -677,6 +685,7 @@ dlo_status dlo_engine_create(const dlo_engine_desc* d, dlo_engine** out) {
   e->slot_bytes = d->slot_bytes;
   e->compute = static_cast<cudaStream_t>(d->compute_stream);
   e->copy = static_cast<cudaStream_t>(d->copy_stream);
+  e->slot_copy[0] = e->slot_copy[1] = e->copy;
   e->mode = d->copy_mode;
   e->copy_ctas = d->copy_ctas;
   e->timing = d->timing != 0;
@@ -703,6 +712,10 @@ dlo_status dlo_engine_create(const dlo_engine_desc* d, dlo_engine** out) {
     e->host_staging_bytes = d->host_staging_bytes;
     for (int s = 0; s < 2; ++s)
       ok = ok && cudaEventCreateWithFlags(&e->hs_read[s], cudaEventDisableTiming) == cudaSuccess;
+  }
+  if (d->two_copy_streams) {
+    ok = ok && cudaStreamCreateWithFlags(&e->own_copy, cudaStreamNonBlocking) == cudaSuccess;
+    e->slot_copy[1] = e->own_copy;
   }
   e->pool = new (std::nothrow) PackPool(d->pack_threads > 0 ? d->pack_threads : 4);
   ok = ok && e->pool != nullptr;
@@ -1003,13 +1016,37 @@ dlo_status dlo_engine_copy_times(dlo_engine* e, float* copy_ms, int64_t* copy_by
   return DLO_OK;
 }
 
+dlo_status dlo_engine_copy_spans(dlo_engine* e, float* start_ms, float* end_ms, int32_t cap,
+                                 int32_t* n_out) {
+  using namespace dlo;
+  DLO_TRY(check_engine(e));
+  if (!n_out || (cap > 0 && (!start_ms || !end_ms)))
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_copy_spans: null argument");
+  int32_t n = 0;
+  for (const auto& t : e->timed) {
+    if (n < cap) {
+      DLO_CUDA(cudaEventSynchronize(t.b));
+      float a = 0, b = 0;
+      DLO_CUDA(cudaEventElapsedTime(&a, e->timed.front().a, t.a));
+      DLO_CUDA(cudaEventElapsedTime(&b, e->timed.front().a, t.b));
+      start_ms[n] = a;
+      end_ms[n] = b;
+    }
+    ++n;
+  }
+  *n_out = n;
+  return DLO_OK;
+}
+
 dlo_status dlo_engine_destroy(dlo_engine* e, int32_t timeout_ms) {
   using namespace dlo;
   if (!e) return DLO_OK;
   // drain the streams (bounded): mark their current tails and poll
-  cudaEvent_t tail[3] = {nullptr, nullptr, nullptr};
-  cudaStream_t st[3] = {e->copy, e->compute, e->gather};
-  const int n = e->gather ? 3 : 2;
+  cudaEvent_t tail[4] = {nullptr, nullptr, nullptr, nullptr};
+  cudaStream_t st[4] = {e->copy, e->compute, nullptr, nullptr};
+  int n = 2;
+  if (e->own_copy) st[n++] = e->own_copy;
+  if (e->gather) st[n++] = e->gather;
   auto drop = [&]() {
     for (int i = 0; i < n; ++i)
       if (tail[i]) cudaEventDestroy(tail[i]);

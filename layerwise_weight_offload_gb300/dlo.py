@@ -66,7 +66,7 @@ class EngineDesc(ctypes.Structure):
                 ("copy_ctas", c_i32), ("timing", c_i32), ("dma_streams", c_i32),
                 ("staging", c_vp * 2), ("staging_bytes", c_i64), ("gather_stream", c_vp),
                 ("host_staging", c_vp * 2), ("host_staging_bytes", c_i64),
-                ("pack_threads", c_i32)]
+                ("pack_threads", c_i32), ("two_copy_streams", c_i32)]
 
 
 class SchedEvent(ctypes.Structure):
@@ -119,6 +119,7 @@ _SIGS = {
     "dlo_schedule_log": (c_i32, [c_vp, _P(SchedEvent), c_i32, _P(c_i32)]),
     "dlo_engine_query": (c_i32, [c_vp, _P(EngineStats)]),
     "dlo_engine_copy_times": (c_i32, [c_vp, _P(c_f32), _P(c_i64), c_i32, _P(c_i32)]),
+    "dlo_engine_copy_spans": (c_i32, [c_vp, _P(c_f32), _P(c_f32), c_i32, _P(c_i32)]),
     "dlo_engine_destroy": (c_i32, [c_vp, c_i32]),
     "dlo_kernel_status": (c_i32, [_P(c_i32)]),
     "dlo_last_error": (ctypes.c_char_p, []),
@@ -364,7 +365,7 @@ class Engine:
     def __init__(self, n_blocks, slot0, slot1, slot_bytes, compute_stream, copy_stream,
                  copy_mode=COPY_AUTO, copy_ctas=0, timing=False, dma_streams=0,
                  staging=None, staging_bytes=0, gather_stream=None, host_staging=None,
-                 host_staging_bytes=0, pack_threads=0):
+                 host_staging_bytes=0, pack_threads=0, two_copy_streams=False):
         """staging: two device buffers (and gather_stream) for COPY_STAGED;
         host_staging: two page-locked host buffers for rank-local source
         blocks whose parameters are pageable."""
@@ -389,6 +390,7 @@ class Engine:
             d.host_staging[1] = _ptr(host_staging[1])
         d.host_staging_bytes = int(host_staging_bytes)
         d.pack_threads = int(pack_threads)
+        d.two_copy_streams = 1 if two_copy_streams else 0
         h = c_vp()
         _check(lib().dlo_engine_create(ctypes.byref(d), ctypes.byref(h)), "dlo_engine_create")
         self.handle = h.value
@@ -452,6 +454,17 @@ class Engine:
         _check(lib().dlo_engine_copy_times(self.handle, ms, by, n.value, ctypes.byref(n)),
                "dlo_engine_copy_times")
         return list(ms[:n.value]), list(by[:n.value])
+
+    def copy_spans(self):
+        """[(start_ms, end_ms)] of every timed prefetch, on one clock."""
+        n = c_i32()
+        _check(lib().dlo_engine_copy_spans(self.handle, None, None, 0, ctypes.byref(n)),
+               "dlo_engine_copy_spans")
+        s = (c_f32 * max(1, n.value))()
+        t = (c_f32 * max(1, n.value))()
+        _check(lib().dlo_engine_copy_spans(self.handle, s, t, n.value, ctypes.byref(n)),
+               "dlo_engine_copy_spans")
+        return list(zip(s[:n.value], t[:n.value]))
 
     def destroy(self, timeout_ms=60000):
         if self.handle:

@@ -43,14 +43,16 @@ def _small(name, **kw):
     return W.Workload(**base)
 
 
+@pytest.mark.parametrize("two_streams", [False, True])
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("n_blocks,steps", [(1, 3), (2, 2), (3, 2), (9, 3), (8, 1)])
-def test_schedule_and_slot_contents(n_blocks, steps, mode):
-    # small blocks so that every slot can be snapshotted
+def test_schedule_and_slot_contents(n_blocks, steps, mode, two_streams):
+    # small blocks so that every slot can be snapshotted; with two_streams
+    # slot 1's prefetches run on a second copy stream
     w = W.custom("sched", n_blocks=n_blocks, hidden=256, heads=4, mlp=1024, tokens=64,
                  shards=3, steps=steps, distinct=min(n_blocks, 3))
     host = HostBlocks(w, seed=5, keep_params=True)
-    st = StreamedStack(host, copy_mode=mode)
+    st = StreamedStack(host, copy_mode=mode, two_copy_streams=two_streams)
     images = [_slot_image(host, hb) for hb in range(w.distinct)]
     st.prime()
     snaps = []
@@ -289,5 +291,35 @@ def test_auto_races_on_forward_time():
         want = dlo.COPY_KERNEL if win % 2 else dlo.COPY_DMA
         assert modes[s0 + 6 * win:s0 + 6 * win + 6] == [want] * 6
     assert s.n_kernel_prefetches >= 12
+    st.close()
+    host.close()
+
+
+@pytest.mark.parametrize("two_streams", [False, True])
+def test_copy_spans(two_streams):
+    # the spans sit on one clock: per slot they follow one another, each
+    # lasts what copy_times says, and their union is no longer than the sum
+    w = W.custom("spans", n_blocks=4, hidden=512, heads=4, mlp=2048, tokens=64, shards=2,
+                 steps=3)
+    host = HostBlocks(w, seed=2)
+    st = StreamedStack(host, copy_mode=dlo.COPY_DMA, timing=True, two_copy_streams=two_streams)
+    x = W.gen_x(w, seed=2, device="cuda")
+    torch.cuda.synchronize()
+    for _ in range(w.steps):
+        st.step(x)
+    torch.cuda.synchronize()
+    ms, _ = st.engine.copy_times()
+    spans = st.engine.copy_spans()
+    assert len(spans) == len(ms) == w.n_blocks * w.steps + 1
+    assert spans[0][0] == 0.0
+    for (s, e), d in zip(spans, ms):
+        assert e >= s and abs((e - s) - d) <= 1e-3 + 1e-3 * d
+    for slot in (0, 1):
+        mine = spans[slot::2]                 # prefetch k fills slot k % 2
+        for (s0, e0), (s1, e1) in zip(mine, mine[1:]):
+            assert s1 >= e0 - 1e-3
+    if not two_streams:
+        for (s0, e0), (s1, e1) in zip(spans, spans[1:]):
+            assert s1 >= e0 - 1e-3
     st.close()
     host.close()
