@@ -292,7 +292,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
       const uint64_t dq = sdesc_k_sw128(smem_u32(sQ));
       const uint64_t dkv = sdesc_k_sw128(smem_u32(sKV));
       auto wait_load = [&](int i) {
-        return mbar_wait_bounded(&full[i % NS], static_cast<uint32_t>((i / NS) & 1), abort);
+        return mbar_wait_spin(&full[i % NS], static_cast<uint32_t>((i / NS) & 1), abort);
       };
       // S_t = Q_t K^T with K in stage s
       auto mma_s = [&](int t, int s) {
@@ -337,7 +337,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
         const uint32_t par = static_cast<uint32_t>(j & 1);
         const int iv = 2 * j + 1, ik = 2 * j + 2;
         const bool more = j + 1 < n_kv;
-        if (!pre0 && (!mbar_wait_bounded(&p_full[0], par, abort) || !wait_load(iv))) {
+        if (!pre0 && (!mbar_wait_spin(&p_full[0], par, abort) || !wait_load(iv))) {
           ok = false;
           break;
         }
@@ -366,7 +366,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
           if (nt == 1) continue;
           pre1 = false;
         }
-        if (!pre1 && !mbar_wait_bounded(&p_full[1], par, abort)) {
+        if (!pre1 && !mbar_wait_spin(&p_full[1], par, abort)) {
           ok = false;
           break;
         }

@@ -179,7 +179,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
         const int kb1 = static_cast<int>(static_cast<int64_t>(ks + 1) * num_k / splits);
         const int m_idx = tile % num_m, n_idx = tile / num_m;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, abort)) {
+          if (!mbar_wait_spin(&empty[stage], phase ^ 1u, abort)) {
             record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_PRODUCER);
             ok = false;
             break;
@@ -229,7 +229,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait_bounded(&full[stage], phase, abort)) {
+          if (!mbar_wait_spin(&full[stage], phase, abort)) {
             record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_MMA_FULL);
             ok = false;
             break;

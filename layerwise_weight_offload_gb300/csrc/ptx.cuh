@@ -112,6 +112,23 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// As mbar_wait_bounded, but spinning on the non-blocking test: a thread
+// that must react within a few cycles of the phase completing (an MMA issuer
+// waiting for its operands) does not pay the wake-up of a suspended wait.
+// Bounded the same way; *abort and the clock are read every 256 tests.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_test(bar, parity)) return true;
+    if ((n & 255u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+    }
+  }
+}
+
 // ---- TMA -----------------------------------------------------------------
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
