@@ -260,14 +260,15 @@ typedef struct {
 enum { DLO_FWD_GRAPH = 1 };
 
 /* Bytes of device scratch one block forward needs (bf16 h, qkv, V
- * transposed, o, u, and the fp32 split-K workspace of its narrow linears).
- * The split choice depends on the device's SM count. */
+ * transposed, o, u, and the fp32 workspace of the linears run as K slices:
+ * every tile when there are fewer tiles than SMs, or only the tiles of a
+ * short last wave).  The split choice depends on the device's SM count. */
 size_t dlo_forward_scratch_bytes(const dlo_dit_cfg* cfg);
 
 /* Number of kernel launches one dlo_forward (or dlo_forward_noalloc) makes
- * for this configuration — two norm launches, the QKV linear, attention,
- * and for the out-projection, fc1 and fc2 one GEMM each plus one ordered
- * reduction when the linear runs as K slices (the split depends on the
+ * for this configuration — two norm launches, attention, and for each of
+ * the four linears (QKV, out-projection, fc1, fc2) one GEMM plus one ordered
+ * reduction when some of its tiles run as K slices (the split depends on the
  * current device's SM count; 152 when none is visible) — or 0 for an
  * invalid configuration.  Launches nothing. */
 int32_t dlo_forward_launches(const dlo_dit_cfg* cfg);

@@ -332,17 +332,30 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
       auto test_load = [&](int i) {
         return mbar_test(&full[i % NS], static_cast<uint32_t>((i / NS) & 1));
       };
+      // pre0 also covers K_{j+1}; without it, the loads (almost always
+      // ready) are checked before the wait for P, so that only that one
+      // barrier read stands between the softmax finishing and the PV issue.
+      auto next_ready = [&](int ik_next) {
+        return test_load(ik_next - 1) && (ik_next >= 2 * n_kv || test_load(ik_next));
+      };
       bool pre0 = false, pre1 = false;
       for (int j = 0; ok && j < n_kv; ++j) {
         const uint32_t par = static_cast<uint32_t>(j & 1);
         const int iv = 2 * j + 1, ik = 2 * j + 2;
         const bool more = j + 1 < n_kv;
-        if (!pre0 && (!mbar_wait_spin(&p_full[0], par, abort) || !wait_load(iv))) {
-          ok = false;
-          break;
+        bool k_ready = more;
+        if (!pre0) {
+          if (!wait_load(iv)) {
+            ok = false;
+            break;
+          }
+          k_ready = more && test_load(ik);
+          if (!mbar_wait_spin(&p_full[0], par, abort)) {
+            ok = false;
+            break;
+          }
         }
         tc_fence_after();
-        const bool k_ready = more && test_load(ik);
         mma_pv(0, iv % NS, j > 0);
         if (nt == 1) umma_commit(&empty[iv % NS]);
         if (more) {
@@ -352,7 +365,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
           }
           tc_fence_after();
           const bool nxt = nt == 2 ? mbar_test(&p_full[1], par)
-                                   : mbar_test(&p_full[0], par ^ 1u) && test_load(ik + 1);
+                                   : mbar_test(&p_full[0], par ^ 1u) && next_ready(ik + 2);
           mma_s(0, ik % NS);
           umma_commit(&s_full[0]);
           if (nt == 1) {
@@ -374,7 +387,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
         mma_pv(1, iv % NS, j > 0);
         umma_commit(&empty[iv % NS]);
         if (more) {
-          pre0 = mbar_test(&p_full[0], par ^ 1u) && test_load(ik + 1);
+          pre0 = mbar_test(&p_full[0], par ^ 1u) && next_ready(ik + 2);
           mma_s(1, ik % NS);
           umma_commit(&empty[ik % NS]);
           umma_commit(&s_full[1]);

@@ -129,8 +129,19 @@ struct EpiArgs {
   size_t ws_bytes;
   int64_t ws_rows;      // M, set for the partial epilogue
 };
-// K slices a linear of this shape is split into (1: no split; the QKV
-// epilogue never splits) and the fp32 workspace that needs.
+// How a linear of this shape is run on this GPU's SMs: `splits` K slices
+// for every tile (fewer tiles than SMs), or `tail_splits` K slices for the
+// last `tail` tiles only (a last wave of at most half the SMs); the fp32
+// workspace that needs and the kernel launches (2 with a reduction).
+// Without a large enough workspace a linear runs unsplit.
+struct LinearPlan {
+  int splits;
+  int tail;
+  int tail_splits;
+  size_t ws_bytes;
+  int launches;
+};
+LinearPlan linear_plan(int64_t M, int64_t N, int64_t K, int epilogue);
 int linear_splits(int64_t M, int64_t N, int64_t K, int epilogue);
 size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int epilogue);
 dlo_status launch_linear(const uint16_t* a, int64_t M, int64_t K,

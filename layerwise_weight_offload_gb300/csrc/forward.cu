@@ -26,7 +26,8 @@ struct ScratchLayout {
 
 // Scratch of one forward: bf16 h [M, d] (both norms), qkv [M, 3d] (Q and K
 // used), vt [batch*d, vt_ld] (V transposed), o [M, d], u [M, f], and the
-// fp32 split-K workspace of the largest split linear (0 if none splits).
+// fp32 K-slice workspace of the linear that needs the most (0 if none
+// splits; one buffer serves all four, as they run one after the other).
 ScratchLayout scratch_layout(const dlo_dit_cfg& c) {
   const size_t M = static_cast<size_t>(c.batch) * c.tokens;
   const size_t d = c.hidden, f = c.mlp;
@@ -40,7 +41,8 @@ ScratchLayout scratch_layout(const dlo_dit_cfg& c) {
   s.u = r(s.o + M * d * 2);
   s.ws = r(s.u + M * f * 2);
   const int64_t Mi = static_cast<int64_t>(M), di = c.hidden, fi = c.mlp;
-  size_t w = linear_workspace_bytes(Mi, di, di, EPI_RESID_F32);
+  size_t w = linear_workspace_bytes(Mi, 3 * di, di, EPI_QKV);
+  w = std::max(w, linear_workspace_bytes(Mi, di, di, EPI_RESID_F32));
   w = std::max(w, linear_workspace_bytes(Mi, fi, di, EPI_GELU_BF16));
   w = std::max(w, linear_workspace_bytes(Mi, di, fi, EPI_RESID_F32));
   s.ws_bytes = w;
@@ -110,6 +112,8 @@ dlo_status launch_all(const dlo_dit_cfg* cfg, const dlo_plan* plan, const Scratc
   qa.vt_ld = sl.vt_ld;
   qa.tokens = cfg->tokens;
   qa.v_col0 = static_cast<int>(2 * d);
+  qa.ws = ws;
+  qa.ws_bytes = sl.ws_bytes;
   DLO_TRY(launch_linear_ex(h, M, d, H(R_WQKV), 3 * d, EPI_QKV, qa, stream));
   DLO_TRY(launch_attention_vt(qkv, vt, sl.vt_ld, cfg->batch, cfg->tokens, d, cfg->heads, o,
                               stream));
@@ -241,12 +245,13 @@ int32_t dlo_forward_launches(const dlo_dit_cfg* cfg) {
   if (check_cfg(cfg) != DLO_OK) return 0;
   const int64_t M = static_cast<int64_t>(cfg->batch) * cfg->tokens, d = cfg->hidden,
                 f = cfg->mlp;
-  // norm x2, QKV linear, attention; out-projection, fc1, fc2 (+ reduction each
-  // when split), as launch_all issues them
-  int32_t n = 4;
-  n += linear_splits(M, d, d, EPI_RESID_F32) > 1 ? 2 : 1;
-  n += linear_splits(M, f, d, EPI_GELU_BF16) > 1 ? 2 : 1;
-  n += linear_splits(M, d, f, EPI_RESID_F32) > 1 ? 2 : 1;
+  // norm x2, attention; the four linears (+ a reduction each when split),
+  // as launch_all issues them
+  int32_t n = 3;
+  n += linear_plan(M, 3 * d, d, EPI_QKV).launches;
+  n += linear_plan(M, d, d, EPI_RESID_F32).launches;
+  n += linear_plan(M, f, d, EPI_GELU_BF16).launches;
+  n += linear_plan(M, d, f, EPI_RESID_F32).launches;
   return n;
 }
 

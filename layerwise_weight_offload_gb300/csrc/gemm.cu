@@ -15,9 +15,14 @@
 //   warps 2-5  epilogue: tcgen05.ld of their 32-lane quarter, the fused
 //              epilogue, stores to global; they release the accumulator so
 //              the next tile's MMAs overlap this tile's epilogue.
-// Ragged M, N and K are covered by TMA zero fill and epilogue masks.  No
-// split-K and no atomics: every output element is produced by one thread in
-// a fixed order, so results do not depend on addresses or scheduling.
+// Ragged M, N and K are covered by TMA zero fill and epilogue masks.
+// Work units: output tiles, or (tile, K slice) when K is split — for every
+// tile when there are too few tiles for the SMs, or only for the tiles of a
+// short last wave (the tail), which then spread over the idle SMs.  Split
+// units write fp32 partials to a workspace that a second kernel sums in slice
+// order before the epilogue.  No atomics: every output element is produced
+// by one thread in a fixed order, so results do not depend on addresses or
+// scheduling.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -117,7 +122,7 @@ template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
                     const __grid_constant__ CUtensorMap tma_b, int M, int N, int K,
-                    int splits, const EpiArgs ea, int* err) {
+                    int splits, int tail, int tail_splits, const EpiArgs ea, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -164,8 +169,24 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
   const int num_n = (N + BN - 1) / BN;
   const int num_tiles = num_m * num_n;
   const int num_k = (K + BK - 1) / BK;
-  // work unit u = (tile, K slice); slice ks covers k-blocks [kb0, kb1)
-  const int num_units = num_tiles * splits;
+  // work units: (tile, K slice of `splits`) for the first num_tiles - tail
+  // tiles, then (tail tile, K slice of `tail_splits`); slice ks of nks covers
+  // k-blocks [ks num_k / nks, (ks + 1) num_k / nks)
+  const int n_main = (num_tiles - tail) * splits;
+  const int num_units = n_main + tail * tail_splits;
+  auto unit_of = [&](int u, int& tile, int& ks, int& nks, int& tt) {
+    if (u < n_main) {
+      tile = u / splits;
+      ks = u - tile * splits;
+      nks = splits;
+      tt = -1;
+    } else {
+      tt = (u - n_main) / tail_splits;
+      ks = (u - n_main) - tt * tail_splits;
+      nks = tail_splits;
+      tile = num_tiles - tail + tt;
+    }
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -174,9 +195,10 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
       int issued = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const int tile = u / splits, ks = u - tile * splits;
-        const int kb0 = static_cast<int>(static_cast<int64_t>(ks) * num_k / splits);
-        const int kb1 = static_cast<int>(static_cast<int64_t>(ks + 1) * num_k / splits);
+        int tile, ks, nks, tt;
+        unit_of(u, tile, ks, nks, tt);
+        const int kb0 = static_cast<int>(static_cast<int64_t>(ks) * num_k / nks);
+        const int kb1 = static_cast<int>(static_cast<int64_t>(ks + 1) * num_k / nks);
         const int m_idx = tile % num_m, n_idx = tile / num_m;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_spin(&empty[stage], phase ^ 1u, abort)) {
@@ -218,9 +240,10 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const int ks = u % splits;
-        const int kb0 = static_cast<int>(static_cast<int64_t>(ks) * num_k / splits);
-        const int kb1 = static_cast<int>(static_cast<int64_t>(ks + 1) * num_k / splits);
+        int tile, ks, nks, tt;
+        unit_of(u, tile, ks, nks, tt);
+        const int kb0 = static_cast<int>(static_cast<int64_t>(ks) * num_k / nks);
+        const int kb1 = static_cast<int>(static_cast<int64_t>(ks + 1) * num_k / nks);
         if (!mbar_wait_bounded(&tempty[acc], acc_phase ^ 1u, abort)) {
           record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_MMA_EMPTY);
           ok = false;
@@ -266,8 +289,13 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
-      const int tile = u / splits, ks = u - tile * splits;
+      int tile, ks, nks, tt;
+      unit_of(u, tile, ks, nks, tt);
       const int m_idx = tile % num_m, n_idx = tile / num_m;
+      // a tail unit's fp32 partial: its own BM x BN block of the workspace
+      float* tail_ws = tt >= 0 ? ea.ws + (static_cast<int64_t>(tt) * tail_splits + ks) * BM * BN +
+                                     static_cast<int64_t>(quad * 32 + lane) * BN
+                               : nullptr;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tfull[acc], acc_phase, abort))) {
         if (lane == 0) record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_EPILOGUE);
         break;
@@ -283,7 +311,17 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c * 32, r);
         tmem_ld_wait();
-        if (row < M) epilogue_store<EPI>(r, row, n0, N, ks, ea);
+        if (row < M) {
+          if (tail_ws) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              *reinterpret_cast<float4*>(tail_ws + c * 32 + 4 * g) =
+                  make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                              __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+          } else {
+            epilogue_store<EPI>(r, row, n0, N, ks, ea);
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -326,19 +364,72 @@ void set_all_attrs() {
 
 template <int EPI>
 dlo_status launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int K,
-                      int splits, const EpiArgs& ea, int* err, cudaStream_t stream) {
+                      int splits, int tail, int tail_splits, const EpiArgs& ea, int* err,
+                      cudaStream_t stream) {
   set_all_attrs();
   DLO_CUDA(g_attr_err);
-  const int units = ((M + BM - 1) / BM) * ((N + BN - 1) / BN) * splits;
+  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int units = (tiles - tail) * splits + tail * tail_splits;
   const int grid = units < sm_count() ? units : sm_count();
-  gemm_tcgen05_kernel<EPI><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ma, mb, M, N, K, splits, ea,
-                                                                      err);
+  gemm_tcgen05_kernel<EPI><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
+      ma, mb, M, N, K, splits, tail, tail_splits, ea, err);
   DLO_CUDA(cudaGetLastError());
   return DLO_OK;
 }
 
-// Sums the K slices of a split linear in slice order and applies the
-// final epilogue (bf16 store, GELU-tanh, or gated residual).
+// The final epilogue (bf16 store, GELU-tanh, gated residual, or the QKV
+// split with V transposed) of four summed outputs at (row, c..c+3).
+template <int EPI>
+__device__ __forceinline__ void finish4(float4 acc, int64_t row, int64_t c, int64_t N,
+                                        const EpiArgs& ea) {
+  if (EPI == EPI_QKV && c >= ea.v_col0) {
+    // V columns (v_col0 is a multiple of 64, so all four are V): vt[b*d + c', t]
+    const int64_t b = row / ea.tokens, t = row - b * ea.tokens;
+    const int64_t d = ea.v_col0 / 2;
+    uint16_t* dst = ea.vt + (b * d + (c - ea.v_col0)) * ea.vt_ld + t;
+    const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat16 h = __float2bfloat16_rn(v[i]);
+      dst[static_cast<int64_t>(i) * ea.vt_ld] = *reinterpret_cast<uint16_t*>(&h);
+    }
+    return;
+  }
+  if (EPI == EPI_RESID_F32) {
+    float4* xp = reinterpret_cast<float4*>(static_cast<float*>(ea.out) + row * N + c);
+    const float4 gv = __ldg(reinterpret_cast<const float4*>(ea.gate + c));
+    float4 xv = *xp;
+    xv.x += gv.x * acc.x;
+    xv.y += gv.y * acc.y;
+    xv.z += gv.z * acc.z;
+    xv.w += gv.w * acc.w;
+    *xp = xv;
+  } else {
+    if (EPI == EPI_GELU_BF16) {
+      acc.x = gelu_tanh(acc.x);
+      acc.y = gelu_tanh(acc.y);
+      acc.z = gelu_tanh(acc.z);
+      acc.w = gelu_tanh(acc.w);
+    }
+    __nv_bfloat162 p0 = __floats2bfloat162_rn(acc.x, acc.y);
+    __nv_bfloat162 p1 = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&p0);
+    pk.y = *reinterpret_cast<uint32_t*>(&p1);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(ea.out) + row * N + c) = pk;
+  }
+}
+
+__device__ __forceinline__ void add4(float4& acc, const float* p) {
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  acc.x += v.x;
+  acc.y += v.y;
+  acc.z += v.z;
+  acc.w += v.w;
+}
+
+// Sums the K slices of a split linear, ws [splits, M, N], in slice order and
+// applies the final epilogue.
 template <int EPI>
 __global__ void __launch_bounds__(256)
 splitk_reduce_kernel(const float* __restrict__ ws, int splits, int64_t M, int64_t N,
@@ -348,37 +439,49 @@ splitk_reduce_kernel(const float* __restrict__ ws, int splits, int64_t M, int64_
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t row = i / n4, c = (i - row * n4) * 4;
     float4 acc = *reinterpret_cast<const float4*>(ws + row * N + c);
-    for (int s = 1; s < splits; ++s) {
-      const float4 v = *reinterpret_cast<const float4*>(ws + (s * M + row) * N + c);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
-    if (EPI == EPI_RESID_F32) {
-      float4* xp = reinterpret_cast<float4*>(static_cast<float*>(ea.out) + row * N + c);
-      const float4 gv = __ldg(reinterpret_cast<const float4*>(ea.gate + c));
-      float4 xv = *xp;
-      xv.x += gv.x * acc.x;
-      xv.y += gv.y * acc.y;
-      xv.z += gv.z * acc.z;
-      xv.w += gv.w * acc.w;
-      *xp = xv;
-    } else {
-      if (EPI == EPI_GELU_BF16) {
-        acc.x = gelu_tanh(acc.x);
-        acc.y = gelu_tanh(acc.y);
-        acc.z = gelu_tanh(acc.z);
-        acc.w = gelu_tanh(acc.w);
-      }
-      __nv_bfloat162 p0 = __floats2bfloat162_rn(acc.x, acc.y);
-      __nv_bfloat162 p1 = __floats2bfloat162_rn(acc.z, acc.w);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&p0);
-      pk.y = *reinterpret_cast<uint32_t*>(&p1);
-      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(ea.out) + row * N + c) = pk;
-    }
+    for (int s = 1; s < splits; ++s) add4(acc, ws + (s * M + row) * N + c);
+    finish4<EPI>(acc, row, c, N, ea);
   }
+}
+
+// The same for the tail tiles only: ws [tail, tail_splits, BM, BN], tail
+// tile tt being output tile num_tiles - tail + tt (tile t at row block
+// t % num_m, column block t / num_m).
+template <int EPI>
+__global__ void __launch_bounds__(256)
+tail_reduce_kernel(const float* __restrict__ ws, int tail, int tail_splits, int num_tiles,
+                   int num_m, int64_t M, int64_t N, const EpiArgs ea) {
+  constexpr int64_t per_tile = static_cast<int64_t>(BM) * (BN / 4);
+  const int64_t total = tail * per_tile;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int tt = static_cast<int>(i / per_tile);
+    const int64_t e = i - tt * per_tile;
+    const int64_t r = e / (BN / 4), c = (e - r * (BN / 4)) * 4;
+    const int tile = num_tiles - tail + tt;
+    const int64_t row = static_cast<int64_t>(tile % num_m) * BM + r;
+    const int64_t col = static_cast<int64_t>(tile / num_m) * BN + c;
+    if (row >= M || col >= N) continue;
+    const float* p = ws + (static_cast<int64_t>(tt) * tail_splits * BM + r) * BN + c;
+    float4 acc = *reinterpret_cast<const float4*>(p);
+    for (int s = 1; s < tail_splits; ++s) add4(acc, p + static_cast<int64_t>(s) * BM * BN);
+    finish4<EPI>(acc, row, col, N, ea);
+  }
+}
+
+template <int EPI>
+dlo_status launch_tail_reduce(const float* ws, int tail, int tail_splits, int64_t M, int64_t N,
+                              const EpiArgs& ea, cudaStream_t stream) {
+  const int num_m = static_cast<int>((M + BM - 1) / BM);
+  const int num_tiles = num_m * static_cast<int>((N + BN - 1) / BN);
+  const int64_t total = static_cast<int64_t>(tail) * BM * (BN / 4);
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  tail_reduce_kernel<EPI><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      ws, tail, tail_splits, num_tiles, num_m, M, N, ea);
+  DLO_CUDA(cudaGetLastError());
+  return DLO_OK;
 }
 
 template <int EPI>
@@ -396,19 +499,44 @@ dlo_status launch_reduce(const float* ws, int splits, int64_t M, int64_t N, cons
 
 }  // namespace
 
-int linear_splits(int64_t M, int64_t N, int64_t K, int epilogue) {
-  if (epilogue == EPI_QKV) return 1;
+LinearPlan linear_plan(int64_t M, int64_t N, int64_t K, int epilogue) {
+  LinearPlan p{1, 0, 1, 0, 1};
+  const int64_t sms = sm_count();
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int64_t num_k = (K + BK - 1) / BK;
-  int64_t s = sm_count() / (tiles > 0 ? tiles : 1);
-  if (s > num_k / 4) s = num_k / 4;      // every slice keeps at least 4 k-blocks
-  if (s > 8) s = 8;
-  return s < 2 ? 1 : static_cast<int>(s);
+  auto clamp = [&](int64_t s) {
+    if (s > num_k / 4) s = num_k / 4;    // every slice keeps at least 4 k-blocks
+    if (s > 8) s = 8;
+    return s;
+  };
+  // fewer tiles than SMs: every tile split
+  const int64_t s = clamp(sms / (tiles > 0 ? tiles : 1));
+  if (s >= 2) {
+    p.splits = static_cast<int>(s);
+    p.ws_bytes = static_cast<size_t>(s) * M * N * 4;
+    p.launches = 2;
+    return p;
+  }
+  // a last wave of at most half the SMs: its tiles split over the idle SMs
+  const int64_t tail = tiles % sms;
+  if (tiles >= sms && tail > 0) {
+    const int64_t ts = clamp(sms / tail);
+    if (ts >= 2) {
+      p.tail = static_cast<int>(tail);
+      p.tail_splits = static_cast<int>(ts);
+      p.ws_bytes = static_cast<size_t>(tail) * ts * BM * BN * 4;
+      p.launches = 2;
+    }
+  }
+  return p;
+}
+
+int linear_splits(int64_t M, int64_t N, int64_t K, int epilogue) {
+  return linear_plan(M, N, K, epilogue).splits;
 }
 
 size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int epilogue) {
-  const int s = linear_splits(M, N, K, epilogue);
-  return s > 1 ? static_cast<size_t>(s) * M * N * 4 : 0;
+  return linear_plan(M, N, K, epilogue).ws_bytes;
 }
 
 namespace {
@@ -447,27 +575,51 @@ dlo_status launch_linear_ex(const uint16_t* a, int64_t M, int64_t K, const uint1
   DLO_TRY(make_tmap_2d(&ma, a, M, K, K, BM, BK));
   DLO_TRY(make_tmap_2d(&mb, w, N, K, K, BN, BK));
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
-  const int splits = linear_splits(M, N, K, epilogue);
-  const size_t ws_need = splits > 1 ? static_cast<size_t>(splits) * M * N * 4 : 0;
-  if (splits > 1 && ea.ws && ea.ws_bytes >= ws_need &&
-      !(reinterpret_cast<uintptr_t>(ea.ws) & 15u)) {
+  const LinearPlan plan = linear_plan(M, N, K, epilogue);
+  const bool have_ws = plan.ws_bytes > 0 && ea.ws && ea.ws_bytes >= plan.ws_bytes &&
+                       !(reinterpret_cast<uintptr_t>(ea.ws) & 15u);
+  const int splits = plan.splits;
+  if (splits > 1 && have_ws) {
     // K split across CTAs: fp32 partials, then an ordered reduction with
     // the epilogue (deterministic: the slice order is fixed)
     EpiArgs pa = ea;
     pa.ws_rows = M;
-    DLO_TRY(launch_epi<EPI_PARTIAL>(ma, mb, m, n, k, splits, pa, err, stream));
+    DLO_TRY(launch_epi<EPI_PARTIAL>(ma, mb, m, n, k, splits, 0, 1, pa, err, stream));
     switch (epilogue) {
       case EPI_BF16: return launch_reduce<EPI_BF16>(ea.ws, splits, M, N, ea, stream);
       case EPI_GELU_BF16: return launch_reduce<EPI_GELU_BF16>(ea.ws, splits, M, N, ea, stream);
       case EPI_RESID_F32: return launch_reduce<EPI_RESID_F32>(ea.ws, splits, M, N, ea, stream);
+      case EPI_QKV: return launch_reduce<EPI_QKV>(ea.ws, splits, M, N, ea, stream);
+      default: DLO_FAIL(DLO_ERR_INVALID, "linear: unknown epilogue %d", epilogue);
+    }
+  }
+  if (plan.tail > 0 && have_ws) {
+    // the short last wave's tiles split in K (partials in ws), the others
+    // finished in the kernel; then the tail's ordered reduction
+    const int tl = plan.tail, ts = plan.tail_splits;
+    switch (epilogue) {
+      case EPI_BF16:
+        DLO_TRY(launch_epi<EPI_BF16>(ma, mb, m, n, k, 1, tl, ts, ea, err, stream));
+        return launch_tail_reduce<EPI_BF16>(ea.ws, tl, ts, M, N, ea, stream);
+      case EPI_GELU_BF16:
+        DLO_TRY(launch_epi<EPI_GELU_BF16>(ma, mb, m, n, k, 1, tl, ts, ea, err, stream));
+        return launch_tail_reduce<EPI_GELU_BF16>(ea.ws, tl, ts, M, N, ea, stream);
+      case EPI_RESID_F32:
+        DLO_TRY(launch_epi<EPI_RESID_F32>(ma, mb, m, n, k, 1, tl, ts, ea, err, stream));
+        return launch_tail_reduce<EPI_RESID_F32>(ea.ws, tl, ts, M, N, ea, stream);
+      case EPI_QKV:
+        DLO_TRY(launch_epi<EPI_QKV>(ma, mb, m, n, k, 1, tl, ts, ea, err, stream));
+        return launch_tail_reduce<EPI_QKV>(ea.ws, tl, ts, M, N, ea, stream);
       default: DLO_FAIL(DLO_ERR_INVALID, "linear: unknown epilogue %d", epilogue);
     }
   }
   switch (epilogue) {
-    case EPI_BF16: return launch_epi<EPI_BF16>(ma, mb, m, n, k, 1, ea, err, stream);
-    case EPI_GELU_BF16: return launch_epi<EPI_GELU_BF16>(ma, mb, m, n, k, 1, ea, err, stream);
-    case EPI_RESID_F32: return launch_epi<EPI_RESID_F32>(ma, mb, m, n, k, 1, ea, err, stream);
-    case EPI_QKV: return launch_epi<EPI_QKV>(ma, mb, m, n, k, 1, ea, err, stream);
+    case EPI_BF16: return launch_epi<EPI_BF16>(ma, mb, m, n, k, 1, 0, 1, ea, err, stream);
+    case EPI_GELU_BF16:
+      return launch_epi<EPI_GELU_BF16>(ma, mb, m, n, k, 1, 0, 1, ea, err, stream);
+    case EPI_RESID_F32:
+      return launch_epi<EPI_RESID_F32>(ma, mb, m, n, k, 1, 0, 1, ea, err, stream);
+    case EPI_QKV: return launch_epi<EPI_QKV>(ma, mb, m, n, k, 1, 0, 1, ea, err, stream);
     default: DLO_FAIL(DLO_ERR_INVALID, "linear: unknown epilogue %d", epilogue);
   }
 }

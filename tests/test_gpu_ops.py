@@ -91,6 +91,59 @@ def test_linear(M, K, N, epi, split):
         assert np.all(np.abs(got - ref) <= tol), np.abs(got - ref).max()
 
 
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("epi", [dlo.EPI_BF16, dlo.EPI_GELU_BF16, dlo.EPI_RESID_F32])
+@pytest.mark.parametrize("shape", ["column", "grid"])
+def test_linear_tail_split(epi, shape):
+    # a short last wave: only its tiles are split in K, the rest finish in
+    # the kernel; "grid": 3 column blocks, the tail tile being the ragged
+    # last row block of the ragged last column block.  Checked on the rows of
+    # the last 6 row blocks (every tail tile) and a sample of the others.
+    sms = _sms()
+    K = 2048
+    if shape == "column":
+        tail = 5
+        M, N = 128 * (sms + tail) - 37, 256
+    else:
+        tail = next(t for t in range(1, sms) if (sms + t) % 3 == 0)
+        M, N = 128 * ((sms + tail) // 3) - 50, 760
+    ts = min(sms // tail, K // 64 // 4, 8)
+    nws = dlo.op_linear_workspace_bytes(M, N, K, epi)
+    assert nws == tail * ts * 128 * 256 * 4
+    r = _gen(M + N + epi)
+    a = r(M, K).to(torch.bfloat16)
+    w = r(N, K, std=0.05).to(torch.bfloat16)
+    ad, wd = a.cuda(), w.cuda()
+    ws = torch.full((nws // 4,), float("nan"), device="cuda")
+    rng = np.random.default_rng(M)
+    sel = np.unique(np.concatenate([np.arange(max(0, M - 6 * 128), M),
+                                    rng.integers(0, M, 256)]))
+    ref = oracle.linear(a[sel].float().numpy(), w.float().numpy())
+    if epi == dlo.EPI_RESID_F32:
+        x = r(M, N)
+        gate = r(N, std=0.1)
+        xd = x.cuda()
+        dlo.op_linear(ad, M, K, wd, N, epi, xd, gate.cuda(), None, ws, nws)
+        _status_clean()
+        got = xd.cpu().numpy()[sel]
+        exp = x.numpy()[sel].astype(np.float64) + gate.numpy().astype(np.float64) * ref
+        assert np.abs(got - exp).max() <= 1e-4 * max(1.0, np.abs(exp).max())
+    else:
+        out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        dlo.op_linear(ad, M, K, wd, N, epi, out, None, None, ws, nws)
+        _status_clean()
+        full = out.float().cpu().numpy()
+        assert not np.isnan(full).any()
+        got = full[sel]
+        if epi == dlo.EPI_GELU_BF16:
+            ref = np.vectorize(oracle.gelu_tanh)(ref)
+        tol = 2.0 ** -8 * np.abs(ref) + 1e-5 * np.sqrt(K) * np.abs(ref).max()
+        assert np.all(np.abs(got - ref) <= tol), np.abs(got - ref).max()
+
+
 def _attention(qkv, B, T, d, H, o):
     n = dlo.op_attention_scratch_bytes(B, T, d)
     scratch = torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda")   # NaN-filled

@@ -223,6 +223,26 @@ def test_ragged_streamed_vs_resident_vs_oracle(cfg):
     host.close()
 
 
+def test_forward_with_split_tails_vs_oracle():
+    # tokens chosen so that the QKV linear's tiles (6 column blocks at
+    # d = 512) leave a short last wave on this GPU: that tail runs as K slices
+    # with the transposed-V epilogue in the reduction; the out-projection and
+    # fc2 have fewer tiles than SMs and split every tile
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    num_m = -(-(sms + 1) // 6)
+    assert 1 <= 6 * num_m - sms <= sms // 2
+    w = W.custom("tails", n_blocks=1, hidden=512, heads=4, mlp=2048, tokens=128 * num_m - 28,
+                 shards=2, steps=1)
+    cfg = dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp)
+    assert dlo.forward_launches(cfg) == 11
+    host = HostBlocks(w, seed=3, keep_params=True)
+    x0 = W.gen_x(w, seed=3)
+    res, per_block = _run_resident(host, x0, w.steps)
+    _check_against_oracle(host, per_block, [0])
+    assert dlo.kernel_status() == 0
+    host.close()
+
+
 def test_graph_replay_equals_direct_launches():
     w = W.custom("graph", n_blocks=2, hidden=256, heads=4, mlp=1024, tokens=130, shards=2)
     host = HostBlocks(w, seed=4)
