@@ -1,8 +1,10 @@
 // norm.cu — RMSNorm fused with the adaLN modulation of the synthetic DiT
 // block: h = bf16( x / sqrt(mean(x^2) + eps) * g * (1 + scale) + shift ).
-// One warp per row; the row is read twice (the second read hits L1/L2), the
-// mean square is reduced in a fixed shuffle-tree order, so results are
-// deterministic.
+// One CTA per row (d <= 8192): every thread loads its float4s of the row
+// into registers up front, so x is read from HBM once and all loads are in
+// flight together; the mean square is reduced per thread, then by a fixed
+// shuffle tree per warp, then over the warps in warp order, so results are
+// deterministic.  Wider rows: one warp per row, reading the row twice.
 #include <cuda_bf16.h>
 
 #include "common.h"
@@ -12,6 +14,58 @@ namespace {
 
 constexpr int kNormThreads = 256;            // 8 warps, one row per warp
 constexpr int kRowsPerCta = kNormThreads / 32;
+constexpr int kRowThreads = 256;             // one row per CTA
+
+// One row per CTA of blockDim.x (a multiple of 32, <= kRowThreads) threads;
+// thread t holds float4s t, t + blockDim.x, ... (V of them) of the row.
+template <int V>
+__global__ void __launch_bounds__(kRowThreads)
+rmsnorm_mod_row_kernel(const float* __restrict__ x, int64_t d, const float* __restrict__ g,
+                       const float* __restrict__ shift, const float* __restrict__ scale,
+                       float eps, uint16_t* __restrict__ h) {
+  __shared__ float part[kRowThreads / 32];
+  const int64_t row = blockIdx.x;
+  const int n4 = static_cast<int>(d / 4);
+  const int nt = blockDim.x;
+  const float4* xr = reinterpret_cast<const float4*>(x + row * d);
+  float4 v[V];
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    const int i = threadIdx.x + k * nt;
+    v[k] = i < n4 ? xr[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < V; ++k) ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z +
+                                    v[k].w * v[k].w;
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < nt / 32; ++w) tot += part[w];
+  const float inv = rsqrtf(tot / static_cast<float>(d) + eps);
+  const float4* g4 = reinterpret_cast<const float4*>(g);
+  const float4* s4 = reinterpret_cast<const float4*>(scale);
+  const float4* b4 = reinterpret_cast<const float4*>(shift);
+  uint2* hr = reinterpret_cast<uint2*>(h + row * d);
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    const int i = threadIdx.x + k * nt;
+    if (i < n4) {
+      const float4 gg = __ldg(g4 + i), sc = __ldg(s4 + i), sh = __ldg(b4 + i);
+      const float o0 = v[k].x * inv * gg.x * (1.f + sc.x) + sh.x;
+      const float o1 = v[k].y * inv * gg.y * (1.f + sc.y) + sh.y;
+      const float o2 = v[k].z * inv * gg.z * (1.f + sc.z) + sh.z;
+      const float o3 = v[k].w * inv * gg.w * (1.f + sc.w) + sh.w;
+      __nv_bfloat162 p0 = __floats2bfloat162_rn(o0, o1);
+      __nv_bfloat162 p1 = __floats2bfloat162_rn(o2, o3);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&p0);
+      pk.y = *reinterpret_cast<uint32_t*>(&p1);
+      hr[i] = pk;
+    }
+  }
+}
 
 __global__ void __launch_bounds__(kNormThreads)
 rmsnorm_mod_kernel(const float* __restrict__ x, int64_t rows, int64_t d,
@@ -61,6 +115,23 @@ dlo_status launch_rmsnorm_mod(const float* x, int64_t rows, int64_t d, const flo
        reinterpret_cast<uintptr_t>(shift) | reinterpret_cast<uintptr_t>(scale)) & 15u ||
       reinterpret_cast<uintptr_t>(h) & 7u)
     DLO_FAIL(DLO_ERR_INVALID, "rmsnorm_mod: pointers must be 16-byte (h: 8-byte) aligned");
+  const int64_t n4 = d / 4;
+  if (n4 <= 8 * kRowThreads) {
+    if (rows > 0x7fffffffLL) DLO_FAIL(DLO_ERR_INVALID, "rmsnorm_mod: too many rows");
+    const int nt = n4 >= kRowThreads ? kRowThreads : static_cast<int>((n4 + 31) / 32 * 32);
+    const int64_t per = (n4 + nt - 1) / nt;   // float4s per thread, <= 8
+    const unsigned grid = static_cast<unsigned>(rows);
+    if (per <= 1)
+      rmsnorm_mod_row_kernel<1><<<grid, nt, 0, stream>>>(x, d, g, shift, scale, eps, h);
+    else if (per <= 2)
+      rmsnorm_mod_row_kernel<2><<<grid, nt, 0, stream>>>(x, d, g, shift, scale, eps, h);
+    else if (per <= 4)
+      rmsnorm_mod_row_kernel<4><<<grid, nt, 0, stream>>>(x, d, g, shift, scale, eps, h);
+    else
+      rmsnorm_mod_row_kernel<8><<<grid, nt, 0, stream>>>(x, d, g, shift, scale, eps, h);
+    DLO_CUDA(cudaGetLastError());
+    return DLO_OK;
+  }
   const int64_t ctas = (rows + kRowsPerCta - 1) / kRowsPerCta;
   if (ctas > 0x7fffffffLL) DLO_FAIL(DLO_ERR_INVALID, "rmsnorm_mod: too many rows");
   rmsnorm_mod_kernel<<<static_cast<unsigned>(ctas), kNormThreads, 0, stream>>>(

@@ -28,7 +28,8 @@ def _status_clean():
     assert dlo.kernel_status() == 0
 
 
-@pytest.mark.parametrize("rows,d", [(1, 64), (7, 256), (200, 1024), (33, 3840)])
+@pytest.mark.parametrize("rows,d", [(1, 64), (7, 256), (200, 1024), (33, 3840), (5, 6656),
+                                    (3, 8192), (2, 8196), (4, 100)])
 def test_rmsnorm_mod(rows, d):
     r = _gen(rows * 7 + d)
     x = r(rows, d)
