@@ -266,9 +266,10 @@ enum { DLO_FWD_GRAPH = 1 };
 size_t dlo_forward_scratch_bytes(const dlo_dit_cfg* cfg);
 
 /* Number of kernel launches one dlo_forward (or dlo_forward_noalloc) makes
- * for this configuration — two norm launches, attention, and for each of
+ * for this configuration — two norm launches, attention plus one merge
+ * launch when the items of its last wave run as KV slices, and for each of
  * the four linears (QKV, out-projection, fc1, fc2) one GEMM plus one ordered
- * reduction when some of its tiles run as K slices (the split depends on the
+ * reduction when some of its tiles run as K slices (the splits depend on the
  * current device's SM count; 152 when none is visible) — or 0 for an
  * invalid configuration.  Launches nothing. */
 int32_t dlo_forward_launches(const dlo_dit_cfg* cfg);
@@ -320,17 +321,22 @@ dlo_status dlo_forward_noalloc(const dlo_dit_cfg* cfg, const dlo_plan* plan,
  *                         2: out fp32 [M,N] += gate[N] * acc  (in place)
  *                K and N multiples of 8; pointers 16-byte aligned.
  *                workspace (device, may be null): when the output has too
- *                few 128x256 tiles to fill the GPU, K is split into slices
- *                computed in parallel into fp32 partials in the workspace,
- *                then summed in slice order (deterministic) by a second
- *                kernel that applies the epilogue; this needs
- *                dlo_op_linear_workspace_bytes(M, N, K, epilogue) bytes
- *                (0: the shape does not split).  Without enough workspace
- *                the linear runs unsplit.
+ *                few 128x256 tiles to fill the GPU — or its tiles leave a
+ *                last wave of at most half the SMs, for that wave's tiles
+ *                only — K is split into slices computed in parallel into
+ *                fp32 partials in the workspace, then summed in slice order
+ *                (deterministic) by a second kernel that applies the
+ *                epilogue; this needs dlo_op_linear_workspace_bytes(M, N, K,
+ *                epilogue) bytes (0: the shape does not split).  Without
+ *                enough workspace the linear runs unsplit.
  *   attention:   o bf16 [batch*tokens, d] from qkv bf16 [batch*tokens, 3d];
- *                scratch (device, 16-byte aligned) holds V transposed,
+ *                scratch (device, 16-byte aligned) holds V transposed and,
+ *                when the (batch, head, query group) items leave a last
+ *                wave of at most half the SMs, the fp32 partial results of
+ *                that wave's items split into KV slices (merged in slice
+ *                order by a second kernel):
  *                dlo_op_attention_scratch_bytes(batch, tokens, d) bytes
- *                (inside dlo_forward the QKV linear writes that layout
+ *                (inside dlo_forward the QKV linear writes V transposed
  *                directly). */
 dlo_status dlo_op_rmsnorm_mod(const float* x, int64_t rows, int64_t d,
                               const float* g, const float* shift,

@@ -188,7 +188,8 @@ template <int HD>
 __global__ void __launch_bounds__(ATT_THREADS, 1)
 attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
                     const __grid_constant__ CUtensorMap tm_vt, int tokens, int d, int heads,
-                    uint16_t* __restrict__ o, float scale_log2, int nt, int* err) {
+                    uint16_t* __restrict__ o, float scale_log2, int nt, int n_main, int parts,
+                    float* __restrict__ part_ws, int* err) {
   using L = AttLayout<HD>;
   constexpr int NS = L::NS;
   extern __shared__ uint8_t smem_raw[];
@@ -209,9 +210,21 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wg = warp >> 2;
-  const int q0 = blockIdx.x * nt * BQ;       // nt: query tiles of this CTA (1 or 2)
-  const int head = blockIdx.y, b = blockIdx.z;
-  const int n_kv = (tokens + BKV - 1) / BKV;
+  // Unit blockIdx.x: the first n_main are whole (batch, head, query group)
+  // items (nt query tiles), numbered query group fastest, then head, then
+  // batch; each later one is a slice `part` of the KV tiles of one of the
+  // remaining items (a short last wave spread over the idle SMs), which
+  // writes its unnormalised O, m and l to part_ws for attention_combine.
+  const int n_groups = (tokens + nt * BQ - 1) / (nt * BQ);
+  const int u = blockIdx.x;
+  const int item = u < n_main ? u : n_main + (u - n_main) / parts;
+  const int part = u < n_main ? -1 : (u - n_main) % parts;
+  const int q0 = (item % n_groups) * nt * BQ;
+  const int head = (item / n_groups) % heads, b = item / (n_groups * heads);
+  const int n_kv_all = (tokens + BKV - 1) / BKV;
+  const int kv_base = part < 0 ? 0 : part * n_kv_all / parts;
+  // KV tiles of this unit: kv_base .. kv_base + n_kv - 1 (local index j)
+  const int n_kv = part < 0 ? n_kv_all : (part + 1) * n_kv_all / parts - kv_base;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -255,7 +268,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
       for (int i = 0; i < 2 * n_kv; ++i) {
         const int s = i % NS;
         const uint32_t use = static_cast<uint32_t>(i / NS);
-        const int kv0 = (i >> 1) * BKV;
+        const int kv0 = (kv_base + (i >> 1)) * BKV;
         if (!mbar_wait_bounded(&empty[s], (use & 1u) ^ 1u, abort)) {
           att_fail(err, abort, DEV_TIMEOUT_PRODUCER);
           break;
@@ -418,7 +431,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
         break;
       }
       tc_fence_after();
-      const int valid = tokens - j * BKV;      // keys of this tile that exist
+      const int valid = tokens - (kv_base + j) * BKV;   // keys of this tile that exist
       if (j == 0) {
         // the first KV tile fixes m: its row maximum, read chunk by chunk
         float mx = -INFINITY;
@@ -496,7 +509,26 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
       if (lane == 0) att_fail(err, abort, DEV_TIMEOUT_EPILOGUE);
       ok = false;
     }
-    if (ok && !*abort) {
+    if (ok && !*abort && part >= 0) {
+      // a KV slice: O (fp32, not yet divided by l), then m and l, per row
+      tc_fence_after();
+      const int64_t slot = (static_cast<int64_t>(item - n_main) * parts + part) * nt + t;
+      float* orow = part_ws + (slot * BQ + row) * HD;
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t oa[32];
+        tmem_ld_32x32b_x32(tOt + c * 32, oa);
+        tmem_ld_wait();
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          *reinterpret_cast<float4*>(orow + c * 32 + 4 * g) =
+              make_float4(__uint_as_float(oa[4 * g]), __uint_as_float(oa[4 * g + 1]),
+                          __uint_as_float(oa[4 * g + 2]), __uint_as_float(oa[4 * g + 3]));
+      }
+      const int64_t n_slots = static_cast<int64_t>(gridDim.x - n_main) * nt;
+      *reinterpret_cast<float2*>(part_ws + n_slots * BQ * HD + (slot * BQ + row) * 2) =
+          make_float2(m, l);
+    } else if (ok && !*abort) {
       tc_fence_after();
       const float inv = 1.f / l;
       const int q = q0 + t * BQ + row;
@@ -527,6 +559,50 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
     tc_fence_after();
     tmem_dealloc(tmem, ATT_TMEM_COLS);
   }
+}
+
+// Merges the KV slices of the split items: for each of their query rows,
+// M = max_p m_p, o = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p, the
+// parts taken in order.  One warp per row, HD / 32 columns per lane.
+template <int HD>
+__global__ void __launch_bounds__(256)
+attention_combine_kernel(const float* __restrict__ part_ws, int n_main, int n_split, int parts,
+                         int nt, int tokens, int d, int heads, uint16_t* __restrict__ o) {
+  constexpr int CPL = HD / 32;                      // columns per lane
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = static_cast<int64_t>(n_split) * nt * BQ;
+  if (w >= rows) return;
+  const int si = static_cast<int>(w / (nt * BQ));   // split item
+  const int t = static_cast<int>((w / BQ) % nt), row = static_cast<int>(w % BQ);
+  const int item = n_main + si;
+  const int n_groups = (tokens + nt * BQ - 1) / (nt * BQ);
+  const int q = (item % n_groups) * nt * BQ + t * BQ + row;
+  if (q >= tokens) return;
+  const int head = (item / n_groups) % heads, b = item / (n_groups * heads);
+  const int64_t n_slots = static_cast<int64_t>(n_split) * parts * nt;
+  const float* ml = part_ws + n_slots * BQ * HD;
+  float mx = -INFINITY;
+  for (int p = 0; p < parts; ++p) {
+    const int64_t slot = (static_cast<int64_t>(si) * parts + p) * nt + t;
+    mx = fmaxf(mx, ml[(slot * BQ + row) * 2]);
+  }
+  float acc[CPL], l = 0.f;
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+  for (int p = 0; p < parts; ++p) {
+    const int64_t slot = (static_cast<int64_t>(si) * parts + p) * nt + t;
+    const float wgt = exp2f(ml[(slot * BQ + row) * 2] - mx);
+    l += wgt * ml[(slot * BQ + row) * 2 + 1];
+    const float* op = part_ws + (slot * BQ + row) * HD + lane * CPL;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[c] += wgt * op[c];
+  }
+  const float inv = 1.f / l;
+  uint16_t* orow = o + (static_cast<int64_t>(b) * tokens + q) * d + head * HD + lane * CPL;
+#pragma unroll
+  for (int c = 0; c < CPL; c += 2)
+    *reinterpret_cast<uint32_t*>(orow + c) = pack_bf16(acc[c] * inv, acc[c + 1] * inv);
 }
 
 // V block of qkv ([rows, 3d], columns [2d, 3d)) -> vt [b*d + c, t] with row
@@ -567,28 +643,64 @@ void set_att_attrs() {
 }
 
 template <int HD>
-dlo_status launch_hd(const CUtensorMap& tm_qk, const CUtensorMap& tm_vt, int64_t batch,
-                     int64_t tokens, int64_t d, int64_t heads, uint16_t* o, int* err,
+dlo_status launch_hd(const CUtensorMap& tm_qk, const CUtensorMap& tm_vt, const AttPlan& pl,
+                     int64_t tokens, int64_t d, int64_t heads, uint16_t* o, float* ws, int* err,
                      cudaStream_t stream) {
   set_att_attrs();
   DLO_CUDA(g_att_err);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
-  // Two query tiles per CTA halve the K/V traffic per query; when that
-  // leaves SMs idle (fewer CTAs than SMs), one tile per CTA doubles the CTAs.
-  const int64_t pairs = (tokens + 2 * BQ - 1) / (2 * BQ);
-  const int nt = pairs * heads * batch >= sm_count() ? 2 : 1;
-  dim3 grid(static_cast<unsigned>((tokens + nt * BQ - 1) / (nt * BQ)),
-            static_cast<unsigned>(heads), static_cast<unsigned>(batch));
-  attention_tc_kernel<HD><<<grid, ATT_THREADS, AttLayout<HD>::SMEM, stream>>>(
+  const int n_split = static_cast<int>(pl.items - pl.n_main);
+  attention_tc_kernel<HD><<<static_cast<unsigned>(pl.units), ATT_THREADS, AttLayout<HD>::SMEM,
+                            stream>>>(
       tm_qk, tm_vt, static_cast<int>(tokens), static_cast<int>(d), static_cast<int>(heads), o,
-      scale_log2, nt, err);
+      scale_log2, pl.nt, static_cast<int>(pl.n_main), pl.parts, ws, err);
   DLO_CUDA(cudaGetLastError());
+  if (n_split > 0) {
+    const int64_t rows = static_cast<int64_t>(n_split) * pl.nt * BQ;
+    attention_combine_kernel<HD><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0,
+                                   stream>>>(
+        ws, static_cast<int>(pl.n_main), n_split, pl.parts, pl.nt, static_cast<int>(tokens),
+        static_cast<int>(d), static_cast<int>(heads), o);
+    DLO_CUDA(cudaGetLastError());
+  }
   return DLO_OK;
 }
 
 }  // namespace
 
 int64_t vt_ld_for(int64_t tokens) { return (tokens + 7) / 8 * 8; }
+
+AttPlan attention_plan(int64_t batch, int64_t tokens, int64_t d, int64_t heads) {
+  AttPlan p{};
+  p.nt = 1;
+  p.parts = 1;
+  p.launches = 1;
+  if (batch <= 0 || tokens <= 0 || heads <= 0 || d % heads != 0) return p;
+  const int64_t hd = d / heads;
+  const int64_t sms = sm_count();
+  // Two query tiles per CTA halve the K/V traffic per query; when that
+  // leaves SMs idle (fewer CTAs than SMs), one tile per CTA doubles the CTAs.
+  const int64_t pairs = (tokens + 2 * BQ - 1) / (2 * BQ);
+  p.nt = pairs * heads * batch >= sms ? 2 : 1;
+  p.items = (tokens + p.nt * BQ - 1) / (p.nt * BQ) * heads * batch;
+  p.n_main = p.items;
+  p.units = p.items;
+  // a last wave of at most half the SMs: its items' KV tiles are split over
+  // the idle SMs (at least 2 KV tiles per slice)
+  const int64_t tail = p.items % sms, n_kv = (tokens + BKV - 1) / BKV;
+  if (p.items >= sms && tail > 0) {
+    int64_t parts = sms / tail;
+    if (parts > n_kv / 2) parts = n_kv / 2;
+    if (parts >= 2) {
+      p.parts = static_cast<int>(parts);
+      p.n_main = p.items - tail;
+      p.units = p.n_main + tail * parts;
+      p.ws_bytes = static_cast<size_t>(tail) * parts * p.nt * BQ * (hd + 2) * 4;
+      p.launches = 2;
+    }
+  }
+  return p;
+}
 
 dlo_status attention_preload() {
   set_att_attrs();
@@ -598,7 +710,7 @@ dlo_status attention_preload() {
 
 dlo_status launch_attention_vt(const uint16_t* qkv, const uint16_t* vt, int64_t vt_ld,
                                int64_t batch, int64_t tokens, int64_t d, int64_t heads,
-                               uint16_t* o, cudaStream_t stream) {
+                               uint16_t* o, float* ws, size_t ws_bytes, cudaStream_t stream) {
   if (batch == 0 || tokens == 0) return DLO_OK;
   if (!qkv || !vt || !o || batch < 0 || tokens < 0 || d <= 0 || heads <= 0 || d % heads != 0)
     DLO_FAIL(DLO_ERR_INVALID, "attention: bad arguments (d %lld, heads %lld)", (long long)d,
@@ -618,8 +730,15 @@ dlo_status launch_attention_vt(const uint16_t* qkv, const uint16_t* vt, int64_t 
   CUtensorMap tm_qk, tm_vt;
   DLO_TRY(make_tmap_2d(&tm_qk, qkv, batch * tokens, 3 * d, 3 * d, BQ, 64));
   DLO_TRY(make_tmap_2d(&tm_vt, vt, batch * d, tokens, vt_ld, static_cast<uint32_t>(hd), 64));
-  if (hd == 64) return launch_hd<64>(tm_qk, tm_vt, batch, tokens, d, heads, o, err, stream);
-  return launch_hd<128>(tm_qk, tm_vt, batch, tokens, d, heads, o, err, stream);
+  AttPlan pl = attention_plan(batch, tokens, d, heads);
+  if (pl.parts > 1 && (!ws || ws_bytes < pl.ws_bytes || (reinterpret_cast<uintptr_t>(ws) & 15u))) {
+    // no room for the KV slices: the tail runs whole
+    pl.parts = 1;
+    pl.n_main = pl.units = pl.items;
+  }
+  if (pl.units > 0x7fffffffLL) DLO_FAIL(DLO_ERR_INVALID, "attention: too many work units");
+  if (hd == 64) return launch_hd<64>(tm_qk, tm_vt, pl, tokens, d, heads, o, ws, err, stream);
+  return launch_hd<128>(tm_qk, tm_vt, pl, tokens, d, heads, o, ws, err, stream);
 }
 
 dlo_status launch_transpose_v(const uint16_t* qkv, int64_t batch, int64_t tokens, int64_t d,

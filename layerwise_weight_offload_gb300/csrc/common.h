@@ -152,9 +152,24 @@ dlo_status launch_linear_ex(const uint16_t* a, int64_t M, int64_t K, const uint1
 
 // attention.cu
 int64_t vt_ld_for(int64_t tokens);   // row stride of vt: tokens rounded up to 8
+// How attention runs on this GPU's SMs: nt query tiles per CTA, `items`
+// (batch, head, query group) items of which the first n_main run whole and
+// the rest (a last wave of at most half the SMs) as `parts` KV slices each,
+// merged by a second kernel; `units` CTAs, the fp32 workspace of the slices
+// and the launches (1, or 2 with the merge).
+struct AttPlan {
+  int nt;
+  int64_t items, n_main, units;
+  int parts;
+  size_t ws_bytes;
+  int launches;
+};
+AttPlan attention_plan(int64_t batch, int64_t tokens, int64_t d, int64_t heads);
+// ws: the slices' workspace (ws_bytes >= attention_plan(...).ws_bytes), or
+// null: then every item runs whole.
 dlo_status launch_attention_vt(const uint16_t* qkv, const uint16_t* vt, int64_t vt_ld,
                                int64_t batch, int64_t tokens, int64_t d, int64_t heads,
-                               uint16_t* o, cudaStream_t stream);
+                               uint16_t* o, float* ws, size_t ws_bytes, cudaStream_t stream);
 dlo_status launch_transpose_v(const uint16_t* qkv, int64_t batch, int64_t tokens, int64_t d,
                               uint16_t* vt, int64_t vt_ld, cudaStream_t stream);
 

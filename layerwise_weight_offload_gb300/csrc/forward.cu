@@ -42,6 +42,7 @@ ScratchLayout scratch_layout(const dlo_dit_cfg& c) {
   s.ws = r(s.u + M * f * 2);
   const int64_t Mi = static_cast<int64_t>(M), di = c.hidden, fi = c.mlp;
   size_t w = linear_workspace_bytes(Mi, 3 * di, di, EPI_QKV);
+  w = std::max(w, attention_plan(c.batch, c.tokens, c.hidden, c.heads).ws_bytes);
   w = std::max(w, linear_workspace_bytes(Mi, di, di, EPI_RESID_F32));
   w = std::max(w, linear_workspace_bytes(Mi, fi, di, EPI_GELU_BF16));
   w = std::max(w, linear_workspace_bytes(Mi, di, fi, EPI_RESID_F32));
@@ -115,8 +116,8 @@ dlo_status launch_all(const dlo_dit_cfg* cfg, const dlo_plan* plan, const Scratc
   qa.ws = ws;
   qa.ws_bytes = sl.ws_bytes;
   DLO_TRY(launch_linear_ex(h, M, d, H(R_WQKV), 3 * d, EPI_QKV, qa, stream));
-  DLO_TRY(launch_attention_vt(qkv, vt, sl.vt_ld, cfg->batch, cfg->tokens, d, cfg->heads, o,
-                              stream));
+  DLO_TRY(launch_attention_vt(qkv, vt, sl.vt_ld, cfg->batch, cfg->tokens, d, cfg->heads, o, ws,
+                              sl.ws_bytes, stream));
   DLO_TRY(launch_linear(o, M, d, H(R_WO), d, EPI_RESID_F32, x, F(R_GATE1), ws, sl.ws_bytes,
                         stream));
   DLO_TRY(launch_rmsnorm_mod(x, M, d, F(R_G2), F(R_SHIFT2), F(R_SCALE2), cfg->eps, h, stream));
@@ -245,9 +246,9 @@ int32_t dlo_forward_launches(const dlo_dit_cfg* cfg) {
   if (check_cfg(cfg) != DLO_OK) return 0;
   const int64_t M = static_cast<int64_t>(cfg->batch) * cfg->tokens, d = cfg->hidden,
                 f = cfg->mlp;
-  // norm x2, attention; the four linears (+ a reduction each when split),
-  // as launch_all issues them
-  int32_t n = 3;
+  // norm x2, attention (+ the merge of its KV slices), the four linears (+ a
+  // reduction each when split), as launch_all issues them
+  int32_t n = 2 + attention_plan(cfg->batch, cfg->tokens, d, cfg->heads).launches;
   n += linear_plan(M, 3 * d, d, EPI_QKV).launches;
   n += linear_plan(M, d, d, EPI_RESID_F32).launches;
   n += linear_plan(M, f, d, EPI_GELU_BF16).launches;
@@ -283,7 +284,12 @@ dlo_status dlo_op_linear(const uint16_t* a, int64_t M, int64_t K, const uint16_t
 
 size_t dlo_op_attention_scratch_bytes(int64_t batch, int64_t tokens, int64_t d) {
   if (batch <= 0 || tokens <= 0 || d <= 0) return 0;
-  return static_cast<size_t>(batch * d * dlo::vt_ld_for(tokens) * 2);
+  // V transposed, then the KV-slice workspace of either head dim
+  const size_t vt = static_cast<size_t>(batch * d * dlo::vt_ld_for(tokens) * 2);
+  size_t ws = 0;
+  for (int64_t hd : {64, 128})
+    if (d % hd == 0) ws = std::max(ws, dlo::attention_plan(batch, tokens, d, d / hd).ws_bytes);
+  return (vt + 255) / 256 * 256 + ws;
 }
 
 dlo_status dlo_op_attention(const uint16_t* qkv, int64_t batch, int64_t tokens, int64_t d,
@@ -301,8 +307,11 @@ dlo_status dlo_op_attention(const uint16_t* qkv, int64_t batch, int64_t tokens, 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint16_t* vt = static_cast<uint16_t*>(scratch);
   const int64_t vt_ld = vt_ld_for(tokens);
+  const size_t vt_bytes = (static_cast<size_t>(batch * d * vt_ld * 2) + 255) / 256 * 256;
+  float* ws = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + vt_bytes);
   DLO_TRY(launch_transpose_v(qkv, batch, tokens, d, vt, vt_ld, st));
-  return launch_attention_vt(qkv, vt, vt_ld, batch, tokens, d, heads, o, st);
+  return launch_attention_vt(qkv, vt, vt_ld, batch, tokens, d, heads, o, ws,
+                             scratch_bytes - vt_bytes, st);
 }
 
 }  // extern "C"

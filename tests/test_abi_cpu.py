@@ -214,10 +214,10 @@ def test_scratch_bytes_cover_the_buffers():
 
 
 def test_forward_launch_count():
-    # norms, attention, and the four linears with a reduction each when some
-    # of their tiles are split into K slices
+    # norms, attention (+ the merge of its KV slices), and the four linears
+    # with a reduction each when some of their tiles are split into K slices
     for name in ("tiny", "odd", "nano", "super"):
         w = W.CONFIGS[name]
         n = dlo.forward_launches(dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp))
-        assert 7 <= n <= 11
+        assert 7 <= n <= 12
     assert dlo.forward_launches(dlo.dit_cfg(1, 16, 96, 1, 256)) == 0       # invalid config

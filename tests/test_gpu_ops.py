@@ -161,8 +161,11 @@ ATT_SHAPES = [
     (1, 2500, 256, 2),   # many KV tiles: rescaling path, hd 128
     (3, 129, 128, 2),    # three batch items, one key past a tile
     # grids of at least one CTA per SM take two query tiles per CTA
-    (2, 1100, 2048, 16),  # hd 128, ragged last pair, second batch item
+    (2, 1100, 2048, 16),  # hd 128, ragged last pair, second batch item; on 152 SMs the
+                          # last wave (8 pairs) runs as KV slices merged by a second kernel
     (1, 2000, 1216, 19),  # hd 64, last CTA's second tile partly past the end
+    (1, 2100, 1280, 20),  # hd 64, ragged: 180 pairs, the last 28 as 5 KV slices each
+    (1, 1536, 2048, 16),  # one query tile per CTA: 192 tiles, the last 40 as 3 KV slices
 ]
 
 
@@ -204,7 +207,7 @@ def test_rejects_unsupported_shapes():
         _attention(q, 1, 4, 96, 3, q)                              # head dim 32
 
 
-@pytest.mark.parametrize("d,H", [(256, 4), (256, 2)])
+@pytest.mark.parametrize("d,H", [(256, 4), (256, 2), (3072, 24)])
 def test_attention_scores_growing_across_tiles(d, H):
     # scores rise with the key index, so later KV tiles have a much larger
     # row maximum than the first one: exercises the rescale-and-redo path
