@@ -42,6 +42,26 @@ constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
+// Output tile t -> (row block, column block) in groups of group_m row
+// blocks, row blocks fastest within a group: the tiles of one wave
+// (consecutive t) then cover group_m row blocks by about 152/group_m column
+// blocks.  With A larger than L2 this keeps the operands a wave streams
+// small (Super's fc2: 16 x 9.5 blocks instead of all 64 row blocks of a
+// 403 MB A by 2.4 column blocks, which read A from DRAM ten times); with A
+// small enough to stay in L2 one group spans all rows (column-major), so
+// that each weight column block is read once.
+constexpr int kGroupM = 16;
+constexpr int64_t kAResidentBytes = 64ll << 20;
+__host__ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int group_m,
+                                                     int& m_idx, int& n_idx) {
+  const int per_group = group_m * num_n;
+  const int first_m = (t / per_group) * group_m;
+  const int rows = num_m - first_m < group_m ? num_m - first_m : group_m;
+  const int r = t - (t / per_group) * per_group;
+  m_idx = first_m + r % rows;
+  n_idx = r / rows;
+}
+
 __device__ __forceinline__ void record_failure(int* err, volatile int* abort, int code) {
   atomicCAS(err, 0, code);
   *abort = 1;
@@ -122,7 +142,8 @@ template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
                     const __grid_constant__ CUtensorMap tma_b, int M, int N, int K,
-                    int splits, int tail, int tail_splits, const EpiArgs ea, int* err) {
+                    int splits, int tail, int tail_splits, int group_m, const EpiArgs ea,
+                    int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -199,7 +220,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
         unit_of(u, tile, ks, nks, tt);
         const int kb0 = static_cast<int>(static_cast<int64_t>(ks) * num_k / nks);
         const int kb1 = static_cast<int>(static_cast<int64_t>(ks + 1) * num_k / nks);
-        const int m_idx = tile % num_m, n_idx = tile / num_m;
+        int m_idx, n_idx;
+        tile_coords(tile, num_m, num_n, group_m, m_idx, n_idx);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_spin(&empty[stage], phase ^ 1u, abort)) {
             record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_PRODUCER);
@@ -291,7 +313,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
     for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
       int tile, ks, nks, tt;
       unit_of(u, tile, ks, nks, tt);
-      const int m_idx = tile % num_m, n_idx = tile / num_m;
+      int m_idx, n_idx;
+      tile_coords(tile, num_m, num_n, group_m, m_idx, n_idx);
       // a tail unit's fp32 partial: its own BM x BN block of the workspace
       float* tail_ws = tt >= 0 ? ea.ws + (static_cast<int64_t>(tt) * tail_splits + ks) * BM * BN +
                                      static_cast<int64_t>(quad * 32 + lane) * BN
@@ -341,6 +364,11 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
   }
 }
 
+int group_rows(int64_t M, int64_t K) {
+  const int num_m = static_cast<int>((M + BM - 1) / BM);
+  return M * K * 2 <= kAResidentBytes || num_m < kGroupM ? num_m : kGroupM;
+}
+
 template <int EPI>
 cudaError_t set_attr() {
   return cudaFuncSetAttribute(gemm_tcgen05_kernel<EPI>,
@@ -372,7 +400,7 @@ dlo_status launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N
   const int units = (tiles - tail) * splits + tail * tail_splits;
   const int grid = units < sm_count() ? units : sm_count();
   gemm_tcgen05_kernel<EPI><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
-      ma, mb, M, N, K, splits, tail, tail_splits, ea, err);
+      ma, mb, M, N, K, splits, tail, tail_splits, group_rows(M, K), ea, err);
   DLO_CUDA(cudaGetLastError());
   return DLO_OK;
 }
@@ -446,11 +474,12 @@ splitk_reduce_kernel(const float* __restrict__ ws, int splits, int64_t M, int64_
 
 // The same for the tail tiles only: ws [tail, tail_splits, BM, BN], tail
 // tile tt being output tile num_tiles - tail + tt (tile t at row block
-// t % num_m, column block t / num_m).
+// and column block from tile_coords).
 template <int EPI>
 __global__ void __launch_bounds__(256)
 tail_reduce_kernel(const float* __restrict__ ws, int tail, int tail_splits, int num_tiles,
-                   int num_m, int64_t M, int64_t N, const EpiArgs ea) {
+                   int num_m, int num_n, int group_m, int64_t M, int64_t N,
+                   const EpiArgs ea) {
   constexpr int64_t per_tile = static_cast<int64_t>(BM) * (BN / 4);
   const int64_t total = tail * per_tile;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -459,8 +488,10 @@ tail_reduce_kernel(const float* __restrict__ ws, int tail, int tail_splits, int 
     const int64_t e = i - tt * per_tile;
     const int64_t r = e / (BN / 4), c = (e - r * (BN / 4)) * 4;
     const int tile = num_tiles - tail + tt;
-    const int64_t row = static_cast<int64_t>(tile % num_m) * BM + r;
-    const int64_t col = static_cast<int64_t>(tile / num_m) * BN + c;
+    int m_idx, n_idx;
+    tile_coords(tile, num_m, num_n, group_m, m_idx, n_idx);
+    const int64_t row = static_cast<int64_t>(m_idx) * BM + r;
+    const int64_t col = static_cast<int64_t>(n_idx) * BN + c;
     if (row >= M || col >= N) continue;
     const float* p = ws + (static_cast<int64_t>(tt) * tail_splits * BM + r) * BN + c;
     float4 acc = *reinterpret_cast<const float4*>(p);
@@ -471,15 +502,16 @@ tail_reduce_kernel(const float* __restrict__ ws, int tail, int tail_splits, int 
 
 template <int EPI>
 dlo_status launch_tail_reduce(const float* ws, int tail, int tail_splits, int64_t M, int64_t N,
-                              const EpiArgs& ea, cudaStream_t stream) {
+                              int64_t K, const EpiArgs& ea, cudaStream_t stream) {
   const int num_m = static_cast<int>((M + BM - 1) / BM);
-  const int num_tiles = num_m * static_cast<int>((N + BN - 1) / BN);
+  const int num_n = static_cast<int>((N + BN - 1) / BN);
+  const int num_tiles = num_m * num_n;
   const int64_t total = static_cast<int64_t>(tail) * BM * (BN / 4);
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   if (blocks > cap) blocks = cap;
   tail_reduce_kernel<EPI><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      ws, tail, tail_splits, num_tiles, num_m, M, N, ea);
+      ws, tail, tail_splits, num_tiles, num_m, num_n, group_rows(M, K), M, N, ea);
   DLO_CUDA(cudaGetLastError());
   return DLO_OK;
 }
@@ -600,16 +632,16 @@ dlo_status launch_linear_ex(const uint16_t* a, int64_t M, int64_t K, const uint1
     switch (epilogue) {
       case EPI_BF16:
         DLO_TRY(launch_epi<EPI_BF16>(ma, mb, m, n, k, 1, tl, ts, ea, err, stream));
-        return launch_tail_reduce<EPI_BF16>(ea.ws, tl, ts, M, N, ea, stream);
+        return launch_tail_reduce<EPI_BF16>(ea.ws, tl, ts, M, N, K, ea, stream);
       case EPI_GELU_BF16:
         DLO_TRY(launch_epi<EPI_GELU_BF16>(ma, mb, m, n, k, 1, tl, ts, ea, err, stream));
-        return launch_tail_reduce<EPI_GELU_BF16>(ea.ws, tl, ts, M, N, ea, stream);
+        return launch_tail_reduce<EPI_GELU_BF16>(ea.ws, tl, ts, M, N, K, ea, stream);
       case EPI_RESID_F32:
         DLO_TRY(launch_epi<EPI_RESID_F32>(ma, mb, m, n, k, 1, tl, ts, ea, err, stream));
-        return launch_tail_reduce<EPI_RESID_F32>(ea.ws, tl, ts, M, N, ea, stream);
+        return launch_tail_reduce<EPI_RESID_F32>(ea.ws, tl, ts, M, N, K, ea, stream);
       case EPI_QKV:
         DLO_TRY(launch_epi<EPI_QKV>(ma, mb, m, n, k, 1, tl, ts, ea, err, stream));
-        return launch_tail_reduce<EPI_QKV>(ea.ws, tl, ts, M, N, ea, stream);
+        return launch_tail_reduce<EPI_QKV>(ea.ws, tl, ts, M, N, K, ea, stream);
       default: DLO_FAIL(DLO_ERR_INVALID, "linear: unknown epilogue %d", epilogue);
     }
   }
