@@ -45,6 +45,13 @@ def lib():
         L.oracle_attention.argtypes = [vp, i64, i64, i64, i64, vp, i32]
         L.oracle_block_forward.restype = None
         L.oracle_block_forward.argtypes = [vp, i64, i64, i64, i64, i64, dbl, vp, vp, i32]
+        L.oracle_qk_norm.restype = None
+        L.oracle_qk_norm.argtypes = [vp, i64, i64, i64, vp, vp, dbl]
+        L.oracle_rope.restype = None
+        L.oracle_rope.argtypes = [vp, i64, i64, i64, i64, dbl]
+        L.oracle_block_forward_ex.restype = None
+        L.oracle_block_forward_ex.argtypes = [vp, i64, i64, i64, i64, i64, dbl, vp, vp, vp, vp,
+                                              vp, vp, vp, dbl, vp, i32]
         L.oracle_block_forward_rows.restype = None
         L.oracle_block_forward_rows.argtypes = [vp, i64, i64, i64, i64, i64, dbl, vp, vp, i64,
                                                 vp, i32]
@@ -193,11 +200,43 @@ PARAM_ORDER = ("norm1.weight", "ada1.shift", "ada1.scale", "ada1.gate",
                "mlp.fc1.weight", "mlp.fc2.weight")
 
 
-def block_forward(x, params, batch, tokens, d, heads, f, eps=1e-6, threads=None):
-    """x: float32 [batch*tokens, d]; params: dict name -> float32 ndarray."""
+# the checkpoint-shaped block's optional parameters, in the C call's order
+EXTRA_ORDER = ("attn.qkv.bias", "attn.out.bias", "mlp.fc1.bias", "mlp.fc2.bias",
+               "attn.q_norm.weight", "attn.k_norm.weight")
+
+
+def qk_norm(qkv, d, heads, gq, gk, eps=1e-6):
+    """Per-head RMSNorm of the q and k columns of qkv [rows, 3d] (a copy)."""
+    q = np.array(qkv, dtype=np.float64, order="C", copy=True)
+    gq = np.ascontiguousarray(gq, dtype=np.float32)
+    gk = np.ascontiguousarray(gk, dtype=np.float32)
+    lib().oracle_qk_norm(_ptr(q), q.shape[0], d, heads, _ptr(gq), _ptr(gk), eps)
+    return q
+
+
+def rope(qkv, batch, tokens, d, heads, base=10000.0):
+    """Rotary embedding of the q and k columns of qkv [batch*tokens, 3d] (a copy)."""
+    q = np.array(qkv, dtype=np.float64, order="C", copy=True)
+    lib().oracle_rope(_ptr(q), batch, tokens, d, heads, base)
+    return q
+
+
+def block_forward(x, params, batch, tokens, d, heads, f, eps=1e-6, threads=None,
+                  rope_base=0.0):
+    """x: float32 [batch*tokens, d]; params: dict name -> float32 ndarray.
+    Parameters named in EXTRA_ORDER are applied when present (the
+    checkpoint-shaped block); rope_base > 0 applies rotary embedding."""
     x = np.ascontiguousarray(x, dtype=np.float32).reshape(batch * tokens, d)
     arrs = [np.ascontiguousarray(params[n], dtype=np.float32) for n in PARAM_ORDER]
     out = np.zeros((batch * tokens, d), dtype=np.float64)
+    extras = [np.ascontiguousarray(params[n], dtype=np.float32) if n in params else None
+              for n in EXTRA_ORDER]
+    if any(e is not None for e in extras) or rope_base > 0:
+        ptrs = [e.ctypes.data if e is not None else None for e in extras]
+        lib().oracle_block_forward_ex(_ptr(x), batch, tokens, d, heads, f, eps,
+                                      _ptr_array(arrs), *ptrs, float(rope_base), _ptr(out),
+                                      threads or default_threads())
+        return out
     lib().oracle_block_forward(_ptr(x), batch, tokens, d, heads, f, eps,
                                _ptr_array(arrs), _ptr(out), threads or default_threads())
     return out

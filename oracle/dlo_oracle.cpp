@@ -22,6 +22,10 @@
 // weights.  The block below is the synthetic DiT block the workload
 // specifies (RMSNorm, adaLN shift/scale/gate, QKV linear, softmax attention,
 // out-projection, GELU-tanh MLP); its readings are listed with each function.
+// The checkpoint-shaped variant adds what real DiT checkpoints carry and the
+// pages do not define either: biases on the four linears, a per-head RMSNorm
+// of q and k with learned gains, and rotary position embedding of q and k
+// (plainest readings, stated with oracle_qk_norm and oracle_rope).
 //
 // Arithmetic: every floating-point step runs in IEEE double.  Weights arrive
 // as float (bf16 values widened exactly).  Threads split independent output
@@ -304,6 +308,98 @@ void oracle_attention(const double* qkv, int64_t batch, int64_t tokens,
       }
     }
   });
+}
+
+// Per-head RMSNorm of q and k (the checkpoint-shaped block): for every row
+// and head j, q_j <- q_j / sqrt(mean(q_j^2) + eps) * gq and likewise k_j
+// with gk, each over the head's hd values; gq, gk: [hd].  qkv: [rows, 3d],
+// q in columns [0, d), k in [d, 2d); v untouched.
+void oracle_qk_norm(double* qkv, int64_t rows, int64_t d, int64_t heads, const float* gq,
+                    const float* gk, double eps) {
+  const int64_t hd = d / heads;
+  for (int64_t t = 0; t < rows; ++t)
+    for (int64_t part = 0; part < 2; ++part) {
+      const float* g = part == 0 ? gq : gk;
+      for (int64_t j = 0; j < heads; ++j) {
+        double* v = qkv + t * 3 * d + part * d + j * hd;
+        double ss = 0.0;
+        for (int64_t c = 0; c < hd; ++c) ss += v[c] * v[c];
+        const double inv = 1.0 / std::sqrt(ss / static_cast<double>(hd) + eps);
+        for (int64_t c = 0; c < hd; ++c) v[c] = v[c] * inv * static_cast<double>(g[c]);
+      }
+    }
+}
+
+// Rotary position embedding of q and k (the checkpoint-shaped block), in the
+// form of Su et al., "RoFormer": the head's values are taken in pairs
+// (2i, 2i+1), i = 0 .. hd/2 - 1, and the pair of the token at position p is
+// rotated by the angle p * base^(-2i/hd):
+//   (a, b) <- (a cos - b sin, a sin + b cos).
+// The position is the token's index within its batch item (1-D positions).
+void oracle_rope(double* qkv, int64_t batch, int64_t tokens, int64_t d, int64_t heads,
+                 double base) {
+  const int64_t hd = d / heads;
+  for (int64_t r = 0; r < batch * tokens; ++r) {
+    const double pos = static_cast<double>(r % tokens);
+    for (int64_t part = 0; part < 2; ++part)
+      for (int64_t j = 0; j < heads; ++j) {
+        double* v = qkv + r * 3 * d + part * d + j * hd;
+        for (int64_t i = 0; i < hd / 2; ++i) {
+          const double ang = pos * std::pow(base, -2.0 * static_cast<double>(i) /
+                                                      static_cast<double>(hd));
+          const double c = std::cos(ang), s = std::sin(ang);
+          const double a0 = v[2 * i], b0 = v[2 * i + 1];
+          v[2 * i] = a0 * c - b0 * s;
+          v[2 * i + 1] = a0 * s + b0 * c;
+        }
+      }
+  }
+}
+
+// The block forward with the checkpoint-shaped additions, each optional
+// (null / 0 = absent): biases bqkv[3d], bo[d], b1[f], b2[d] added to the
+// linears' outputs (before the GELU and before the gates); q/k RMSNorm gains
+// gq, gk [hd] (both or neither), applied after the QKV bias; RoPE with
+// rope_base > 0, applied after the q/k norm.  Order of operations:
+//   h = rmsnorm_mod(x); qkv = h Wqkv^T + bqkv; qk-norm; rope; o = attention
+//   x += gate1 * (o Wo^T + bo)
+//   h2 = rmsnorm_mod(x); x += gate2 * (gelu(h2 W1^T + b1) W2^T + b2)
+void oracle_block_forward_ex(const float* x_in, int64_t batch, int64_t tokens, int64_t d,
+                             int64_t heads, int64_t f, double eps, const float* const* p,
+                             const float* bqkv, const float* bo, const float* b1,
+                             const float* b2, const float* gq, const float* gk,
+                             double rope_base, double* x_out, int32_t threads) {
+  const int64_t M = batch * tokens;
+  std::vector<double> x(M * d), h(M * d), qkv(M * 3 * d), o(M * d), y(M * d), u(M * f);
+  for (int64_t e = 0; e < M * d; ++e) x[e] = static_cast<double>(x_in[e]);
+  auto add_bias = [](double* v, int64_t rows, int64_t n, const float* b) {
+    if (!b) return;
+    for (int64_t t = 0; t < rows; ++t)
+      for (int64_t c = 0; c < n; ++c) v[t * n + c] += static_cast<double>(b[c]);
+  };
+  // attention branch
+  oracle_rmsnorm_mod(x.data(), M, d, p[0], p[1], p[2], eps, h.data());
+  oracle_linear(h.data(), M, d, p[4], 3 * d, qkv.data(), threads);
+  add_bias(qkv.data(), M, 3 * d, bqkv);
+  if (gq && gk) oracle_qk_norm(qkv.data(), M, d, heads, gq, gk, eps);
+  if (rope_base > 0.0) oracle_rope(qkv.data(), batch, tokens, d, heads, rope_base);
+  oracle_attention(qkv.data(), batch, tokens, d, heads, o.data(), threads);
+  oracle_linear(o.data(), M, d, p[5], d, y.data(), threads);
+  add_bias(y.data(), M, d, bo);
+  for (int64_t t = 0; t < M; ++t)
+    for (int64_t c = 0; c < d; ++c)
+      x[t * d + c] += static_cast<double>(p[3][c]) * y[t * d + c];
+  // MLP branch
+  oracle_rmsnorm_mod(x.data(), M, d, p[6], p[7], p[8], eps, h.data());
+  oracle_linear(h.data(), M, d, p[10], f, u.data(), threads);
+  add_bias(u.data(), M, f, b1);
+  for (int64_t e = 0; e < M * f; ++e) u[e] = oracle_gelu_tanh(u[e]);
+  oracle_linear(u.data(), M, f, p[11], d, y.data(), threads);
+  add_bias(y.data(), M, d, b2);
+  for (int64_t t = 0; t < M; ++t)
+    for (int64_t c = 0; c < d; ++c)
+      x[t * d + c] += static_cast<double>(p[9][c]) * y[t * d + c];
+  std::memcpy(x_out, x.data(), sizeof(double) * M * d);
 }
 
 // One block forward.  Parameter order of `p` (all float arrays):

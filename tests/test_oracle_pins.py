@@ -433,3 +433,156 @@ def test_transposed_view_survives_physical_order_packing(esize):
             strides=(t_strides[0] * esize, t_strides[1] * esize, 1))
         want = a.reshape(m, n, esize).transpose(1, 0, 2)
         assert np.array_equal(back, want)
+
+
+# ---- the checkpoint-shaped block: biases, per-head q/k RMSNorm, rotary
+# embedding (readings stated in the oracle; RoPE after Su et al., RoFormer) --
+
+def test_rope_two_dims_is_a_rotation_by_the_position():
+    # hd = 2: one pair, frequency base^0 = 1, so the token at position p is
+    # rotated by p radians, q and k alike; v is untouched
+    t = 5
+    qkv = np.zeros((t, 6))
+    qkv[:, 0], qkv[:, 2], qkv[:, 3], qkv[:, 4] = 1.0, 2.0, -1.0, 7.0
+    r = oracle.rope(qkv, 1, t, 2, 1, 10000.0)
+    p = np.arange(t)
+    assert np.allclose(r[:, 0], np.cos(p), atol=1e-15) and np.allclose(r[:, 1], np.sin(p), atol=1e-15)
+    # k = (2, -1): (2 cos + sin, 2 sin - cos)
+    assert np.allclose(r[:, 2], 2 * np.cos(p) + np.sin(p), atol=1e-14)
+    assert np.allclose(r[:, 3], 2 * np.sin(p) - np.cos(p), atol=1e-14)
+    assert np.array_equal(r[:, 4:], qkv[:, 4:])
+
+
+def test_rope_frequencies_and_positions_per_batch_item():
+    # hd = 4: pair i rotates by p * base^(-2i/4); positions restart at 0 in
+    # every batch item (its first token is unrotated)
+    base, t = 10000.0, 4
+    qkv = np.zeros((2 * t, 12))
+    qkv[:, 0:4] = [1.0, 0.0, 1.0, 0.0]
+    r = oracle.rope(qkv, 2, t, 4, 1, base)
+    for row in range(2 * t):
+        p = row % t
+        for i in range(2):
+            ang = p * base ** (-2.0 * i / 4)
+            assert abs(r[row, 2 * i] - math.cos(ang)) < 1e-14
+            assert abs(r[row, 2 * i + 1] - math.sin(ang)) < 1e-14
+    assert np.array_equal(r[t], qkv[t])
+
+
+def test_rope_preserves_pair_norms_and_depends_on_relative_position():
+    rng = np.random.default_rng(21)
+    t, d, heads = 9, 16, 2
+    hd = d // heads
+    qkv = rng.standard_normal((t, 3 * d))
+    r = oracle.rope(qkv, 1, t, d, heads, 10000.0)
+    pair = lambda a: a[:, :2 * d].reshape(t, -1, 2)
+    assert np.allclose(np.linalg.norm(pair(r), axis=2), np.linalg.norm(pair(qkv), axis=2),
+                       atol=1e-12)
+    # the same q and k at every position: rotated q_m . k_n depends on n - m only
+    same = np.tile(rng.standard_normal((1, 3 * d)), (t, 1))
+    rs = oracle.rope(same, 1, t, d, heads, 10000.0)
+    dot = lambda m, n, j: rs[m, j * hd:(j + 1) * hd] @ rs[n, d + j * hd:d + (j + 1) * hd]
+    for j in range(heads):
+        for m, n in [(3, 5), (1, 7), (6, 2)]:
+            assert abs(dot(m, n, j) - dot(0, n - m, j) if n >= m else
+                       dot(m, n, j) - dot(m - n, 0, j)) < 1e-12
+
+
+def test_qk_norm_per_head_unit_rms_and_scale_invariance():
+    rng = np.random.default_rng(22)
+    t, d, heads = 5, 24, 3
+    hd = d // heads
+    qkv = rng.standard_normal((t, 3 * d))
+    qkv[:, :hd] *= 50.0                            # heads normalised separately
+    ones = np.ones(hd, np.float32)
+    r = oracle.qk_norm(qkv, d, heads, ones, ones, eps=0.0)
+    for part in range(2):
+        for j in range(heads):
+            v = r[:, part * d + j * hd:part * d + (j + 1) * hd]
+            assert np.allclose((v ** 2).mean(axis=1), 1.0, atol=1e-13)
+    assert np.array_equal(r[:, 2 * d:], qkv[:, 2 * d:])
+    r2 = oracle.qk_norm(3.5 * qkv, d, heads, ones, ones, eps=0.0)
+    assert np.allclose(r2[:, :2 * d], r[:, :2 * d], atol=1e-13)
+    g = (1 + rng.standard_normal(hd)).astype(np.float32)
+    gk = (1 + rng.standard_normal(hd)).astype(np.float32)
+    rg = oracle.qk_norm(qkv, d, heads, g, gk, eps=0.0)
+    for j in range(heads):
+        assert np.allclose(rg[:, j * hd:(j + 1) * hd], r[:, j * hd:(j + 1) * hd] * g, atol=1e-13)
+        assert np.allclose(rg[:, d + j * hd:d + (j + 1) * hd],
+                           r[:, d + j * hd:d + (j + 1) * hd] * gk, atol=1e-13)
+
+
+def _extras(rng, d, f, hd):
+    return {"attn.qkv.bias": (0.02 * rng.standard_normal(3 * d)).astype(np.float32),
+            "attn.out.bias": (0.02 * rng.standard_normal(d)).astype(np.float32),
+            "mlp.fc1.bias": (0.02 * rng.standard_normal(f)).astype(np.float32),
+            "mlp.fc2.bias": (0.02 * rng.standard_normal(d)).astype(np.float32),
+            "attn.q_norm.weight": (1 + 0.1 * rng.standard_normal(hd)).astype(np.float32),
+            "attn.k_norm.weight": (1 + 0.1 * rng.standard_normal(hd)).astype(np.float32)}
+
+
+def test_full_block_with_zero_weights_adds_the_gated_biases():
+    # every weight zero: attention mixes equal values (v = bv for every
+    # token), so o = bv and the out-projection gives bo; the MLP gives b2:
+    # x_out = x + gate1 * bo + gate2 * b2 exactly, with q/k norm and RoPE on
+    rng = np.random.default_rng(23)
+    d, f, t, heads = 16, 64, 6, 2
+    p = _params(rng, d, f)
+    for k in ("attn.qkv.weight", "attn.out.weight", "mlp.fc1.weight", "mlp.fc2.weight"):
+        p[k][:] = 0
+    p.update(_extras(rng, d, f, d // heads))
+    x = rng.standard_normal((2 * t, d)).astype(np.float32)
+    y = oracle.block_forward(x, p, 2, t, d, heads, f, rope_base=10000.0)
+    g1, g2 = p["ada1.gate"].astype(np.float64), p["ada2.gate"].astype(np.float64)
+    x1 = x.astype(np.float64) + g1 * p["attn.out.bias"].astype(np.float64)
+    expect = x1 + g2 * p["mlp.fc2.bias"].astype(np.float64)
+    assert np.allclose(y, expect, atol=1e-15)
+
+
+def test_full_block_attention_branch_closed_form_with_norm_and_rope():
+    # Wq = Wk = 0 with q/k biases: after the q/k norm and RoPE the scores are
+    # computed from the rotated bias vectors; against that attention written
+    # out here in numpy, with v a permutation of h and Wo a permutation
+    rng = np.random.default_rng(24)
+    d, f, t, heads = 8, 32, 5, 2
+    hd = d // heads
+    p = _params(rng, d, f)
+    p.update(_extras(rng, d, f, hd))
+    pv, po = rng.permutation(d), rng.permutation(d)
+    w = np.zeros((3 * d, d), np.float32)
+    w[2 * d:] = _perm_matrix(pv)
+    p["attn.qkv.weight"] = w
+    p["attn.out.weight"] = _perm_matrix(po)
+    p["ada2.gate"][:] = 0
+    x = rng.standard_normal((t, d)).astype(np.float32)
+    y = oracle.block_forward(x, p, 1, t, d, heads, f, rope_base=100.0)
+    h = oracle.rmsnorm_mod(x.astype(np.float64), p["norm1.weight"], p["ada1.shift"], p["ada1.scale"])
+    b = p["attn.qkv.bias"].astype(np.float64)
+    o = np.zeros((t, d))
+    for j in range(heads):
+        def prep(vec, g, pos):
+            v = vec / np.sqrt((vec ** 2).mean() + 1e-6) * g.astype(np.float64)
+            out = v.copy()
+            for i in range(hd // 2):
+                ang = pos * 100.0 ** (-2.0 * i / hd)
+                out[2 * i] = v[2 * i] * math.cos(ang) - v[2 * i + 1] * math.sin(ang)
+                out[2 * i + 1] = v[2 * i] * math.sin(ang) + v[2 * i + 1] * math.cos(ang)
+            return out
+        qb, kb = b[j * hd:(j + 1) * hd], b[d + j * hd:d + (j + 1) * hd]
+        vv = h[:, pv][:, j * hd:(j + 1) * hd] + b[2 * d + j * hd:2 * d + (j + 1) * hd]
+        for tq in range(t):
+            q = prep(qb, p["attn.q_norm.weight"], tq)
+            s = np.array([q @ prep(kb, p["attn.k_norm.weight"], u) for u in range(t)]) / math.sqrt(hd)
+            wgt = np.exp(s - s.max())
+            o[tq, j * hd:(j + 1) * hd] = (wgt[:, None] * vv).sum(axis=0) / wgt.sum()
+    expect = x + p["ada1.gate"] * (o[:, po] + p["attn.out.bias"])
+    assert np.allclose(y, expect, atol=1e-12)
+
+
+def test_full_block_without_extras_equals_plain_block():
+    rng = np.random.default_rng(25)
+    d, f, t = 16, 64, 5
+    p = _params(rng, d, f)
+    x = rng.standard_normal((t, d)).astype(np.float32)
+    assert np.array_equal(oracle.block_forward(x, p, 1, t, d, 4, f),
+                          oracle.block_forward(x, p, 1, t, d, 4, f, rope_base=0.0))
