@@ -251,13 +251,27 @@ typedef struct {
   int32_t heads;    /* hidden / heads must be 64 or 128 */
   int32_t mlp;      /* multiple of 64 */
   float eps;        /* RMSNorm epsilon */
-  int32_t flags;    /* DLO_FWD_GRAPH: launch the seven kernels as one cached
-                       CUDA graph (captured on first use for this config,
-                       plan, weight base, x and scratch); results are the
-                       same bits as direct launches */
+  int32_t flags;    /* DLO_FWD_* below.  DLO_FWD_GRAPH: launch the block's
+                       kernels as one cached CUDA graph (captured on first
+                       use for this config, plan, weight base, x and
+                       scratch); results are the same bits as direct
+                       launches */
 } dlo_dit_cfg;
 
-enum { DLO_FWD_GRAPH = 1 };
+/* dlo_dit_cfg.flags:
+ *   DLO_FWD_GRAPH    launch the block's kernels as one cached CUDA graph;
+ *   DLO_FWD_ROPE     rotary position embedding of q and k after the QKV linear
+ *                    (checkpoint-shaped block): the head's values in pairs
+ *                    (2i, 2i+1) rotated by p * 10000^(-2i/hd) for the token at
+ *                    position p within its batch item (RoFormer's form);
+ *   DLO_FWD_QK_NORM  per-head RMSNorm of q and k (eps = cfg eps) with the
+ *                    plan's fp32 gains "attn.q_norm.weight" and
+ *                    "attn.k_norm.weight" [hd], before the rotary embedding;
+ *                    required exactly when the plan has those gains.
+ * Biases ("attn.qkv.bias" [3d], "attn.out.bias" [d], "mlp.fc1.bias" [f],
+ * "mlp.fc2.bias" [d], bf16) are added to the linears' outputs whenever the
+ * plan has them (before the GELU and before the gates). */
+enum { DLO_FWD_GRAPH = 1, DLO_FWD_ROPE = 2, DLO_FWD_QK_NORM = 4 };
 
 /* Bytes of device scratch one block forward needs (bf16 h, qkv, V
  * transposed, o, u, and the fp32 workspace of the linears run as K slices:
@@ -315,7 +329,8 @@ dlo_status dlo_forward_noalloc(const dlo_dit_cfg* cfg, const dlo_plan* plan,
 
 /* Single steps of the block, for per-kernel checks (device pointers):
  *   rmsnorm_mod: h = bf16(x / sqrt(mean(x^2)+eps) * g * (1+scale) + shift)
- *   linear:      out = epilogue(a W^T), a bf16 [M,K], W bf16 [N,K];
+ *   linear:      out = epilogue(a W^T + bias), a bf16 [M,K], W bf16 [N,K],
+ *                bias bf16 [N] or null (none);
  *                epilogue 0: out bf16 [M,N] = acc
  *                         1: out bf16 [M,N] = GELU_tanh(acc)
  *                         2: out fp32 [M,N] += gate[N] * acc  (in place)
@@ -337,7 +352,13 @@ dlo_status dlo_forward_noalloc(const dlo_dit_cfg* cfg, const dlo_plan* plan,
  *                order by a second kernel):
  *                dlo_op_attention_scratch_bytes(batch, tokens, d) bytes
  *                (inside dlo_forward the QKV linear writes V transposed
- *                directly). */
+ *                directly).
+ *   qk_norm_rope: in place on the q and k columns of qkv bf16
+ *                [batch*tokens, 3d] (v untouched), per row and head of hd =
+ *                d/heads (64 or 128): RMSNorm over the head with gains
+ *                gq / gk fp32 [hd] (both null: none), then rotary embedding
+ *                with base rope_base (0: none) as DLO_FWD_ROPE describes;
+ *                pointers 16-byte aligned.  The angle is formed in fp32. */
 dlo_status dlo_op_rmsnorm_mod(const float* x, int64_t rows, int64_t d,
                               const float* g, const float* shift,
                               const float* scale, float eps, uint16_t* h,
@@ -345,12 +366,16 @@ dlo_status dlo_op_rmsnorm_mod(const float* x, int64_t rows, int64_t d,
 size_t dlo_op_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t epilogue);
 dlo_status dlo_op_linear(const uint16_t* a, int64_t M, int64_t K,
                          const uint16_t* w, int64_t N, int32_t epilogue,
-                         void* out, const float* gate, void* workspace,
-                         size_t workspace_bytes, void* stream);
+                         void* out, const float* gate, const uint16_t* bias,
+                         void* workspace, size_t workspace_bytes, void* stream);
 size_t dlo_op_attention_scratch_bytes(int64_t batch, int64_t tokens, int64_t d);
 dlo_status dlo_op_attention(const uint16_t* qkv, int64_t batch, int64_t tokens,
                             int64_t d, int64_t heads, uint16_t* o, void* scratch,
                             size_t scratch_bytes, void* stream);
+dlo_status dlo_op_qk_norm_rope(uint16_t* qkv, int64_t batch, int64_t tokens,
+                               int64_t d, int64_t heads, const float* gq,
+                               const float* gk, float eps, float rope_base,
+                               void* stream);
 
 /* ------------------------------------------------------------------------
  * Engine: two slots, the hook schedule, events ([B1] "Double-Buffer Memory

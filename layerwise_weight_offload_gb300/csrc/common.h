@@ -44,10 +44,13 @@ constexpr int kMaxSegments = 64;   // (dtype group, shard) pairs per prefetch
 
 inline int64_t round_up(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 
-// Roles of the synthetic DiT block's parameters.
+// Roles of the synthetic DiT block's parameters: the first R_REQUIRED are
+// required; the rest are the checkpoint-shaped block's optional ones (bf16
+// biases of the four linears, fp32 per-head q/k RMSNorm gains).
 enum Role {
   R_G1 = 0, R_SHIFT1, R_SCALE1, R_GATE1, R_WQKV, R_WO,
-  R_G2, R_SHIFT2, R_SCALE2, R_GATE2, R_W1, R_W2, R_COUNT
+  R_G2, R_SHIFT2, R_SCALE2, R_GATE2, R_W1, R_W2, R_REQUIRED,
+  R_BQKV = R_REQUIRED, R_BO, R_B1, R_B2, R_QNORM, R_KNORM, R_COUNT
 };
 extern const char* const kRoleNames[R_COUNT];
 
@@ -125,6 +128,7 @@ struct EpiArgs {
   int64_t vt_ld;        // EPI_QKV: row stride of vt (>= tokens)
   int tokens;           // EPI_QKV: rows per batch item
   int v_col0;           // EPI_QKV: first V column (2d)
+  const uint16_t* bias; // bf16 [N] added to the product before the epilogue (null: none)
   float* ws;            // split-K workspace [splits, M, N] fp32 (null: no split)
   size_t ws_bytes;
   int64_t ws_rows;      // M, set for the partial epilogue
@@ -146,7 +150,14 @@ int linear_splits(int64_t M, int64_t N, int64_t K, int epilogue);
 size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int epilogue);
 dlo_status launch_linear(const uint16_t* a, int64_t M, int64_t K,
                          const uint16_t* w, int64_t N, int epilogue, void* out,
-                         const float* gate, float* ws, size_t ws_bytes, cudaStream_t stream);
+                         const float* gate, const uint16_t* bias, float* ws, size_t ws_bytes,
+                         cudaStream_t stream);
+// Per-head RMSNorm (gains gq, gk [hd]; both null: none) and rotary
+// embedding (rope_base > 0; 0: none) of the q and k columns of the bf16 qkv
+// buffer [batch*tokens, 3d], in place.
+dlo_status launch_qk_norm_rope(uint16_t* qkv, int64_t batch, int64_t tokens, int64_t d,
+                               int64_t heads, const float* gq, const float* gk, float eps,
+                               float rope_base, cudaStream_t stream);
 dlo_status launch_linear_ex(const uint16_t* a, int64_t M, int64_t K, const uint16_t* w,
                             int64_t N, int epilogue, const EpiArgs& ea, cudaStream_t stream);
 

@@ -19,6 +19,10 @@
 namespace dlo {
 namespace {
 
+// Rotary embedding base of the checkpoint-shaped block (DLO_FWD_ROPE): the
+// RoFormer value.
+constexpr float kRopeBase = 10000.f;
+
 struct ScratchLayout {
   size_t h, qkv, vt, o, u, ws, ws_bytes, total;
   int64_t vt_ld;
@@ -88,6 +92,29 @@ dlo_status check_plan(const dlo_dit_cfg& c, const dlo_plan* plan) {
       DLO_FAIL(DLO_ERR_INVALID, "forward: parameter %s is not 16-byte aligned in the slot",
                kRoleNames[w.role]);
   }
+  // the checkpoint-shaped block's optional parameters: biases used when
+  // present; q/k norm gains exactly when the configuration asks for them
+  const int64_t hd = d / c.heads;
+  const Want opt[] = {{R_BQKV, DLO_BF16, 3 * d, 0}, {R_BO, DLO_BF16, d, 0},
+                      {R_B1, DLO_BF16, f, 0},       {R_B2, DLO_BF16, d, 0},
+                      {R_QNORM, DLO_F32, hd, 0},    {R_KNORM, DLO_F32, hd, 0}};
+  for (const Want& w : opt) {
+    if (plan->role[w.role] < 0) continue;
+    const auto& p = plan->params[plan->role[w.role]];
+    if (p.dtype != w.dtype || p.ndim != 1 || p.shape[0] != w.a)
+      DLO_FAIL(DLO_ERR_INVALID, "forward: parameter %s has the wrong shape or dtype",
+               kRoleNames[w.role]);
+    if (p.slot_offset % 16 != 0)
+      DLO_FAIL(DLO_ERR_INVALID, "forward: parameter %s is not 16-byte aligned in the slot",
+               kRoleNames[w.role]);
+  }
+  const bool has_qk = plan->role[R_QNORM] >= 0 && plan->role[R_KNORM] >= 0;
+  const bool want_qk = (c.flags & DLO_FWD_QK_NORM) != 0;
+  if (want_qk && !has_qk)
+    DLO_FAIL(DLO_ERR_INVALID, "forward: DLO_FWD_QK_NORM without both q/k norm gains in the plan");
+  if (!want_qk && (plan->role[R_QNORM] >= 0 || plan->role[R_KNORM] >= 0))
+    DLO_FAIL(DLO_ERR_INVALID, "forward: the plan has q/k norm gains but the configuration "
+                              "lacks DLO_FWD_QK_NORM");
   return DLO_OK;
 }
 
@@ -97,6 +124,8 @@ dlo_status launch_all(const dlo_dit_cfg* cfg, const dlo_plan* plan, const Scratc
   auto W = [&](int role) { return base + plan->params[plan->role[role]].slot_offset; };
   auto F = [&](int role) { return reinterpret_cast<const float*>(W(role)); };
   auto H = [&](int role) { return reinterpret_cast<const uint16_t*>(W(role)); };
+  // optional parameters: null when absent
+  auto HO = [&](int role) { return plan->role[role] >= 0 ? H(role) : nullptr; };
   uint8_t* s = static_cast<uint8_t*>(scratch);
   uint16_t* h = reinterpret_cast<uint16_t*>(s + sl.h);
   uint16_t* qkv = reinterpret_cast<uint16_t*>(s + sl.qkv);
@@ -115,15 +144,22 @@ dlo_status launch_all(const dlo_dit_cfg* cfg, const dlo_plan* plan, const Scratc
   qa.v_col0 = static_cast<int>(2 * d);
   qa.ws = ws;
   qa.ws_bytes = sl.ws_bytes;
+  qa.bias = HO(R_BQKV);
   DLO_TRY(launch_linear_ex(h, M, d, H(R_WQKV), 3 * d, EPI_QKV, qa, stream));
+  if (cfg->flags & (DLO_FWD_QK_NORM | DLO_FWD_ROPE))
+    DLO_TRY(launch_qk_norm_rope(qkv, cfg->batch, cfg->tokens, d, cfg->heads,
+                                (cfg->flags & DLO_FWD_QK_NORM) ? F(R_QNORM) : nullptr,
+                                (cfg->flags & DLO_FWD_QK_NORM) ? F(R_KNORM) : nullptr, cfg->eps,
+                                (cfg->flags & DLO_FWD_ROPE) ? kRopeBase : 0.f, stream));
   DLO_TRY(launch_attention_vt(qkv, vt, sl.vt_ld, cfg->batch, cfg->tokens, d, cfg->heads, o, ws,
                               sl.ws_bytes, stream));
-  DLO_TRY(launch_linear(o, M, d, H(R_WO), d, EPI_RESID_F32, x, F(R_GATE1), ws, sl.ws_bytes,
-                        stream));
+  DLO_TRY(launch_linear(o, M, d, H(R_WO), d, EPI_RESID_F32, x, F(R_GATE1), HO(R_BO), ws,
+                        sl.ws_bytes, stream));
   DLO_TRY(launch_rmsnorm_mod(x, M, d, F(R_G2), F(R_SHIFT2), F(R_SCALE2), cfg->eps, h, stream));
-  DLO_TRY(launch_linear(h, M, d, H(R_W1), f, EPI_GELU_BF16, u, nullptr, ws, sl.ws_bytes, stream));
-  DLO_TRY(launch_linear(u, M, f, H(R_W2), d, EPI_RESID_F32, x, F(R_GATE2), ws, sl.ws_bytes,
-                        stream));
+  DLO_TRY(launch_linear(h, M, d, H(R_W1), f, EPI_GELU_BF16, u, nullptr, HO(R_B1), ws,
+                        sl.ws_bytes, stream));
+  DLO_TRY(launch_linear(u, M, f, H(R_W2), d, EPI_RESID_F32, x, F(R_GATE2), HO(R_B2), ws,
+                        sl.ws_bytes, stream));
   return DLO_OK;
 }
 
@@ -132,7 +168,7 @@ dlo_status launch_all(const dlo_dit_cfg* cfg, const dlo_plan* plan, const Scratc
 // on: the shape, the plan (by id: addresses of freed plans can be reused),
 // the weight base, x, scratch and the device.
 struct GraphKey {
-  int32_t batch, tokens, hidden, heads, mlp;
+  int32_t batch, tokens, hidden, heads, mlp, flags;
   float eps;
   uint64_t plan_id;
   const void* base;
@@ -141,7 +177,7 @@ struct GraphKey {
   int device;
   bool operator==(const GraphKey& o) const {
     return batch == o.batch && tokens == o.tokens && hidden == o.hidden && heads == o.heads &&
-           mlp == o.mlp && eps == o.eps && plan_id == o.plan_id && base == o.base &&
+           mlp == o.mlp && flags == o.flags && eps == o.eps && plan_id == o.plan_id && base == o.base &&
            x == o.x && scratch == o.scratch && device == o.device;
   }
 };
@@ -157,8 +193,9 @@ dlo_status forward_graph(const dlo_dit_cfg* cfg, const dlo_plan* plan, const Scr
   int dev = 0;
   DLO_CUDA(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) DLO_FAIL(DLO_ERR_INVALID, "forward: device %d out of range", dev);
-  const GraphKey key{cfg->batch, cfg->tokens, cfg->hidden, cfg->heads, cfg->mlp, cfg->eps,
-                     plan->id, block_base, x, scratch, dev};
+  const GraphKey key{cfg->batch, cfg->tokens, cfg->hidden, cfg->heads, cfg->mlp,
+                     cfg->flags & ~static_cast<int32_t>(DLO_FWD_GRAPH), cfg->eps, plan->id,
+                     block_base, x, scratch, dev};
   cudaGraphExec_t exec = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_graph_mu);
@@ -249,6 +286,7 @@ int32_t dlo_forward_launches(const dlo_dit_cfg* cfg) {
   // norm x2, attention (+ the merge of its KV slices), the four linears (+ a
   // reduction each when split), as launch_all issues them
   int32_t n = 2 + attention_plan(cfg->batch, cfg->tokens, d, cfg->heads).launches;
+  if (cfg->flags & (DLO_FWD_QK_NORM | DLO_FWD_ROPE)) ++n;   // q/k norm and rotary embedding
   n += linear_plan(M, 3 * d, d, EPI_QKV).launches;
   n += linear_plan(M, d, d, EPI_RESID_F32).launches;
   n += linear_plan(M, f, d, EPI_GELU_BF16).launches;
@@ -275,11 +313,19 @@ size_t dlo_op_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t ep
 }
 
 dlo_status dlo_op_linear(const uint16_t* a, int64_t M, int64_t K, const uint16_t* w, int64_t N,
-                         int32_t epilogue, void* out, const float* gate, void* workspace,
-                         size_t workspace_bytes, void* stream) {
+                         int32_t epilogue, void* out, const float* gate, const uint16_t* bias,
+                         void* workspace, size_t workspace_bytes, void* stream) {
   DLO_TRY(dlo::preload_kernels());
-  return dlo::launch_linear(a, M, K, w, N, epilogue, out, gate, static_cast<float*>(workspace),
-                            workspace_bytes, static_cast<cudaStream_t>(stream));
+  return dlo::launch_linear(a, M, K, w, N, epilogue, out, gate, bias,
+                            static_cast<float*>(workspace), workspace_bytes,
+                            static_cast<cudaStream_t>(stream));
+}
+
+dlo_status dlo_op_qk_norm_rope(uint16_t* qkv, int64_t batch, int64_t tokens, int64_t d,
+                               int64_t heads, const float* gq, const float* gk, float eps,
+                               float rope_base, void* stream) {
+  return dlo::launch_qk_norm_rope(qkv, batch, tokens, d, heads, gq, gk, eps, rope_base,
+                                  static_cast<cudaStream_t>(stream));
 }
 
 size_t dlo_op_attention_scratch_bytes(int64_t batch, int64_t tokens, int64_t d) {

@@ -73,6 +73,24 @@ __device__ __forceinline__ float gelu_tanh(float z) {
   return 0.5f * z * (1.f + tanhf(k0 * (z + k1 * z * z * z)));
 }
 
+// r[i] (fp32 bits) += bias[n0 + i] for the columns below N (N a multiple of 8).
+__device__ __forceinline__ void add_bias32(uint32_t (&r)[32], const uint16_t* bias, int64_t n0,
+                                           int64_t N) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    if (n0 + 8 * g + 8 > N) break;
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(bias + n0 + 8 * g));
+    const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      r[8 * g + 2 * e] = __float_as_uint(__uint_as_float(r[8 * g + 2 * e]) +
+                                         __uint_as_float(w[e] << 16));
+      r[8 * g + 2 * e + 1] = __float_as_uint(__uint_as_float(r[8 * g + 2 * e + 1]) +
+                                             __uint_as_float(w[e] & 0xFFFF0000u));
+    }
+  }
+}
+
 template <int EPI>
 __device__ __forceinline__ void epilogue_store(const uint32_t (&r)[32], int64_t row, int64_t n0,
                                                int64_t N, int ks, const EpiArgs& ea) {
@@ -342,6 +360,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
                   make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
                               __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
           } else {
+            if (EPI != EPI_PARTIAL && ea.bias) add_bias32(r, ea.bias, n0, N);
             epilogue_store<EPI>(r, row, n0, N, ks, ea);
           }
         }
@@ -410,6 +429,13 @@ dlo_status launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N
 template <int EPI>
 __device__ __forceinline__ void finish4(float4 acc, int64_t row, int64_t c, int64_t N,
                                         const EpiArgs& ea) {
+  if (ea.bias) {
+    const uint2 b = __ldg(reinterpret_cast<const uint2*>(ea.bias + c));
+    acc.x += __uint_as_float(b.x << 16);
+    acc.y += __uint_as_float(b.x & 0xFFFF0000u);
+    acc.z += __uint_as_float(b.y << 16);
+    acc.w += __uint_as_float(b.y & 0xFFFF0000u);
+  }
   if (EPI == EPI_QKV && c >= ea.v_col0) {
     // V columns (v_col0 is a multiple of 64, so all four are V): vt[b*d + c', t]
     const int64_t b = row / ea.tokens, t = row - b * ea.tokens;
@@ -595,6 +621,8 @@ dlo_status launch_linear_ex(const uint16_t* a, int64_t M, int64_t K, const uint1
   if ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(w) |
        reinterpret_cast<uintptr_t>(ea.out)) & 15u)
     DLO_FAIL(DLO_ERR_INVALID, "linear: a, w and out must be 16-byte aligned");
+  if (ea.bias && (reinterpret_cast<uintptr_t>(ea.bias) & 15u))
+    DLO_FAIL(DLO_ERR_INVALID, "linear: the bias must be 16-byte aligned");
   if (epilogue == EPI_RESID_F32 && (!ea.gate || (reinterpret_cast<uintptr_t>(ea.gate) & 15u)))
     DLO_FAIL(DLO_ERR_INVALID, "linear: the residual epilogue needs a 16-byte aligned gate");
   if (epilogue == EPI_QKV &&
@@ -657,12 +685,13 @@ dlo_status launch_linear_ex(const uint16_t* a, int64_t M, int64_t K, const uint1
 }
 
 dlo_status launch_linear(const uint16_t* a, int64_t M, int64_t K, const uint16_t* w, int64_t N,
-                         int epilogue, void* out, const float* gate, float* ws, size_t ws_bytes,
-                         cudaStream_t stream) {
+                         int epilogue, void* out, const float* gate, const uint16_t* bias,
+                         float* ws, size_t ws_bytes, cudaStream_t stream) {
   if (epilogue == EPI_QKV) DLO_FAIL(DLO_ERR_INVALID, "linear: the QKV epilogue is internal");
   EpiArgs ea{};
   ea.out = out;
   ea.gate = gate;
+  ea.bias = bias;
   ea.ws = ws;
   ea.ws_bytes = ws_bytes;
   return launch_linear_ex(a, M, K, w, N, epilogue, ea, stream);

@@ -102,7 +102,107 @@ rmsnorm_mod_kernel(const float* __restrict__ x, int64_t rows, int64_t d,
   }
 }
 
+// Checkpoint-shaped block, after the QKV linear: for each row and head, q
+// and k (bf16 in qkv [rows, 3d], columns [0, d) and [d, 2d)) get an RMSNorm
+// over the head's HD values with gains gq / gk (when given), then rotary
+// embedding (when log2_base > 0): pair (2i, 2i+1) of the token at position
+// p (its index within the batch item) is rotated by p * base^(-2i/HD).  One
+// warp per (row, head, q or k); lane l holds elements l*E .. l*E+E-1
+// (E = HD/32, even), so each pair sits in one lane.  The angle is formed in
+// fp32 (absolute error up to about 1e-3 rad at position 16384, below half a
+// bf16 unit of the rotated values); cos and sin come from sincosf.
+template <int HD>
+__global__ void __launch_bounds__(256)
+qk_norm_rope_kernel(uint16_t* __restrict__ qkv, int64_t rows, int tokens, int d, int heads,
+                    const float* __restrict__ gq, const float* __restrict__ gk, float eps,
+                    float log2_base) {
+  constexpr int E = HD / 32;
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= rows * heads * 2) return;                 // whole warps leave together
+  const int part = static_cast<int>(w & 1);
+  const int head = static_cast<int>((w >> 1) % heads);
+  const int64_t row = (w >> 1) / heads;
+  uint16_t* p = qkv + row * 3 * d + part * d + head * HD + lane * E;
+  float v[E];
+  if (E == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    v[0] = __uint_as_float(u.x << 16);
+    v[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(u.y << 16);
+    v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+  } else {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+    v[0] = __uint_as_float(u << 16);
+    v[1] = __uint_as_float(u & 0xFFFF0000u);
+  }
+  const float* g = part == 0 ? gq : gk;
+  if (g) {
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) ss += v[e] * v[e];
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float inv = rsqrtf(ss / static_cast<float>(HD) + eps);
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = v[e] * inv * __ldg(g + lane * E + e);
+  }
+  if (log2_base > 0.f) {
+    const float pos = static_cast<float>(row % tokens);
+#pragma unroll
+    for (int k = 0; k < E / 2; ++k) {
+      const int i = lane * (E / 2) + k;              // pair index
+      const float theta = exp2f(-2.f * static_cast<float>(i) / static_cast<float>(HD) * log2_base);
+      float s, c;
+      sincosf(pos * theta, &s, &c);
+      const float a0 = v[2 * k], b0 = v[2 * k + 1];
+      v[2 * k] = a0 * c - b0 * s;
+      v[2 * k + 1] = a0 * s + b0 * c;
+    }
+  }
+  uint32_t pk[E / 2];
+#pragma unroll
+  for (int k = 0; k < E / 2; ++k) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+    pk[k] = *reinterpret_cast<uint32_t*>(&b);
+  }
+  if (E == 4)
+    *reinterpret_cast<uint2*>(p) = make_uint2(pk[0], pk[E / 2 - 1]);
+  else
+    *reinterpret_cast<uint32_t*>(p) = pk[0];
+}
+
 }  // namespace
+
+dlo_status launch_qk_norm_rope(uint16_t* qkv, int64_t batch, int64_t tokens, int64_t d,
+                               int64_t heads, const float* gq, const float* gk, float eps,
+                               float rope_base, cudaStream_t stream) {
+  if (batch == 0 || tokens == 0) return DLO_OK;
+  if (!qkv || batch < 0 || tokens < 0 || heads <= 0 || d <= 0 || d % heads != 0 ||
+      (!gq) != (!gk) || !(rope_base >= 0.f))
+    DLO_FAIL(DLO_ERR_INVALID, "qk_norm_rope: bad arguments");
+  const int64_t hd = d / heads;
+  if (hd != 64 && hd != 128) DLO_FAIL(DLO_ERR_INVALID, "qk_norm_rope: head dim %lld", (long long)hd);
+  if ((reinterpret_cast<uintptr_t>(qkv) & 15u) ||
+      (gq && ((reinterpret_cast<uintptr_t>(gq) | reinterpret_cast<uintptr_t>(gk)) & 15u)))
+    DLO_FAIL(DLO_ERR_INVALID, "qk_norm_rope: pointers must be 16-byte aligned");
+  if (!gq && rope_base == 0.f) return DLO_OK;
+  const int64_t rows = batch * tokens;
+  const int64_t warps = rows * heads * 2;
+  const int64_t blocks = (warps * 32 + 255) / 256;
+  if (blocks > 0x7fffffffLL || tokens > 0x7fffffff || d > 0x7fffffff)
+    DLO_FAIL(DLO_ERR_INVALID, "qk_norm_rope: too large");
+  const float l2b = rope_base > 0.f ? log2f(rope_base) : 0.f;
+  if (hd == 64)
+    qk_norm_rope_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        qkv, rows, static_cast<int>(tokens), static_cast<int>(d), static_cast<int>(heads), gq,
+        gk, eps, l2b);
+  else
+    qk_norm_rope_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        qkv, rows, static_cast<int>(tokens), static_cast<int>(d), static_cast<int>(heads), gq,
+        gk, eps, l2b);
+  DLO_CUDA(cudaGetLastError());
+  return DLO_OK;
+}
 
 dlo_status launch_rmsnorm_mod(const float* x, int64_t rows, int64_t d, const float* g,
                               const float* shift, const float* scale, float eps, uint16_t* h,

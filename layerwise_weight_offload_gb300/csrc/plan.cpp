@@ -40,7 +40,9 @@ const char* const kRoleNames[R_COUNT] = {
     "norm1.weight", "ada1.shift", "ada1.scale", "ada1.gate",
     "attn.qkv.weight", "attn.out.weight",
     "norm2.weight", "ada2.shift", "ada2.scale", "ada2.gate",
-    "mlp.fc1.weight", "mlp.fc2.weight"};
+    "mlp.fc1.weight", "mlp.fc2.weight",
+    "attn.qkv.bias", "attn.out.bias", "mlp.fc1.bias", "mlp.fc2.bias",
+    "attn.q_norm.weight", "attn.k_norm.weight"};
 
 static int32_t esize_of(int32_t dtype) {
   switch (dtype) {
@@ -58,7 +60,10 @@ static int32_t esize_of(int32_t dtype) {
 
 // dtype the block forward reads for each DiT role
 static int32_t role_dtype(int r) {
-  return (r == R_WQKV || r == R_WO || r == R_W1 || r == R_W2) ? DLO_BF16 : DLO_F32;
+  return (r == R_WQKV || r == R_WO || r == R_W1 || r == R_W2 || r == R_BQKV || r == R_BO ||
+          r == R_B1 || r == R_B2)
+             ? DLO_BF16
+             : DLO_F32;
 }
 
 }  // namespace dlo
@@ -155,7 +160,7 @@ dlo_status dlo_plan_create(const dlo_param_desc* params, int32_t n_params,
       if (q.name == kRoleNames[r] && q.dtype == role_dtype(r) && q.contiguous)
         plan->role[r] = static_cast<int32_t>(p);
     }
-    if (plan->role[r] < 0) all = false;
+    if (plan->role[r] < 0 && r < R_REQUIRED) all = false;
   }
   plan->has_dit_roles = all;
   *out = plan;

@@ -98,8 +98,10 @@ _SIGS = {
     "dlo_forward_noalloc": (c_i32, [_P(DitCfg), c_vp, c_vp, c_vp, c_vp]),
     "dlo_op_rmsnorm_mod": (c_i32, [c_vp, c_i64, c_i64, c_vp, c_vp, c_vp, c_f32, c_vp, c_vp]),
     "dlo_op_linear_workspace_bytes": (c_sz, [c_i64, c_i64, c_i64, c_i32]),
-    "dlo_op_linear": (c_i32, [c_vp, c_i64, c_i64, c_vp, c_i64, c_i32, c_vp, c_vp, c_vp, c_sz,
-                              c_vp]),
+    "dlo_op_linear": (c_i32, [c_vp, c_i64, c_i64, c_vp, c_i64, c_i32, c_vp, c_vp, c_vp, c_vp,
+                              c_sz, c_vp]),
+    "dlo_op_qk_norm_rope": (c_i32, [c_vp, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp, c_f32, c_f32,
+                                    c_vp]),
     "dlo_op_attention_scratch_bytes": (c_sz, [c_i64, c_i64, c_i64]),
     "dlo_op_attention": (c_i32, [c_vp, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp, c_sz, c_vp]),
     "dlo_engine_create": (c_i32, [_P(EngineDesc), _P(c_vp)]),
@@ -270,12 +272,14 @@ def reassemble_staged(plan, shard_ptrs, staging, staging_bytes, dst, copy_stream
 
 # ---- block forward -----------------------------------------------------------
 
-FWD_GRAPH = 1
+FWD_GRAPH, FWD_ROPE, FWD_QK_NORM = 1, 2, 4
+ROPE_BASE = 10000.0
 
 
-def dit_cfg(batch, tokens, hidden, heads, mlp, eps=1e-6, graph=True):
-    return DitCfg(int(batch), int(tokens), int(hidden), int(heads), int(mlp), float(eps),
-                  FWD_GRAPH if graph else 0)
+def dit_cfg(batch, tokens, hidden, heads, mlp, eps=1e-6, graph=True, rope=False, qk_norm=False):
+    flags = (FWD_GRAPH if graph else 0) | (FWD_ROPE if rope else 0) | \
+        (FWD_QK_NORM if qk_norm else 0)
+    return DitCfg(int(batch), int(tokens), int(hidden), int(heads), int(mlp), float(eps), flags)
 
 
 def forward_launches(cfg):
@@ -307,10 +311,18 @@ def op_linear_workspace_bytes(M, N, K, epilogue):
 
 
 def op_linear(a, M, K, w, N, epilogue, out, gate=None, stream=None, workspace=None,
-              workspace_bytes=0):
+              workspace_bytes=0, bias=None):
     _check(lib().dlo_op_linear(_ptr(a), M, K, _ptr(w), N, int(epilogue), _ptr(out), _ptr(gate),
-                               _ptr(workspace), int(workspace_bytes), _stream(stream)),
+                               _ptr(bias), _ptr(workspace), int(workspace_bytes),
+                               _stream(stream)),
            "dlo_op_linear")
+
+
+def op_qk_norm_rope(qkv, batch, tokens, d, heads, gq=None, gk=None, eps=1e-6, rope_base=0.0,
+                    stream=None):
+    _check(lib().dlo_op_qk_norm_rope(_ptr(qkv), batch, tokens, d, heads, _ptr(gq), _ptr(gk),
+                                     float(eps), float(rope_base), _stream(stream)),
+           "dlo_op_qk_norm_rope")
 
 
 def op_attention_scratch_bytes(batch, tokens, d):

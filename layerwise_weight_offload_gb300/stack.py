@@ -440,7 +440,8 @@ class StreamedStack:
                                  gather_stream=self.gather, two_copy_streams=two_copy_streams)
         for i in range(w.n_blocks):
             self.engine.register_block(i, self.plan, host.shard_ptrs(i % w.distinct))
-        self.cfg = dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps)
+        self.cfg = dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
+                               **W.cfg_flags(w))
         self.scratch_bytes = dlo.forward_scratch_bytes(self.cfg)
         self.scratch = torch.empty(self.scratch_bytes, dtype=torch.uint8, device=device)
         self.primed = False
@@ -508,7 +509,8 @@ class SourceStack:
                                  pack_threads=pack_threads)
         for i in range(w.n_blocks):
             self.engine.register_block_source(i, self.plan, self.srcs[i % w.distinct])
-        self.cfg = dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps)
+        self.cfg = dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
+                               **W.cfg_flags(w))
         self.scratch_bytes = dlo.forward_scratch_bytes(self.cfg)
         self.scratch = torch.empty(self.scratch_bytes, dtype=torch.uint8, device=device)
         self.primed = False
@@ -551,7 +553,8 @@ class ResidentStack:
             dlo.reassemble(self.plan, host.shard_ptrs(hb), b, dlo.COPY_DMA, self.stream)
             self.bufs.append(b)
         self.stream.synchronize()
-        self.cfg = dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps)
+        self.cfg = dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
+                               **W.cfg_flags(w))
         self.scratch_bytes = dlo.forward_scratch_bytes(self.cfg)
         self.scratch = torch.empty(self.scratch_bytes, dtype=torch.uint8, device=device)
 

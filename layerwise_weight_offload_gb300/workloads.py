@@ -16,6 +16,11 @@ Values: linear weights ~ N(0, 0.02) rounded to bf16 (round to nearest even),
 RMSNorm gains = 1, adaLN shift/scale/gate ~ N(0, 0.1) in f32, activations
 x ~ N(0, 1) in f32.  Every tensor has its own torch.Generator seeded from
 (seed, block, parameter index), so any block can be regenerated alone.
+
+The checkpoint-shaped variant ("full") adds what real DiT checkpoints carry:
+bf16 biases ~ N(0, 0.02) after each linear weight, and fp32 per-head q/k
+RMSNorm gains ~ 1 + N(0, 0.1) [hd] after the QKV bias; its forward also
+applies rotary position embedding to q and k.
 """
 from dataclasses import dataclass, replace
 
@@ -40,6 +45,7 @@ class Workload:
     distinct: int         # distinct host blocks; block i uses host block i % distinct
     batch: int = 1
     eps: float = 1e-6
+    variant: str = "dit"  # "full": biases, q/k RMSNorm and RoPE (checkpoint-shaped)
 
     @property
     def head_dim(self):
@@ -78,6 +84,9 @@ CONFIGS = {
     "nano": Workload("nano", 72, 3840, 30, 15360, 4096, 4, 4, 72),
     "super": Workload("super", 128, 6144, 48, 24576, 8192, 2, 2, 32),
 }
+CONFIGS["tiny-full"] = replace(CONFIGS["tiny"], name="tiny-full", variant="full")
+CONFIGS["odd-full"] = replace(CONFIGS["odd"], name="odd-full", variant="full")
+CONFIGS["nano-full"] = replace(CONFIGS["nano"], name="nano-full", variant="full")
 CONFIGS.update(_sweep())
 
 
@@ -93,6 +102,19 @@ def custom(name="custom", **kw):
 def block_param_descs(w: Workload):
     """(name, shape, dtype code) in registration order."""
     d, f = w.hidden, w.mlp
+    if w.variant == "full":
+        hd = d // w.heads
+        return [
+            ("norm1.weight", (d,), F32), ("ada1.shift", (d,), F32),
+            ("ada1.scale", (d,), F32), ("ada1.gate", (d,), F32),
+            ("attn.qkv.weight", (3 * d, d), BF16), ("attn.qkv.bias", (3 * d,), BF16),
+            ("attn.q_norm.weight", (hd,), F32), ("attn.k_norm.weight", (hd,), F32),
+            ("attn.out.weight", (d, d), BF16), ("attn.out.bias", (d,), BF16),
+            ("norm2.weight", (d,), F32), ("ada2.shift", (d,), F32),
+            ("ada2.scale", (d,), F32), ("ada2.gate", (d,), F32),
+            ("mlp.fc1.weight", (f, d), BF16), ("mlp.fc1.bias", (f,), BF16),
+            ("mlp.fc2.weight", (d, f), BF16), ("mlp.fc2.bias", (d,), BF16),
+        ]
     return [
         ("norm1.weight", (d,), F32), ("ada1.shift", (d,), F32),
         ("ada1.scale", (d,), F32), ("ada1.gate", (d,), F32),
@@ -101,6 +123,17 @@ def block_param_descs(w: Workload):
         ("ada2.scale", (d,), F32), ("ada2.gate", (d,), F32),
         ("mlp.fc1.weight", (f, d), BF16), ("mlp.fc2.weight", (d, f), BF16),
     ]
+
+
+def cfg_flags(w: Workload):
+    """Keyword arguments of dlo.dit_cfg for the workload's block variant."""
+    full = w.variant == "full"
+    return {"rope": full, "qk_norm": full}
+
+
+def oracle_rope_base(w: Workload):
+    """rope_base argument of the oracle's block forward for this variant."""
+    return 10000.0 if w.variant == "full" else 0.0
 
 
 def block_param_descs_quantized(w: Workload, kind: str):
@@ -140,6 +173,9 @@ def gen_block(w: Workload, block: int, seed: int = 0, device="cpu"):
     for idx, (name, shape, code) in enumerate(block_param_descs(w)):
         if name.startswith("norm"):
             t = torch.ones(shape, dtype=torch.float32, device=device)
+        elif name.endswith("_norm.weight"):
+            t = 1.0 + 0.1 * torch.randn(shape, generator=_generator(device, seed, block, idx),
+                                        dtype=torch.float32, device=device)
         elif code == F32:
             t = 0.1 * torch.randn(shape, generator=_generator(device, seed, block, idx),
                                   dtype=torch.float32, device=device)

@@ -92,6 +92,66 @@ def test_linear(M, K, N, epi, split):
         assert np.all(np.abs(got - ref) <= tol), np.abs(got - ref).max()
 
 
+@pytest.mark.parametrize("B,T,d,H", [(1, 7, 256, 4), (2, 300, 512, 4), (1, 1000, 1024, 16)])
+@pytest.mark.parametrize("norm,rope", [(True, True), (True, False), (False, True)])
+def test_qk_norm_rope(B, T, d, H, norm, rope):
+    r = _gen(B * T + d + 2 * norm + rope)
+    hd = d // H
+    qkv = (r(B * T, 3 * d)).to(torch.bfloat16)
+    gq, gk = (1.0 + r(hd, std=0.1)), (1.0 + r(hd, std=0.1))
+    dev = qkv.cuda()
+    dlo.op_qk_norm_rope(dev, B, T, d, H, gq.cuda() if norm else None,
+                        gk.cuda() if norm else None, 1e-6, 10000.0 if rope else 0.0)
+    _status_clean()
+    ref = qkv.double().numpy()
+    if norm:
+        ref = oracle.qk_norm(ref, d, H, gq.numpy(), gk.numpy(), 1e-6)
+    if rope:
+        ref = oracle.rope(ref, B, T, d, H, 10000.0)
+    got = dev.double().cpu().numpy()
+    # v untouched bit for bit; q and k within a bf16 rounding plus the fp32
+    # angle (position * frequency rounded to fp32: up to T * 2^-24 rad)
+    assert np.array_equal(got[:, 2 * d:], qkv.double().numpy()[:, 2 * d:])
+    err = np.abs(got[:, :2 * d] - ref[:, :2 * d])
+    scale = np.abs(ref[:, :2 * d]).max()
+    assert np.all(err <= 2.0 ** -8 * np.abs(ref[:, :2 * d]) + (T * 2.0 ** -23 + 1e-5) * scale), \
+        err.max()
+
+
+@pytest.mark.parametrize("epi", [dlo.EPI_BF16, dlo.EPI_GELU_BF16, dlo.EPI_RESID_F32])
+@pytest.mark.parametrize("M,K,N,split", [(200, 320, 264, False), (77, 4096, 1024, True),
+                                         (1000, 1024, 1024, False)])
+def test_linear_bias(M, K, N, epi, split):
+    r = _gen(M + K + N + epi)
+    a = r(M, K).to(torch.bfloat16)
+    w = r(N, K, std=0.05).to(torch.bfloat16)
+    bias = r(N, std=0.5).to(torch.bfloat16)
+    nws = dlo.op_linear_workspace_bytes(M, N, K, epi) if split else 0
+    if split and nws == 0:
+        pytest.skip("this shape does not split")
+    ws = torch.full((max(nws, 16) // 4,), float("nan"), device="cuda") if split else None
+    ref = oracle.linear(a.float().numpy(), w.float().numpy()) + bias.double().numpy()
+    if epi == dlo.EPI_RESID_F32:
+        x = r(M, N)
+        gate = r(N, std=0.1)
+        xd = x.cuda()
+        dlo.op_linear(a.cuda(), M, K, w.cuda(), N, epi, xd, gate.cuda(), None, ws, nws,
+                      bias=bias.cuda())
+        _status_clean()
+        exp = x.numpy().astype(np.float64) + gate.numpy().astype(np.float64) * ref
+        assert np.abs(xd.cpu().numpy() - exp).max() <= 1e-4 * max(1.0, np.abs(exp).max())
+    else:
+        out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        dlo.op_linear(a.cuda(), M, K, w.cuda(), N, epi, out, None, None, ws, nws,
+                      bias=bias.cuda())
+        _status_clean()
+        got = out.float().cpu().numpy()
+        if epi == dlo.EPI_GELU_BF16:
+            ref = np.vectorize(oracle.gelu_tanh)(ref)
+        tol = 2.0 ** -8 * np.abs(ref) + 1e-5 * np.sqrt(K) * np.abs(ref).max()
+        assert np.all(np.abs(got - ref) <= tol), np.abs(got - ref).max()
+
+
 def _sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 

@@ -169,7 +169,8 @@ def _check_against_oracle(host, per_block, which):
         i, xin, xout = per_block[idx]
         p = params_f32(host.params[i % w.distinct])
         xin_np = xin.cpu().numpy()
-        ref = oracle.block_forward(xin_np, p, w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps)
+        ref = oracle.block_forward(xin_np, p, w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
+                                   rope_base=W.oracle_rope_base(w))
         got = xout.cpu().numpy()
         assert_oracle_close(got, ref, "block %d output" % idx)
         # the branch updates alone, which the residual would otherwise mask
@@ -220,6 +221,34 @@ def test_ragged_streamed_vs_resident_vs_oracle(cfg):
     for a, b in zip(res, stm):
         assert torch.equal(a, b)
     _check_against_oracle(host, per_block, range(len(per_block)))
+    host.close()
+
+
+@pytest.mark.parametrize("mode", [dlo.COPY_DMA, dlo.COPY_KERNEL, dlo.COPY_STAGED])
+@pytest.mark.parametrize("cfg", [
+    dict(name="tiny-full"),
+    dict(name="ragged-full", n_blocks=3, hidden=384, heads=3, mlp=1536, tokens=77, shards=5,
+         batch=2),
+    dict(name="hd64-full", n_blocks=2, hidden=512, heads=8, mlp=2048, tokens=300, shards=3),
+])
+def test_checkpoint_shaped_block_streamed_vs_resident_vs_oracle(cfg, mode):
+    # biases on the four linears, per-head q/k RMSNorm, rotary embedding
+    # (positions restart in the second batch item): streamed equals resident
+    # bit for bit, both match the oracle's block with the same additions
+    if cfg["name"] == "tiny-full":
+        w = W.CONFIGS["tiny-full"]
+    else:
+        kw = dict(cfg)
+        name = kw.pop("name")
+        w = W.custom(name, steps=2, variant="full", **kw)
+    host = HostBlocks(w, seed=13, keep_params=True)
+    x0 = W.gen_x(w, seed=13)
+    res, per_block = _run_resident(host, x0, w.steps)
+    stm = _run_streamed(host, x0, w.steps, mode)
+    for a, b in zip(res, stm):
+        assert torch.equal(a, b)
+    _check_against_oracle(host, per_block, range(len(per_block)))
+    assert dlo.kernel_status() == 0
     host.close()
 
 
