@@ -315,7 +315,7 @@ dlo_status dlo_forward(const dlo_dit_cfg* cfg, const dlo_plan* plan,
  * until the process exits).  A shape whose scratch
  * (dlo_forward_scratch_bytes) exceeds 32 MiB is rejected with
  * DLO_ERR_NOMEM.  The call allocates nothing: no cudaMalloc/cudaFree, no
- * graph instantiation (the seven kernels are launched directly, whatever
+ * graph instantiation (the block's kernels are launched directly, whatever
  * cfg->flags says).
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call

@@ -5,11 +5,13 @@
 // gather event ("Distributed Layerwise Offload" (vLLM blog preview,
 // 2026-07-30), "Weight Sharding + AllGather", step 4) with parameters
 // re-pointed into the gathered buffer (step 3).  Here the re-pointing is the
-// plan's slot offsets added to the slot's base; the forward is seven
-// launches on one stream:
-//   rmsnorm_mod -> linear(qkv, bf16) -> attention -> linear(out, gated
-//   residual) -> rmsnorm_mod -> linear(fc1, GELU) -> linear(fc2, gated
-//   residual).
+// plan's slot offsets added to the slot's base; the forward is one stream
+// of launches:
+//   rmsnorm_mod -> linear(qkv, bf16; V transposed) [-> q/k norm + rotary
+//   embedding] -> attention -> linear(out, gated residual) -> rmsnorm_mod ->
+//   linear(fc1, GELU) -> linear(fc2, gated residual),
+// each linear followed by its ordered reduction when some of its tiles run
+// as K slices, and attention by the merge of its KV slices.
 #include <algorithm>
 #include <mutex>
 #include <utility>
@@ -163,7 +165,7 @@ dlo_status launch_all(const dlo_dit_cfg* cfg, const dlo_plan* plan, const Scratc
   return DLO_OK;
 }
 
-// Cached CUDA graphs of the seven launches.  A graph bakes in every kernel
+// Cached CUDA graphs of the block's launches.  A graph bakes in every kernel
 // argument (tensor maps included), so its key is everything those depend
 // on: the shape, the plan (by id: addresses of freed plans can be reused),
 // the weight base, x, scratch and the device.
