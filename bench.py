@@ -61,7 +61,7 @@ def parse():
     ap.add_argument("--pretouch", type=int, default=1,
                     help="1: read every pinned host block once from the GPU before timing")
     ap.add_argument("--only", default=None,
-                    choices=["linear", "fc2", "attention", "norm", "copy", "forward"],
+                    choices=["linear", "fc2", "outproj", "attention", "norm", "copy", "forward"],
                     help="run one kernel of the workload's block `--reps` times (for ncu)")
     ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--source", default="shards", choices=["shards", "pageable", "registered"],
@@ -561,6 +561,14 @@ def run_only(args):
         nws = dlo.op_linear_workspace_bytes(M, d, f, dlo.EPI_RESID_F32)
         ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
         fn = lambda: dlo.op_linear(a, M, f, wt, d, dlo.EPI_RESID_F32, x, gate, s, ws, nws)
+    elif args.only == "outproj":
+        a = torch.randn(M, d, device=dev).to(torch.bfloat16)
+        wt = (0.02 * torch.randn(d, d, device=dev)).to(torch.bfloat16)
+        x = torch.randn(M, d, device=dev)
+        gate = 0.1 * torch.randn(d, device=dev)
+        nws = dlo.op_linear_workspace_bytes(M, d, d, dlo.EPI_RESID_F32)
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev)
+        fn = lambda: dlo.op_linear(a, M, d, wt, d, dlo.EPI_RESID_F32, x, gate, s, ws, nws)
     elif args.only == "attention":
         qkv = torch.randn(M, 3 * d, device=dev).to(torch.bfloat16)
         o = torch.empty(M, d, dtype=torch.bfloat16, device=dev)

@@ -122,17 +122,26 @@ __device__ __forceinline__ void epilogue_store(const uint32_t (&r)[32], int64_t 
     return;
   }
   if (EPI == EPI_RESID_F32) {
+    // all eight loads of x (and of the gate) are issued before the first
+    // store, so the read-modify-write waits for one memory latency per
+    // 32 columns, not eight: with a short K the epilogue is otherwise
+    // slower than the next tile's mainloop it should hide behind
     float* xr = static_cast<float*>(out) + row * N + n0;
+    float4 xv[8], gv[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+      if (n0 + 4 * g + 4 <= N) {
+        xv[g] = *reinterpret_cast<const float4*>(xr + 4 * g);
+        gv[g] = __ldg(reinterpret_cast<const float4*>(gate + n0 + 4 * g));
+      }
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
       if (n0 + 4 * g + 4 <= N) {
-        float4 xv = *reinterpret_cast<float4*>(xr + 4 * g);
-        const float4 gv = __ldg(reinterpret_cast<const float4*>(gate + n0 + 4 * g));
-        xv.x += gv.x * __uint_as_float(r[4 * g + 0]);
-        xv.y += gv.y * __uint_as_float(r[4 * g + 1]);
-        xv.z += gv.z * __uint_as_float(r[4 * g + 2]);
-        xv.w += gv.w * __uint_as_float(r[4 * g + 3]);
-        *reinterpret_cast<float4*>(xr + 4 * g) = xv;
+        xv[g].x += gv[g].x * __uint_as_float(r[4 * g + 0]);
+        xv[g].y += gv[g].y * __uint_as_float(r[4 * g + 1]);
+        xv[g].z += gv[g].z * __uint_as_float(r[4 * g + 2]);
+        xv[g].w += gv[g].w * __uint_as_float(r[4 * g + 3]);
+        *reinterpret_cast<float4*>(xr + 4 * g) = xv[g];
       }
     }
   } else {
