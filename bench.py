@@ -23,6 +23,7 @@ cores; under torchrun only rank 0 runs it.
 """
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -41,7 +42,9 @@ DEFAULT_CONFIG = "odd"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for about 1.5 s, at least 20; "
+                         "the reference arm: 20)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--copy-mode", default="auto", choices=["auto", "dma", "kernel", "staged"])
@@ -125,8 +128,11 @@ class ClockSampler:
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.pre = None
 
     def start(self):
+        """Starts sampling and returns once the first sample is in (at most
+        3 s), so that the samples kept come from the region that follows."""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
@@ -134,6 +140,11 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
+            return
+        import select
+        ready, _, _ = select.select([self.proc.stdout], [], [], 3.0)
+        if ready:
+            self.pre = self.proc.stdout.readline()   # the sample taken before the region
 
     def stop(self):
         if self.proc is None:
@@ -144,9 +155,23 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
+        lines = out.splitlines()
+        adjacent = False
+        if not any(len(l.split(",")) >= 9 for l in lines):
+            # a region shorter than the sampling interval: the samples just
+            # before and just after it stand in, marked as such
+            adjacent = True
+            lines = [self.pre or ""]
+            try:
+                lines += subprocess.run(
+                    ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                     "-i", str(self.index)], capture_output=True, text=True,
+                    timeout=10).stdout.splitlines()
+            except (OSError, subprocess.SubprocessError):
+                pass
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
+        for line in lines:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -158,8 +183,12 @@ class ClockSampler:
             for n, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        res = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+               "reasons": sorted(reasons), "samples": len(sm)}
+        if adjacent:
+            res["adjacent"] = "region shorter than the 200 ms sampling interval: samples " \
+                              "taken just before and just after it"
+        return res
 
 
 def measured_peaks():
@@ -184,7 +213,7 @@ def oracle_block_rate(w, seconds, seed=0):
     n, t0 = 0, time.perf_counter()
     while True:
         oracle.block_forward(x, p, w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
-                             threads=threads)
+                             threads=threads, rope_base=W.oracle_rope_base(w))
         n += 1
         el = time.perf_counter() - t0
         if el >= seconds:
@@ -239,13 +268,16 @@ def run_reference(args, ws, rank):
     p = {k: v.float().numpy() for k, v in W.gen_block(w, 0, args.seed).items()}
     x = W.gen_x(w, args.seed).numpy()
     threads = oracle.default_threads()
+    if args.steps is None:
+        args.steps = 20
+    rb = W.oracle_rope_base(w)
     for _ in range(args.warmup):
         oracle.block_forward(x, p, w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
-                             threads=threads)
+                             threads=threads, rope_base=rb)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         oracle.block_forward(x, p, w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
-                             threads=threads)
+                             threads=threads, rope_base=rb)
     el = time.perf_counter() - t0
     v = args.steps / el
     sample = ("%d oracle block forwards (fp64, naive loops) of host block 0 of workload %s"
@@ -336,6 +368,18 @@ def run_ours(args, ws, rank, local):
 
     run_steps(args.warmup)
     torch.cuda.synchronize()
+    if args.steps is None:
+        # enough timed steps for about 1.5 s of device time (at least 20), so
+        # that the clock samples cover the region; one more untimed step
+        # measures the step time
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st.compute)
+        st.step(x)
+        e1.record(st.compute)
+        torch.cuda.synchronize()
+        est = e0.elapsed_time(e1)
+        args.steps = int(max_over_ranks(max(20, min(5000, math.ceil(1500.0 / max(est, 1e-3)))),
+                                        ws))
     n_copies_before = len(st.engine.copy_times()[0])
     stats0 = st.engine.query()
     barrier(ws)
