@@ -467,8 +467,11 @@ def run_ours(args, ws, rank, local):
     if not args.no_e2e:
         # End to end, as a serving loop runs it: every step's input is copied
         # from pinned host memory and its result read back inside the timed
-        # region, on a data stream and double-buffered, so that step s+1's
-        # input lands and step s's result returns while step s computes.
+        # region, double-buffered, so that step s+1's input lands and step
+        # s's result returns while step s computes.  The input goes through
+        # the weight stream's copy queue (between the block copies, rather
+        # than beside them on a second host-to-device queue); the result
+        # returns on a data stream (the other direction of the link).
         xh = torch.empty_like(x0, device="cpu").pin_memory()
         xh.copy_(x0.cpu())
         yh = [torch.empty_like(xh).pin_memory() for _ in range(2)]
@@ -476,6 +479,8 @@ def run_ours(args, ws, rank, local):
         data = torch.cuda.Stream()
         h2d_ev = [torch.cuda.Event() for _ in range(2)]
         done_ev = [torch.cuda.Event() for _ in range(2)]
+        rb_ev = [torch.cuda.Event() for _ in range(2)]
+        in_q = st.copy if hasattr(st, "copy") else data
         # untimed: one step on each device buffer, so that the forward's cached
         # CUDA graphs for these buffers exist before the timed region
         st.compute.wait_stream(cur)
@@ -486,23 +491,28 @@ def run_ours(args, ws, rank, local):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         barrier(ws)
-        e0.record(data)
-        with torch.cuda.stream(data):
+        e0.record(in_q)
+        with torch.cuda.stream(in_q):
             xd[0].copy_(xh, non_blocking=True)
-        h2d_ev[0].record(data)
+        h2d_ev[0].record(in_q)
         for s in range(args.steps):
             b = s & 1
             st.compute.wait_event(h2d_ev[b])
             st.step(xd[b])
             done_ev[b].record(st.compute)
             with torch.cuda.stream(data):
-                if s + 1 < args.steps:
-                    # the other buffer's last reader was step s-1, whose
-                    # result read-back is already queued on this stream
-                    xd[b ^ 1].copy_(xh, non_blocking=True)
-                    h2d_ev[b ^ 1].record(data)
                 data.wait_event(done_ev[b])
                 yh[b].copy_(xd[b], non_blocking=True)
+                rb_ev[b].record(data)
+            if s + 1 < args.steps:
+                # the other buffer's last reader was step s-1: its result
+                # read-back must be done before the next input lands there
+                with torch.cuda.stream(in_q):
+                    if s >= 1:
+                        in_q.wait_event(rb_ev[b ^ 1])
+                    xd[b ^ 1].copy_(xh, non_blocking=True)
+                    h2d_ev[b ^ 1].record(in_q)
+        data.wait_stream(in_q)
         e1.record(data)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(e0.elapsed_time(e1), ws)
@@ -511,7 +521,8 @@ def run_ours(args, ws, rank, local):
                "h2d_bytes_per_step": xb + w.n_blocks * bytes_per_block,
                "d2h_bytes_per_step": xb,
                "note": "h2d counts x plus every streamed weight shard of the step; x in and "
-                       "the result out are double-buffered on a data stream"}
+                       "the result out are double-buffered; x goes through the weight copy "
+                       "stream, the result returns on a data stream"}
 
     status = dlo.kernel_status()
     if status != 0:
