@@ -272,21 +272,51 @@ def test_forward_with_split_tails_vs_oracle():
     host.close()
 
 
+def _forward_outputs(rs, w, x0, cfgs):
+    # one x buffer (so a graph call with the same configuration replays the
+    # cached graph), reset before each call; the outputs are copied out
+    x = x0.clone()
+    outs = []
+    for cfg in cfgs:
+        rs.cfg = cfg
+        x.copy_(x0)
+        rs.stream.wait_stream(torch.cuda.current_stream())
+        rs.step(x)
+        torch.cuda.current_stream().wait_stream(rs.stream)
+        outs.append(x.clone())
+    torch.cuda.synchronize()
+    return outs
+
+
 def test_graph_replay_equals_direct_launches():
     w = W.custom("graph", n_blocks=2, hidden=256, heads=4, mlp=1024, tokens=130, shards=2)
     host = HostBlocks(w, seed=4)
     rs = ResidentStack(host)
     x0 = W.gen_x(w, seed=4, device="cuda")
-    outs = []
-    for graph in (False, True, True):        # second graph call replays the cached graph
-        rs.cfg = dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps, graph=graph)
-        x = x0.clone()
-        rs.stream.wait_stream(torch.cuda.current_stream())
-        rs.step(x)
-        torch.cuda.current_stream().wait_stream(rs.stream)
-        outs.append(x)
-    torch.cuda.synchronize()
+    cfg = lambda graph: dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
+                                    graph=graph)
+    # direct launches, a captured graph, then its replay
+    outs = _forward_outputs(rs, w, x0, [cfg(False), cfg(True), cfg(True)])
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    host.close()
+
+
+def test_graph_cache_keys_on_the_block_variant_flags():
+    # the checkpoint-shaped block on the same plan, weights, x and scratch with
+    # and without rotary embedding: each flag set gets its own graph (a graph
+    # keyed without the flags would replay the other's launches)
+    w = W.custom("graphfull", n_blocks=1, hidden=256, heads=4, mlp=1024, tokens=96, shards=2,
+                 variant="full")
+    host = HostBlocks(w, seed=6)
+    rs = ResidentStack(host)
+    x0 = W.gen_x(w, seed=6, device="cuda")
+    cfg = lambda graph, rope: dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
+                                          graph=graph, rope=rope, qk_norm=True)
+    outs = _forward_outputs(rs, w, x0, [cfg(False, True), cfg(False, False), cfg(True, True),
+                                        cfg(True, False), cfg(True, True), cfg(True, False)])
+    assert torch.equal(outs[0], outs[2]) and torch.equal(outs[2], outs[4])
+    assert torch.equal(outs[1], outs[3]) and torch.equal(outs[3], outs[5])
+    assert not torch.equal(outs[0], outs[1])
     host.close()
 
 
