@@ -64,9 +64,13 @@ def parse():
     ap.add_argument("--pretouch", type=int, default=1,
                     help="1: read every pinned host block once from the GPU before timing")
     ap.add_argument("--only", default=None,
-                    choices=["linear", "fc2", "outproj", "attention", "norm", "copy", "forward"],
+                    choices=["linear", "qkv", "fc2", "outproj", "attention", "norm", "copy",
+                             "forward"],
                     help="run one kernel of the workload's block `--reps` times (for ncu)")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--gemm-pair", default="auto", choices=["auto", "on", "off"],
+                    help="GEMM kernel of the linears: by shape (auto), CTA pairs for all (on), "
+                         "single CTAs for all (off)")
     ap.add_argument("--source", default="shards", choices=["shards", "pageable", "registered"],
                     help="shards: pinned host shards (default); pageable / registered: the "
                          "rank-local path with one shard, blocks by parameter address")
@@ -298,7 +302,8 @@ def workload_config(w, args):
                         "steps in the workload" % (w.name, w.n_blocks, w.distinct, w.hidden,
                                                    w.heads, w.mlp, w.tokens, w.batch, w.shards,
                                                    w.steps),
-            "name": w.name, "copy_mode": args.copy_mode, "host_source": args.source}
+            "name": w.name, "copy_mode": args.copy_mode, "host_source": args.source,
+            "gemm_pair": args.gemm_pair}
 
 
 def h2d_ceiling_gbs(torch, nbytes=1 << 30, reps=10):
@@ -324,11 +329,17 @@ def h2d_ceiling_gbs(torch, nbytes=1 << 30, reps=10):
     return nbytes / best / 1e6
 
 
+def apply_gemm_pair(dlo, args):
+    dlo.set_gemm_pair_mode({"auto": dlo.GEMM_PAIR_AUTO, "on": dlo.GEMM_PAIR_ON,
+                            "off": dlo.GEMM_PAIR_OFF}[args.gemm_pair])
+
+
 def run_ours(args, ws, rank, local):
     import torch
     from layerwise_weight_offload_gb300 import build as B
     B.build()
     from layerwise_weight_offload_gb300 import dlo, workloads as W
+    apply_gemm_pair(dlo, args)
     from layerwise_weight_offload_gb300.stack import HostBlocks, StreamedStack, ResidentStack
 
     torch.cuda.set_device(local)
@@ -597,6 +608,7 @@ def run_only(args):
     from layerwise_weight_offload_gb300 import build as B
     B.build()
     from layerwise_weight_offload_gb300 import dlo, workloads as W
+    apply_gemm_pair(dlo, args)
     from layerwise_weight_offload_gb300.stack import HostBlocks, ResidentStack
     w = W.CONFIGS[args.config]
     w = W.Workload(**{**w.__dict__, "distinct": 1, "n_blocks": 1})
@@ -608,6 +620,13 @@ def run_only(args):
         wt = (0.02 * torch.randn(f, d, device=dev)).to(torch.bfloat16)
         out = torch.empty(M, f, dtype=torch.bfloat16, device=dev)
         fn = lambda: dlo.op_linear(a, M, d, wt, f, dlo.EPI_GELU_BF16, out, None, s)
+    elif args.only == "qkv":
+        # the QKV linear's shape (its V-transposing epilogue runs only inside
+        # the block forward; the bf16 store stands in for it)
+        a = torch.randn(M, d, device=dev).to(torch.bfloat16)
+        wt = (0.02 * torch.randn(3 * d, d, device=dev)).to(torch.bfloat16)
+        out = torch.empty(M, 3 * d, dtype=torch.bfloat16, device=dev)
+        fn = lambda: dlo.op_linear(a, M, d, wt, 3 * d, dlo.EPI_BF16, out, None, s)
     elif args.only == "fc2":
         a = torch.randn(M, f, device=dev).to(torch.bfloat16)
         wt = (0.02 * torch.randn(d, f, device=dev)).to(torch.bfloat16)
@@ -660,6 +679,7 @@ def run_only(args):
     torch.cuda.synchronize()
     assert dlo.kernel_status() == 0
     print(json.dumps({"only": args.only, "config": args.config, "reps": args.reps,
+                      "gemm_pair": args.gemm_pair,
                       "ms_per_rep": e0.elapsed_time(e1) / args.reps}), flush=True)
 
 
@@ -723,6 +743,7 @@ def run_sweep(args):
     from layerwise_weight_offload_gb300 import build as B
     B.build()
     from layerwise_weight_offload_gb300 import dlo, workloads as W
+    apply_gemm_pair(dlo, args)
     from layerwise_weight_offload_gb300.stack import HostBlocks, StreamedStack, ResidentStack
     bf16_peak, bf16_sust, _, _ = measured_peaks()
     ceiling = h2d_ceiling_gbs(torch)

@@ -377,6 +377,23 @@ dlo_status dlo_op_qk_norm_rope(uint16_t* qkv, int64_t batch, int64_t tokens,
                                const float* gk, float eps, float rope_base,
                                void* stream);
 
+/* Which GEMM kernel runs the linears (a tuning and test switch; the
+ * product of a linear is the same operation either way).  The linears run
+ * either on single CTAs in 128 x 256 output tiles (with the K splits
+ * described under dlo_op_linear) or unsplit on pairs of CTAs in 256 x 256
+ * tiles, each CTA of a pair loading half of both operand tiles for one
+ * tcgen05 MMA over the two SMs (cta_group::2).
+ * mode: -1 (default) by shape: pairs when they fill at least one wave
+ *       and an estimate of the two kernels' time (whole waves of pairs
+ *       against the one-CTA kernel's waves plus the reduction of a split
+ *       last wave) favours them; 0 never; 1 pairs for every linear.
+ * Process-wide; takes effect for linears enqueued afterwards (a block
+ * forward graph already captured keeps the kernels it was captured with).
+ * The split workspace sizes (dlo_op_linear_workspace_bytes,
+ * dlo_forward_scratch_bytes) and dlo_forward_launches follow the mode.
+ * DLO_ERR_INVALID for another mode. */
+dlo_status dlo_set_gemm_pair_mode(int32_t mode);
+
 /* ------------------------------------------------------------------------
  * Engine: two slots, the hook schedule, events ([B1] "Double-Buffer Memory
  * Bound", "Slot Tracking: i%2 + Dynamic Correction"; [B2] §3; [D5]

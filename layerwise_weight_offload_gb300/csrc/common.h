@@ -133,7 +133,9 @@ struct EpiArgs {
   size_t ws_bytes;
   int64_t ws_rows;      // M, set for the partial epilogue
 };
-// How a linear of this shape is run on this GPU's SMs: `splits` K slices
+// How a linear of this shape is run on this GPU's SMs: on CTA pairs in
+// 256 x 256 tiles (`pair`, when the tiles fill the pairs' waves well), else
+// on single CTAs with `splits` K slices
 // for every tile (fewer tiles than SMs), or `tail_splits` K slices for the
 // last `tail` tiles only (a last wave of at most half the SMs); the fp32
 // workspace that needs and the kernel launches (2 with a reduction).
@@ -144,6 +146,7 @@ struct LinearPlan {
   int tail_splits;
   size_t ws_bytes;
   int launches;
+  int pair;             // 1: unsplit on CTA pairs (gemm_pair_kernel), 256 x 256 tiles
 };
 LinearPlan linear_plan(int64_t M, int64_t N, int64_t K, int epilogue);
 int linear_splits(int64_t M, int64_t N, int64_t K, int epilogue);
@@ -199,6 +202,8 @@ int* device_error_word();  // device address (cached per device)
 // module loading), so that no first-launch cost lands in a timed window or
 // inside a graph capture.
 dlo_status gemm_preload();
+dlo_status set_gemm_pair_mode(int mode);   // -1 by shape, 0 never, 1 always
+int gemm_pair_mode();
 dlo_status attention_preload();
 dlo_status copy_preload();
 

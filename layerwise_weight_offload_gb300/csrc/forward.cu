@@ -168,7 +168,7 @@ dlo_status launch_all(const dlo_dit_cfg* cfg, const dlo_plan* plan, const Scratc
 // Cached CUDA graphs of the block's launches.  A graph bakes in every kernel
 // argument (tensor maps included), so its key is everything those depend
 // on: the shape, the plan (by id: addresses of freed plans can be reused),
-// the weight base, x, scratch and the device.
+// the weight base, x, scratch, the device and the GEMM kernel choice.
 struct GraphKey {
   int32_t batch, tokens, hidden, heads, mlp, flags;
   float eps;
@@ -177,10 +177,11 @@ struct GraphKey {
   const float* x;
   const void* scratch;
   int device;
+  int gemm_mode;
   bool operator==(const GraphKey& o) const {
     return batch == o.batch && tokens == o.tokens && hidden == o.hidden && heads == o.heads &&
            mlp == o.mlp && flags == o.flags && eps == o.eps && plan_id == o.plan_id && base == o.base &&
-           x == o.x && scratch == o.scratch && device == o.device;
+           x == o.x && scratch == o.scratch && device == o.device && gemm_mode == o.gemm_mode;
   }
 };
 
@@ -197,7 +198,7 @@ dlo_status forward_graph(const dlo_dit_cfg* cfg, const dlo_plan* plan, const Scr
   if (dev < 0 || dev >= 64) DLO_FAIL(DLO_ERR_INVALID, "forward: device %d out of range", dev);
   const GraphKey key{cfg->batch, cfg->tokens, cfg->hidden, cfg->heads, cfg->mlp,
                      cfg->flags & ~static_cast<int32_t>(DLO_FWD_GRAPH), cfg->eps, plan->id,
-                     block_base, x, scratch, dev};
+                     block_base, x, scratch, dev, gemm_pair_mode()};
   cudaGraphExec_t exec = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_graph_mu);
@@ -322,6 +323,8 @@ dlo_status dlo_op_linear(const uint16_t* a, int64_t M, int64_t K, const uint16_t
                             static_cast<float*>(workspace), workspace_bytes,
                             static_cast<cudaStream_t>(stream));
 }
+
+dlo_status dlo_set_gemm_pair_mode(int32_t mode) { return dlo::set_gemm_pair_mode(mode); }
 
 dlo_status dlo_op_qk_norm_rope(uint16_t* qkv, int64_t batch, int64_t tokens, int64_t d,
                                int64_t heads, const float* gq, const float* gk, float eps,

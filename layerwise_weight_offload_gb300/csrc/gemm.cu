@@ -23,6 +23,9 @@
 // order before the epilogue.  No atomics: every output element is produced
 // by one thread in a fixed order, so results do not depend on addresses or
 // scheduling.
+// Large linears run instead on pairs of CTAs (gemm_pair_kernel below): one
+// tcgen05.mma.cta_group::2 over two SMs per 256 x 256 tile, each CTA loading
+// half of both operand tiles; pair_auto chooses between the two kernels.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -392,19 +395,250 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
   }
 }
 
+// ---- CTA-pair variant ------------------------------------------------------
+//
+// A cluster of two CTAs on two SMs computes one 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16): CTA r of the pair
+// loads rows 128 r .. 128 r + 127 of the tile's A block and of its W block
+// (the MMA reads A's rows from both CTAs and the two W halves as one N = 256
+// operand) and holds rows 128 r .. of the accumulator in its own tensor
+// memory.  Per SM and k-block that is 32 KB of operands for the same
+// 128 x 256 x 64 products the one-CTA kernel feeds with 48 KB, so six stages
+// fit in shared memory instead of four, and each MMA reads 64 bytes of
+// shared memory per cycle instead of 96.
+//   warp 0 (both CTAs)  TMA of its halves into its own ring; both signal
+//                       the even CTA's `full` barrier, which expects the
+//                       bytes of both;
+//   warp 1              allocates the pair's tensor memory (with the peer's
+//                       warp 1); in the even CTA one thread issues the MMAs,
+//                       whose commits arrive on `empty` / `tfull` of both
+//                       CTAs;
+//   warps 2-5           epilogue of the CTA's 128 rows; they release the
+//                       accumulator on the even CTA's `tempty` (8 arrivals).
+constexpr int BM2 = 256, PAIR_STAGES = 6;
+constexpr int PAIR_A_BYTES = (BM2 / 2) * BK * 2;    // 16 KB
+constexpr int PAIR_B_BYTES = (BN / 2) * BK * 2;     // 16 KB
+constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
+constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + 1024 + 256;
+
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
+                 const __grid_constant__ CUtensorMap tma_b, int M, int N, int K, int group_m,
+                 const EpiArgs ea, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + PAIR_STAGES * PAIR_A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + PAIR_STAGES * PAIR_B_BYTES);
+  uint64_t* empty = full + PAIR_STAGES;
+  uint64_t* tfull = empty + PAIR_STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  constexpr uint16_t kBoth = 0x3;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < PAIR_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);
+    }
+    mbar_init(drain, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tma_a);
+    tma_prefetch_desc(&tma_b);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  // both CTAs' barriers are initialised before either may signal the other's
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_m = (M + BM2 - 1) / BM2;
+  const int num_n = (N + BN - 1) / BN;
+  const int num_tiles = num_m * num_n;
+  const int num_k = (K + BK - 1) / BK;
+  const int cid = static_cast<int>(cluster_id_x());
+  const int ncl = static_cast<int>(cluster_count_x());
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = cid; t < num_tiles && ok; t += ncl) {
+        int m_idx, n_idx;
+        tile_coords(t, num_m, num_n, group_m, m_idx, n_idx);
+        const int arow = m_idx * BM2 + static_cast<int>(rank) * (BM2 / 2);
+        const int brow = n_idx * BN + static_cast<int>(rank) * (BN / 2);
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait_spin(&empty[stage], phase ^ 1u, abort)) {
+            record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_PRODUCER);
+            ok = false;
+            break;
+          }
+          const uint32_t bar = cluster_addr(&full[stage], 0);
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * PAIR_STAGE_BYTES);
+          tma_load_2d_pair(sA + stage * PAIR_A_BYTES, &tma_a, bar, kb * BK, arow);
+          tma_load_2d_pair(sB + stage * PAIR_B_BYTES, &tma_b, bar, kb * BK, brow);
+          if (++stage == PAIR_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // loads already issued signal the even CTA's barriers; give them
+        // time to land before the pair can exit (failure path only)
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 2000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM2, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = cid; t < num_tiles && ok; t += ncl) {
+        if (!mbar_wait_spin_cluster(&tempty[acc], acc_phase ^ 1u, abort)) {
+          record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_MMA_EMPTY);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_k; ++kb) {
+          if (!mbar_wait_spin(&full[stage], phase, abort)) {
+            record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_MMA_FULL);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * PAIR_A_BYTES);
+          const uint32_t b_addr = smem_u32(sB + stage * PAIR_B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16_pair(d_tmem, sdesc_k_sw128(a_addr + kk * 32),
+                           sdesc_k_sw128(b_addr + kk * 32), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          umma_commit_pair(&empty[stage], kBoth);
+          if (++stage == PAIR_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair(&tfull[acc], kBoth);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // every MMA issued has completed (and its commits have arrived)
+      // before either CTA frees tensor memory or exits
+      umma_commit_pair(drain, kBoth);
+    }
+  } else {
+    const int quad = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const uint32_t tempty_leader0 = cluster_addr(&tempty[0], 0);
+    const uint32_t tempty_leader1 = cluster_addr(&tempty[1], 0);
+    for (int t = cid; t < num_tiles; t += ncl) {
+      int m_idx, n_idx;
+      tile_coords(t, num_m, num_n, group_m, m_idx, n_idx);
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tfull[acc], acc_phase, abort))) {
+        if (lane == 0) record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_EPILOGUE);
+        break;
+      }
+      tc_fence_after();
+      const int64_t row = static_cast<int64_t>(m_idx) * BM2 + rank * (BM2 / 2) + quad * 32 + lane;
+      const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) +
+                             (static_cast<uint32_t>(quad * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int64_t n0 = static_cast<int64_t>(n_idx) * BN + c * 32;
+        if (n0 >= N) break;
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + c * 32, r);
+        tmem_ld_wait();
+        if (row < M) {
+          if (ea.bias) add_bias32(r, ea.bias, n0, N);
+          epilogue_store<EPI>(r, row, n0, N, 0, ea);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc == 0 ? tempty_leader0 : tempty_leader1);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  // the even CTA's last commit (drain) reaches both CTAs once every MMA of
+  // the pair is done; then neither CTA's shared or tensor memory is used by
+  // the other any more
+  if (warp == 1 && lane == 0) {
+    volatile int never = 0;
+    if (!mbar_wait_bounded(drain, 0, &never)) record_failure(err, abort, DEV_TIMEOUT_MMA_FULL);
+  }
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
 int group_rows(int64_t M, int64_t K) {
   const int num_m = static_cast<int>((M + BM - 1) / BM);
   return M * K * 2 <= kAResidentBytes || num_m < kGroupM ? num_m : kGroupM;
 }
 
+// The same grouping for the pair kernel's 256-row blocks (the same rows
+// per group).
+int group_rows_pair(int64_t M, int64_t K) {
+  const int num_m = static_cast<int>((M + BM2 - 1) / BM2);
+  constexpr int g = kGroupM * BM / BM2;
+  return M * K * 2 <= kAResidentBytes || num_m < g ? num_m : g;
+}
+
 template <int EPI>
 cudaError_t set_attr() {
-  return cudaFuncSetAttribute(gemm_tcgen05_kernel<EPI>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t e = cudaFuncSetAttribute(gemm_tcgen05_kernel<EPI>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess || EPI == EPI_PARTIAL) return e;
+  return cudaFuncSetAttribute(gemm_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              PAIR_SMEM_BYTES);
 }
 
 cudaError_t g_attr_err = cudaSuccess;
 std::once_flag g_attr_once;
+int g_pair_clusters = 0;   // co-resident CTA pairs of the pair kernel (0: not available)
 
 void set_all_attrs() {
   std::call_once(g_attr_once, [] {
@@ -415,7 +649,89 @@ void set_all_attrs() {
     g_attr_err = cudaSuccess;
     for (cudaError_t e : all)
       if (e != cudaSuccess) g_attr_err = e;
+    if (g_attr_err != cudaSuccess) return;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * sm_count());
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<EPI_BF16>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    g_pair_clusters = n;
   });
+}
+
+// -1: choose by shape (pair_auto), 0: never the pair kernel, 1: the pair
+// kernel for every linear it can run (tests and measurements).
+int g_pair_mode = -1;
+
+// The pair kernel runs a linear unsplit in 256 x 256 tiles, in whole waves
+// of CTA pairs; the one-CTA kernel runs 128 x 256 tiles and spreads a short
+// last wave over the idle SMs as K slices, at the cost of a reduction
+// launch.  Estimated in k-block steps of one wave: the pair kernel takes
+// ceil(pair tiles / pairs) waves of num_k steps at 0.9 of the one-CTA step
+// time (measured on GB300: 1.86 vs 1.71 PFLOP/s on Super's fc1); the one-CTA
+// kernel tiles / SMs waves when its tail splits, plus about 40 steps for the
+// split tail's reduction (the reduction's launch and partial-sum traffic),
+// else whole waves.  On GB300 this picks pairs for all four linears at
+// Super's shapes and for Nano's QKV, fc1 and out-projection, and keeps
+// Nano's fc2 (long K, a last pair wave under a fifth full) on single CTAs;
+// grids with fewer pair tiles than pairs keep the one-CTA kernel's K splits.
+bool pair_auto(int64_t M, int64_t N, int64_t K, int clusters) {
+  const int64_t tiles2 = ((M + BM2 - 1) / BM2) * ((N + BN - 1) / BN);
+  const int64_t num_k = (K + BK - 1) / BK;
+  if (tiles2 < clusters || num_k < 4) return false;
+  const int64_t sms = sm_count();
+  const int64_t tiles1 = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const double pair_cost = 0.9 * static_cast<double>((tiles2 + clusters - 1) / clusters) * num_k;
+  const int64_t tail = tiles1 % sms;
+  int64_t ts = tail > 0 ? sms / tail : 0;
+  if (ts > num_k / 4) ts = num_k / 4;
+  const double one_cost =
+      tail > 0 && ts >= 2
+          ? static_cast<double>(tiles1) / static_cast<double>(sms) * num_k + 40.0
+          : static_cast<double>((tiles1 + sms - 1) / sms) * num_k;
+  return pair_cost < one_cost;
+}
+
+bool use_pair(int64_t M, int64_t N, int64_t K) {
+  set_all_attrs();
+  if (g_attr_err != cudaSuccess || g_pair_clusters <= 0 || g_pair_mode == 0) return false;
+  if (g_pair_mode == 1) return true;
+  return pair_auto(M, N, K, g_pair_clusters);
+}
+
+template <int EPI>
+dlo_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int K,
+                       const EpiArgs& ea, int* err, cudaStream_t stream) {
+  set_all_attrs();
+  DLO_CUDA(g_attr_err);
+  const int tiles = ((M + BM2 - 1) / BM2) * ((N + BN - 1) / BN);
+  const int clusters = tiles < g_pair_clusters ? tiles : g_pair_clusters;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  DLO_CUDA(cudaLaunchKernelEx(&cfg, gemm_pair_kernel<EPI>, ma, mb, M, N, K,
+                              group_rows_pair(M, K), ea, err));
+  return DLO_OK;
 }
 
 template <int EPI>
@@ -567,7 +883,11 @@ dlo_status launch_reduce(const float* ws, int splits, int64_t M, int64_t N, cons
 }  // namespace
 
 LinearPlan linear_plan(int64_t M, int64_t N, int64_t K, int epilogue) {
-  LinearPlan p{1, 0, 1, 0, 1};
+  LinearPlan p{1, 0, 1, 0, 1, 0};
+  if (epilogue != EPI_PARTIAL && use_pair(M, N, K)) {
+    p.pair = 1;
+    return p;
+  }
   const int64_t sms = sm_count();
   const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int64_t num_k = (K + BK - 1) / BK;
@@ -609,6 +929,14 @@ size_t linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int epilogue) {
 namespace {
 }  // namespace
 
+dlo_status set_gemm_pair_mode(int mode) {
+  if (mode < -1 || mode > 1) DLO_FAIL(DLO_ERR_INVALID, "gemm pair mode %d (expected -1, 0, 1)", mode);
+  g_pair_mode = mode;
+  return DLO_OK;
+}
+
+int gemm_pair_mode() { return g_pair_mode; }
+
 dlo_status gemm_preload() {
   set_all_attrs();
   DLO_CUDA(g_attr_err);
@@ -640,11 +968,22 @@ dlo_status launch_linear_ex(const uint16_t* a, int64_t M, int64_t K, const uint1
     DLO_FAIL(DLO_ERR_INVALID, "linear: bad arguments for the QKV epilogue");
   int* err = device_error_word();
   if (!err) DLO_FAIL(DLO_ERR_CUDA, "linear: cannot resolve the device error word");
-  CUtensorMap ma, mb;
-  DLO_TRY(make_tmap_2d(&ma, a, M, K, K, BM, BK));
-  DLO_TRY(make_tmap_2d(&mb, w, N, K, K, BN, BK));
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   const LinearPlan plan = linear_plan(M, N, K, epilogue);
+  CUtensorMap ma, mb;
+  if (plan.pair) {
+    DLO_TRY(make_tmap_2d(&ma, a, M, K, K, BM2 / 2, BK));
+    DLO_TRY(make_tmap_2d(&mb, w, N, K, K, BN / 2, BK));
+    switch (epilogue) {
+      case EPI_BF16: return launch_pair<EPI_BF16>(ma, mb, m, n, k, ea, err, stream);
+      case EPI_GELU_BF16: return launch_pair<EPI_GELU_BF16>(ma, mb, m, n, k, ea, err, stream);
+      case EPI_RESID_F32: return launch_pair<EPI_RESID_F32>(ma, mb, m, n, k, ea, err, stream);
+      case EPI_QKV: return launch_pair<EPI_QKV>(ma, mb, m, n, k, ea, err, stream);
+      default: DLO_FAIL(DLO_ERR_INVALID, "linear: unknown epilogue %d", epilogue);
+    }
+  }
+  DLO_TRY(make_tmap_2d(&ma, a, M, K, K, BM, BK));
+  DLO_TRY(make_tmap_2d(&mb, w, N, K, K, BN, BK));
   const bool have_ws = plan.ws_bytes > 0 && ea.ws && ea.ws_bytes >= plan.ws_bytes &&
                        !(reinterpret_cast<uintptr_t>(ea.ws) & 15u);
   const int splits = plan.splits;

@@ -102,6 +102,7 @@ _SIGS = {
                               c_sz, c_vp]),
     "dlo_op_qk_norm_rope": (c_i32, [c_vp, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp, c_f32, c_f32,
                                     c_vp]),
+    "dlo_set_gemm_pair_mode": (c_i32, [c_i32]),
     "dlo_op_attention_scratch_bytes": (c_sz, [c_i64, c_i64, c_i64]),
     "dlo_op_attention": (c_i32, [c_vp, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp, c_sz, c_vp]),
     "dlo_engine_create": (c_i32, [_P(EngineDesc), _P(c_vp)]),
@@ -316,6 +317,15 @@ def op_linear(a, M, K, w, N, epilogue, out, gate=None, stream=None, workspace=No
                                _ptr(bias), _ptr(workspace), int(workspace_bytes),
                                _stream(stream)),
            "dlo_op_linear")
+
+
+GEMM_PAIR_AUTO, GEMM_PAIR_OFF, GEMM_PAIR_ON = -1, 0, 1
+
+
+def set_gemm_pair_mode(mode):
+    """Which GEMM kernel runs the linears: GEMM_PAIR_AUTO (by shape),
+    GEMM_PAIR_OFF (single CTAs) or GEMM_PAIR_ON (CTA pairs for all)."""
+    _check(lib().dlo_set_gemm_pair_mode(int(mode)), "dlo_set_gemm_pair_mode")
 
 
 def op_qk_norm_rope(qkv, batch, tokens, d, heads, gq=None, gk=None, eps=1e-6, rope_base=0.0,
