@@ -156,9 +156,18 @@ def _sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
+@pytest.fixture
+def one_cta_gemm():
+    # the single-CTA kernel and its K splits for every linear (a shape with
+    # enough tiles would otherwise run on CTA pairs)
+    dlo.set_gemm_pair_mode(dlo.GEMM_PAIR_OFF)
+    yield
+    dlo.set_gemm_pair_mode(dlo.GEMM_PAIR_AUTO)
+
+
 @pytest.mark.parametrize("epi", [dlo.EPI_BF16, dlo.EPI_GELU_BF16, dlo.EPI_RESID_F32])
 @pytest.mark.parametrize("shape", ["column", "grid"])
-def test_linear_tail_split(epi, shape):
+def test_linear_tail_split(epi, shape, one_cta_gemm):
     # a short last wave: only its tiles are split in K, the rest finish in
     # the kernel; "grid": 3 column blocks, the tail tile being the ragged
     # last row block of the ragged last column block.  Checked on the rows of

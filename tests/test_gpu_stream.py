@@ -256,7 +256,16 @@ def test_forward_with_split_tails_vs_oracle():
     # tokens chosen so that the QKV linear's tiles (6 column blocks at
     # d = 512) leave a short last wave on this GPU: that tail runs as K slices
     # with the transposed-V epilogue in the reduction; the out-projection and
-    # fc2 have fewer tiles than SMs and split every tile
+    # fc2 have fewer tiles than SMs and split every tile (all on the
+    # single-CTA kernel: by shape the QKV linear would run on CTA pairs)
+    dlo.set_gemm_pair_mode(dlo.GEMM_PAIR_OFF)
+    try:
+        _forward_with_split_tails_vs_oracle()
+    finally:
+        dlo.set_gemm_pair_mode(dlo.GEMM_PAIR_AUTO)
+
+
+def _forward_with_split_tails_vs_oracle():
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     num_m = -(-(sms + 1) // 6)
     assert 1 <= 6 * num_m - sms <= sms // 2
