@@ -421,11 +421,15 @@ constexpr int PAIR_B_BYTES = (BN / 2) * BK * 2;     // 16 KB
 constexpr int PAIR_STAGE_BYTES = PAIR_A_BYTES + PAIR_B_BYTES;
 constexpr int PAIR_SMEM_BYTES = PAIR_STAGES * PAIR_STAGE_BYTES + 1024 + 256;
 
+// Work units as in the one-CTA kernel without the all-tile split: output
+// tiles, then the last `tail` tiles (a short last wave of pairs) as
+// `tail_splits` K slices each, whose fp32 partials go to the workspace as
+// 256 x 256 blocks for tail_reduce_kernel.
 template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
-                 const __grid_constant__ CUtensorMap tma_b, int M, int N, int K, int group_m,
-                 const EpiArgs ea, int* err) {
+                 const __grid_constant__ CUtensorMap tma_b, int M, int N, int K, int tail,
+                 int tail_splits, int group_m, const EpiArgs ea, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -478,18 +482,38 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
   const int num_k = (K + BK - 1) / BK;
   const int cid = static_cast<int>(cluster_id_x());
   const int ncl = static_cast<int>(cluster_count_x());
+  const int n_main = num_tiles - tail;
+  const int num_units = n_main + tail * tail_splits;
+  // unit -> tile, its k-blocks [kb0, kb1), and (tail units) tail index and slice
+  auto unit_of = [&](int u, int& tile, int& kb0, int& kb1, int& tt, int& ks) {
+    if (u < n_main) {
+      tile = u;
+      kb0 = 0;
+      kb1 = num_k;
+      tt = -1;
+      ks = 0;
+    } else {
+      tt = (u - n_main) / tail_splits;
+      ks = (u - n_main) - tt * tail_splits;
+      tile = n_main + tt;
+      kb0 = static_cast<int>(static_cast<int64_t>(ks) * num_k / tail_splits);
+      kb1 = static_cast<int>(static_cast<int64_t>(ks + 1) * num_k / tail_splits);
+    }
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = cid; t < num_tiles && ok; t += ncl) {
+      for (int u = cid; u < num_units && ok; u += ncl) {
+        int t, kb0, kb1, tt, ks;
+        unit_of(u, t, kb0, kb1, tt, ks);
         int m_idx, n_idx;
         tile_coords(t, num_m, num_n, group_m, m_idx, n_idx);
         const int arow = m_idx * BM2 + static_cast<int>(rank) * (BM2 / 2);
         const int brow = n_idx * BN + static_cast<int>(rank) * (BN / 2);
-        for (int kb = 0; kb < num_k; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_spin(&empty[stage], phase ^ 1u, abort)) {
             record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_PRODUCER);
             ok = false;
@@ -521,7 +545,9 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int t = cid; t < num_tiles && ok; t += ncl) {
+      for (int u = cid; u < num_units && ok; u += ncl) {
+        int t, kb0, kb1, tt, ks;
+        unit_of(u, t, kb0, kb1, tt, ks);
         if (!mbar_wait_spin_cluster(&tempty[acc], acc_phase ^ 1u, abort)) {
           record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_MMA_EMPTY);
           ok = false;
@@ -529,7 +555,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < num_k; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait_spin(&full[stage], phase, abort)) {
             record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_MMA_FULL);
             ok = false;
@@ -541,7 +567,8 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             umma_bf16_pair(d_tmem, sdesc_k_sw128(a_addr + kk * 32),
-                           sdesc_k_sw128(b_addr + kk * 32), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                           sdesc_k_sw128(b_addr + kk * 32), idesc,
+                           (kb > kb0 || kk > 0) ? 1u : 0u);
           umma_commit_pair(&empty[stage], kBoth);
           if (++stage == PAIR_STAGES) {
             stage = 0;
@@ -565,15 +592,22 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
     uint32_t acc_phase = 0;
     const uint32_t tempty_leader0 = cluster_addr(&tempty[0], 0);
     const uint32_t tempty_leader1 = cluster_addr(&tempty[1], 0);
-    for (int t = cid; t < num_tiles; t += ncl) {
+    for (int u = cid; u < num_units; u += ncl) {
+      int t, kb0, kb1, tt, ks;
+      unit_of(u, t, kb0, kb1, tt, ks);
       int m_idx, n_idx;
       tile_coords(t, num_m, num_n, group_m, m_idx, n_idx);
+      const int r_tile = static_cast<int>(rank) * (BM2 / 2) + quad * 32 + lane;  // row in tile
+      // a tail unit's fp32 partial: its own BM2 x BN block of the workspace
+      float* tail_ws = tt >= 0 ? ea.ws + ((static_cast<int64_t>(tt) * tail_splits + ks) * BM2 +
+                                          r_tile) * BN
+                               : nullptr;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(&tfull[acc], acc_phase, abort))) {
         if (lane == 0) record_failure(err, abort, *abort ? DEV_ABORTED : DEV_TIMEOUT_EPILOGUE);
         break;
       }
       tc_fence_after();
-      const int64_t row = static_cast<int64_t>(m_idx) * BM2 + rank * (BM2 / 2) + quad * 32 + lane;
+      const int64_t row = static_cast<int64_t>(m_idx) * BM2 + r_tile;
       const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) +
                              (static_cast<uint32_t>(quad * 32) << 16);
 #pragma unroll 1
@@ -584,8 +618,16 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
         tmem_ld_32x32b_x32(t_row + c * 32, r);
         tmem_ld_wait();
         if (row < M) {
-          if (ea.bias) add_bias32(r, ea.bias, n0, N);
-          epilogue_store<EPI>(r, row, n0, N, 0, ea);
+          if (tail_ws) {
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+              *reinterpret_cast<float4*>(tail_ws + c * 32 + 4 * g) =
+                  make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                              __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+          } else {
+            if (ea.bias) add_bias32(r, ea.bias, n0, N);
+            epilogue_store<EPI>(r, row, n0, N, 0, ea);
+          }
         }
       }
       tc_fence_before();
@@ -674,33 +716,39 @@ void set_all_attrs() {
 // kernel for every linear it can run (tests and measurements).
 int g_pair_mode = -1;
 
-// The pair kernel runs a linear unsplit in 256 x 256 tiles, in whole waves
-// of CTA pairs; the one-CTA kernel runs 128 x 256 tiles and spreads a short
-// last wave over the idle SMs as K slices, at the cost of a reduction
-// launch.  Estimated in k-block steps of one wave: the pair kernel takes
-// ceil(pair tiles / pairs) waves of num_k steps at 0.9 of the one-CTA step
-// time (measured on GB300: 1.86 vs 1.71 PFLOP/s on Super's fc1); the one-CTA
-// kernel tiles / SMs waves when its tail splits, plus about 40 steps for the
-// split tail's reduction (the reduction's launch and partial-sum traffic),
-// else whole waves.  On GB300 this picks pairs for all four linears at
-// Super's shapes and for Nano's QKV, fc1 and out-projection, and keeps
-// Nano's fc2 (long K, a last pair wave under a fifth full) on single CTAs;
-// grids with fewer pair tiles than pairs keep the one-CTA kernel's K splits.
+// The pair kernel runs 256 x 256 tiles in waves of CTA pairs, the one-CTA
+// kernel 128 x 256 tiles in waves of SMs; both spread a short last wave over
+// the idle workers as K slices, at the cost of a reduction launch.  Both are
+// estimated by wave_cost in k-block steps of one wave, the pair kernel's
+// steps at 0.9 of the one-CTA kernel's (measured on GB300: 1.86 vs 1.71
+// PFLOP/s on Super's fc1).  Grids with fewer pair tiles than pairs keep the
+// one-CTA kernel and its K splits of every tile.
+// K slices for the tiles of a short last wave of `slots` workers (at least
+// 4 k-blocks a slice, at most 8 slices); 1: no split.
+int64_t tail_slices(int64_t tiles, int64_t slots, int64_t num_k) {
+  const int64_t tail = tiles % slots;
+  if (tiles < slots || tail == 0) return 1;
+  int64_t ts = slots / tail;
+  if (ts > num_k / 4) ts = num_k / 4;
+  if (ts > 8) ts = 8;
+  return ts >= 2 ? ts : 1;
+}
+
+// Estimated time of `tiles` on `slots` workers in k-block steps of a wave:
+// fractional waves plus ~40 steps for the reduction when the last wave's
+// tiles split, else whole waves.
+double wave_cost(int64_t tiles, int64_t slots, int64_t num_k) {
+  if (tail_slices(tiles, slots, num_k) > 1)
+    return static_cast<double>(tiles) / static_cast<double>(slots) * num_k + 40.0;
+  return static_cast<double>((tiles + slots - 1) / slots) * num_k;
+}
+
 bool pair_auto(int64_t M, int64_t N, int64_t K, int clusters) {
   const int64_t tiles2 = ((M + BM2 - 1) / BM2) * ((N + BN - 1) / BN);
   const int64_t num_k = (K + BK - 1) / BK;
   if (tiles2 < clusters || num_k < 4) return false;
-  const int64_t sms = sm_count();
   const int64_t tiles1 = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const double pair_cost = 0.9 * static_cast<double>((tiles2 + clusters - 1) / clusters) * num_k;
-  const int64_t tail = tiles1 % sms;
-  int64_t ts = tail > 0 ? sms / tail : 0;
-  if (ts > num_k / 4) ts = num_k / 4;
-  const double one_cost =
-      tail > 0 && ts >= 2
-          ? static_cast<double>(tiles1) / static_cast<double>(sms) * num_k + 40.0
-          : static_cast<double>((tiles1 + sms - 1) / sms) * num_k;
-  return pair_cost < one_cost;
+  return 0.9 * wave_cost(tiles2, clusters, num_k) < wave_cost(tiles1, sm_count(), num_k);
 }
 
 bool use_pair(int64_t M, int64_t N, int64_t K) {
@@ -712,11 +760,13 @@ bool use_pair(int64_t M, int64_t N, int64_t K) {
 
 template <int EPI>
 dlo_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int K,
-                       const EpiArgs& ea, int* err, cudaStream_t stream) {
+                       int tail, int tail_splits, const EpiArgs& ea, int* err,
+                       cudaStream_t stream) {
   set_all_attrs();
   DLO_CUDA(g_attr_err);
   const int tiles = ((M + BM2 - 1) / BM2) * ((N + BN - 1) / BN);
-  const int clusters = tiles < g_pair_clusters ? tiles : g_pair_clusters;
+  const int units = tiles - tail + tail * tail_splits;
+  const int clusters = units < g_pair_clusters ? units : g_pair_clusters;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(2 * clusters);
   cfg.blockDim = dim3(NUM_THREADS);
@@ -729,10 +779,11 @@ dlo_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, int M, int 
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  DLO_CUDA(cudaLaunchKernelEx(&cfg, gemm_pair_kernel<EPI>, ma, mb, M, N, K,
+  DLO_CUDA(cudaLaunchKernelEx(&cfg, gemm_pair_kernel<EPI>, ma, mb, M, N, K, tail, tail_splits,
                               group_rows_pair(M, K), ea, err));
   return DLO_OK;
 }
+
 
 template <int EPI>
 dlo_status launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int K,
@@ -823,15 +874,16 @@ splitk_reduce_kernel(const float* __restrict__ ws, int splits, int64_t M, int64_
   }
 }
 
-// The same for the tail tiles only: ws [tail, tail_splits, BM, BN], tail
+// The same for the tail tiles only: ws [tail, tail_splits, TM, BN], tail
 // tile tt being output tile num_tiles - tail + tt (tile t at row block
-// and column block from tile_coords).
-template <int EPI>
+// and column block from tile_coords); TM = BM for the one-CTA kernel's
+// tiles, BM2 for the pair kernel's.
+template <int EPI, int TM>
 __global__ void __launch_bounds__(256)
 tail_reduce_kernel(const float* __restrict__ ws, int tail, int tail_splits, int num_tiles,
                    int num_m, int num_n, int group_m, int64_t M, int64_t N,
                    const EpiArgs ea) {
-  constexpr int64_t per_tile = static_cast<int64_t>(BM) * (BN / 4);
+  constexpr int64_t per_tile = static_cast<int64_t>(TM) * (BN / 4);
   const int64_t total = tail * per_tile;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -841,28 +893,29 @@ tail_reduce_kernel(const float* __restrict__ ws, int tail, int tail_splits, int 
     const int tile = num_tiles - tail + tt;
     int m_idx, n_idx;
     tile_coords(tile, num_m, num_n, group_m, m_idx, n_idx);
-    const int64_t row = static_cast<int64_t>(m_idx) * BM + r;
+    const int64_t row = static_cast<int64_t>(m_idx) * TM + r;
     const int64_t col = static_cast<int64_t>(n_idx) * BN + c;
     if (row >= M || col >= N) continue;
-    const float* p = ws + (static_cast<int64_t>(tt) * tail_splits * BM + r) * BN + c;
+    const float* p = ws + (static_cast<int64_t>(tt) * tail_splits * TM + r) * BN + c;
     float4 acc = *reinterpret_cast<const float4*>(p);
-    for (int s = 1; s < tail_splits; ++s) add4(acc, p + static_cast<int64_t>(s) * BM * BN);
+    for (int s = 1; s < tail_splits; ++s) add4(acc, p + static_cast<int64_t>(s) * TM * BN);
     finish4<EPI>(acc, row, col, N, ea);
   }
 }
 
-template <int EPI>
+template <int EPI, int TM = BM>
 dlo_status launch_tail_reduce(const float* ws, int tail, int tail_splits, int64_t M, int64_t N,
                               int64_t K, const EpiArgs& ea, cudaStream_t stream) {
-  const int num_m = static_cast<int>((M + BM - 1) / BM);
+  const int num_m = static_cast<int>((M + TM - 1) / TM);
   const int num_n = static_cast<int>((N + BN - 1) / BN);
   const int num_tiles = num_m * num_n;
-  const int64_t total = static_cast<int64_t>(tail) * BM * (BN / 4);
+  const int64_t total = static_cast<int64_t>(tail) * TM * (BN / 4);
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   if (blocks > cap) blocks = cap;
-  tail_reduce_kernel<EPI><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      ws, tail, tail_splits, num_tiles, num_m, num_n, group_rows(M, K), M, N, ea);
+  const int group_m = TM == BM ? group_rows(M, K) : group_rows_pair(M, K);
+  tail_reduce_kernel<EPI, TM><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      ws, tail, tail_splits, num_tiles, num_m, num_n, group_m, M, N, ea);
   DLO_CUDA(cudaGetLastError());
   return DLO_OK;
 }
@@ -880,12 +933,31 @@ dlo_status launch_reduce(const float* ws, int splits, int64_t M, int64_t N, cons
   return DLO_OK;
 }
 
+// The pair kernel, then (a split tail) the ordered reduction of its tail
+// tiles' K slices with the epilogue.
+template <int EPI>
+dlo_status launch_pair_linear(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int K,
+                              int tail, int tail_splits, const EpiArgs& ea, int* err,
+                              cudaStream_t stream) {
+  DLO_TRY(launch_pair<EPI>(ma, mb, M, N, K, tail, tail_splits, ea, err, stream));
+  if (tail == 0) return DLO_OK;
+  return launch_tail_reduce<EPI, BM2>(ea.ws, tail, tail_splits, M, N, K, ea, stream);
+}
+
 }  // namespace
 
 LinearPlan linear_plan(int64_t M, int64_t N, int64_t K, int epilogue) {
   LinearPlan p{1, 0, 1, 0, 1, 0};
   if (epilogue != EPI_PARTIAL && use_pair(M, N, K)) {
     p.pair = 1;
+    const int64_t tiles2 = ((M + BM2 - 1) / BM2) * ((N + BN - 1) / BN);
+    const int64_t ts = tail_slices(tiles2, g_pair_clusters, (K + BK - 1) / BK);
+    if (ts > 1) {
+      p.tail = static_cast<int>(tiles2 % g_pair_clusters);
+      p.tail_splits = static_cast<int>(ts);
+      p.ws_bytes = static_cast<size_t>(p.tail) * ts * BM2 * BN * 4;
+      p.launches = 2;
+    }
     return p;
   }
   const int64_t sms = sm_count();
@@ -974,11 +1046,17 @@ dlo_status launch_linear_ex(const uint16_t* a, int64_t M, int64_t K, const uint1
   if (plan.pair) {
     DLO_TRY(make_tmap_2d(&ma, a, M, K, K, BM2 / 2, BK));
     DLO_TRY(make_tmap_2d(&mb, w, N, K, K, BN / 2, BK));
+    // the tail's K slices need the workspace; without it the tail runs whole
+    const bool split = plan.tail > 0 && ea.ws && ea.ws_bytes >= plan.ws_bytes &&
+                       !(reinterpret_cast<uintptr_t>(ea.ws) & 15u);
+    const int tl = split ? plan.tail : 0, ts = split ? plan.tail_splits : 1;
     switch (epilogue) {
-      case EPI_BF16: return launch_pair<EPI_BF16>(ma, mb, m, n, k, ea, err, stream);
-      case EPI_GELU_BF16: return launch_pair<EPI_GELU_BF16>(ma, mb, m, n, k, ea, err, stream);
-      case EPI_RESID_F32: return launch_pair<EPI_RESID_F32>(ma, mb, m, n, k, ea, err, stream);
-      case EPI_QKV: return launch_pair<EPI_QKV>(ma, mb, m, n, k, ea, err, stream);
+      case EPI_BF16: return launch_pair_linear<EPI_BF16>(ma, mb, m, n, k, tl, ts, ea, err, stream);
+      case EPI_GELU_BF16:
+        return launch_pair_linear<EPI_GELU_BF16>(ma, mb, m, n, k, tl, ts, ea, err, stream);
+      case EPI_RESID_F32:
+        return launch_pair_linear<EPI_RESID_F32>(ma, mb, m, n, k, tl, ts, ea, err, stream);
+      case EPI_QKV: return launch_pair_linear<EPI_QKV>(ma, mb, m, n, k, tl, ts, ea, err, stream);
       default: DLO_FAIL(DLO_ERR_INVALID, "linear: unknown epilogue %d", epilogue);
     }
   }

@@ -1,7 +1,8 @@
 """The CTA-pair GEMM kernel (one tcgen05 MMA over two SMs, 256 x 256 output
 tiles) against the oracle's linear: every epilogue with and without a bias,
 ragged M, N and K (including pairs whose second CTA's half of A or of W lies
-wholly past the edge), more tiles than CTA pairs; then whole block forwards
+wholly past the edge), more tiles than CTA pairs, a short last wave split in
+K over the idle pairs; then whole block forwards
 with every linear on CTA pairs (the QKV epilogue's transposed V included),
 streamed equal to resident and both against the oracle's block."""
 import numpy as np
@@ -71,6 +72,54 @@ def test_linear_pair(M, K, N, epi, bias):
         torch.cuda.synchronize()
         assert dlo.kernel_status() == 0
         got = out.float().cpu().numpy()
+        if epi == dlo.EPI_GELU_BF16:
+            ref = np.vectorize(oracle.gelu_tanh)(ref)
+        tol = 2.0 ** -8 * np.abs(ref) + 1e-5 * np.sqrt(K) * np.abs(ref).max()
+        assert np.all(np.abs(got - ref) <= tol), np.abs(got - ref).max()
+
+
+@pytest.mark.parametrize("epi", [dlo.EPI_BF16, dlo.EPI_GELU_BF16, dlo.EPI_RESID_F32])
+@pytest.mark.parametrize("shape", ["column", "grid"])
+def test_linear_pair_tail_split(epi, shape):
+    # a short last wave of pairs: its tiles run as K slices on the idle pairs
+    # (fp32 partials of 256 x 256 blocks), summed in slice order by the tail
+    # reduction; "grid": 3 column blocks, the tail's last tile being the
+    # ragged last row block of the ragged last column block.  Checked on the
+    # rows of the last 6 row blocks (every tail tile) and a sample of the others.
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    K = 2048
+    if shape == "column":
+        M, N = 256 * (pairs + 5) - 37, 256
+    else:
+        t = next(t for t in range(1, pairs) if (pairs + t) % 3 == 0)
+        M, N = 256 * ((pairs + t) // 3) - 50, 760
+    nws = dlo.op_linear_workspace_bytes(M, N, K, epi)
+    assert nws > 0 and nws % (256 * 256 * 4) == 0
+    g = torch.Generator().manual_seed(M + N + epi)
+    a = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    w = (0.05 * torch.randn(N, K, generator=g)).to(torch.bfloat16)
+    ws = torch.full((nws // 4,), float("nan"), device="cuda")
+    rng = np.random.default_rng(M)
+    sel = np.unique(np.concatenate([np.arange(max(0, M - 6 * 256), M), rng.integers(0, M, 256)]))
+    ref = oracle.linear(a[sel].float().numpy(), w.float().numpy())
+    if epi == dlo.EPI_RESID_F32:
+        x = torch.randn(M, N, generator=g)
+        gate = 0.1 * torch.randn(N, generator=g)
+        xd = x.cuda()
+        dlo.op_linear(a.cuda(), M, K, w.cuda(), N, epi, xd, gate.cuda(), None, ws, nws)
+        torch.cuda.synchronize()
+        assert dlo.kernel_status() == 0
+        got = xd.cpu().numpy()[sel]
+        exp = x.numpy()[sel].astype(np.float64) + gate.numpy().astype(np.float64) * ref
+        assert np.abs(got - exp).max() <= 1e-4 * max(1.0, np.abs(exp).max())
+    else:
+        out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        dlo.op_linear(a.cuda(), M, K, w.cuda(), N, epi, out, None, None, ws, nws)
+        torch.cuda.synchronize()
+        assert dlo.kernel_status() == 0
+        full = out.float().cpu().numpy()
+        assert not np.isnan(full).any()
+        got = full[sel]
         if epi == dlo.EPI_GELU_BF16:
             ref = np.vectorize(oracle.gelu_tanh)(ref)
         tol = 2.0 ** -8 * np.abs(ref) + 1e-5 * np.sqrt(K) * np.abs(ref).max()
