@@ -589,7 +589,9 @@ def run_ours(args, ws, rank, local):
                      "frac": achieved / ceiling if achieved else None, "traffic": None,
                      "peak_source": "pinned cudaMemcpyAsync 1 GiB ceiling measured in this run",
                      "bytes_per_launch": bytes_per_block},
-        "roofline_compute": {"name": "gemm_tcgen05_kernel (fc1, GELU epilogue)",
+        "roofline_compute": {"name": ("gemm_pair_kernel" if dlo.op_linear_on_pairs(
+                                 M, N, K, dlo.EPI_GELU_BF16) else "gemm_tcgen05_kernel")
+                             + " (fc1, GELU epilogue)",
                              "bound": "tensor", "achieved": lin_tflops, "peak": bf16_peak,
                              "unit": "TFLOP/s", "frac": lin_tflops / bf16_peak,
                              "traffic": None, "peak_source": peak_src + " burst bf16",

@@ -393,6 +393,10 @@ dlo_status dlo_op_qk_norm_rope(uint16_t* qkv, int64_t batch, int64_t tokens,
  * dlo_forward_scratch_bytes) and dlo_forward_launches follow the mode.
  * DLO_ERR_INVALID for another mode. */
 dlo_status dlo_set_gemm_pair_mode(int32_t mode);
+/* 1 if dlo_op_linear (and the block forward) runs a linear of this shape on
+ * CTA pairs under the current mode on this GPU, else 0 (also for empty or
+ * negative extents). */
+int32_t dlo_op_linear_on_pairs(int64_t M, int64_t N, int64_t K, int32_t epilogue);
 
 /* ------------------------------------------------------------------------
  * Engine: two slots, the hook schedule, events ([B1] "Double-Buffer Memory

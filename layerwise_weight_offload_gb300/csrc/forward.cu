@@ -326,6 +326,11 @@ dlo_status dlo_op_linear(const uint16_t* a, int64_t M, int64_t K, const uint16_t
 
 dlo_status dlo_set_gemm_pair_mode(int32_t mode) { return dlo::set_gemm_pair_mode(mode); }
 
+int32_t dlo_op_linear_on_pairs(int64_t M, int64_t N, int64_t K, int32_t epilogue) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  return dlo::linear_plan(M, N, K, epilogue).pair;
+}
+
 dlo_status dlo_op_qk_norm_rope(uint16_t* qkv, int64_t batch, int64_t tokens, int64_t d,
                                int64_t heads, const float* gq, const float* gk, float eps,
                                float rope_base, void* stream) {

@@ -103,6 +103,7 @@ _SIGS = {
     "dlo_op_qk_norm_rope": (c_i32, [c_vp, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp, c_f32, c_f32,
                                     c_vp]),
     "dlo_set_gemm_pair_mode": (c_i32, [c_i32]),
+    "dlo_op_linear_on_pairs": (c_i32, [c_i64, c_i64, c_i64, c_i32]),
     "dlo_op_attention_scratch_bytes": (c_sz, [c_i64, c_i64, c_i64]),
     "dlo_op_attention": (c_i32, [c_vp, c_i64, c_i64, c_i64, c_i64, c_vp, c_vp, c_sz, c_vp]),
     "dlo_engine_create": (c_i32, [_P(EngineDesc), _P(c_vp)]),
@@ -326,6 +327,11 @@ def set_gemm_pair_mode(mode):
     """Which GEMM kernel runs the linears: GEMM_PAIR_AUTO (by shape),
     GEMM_PAIR_OFF (single CTAs) or GEMM_PAIR_ON (CTA pairs for all)."""
     _check(lib().dlo_set_gemm_pair_mode(int(mode)), "dlo_set_gemm_pair_mode")
+
+
+def op_linear_on_pairs(M, N, K, epilogue):
+    """True if a linear of this shape runs on CTA pairs (gemm_pair_kernel)."""
+    return bool(lib().dlo_op_linear_on_pairs(M, N, K, int(epilogue)))
 
 
 def op_qk_norm_rope(qkv, batch, tokens, d, heads, gq=None, gk=None, eps=1e-6, rope_base=0.0,

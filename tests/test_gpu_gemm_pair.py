@@ -126,6 +126,17 @@ def test_linear_pair_tail_split(epi, shape):
         assert np.all(np.abs(got - ref) <= tol), np.abs(got - ref).max()
 
 
+def test_auto_policy_on_the_workload_shapes():
+    # by shape: pairs for every linear of the Super and Nano blocks, none at
+    # the odd workload's sizes (fewer pair tiles than pairs)
+    dlo.set_gemm_pair_mode(dlo.GEMM_PAIR_AUTO)
+    for T, d, f, want in [(8192, 6144, 24576, True), (4096, 3840, 15360, True),
+                          (1024, 1024, 4096, False)]:
+        for N, K, epi in [(3 * d, d, dlo.EPI_BF16), (d, d, dlo.EPI_RESID_F32),
+                          (f, d, dlo.EPI_GELU_BF16), (d, f, dlo.EPI_RESID_F32)]:
+            assert dlo.op_linear_on_pairs(T, N, K, epi) == want, (T, N, K)
+
+
 def test_mode_switch_changes_the_plan():
     # a shape that splits in K on single CTAs runs unsplit on pairs
     M, K, N = 77, 4096, 1024
