@@ -716,13 +716,6 @@ void set_all_attrs() {
 // kernel for every linear it can run (tests and measurements).
 int g_pair_mode = -1;
 
-// The pair kernel runs 256 x 256 tiles in waves of CTA pairs, the one-CTA
-// kernel 128 x 256 tiles in waves of SMs; both spread a short last wave over
-// the idle workers as K slices, at the cost of a reduction launch.  Both are
-// estimated by wave_cost in k-block steps of one wave, the pair kernel's
-// steps at 0.9 of the one-CTA kernel's (measured on GB300: 1.86 vs 1.71
-// PFLOP/s on Super's fc1).  Grids with fewer pair tiles than pairs keep the
-// one-CTA kernel and its K splits of every tile.
 // K slices for the tiles of a short last wave of `slots` workers (at least
 // 4 k-blocks a slice, at most 8 slices); 1: no split.
 int64_t tail_slices(int64_t tiles, int64_t slots, int64_t num_k) {
@@ -743,6 +736,13 @@ double wave_cost(int64_t tiles, int64_t slots, int64_t num_k) {
   return static_cast<double>((tiles + slots - 1) / slots) * num_k;
 }
 
+// The pair kernel runs 256 x 256 tiles in waves of CTA pairs, the one-CTA
+// kernel 128 x 256 tiles in waves of SMs; both spread a short last wave over
+// the idle workers as K slices, at the cost of a reduction launch.  Both are
+// estimated by wave_cost in k-block steps of one wave, the pair kernel's
+// steps at 0.9 of the one-CTA kernel's (measured on GB300: 1.86 vs 1.71
+// PFLOP/s on Super's fc1).  Grids with fewer pair tiles than pairs keep the
+// one-CTA kernel and its K splits of every tile.
 bool pair_auto(int64_t M, int64_t N, int64_t K, int clusters) {
   const int64_t tiles2 = ((M + BM2 - 1) / BM2) * ((N + BN - 1) / BN);
   const int64_t num_k = (K + BK - 1) / BK;
