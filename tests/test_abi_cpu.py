@@ -221,3 +221,24 @@ def test_forward_launch_count():
         n = dlo.forward_launches(dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp))
         assert 7 <= n <= 12
     assert dlo.forward_launches(dlo.dit_cfg(1, 16, 96, 1, 256)) == 0       # invalid config
+
+
+def test_gemm_pair_mode_and_query():
+    # the mode takes -1, 0 or 1 and refuses anything else (no GPU needed);
+    # the query answers 0 for empty or negative extents, and with no GPU the
+    # pair kernel is never available, whatever the mode
+    for mode in (dlo.GEMM_PAIR_OFF, dlo.GEMM_PAIR_ON, dlo.GEMM_PAIR_AUTO):
+        dlo.set_gemm_pair_mode(mode)
+    with pytest.raises(dlo.DLOError):
+        dlo.set_gemm_pair_mode(2)
+    with pytest.raises(dlo.DLOError):
+        dlo.set_gemm_pair_mode(-2)
+    assert not dlo.op_linear_on_pairs(0, 256, 256, dlo.EPI_BF16)
+    assert not dlo.op_linear_on_pairs(256, -1, 256, dlo.EPI_BF16)
+    import torch
+    if not torch.cuda.is_available():
+        dlo.set_gemm_pair_mode(dlo.GEMM_PAIR_ON)
+        try:
+            assert not dlo.op_linear_on_pairs(8192, 24576, 6144, dlo.EPI_GELU_BF16)
+        finally:
+            dlo.set_gemm_pair_mode(dlo.GEMM_PAIR_AUTO)
