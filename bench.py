@@ -7,10 +7,12 @@ i+1 overlapping block i's forward) and the block forward run on them.
 Prints one JSON line:
   value       streamed block forwards per second (whole job, all ranks),
               inputs (pinned host shards, x on the device) in place before
-              the timed region;
+              the timed region, the engine as it runs in use;
   e2e         the same, with x copied from pinned host memory and the result
               read back every step inside the timed region;
-  h2d_gbs     bytes moved host->device / copy-stream busy time;
+  h2d_gbs     bytes moved host->device / copy-stream busy time, from a
+              second pass of the same steps with an event pair around every
+              prefetch (the copy statistics come from that pass);
   exposed_transfer_ms_per_step  streamed minus all-resident step time;
   roofline    the dominant operation (the host->device copy) against the
               measured pinned cudaMemcpyAsync ceiling of this box;
@@ -361,23 +363,32 @@ def run_ours(args, ws, rank, local):
         t0 = time.perf_counter()
         host.pretouch()
         pretouch_s = time.perf_counter() - t0
-    if args.source != "shards":
-        from layerwise_weight_offload_gb300.stack import SourceStack
-        st = SourceStack(host, transport=args.source, timing=True)
-    else:
-        st = StreamedStack(host, copy_mode=mode, copy_ctas=args.copy_ctas, timing=True,
-                           two_copy_streams=args.two_copy_streams)
+
+    def make_stack(timing):
+        if args.source != "shards":
+            from layerwise_weight_offload_gb300.stack import SourceStack
+            return SourceStack(host, transport=args.source, timing=timing)
+        return StreamedStack(host, copy_mode=mode, copy_ctas=args.copy_ctas, timing=timing,
+                             two_copy_streams=args.two_copy_streams)
+
     x0 = W.gen_x(w, args.seed, device="cuda")
     x = x0.clone()
     cur = torch.cuda.current_stream()
 
-    def run_steps(n):
-        st.compute.wait_stream(cur)
+    def run_steps(stack, n):
+        stack.compute.wait_stream(cur)
         for _ in range(n):
-            st.step(x)
-        cur.wait_stream(st.compute)
+            stack.step(x)
+        cur.wait_stream(stack.compute)
 
-    run_steps(args.warmup)
+    # Two passes of the same length.  The first measures the stream as it
+    # runs in use (no per-copy timing events: a timing event recorded between
+    # two block copies on the copy queue costs the link ~3% of a 25 MB copy);
+    # it gives `value`, the step time and the clocks.  The second records an
+    # event pair around every prefetch for the copy statistics (H2D GB/s,
+    # busy time, overlap, the copy-time distribution).
+    st = make_stack(False)
+    run_steps(st, args.warmup)
     torch.cuda.synchronize()
     if args.steps is None:
         # enough timed steps for about 1.5 s of device time (at least 20), so
@@ -391,7 +402,6 @@ def run_ours(args, ws, rank, local):
         est = e0.elapsed_time(e1)
         args.steps = int(max_over_ranks(max(20, min(5000, math.ceil(1500.0 / max(est, 1e-3)))),
                                         ws))
-    n_copies_before = len(st.engine.copy_times()[0])
     stats0 = st.engine.query()
     barrier(ws)
     torch.cuda.synchronize()
@@ -408,20 +418,7 @@ def run_ours(args, ws, rank, local):
     barrier(ws)
     ms = max_over_ranks(ev0.elapsed_time(ev1), ws)
     stats1 = st.engine.query()
-    copy_ms, copy_bytes = st.engine.copy_times()
-    copy_ms, copy_bytes = copy_ms[n_copies_before:], copy_bytes[n_copies_before:]
-    # the prefetches enqueued by the timed forwards (the last one prefetches
-    # block 0 of the next step); the setup and warm-up ones are excluded
     n_fwd = w.n_blocks * args.steps
-    copy_ms, copy_bytes = copy_ms[:n_fwd], copy_bytes[:n_fwd]
-    spans = st.engine.copy_spans()[n_copies_before:][:n_fwd]
-    # prefetches into the two slots run on two copy streams and may overlap:
-    # the copy engines' busy time is the union of the intervals
-    busy_ms = union_ms(spans)
-    h2d = sum(copy_bytes) / (busy_ms * 1e6) if busy_ms > 0 else None
-    qs = sorted(copy_ms)
-    copy_dist = {"min": qs[0], "median": qs[len(qs) // 2], "max": qs[-1],
-                 "first": copy_ms[:3], "last": copy_ms[-3:]} if qs else None
     value = ws * n_fwd / (ms / 1e3)
     ms_step = ms / args.steps
     chosen = dlo.COPY_MODE_NAMES[stats1.chosen_mode]
@@ -429,6 +426,36 @@ def run_ours(args, ws, rank, local):
     # plus the copy-kernel launches of the prefetches the timed forwards issued
     gpu_launches = (n_fwd * dlo.forward_launches(st.cfg) +
                     stats1.n_copy_kernel_launches - stats0.n_copy_kernel_launches)
+
+    # second pass: the same steps with every prefetch timed
+    stt = make_stack(True)
+    x.copy_(x0)
+    run_steps(stt, args.warmup)
+    torch.cuda.synchronize()
+    n_copies_before = len(stt.engine.copy_times()[0])
+    t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0e.record(stt.compute)
+    for _ in range(args.steps):
+        stt.step(x)
+    t1e.record(stt.compute)
+    torch.cuda.synchronize()
+    ms_timed_step = t0e.elapsed_time(t1e) / args.steps
+    stats_t = stt.engine.query()
+    copy_ms, copy_bytes = stt.engine.copy_times()
+    copy_ms, copy_bytes = copy_ms[n_copies_before:], copy_bytes[n_copies_before:]
+    # the prefetches enqueued by the timed forwards (the last one prefetches
+    # block 0 of the next step); the setup and warm-up ones are excluded
+    copy_ms, copy_bytes = copy_ms[:n_fwd], copy_bytes[:n_fwd]
+    spans = stt.engine.copy_spans()[n_copies_before:][:n_fwd]
+    # prefetches into the two slots run on two copy streams and may overlap:
+    # the copy engines' busy time is the union of the intervals
+    busy_ms = union_ms(spans)
+    h2d = sum(copy_bytes) / (busy_ms * 1e6) if busy_ms > 0 else None
+    qs = sorted(copy_ms)
+    copy_dist = {"min": qs[0], "median": qs[len(qs) // 2], "max": qs[-1],
+                 "first": copy_ms[:3], "last": copy_ms[-3:]} if qs else None
+    chosen_t = dlo.COPY_MODE_NAMES[stats_t.chosen_mode]
+    stt.close()
 
     # all-resident reference run: same kernels, no transfer
     rs = ResidentStack(host)
@@ -573,6 +600,12 @@ def run_ours(args, ws, rank, local):
                            "t_link_ms": t_link * 1e3, "t_compute_ms": t_comp * 1e3,
                            "bound": "h2d" if t_link >= t_comp else "tensor"},
         "auto_race_us_per_forward": {"dma": stats1.race_dma_us, "kernel": stats1.race_kernel_us},
+        "copy_stats_pass": {
+            "ms_per_step": ms_timed_step, "chosen_copy_mode": chosen_t,
+            "note": "h2d_gbs, copy_busy_ms_per_step, overlap_fraction, copy_ms_distribution "
+                    "and roofline come from this second pass of the same steps, with an event "
+                    "pair recorded around every prefetch; value, ms_per_step and clocks come "
+                    "from the first pass, without them"},
         "copy_ms_distribution": copy_dist, "pretouch_s": pretouch_s,
         "host_huge_page_fraction": host.buf.huge_fraction(),
         "host_huge_ranges_used_fraction": host.buf.good_fraction(),
@@ -763,23 +796,31 @@ def run_sweep(args):
             for T in [int(v) for v in args.sweep_t.split(",")]:
                 w = W.CONFIGS["sweep-d%d-t%d-s%d" % (d, T, s)]
                 host.w = w
-                st = StreamedStack(host, copy_mode=dlo.COPY_AUTO, timing=True)
                 x = W.gen_x(w, args.seed, device="cuda")
                 cur = torch.cuda.current_stream()
                 steps = 3 if T < 16384 else 2
                 warm = 3
-                st.compute.wait_stream(cur)
-                for _ in range(warm):
-                    st.step(x)
-                torch.cuda.synchronize()
-                n_before = len(st.engine.copy_times()[0])
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(st.compute)
-                for _ in range(steps):
-                    st.step(x)
-                e1.record(st.compute)
-                torch.cuda.synchronize()
-                ms = e0.elapsed_time(e1) / steps
+
+                def timed_pass(timing):
+                    # the step time without per-copy timing events (as the
+                    # stream runs in use); with them, the copy statistics
+                    stk = StreamedStack(host, copy_mode=dlo.COPY_AUTO, timing=timing)
+                    stk.compute.wait_stream(cur)
+                    for _ in range(warm):
+                        stk.step(x)
+                    torch.cuda.synchronize()
+                    nb = len(stk.engine.copy_times()[0]) if timing else 0
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stk.compute)
+                    for _ in range(steps):
+                        stk.step(x)
+                    b.record(stk.compute)
+                    torch.cuda.synchronize()
+                    return stk, nb, a.elapsed_time(b) / steps
+
+                st, _, ms = timed_pass(False)
+                st.close()
+                st, n_before, _ = timed_pass(True)
                 cms, cby = st.engine.copy_times()
                 cms = cms[n_before:n_before + w.n_blocks * steps]
                 cby = cby[n_before:n_before + w.n_blocks * steps]
