@@ -1,6 +1,7 @@
 """Pins of the CPU oracle to facts that do not come from the oracle itself:
 numbers the pages print, closed forms, invariants, special cases that reduce
 to a textbook result, and library routines on small shapes.  No GPU."""
+import ctypes
 import itertools
 import math
 import os
@@ -359,6 +360,92 @@ def test_block_mlp_branch_closed_form():
     assert np.allclose(y, expect, atol=1e-13)
 
 
+def _np_rmsnorm_mod(x, g, shift, scale, eps=1e-6):
+    """RMSNorm with adaLN modulation written out in numpy."""
+    x = np.asarray(x, dtype=np.float64)
+    inv = 1.0 / np.sqrt((x * x).mean(axis=1, keepdims=True) + eps)
+    f = lambda a: np.asarray(a, dtype=np.float64)
+    return x * inv * f(g) * (1.0 + f(scale)) + f(shift)
+
+
+def _np_gelu_tanh(z):
+    return 0.5 * z * (1.0 + np.tanh(math.sqrt(2.0 / math.pi) * (z + 0.044715 * z ** 3)))
+
+
+def _both_branch_weights(rng, p, d, f):
+    """Wq = Wk = 0 (uniform attention), Wv, Wo, W1's first d rows and W2's
+    first d columns permutations, every other weight zero."""
+    pv, po, p1, p2 = (rng.permutation(d) for _ in range(4))
+    w = np.zeros((3 * d, d), np.float32)
+    w[2 * d:] = _perm_matrix(pv)
+    w1 = np.zeros((f, d), np.float32)
+    w1[:d] = _perm_matrix(p1)
+    w2 = np.zeros((d, f), np.float32)
+    w2[:, :d] = _perm_matrix(p2)
+    p["attn.qkv.weight"], p["attn.out.weight"] = w, _perm_matrix(po)
+    p["mlp.fc1.weight"], p["mlp.fc2.weight"] = w1, w2
+    return pv, po, p1, p2
+
+
+def test_block_both_branches_closed_form_mlp_reads_the_updated_residual():
+    # Both branches on at once.  Attention is uniform per batch item (q = k =
+    # 0), so o is the item's mean of v = h[:, pv]; the MLP's RMSNorm must read
+    # the residual AFTER the attention update, x1 = x + gate1 * o Wo^T.  The
+    # expected value is written out in numpy; a block whose MLP normalised
+    # the block input (parallel branches) differs from it by far more than
+    # the tolerance, which the second assertion checks.
+    rng = np.random.default_rng(30)
+    d, f, t, heads, batch = 8, 32, 5, 2, 2
+    p = _params(rng, d, f)
+    p["ada1.gate"] = (0.5 + rng.random(d)).astype(np.float32)
+    p["ada2.gate"] = (0.5 + rng.random(d)).astype(np.float32)
+    pv, po, p1, p2 = _both_branch_weights(rng, p, d, f)
+    x = (2 * rng.standard_normal((batch * t, d))).astype(np.float32)
+    y = oracle.block_forward(x, p, batch, t, d, heads, f)
+    xd = x.astype(np.float64)
+    h = _np_rmsnorm_mod(xd, p["norm1.weight"], p["ada1.shift"], p["ada1.scale"])
+    v = h[:, pv]
+    o = np.concatenate([np.tile(v[i * t:(i + 1) * t].mean(axis=0), (t, 1))
+                        for i in range(batch)])
+    x1 = xd + p["ada1.gate"].astype(np.float64) * o[:, po]
+    h2 = _np_rmsnorm_mod(x1, p["norm2.weight"], p["ada2.shift"], p["ada2.scale"])
+    expect = x1 + p["ada2.gate"].astype(np.float64) * _np_gelu_tanh(h2[:, p1])[:, p2]
+    assert np.allclose(y, expect, atol=1e-12, rtol=0)
+    h2_par = _np_rmsnorm_mod(xd, p["norm2.weight"], p["ada2.shift"], p["ada2.scale"])
+    parallel = x1 + p["ada2.gate"].astype(np.float64) * _np_gelu_tanh(h2_par[:, p1])[:, p2]
+    assert np.abs(parallel - expect).max() > 1e-3
+
+
+def test_full_block_both_branches_closed_form_with_biases():
+    # The checkpoint-shaped block with both branches on: q = k = 0 (zero
+    # weights and zero q/k biases, so the q/k norm and RoPE leave zeros and
+    # attention is uniform), v = h[:, pv] + bv, out = o Wo^T + bo, and the
+    # MLP with its biases on the updated residual x1; written out in numpy.
+    rng = np.random.default_rng(31)
+    d, f, t, heads = 8, 32, 6, 2
+    p = _params(rng, d, f)
+    p.update(_extras(rng, d, f, d // heads))
+    p["attn.qkv.bias"][:2 * d] = 0
+    p["ada1.gate"] = (0.5 + rng.random(d)).astype(np.float32)
+    p["ada2.gate"] = (0.5 + rng.random(d)).astype(np.float32)
+    pv, po, p1, p2 = _both_branch_weights(rng, p, d, f)
+    x = (2 * rng.standard_normal((t, d))).astype(np.float32)
+    y = oracle.block_forward(x, p, 1, t, d, heads, f, rope_base=10000.0)
+    b = {k: p[k].astype(np.float64) for k in
+         ("attn.qkv.bias", "attn.out.bias", "mlp.fc1.bias", "mlp.fc2.bias")}
+    xd = x.astype(np.float64)
+    h = _np_rmsnorm_mod(xd, p["norm1.weight"], p["ada1.shift"], p["ada1.scale"])
+    v = h[:, pv] + b["attn.qkv.bias"][2 * d:]
+    o = np.tile(v.mean(axis=0), (t, 1))
+    x1 = xd + p["ada1.gate"].astype(np.float64) * (o[:, po] + b["attn.out.bias"])
+    h2 = _np_rmsnorm_mod(x1, p["norm2.weight"], p["ada2.shift"], p["ada2.scale"])
+    u = np.zeros((t, f))
+    u[:, :d] = h2[:, p1]
+    u = _np_gelu_tanh(u + b["mlp.fc1.bias"])
+    expect = x1 + p["ada2.gate"].astype(np.float64) * (u[:, :d][:, p2] + b["mlp.fc2.bias"])
+    assert np.allclose(y, expect, atol=1e-12, rtol=0)
+
+
 def test_block_token_permutation_equivariance_and_batch():
     rng = np.random.default_rng(11)
     d, f, t = 16, 64, 7
@@ -584,5 +671,10 @@ def test_full_block_without_extras_equals_plain_block():
     d, f, t = 16, 64, 5
     p = _params(rng, d, f)
     x = rng.standard_normal((t, d)).astype(np.float32)
-    assert np.array_equal(oracle.block_forward(x, p, 1, t, d, 4, f),
-                          oracle.block_forward(x, p, 1, t, d, 4, f, rope_base=0.0))
+    # the extended entry point itself, every extra absent (null pointers)
+    arrs = [np.ascontiguousarray(p[n], dtype=np.float32) for n in oracle.PARAM_ORDER]
+    ptrs = (ctypes.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
+    out = np.zeros((t, d), dtype=np.float64)
+    oracle.lib().oracle_block_forward_ex(x.ctypes.data, 1, t, d, 4, f, 1e-6, ptrs, None, None,
+                                         None, None, None, None, 0.0, out.ctypes.data, 2)
+    assert np.array_equal(out, oracle.block_forward(x, p, 1, t, d, 4, f))
