@@ -483,6 +483,13 @@ typedef struct {
                              ends (each still waits for its slot's free
                              event).  Measured on GB300 with one H2D link: no
                              gain, the copy engines run them one at a time */
+  int32_t log_capacity;   /* entries kept by the schedule log (one per
+                             forward) and by the timing record (one per
+                             prefetch, timing = 1): the newest ones; once full
+                             each new entry overwrites the oldest, which is
+                             counted as dropped, so a serving loop of any
+                             length holds constant memory.  0 = 65536;
+                             at most 2^24 */
 } dlo_engine_desc;
 
 typedef struct {
@@ -539,7 +546,11 @@ dlo_status dlo_register_block_source(dlo_engine* e, int32_t block, const dlo_pla
 dlo_status dlo_prefetch(dlo_engine* e, int32_t block, int32_t slot);
 
 /* Makes the compute stream wait for the ready event of the slot holding
- * `block` (non-blocking on the host).  DLO_ERR_STATE if no slot holds it. */
+ * `block` (non-blocking on the host).  During that block's forward this is
+ * the slot its hook picked; otherwise the slot filled with it last (with a
+ * one-block pass both slots hold the block, and the newer copy is the one
+ * the next forward reads).  The same slot resolves dlo_wait_host and
+ * dlo_param_view.  DLO_ERR_STATE if no slot holds it. */
 dlo_status dlo_wait(dlo_engine* e, int32_t block);
 
 /* Host-side poll of the same event, bounded by timeout_ms; DLO_ERR_TIMEOUT
@@ -571,7 +582,10 @@ dlo_status dlo_post_forward(dlo_engine* e, int32_t block);
 dlo_status dlo_block_forward(dlo_engine* e, int32_t block, const dlo_dit_cfg* cfg,
                              float* x, void* scratch, size_t scratch_bytes);
 
-/* Copies up to `cap` entries of the schedule log (one per forward). */
+/* Copies the newest min(cap, kept) entries of the schedule log (one per
+ * forward, oldest first) to buf; *n_out = the number of entries kept (at
+ * most desc.log_capacity; older ones are counted in
+ * dlo_engine_stats.log_dropped).  cap = 0 with a null buf queries *n_out. */
 dlo_status dlo_schedule_log(const dlo_engine* e, dlo_sched_event* buf,
                             int32_t cap, int32_t* n_out);
 
@@ -586,7 +600,9 @@ dlo_status dlo_schedule_log(const dlo_engine* e, dlo_sched_event* buf,
  * the prefetches issued in windows 1 and 3 use DMA, in windows 2 and 4 the
  * copy kernel; race_dma_us / race_kernel_us are each mode's better
  * window's mean interval between consecutive free events (0 until
- * measured). */
+ * measured; -1 if the events could not be timed, in which case DMA is
+ * chosen).  The timing record keeps the newest desc.log_capacity prefetches:
+ * copy_times and copy_spans report those, oldest first. */
 typedef struct {
   int32_t chosen_mode;
   int32_t n_forwards;
@@ -601,13 +617,15 @@ typedef struct {
   int32_t n_copy_kernel_launches; /* copy-kernel launches of all prefetches:
                                   KERNEL prefetches, DMA prefetches' small
                                   groups, STAGED gathers */
+  int64_t log_dropped;         /* schedule-log entries overwritten (full ring) */
+  int64_t timed_dropped;       /* timing entries overwritten (full ring) */
 } dlo_engine_stats;
 dlo_status dlo_engine_query(dlo_engine* e, dlo_engine_stats* out);
 dlo_status dlo_engine_copy_times(dlo_engine* e, float* copy_ms, int64_t* copy_bytes,
                                  int32_t cap, int32_t* n_out);
-/* With timing = 1: each prefetch's start and end (ms) on one clock, counted
- * from the first timed prefetch's start, for the first `cap` prefetches;
- * *n_out = how many were timed.  Prefetches into the two slots may overlap
+/* With timing = 1: each kept prefetch's start and end (ms) on one clock,
+ * counted from the oldest kept prefetch's start, for the first `cap` of
+ * them; *n_out = how many are kept.  Prefetches into the two slots may overlap
  * (two copy streams), so the copy engines' busy time is the union of these
  * intervals, not the sum of copy_times.  Blocks until the spans' end events
  * have completed. */
@@ -625,6 +643,24 @@ dlo_status dlo_engine_destroy(dlo_engine* e, int32_t timeout_ms);
  * kernel returns early.  Reads and clears the word (synchronises the
  * device).  *code = 0 means no wait ran out. */
 dlo_status dlo_kernel_status(int32_t* code);
+
+/* Fail-closed check of the kernels' bounded device waits (the pages' "fail
+ * closed" rule: [B1] "Fail-Closed Design"; [B2] "Validation Results", a
+ * partial wave that times out fails closed).  Launches one small library
+ * kernel (one CTA, synchronously, on the legacy default stream) whose
+ * thread waits, with the wait routine every kernel of the library uses
+ * (spin = 1: the spinning form of MMA issuers, 0: the suspending form),
+ * on an mbarrier phase that no thread completes, with limit_ns in place of
+ * the kernels' 4 s; if abort_ns > 0 a second warp raises the CTA's abort
+ * flag after abort_ns instead, the path by which one role of a kernel stops
+ * the others.  The wait gives up, the kernel records its code in the
+ * device error word and returns; the context stays usable.
+ * *elapsed_ns: how long the wait ran (device clock); *code: the recorded
+ * code (7 = timed out, 6 = aborted), which is also cleared from the word.
+ * Returns DLO_ERR_TIMEOUT when the wait gave up (the expected outcome),
+ * DLO_ERR_INVALID for limits outside 0..2 s.  Allocates nothing. */
+dlo_status dlo_debug_wait_probe(int32_t spin, int64_t limit_ns, int64_t abort_ns,
+                                int64_t* elapsed_ns, int32_t* code);
 
 /* Message of the last failed call on this thread ("" if none). */
 const char* dlo_last_error(void);

@@ -52,13 +52,6 @@ constexpr uint32_t ATT_TMEM_COLS = 512;
 // 2^64, far from the fp32 and bf16 range limits (without loss of relative
 // precision), and O needs no rescaling in the common case.
 constexpr float kGrowLimit = 64.f;
-// Of every 8 score pairs, this many take 2^x from the polynomial on the FMA
-// pipes and the rest from the MUFU: the MUFU alone (16 per clock per SM)
-// would take about as long as the tensor products of a tile.
-#ifndef ATT_POLY_PAIRS
-#define ATT_POLY_PAIRS 0
-#endif
-constexpr int kPolyPairs = ATT_POLY_PAIRS;
 
 template <int HD>
 struct AttLayout {
@@ -112,38 +105,10 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
 __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   uint64_t r;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
-}
-
-// 2^x for a pair on the FMA pipes instead of the MUFU: x = n + f with
-// n = round(x) (adding and removing 1.5 * 2^23 leaves round(x) in the low
-// mantissa bits), 2^f from a cubic in f on [-1/2, 1/2] whose coefficients
-// minimise the largest relative error (7.5e-5 in fp32 evaluation, well under
-// the bf16 half-ulp of P; exp2_poly.py beside this file derives them), and n
-// added to the exponent field.  x is first clamped to >= -126 so that the
-// exponent field cannot wrap below zero (the result for anything smaller is
-// at most 2^-126, a stand-in for 0 next to the row's maximum of 1); callers
-// keep x <= 64.
-__device__ __forceinline__ uint64_t exp2_poly_pair(uint64_t x) {
-  x = f2(fmaxf(f2_lo(x), -126.f), fmaxf(f2_hi(x), -126.f));
-  const uint64_t magic = 0x4B4000004B400000ull;      // 1.5 * 2^23, both lanes
-  const uint64_t t = f2_add(x, magic);
-  const uint64_t f = f2_sub(x, f2_sub(t, magic));
-  uint64_t p = f2_fma(f2(5.517166853e-02f, 5.517166853e-02f), f,
-                      f2(2.426111251e-01f, 2.426111251e-01f));
-  p = f2_fma(p, f, f2(6.932609677e-01f, 6.932609677e-01f));
-  p = f2_fma(p, f, f2(9.999280572e-01f, 9.999280572e-01f));
-  const uint32_t lo = static_cast<uint32_t>(p) + (static_cast<uint32_t>(t) << 23);
-  const uint32_t hi = static_cast<uint32_t>(p >> 32) + (static_cast<uint32_t>(t >> 32) << 23);
-  return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
 // Maximum of the first n (clamped to 0..32) of 32 fp32 scores; -inf if none.
@@ -488,11 +453,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
         for (int h = 0; h < 16; ++h) {
           const uint64_t x = f2_fma(f2(__uint_as_float(sr[2 * h]), __uint_as_float(sr[2 * h + 1])),
                                     sc2, nm2);
-          uint64_t pp;
-          if ((h & 7) < kPolyPairs)
-            pp = exp2_poly_pair(x);
-          else
-            pp = f2(ex2_approx(f2_lo(x)), ex2_approx(f2_hi(x)));
+          const uint64_t pp = f2(ex2_approx(f2_lo(x)), ex2_approx(f2_hi(x)));
           ls[h & 3] = f2_add(ls[h & 3], pp);
           pk[h] = pack_bf16(f2_lo(pp), f2_hi(pp));
         }

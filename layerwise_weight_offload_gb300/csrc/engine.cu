@@ -107,6 +107,38 @@ class PackPool {
   bool stop_ = false;
 };
 
+// Fixed-capacity ring: grows to `cap` entries, then each push overwrites
+// the oldest one (counted in `dropped`).  at(0) is the oldest entry kept.
+template <class T>
+class Ring {
+ public:
+  void set_capacity(size_t cap) { cap_ = cap; }
+  // The entry to fill next; *reused = true when it is an evicted old entry
+  // (its fields still hold that entry's values).
+  T& push(bool* reused) {
+    if (buf_.size() < cap_) {
+      buf_.emplace_back();
+      *reused = false;
+      return buf_.back();
+    }
+    T& t = buf_[head_];
+    head_ = (head_ + 1) % cap_;
+    ++dropped_;
+    *reused = true;
+    return t;
+  }
+  size_t size() const { return buf_.size(); }
+  const T& at(size_t i) const { return buf_.size() < cap_ ? buf_[i] : buf_[(head_ + i) % cap_]; }
+  int64_t dropped() const { return dropped_; }
+  // every stored entry, in storage order (for releasing resources)
+  const std::vector<T>& storage() const { return buf_; }
+
+ private:
+  std::vector<T> buf_;
+  size_t cap_ = 0, head_ = 0;
+  int64_t dropped_ = 0;
+};
+
 }  // namespace dlo
 
 struct dlo_engine {
@@ -159,8 +191,11 @@ struct dlo_engine {
   int64_t k = 0;                     // next global forward index
   bool in_forward = false;
   int32_t cur_block = -1, cur_slot = -1;
-  std::vector<dlo_sched_event> log;
-  std::vector<Timed> timed;          // with timing = 1: every prefetch
+  int64_t fill_seq[2] = {-1, -1};    // prefetch count when each slot was last filled
+  // the newest entries only: one per forward, and (timing = 1) one per
+  // prefetch; a full ring overwrites its oldest entry and counts it dropped
+  dlo::Ring<dlo_sched_event> log;
+  dlo::Ring<Timed> timed;
   // DMA fan-out (library-owned streams forked from / joined to `copy`)
   int32_t fan = 1;
   cudaStream_t aux[kMaxFan] = {};
@@ -214,6 +249,7 @@ namespace {
 // so that one-time costs (module loading, first launches, the first
 // device access to each pinned host page) stay out of every window.
 constexpr int64_t kRaceWindow = 6;
+constexpr int32_t kDefaultLogCapacity = 65536;
 constexpr int kRaceWindows = 4;
 inline int64_t race_start(int32_t n_blocks) { return static_cast<int64_t>(n_blocks) + 2; }
 
@@ -309,7 +345,6 @@ dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, in
   }
   struct Piece { uint8_t* dst; const void* src; int64_t bytes; };
   std::vector<Piece> pieces;
-  bool joined = false;
   for (size_t g = 0; g < p->groups.size(); ++g) {
     const auto& grp = p->groups[g];
     if (by_kernel[g]) continue;
@@ -340,7 +375,6 @@ dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, in
       }
     return DLO_OK;
   };
-  (void)joined;
   if (pieces.empty()) return join_side();
   const int used = static_cast<int>(std::min<size_t>(fan, pieces.size()));
   if (used <= 1) {
@@ -432,7 +466,14 @@ void try_decide(dlo_engine* e) {
   double best[2] = {1e30, 1e30};   // [0] DMA, [1] kernel
   for (int w = 0; w < kRaceWindows; ++w) {
     float ms = 0;
-    cudaEventElapsedTime(&ms, e->race_ev[2 * w], e->race_ev[2 * w + 1]);
+    if (cudaEventElapsedTime(&ms, e->race_ev[2 * w], e->race_ev[2 * w + 1]) != cudaSuccess) {
+      // no measurement: no choice can rest on it, so DMA (which takes no
+      // SM time from the forward) is kept; -1 marks the race unmeasured
+      cudaGetLastError();
+      e->race_dma_us = e->race_kernel_us = -1.0;
+      e->chosen = DLO_COPY_DMA;
+      return;
+    }
     const double us = 1e3 * ms / (kRaceWindow - 1);
     best[w & 1] = std::min(best[w & 1], us);
   }
@@ -458,13 +499,30 @@ int32_t mode_for(dlo_engine* e, int64_t k, const dlo_engine::Block& b) {
   return DLO_COPY_DMA;
 }
 
-dlo_status make_timed(dlo_engine::Timed* t) {
-  DLO_CUDA(cudaEventCreate(&t->a));
-  if (cudaEventCreate(&t->b) != cudaSuccess) {
-    cudaEventDestroy(t->a);
-    DLO_FAIL(DLO_ERR_CUDA, "cudaEventCreate failed");
+// The timing entry of the prefetch about to be enqueued: a new entry with
+// two new events, or (ring full) the oldest entry, whose events are
+// recorded again.
+dlo_status timed_entry(dlo_engine* e, int64_t bytes, int32_t mode, dlo_engine::Timed** out) {
+  bool reused = false;
+  dlo_engine::Timed& t = e->timed.push(&reused);
+  if (!reused) {
+    t.a = t.b = nullptr;
+    if (cudaEventCreate(&t.a) != cudaSuccess || cudaEventCreate(&t.b) != cudaSuccess) {
+      cudaGetLastError();
+      DLO_FAIL(DLO_ERR_CUDA, "cudaEventCreate failed");
+    }
   }
+  t.bytes = bytes;
+  t.mode = mode;
+  *out = &t;
   return DLO_OK;
+}
+
+// Bookkeeping of a prefetch just enqueued into `slot`.
+void mark_filled(dlo_engine* e, int32_t slot, int32_t block) {
+  e->slot_holds[slot] = block;
+  e->fill_seq[slot] = e->n_prefetches;
+  e->n_prefetches++;
 }
 
 // Host-side bounded wait for an event (polls; false after timeout_ms).
@@ -490,16 +548,11 @@ constexpr int kHostStagingWaitMs = 60000;
 dlo_status prefetch_source(dlo_engine* e, int32_t block, int32_t slot) {
   const dlo_engine::Block& b = e->blocks[block];
   cudaStream_t cs = e->slot_copy[slot];
-  dlo_engine::Timed t{};
-  if (e->timing) {
-    DLO_TRY(make_timed(&t));
-    t.bytes = b.bytes;
-    t.mode = DLO_COPY_DMA;
-    e->timed.push_back(t);
-  }
+  dlo_engine::Timed* t = nullptr;
+  if (e->timing) DLO_TRY(timed_entry(e, b.bytes, DLO_COPY_DMA, &t));
   if (b.direct) {
     DLO_CUDA(cudaStreamWaitEvent(cs, e->freed[slot], 0));
-    if (e->timing) DLO_CUDA(cudaEventRecord(t.a, cs));
+    if (t) DLO_CUDA(cudaEventRecord(t->a, cs));
     for (const auto& s : b.src)
       DLO_CUDA(cudaMemcpyAsync(e->slot[slot] + s.off, s.p, static_cast<size_t>(s.bytes),
                                cudaMemcpyHostToDevice, cs));
@@ -518,7 +571,7 @@ dlo_status prefetch_source(dlo_engine* e, int32_t block, int32_t slot) {
     e->pack_ms += std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0)
                       .count();
     DLO_CUDA(cudaStreamWaitEvent(cs, e->freed[slot], 0));
-    if (e->timing) DLO_CUDA(cudaEventRecord(t.a, cs));
+    if (t) DLO_CUDA(cudaEventRecord(t->a, cs));
     DLO_CUDA(cudaMemcpyAsync(e->slot[slot], e->host_staging[slot],
                              static_cast<size_t>(b.plan->slot_bytes), cudaMemcpyHostToDevice,
                              cs));
@@ -526,10 +579,9 @@ dlo_status prefetch_source(dlo_engine* e, int32_t block, int32_t slot) {
     e->hs_pending[slot] = true;
     e->n_packed++;
   }
-  if (e->timing) DLO_CUDA(cudaEventRecord(t.b, cs));
+  if (t) DLO_CUDA(cudaEventRecord(t->b, cs));
   DLO_CUDA(cudaEventRecord(e->ready[slot], cs));
-  e->slot_holds[slot] = block;
-  e->n_prefetches++;
+  mark_filled(e, slot, block);
   return DLO_OK;
 }
 
@@ -548,16 +600,13 @@ dlo_status enqueue_prefetch(dlo_engine* e, int32_t block, int32_t slot, int64_t 
     // H2D into staging[slot] once the gather that last read it is done;
     // the gather then waits for the H2D and for the slot's free event
     DLO_CUDA(cudaStreamWaitEvent(cs, e->stage_free[slot], 0));
-    dlo_engine::Timed t{};
+    dlo_engine::Timed* t = nullptr;
     if (e->timing) {
-      DLO_TRY(make_timed(&t));
-      t.bytes = b.bytes;
-      t.mode = mode;
-      e->timed.push_back(t);
-      DLO_CUDA(cudaEventRecord(t.a, cs));
+      DLO_TRY(timed_entry(e, b.bytes, mode, &t));
+      DLO_CUDA(cudaEventRecord(t->a, cs));
     }
     DLO_TRY(stage_h2d(b, e->staging[slot], cs));
-    if (e->timing) DLO_CUDA(cudaEventRecord(t.b, cs));
+    if (t) DLO_CUDA(cudaEventRecord(t->b, cs));
     DLO_CUDA(cudaEventRecord(e->staged[slot], cs));
     DLO_CUDA(cudaStreamWaitEvent(e->gather, e->staged[slot], 0));
     DLO_CUDA(cudaStreamWaitEvent(e->gather, e->freed[slot], 0));
@@ -565,25 +614,20 @@ dlo_status enqueue_prefetch(dlo_engine* e, int32_t block, int32_t slot, int64_t 
     e->n_copy_launches++;
     DLO_CUDA(cudaEventRecord(e->stage_free[slot], e->gather));
     DLO_CUDA(cudaEventRecord(e->ready[slot], e->gather));
-    e->slot_holds[slot] = block;
-    e->n_prefetches++;
+    mark_filled(e, slot, block);
     return DLO_OK;
   }
   DLO_CUDA(cudaStreamWaitEvent(cs, e->freed[slot], 0));
-  dlo_engine::Timed t{};
+  dlo_engine::Timed* t = nullptr;
   if (e->timing) {
-    DLO_TRY(make_timed(&t));
-    t.bytes = b.bytes;
-    t.mode = mode;
-    e->timed.push_back(t);
-    DLO_CUDA(cudaEventRecord(t.a, cs));
+    DLO_TRY(timed_entry(e, b.bytes, mode, &t));
+    DLO_CUDA(cudaEventRecord(t->a, cs));
   }
   DLO_TRY(copy_block(b, e->slot[slot], mode, e->copy_ctas, cs, e->fan, e->aux, e->fork_ev,
                      e->join_ev, e->side, e->side_fork, e->side_join, &e->n_copy_launches));
-  if (e->timing) DLO_CUDA(cudaEventRecord(t.b, cs));
+  if (t) DLO_CUDA(cudaEventRecord(t->b, cs));
   DLO_CUDA(cudaEventRecord(e->ready[slot], cs));
-  e->slot_holds[slot] = block;
-  e->n_prefetches++;
+  mark_filled(e, slot, block);
   if (mode == DLO_COPY_KERNEL) e->n_kernel_prefetches++;
   return DLO_OK;
 }
@@ -593,9 +637,16 @@ dlo_status check_engine(const dlo_engine* e) {
   return DLO_OK;
 }
 
+// The slot whose copy of `block` a forward reads: during that block's
+// forward, the slot the hook picked; otherwise the slot filled with it last
+// (both slots hold the same block when the pass has one block: the newer
+// copy is the one the next forward reads).
 int32_t slot_of(const dlo_engine* e, int32_t block) {
-  if (e->slot_holds[0] == block) return 0;
-  if (e->slot_holds[1] == block) return 1;
+  if (e->in_forward && block == e->cur_block) return e->cur_slot;
+  const bool h0 = e->slot_holds[0] == block, h1 = e->slot_holds[1] == block;
+  if (h0 && h1) return e->fill_seq[1] > e->fill_seq[0] ? 1 : 0;
+  if (h0) return 0;
+  if (h1) return 1;
   return -1;
 }
 
@@ -609,9 +660,9 @@ void release(dlo_engine* e) {
   }
   delete e->pool;
   if (e->own_copy) cudaStreamDestroy(e->own_copy);
-  for (auto& t : e->timed) {
-    cudaEventDestroy(t.a);
-    cudaEventDestroy(t.b);
+  for (const auto& t : e->timed.storage()) {
+    if (t.a) cudaEventDestroy(t.a);
+    if (t.b) cudaEventDestroy(t.b);
   }
   for (int i = 0; i < 8; ++i)
     if (e->race_ev[i]) cudaEventDestroy(e->race_ev[i]);
@@ -663,6 +714,8 @@ dlo_status dlo_engine_create(const dlo_engine_desc* d, dlo_engine** out) {
     if (d->pack_threads < 0 || d->pack_threads > 64)
       DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: pack_threads must be 0..64");
   }
+  if (d->log_capacity < 0 || d->log_capacity > (1 << 24))
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: log_capacity must be 0..%d", 1 << 24);
   if (d->dma_streams < 0 || d->dma_streams > dlo_engine::kMaxFan)
     DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_create: dma_streams must be 0..%d",
              dlo_engine::kMaxFan);
@@ -690,6 +743,10 @@ dlo_status dlo_engine_create(const dlo_engine_desc* d, dlo_engine** out) {
   e->copy_ctas = d->copy_ctas;
   e->timing = d->timing != 0;
   e->fan = d->dma_streams == 0 ? 1 : d->dma_streams;
+  const size_t log_cap = d->log_capacity > 0 ? static_cast<size_t>(d->log_capacity)
+                                             : static_cast<size_t>(kDefaultLogCapacity);
+  e->log.set_capacity(log_cap);
+  e->timed.set_capacity(log_cap);
   if (d->copy_mode == DLO_COPY_STAGED) {
     e->staging[0] = static_cast<uint8_t*>(d->staging[0]);
     e->staging[1] = static_cast<uint8_t*>(d->staging[1]);
@@ -921,7 +978,8 @@ dlo_status dlo_pre_forward(dlo_engine* e, int32_t block, int32_t* slot_out) {
   ev.prefetch_slot = ps;
   ev.waits_on_free_of_k = waits;
   ev.copy_mode = used_mode;
-  e->log.push_back(ev);
+  bool reused = false;
+  e->log.push(&reused) = ev;
   e->in_forward = true;
   e->cur_block = block;
   e->cur_slot = slot;
@@ -972,7 +1030,8 @@ dlo_status dlo_schedule_log(const dlo_engine* e, dlo_sched_event* buf, int32_t c
   if (!n_out || (cap > 0 && !buf)) DLO_FAIL(DLO_ERR_INVALID, "dlo_schedule_log: null argument");
   const int32_t n = static_cast<int32_t>(e->log.size());
   const int32_t m = n < cap ? n : cap;
-  for (int32_t i = 0; i < m; ++i) buf[i] = e->log[i];
+  // the newest m entries, oldest first
+  for (int32_t i = 0; i < m; ++i) buf[i] = e->log.at(static_cast<size_t>(n - m + i));
   *n_out = n;
   return DLO_OK;
 }
@@ -992,6 +1051,8 @@ dlo_status dlo_engine_query(dlo_engine* e, dlo_engine_stats* out) {
   out->n_packed_prefetches = static_cast<int32_t>(e->n_packed);
   out->pack_ms = e->pack_ms;
   out->n_copy_kernel_launches = static_cast<int32_t>(e->n_copy_launches);
+  out->log_dropped = e->log.dropped();
+  out->timed_dropped = e->timed.dropped();
   return DLO_OK;
 }
 
@@ -1001,16 +1062,14 @@ dlo_status dlo_engine_copy_times(dlo_engine* e, float* copy_ms, int64_t* copy_by
   DLO_TRY(check_engine(e));
   if (!n_out || (cap > 0 && (!copy_ms || !copy_bytes)))
     DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_copy_times: null argument");
-  int32_t n = 0;
-  for (const auto& t : e->timed) {
-    if (n < cap) {
-      DLO_CUDA(cudaEventSynchronize(t.b));
-      float ms = 0;
-      DLO_CUDA(cudaEventElapsedTime(&ms, t.a, t.b));
-      copy_ms[n] = ms;
-      copy_bytes[n] = t.bytes;
-    }
-    ++n;
+  const int32_t n = static_cast<int32_t>(e->timed.size());
+  for (int32_t i = 0; i < n && i < cap; ++i) {
+    const dlo_engine::Timed& t = e->timed.at(static_cast<size_t>(i));
+    DLO_CUDA(cudaEventSynchronize(t.b));
+    float ms = 0;
+    DLO_CUDA(cudaEventElapsedTime(&ms, t.a, t.b));
+    copy_ms[i] = ms;
+    copy_bytes[i] = t.bytes;
   }
   *n_out = n;
   return DLO_OK;
@@ -1022,17 +1081,16 @@ dlo_status dlo_engine_copy_spans(dlo_engine* e, float* start_ms, float* end_ms, 
   DLO_TRY(check_engine(e));
   if (!n_out || (cap > 0 && (!start_ms || !end_ms)))
     DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_copy_spans: null argument");
-  int32_t n = 0;
-  for (const auto& t : e->timed) {
-    if (n < cap) {
-      DLO_CUDA(cudaEventSynchronize(t.b));
-      float a = 0, b = 0;
-      DLO_CUDA(cudaEventElapsedTime(&a, e->timed.front().a, t.a));
-      DLO_CUDA(cudaEventElapsedTime(&b, e->timed.front().a, t.b));
-      start_ms[n] = a;
-      end_ms[n] = b;
-    }
-    ++n;
+  const int32_t n = static_cast<int32_t>(e->timed.size());
+  for (int32_t i = 0; i < n && i < cap; ++i) {
+    const dlo_engine::Timed& t = e->timed.at(static_cast<size_t>(i));
+    const cudaEvent_t origin = e->timed.at(0).a;
+    DLO_CUDA(cudaEventSynchronize(t.b));
+    float a = 0, b = 0;
+    DLO_CUDA(cudaEventElapsedTime(&a, origin, t.a));
+    DLO_CUDA(cudaEventElapsedTime(&b, origin, t.b));
+    start_ms[i] = a;
+    end_ms[i] = b;
   }
   *n_out = n;
   return DLO_OK;

@@ -19,7 +19,8 @@ enum DeviceError : int {
   DEV_TIMEOUT_MMA_EMPTY = 3,  // MMA issuer: accumulator never drained
   DEV_TIMEOUT_EPILOGUE = 4,   // epilogue: accumulator never completed
   DEV_TIMEOUT_ATTN = 5,       // attention: K/V tile never arrived
-  DEV_ABORTED = 6             // another role of the CTA gave up first
+  DEV_ABORTED = 6,            // another role of the CTA gave up first
+  DEV_TIMEOUT_PROBE = 7       // dlo_debug_wait_probe: its wait ran out (by design)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -98,17 +99,19 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
 }
 
 // Waits for the phase of `bar` with the given parity to complete.  Returns
-// false if *abort becomes non-zero or the wait exceeds kWaitTimeoutNs.  The
+// false if *abort becomes non-zero or the wait exceeds limit_ns (every
+// kernel uses kWaitTimeoutNs; a test probe passes a short one).  The
 // waiting thread sleeps in 20-microsecond slices (the hardware wakes it when
 // the phase completes), so a role that sets *abort is seen within one slice.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  volatile int* abort) {
+                                                  volatile int* abort,
+                                                  uint64_t limit_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -117,14 +120,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // waiting for its operands) does not pay the wake-up of a suspended wait.
 // Bounded the same way; *abort and the clock are read every 256 tests.
 __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity,
-                                               volatile int* abort) {
+                                               volatile int* abort,
+                                               uint64_t limit_ns = kWaitTimeoutNs) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_test(bar, parity)) return true;
     if ((n & 255u) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
     }
   }
 }

@@ -66,7 +66,8 @@ class EngineDesc(ctypes.Structure):
                 ("copy_ctas", c_i32), ("timing", c_i32), ("dma_streams", c_i32),
                 ("staging", c_vp * 2), ("staging_bytes", c_i64), ("gather_stream", c_vp),
                 ("host_staging", c_vp * 2), ("host_staging_bytes", c_i64),
-                ("pack_threads", c_i32), ("two_copy_streams", c_i32)]
+                ("pack_threads", c_i32), ("two_copy_streams", c_i32),
+                ("log_capacity", c_i32)]
 
 
 class SchedEvent(ctypes.Structure):
@@ -79,7 +80,8 @@ class EngineStats(ctypes.Structure):
                 ("n_kernel_prefetches", c_i32), ("race_dma_us", ctypes.c_double),
                 ("race_kernel_us", ctypes.c_double), ("n_direct_prefetches", c_i32),
                 ("n_packed_prefetches", c_i32), ("pack_ms", ctypes.c_double),
-                ("n_copy_kernel_launches", c_i32)]
+                ("n_copy_kernel_launches", c_i32), ("log_dropped", c_i64),
+                ("timed_dropped", c_i64)]
 
 
 _P = ctypes.POINTER
@@ -126,6 +128,7 @@ _SIGS = {
     "dlo_engine_copy_spans": (c_i32, [c_vp, _P(c_f32), _P(c_f32), c_i32, _P(c_i32)]),
     "dlo_engine_destroy": (c_i32, [c_vp, c_i32]),
     "dlo_kernel_status": (c_i32, [_P(c_i32)]),
+    "dlo_debug_wait_probe": (c_i32, [c_i32, c_i64, c_i64, _P(c_i64), _P(c_i32)]),
     "dlo_last_error": (ctypes.c_char_p, []),
     "dlo_version": (ctypes.c_char_p, []),
 }
@@ -387,13 +390,23 @@ def kernel_status():
     return v.value
 
 
+def debug_wait_probe(spin, limit_ns, abort_ns=0):
+    """Runs the library's bounded device wait against a phase nobody
+    completes; returns (status, elapsed_ns, code) without raising."""
+    el, code = c_i64(), c_i32()
+    st = lib().dlo_debug_wait_probe(1 if spin else 0, int(limit_ns), int(abort_ns),
+                                    ctypes.byref(el), ctypes.byref(code))
+    return st, el.value, code.value
+
+
 # ---- engine ------------------------------------------------------------------
 
 class Engine:
     def __init__(self, n_blocks, slot0, slot1, slot_bytes, compute_stream, copy_stream,
                  copy_mode=COPY_AUTO, copy_ctas=0, timing=False, dma_streams=0,
                  staging=None, staging_bytes=0, gather_stream=None, host_staging=None,
-                 host_staging_bytes=0, pack_threads=0, two_copy_streams=False):
+                 host_staging_bytes=0, pack_threads=0, two_copy_streams=False,
+                 log_capacity=0):
         """staging: two device buffers (and gather_stream) for COPY_STAGED;
         host_staging: two page-locked host buffers for rank-local source
         blocks whose parameters are pageable."""
@@ -419,6 +432,7 @@ class Engine:
         d.host_staging_bytes = int(host_staging_bytes)
         d.pack_threads = int(pack_threads)
         d.two_copy_streams = 1 if two_copy_streams else 0
+        d.log_capacity = int(log_capacity)
         h = c_vp()
         _check(lib().dlo_engine_create(ctypes.byref(d), ctypes.byref(h)), "dlo_engine_create")
         self.handle = h.value

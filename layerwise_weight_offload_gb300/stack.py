@@ -418,7 +418,7 @@ class StreamedStack:
     """Two slots and the hook schedule: the path the pages describe."""
 
     def __init__(self, host: HostBlocks, copy_mode=dlo.COPY_AUTO, copy_ctas=0, timing=False,
-                 device="cuda", two_copy_streams=False):
+                 device="cuda", two_copy_streams=False, log_capacity=0):
         w = host.w
         self.w, self.host, self.plan = w, host, host.plan
         self.slot_bytes = _round_up(self.plan.info().slot_bytes, 256)
@@ -437,7 +437,8 @@ class StreamedStack:
         self.engine = dlo.Engine(w.n_blocks, self.slots[0], self.slots[1], self.slot_bytes,
                                  self.compute, self.copy, copy_mode, copy_ctas, timing,
                                  staging=self.staging, staging_bytes=staging_bytes,
-                                 gather_stream=self.gather, two_copy_streams=two_copy_streams)
+                                 gather_stream=self.gather, two_copy_streams=two_copy_streams,
+                                 log_capacity=log_capacity)
         for i in range(w.n_blocks):
             self.engine.register_block(i, self.plan, host.shard_ptrs(i % w.distinct))
         self.cfg = dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
