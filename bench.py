@@ -7,7 +7,9 @@ i+1 overlapping block i's forward) and the block forward run on them.
 Prints one JSON line:
   value       streamed block forwards per second (whole job, all ranks),
               inputs (pinned host shards, x on the device) in place before
-              the timed region, the engine as it runs in use;
+              the timed region, the engine as it runs in use; the K timed
+              steps run as 5 regions (each bracketed by a device
+              synchronisation) and value is the median region's rate;
   e2e         the same, with x copied from pinned host memory and the result
               read back every step inside the timed region;
   h2d_gbs     bytes moved host->device / copy-stream busy time, from a
@@ -21,7 +23,8 @@ Prints one JSON line:
 
 --impl reference times the CPU oracle (the reference arm of this build):
 each step is one oracle block forward of the same workload on the host
-cores; under torchrun only rank 0 runs it.
+cores (for blocks above 1e11 FLOPs a bounded 1/H share of one, see
+oracle_sample); under torchrun only rank 0 runs it.
 """
 import argparse
 import json
@@ -38,7 +41,8 @@ if ROOT not in sys.path:
 
 METRIC = "streamed block-fwd/s; H2D GB/s vs roofline; exposed transfer ms/step (1×GB300)"
 UNIT = "block-fwd/s"
-DEFAULT_CONFIG = "odd"
+DEFAULT_CONFIG = "super"
+REGIONS = 5          # timed regions per pass; value is the median region
 
 
 def parse():
@@ -106,6 +110,40 @@ def union_ms(spans):
     if cur_e is not None:
         total += cur_e - cur_s
     return total
+
+
+def region_sizes(steps, regions=REGIONS):
+    """Splits `steps` timed steps into up to `regions` regions, as evenly as
+    possible (the earlier regions take the remainder)."""
+    n = max(1, min(regions, steps))
+    return [steps // n + (1 if i < steps % n else 0) for i in range(n)]
+
+
+def median_region(sizes, ms):
+    """Index of the median region by rate (steps per ms)."""
+    order = sorted(range(len(sizes)), key=lambda i: sizes[i] / ms[i])
+    return order[len(order) // 2]
+
+
+def timed_regions(step, stream, sizes, ws):
+    """Runs sum(sizes) steps as one timed region, bracketed by a barrier and
+    a device synchronisation on both sides, with a CUDA event on `stream`
+    (the stream the steps end on) after every sizes[i] steps, so that the
+    regions follow each other without a pause (the stream stays in its
+    steady state); returns each region's time in ms, the maximum over
+    ranks."""
+    import torch
+    barrier(ws)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(sizes) + 1)]
+    ev[0].record(stream)
+    for i, k in enumerate(sizes):
+        for _ in range(k):
+            step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    return [max_over_ranks(ev[i].elapsed_time(ev[i + 1]), ws) for i in range(len(sizes))]
 
 
 def max_over_ranks(v, ws):
@@ -207,24 +245,78 @@ def measured_peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
-def oracle_block_rate(w, seconds, seed=0):
-    """CPU oracle block forwards per second on a bounded sample: host block
-    0 of the workload, repeated until `seconds` have passed (at least once)."""
+FULL_ORACLE_FLOPS = 1e11   # blocks up to this run whole in the oracle samples
+
+
+def oracle_sample(w, seed=0, gen_device="cpu"):
+    """One bounded piece of the fp64 oracle's work on host block 0 of `w`:
+    returns (run, share, text), run() doing the piece once, share the
+    fraction of one block forward's FLOPs it is.
+
+    A block of at most FULL_ORACLE_FLOPS runs whole (oracle.block_forward,
+    share 1).  A larger one (Nano, Super, the T = 16384 sweep cells, where
+    one oracle forward takes minutes) is sampled as 1/H of a block, H the
+    head count: the oracle's QKV projection and attention for head 0 over
+    all T tokens of the first batch item (1/H of those FLOPs), then its
+    out-projection, gated residual, second norm, MLP (GELU included) and
+    gated residual on round(B*T/H) token rows (the out-projection's input
+    is head 0's attention output in its columns, zeros in the others).
+    The first norm runs over all T rows (a little more than 1/H of it);
+    share is the piece's exact dense-contraction FLOPs over the block's."""
     import numpy as np
     import oracle
     from layerwise_weight_offload_gb300 import workloads as W
-    p = {k: v.float().numpy() for k, v in W.gen_block(w, 0, seed).items()}
-    x = W.gen_x(w, seed).numpy()
+    p = {k: v.float().cpu().numpy() for k, v in W.gen_block(w, 0, seed, device=gen_device).items()}
+    x = W.gen_x(w, seed, device=gen_device).cpu().numpy()
     threads = oracle.default_threads()
+    rb = W.oracle_rope_base(w)
+    if w.flops_per_block() <= FULL_ORACLE_FLOPS:
+        def run():
+            oracle.block_forward(x, p, w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
+                                 threads=threads, rope_base=rb)
+        return run, 1.0, "one fp64 oracle block forward of host block 0 of %s" % w.name, threads
+    d, f, T, H = w.hidden, w.mlp, w.tokens, w.heads
+    hd = d // H
+    r = max(1, round(w.batch * T / H))
+    wqkv = p["attn.qkv.weight"]
+    w_head = np.ascontiguousarray(np.concatenate([wqkv[0:hd], wqkv[d:d + hd],
+                                                  wqkv[2 * d:2 * d + hd]]))
+    x0, xr = x[:T], x[:r]
+
+    def run():
+        h = oracle.rmsnorm_mod(x0, p["norm1.weight"], p["ada1.shift"], p["ada1.scale"], w.eps)
+        qkv_h = oracle.linear(h, w_head, threads)
+        o_h = oracle.attention(qkv_h, 1, T, hd, 1, threads)
+        o_r = np.zeros((r, d))
+        o_r[:, :hd] = o_h[np.arange(r) % T]
+        y = oracle.linear(o_r, p["attn.out.weight"], threads)
+        x1 = xr.astype(np.float64) + p["ada1.gate"].astype(np.float64) * y
+        h2 = oracle.rmsnorm_mod(x1, p["norm2.weight"], p["ada2.shift"], p["ada2.scale"], w.eps)
+        u = oracle.gelu_tanh_array(oracle.linear(h2, p["mlp.fc1.weight"], threads))
+        y2 = oracle.linear(u, p["mlp.fc2.weight"], threads)
+        return x1 + p["ada2.gate"].astype(np.float64) * y2
+
+    flops = 2 * T * d * 3 * hd + 4 * T * T * hd + 2 * r * (d * d + 2 * d * f)
+    text = ("1/%d of an fp64 oracle block forward of host block 0 of %s: QKV projection and "
+            "attention of head 0 over all %d tokens, out-projection, norms, MLP and residuals "
+            "on %d token rows (%.3g FLOPs of the block's %.3g)"
+            % (H, w.name, T, r, flops, w.flops_per_block()))
+    return run, flops / w.flops_per_block(), text, threads
+
+
+def oracle_block_rate(w, seconds, seed=0, gen_device="cpu"):
+    """CPU oracle block forwards per second on a bounded sample: the
+    oracle_sample piece of host block 0, repeated until `seconds` have
+    passed (at least once), counted as `share` block forwards each."""
+    run, share, text, threads = oracle_sample(w, seed, gen_device)
     n, t0 = 0, time.perf_counter()
     while True:
-        oracle.block_forward(x, p, w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
-                             threads=threads, rope_base=W.oracle_rope_base(w))
+        run()
         n += 1
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return n / el, n, el, threads
+    return n * share / el, n, el, threads, text
 
 
 def oracle_extras(w, seed=0, seconds=3.0):
@@ -264,48 +356,50 @@ def oracle_extras(w, seed=0, seconds=3.0):
 
 
 def run_reference(args, ws, rank):
-    """The oracle as the reference arm: K timed steps of one oracle block
-    forward each (after W untimed), on the host cores."""
+    """The oracle as the reference arm: K timed steps (after W untimed) of
+    one oracle_sample piece each on the host cores, counted as `share`
+    block forwards per step."""
     if rank != 0:
         return
-    import oracle
     from layerwise_weight_offload_gb300 import workloads as W
     w = W.CONFIGS[args.config]
-    p = {k: v.float().numpy() for k, v in W.gen_block(w, 0, args.seed).items()}
-    x = W.gen_x(w, args.seed).numpy()
-    threads = oracle.default_threads()
+    run, share, text, threads = oracle_sample(w, args.seed)
     if args.steps is None:
         args.steps = 20
-    rb = W.oracle_rope_base(w)
     for _ in range(args.warmup):
-        oracle.block_forward(x, p, w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
-                             threads=threads, rope_base=rb)
+        run()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.block_forward(x, p, w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
-                             threads=threads, rope_base=rb)
+        run()
     el = time.perf_counter() - t0
-    v = args.steps / el
-    sample = ("%d oracle block forwards (fp64, naive loops) of host block 0 of workload %s"
-              % (args.steps, args.config))
+    v = args.steps * share / el
+    sample = "%d steps, each %s" % (args.steps, text)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(w, args),
+            "data": DATA, "config": workload_config(w, args, ws),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def workload_config(w, args):
+DATA = ("synthetic: seeded torch.randn, bf16 linear weights ~N(0,0.02), f32 adaLN ~N(0,0.1), "
+        "norm gains 1, x ~N(0,1)")
+
+
+def workload_config(w, args, ws=1):
+    """The workload as both arms name it (the same dict in each)."""
+    mb = (w.bf16_numel() * 2 + w.f32_numel() * 4) * w.n_blocks / 1e6
     return {"workload": "%s: %d blocks/step (%d distinct host blocks), hidden %d, %d heads, "
                         "mlp %d, %d tokens, batch %d, %d shards per dtype group, %d denoising "
                         "steps in the workload" % (w.name, w.n_blocks, w.distinct, w.hidden,
                                                    w.heads, w.mlp, w.tokens, w.batch, w.shards,
                                                    w.steps),
             "name": w.name, "copy_mode": args.copy_mode, "host_source": args.source,
-            "gemm_pair": args.gemm_pair}
+            "gemm_pair": args.gemm_pair,
+            "l2": "streamed weights %.0f MB per step > 129 MB L2" % mb,
+            "parallelism": "replicas" if ws > 1 else "single GPU"}
 
 
 def h2d_ceiling_gbs(torch, nbytes=1 << 30, reps=10):
@@ -391,36 +485,32 @@ def run_ours(args, ws, rank, local):
     run_steps(st, args.warmup)
     torch.cuda.synchronize()
     if args.steps is None:
-        # enough timed steps for about 1.5 s of device time (at least 20), so
-        # that the clock samples cover the region; one more untimed step
-        # measures the step time
+        # enough timed steps for REGIONS regions of about 1.5 s of device
+        # time each (at least 20 steps), so that every region's clock
+        # samples and copies are many; one more untimed step measures the
+        # step time
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(st.compute)
         st.step(x)
         e1.record(st.compute)
         torch.cuda.synchronize()
         est = e0.elapsed_time(e1)
-        args.steps = int(max_over_ranks(max(20, min(5000, math.ceil(1500.0 / max(est, 1e-3)))),
-                                        ws))
+        args.steps = int(max_over_ranks(
+            max(20, min(50000, math.ceil(REGIONS * 1500.0 / max(est, 1e-3)))), ws))
+    sizes = region_sizes(args.steps)
     stats0 = st.engine.query()
-    barrier(ws)
-    torch.cuda.synchronize()
     clocks = ClockSampler(local)
     if not args.no_clocks:
         clocks.start()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(st.compute)
-    for _ in range(args.steps):
-        st.step(x)
-    ev1.record(st.compute)
-    torch.cuda.synchronize()
+    region_ms = timed_regions(lambda: st.step(x), st.compute, sizes, ws)
     clk = clocks.stop()
-    barrier(ws)
-    ms = max_over_ranks(ev0.elapsed_time(ev1), ws)
     stats1 = st.engine.query()
     n_fwd = w.n_blocks * args.steps
-    value = ws * n_fwd / (ms / 1e3)
-    ms_step = ms / args.steps
+    rates = [w.n_blocks * k / (ms / 1e3) for k, ms in zip(sizes, region_ms)]
+    med = median_region(sizes, region_ms)
+    value = ws * w.n_blocks * sizes[med] / (region_ms[med] / 1e3)
+    ms_step = region_ms[med] / sizes[med]
+    total_ms = sum(region_ms)
     chosen = dlo.COPY_MODE_NAMES[stats1.chosen_mode]
     # the library's own kernels in the timed region: every forward's launches
     # plus the copy-kernel launches of the prefetches the timed forwards issued
@@ -433,6 +523,7 @@ def run_ours(args, ws, rank, local):
     run_steps(stt, args.warmup)
     torch.cuda.synchronize()
     n_copies_before = len(stt.engine.copy_times()[0])
+    dropped_before = stt.engine.query().timed_dropped
     t0e, t1e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0e.record(stt.compute)
     for _ in range(args.steps):
@@ -442,44 +533,51 @@ def run_ours(args, ws, rank, local):
     ms_timed_step = t0e.elapsed_time(t1e) / args.steps
     stats_t = stt.engine.query()
     copy_ms, copy_bytes = stt.engine.copy_times()
-    copy_ms, copy_bytes = copy_ms[n_copies_before:], copy_bytes[n_copies_before:]
+    spans_all = stt.engine.copy_spans()
     # the prefetches enqueued by the timed forwards (the last one prefetches
-    # block 0 of the next step); the setup and warm-up ones are excluded
-    copy_ms, copy_bytes = copy_ms[:n_fwd], copy_bytes[:n_fwd]
-    spans = stt.engine.copy_spans()[n_copies_before:][:n_fwd]
+    # block 0 of the next step); the setup and warm-up ones are excluded.
+    # The timing record keeps the newest entries: shift by what it dropped.
+    first = n_copies_before - (stats_t.timed_dropped - dropped_before)
+    if first < 0:
+        raise RuntimeError("timing record too small for %d timed prefetches" % n_fwd)
+    copy_ms, copy_bytes = copy_ms[first:first + n_fwd], copy_bytes[first:first + n_fwd]
+    spans = spans_all[first:first + n_fwd]
     # prefetches into the two slots run on two copy streams and may overlap:
     # the copy engines' busy time is the union of the intervals
     busy_ms = union_ms(spans)
     h2d = sum(copy_bytes) / (busy_ms * 1e6) if busy_ms > 0 else None
     qs = sorted(copy_ms)
-    copy_dist = {"min": qs[0], "median": qs[len(qs) // 2], "max": qs[-1],
+    copy_dist = {"min": qs[0], "p50": qs[len(qs) // 2],
+                 "p99": qs[min(len(qs) - 1, int(math.ceil(0.99 * len(qs))) - 1)],
+                 "max": qs[-1], "n": len(qs),
+                 "slow_over_2x_p50": sum(1 for v in qs if v > 2 * qs[len(qs) // 2]),
                  "first": copy_ms[:3], "last": copy_ms[-3:]} if qs else None
     chosen_t = dlo.COPY_MODE_NAMES[stats_t.chosen_mode]
     stt.close()
 
-    # all-resident reference run: same kernels, no transfer
+    # all-resident reference run: same kernels, no transfer, the same regions
     rs = ResidentStack(host)
     xr = x0.clone()
     rs.stream.wait_stream(cur)
     for _ in range(args.warmup):
         rs.step(xr)
-    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    r0.record(rs.stream)
-    for _ in range(args.steps):
-        rs.step(xr)
-    r1.record(rs.stream)
-    torch.cuda.synchronize()
-    res_ms_step = r0.elapsed_time(r1) / args.steps
+    res_region_ms = timed_regions(lambda: rs.step(xr), rs.stream, sizes, ws)
+    rmed = median_region(sizes, res_region_ms)
+    res_ms_step = res_region_ms[rmed] / sizes[rmed]
     exposed = ms_step - res_ms_step
     copy_per_step = busy_ms / args.steps
     overlap = 1.0 - exposed / copy_per_step if copy_per_step > 0 else None
 
-    # block roofline: max(bytes / link ceiling, flops / bf16 peak)
+    # block roofline: max(bytes / link ceiling, flops / bf16 peak), the
+    # peak being the measured burst figure (the sustained one as a second
+    # field: the streamed step is a long run under the power cap)
     flops = w.flops_per_block()
     t_link = bytes_per_block / (ceiling * 1e9)
-    t_comp = flops / (bf16_sust * 1e12)
+    t_comp = flops / (bf16_peak * 1e12)
+    t_comp_sust = flops / (bf16_sust * 1e12)
     t_roof = max(t_link, t_comp)
     roof_frac = (w.n_blocks * t_roof * 1e3) / ms_step
+    roof_frac_sust = (w.n_blocks * max(t_link, t_comp_sust) * 1e3) / ms_step
 
     # largest linear alone (fc1: T x d -> f), event-timed on its stream
     M, K, N = w.batch * w.tokens, w.hidden, w.mlp
@@ -569,10 +667,11 @@ def run_ours(args, ws, rank, local):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        v, n, el, threads = oracle_block_rate(w, args.cpu_seconds, args.seed)
+        v, n, el, threads, text = oracle_block_rate(w, args.cpu_seconds, args.seed,
+                                                    gen_device="cuda")
         cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": "%d fp64 oracle block forward(s) of host block 0 of %s in %.1f s; "
-                         "the oracle's reassembly is not included" % (n, w.name, el),
+               "sample": "%d x (%s) in %.1f s; the oracle's reassembly is not included"
+                         % (n, text, el),
                **oracle_extras(w, args.seed)}
 
     copy_name = {"kernel": "copy_reassemble_kernel",
@@ -585,19 +684,29 @@ def run_ours(args, ws, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic: seeded torch.randn, bf16 linear weights ~N(0,0.02), f32 adaLN "
-                "~N(0,0.1), norm gains 1, x ~N(0,1)",
-        "config": dict(workload_config(w, args), chosen_copy_mode=chosen,
-                       l2="streamed weights %.0f MB per step > 129 MB L2"
-                          % (w.n_blocks * bytes_per_block / 1e6),
-                       parallelism="replicas" if ws > 1 else "single GPU"),
+        "data": DATA, "config": workload_config(w, args, ws), "chosen_copy_mode": chosen,
+        "timing": {"regions": len(sizes), "steps_per_region": sizes,
+                   "streamed_ms_per_region": region_ms,
+                   "streamed_block_fwd_per_s_per_region": [ws * r for r in rates],
+                   "streamed_ms_per_step_all_steps": total_ms / args.steps,
+                   "resident_ms_per_region": res_region_ms,
+                   "note": "the K timed steps run back to back as these regions (CUDA events "
+                           "between them, one synchronisation before and after); value, "
+                           "ms_per_step and resident_ms_per_step are the median region's"},
         "h2d_gbs": h2d, "h2d_ceiling_gbs": ceiling,
         "h2d_nominal_pcie5_x16_gbs": 63.0,
-        "exposed_transfer_ms_per_step": exposed, "resident_ms_per_step": res_ms_step,
+        "exposed_transfer_ms_per_step": exposed,
+        "exposed_transfer_fraction_of_step": exposed / ms_step,
+        "resident_ms_per_step": res_ms_step,
         "copy_busy_ms_per_step": copy_per_step, "overlap_fraction": overlap,
         "block_roofline_fraction": roof_frac,
+        "block_roofline_fraction_sustained_peak": roof_frac_sust,
         "block_roofline": {"bytes_per_block": bytes_per_block, "flops_per_block": flops,
                            "t_link_ms": t_link * 1e3, "t_compute_ms": t_comp * 1e3,
+                           "t_compute_sustained_ms": t_comp_sust * 1e3,
+                           "bf16_peak_tflops": bf16_peak, "bf16_sustained_tflops": bf16_sust,
+                           "peak_source": peak_src + " burst bf16 (the sustained figure for "
+                                          "block_roofline_fraction_sustained_peak)",
                            "bound": "h2d" if t_link >= t_comp else "tensor"},
         "auto_race_us_per_forward": {"dma": stats1.race_dma_us, "kernel": stats1.race_kernel_us},
         "copy_stats_pass": {
@@ -840,7 +949,9 @@ def run_sweep(args):
                 res = r0.elapsed_time(r1) / steps
                 del rs
                 bytes_block = sum(g.shard_bytes * s for g in host.plan.groups())
-                t_roof = max(bytes_block / (ceiling * 1e9), w.flops_per_block() / (bf16_sust * 1e12))
+                t_link = bytes_block / (ceiling * 1e9)
+                t_roof = max(t_link, w.flops_per_block() / (bf16_peak * 1e12))
+                t_roof_s = max(t_link, w.flops_per_block() / (bf16_sust * 1e12))
                 copy_step = busy / steps
                 exposed = ms - res
                 print(json.dumps({
@@ -852,7 +963,9 @@ def run_sweep(args):
                     "overlap_fraction": 1 - exposed / copy_step if copy_step > 0 else None,
                     "block_fwd_per_s": w.n_blocks / (ms / 1e3),
                     "block_roofline_fraction": w.n_blocks * t_roof * 1e3 / ms,
-                    "bound": "h2d" if bytes_block / (ceiling * 1e9) >= w.flops_per_block() / (bf16_sust * 1e12) else "tensor",
+                    "block_roofline_fraction_sustained_peak": w.n_blocks * t_roof_s * 1e3 / ms,
+                    "bound": "h2d" if t_link >= w.flops_per_block() / (bf16_peak * 1e12)
+                    else "tensor",
                     "copy_mode": chosen}), flush=True)
                 del x, xr
                 torch.cuda.empty_cache()

@@ -37,6 +37,8 @@ def lib():
         L.oracle_schedule.argtypes = [i32, i32, i32, vp]
         L.oracle_gelu_tanh.restype = dbl
         L.oracle_gelu_tanh.argtypes = [dbl]
+        L.oracle_gelu_tanh_array.restype = None
+        L.oracle_gelu_tanh_array.argtypes = [vp, i64, vp]
         L.oracle_rmsnorm_mod.restype = None
         L.oracle_rmsnorm_mod.argtypes = [vp, i64, i64, vp, vp, vp, dbl, vp]
         L.oracle_linear.restype = None
@@ -163,6 +165,14 @@ def schedule(n_blocks, n_steps, use_correction=True):
 
 def gelu_tanh(z):
     return float(lib().oracle_gelu_tanh(float(z)))
+
+
+def gelu_tanh_array(z):
+    """gelu_tanh applied element by element (float64 copy)."""
+    z = np.ascontiguousarray(z, dtype=np.float64)
+    out = np.empty_like(z)
+    lib().oracle_gelu_tanh_array(_ptr(z), z.size, _ptr(out))
+    return out
 
 
 def rmsnorm_mod(x, g, shift, scale, eps=1e-6):

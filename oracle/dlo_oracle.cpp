@@ -242,6 +242,12 @@ double oracle_gelu_tanh(double z) {
   return 0.5 * z * (1.0 + std::tanh(c * (z + 0.044715 * z * z * z)));
 }
 
+// out[e] = oracle_gelu_tanh(z[e]) for e < n (the block's MLP activation,
+// element by element).
+void oracle_gelu_tanh_array(const double* z, int64_t n, double* out) {
+  for (int64_t e = 0; e < n; ++e) out[e] = oracle_gelu_tanh(z[e]);
+}
+
 // h[t,:] = x[t,:] / sqrt(mean(x[t,:]^2) + eps) * g * (1 + scale) + shift
 void oracle_rmsnorm_mod(const double* x, int64_t rows, int64_t d,
                         const float* g, const float* shift, const float* scale,

@@ -41,3 +41,14 @@ def test_max_over_ranks_gloo_world_2():
         p.join(120)
         assert p.exitcode == 0
     assert out[0] == out[1] == 15.0
+
+
+def test_region_split_and_median():
+    import bench
+    assert bench.region_sizes(20) == [4, 4, 4, 4, 4]
+    assert bench.region_sizes(7) == [2, 2, 1, 1, 1]
+    assert bench.region_sizes(3) == [1, 1, 1]
+    assert sum(bench.region_sizes(1307)) == 1307
+    # rates 1, 4, 2, 5, 3 steps/ms: the median region is the one at 3
+    sizes, ms = [2, 4, 2, 5, 3], [2.0, 1.0, 1.0, 1.0, 1.0]
+    assert bench.median_region(sizes, ms) == 4

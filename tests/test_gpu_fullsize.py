@@ -1,12 +1,16 @@
-"""Full-size checks at the Nano workload's shapes (hidden 3840, 30 heads,
-MLP 15360, 4096 tokens, 4 shards), in the launch configuration bench.py
-times (two-slot engine, AUTO copy mode, CUDA-graph forwards):
+"""Full-size checks at the shapes of the Nano workload (hidden 3840, 30
+heads, MLP 15360, 4096 tokens, 4 shards), the Super workload (hidden 6144,
+48 heads, MLP 24576, 8192 tokens, 2 shards) and the longest-sequence sweep
+cell (hidden 1664, 13 heads, MLP 6656, 16384 tokens, 2 shards), in the
+launch configuration bench.py times (two-slot engine, AUTO copy mode,
+CUDA-graph forwards):
 - every prefetched slot equals the oracle's reassembled block, byte for byte;
 - the streamed output equals the all-resident output bit for bit;
 - sampled output rows match the oracle's block forward for those rows.
-Two distinct host blocks stand in for the 72 (the per-block work and the
-launch shapes are the workload's; only the number of distinct blocks is
-smaller, to keep host memory and run time small)."""
+Two distinct host blocks and three block forwards stand in for each
+workload's full count (the per-block work and the launch shapes are the
+workload's; only the number of blocks is smaller, to keep host memory and
+run time small)."""
 import numpy as np
 import pytest
 import torch
@@ -19,9 +23,14 @@ from layerwise_weight_offload_gb300.stack import HostBlocks, StreamedStack, Resi
 pytestmark = pytest.mark.gpu
 
 
-def test_nano_shapes_streamed_resident_and_sampled_oracle():
+@pytest.mark.parametrize("name,rows", [
+    ("nano", [0, 1, 777, 2048, 4095]),
+    ("super", [0, 1, 3333, 4096, 8191]),
+    ("sweep-d1664-t16384-s2", [0, 1, 5000, 12345, 16383]),
+])
+def test_full_shapes_streamed_resident_and_sampled_oracle(name, rows):
     build_lib()
-    base = W.CONFIGS["nano"]
+    base = W.CONFIGS[name]
     w = W.Workload(**{**base.__dict__, "n_blocks": 3, "distinct": 2, "steps": 2})
     host = HostBlocks(w, seed=0, gen_device="cuda", keep_params=True)
     # bytes: one-shot reassembly of each host block against the oracle image
@@ -68,12 +77,11 @@ def test_nano_shapes_streamed_resident_and_sampled_oracle():
     assert dlo.kernel_status() == 0
     st.close()
     # sampled rows of block 0 against the oracle (K and V over all tokens)
-    rows = [0, 1, 777, 2048, 4095]
     p = params_f32(host.params[0])
     ref = oracle.block_forward_rows(x_in_block0.cpu().numpy(), p, rows, w.batch, w.tokens,
                                     w.hidden, w.heads, w.mlp, w.eps)
     got = x_out_block0.cpu().numpy()[rows]
-    assert_oracle_close(got, ref, "nano rows")
+    assert_oracle_close(got, ref, name + " rows")
     xin = x_in_block0.cpu().numpy()[rows]
-    assert_oracle_close(got - xin, ref - xin, "nano row updates", 2e-2, 1e-2)
+    assert_oracle_close(got - xin, ref - xin, name + " row updates", 2e-2, 1e-2)
     host.close()

@@ -179,6 +179,13 @@ def test_at_most_two_blocks_resident():
 
 # ---------------------------------------------------------------- block math
 
+def test_gelu_array_is_the_scalar_gelu_element_by_element():
+    z = np.random.default_rng(40).standard_normal((7, 13)) * 4
+    got = oracle.gelu_tanh_array(z)
+    assert got.shape == z.shape
+    assert all(got.flat[i] == oracle.gelu_tanh(float(z.flat[i])) for i in range(z.size))
+
+
 def test_gelu_tanh_close_to_erf_gelu_and_odd_identity():
     for z in np.linspace(-8, 8, 1601):
         exact = 0.5 * z * (1 + math.erf(z / math.sqrt(2)))
