@@ -304,12 +304,11 @@ dlo_status dlo_forward(const dlo_dit_cfg* cfg, const dlo_plan* plan,
                        size_t scratch_bytes, void* stream);
 
 /* dlo_forward without a caller scratch buffer, for callers that cannot
- * allocate device memory: code running while a stream is captured into a
- * CUDA graph (cudaMalloc is refused or breaks the capture there), serving
- * loops that must not allocate after warm-up (cudaMalloc/cudaFree can
- * synchronise the device and stall every stream), and hosts whose device
- * memory belongs to another allocator with a fixed budget.  The pages have
- * no counterpart of this call; it is an addition of this library.
+ * allocate device memory: serving loops that must not allocate once warm
+ * (cudaMalloc/cudaFree can synchronise the device and stall every stream),
+ * and hosts whose device memory belongs to another allocator with a fixed
+ * budget.  The pages have no counterpart of this call; it is an addition
+ * of this library.
  * Scratch comes from a 32 MiB array in the library's own device memory
  * (a file-scope __device__ array, held by every GPU that loads the library
  * until the process exits).  A shape whose scratch

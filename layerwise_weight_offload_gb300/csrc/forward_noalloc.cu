@@ -2,14 +2,13 @@
 // device memory.
 //
 // dlo_forward needs a scratch buffer from its caller.  Some callers cannot
-// get one: code that runs while a stream is being captured into a CUDA
-// graph (cudaMalloc is not a stream operation, is refused or breaks the
-// capture there), serving loops that must not allocate after warm-up
+// get one: serving loops that must not allocate once they are warm
 // (cudaMalloc and cudaFree may synchronise the whole device and stall every
-// stream in flight), and hosts whose device memory belongs to another
-// allocator with a fixed budget.  dlo_forward_noalloc takes its scratch from
-// a fixed array in this library's own device memory instead, so it
-// allocates nothing.
+// stream in flight, which a latency budget cannot absorb), and hosts whose
+// device memory is owned by another allocator with a fixed budget, so that
+// an extra cudaMalloc would fail or overrun it.  dlo_forward_noalloc takes
+// its scratch from a fixed array in this library's own device memory
+// instead, so it allocates nothing.
 //
 // The array is a file-scope __device__ array; every GPU on which this
 // library's code is loaded holds it until the process exits.  Host code

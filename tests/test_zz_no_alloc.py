@@ -1,9 +1,9 @@
 """dlo_forward_noalloc: the block forward for callers that cannot allocate
-device memory (stream capture in progress, no-allocation serving loops,
-memory owned by another allocator).  It takes its scratch from the
-library's static device array; its output must match dlo_forward with a
-caller-provided scratch buffer, on two calls in a row (the second call
-finds the first call's leftovers in the shared array)."""
+device memory (serving loops that must not allocate once warm, device
+memory owned by another allocator with a fixed budget).  It takes its
+scratch from the library's static device array; its output must match
+dlo_forward with a caller-provided scratch buffer, on two calls in a row
+(the second call finds the first call's leftovers in the shared array)."""
 import pytest
 import torch
 
