@@ -69,6 +69,13 @@ def parse():
                     help="add every timed prefetch's duration to the JSON line")
     ap.add_argument("--pretouch", type=int, default=1,
                     help="1: read every pinned host block once from the GPU before timing")
+    ap.add_argument("--verify", type=int, default=1,
+                    help="1: after the shards are written, time every host block's copy and "
+                         "relocate the slow ones (setup, untimed)")
+    ap.add_argument("--heal", default="auto", choices=["auto", "on", "off"],
+                    help="move host blocks whose copies turn slow while the stream runs "
+                         "(auto: for blocks of 128 MB or more, where timing every copy costs "
+                         "nothing measurable)")
     ap.add_argument("--only", default=None,
                     choices=["linear", "qkv", "fc2", "outproj", "attention", "norm", "copy",
                              "forward"],
@@ -80,6 +87,9 @@ def parse():
     ap.add_argument("--source", default="shards", choices=["shards", "pageable", "registered"],
                     help="shards: pinned host shards (default); pageable / registered: the "
                          "rank-local path with one shard, blocks by parameter address")
+    ap.add_argument("--source-pages", default="huge", choices=["huge", "base"],
+                    help="--source registered: the parameters' memory as huge pages (a "
+                         "huge-page-backed mapping) or the tensors' own base pages")
     ap.add_argument("--layout", default="dit", choices=["dit", "mxfp8", "int8"],
                     help="with --only copy: the block's linears as bf16 (dit) or in a 1-byte layout")
     ap.add_argument("--sweep", action="store_true",
@@ -457,13 +467,23 @@ def run_ours(args, ws, rank, local):
         t0 = time.perf_counter()
         host.pretouch()
         pretouch_s = time.perf_counter() - t0
+    host_verify = None
+    if args.verify and args.source == "shards":
+        # setup, untimed: every host block's copy timed after the weights are
+        # in place; the slow ones move to fresh host ranges
+        t0 = time.perf_counter()
+        host_verify = host.verify()
+        host_verify["seconds"] = time.perf_counter() - t0
+    heal = args.source == "shards" and (
+        args.heal == "on" or (args.heal == "auto" and bytes_per_block >= 128 << 20))
 
     def make_stack(timing):
         if args.source != "shards":
             from layerwise_weight_offload_gb300.stack import SourceStack
-            return SourceStack(host, transport=args.source, timing=timing)
+            return SourceStack(host, transport=args.source, timing=timing,
+                               pages=args.source_pages)
         return StreamedStack(host, copy_mode=mode, copy_ctas=args.copy_ctas, timing=timing,
-                             two_copy_streams=args.two_copy_streams)
+                             two_copy_streams=args.two_copy_streams, heal=heal)
 
     x0 = W.gen_x(w, args.seed, device="cuda")
     x = x0.clone()
@@ -553,6 +573,7 @@ def run_ours(args, ws, rank, local):
                  "slow_over_2x_p50": sum(1 for v in qs if v > 2 * qs[len(qs) // 2]),
                  "first": copy_ms[:3], "last": copy_ms[-3:]} if qs else None
     chosen_t = dlo.COPY_MODE_NAMES[stats_t.chosen_mode]
+    heal_log_t = list(getattr(stt, "heal_log", []))
     stt.close()
 
     # all-resident reference run: same kernels, no transfer, the same regions
@@ -716,10 +737,17 @@ def run_ours(args, ws, rank, local):
                     "pair recorded around every prefetch; value, ms_per_step and clocks come "
                     "from the first pass, without them"},
         "copy_ms_distribution": copy_dist, "pretouch_s": pretouch_s,
+        "host_verify": host_verify,
+        "heal": {"enabled": heal,
+                 "moves_value_pass": [list(m) for m in getattr(st, "heal_log", [])],
+                 "moves_copy_stats_pass": [list(m) for m in heal_log_t],
+                 "note": "(forwards so far, host block, moved to a range that streamed at "
+                         "speed); the value pass's moves include those of its warm-up and of "
+                         "the e2e pass, which runs on the same stack"},
         "host_huge_page_fraction": host.buf.huge_fraction(),
         "host_huge_ranges_used_fraction": host.buf.good_fraction(),
         "host_range_survey": host.buf.survey_summary(),
-        "source_path": ({"transport": args.source,
+        "source_path": ({"transport": args.source, "pages": args.source_pages,
                          "direct_prefetches": stats1.n_direct_prefetches,
                          "packed_prefetches": stats1.n_packed_prefetches,
                          "pack_ms_per_packed_block": (stats1.pack_ms - stats0.pack_ms) /

@@ -516,6 +516,23 @@ dlo_status dlo_engine_create(const dlo_engine_desc* desc, dlo_engine** out);
 dlo_status dlo_register_block(dlo_engine* e, int32_t block, const dlo_plan* plan,
                               const void* const* shard_ptrs);
 
+/* Points registered `block` at a new copy of its shards (same plan; the
+ * pointers obey dlo_register_block's rules), for a caller that moves a
+ * block's host memory while the stream runs — for example off host ranges
+ * that have turned slow for the GPU to read.  First waits (host side,
+ * bounded by timeout_ms) until every copy already enqueued from the old
+ * shards has completed, so that the caller may reuse the old memory once
+ * the call returns; later prefetches read the new shards.  Several engine
+ * blocks registered with the same shards are replaced one by one.
+ * The pages have no counterpart: they load every shard once ([B2] §2);
+ * their nearest step is the drain of in-flight host-to-device copies
+ * before host memory is released ([D5] "Lease ownership").
+ * Errors: DLO_ERR_INVALID (range, pointers), DLO_ERR_STATE (the block is
+ * not registered with shards), DLO_ERR_TIMEOUT (a pending copy did not
+ * finish in time; nothing is changed). */
+dlo_status dlo_replace_block_shards(dlo_engine* e, int32_t block,
+                                    const void* const* shard_ptrs, int32_t timeout_ms);
+
 /* Rank-local source blocks ([D5] "Rank-local path without DLO AllGather"):
  * registers `block` by the host addresses of its parameters instead of by
  * shards.  The plan must have n_shards = 1 (no sharding on this path).
@@ -630,6 +647,25 @@ dlo_status dlo_engine_copy_times(dlo_engine* e, float* copy_ms, int64_t* copy_by
  * have completed. */
 dlo_status dlo_engine_copy_spans(dlo_engine* e, float* start_ms, float* end_ms,
                                  int32_t cap, int32_t* n_out);
+
+/* One timed prefetch (desc.timing = 1). */
+typedef struct {
+  int64_t seq;          /* 0, 1, 2, ...: the engine's n-th timed prefetch */
+  int32_t block;        /* block copied */
+  int32_t slot;         /* slot written */
+  float copy_ms;        /* time between the events around its copies */
+  int64_t bytes;        /* bytes moved */
+} dlo_copy_record;
+
+/* Incremental, non-blocking read of the timing record: copies to buf, in
+ * order, up to `cap` records of timed prefetches with seq >= since whose
+ * copies have completed, stopping at the first one still in flight;
+ * *n_out = how many, *next = the seq to pass as `since` next time.  Records
+ * older than the ring kept (desc.log_capacity) are skipped.  A monitor in a
+ * serving loop calls this between steps without waiting on the GPU.
+ * Errors: DLO_ERR_INVALID (null n_out/next, or cap > 0 with a null buf). */
+dlo_status dlo_engine_copy_log(dlo_engine* e, int64_t since, dlo_copy_record* buf, int32_t cap,
+                               int32_t* n_out, int64_t* next);
 
 /* Waits (host side, bounded by timeout_ms) for both streams' enqueued
  * engine work, then releases the engine's events.  The caller's buffers are

@@ -167,6 +167,8 @@ struct dlo_engine {
     cudaEvent_t a, b;
     int64_t bytes;
     int32_t mode;
+    int64_t seq;                     // n-th timed prefetch of the engine
+    int32_t block, slot;
   };
   static constexpr int kMaxFan = 8;
 
@@ -232,6 +234,7 @@ struct dlo_engine {
   double race_dma_us = 0, race_kernel_us = 0;
   int64_t n_prefetches = 0;
   int64_t n_kernel_prefetches = 0;
+  int64_t n_timed = 0;               // timed prefetches so far (next seq)
 };
 
 namespace dlo {
@@ -502,7 +505,8 @@ int32_t mode_for(dlo_engine* e, int64_t k, const dlo_engine::Block& b) {
 // The timing entry of the prefetch about to be enqueued: a new entry with
 // two new events, or (ring full) the oldest entry, whose events are
 // recorded again.
-dlo_status timed_entry(dlo_engine* e, int64_t bytes, int32_t mode, dlo_engine::Timed** out) {
+dlo_status timed_entry(dlo_engine* e, int64_t bytes, int32_t mode, int32_t block, int32_t slot,
+                       dlo_engine::Timed** out) {
   bool reused = false;
   dlo_engine::Timed& t = e->timed.push(&reused);
   if (!reused) {
@@ -514,6 +518,9 @@ dlo_status timed_entry(dlo_engine* e, int64_t bytes, int32_t mode, dlo_engine::T
   }
   t.bytes = bytes;
   t.mode = mode;
+  t.seq = e->n_timed++;
+  t.block = block;
+  t.slot = slot;
   *out = &t;
   return DLO_OK;
 }
@@ -549,7 +556,7 @@ dlo_status prefetch_source(dlo_engine* e, int32_t block, int32_t slot) {
   const dlo_engine::Block& b = e->blocks[block];
   cudaStream_t cs = e->slot_copy[slot];
   dlo_engine::Timed* t = nullptr;
-  if (e->timing) DLO_TRY(timed_entry(e, b.bytes, DLO_COPY_DMA, &t));
+  if (e->timing) DLO_TRY(timed_entry(e, b.bytes, DLO_COPY_DMA, block, slot, &t));
   if (b.direct) {
     DLO_CUDA(cudaStreamWaitEvent(cs, e->freed[slot], 0));
     if (t) DLO_CUDA(cudaEventRecord(t->a, cs));
@@ -602,7 +609,7 @@ dlo_status enqueue_prefetch(dlo_engine* e, int32_t block, int32_t slot, int64_t 
     DLO_CUDA(cudaStreamWaitEvent(cs, e->stage_free[slot], 0));
     dlo_engine::Timed* t = nullptr;
     if (e->timing) {
-      DLO_TRY(timed_entry(e, b.bytes, mode, &t));
+      DLO_TRY(timed_entry(e, b.bytes, mode, block, slot, &t));
       DLO_CUDA(cudaEventRecord(t->a, cs));
     }
     DLO_TRY(stage_h2d(b, e->staging[slot], cs));
@@ -620,7 +627,7 @@ dlo_status enqueue_prefetch(dlo_engine* e, int32_t block, int32_t slot, int64_t 
   DLO_CUDA(cudaStreamWaitEvent(cs, e->freed[slot], 0));
   dlo_engine::Timed* t = nullptr;
   if (e->timing) {
-    DLO_TRY(timed_entry(e, b.bytes, mode, &t));
+    DLO_TRY(timed_entry(e, b.bytes, mode, block, slot, &t));
     DLO_CUDA(cudaEventRecord(t->a, cs));
   }
   DLO_TRY(copy_block(b, e->slot[slot], mode, e->copy_ctas, cs, e->fan, e->aux, e->fork_ev,
@@ -799,6 +806,45 @@ dlo_status dlo_engine_create(const dlo_engine_desc* d, dlo_engine** out) {
   return DLO_OK;
 }
 
+}  // extern "C"
+
+namespace dlo {
+namespace {
+
+// A block's shard table from the caller's pointers: each shard non-null,
+// 16-byte aligned and page-locked host memory (its device-mapped address
+// kept for the copy kernel).
+dlo_status shard_table(const char* who, const dlo_plan* plan, const void* const* shard_ptrs,
+                       dlo_engine::Block* b) {
+  const size_t n = plan->groups.size() * static_cast<size_t>(plan->n_shards);
+  if (n > static_cast<size_t>(kMaxSegments))
+    DLO_FAIL(DLO_ERR_INVALID, "%s: %zu (group, shard) pieces, at most %d", who, n,
+             kMaxSegments);
+  b->plan = plan;
+  b->host.assign(shard_ptrs, shard_ptrs + n);
+  b->dev.assign(n, nullptr);
+  b->bytes = 0;
+  for (size_t i = 0; i < n; ++i) {
+    const void* q = shard_ptrs[i];
+    if (!q || (reinterpret_cast<uintptr_t>(q) & 15u))
+      DLO_FAIL(DLO_ERR_INVALID, "%s: shard %zu is null or not 16-byte aligned", who, i);
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, q) != cudaSuccess || a.type != cudaMemoryTypeHost) {
+      cudaGetLastError();
+      DLO_FAIL(DLO_ERR_INVALID, "%s: shard %zu is not page-locked host memory", who, i);
+    }
+    b->dev[i] = a.devicePointer;
+  }
+  for (const auto& g : plan->groups) b->bytes += g.shard_bytes * plan->n_shards;
+  compute_pitches(b);
+  return DLO_OK;
+}
+
+}  // namespace
+}  // namespace dlo
+
+extern "C" {
+
 dlo_status dlo_register_block(dlo_engine* e, int32_t block, const dlo_plan* plan,
                               const void* const* shard_ptrs) {
   using namespace dlo;
@@ -815,31 +861,37 @@ dlo_status dlo_register_block(dlo_engine* e, int32_t block, const dlo_plan* plan
     DLO_FAIL(DLO_ERR_INVALID,
              "dlo_register_block: block needs %lld staging bytes, staging holds %lld",
              (long long)plan->staging_bytes, (long long)e->staging_bytes);
-  const size_t n = plan->groups.size() * static_cast<size_t>(plan->n_shards);
-  if (n > static_cast<size_t>(kMaxSegments))
-    DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block: %zu (group, shard) pieces, at most %d", n,
-             kMaxSegments);
   dlo_engine::Block b;
-  b.plan = plan;
-  b.host.assign(shard_ptrs, shard_ptrs + n);
-  b.dev.assign(n, nullptr);
-  for (size_t i = 0; i < n; ++i) {
-    const void* q = shard_ptrs[i];
-    if (!q || (reinterpret_cast<uintptr_t>(q) & 15u))
-      DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block: shard %zu is null or not 16-byte aligned",
-               i);
-    cudaPointerAttributes a{};
-    if (cudaPointerGetAttributes(&a, q) != cudaSuccess || a.type != cudaMemoryTypeHost) {
-      cudaGetLastError();
-      DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block: shard %zu is not page-locked host memory",
-               i);
-    }
-    b.dev[i] = a.devicePointer;
-  }
-  for (const auto& g : plan->groups) b.bytes += g.shard_bytes * plan->n_shards;
-  compute_pitches(&b);
+  DLO_TRY(shard_table("dlo_register_block", plan, shard_ptrs, &b));
   if (e->mode == DLO_COPY_KERNEL && !all_mapped(b))
     DLO_FAIL(DLO_ERR_INVALID, "dlo_register_block: kernel copies need device-mapped shards");
+  e->blocks[block] = std::move(b);
+  return DLO_OK;
+}
+
+dlo_status dlo_replace_block_shards(dlo_engine* e, int32_t block,
+                                    const void* const* shard_ptrs, int32_t timeout_ms) {
+  using namespace dlo;
+  DLO_TRY(check_engine(e));
+  if (block < 0 || block >= e->n_blocks || !shard_ptrs)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_replace_block_shards: bad block %d or null pointers", block);
+  const dlo_engine::Block& cur = e->blocks[block];
+  if (!cur.plan || cur.source)
+    DLO_FAIL(DLO_ERR_STATE, "dlo_replace_block_shards: block %d has no registered shards",
+             block);
+  dlo_engine::Block b;
+  DLO_TRY(shard_table("dlo_replace_block_shards", cur.plan, shard_ptrs, &b));
+  if (e->mode == DLO_COPY_KERNEL && !all_mapped(b))
+    DLO_FAIL(DLO_ERR_INVALID,
+             "dlo_replace_block_shards: kernel copies need device-mapped shards");
+  // every copy already enqueued from the old shards (a slot holding the
+  // block has one pending until its ready event completes) must finish
+  // before the caller may reuse that memory
+  for (int s = 0; s < 2; ++s)
+    if (e->slot_holds[s] == block && !wait_event_host(e->ready[s], timeout_ms))
+      DLO_FAIL(DLO_ERR_TIMEOUT,
+               "dlo_replace_block_shards: block %d's copy into slot %d not done after %d ms",
+               block, s, timeout_ms);
   e->blocks[block] = std::move(b);
   return DLO_OK;
 }
@@ -1093,6 +1145,38 @@ dlo_status dlo_engine_copy_spans(dlo_engine* e, float* start_ms, float* end_ms, 
     end_ms[i] = b;
   }
   *n_out = n;
+  return DLO_OK;
+}
+
+dlo_status dlo_engine_copy_log(dlo_engine* e, int64_t since, dlo_copy_record* buf, int32_t cap,
+                               int32_t* n_out, int64_t* next) {
+  using namespace dlo;
+  DLO_TRY(check_engine(e));
+  if (!n_out || !next || (cap > 0 && !buf))
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_engine_copy_log: null argument");
+  const size_t kept = e->timed.size();
+  int64_t seq = since;
+  if (kept > 0 && seq < e->timed.at(0).seq) seq = e->timed.at(0).seq;   // older ones dropped
+  int32_t n = 0;
+  if (kept > 0) {
+    for (size_t i = static_cast<size_t>(seq - e->timed.at(0).seq); i < kept && n < cap; ++i) {
+      const dlo_engine::Timed& t = e->timed.at(i);
+      const cudaError_t q = cudaEventQuery(t.b);
+      if (q == cudaErrorNotReady) break;        // not done yet: report it next time
+      DLO_CUDA(q);
+      float ms = 0;
+      DLO_CUDA(cudaEventElapsedTime(&ms, t.a, t.b));
+      buf[n].seq = t.seq;
+      buf[n].block = t.block;
+      buf[n].slot = t.slot;
+      buf[n].copy_ms = ms;
+      buf[n].bytes = t.bytes;
+      ++n;
+      seq = t.seq + 1;
+    }
+  }
+  *n_out = n;
+  *next = seq;
   return DLO_OK;
 }
 

@@ -75,6 +75,11 @@ class SchedEvent(ctypes.Structure):
                 ("prefetch_slot", c_i32), ("waits_on_free_of_k", c_i32), ("copy_mode", c_i32)]
 
 
+class CopyRecord(ctypes.Structure):
+    _fields_ = [("seq", c_i64), ("block", c_i32), ("slot", c_i32), ("copy_ms", c_f32),
+                ("bytes", c_i64)]
+
+
 class EngineStats(ctypes.Structure):
     _fields_ = [("chosen_mode", c_i32), ("n_forwards", c_i32), ("n_prefetches", c_i32),
                 ("n_kernel_prefetches", c_i32), ("race_dma_us", ctypes.c_double),
@@ -126,6 +131,8 @@ _SIGS = {
     "dlo_engine_query": (c_i32, [c_vp, _P(EngineStats)]),
     "dlo_engine_copy_times": (c_i32, [c_vp, _P(c_f32), _P(c_i64), c_i32, _P(c_i32)]),
     "dlo_engine_copy_spans": (c_i32, [c_vp, _P(c_f32), _P(c_f32), c_i32, _P(c_i32)]),
+    "dlo_engine_copy_log": (c_i32, [c_vp, c_i64, _P(CopyRecord), c_i32, _P(c_i32), _P(c_i64)]),
+    "dlo_replace_block_shards": (c_i32, [c_vp, c_i32, _P(c_vp), c_i32]),
     "dlo_engine_destroy": (c_i32, [c_vp, c_i32]),
     "dlo_kernel_status": (c_i32, [_P(c_i32)]),
     "dlo_debug_wait_probe": (c_i32, [c_i32, c_i64, c_i64, _P(c_i64), _P(c_i32)]),
@@ -445,6 +452,20 @@ class Engine:
     def register_block_source(self, block, plan, param_srcs):
         _check(lib().dlo_register_block_source(self.handle, block, plan.handle,
                                                _ptrs(param_srcs)), "dlo_register_block_source")
+
+    def replace_block_shards(self, block, shard_ptrs, timeout_ms=60000):
+        _check(lib().dlo_replace_block_shards(self.handle, block, _ptrs(shard_ptrs),
+                                              int(timeout_ms)), "dlo_replace_block_shards")
+
+    def copy_log(self, since, cap=4096):
+        """Completed timed prefetches with seq >= since: ([(seq, block, slot,
+        ms, bytes)], next_since), without waiting on the GPU."""
+        buf = (CopyRecord * cap)()
+        n, nxt = c_i32(), c_i64()
+        _check(lib().dlo_engine_copy_log(self.handle, int(since), buf, cap, ctypes.byref(n),
+                                         ctypes.byref(nxt)), "dlo_engine_copy_log")
+        return ([(r.seq, r.block, r.slot, r.copy_ms, r.bytes) for r in buf[:n.value]],
+                nxt.value)
 
     def prefetch(self, block, slot):
         _check(lib().dlo_prefetch(self.handle, block, slot), "dlo_prefetch")

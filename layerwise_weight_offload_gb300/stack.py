@@ -54,12 +54,14 @@ class PinnedBuffer:
 
     SMALL = 256 << 20     # below this the footprint is too small to matter
 
-    def __init__(self, nbytes, spare=0.25, tries=3, defer=False):
+    def __init__(self, nbytes, spare=0.25, tries=3, defer=False, extra_ranges=0):
+        """extra_ranges: 512 MiB ranges reserved beyond the spare room for
+        relocate() (address space only until used)."""
         self.nbytes = int(nbytes)
         self.small = self.nbytes < self.SMALL
         n_ranges = max(1, -(-self.nbytes // _HUGE))
         self.capacity = (_round_up(self.nbytes, 1 << 16) if self.small
-                         else (n_ranges + int(n_ranges * spare) + 2) * _HUGE)
+                         else (n_ranges + int(n_ranges * spare) + 2 + extra_ranges) * _HUGE)
         self.tries = tries
         self._map = mmap.mmap(-1, self.capacity + _HUGE,
                               flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
@@ -286,6 +288,65 @@ class PinnedBuffer:
             taken.append((found, found + n))
         return offs
 
+    def relocate(self, pieces, min_gbs, align=256, device="cuda"):
+        """Moves pieces [(offset, nbytes)] (from .ptr) into fresh huge-page
+        ranges after the prepared ones, back to back at `align`: each new
+        range's first touch is the data itself (copied from the old place,
+        which stays intact), then collapse, registration and one timed
+        host->device copy of the new span after a warm-up copy.  Returns the
+        new offsets if that copy reached min_gbs, else None (the new ranges
+        are then marked slow and left unused).  The old ranges are marked
+        slow either way.  Needs room in the reservation (spare); None if
+        there is none.
+
+        Why: on some GB300 hosts ranges that passed the placement survey
+        stream at 3-30 GB/s once the weights are written into them, on every
+        later pass, idle or under compute; a block there stalls the stream
+        each time it is read."""
+        if self.small:
+            return None
+        offs, pos = [], 0
+        for _, n in pieces:
+            pos = _round_up(pos, align)
+            offs.append(pos)
+            pos += int(n)
+        k = -(-pos // _HUGE)
+        r0 = len(self.good)
+        if (r0 + k) * _HUGE > self.capacity:
+            return None
+        base = r0 * _HUGE
+        for (old, n), o in zip(pieces, offs):
+            ctypes.memmove(self.ptr + base + o, self.ptr + old, int(n))
+        if pos < k * _HUGE:
+            ctypes.memset(self.ptr + base + pos, 0, k * _HUGE - pos)
+        for r in range(k):
+            ok = any(_collapse(self.ptr + base + r * _HUGE, _HUGE) for _ in range(self.tries))
+            self.good.append(ok)
+            self.rate.append(None)
+            self.fast.append(None)
+        self.register()
+        for old, n in pieces:
+            for r in range(old // _HUGE, (old + int(n) - 1) // _HUGE + 1):
+                self.fast[r] = False
+        dst = torch.empty(pos, dtype=torch.uint8, device=device)
+        st = torch.cuda.Stream(device=device)
+        ms = None
+        with torch.cuda.stream(st):
+            for _ in range(2):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(st)
+                dst.copy_(self.view(base, pos), non_blocking=True)
+                b.record(st)
+                b.synchronize()
+                ms = a.elapsed_time(b)
+        del dst
+        gbs = pos / (ms * 1e6)
+        good = gbs >= min_gbs and all(self.good[r0:r0 + k])
+        for r in range(r0, r0 + k):
+            self.rate[r] = gbs
+            self.fast[r] = good
+        return [base + o for o in offs] if good else None
+
     def view(self, offset, nbytes):
         return self._t[self.offset + offset:self.offset + offset + nbytes]
 
@@ -363,8 +424,10 @@ class HostBlocks:
         s = w.shards
         self.strides = [_round_up(g.shard_alloc_bytes, 256) for g in self.groups]
         piece = [s * st for st in self.strides]
-        self.buf = PinnedBuffer(w.distinct * sum(_round_up(p, 256) for p in piece), spare=0.5,
-                                defer=True)
+        hb_bytes = sum(_round_up(p, 256) for p in piece)
+        # room to relocate up to 8 host blocks (HostBlocks.relocate_block)
+        self.buf = PinnedBuffer(w.distinct * hb_bytes, spare=0.5, defer=True,
+                                extra_ranges=min(w.distinct, 8) * (-(-hb_bytes // _HUGE)) + 1)
         where = self.buf.place_surveyed([piece[g] for _ in range(w.distinct)
                                          for g in range(len(self.groups))])
         self.offsets = []                  # [hb][g * s + r] offsets from buf.ptr
@@ -410,16 +473,124 @@ class HostBlocks:
             out.append(self.buf.view(o, g.shard_alloc_bytes))
         return out
 
+    def block_copy_ms(self, passes=2, mode=None, stream=None):
+        """Per host block, the time of the last of `passes` reassemblies
+        into a scratch slot (DMA by default), as a prefetch moves it."""
+        mode = dlo.COPY_DMA if mode is None else mode
+        dst = torch.empty(self.plan.info().slot_bytes, dtype=torch.uint8, device="cuda")
+        s = stream or torch.cuda.Stream()
+        ms = {}
+        for _ in range(passes):
+            evs = []
+            for hb in range(self.w.distinct):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                dlo.reassemble(self.plan, self.shard_ptrs(hb), dst, mode, s)
+                b.record(s)
+                evs.append((hb, a, b))
+            s.synchronize()
+            for hb, a, b in evs:
+                ms[hb] = a.elapsed_time(b)
+        del dst
+        return ms
+
+    def relocate_block(self, hb, min_gbs):
+        """Moves host block hb's shards to fresh host ranges (one piece per
+        dtype group, the group's shards at their constant stride); True if
+        the new place streams at min_gbs (else hb stays where it was)."""
+        s = self.w.shards
+        pieces = [(self.offsets[hb][g * s], s * st) for g, st in enumerate(self.strides)]
+        new = self.buf.relocate(pieces, min_gbs)
+        if new is None:
+            return False
+        offs = []
+        for g, st in enumerate(self.strides):
+            offs += [new[g] + r * st for r in range(s)]
+        self.offsets[hb] = offs
+        return True
+
+    def verify(self, factor=1.5, rounds=3):
+        """After the shards are written: times every host block's copy (the
+        second of two passes) and relocates the blocks slower than `factor`
+        x the median by more than 1 ms, up to `rounds` times.  Returns a
+        report.  The placement survey times the ranges before the weights
+        are written into them; on some hosts ranges turn slow after that."""
+        report = {"rounds": 0, "slow_found": [], "relocated": [], "failed": [],
+                  "median_ms": None}
+        for _ in range(rounds):
+            ms = self.block_copy_ms()
+            med = sorted(ms.values())[len(ms) // 2]
+            report["median_ms"] = report["median_ms"] or med
+            slow = [hb for hb, v in ms.items() if v > factor * med and v - med > 1.0]
+            report["rounds"] += 1
+            if not slow:
+                break
+            bytes_hb = sum(g.shard_bytes * self.w.shards for g in self.groups)
+            for hb in slow:
+                report["slow_found"].append((hb, round(ms[hb], 3)))
+                ok = self.relocate_block(hb, bytes_hb / (med * 1e6) / factor)
+                (report["relocated"] if ok else report["failed"]).append(hb)
+        return report
+
     def close(self):
         self.buf.close()
+
+
+class CopyHealer:
+    """Names the host blocks whose prefetches have turned slow, from the
+    engine's copy log: a copy is slow when its rate is below the median rate
+    of the recent copies divided by `factor` and it took at least
+    `min_extra_ms` longer than a copy at that rate would; a host block is
+    named once `strikes` of its copies since it last moved were slow.  A
+    block that keeps turning slow is named at most `max_moves` times."""
+
+    def __init__(self, distinct, factor=2.0, min_extra_ms=1.0, strikes=2, window=512,
+                 max_moves=3):
+        self.distinct = distinct
+        self.factor, self.min_extra_ms, self.strikes = factor, min_extra_ms, strikes
+        self.window, self.max_moves = window, max_moves
+        self.rates = []
+        self.count = {}
+        self.moves = {}
+
+    def observe(self, records):
+        """records: (seq, block, slot, ms, bytes) of completed prefetches;
+        returns the host blocks to move now."""
+        for _, _, _, ms, nbytes in records:
+            if ms > 0:
+                self.rates.append(nbytes / ms)
+        self.rates = self.rates[-self.window:]
+        if len(self.rates) < 8:
+            return []
+        med = sorted(self.rates)[len(self.rates) // 2]
+        out = []
+        for _, block, _, ms, nbytes in records:
+            hb = block % self.distinct
+            expect = nbytes / med
+            if ms * med < nbytes * self.factor or ms - expect < self.min_extra_ms:
+                continue
+            self.count[hb] = self.count.get(hb, 0) + 1
+            if (self.count[hb] >= self.strikes and self.moves.get(hb, 0) < self.max_moves
+                    and hb not in out):
+                out.append(hb)
+        return out
+
+    def moved(self, hb):
+        self.count[hb] = 0
+        self.moves[hb] = self.moves.get(hb, 0) + 1
 
 
 class StreamedStack:
     """Two slots and the hook schedule: the path the pages describe."""
 
     def __init__(self, host: HostBlocks, copy_mode=dlo.COPY_AUTO, copy_ctas=0, timing=False,
-                 device="cuda", two_copy_streams=False, log_capacity=0):
+                 device="cuda", two_copy_streams=False, log_capacity=0, heal=False):
+        """heal: watch every prefetch's copy time (the engine times each
+        one) and, between steps, move host blocks whose copies have turned
+        slow to fresh host ranges (CopyHealer, HostBlocks.relocate_block,
+        dlo_replace_block_shards)."""
         w = host.w
+        timing = timing or heal
         self.w, self.host, self.plan = w, host, host.plan
         self.slot_bytes = _round_up(self.plan.info().slot_bytes, 256)
         self.slots = [torch.empty(self.slot_bytes, dtype=torch.uint8, device=device)
@@ -446,6 +617,9 @@ class StreamedStack:
         self.scratch_bytes = dlo.forward_scratch_bytes(self.cfg)
         self.scratch = torch.empty(self.scratch_bytes, dtype=torch.uint8, device=device)
         self.primed = False
+        self.healer = CopyHealer(w.distinct) if heal else None
+        self.heal_since = 0
+        self.heal_log = []              # (forwards so far, host block, moved?)
 
     def prime(self):
         """Setup prefetch: block 0 into slot 0."""
@@ -459,6 +633,25 @@ class StreamedStack:
             self.prime()
         for i in range(self.w.n_blocks):
             self.engine.block_forward(i, self.cfg, x, self.scratch, self.scratch_bytes)
+        if self.healer is not None:
+            self.heal()
+
+    def heal(self, max_moves=4):
+        """Reads the completed prefetches since the last call (no wait on
+        the GPU) and moves up to max_moves host blocks the healer names."""
+        recs, self.heal_since = self.engine.copy_log(self.heal_since)
+        todo = self.healer.observe(recs)[:max_moves]
+        if not todo:
+            return
+        bytes_hb = sum(g.shard_bytes * self.w.shards for g in self.host.groups)
+        med = sorted(self.healer.rates)[len(self.healer.rates) // 2]
+        for hb in todo:
+            ok = self.host.relocate_block(hb, med / 1e6 / self.healer.factor)
+            if ok:
+                for i in range(hb, self.w.n_blocks, self.w.distinct):
+                    self.engine.replace_block_shards(i, self.host.shard_ptrs(hb))
+            self.healer.moved(hb)
+            self.heal_log.append((self.engine.query().n_forwards, hb, ok))
 
     def close(self):
         if self.engine is not None:
@@ -472,10 +665,17 @@ class SourceStack:
     (host.params, ordinary pageable tensors).  transport "pageable": CPU
     threads pack each block into one of two pinned host staging slots before
     its DMA; "registered": the parameters' memory is page-locked (all or
-    nothing) and copied straight into the slots."""
+    nothing) and copied straight into the slots.
+
+    pages (registered only): "huge" first copies the parameters into an
+    anonymous mapping backed by transparent huge pages (what a checkpoint on
+    a huge-page-backed file system maps), "base" registers the tensors'
+    own memory (base pages).  The GPU streams page-locked memory of 64 KiB
+    pages at a fraction of the link rate once the footprint is several GB
+    (PinnedBuffer), so only the huge-page form keeps up at scale."""
 
     def __init__(self, host: HostBlocks, transport="pageable", pack_threads=0, timing=False,
-                 device="cuda"):
+                 device="cuda", pages="huge"):
         w = host.w
         if w.shards != 1 or host.params is None:
             raise ValueError("SourceStack needs a one-shard HostBlocks with keep_params=True")
@@ -489,6 +689,7 @@ class SourceStack:
                      for hb in range(w.distinct)]
         self.reg = None
         self.hs = None
+        self.arena = None
         staging = None
         if transport == "registered":
             ptrs, sizes = [], []
@@ -497,6 +698,19 @@ class SourceStack:
                     t = host.params[hb][name]
                     ptrs.append(t.data_ptr())
                     sizes.append(t.numel() * t.element_size())
+            if pages == "huge":
+                # huge-page-backed copies of the parameters, registered below
+                # (the arena itself is never registered by PinnedBuffer)
+                self.arena = PinnedBuffer(sum(_round_up(n, 256) for n in sizes), spare=0.1,
+                                          defer=True)
+                offs = self.arena.place(sizes, 256)
+                moved = []
+                for p, n, o in zip(ptrs, sizes, offs):
+                    ctypes.memmove(self.arena.ptr + o, p, n)
+                    moved.append(self.arena.ptr + o)
+                ptrs = moved
+                k = len(host.descs)
+                self.srcs = [ptrs[hb * k:(hb + 1) * k] for hb in range(w.distinct)]
             dlo.host_register_ranges(ptrs, sizes)
             self.reg = (ptrs, sizes)
         else:
@@ -533,6 +747,9 @@ class SourceStack:
         if self.reg is not None:
             dlo.host_unregister_ranges(*self.reg)
             self.reg = None
+        if self.arena is not None:
+            self.arena.close()
+            self.arena = None
         if self.hs is not None:
             self.hs.close()
             self.hs = None

@@ -242,3 +242,40 @@ def test_dit_forward_through_source_blocks_equals_resident(registered):
         hs.close()
     e.destroy()
     host.close()
+
+
+@pytest.mark.parametrize("transport,pages", [("registered", "huge"), ("registered", "base"),
+                                             ("pageable", "huge")])
+def test_source_stack_streams_like_resident(transport, pages):
+    # the stack the bench runs for --source: a footprint above the
+    # huge-page threshold, so the "huge" form copies the parameters into a
+    # huge-page arena and registers that
+    from layerwise_weight_offload_gb300.stack import SourceStack
+    w = W.custom("srcstack", n_blocks=12, hidden=1024, heads=16, mlp=4096, tokens=128,
+                 shards=1, steps=2, distinct=12)
+    host = HostBlocks(w, seed=12, keep_params=True)
+    st = SourceStack(host, transport=transport, pages=pages)
+    if transport == "registered" and pages == "huge":
+        assert st.arena is not None and st.arena.good_fraction() is not None
+        assert st.srcs[3][0] != host.params[3]["norm1.weight"].data_ptr()
+    x0 = W.gen_x(w, 12, device="cuda")
+    x = x0.clone()
+    st.compute.wait_stream(torch.cuda.current_stream())
+    for _ in range(w.steps):
+        st.step(x)
+    torch.cuda.current_stream().wait_stream(st.compute)
+    rs = ResidentStack(host)
+    xr = x0.clone()
+    rs.stream.wait_stream(torch.cuda.current_stream())
+    for _ in range(w.steps):
+        rs.step(xr)
+    torch.cuda.current_stream().wait_stream(rs.stream)
+    torch.cuda.synchronize()
+    assert torch.equal(x, xr)
+    q = st.engine.query()
+    if transport == "registered":
+        assert q.n_direct_prefetches > 0 and q.n_packed_prefetches == 0
+    else:
+        assert q.n_packed_prefetches > 0
+    st.close()
+    host.close()

@@ -73,3 +73,48 @@ def test_fit_random_states(seed):
     offs = b._fit(sizes, 4096)
     if offs is not None:
         _check(b, sizes, offs, 4096)
+
+
+# ---- the copy healer (host logic only: synthetic copy records) -----------
+
+def _records(seq0, times_by_block, nbytes=906_000_000):
+    return [(seq0 + i, blk, i % 2, ms, nbytes) for i, (blk, ms) in enumerate(times_by_block)]
+
+
+def test_healer_names_a_block_after_two_slow_copies_only():
+    from layerwise_weight_offload_gb300.stack import CopyHealer
+    h = CopyHealer(distinct=32)
+    fast = [(b, 4.29 + 0.01 * (b % 3)) for b in range(128)]
+    assert h.observe(_records(0, fast)) == []
+    # host block 3 (engine blocks 3, 35, 67, 99) turns slow: 30x longer
+    step = [(b, 120.0 if b % 32 == 3 else ms) for b, ms in fast]
+    assert h.observe(_records(128, step[:40])) == [3]         # blocks 3 and 35: two strikes
+    h.moved(3)
+    assert h.observe(_records(168, step[40:70])) == []        # block 67: one strike since
+    assert h.observe(_records(198, step[70:])) == [3]          # block 99: the second
+
+
+def test_healer_ignores_one_off_and_small_excess():
+    from layerwise_weight_offload_gb300.stack import CopyHealer
+    h = CopyHealer(distinct=8, min_extra_ms=1.0)
+    base = [(b, 4.3) for b in range(64)]
+    assert h.observe(_records(0, base)) == []
+    # a single slow copy of host block 5: not named; 2.5x of a 0.1 ms copy:
+    # below the absolute margin, not named either
+    assert h.observe(_records(64, [(5, 40.0)] + base[1:8])) == []
+    tiny = [(6, 0.25)] * 4
+    assert h.observe(_records(72, [(b, 0.1) for b in range(64)] + tiny, nbytes=1_000_000)) == []
+
+
+def test_healer_stops_after_max_moves():
+    from layerwise_weight_offload_gb300.stack import CopyHealer
+    h = CopyHealer(distinct=4, strikes=1, max_moves=2)
+    base = [(b, 4.3) for b in range(16)]
+    h.observe(_records(0, base))
+    named = 0
+    for k in range(5):
+        got = h.observe(_records(16 + k, [(1, 90.0)]))
+        if got == [1]:
+            named += 1
+            h.moved(1)
+    assert named == 2
