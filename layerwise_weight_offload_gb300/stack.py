@@ -690,6 +690,7 @@ class SourceStack:
         self.reg = None
         self.hs = None
         self.arena = None
+        self.base_host = None
         staging = None
         if transport == "registered":
             ptrs, sizes = [], []
@@ -711,8 +712,17 @@ class SourceStack:
                 ptrs = moved
                 k = len(host.descs)
                 self.srcs = [ptrs[hb * k:(hb + 1) * k] for hb in range(w.distinct)]
-            dlo.host_register_ranges(ptrs, sizes)
-            self.reg = (ptrs, sizes)
+                dlo.host_register_ranges(ptrs, sizes)
+                self.reg = (ptrs, sizes)
+            else:
+                # the tensors' own memory, registered once for all the stacks
+                # over this HostBlocks (a second registration of a range fails)
+                n = getattr(host, "_base_reg_users", 0)
+                if n == 0:
+                    dlo.host_register_ranges(ptrs, sizes)
+                    host._base_reg = (ptrs, sizes)
+                host._base_reg_users = n + 1
+                self.base_host = host
         else:
             self.hs = PinnedBuffer(2 * self.slot_bytes, defer=True)
             offs = self.hs.place_surveyed([self.slot_bytes, self.slot_bytes])
@@ -747,6 +757,11 @@ class SourceStack:
         if self.reg is not None:
             dlo.host_unregister_ranges(*self.reg)
             self.reg = None
+        if self.base_host is not None:
+            self.base_host._base_reg_users -= 1
+            if self.base_host._base_reg_users == 0:
+                dlo.host_unregister_ranges(*self.base_host._base_reg)
+            self.base_host = None
         if self.arena is not None:
             self.arena.close()
             self.arena = None

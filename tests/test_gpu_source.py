@@ -255,6 +255,9 @@ def test_source_stack_streams_like_resident(transport, pages):
                  shards=1, steps=2, distinct=12)
     host = HostBlocks(w, seed=12, keep_params=True)
     st = SourceStack(host, transport=transport, pages=pages)
+    # a second stack over the same sources (the bench builds two): base
+    # pages are registered once and shared, a huge-page arena is its own
+    SourceStack(host, transport=transport, pages=pages).close()
     if transport == "registered" and pages == "huge":
         assert st.arena is not None and st.arena.good_fraction() is not None
         assert st.srcs[3][0] != host.params[3]["norm1.weight"].data_ptr()
