@@ -84,6 +84,9 @@ def parse():
     ap.add_argument("--gemm-pair", default="auto", choices=["auto", "on", "off"],
                     help="GEMM kernel of the linears: by shape (auto), CTA pairs for all (on), "
                          "single CTAs for all (off)")
+    ap.add_argument("--launch-overlap", default="auto", choices=["auto", "on", "off"],
+                    help="programmatic dependent launch between the forward's kernels "
+                         "(auto: for blocks below 1e11 FLOPs)")
     ap.add_argument("--source", default="shards", choices=["shards", "pageable", "registered"],
                     help="shards: pinned host shards (default); pageable / registered: the "
                          "rank-local path with one shard, blocks by parameter address")
@@ -223,7 +226,7 @@ class ClockSampler:
                     timeout=10).stdout.splitlines()
             except (OSError, subprocess.SubprocessError):
                 pass
-        sm, smax, reasons = [], None, set()
+        sm, smax, reasons, power = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in lines:
             f = [x.strip() for x in line.split(",")]
@@ -234,11 +237,16 @@ class ClockSampler:
                 smax = float(f[2])
             except ValueError:
                 continue
+            try:
+                power.append(float(f[3]))
+            except ValueError:
+                pass
             for n, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         res = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-               "reasons": sorted(reasons), "samples": len(sm)}
+               "reasons": sorted(reasons), "samples": len(sm),
+               "power_w": statistics.median(power) if power else None}
         if adjacent:
             res["adjacent"] = "region shorter than the 200 ms sampling interval: samples " \
                               "taken just before and just after it"
@@ -407,7 +415,7 @@ def workload_config(w, args, ws=1):
                                                    w.heads, w.mlp, w.tokens, w.batch, w.shards,
                                                    w.steps),
             "name": w.name, "copy_mode": args.copy_mode, "host_source": args.source,
-            "gemm_pair": args.gemm_pair,
+            "gemm_pair": args.gemm_pair, "launch_overlap": args.launch_overlap,
             "l2": "streamed weights %.0f MB per step > 129 MB L2" % mb,
             "parallelism": "replicas" if ws > 1 else "single GPU"}
 
@@ -438,6 +446,7 @@ def h2d_ceiling_gbs(torch, nbytes=1 << 30, reps=10):
 def apply_gemm_pair(dlo, args):
     dlo.set_gemm_pair_mode({"auto": dlo.GEMM_PAIR_AUTO, "on": dlo.GEMM_PAIR_ON,
                             "off": dlo.GEMM_PAIR_OFF}[args.gemm_pair])
+    dlo.set_launch_overlap({"auto": -1, "on": 1, "off": 0}[args.launch_overlap])
 
 
 def run_ours(args, ws, rank, local):
@@ -582,7 +591,11 @@ def run_ours(args, ws, rank, local):
     rs.stream.wait_stream(cur)
     for _ in range(args.warmup):
         rs.step(xr)
+    clocks_r = ClockSampler(local)
+    if not args.no_clocks:
+        clocks_r.start()
     res_region_ms = timed_regions(lambda: rs.step(xr), rs.stream, sizes, ws)
+    clk_res = clocks_r.stop()
     rmed = median_region(sizes, res_region_ms)
     res_ms_step = res_region_ms[rmed] / sizes[rmed]
     exposed = ms_step - res_ms_step
@@ -768,6 +781,7 @@ def run_ours(args, ws, rank, local):
                              "shape": [M, K, N], "ms": lin_ms},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
         "clocks": clk,
+        "clocks_resident_pass": clk_res,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -851,7 +865,7 @@ def run_only(args):
     torch.cuda.synchronize()
     assert dlo.kernel_status() == 0
     print(json.dumps({"only": args.only, "config": args.config, "reps": args.reps,
-                      "gemm_pair": args.gemm_pair,
+                      "gemm_pair": args.gemm_pair, "launch_overlap": args.launch_overlap,
                       "ms_per_rep": e0.elapsed_time(e1) / args.reps}), flush=True)
 
 

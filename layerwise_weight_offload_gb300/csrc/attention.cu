@@ -218,6 +218,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dependency_sync();
   const uint32_t tS = tmem;             // S_t (and P_t) at column 128 t
   const uint32_t tO = tmem + 256;       // O_t at column 256 + HD t
 
@@ -530,6 +531,7 @@ __global__ void __launch_bounds__(256)
 attention_combine_kernel(const float* __restrict__ part_ws, int n_main, int n_split, int parts,
                          int nt, int tokens, int d, int heads, uint16_t* __restrict__ o) {
   constexpr int CPL = HD / 32;                      // columns per lane
+  grid_dependency_sync();
   const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t rows = static_cast<int64_t>(n_split) * nt * BQ;
@@ -611,18 +613,18 @@ dlo_status launch_hd(const CUtensorMap& tm_qk, const CUtensorMap& tm_vt, const A
   DLO_CUDA(g_att_err);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
   const int n_split = static_cast<int>(pl.items - pl.n_main);
-  attention_tc_kernel<HD><<<static_cast<unsigned>(pl.units), ATT_THREADS, AttLayout<HD>::SMEM,
-                            stream>>>(
-      tm_qk, tm_vt, static_cast<int>(tokens), static_cast<int>(d), static_cast<int>(heads), o,
-      scale_log2, pl.nt, static_cast<int>(pl.n_main), pl.parts, ws, err);
-  DLO_CUDA(cudaGetLastError());
+  DLO_CUDA(launch_kernel(attention_tc_kernel<HD>, dim3(static_cast<unsigned>(pl.units)),
+                         dim3(ATT_THREADS), AttLayout<HD>::SMEM, stream, 1, tm_qk, tm_vt,
+                         static_cast<int>(tokens), static_cast<int>(d), static_cast<int>(heads),
+                         o, scale_log2, pl.nt, static_cast<int>(pl.n_main), pl.parts, ws, err));
   if (n_split > 0) {
     const int64_t rows = static_cast<int64_t>(n_split) * pl.nt * BQ;
-    attention_combine_kernel<HD><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0,
-                                   stream>>>(
-        ws, static_cast<int>(pl.n_main), n_split, pl.parts, pl.nt, static_cast<int>(tokens),
-        static_cast<int>(d), static_cast<int>(heads), o);
-    DLO_CUDA(cudaGetLastError());
+    DLO_CUDA(launch_kernel(attention_combine_kernel<HD>,
+                           dim3(static_cast<unsigned>((rows * 32 + 255) / 256)), dim3(256), 0,
+                           stream, 1, static_cast<const float*>(ws),
+                           static_cast<int>(pl.n_main), n_split, pl.parts, pl.nt,
+                           static_cast<int>(tokens), static_cast<int>(d),
+                           static_cast<int>(heads), o));
   }
   return DLO_OK;
 }

@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "../../include/dlo.h"
@@ -194,6 +195,46 @@ dlo_status launch_transpose_v(const uint16_t* qkv, int64_t batch, int64_t tokens
 dlo_status make_tmap_2d(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols,
                         int64_t ld, uint32_t box_rows, uint32_t box_cols);
 int sm_count();
+
+// Launches of the block forward: inside a PdlScope(true) (this thread),
+// kernels are launched with programmatic stream serialization, so that a
+// kernel's CTAs may start their set-up while the previous kernel drains
+// (each waits for it in grid_dependency_wait/sync before touching memory).
+// cluster_x > 1 launches clusters of that many CTAs.
+bool pdl_active();
+struct PdlScope {
+  bool prev;
+  explicit PdlScope(bool on);
+  ~PdlScope();
+};
+int launch_overlap_mode();   // -1 by block size (default), 0 off, 1 on
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, int cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[2];
+  unsigned n = 0;
+  if (cluster_x > 1) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl_active()) {
+    at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // status.cu: device-side error word written by bounded waits
 int* device_error_word();  // device address (cached per device)

@@ -215,6 +215,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dependency_wait();
 
   const int num_m = (M + BM - 1) / BM;
   const int num_n = (N + BN - 1) / BN;
@@ -268,6 +269,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tma_a,
           }
         }
       }
+      // every load of this CTA is issued: the next kernel may launch
+      allow_dependent_launch();
       if (!ok) {
         // let the loads already issued land before the CTA's shared memory
         // can be handed to another CTA (bounded; no abort check)
@@ -475,6 +478,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dependency_wait();
 
   const int num_m = (M + BM2 - 1) / BM2;
   const int num_n = (N + BN - 1) / BN;
@@ -529,6 +533,8 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
           }
         }
       }
+      // every load of this CTA is issued: the next kernel may launch
+      allow_dependent_launch();
       if (!ok) {
         // loads already issued signal the even CTA's barriers; give them
         // time to land before the pair can exit (failure path only)
@@ -769,20 +775,9 @@ dlo_status launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, int M, int 
   const int tiles = ((M + BM2 - 1) / BM2) * ((N + BN - 1) / BN);
   const int units = tiles - tail + tail * tail_splits;
   const int clusters = units < g_pair_clusters ? units : g_pair_clusters;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(2 * clusters);
-  cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = PAIR_SMEM_BYTES;
-  cfg.stream = stream;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = 2;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  DLO_CUDA(cudaLaunchKernelEx(&cfg, gemm_pair_kernel<EPI>, ma, mb, M, N, K, tail, tail_splits,
-                              group_rows_pair(M, K), ea, err));
+  DLO_CUDA(launch_kernel(gemm_pair_kernel<EPI>, dim3(2 * clusters), dim3(NUM_THREADS),
+                         PAIR_SMEM_BYTES, stream, 2, ma, mb, M, N, K, tail, tail_splits,
+                         group_rows_pair(M, K), ea, err));
   return DLO_OK;
 }
 
@@ -796,9 +791,9 @@ dlo_status launch_epi(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int units = (tiles - tail) * splits + tail * tail_splits;
   const int grid = units < sm_count() ? units : sm_count();
-  gemm_tcgen05_kernel<EPI><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(
-      ma, mb, M, N, K, splits, tail, tail_splits, group_rows(M, K), ea, err);
-  DLO_CUDA(cudaGetLastError());
+  DLO_CUDA(launch_kernel(gemm_tcgen05_kernel<EPI>, dim3(grid), dim3(NUM_THREADS), SMEM_BYTES,
+                         stream, 1, ma, mb, M, N, K, splits, tail, tail_splits, group_rows(M, K),
+                         ea, err));
   return DLO_OK;
 }
 
@@ -866,6 +861,7 @@ template <int EPI>
 __global__ void __launch_bounds__(256)
 splitk_reduce_kernel(const float* __restrict__ ws, int splits, int64_t M, int64_t N,
                      const EpiArgs ea) {
+  grid_dependency_sync();
   const int64_t n4 = N / 4, total = M * n4;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -885,6 +881,7 @@ __global__ void __launch_bounds__(256)
 tail_reduce_kernel(const float* __restrict__ ws, int tail, int tail_splits, int num_tiles,
                    int num_m, int num_n, int group_m, int64_t M, int64_t N,
                    const EpiArgs ea) {
+  grid_dependency_sync();
   constexpr int64_t per_tile = static_cast<int64_t>(TM) * (BN / 4);
   const int64_t total = tail * per_tile;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -916,9 +913,9 @@ dlo_status launch_tail_reduce(const float* ws, int tail, int tail_splits, int64_
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   if (blocks > cap) blocks = cap;
   const int group_m = TM == BM ? group_rows(M, K) : group_rows_pair(M, K);
-  tail_reduce_kernel<EPI, TM><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      ws, tail, tail_splits, num_tiles, num_m, num_n, group_m, M, N, ea);
-  DLO_CUDA(cudaGetLastError());
+  DLO_CUDA(launch_kernel(tail_reduce_kernel<EPI, TM>, dim3(static_cast<unsigned>(blocks)),
+                         dim3(256), 0, stream, 1, ws, tail, tail_splits, num_tiles, num_m,
+                         num_n, group_m, M, N, ea));
   return DLO_OK;
 }
 
@@ -929,9 +926,8 @@ dlo_status launch_reduce(const float* ws, int splits, int64_t M, int64_t N, cons
   int64_t blocks = (total + 255) / 256;
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   if (blocks > cap) blocks = cap;
-  splitk_reduce_kernel<EPI><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ws, splits, M, N,
-                                                                               ea);
-  DLO_CUDA(cudaGetLastError());
+  DLO_CUDA(launch_kernel(splitk_reduce_kernel<EPI>, dim3(static_cast<unsigned>(blocks)),
+                         dim3(256), 0, stream, 1, ws, splits, M, N, ea));
   return DLO_OK;
 }
 

@@ -8,6 +8,7 @@
 #include <cuda_bf16.h>
 
 #include "common.h"
+#include "ptx.cuh"
 
 namespace dlo {
 namespace {
@@ -24,6 +25,7 @@ rmsnorm_mod_row_kernel(const float* __restrict__ x, int64_t d, const float* __re
                        const float* __restrict__ shift, const float* __restrict__ scale,
                        float eps, uint16_t* __restrict__ h) {
   __shared__ float part[kRowThreads / 32];
+  grid_dependency_sync();
   const int64_t row = blockIdx.x;
   const int n4 = static_cast<int>(d / 4);
   const int nt = blockDim.x;
@@ -71,6 +73,7 @@ __global__ void __launch_bounds__(kNormThreads)
 rmsnorm_mod_kernel(const float* __restrict__ x, int64_t rows, int64_t d,
                    const float* __restrict__ g, const float* __restrict__ shift,
                    const float* __restrict__ scale, float eps, uint16_t* __restrict__ h) {
+  grid_dependency_sync();
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -117,6 +120,7 @@ qk_norm_rope_kernel(uint16_t* __restrict__ qkv, int64_t rows, int tokens, int d,
                     const float* __restrict__ gq, const float* __restrict__ gk, float eps,
                     float log2_base) {
   constexpr int E = HD / 32;
+  grid_dependency_sync();
   const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= rows * heads * 2) return;                 // whole warps leave together
@@ -193,14 +197,13 @@ dlo_status launch_qk_norm_rope(uint16_t* qkv, int64_t batch, int64_t tokens, int
     DLO_FAIL(DLO_ERR_INVALID, "qk_norm_rope: too large");
   const float l2b = rope_base > 0.f ? log2f(rope_base) : 0.f;
   if (hd == 64)
-    qk_norm_rope_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        qkv, rows, static_cast<int>(tokens), static_cast<int>(d), static_cast<int>(heads), gq,
-        gk, eps, l2b);
+    DLO_CUDA(launch_kernel(qk_norm_rope_kernel<64>, dim3(static_cast<unsigned>(blocks)),
+                           dim3(256), 0, stream, 1, qkv, rows, static_cast<int>(tokens),
+                           static_cast<int>(d), static_cast<int>(heads), gq, gk, eps, l2b));
   else
-    qk_norm_rope_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        qkv, rows, static_cast<int>(tokens), static_cast<int>(d), static_cast<int>(heads), gq,
-        gk, eps, l2b);
-  DLO_CUDA(cudaGetLastError());
+    DLO_CUDA(launch_kernel(qk_norm_rope_kernel<128>, dim3(static_cast<unsigned>(blocks)),
+                           dim3(256), 0, stream, 1, qkv, rows, static_cast<int>(tokens),
+                           static_cast<int>(d), static_cast<int>(heads), gq, gk, eps, l2b));
   return DLO_OK;
 }
 
@@ -220,23 +223,17 @@ dlo_status launch_rmsnorm_mod(const float* x, int64_t rows, int64_t d, const flo
     if (rows > 0x7fffffffLL) DLO_FAIL(DLO_ERR_INVALID, "rmsnorm_mod: too many rows");
     const int nt = n4 >= kRowThreads ? kRowThreads : static_cast<int>((n4 + 31) / 32 * 32);
     const int64_t per = (n4 + nt - 1) / nt;   // float4s per thread, <= 8
-    const unsigned grid = static_cast<unsigned>(rows);
-    if (per <= 1)
-      rmsnorm_mod_row_kernel<1><<<grid, nt, 0, stream>>>(x, d, g, shift, scale, eps, h);
-    else if (per <= 2)
-      rmsnorm_mod_row_kernel<2><<<grid, nt, 0, stream>>>(x, d, g, shift, scale, eps, h);
-    else if (per <= 4)
-      rmsnorm_mod_row_kernel<4><<<grid, nt, 0, stream>>>(x, d, g, shift, scale, eps, h);
-    else
-      rmsnorm_mod_row_kernel<8><<<grid, nt, 0, stream>>>(x, d, g, shift, scale, eps, h);
-    DLO_CUDA(cudaGetLastError());
+    const dim3 grid(static_cast<unsigned>(rows)), block(static_cast<unsigned>(nt));
+    auto kern = per <= 1 ? rmsnorm_mod_row_kernel<1>
+                : per <= 2 ? rmsnorm_mod_row_kernel<2>
+                : per <= 4 ? rmsnorm_mod_row_kernel<4> : rmsnorm_mod_row_kernel<8>;
+    DLO_CUDA(launch_kernel(kern, grid, block, 0, stream, 1, x, d, g, shift, scale, eps, h));
     return DLO_OK;
   }
   const int64_t ctas = (rows + kRowsPerCta - 1) / kRowsPerCta;
   if (ctas > 0x7fffffffLL) DLO_FAIL(DLO_ERR_INVALID, "rmsnorm_mod: too many rows");
-  rmsnorm_mod_kernel<<<static_cast<unsigned>(ctas), kNormThreads, 0, stream>>>(
-      x, rows, d, g, shift, scale, eps, h);
-  DLO_CUDA(cudaGetLastError());
+  DLO_CUDA(launch_kernel(rmsnorm_mod_kernel, dim3(static_cast<unsigned>(ctas)),
+                         dim3(kNormThreads), 0, stream, 1, x, rows, d, g, shift, scale, eps, h));
   return DLO_OK;
 }
 

@@ -33,6 +33,31 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ---- programmatic dependent launch ----------------------------------------
+
+// Called by every thread of a CTA of the block forward's kernels after the
+// CTA's own set-up (barriers, tensor memory, descriptor prefetch) and before
+// its first global-memory access: waits until the grid it depends on (the
+// previous kernel in the stream, when launched with programmatic stream
+// serialization) has completed and its writes are visible — a no-op
+// otherwise — then allows the next grid to begin launching.
+__device__ __forceinline__ void grid_dependency_sync() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// The two halves separately, for persistent kernels: the wait after the
+// CTA's set-up, and the permission for the next grid to launch once this
+// CTA has little left to do (a next grid launched at once would keep CTAs
+// resident beside this one, waiting, for its whole run).  One thread of a
+// CTA is enough for the permission.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- mbarrier ------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

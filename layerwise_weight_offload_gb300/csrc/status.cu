@@ -70,7 +70,23 @@ int* device_error_word() {
   return g_addr[dev];
 }
 
+namespace {
+thread_local bool t_pdl_scope = false;
+int g_launch_overlap = -1;
+}  // namespace
+
+bool pdl_active() { return t_pdl_scope; }
+PdlScope::PdlScope(bool on) : prev(t_pdl_scope) { t_pdl_scope = on; }
+PdlScope::~PdlScope() { t_pdl_scope = prev; }
+int launch_overlap_mode() { return g_launch_overlap; }
+
 }  // namespace dlo
+
+extern "C" dlo_status dlo_set_launch_overlap(int32_t on) {
+  if (on < -1 || on > 1) DLO_FAIL(DLO_ERR_INVALID, "dlo_set_launch_overlap: -1, 0 or 1");
+  dlo::g_launch_overlap = on;
+  return DLO_OK;
+}
 
 extern "C" dlo_status dlo_kernel_status(int32_t* code) {
   if (!code) DLO_FAIL(DLO_ERR_INVALID, "dlo_kernel_status: null argument");

@@ -135,6 +135,7 @@ _SIGS = {
     "dlo_replace_block_shards": (c_i32, [c_vp, c_i32, _P(c_vp), c_i32]),
     "dlo_engine_destroy": (c_i32, [c_vp, c_i32]),
     "dlo_kernel_status": (c_i32, [_P(c_i32)]),
+    "dlo_set_launch_overlap": (c_i32, [c_i32]),
     "dlo_debug_wait_probe": (c_i32, [c_i32, c_i64, c_i64, _P(c_i64), _P(c_i32)]),
     "dlo_last_error": (ctypes.c_char_p, []),
     "dlo_version": (ctypes.c_char_p, []),
@@ -389,6 +390,12 @@ def debug_fake_host_register_log():
     _check(lib().dlo_debug_fake_host_register_log(buf, 256, ctypes.byref(n)),
            "dlo_debug_fake_host_register_log")
     return list(buf[:min(n.value, 256)])
+
+
+def set_launch_overlap(mode):
+    """True/1: always, False/0: never, -1: by block size (the default)."""
+    m = -1 if mode == -1 else (1 if mode else 0)
+    _check(lib().dlo_set_launch_overlap(m), "dlo_set_launch_overlap")
 
 
 def kernel_status():
