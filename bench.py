@@ -944,6 +944,8 @@ def run_sweep(args):
             w0 = W.CONFIGS["sweep-d%d-t256-s%d" % (d, s)]
             host = HostBlocks(w0, params=params)
             host.pretouch()
+            verify = host.verify()
+            bytes_hb = sum(g.shard_bytes * s for g in host.plan.groups())
             for T in [int(v) for v in args.sweep_t.split(",")]:
                 w = W.CONFIGS["sweep-d%d-t%d-s%d" % (d, T, s)]
                 host.w = w
@@ -952,10 +954,15 @@ def run_sweep(args):
                 steps = 3 if T < 16384 else 2
                 warm = 3
 
+                heal = bytes_hb >= 128 << 20
+
                 def timed_pass(timing):
                     # the step time without per-copy timing events (as the
-                    # stream runs in use); with them, the copy statistics
-                    stk = StreamedStack(host, copy_mode=dlo.COPY_AUTO, timing=timing)
+                    # stream runs in use; blocks of 128 MB or more heal, which
+                    # times every copy at no measurable cost); with them, the
+                    # copy statistics
+                    stk = StreamedStack(host, copy_mode=dlo.COPY_AUTO, timing=timing,
+                                        heal=heal)
                     stk.compute.wait_stream(cur)
                     for _ in range(warm):
                         stk.step(x)
@@ -970,6 +977,7 @@ def run_sweep(args):
                     return stk, nb, a.elapsed_time(b) / steps
 
                 st, _, ms = timed_pass(False)
+                moves = [list(m) for m in st.heal_log]
                 st.close()
                 st, n_before, _ = timed_pass(True)
                 cms, cby = st.engine.copy_times()
@@ -1008,7 +1016,9 @@ def run_sweep(args):
                     "block_roofline_fraction_sustained_peak": w.n_blocks * t_roof_s * 1e3 / ms,
                     "bound": "h2d" if t_link >= w.flops_per_block() / (bf16_peak * 1e12)
                     else "tensor",
-                    "copy_mode": chosen}), flush=True)
+                    "copy_mode": chosen, "copy_max_ms": max(cms) if cms else None,
+                    "host_verify_relocated": verify["relocated"],
+                    "heal_moves": moves + [list(m) for m in st.heal_log]}), flush=True)
                 del x, xr
                 torch.cuda.empty_cache()
             host.close()
