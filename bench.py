@@ -42,6 +42,11 @@ if ROOT not in sys.path:
 METRIC = "streamed block-fwd/s; H2D GB/s vs roofline; exposed transfer ms/step (1×GB300)"
 UNIT = "block-fwd/s"
 DEFAULT_CONFIG = "super"
+# DRAM bytes (read + written) per launch of fc2 from an ncu capture of that
+# shape (M, K, N, on CTA pairs): python bench.py --only fc2 --config super
+# --reps 3, then ncu --set full --clock-control none -k regex:gemm_pair -s 2
+# -c 1 on the same command (4.343 GB read, 0.194 GB written)
+FC2_DRAM_BYTES = {(8192, 24576, 6144, True): 4_343_431_000 + 194_273_024}
 REGIONS = 5          # timed regions per pass; value is the median region
 
 
@@ -613,24 +618,31 @@ def run_ours(args, ws, rank, local):
     roof_frac = (w.n_blocks * t_roof * 1e3) / ms_step
     roof_frac_sust = (w.n_blocks * max(t_link, t_comp_sust) * 1e3) / ms_step
 
-    # largest linear alone (fc1: T x d -> f), event-timed on its stream
-    M, K, N = w.batch * w.tokens, w.hidden, w.mlp
+    # fc2 alone (T x f -> d, gated residual), event-timed on its stream: the
+    # top kernel of the step's launch list on the large workloads (its
+    # operands, 403 MB of A at Super, exceed L2)
+    M, K, N = w.batch * w.tokens, w.mlp, w.hidden
     a = torch.randn(M, K, device="cuda").to(torch.bfloat16)
     wt = (0.02 * torch.randn(N, K, device="cuda")).to(torch.bfloat16)
-    out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    xr2 = torch.randn(M, N, device="cuda")
+    gate = 0.1 * torch.randn(N, device="cuda")
+    nws = dlo.op_linear_workspace_bytes(M, N, K, dlo.EPI_RESID_F32)
+    lws = torch.empty(max(nws, 16), dtype=torch.uint8, device="cuda")
     ls = torch.cuda.Stream()
     ls.wait_stream(cur)
     for _ in range(3):
-        dlo.op_linear(a, M, K, wt, N, dlo.EPI_GELU_BF16, out, None, ls)
+        dlo.op_linear(a, M, K, wt, N, dlo.EPI_RESID_F32, xr2, gate, ls, lws, nws)
     l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     reps = 20
     l0.record(ls)
     for _ in range(reps):
-        dlo.op_linear(a, M, K, wt, N, dlo.EPI_GELU_BF16, out, None, ls)
+        dlo.op_linear(a, M, K, wt, N, dlo.EPI_RESID_F32, xr2, gate, ls, lws, nws)
     l1.record(ls)
     torch.cuda.synchronize()
     lin_ms = l0.elapsed_time(l1) / reps
     lin_tflops = 2.0 * M * K * N / (lin_ms * 1e-3) / 1e12
+    lin_pair = bool(dlo.op_linear_on_pairs(M, N, K, dlo.EPI_RESID_F32))
+    del a, wt, xr2, lws
 
     # end to end through the public API: x in from pinned host, result out
     e2e = None
@@ -708,12 +720,35 @@ def run_ours(args, ws, rank, local):
                          % (n, text, el),
                **oracle_extras(w, args.seed)}
 
+    # the dominant operation: the block's host->device copy where the link
+    # bounds the step, else the top GEMM (fc2) timed alone
+    roof_h2d = {"name": None, "bound": "h2d", "peak": ceiling, "unit": "GB/s",
+                "traffic": None,
+                "peak_source": "pinned cudaMemcpyAsync 1 GiB ceiling measured in this run",
+                "bytes_per_launch": bytes_per_block,
+                "timing": "CUDA events around every prefetch of the timed steps "
+                          "(copy_stats_pass); busy time per block"}
+    fc2_traffic = FC2_DRAM_BYTES.get((M, K, N, lin_pair))
+    roof_gemm = {"name": ("gemm_pair_kernel<2>" if lin_pair else "gemm_tcgen05_kernel<2>")
+                 + " (fc2, gated residual)", "bound": "tensor", "achieved": lin_tflops,
+                 "peak": bf16_peak, "unit": "TFLOP/s", "frac": lin_tflops / bf16_peak,
+                 "traffic": fc2_traffic,
+                 "traffic_note": ("dram__bytes_read.sum + dram__bytes_write.sum per launch, "
+                                  "from an ncu capture of this shape" if fc2_traffic
+                                  else "no ncu capture of this shape"),
+                 "flops_per_launch": 2 * M * K * N, "algorithmic_bytes_per_launch":
+                     2 * M * K + 2 * N * K + 8 * M * N,
+                 "peak_source": peak_src + " burst bf16 (the kernel is timed alone)",
+                 "shape": [M, K, N], "ms": lin_ms,
+                 "timing": "20 back-to-back launches alone on one stream, CUDA events"}
     copy_name = {"kernel": "copy_reassemble_kernel",
                  "staged": "cudaMemcpyAsync into staging (copy engines), then a device gather"}.get(
         chosen, "cudaMemcpyAsync (copy engines)")
     # per launch: one block's bytes over the busy time per block
     achieved = (sum(copy_bytes) / len(copy_bytes)) / (busy_ms / len(copy_ms) * 1e6) \
         if copy_ms and busy_ms > 0 else None
+    roof_h2d.update(name=copy_name, achieved=achieved,
+                    frac=achieved / ceiling if achieved else None)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -767,18 +802,9 @@ def run_ours(args, ws, rank, local):
                          max(1, stats1.n_packed_prefetches - stats0.n_packed_prefetches)}
                         if args.source != "shards" else None),
         "copy_ms_all": copy_ms if args.dump_copies else None,
-        "roofline": {"name": copy_name, "bound": "h2d", "achieved": achieved,
-                     "peak": ceiling, "unit": "GB/s",
-                     "frac": achieved / ceiling if achieved else None, "traffic": None,
-                     "peak_source": "pinned cudaMemcpyAsync 1 GiB ceiling measured in this run",
-                     "bytes_per_launch": bytes_per_block},
-        "roofline_compute": {"name": ("gemm_pair_kernel" if dlo.op_linear_on_pairs(
-                                 M, N, K, dlo.EPI_GELU_BF16) else "gemm_tcgen05_kernel")
-                             + " (fc1, GELU epilogue)",
-                             "bound": "tensor", "achieved": lin_tflops, "peak": bf16_peak,
-                             "unit": "TFLOP/s", "frac": lin_tflops / bf16_peak,
-                             "traffic": None, "peak_source": peak_src + " burst bf16",
-                             "shape": [M, K, N], "ms": lin_ms},
+        "roofline": roof_h2d if t_link >= t_comp else roof_gemm,
+        "roofline_h2d": roof_h2d,
+        "roofline_compute": roof_gemm,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
         "clocks": clk,
         "clocks_resident_pass": clk_res,
