@@ -657,7 +657,9 @@ typedef struct {
   int64_t bytes;        /* bytes moved */
 } dlo_copy_record;
 
-/* Incremental, non-blocking read of the timing record: copies to buf, in
+/* Incremental, non-blocking read of the timing record ([B1] "Overlap
+ * Analysis" reads prefetch against compute time per block from the run's
+ * log; this is that record, per prefetch): copies to buf, in
  * order, up to `cap` records of timed prefetches with seq >= since whose
  * copies have completed, stopping at the first one still in flight;
  * *n_out = how many, *next = the seq to pass as `since` next time.  Records
@@ -706,7 +708,10 @@ dlo_status dlo_debug_wait_probe(int32_t spin, int64_t limit_ns, int64_t abort_ns
  * -1 (default) for blocks below 1e11 FLOPs only (measured on GB300: 2% off
  * a 1024-hidden, 1024-token block's forward; 1.5% slower on the
  * 6144-hidden, 8192-token one).  The forward's cached CUDA graphs are keyed
- * on the resulting choice.  DLO_ERR_INVALID unless -1, 0 or 1. */
+ * on the resulting choice.  The pages have no counterpart (their forward is
+ * a framework's; [B2] "Validation Results" counts its Python dispatch and
+ * stream switches as overhead, which this launch path and the graphs
+ * address).  DLO_ERR_INVALID unless -1, 0 or 1. */
 dlo_status dlo_set_launch_overlap(int32_t on);
 
 /* Message of the last failed call on this thread ("" if none). */
