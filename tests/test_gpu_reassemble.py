@@ -28,6 +28,18 @@ def _expected_image(host, hb):
     return image
 
 
+def _assert_only_groups_written(got, groups, shards, fill, where):
+    """Canary check: every byte outside the groups' gathered ranges (the
+    gaps up to each 256-aligned group base, and past the last group) still
+    holds the fill pattern."""
+    mask = np.zeros(got.size, dtype=bool)
+    for g in groups:
+        mask[g.base:g.base + shards * g.shard_bytes] = True
+    bad = np.nonzero((~mask) & (got != fill))[0]
+    assert bad.size == 0, "%s: %d bytes outside the groups written, first at %d" % (
+        where, bad.size, int(bad[0]))
+
+
 @pytest.mark.parametrize("mode", [dlo.COPY_DMA, dlo.COPY_KERNEL])
 @pytest.mark.parametrize("name", ["tiny", "odd"])
 def test_workload_slot_bit_exact(name, mode):
@@ -42,11 +54,11 @@ def test_workload_slot_bit_exact(name, mode):
         s.synchronize()
         got = dst.cpu().numpy()
         exp = _expected_image(host, hb)
-        # compare every group's gathered range (gaps between groups untouched)
+        # every group's gathered range equals the image; nothing else written
         for g in host.plan.groups():
             n = w.shards * g.shard_bytes
             assert np.array_equal(got[g.base:g.base + n], exp[g.base:g.base + n]), (hb, g.dtype)
-        assert (got[info.slot_bytes:] == 0xA5).all()     # nothing written past the slot
+        _assert_only_groups_written(got, host.plan.groups(), w.shards, 0xA5, (name, hb))
     host.close()
 
 
@@ -90,7 +102,7 @@ def test_misaligned_shards_bit_exact(mode):
             assert np.array_equal(got[g.base:g.base + n], exp[g.base:g.base + n]), (trial, s)
             if g.shard_bytes % 16:
                 n_cases += 1
-        assert (got[info.slot_bytes:] == 0x5A).all()
+        _assert_only_groups_written(got, groups, s, 0x5A, (trial, s))
         buf.close()
     assert n_cases > 10        # the misaligned paths were exercised
 
@@ -124,7 +136,7 @@ def test_staged_reassembly_bit_exact(name, same_stream):
                 off = g.stage_base + r * g.shard_alloc_bytes
                 assert np.array_equal(st[off:off + g.shard_bytes],
                                       views[gi * w.shards + r][:g.shard_bytes].numpy())
-        assert (got[info.slot_bytes:] == 0xA5).all()
+        _assert_only_groups_written(got, host.plan.groups(), w.shards, 0xA5, (name, hb))
     with pytest.raises(dlo.DLOError):
         dlo.reassemble_staged(host.plan, host.shard_ptrs(0), staging, info.staging_bytes - 16,
                               dst, cs, gs)
