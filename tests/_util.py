@@ -38,3 +38,16 @@ def assert_oracle_close(gpu, ref, what="", max_rel=2e-2, mean_rel=5e-3):
     assert mean_err <= mean_rel * mean_ref + 1e-30, \
         "%s: mean err %.3e > %.1e * %.3e" % (what, mean_err, mean_rel, mean_ref)
     return mx / max(scale, 1e-30), mean_err / max(mean_ref, 1e-30)
+
+
+def assert_only_groups_written(got, groups, shards, fill, where=""):
+    """Canary check of a slot: every byte outside the groups' gathered ranges
+    (the gaps up to each 256-aligned group base, and past the last group)
+    still holds the fill pattern."""
+    got = np.asarray(got)
+    mask = np.zeros(got.size, dtype=bool)
+    for g in groups:
+        mask[g.base:g.base + shards * g.shard_bytes] = True
+    bad = np.nonzero((~mask) & (got != fill))[0]
+    assert bad.size == 0, "%s: %d bytes outside the groups written, first at %d" % (
+        where, bad.size, int(bad[0]))

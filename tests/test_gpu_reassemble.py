@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from tests._util import build_lib, raw_bytes
+from tests._util import build_lib, raw_bytes, assert_only_groups_written
 from layerwise_weight_offload_gb300 import dlo, workloads as W
 from layerwise_weight_offload_gb300.stack import HostBlocks, PinnedBuffer
 
@@ -28,18 +28,6 @@ def _expected_image(host, hb):
     return image
 
 
-def _assert_only_groups_written(got, groups, shards, fill, where):
-    """Canary check: every byte outside the groups' gathered ranges (the
-    gaps up to each 256-aligned group base, and past the last group) still
-    holds the fill pattern."""
-    mask = np.zeros(got.size, dtype=bool)
-    for g in groups:
-        mask[g.base:g.base + shards * g.shard_bytes] = True
-    bad = np.nonzero((~mask) & (got != fill))[0]
-    assert bad.size == 0, "%s: %d bytes outside the groups written, first at %d" % (
-        where, bad.size, int(bad[0]))
-
-
 @pytest.mark.parametrize("mode", [dlo.COPY_DMA, dlo.COPY_KERNEL])
 @pytest.mark.parametrize("name", ["tiny", "odd"])
 def test_workload_slot_bit_exact(name, mode):
@@ -58,7 +46,7 @@ def test_workload_slot_bit_exact(name, mode):
         for g in host.plan.groups():
             n = w.shards * g.shard_bytes
             assert np.array_equal(got[g.base:g.base + n], exp[g.base:g.base + n]), (hb, g.dtype)
-        _assert_only_groups_written(got, host.plan.groups(), w.shards, 0xA5, (name, hb))
+        assert_only_groups_written(got, host.plan.groups(), w.shards, 0xA5, (name, hb))
     host.close()
 
 
@@ -102,7 +90,7 @@ def test_misaligned_shards_bit_exact(mode):
             assert np.array_equal(got[g.base:g.base + n], exp[g.base:g.base + n]), (trial, s)
             if g.shard_bytes % 16:
                 n_cases += 1
-        _assert_only_groups_written(got, groups, s, 0x5A, (trial, s))
+        assert_only_groups_written(got, groups, s, 0x5A, (trial, s))
         buf.close()
     assert n_cases > 10        # the misaligned paths were exercised
 
@@ -136,7 +124,7 @@ def test_staged_reassembly_bit_exact(name, same_stream):
                 off = g.stage_base + r * g.shard_alloc_bytes
                 assert np.array_equal(st[off:off + g.shard_bytes],
                                       views[gi * w.shards + r][:g.shard_bytes].numpy())
-        _assert_only_groups_written(got, host.plan.groups(), w.shards, 0xA5, (name, hb))
+        assert_only_groups_written(got, host.plan.groups(), w.shards, 0xA5, (name, hb))
     with pytest.raises(dlo.DLOError):
         dlo.reassemble_staged(host.plan, host.shard_ptrs(0), staging, info.staging_bytes - 16,
                               dst, cs, gs)

@@ -13,7 +13,8 @@ import pytest
 import torch
 
 import oracle
-from tests._util import build_lib, raw_bytes, params_f32, assert_oracle_close
+from tests._util import (build_lib, raw_bytes, params_f32, assert_oracle_close,
+                         assert_only_groups_written)
 from layerwise_weight_offload_gb300 import dlo, workloads as W
 from layerwise_weight_offload_gb300.stack import HostBlocks, StreamedStack, ResidentStack
 
@@ -54,6 +55,9 @@ def test_schedule_and_slot_contents(n_blocks, steps, mode, two_streams):
     host = HostBlocks(w, seed=5, keep_params=True)
     st = StreamedStack(host, copy_mode=mode, two_copy_streams=two_streams)
     images = [_slot_image(host, hb) for hb in range(w.distinct)]
+    for sl in st.slots:
+        sl.fill_(0xA5)                         # canary: prefetches write only the groups
+    torch.cuda.synchronize()
     st.prime()
     snaps = []
     groups = host.plan.groups()
@@ -75,6 +79,7 @@ def test_schedule_and_slot_contents(n_blocks, steps, mode, two_streams):
         for g in groups:
             n = w.shards * g.shard_bytes
             assert np.array_equal(got[g.base:g.base + n], exp[g.base:g.base + n]), (i, g.dtype)
+        assert_only_groups_written(got, groups, w.shards, 0xA5, i)
     stats = st.engine.query()
     assert stats.n_forwards == n_blocks * steps
     assert stats.n_prefetches == n_blocks * steps + 1
