@@ -489,6 +489,14 @@ typedef struct {
                              counted as dropped, so a serving loop of any
                              length holds constant memory.  0 = 65536;
                              at most 2^24 */
+  int32_t poison;         /* debugging: 1 = after each forward, overwrite the
+                             slot it read with the byte 0xA5 on the compute
+                             stream, before the slot's free event, so that a
+                             forward reading a slot the schedule has
+                             released, or one not yet refilled, sees garbage
+                             rather than a plausible stale block.  Costs one
+                             device memset of the slot per forward; 0 (the
+                             default) = off */
 } dlo_engine_desc;
 
 typedef struct {

@@ -184,6 +184,7 @@ struct dlo_engine {
   int32_t mode = DLO_COPY_AUTO;
   int32_t copy_ctas = 0;
   bool timing = false;
+  bool poison = false;               // debugging: 0xA5 over each slot after its forward
   std::vector<Block> blocks;
   std::vector<Hook> hooks;
   cudaEvent_t ready[2] = {nullptr, nullptr};
@@ -749,6 +750,7 @@ dlo_status dlo_engine_create(const dlo_engine_desc* d, dlo_engine** out) {
   e->mode = d->copy_mode;
   e->copy_ctas = d->copy_ctas;
   e->timing = d->timing != 0;
+  e->poison = d->poison != 0;
   e->fan = d->dma_streams == 0 ? 1 : d->dma_streams;
   const size_t log_cap = d->log_capacity > 0 ? static_cast<size_t>(d->log_capacity)
                                              : static_cast<size_t>(kDefaultLogCapacity);
@@ -1044,6 +1046,9 @@ dlo_status dlo_post_forward(dlo_engine* e, int32_t block) {
   DLO_TRY(check_engine(e));
   if (!e->in_forward || block != e->cur_block)
     DLO_FAIL(DLO_ERR_STATE, "dlo_post_forward: block %d is not the block in flight", block);
+  if (e->poison)
+    DLO_CUDA(cudaMemsetAsync(e->slot[e->cur_slot], 0xA5, static_cast<size_t>(e->slot_bytes),
+                             e->compute));
   DLO_CUDA(cudaEventRecord(e->freed[e->cur_slot], e->compute));
   if (e->chosen < 0) {
     const int64_t s0 = race_start(e->n_blocks);

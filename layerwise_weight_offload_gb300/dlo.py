@@ -67,7 +67,7 @@ class EngineDesc(ctypes.Structure):
                 ("staging", c_vp * 2), ("staging_bytes", c_i64), ("gather_stream", c_vp),
                 ("host_staging", c_vp * 2), ("host_staging_bytes", c_i64),
                 ("pack_threads", c_i32), ("two_copy_streams", c_i32),
-                ("log_capacity", c_i32)]
+                ("log_capacity", c_i32), ("poison", c_i32)]
 
 
 class SchedEvent(ctypes.Structure):
@@ -420,7 +420,7 @@ class Engine:
                  copy_mode=COPY_AUTO, copy_ctas=0, timing=False, dma_streams=0,
                  staging=None, staging_bytes=0, gather_stream=None, host_staging=None,
                  host_staging_bytes=0, pack_threads=0, two_copy_streams=False,
-                 log_capacity=0):
+                 log_capacity=0, poison=False):
         """staging: two device buffers (and gather_stream) for COPY_STAGED;
         host_staging: two page-locked host buffers for rank-local source
         blocks whose parameters are pageable."""
@@ -447,6 +447,7 @@ class Engine:
         d.pack_threads = int(pack_threads)
         d.two_copy_streams = 1 if two_copy_streams else 0
         d.log_capacity = int(log_capacity)
+        d.poison = 1 if poison else 0
         h = c_vp()
         _check(lib().dlo_engine_create(ctypes.byref(d), ctypes.byref(h)), "dlo_engine_create")
         self.handle = h.value

@@ -584,7 +584,8 @@ class StreamedStack:
     """Two slots and the hook schedule: the path the pages describe."""
 
     def __init__(self, host: HostBlocks, copy_mode=dlo.COPY_AUTO, copy_ctas=0, timing=False,
-                 device="cuda", two_copy_streams=False, log_capacity=0, heal=False):
+                 device="cuda", two_copy_streams=False, log_capacity=0, heal=False,
+                 poison=False):
         """heal: watch every prefetch's copy time (the engine times each
         one) and, between steps, move host blocks whose copies have turned
         slow to fresh host ranges (CopyHealer, HostBlocks.relocate_block,
@@ -609,7 +610,7 @@ class StreamedStack:
                                  self.compute, self.copy, copy_mode, copy_ctas, timing,
                                  staging=self.staging, staging_bytes=staging_bytes,
                                  gather_stream=self.gather, two_copy_streams=two_copy_streams,
-                                 log_capacity=log_capacity)
+                                 log_capacity=log_capacity, poison=poison)
         for i in range(w.n_blocks):
             self.engine.register_block(i, self.plan, host.shard_ptrs(i % w.distinct))
         self.cfg = dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,

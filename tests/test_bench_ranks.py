@@ -52,3 +52,24 @@ def test_region_split_and_median():
     # rates 1, 4, 2, 5, 3 steps/ms: the median region is the one at 3
     sizes, ms = [2, 4, 2, 5, 3], [2.0, 1.0, 1.0, 1.0, 1.0]
     assert bench.median_region(sizes, ms) == 4
+
+
+def test_oracle_sample_share_is_the_pieces_flops(monkeypatch):
+    # the bounded oracle baseline: above the threshold a block is sampled as
+    # 1/H of it and counted by the piece's share of the block's FLOPs
+    import numpy as np
+    import bench
+    from layerwise_weight_offload_gb300 import workloads as W
+    w = W.custom("samp", n_blocks=1, hidden=128, heads=2, mlp=512, tokens=64, shards=1)
+    monkeypatch.setattr(bench, "FULL_ORACLE_FLOPS", 0)
+    run, share, text, threads = bench.oracle_sample(w)
+    d, f, T, hd, r = 128, 512, 64, 64, 32
+    flops = 2 * T * d * 3 * hd + 4 * T * T * hd + 2 * r * (d * d + 2 * d * f)
+    assert abs(share - flops / w.flops_per_block()) < 1e-12
+    out = run()
+    assert out.shape == (r, d) and np.isfinite(out).all()
+    assert "1/2 of an fp64 oracle block forward" in text
+    monkeypatch.setattr(bench, "FULL_ORACLE_FLOPS", 1e30)
+    run, share, text, _ = bench.oracle_sample(w)
+    assert share == 1.0 and text.startswith("one fp64 oracle block forward")
+    run()

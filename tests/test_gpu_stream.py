@@ -416,3 +416,37 @@ def test_copy_spans(two_streams):
             assert s1 >= e0 - 1e-3
     st.close()
     host.close()
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("n_blocks,steps", [(1, 3), (9, 3)])
+def test_poisoned_slots_stream_like_resident(n_blocks, steps, mode):
+    # with every slot overwritten by 0xA5 right after the forward that read
+    # it, a forward that read a released or not-yet-refilled slot would see
+    # garbage: the streamed output must still equal the resident one bit for
+    # bit (one block: both slots hold it; nine: the odd-count wrap)
+    w = W.custom("poison", n_blocks=n_blocks, hidden=256, heads=4, mlp=1024, tokens=96,
+                 shards=3, steps=steps, distinct=min(n_blocks, 3))
+    host = HostBlocks(w, seed=13)
+    x0 = W.gen_x(w, seed=13)
+    st = StreamedStack(host, copy_mode=mode, poison=True)
+    xs = x0.clone().cuda()
+    st.compute.wait_stream(torch.cuda.current_stream())
+    for _ in range(steps):
+        st.step(xs)
+    torch.cuda.current_stream().wait_stream(st.compute)
+    torch.cuda.synchronize()
+    # the last slot read now holds the poison
+    last = (n_blocks * steps - 1) % 2
+    assert (st.slots[last][:st.plan.info().slot_bytes] == 0xA5).all()
+    st.close()
+    rs = ResidentStack(host)
+    xr = x0.clone().cuda()
+    rs.stream.wait_stream(torch.cuda.current_stream())
+    for _ in range(steps):
+        rs.step(xr)
+    torch.cuda.current_stream().wait_stream(rs.stream)
+    torch.cuda.synchronize()
+    assert torch.isfinite(xs).all()
+    assert torch.equal(xs, xr)
+    host.close()
