@@ -201,6 +201,45 @@ dlo_status dlo_plan_param(const dlo_plan* plan, int32_t param, dlo_param_info* o
  * Errors: DLO_ERR_INVALID on null pointers. */
 dlo_status dlo_shard_host(const dlo_plan* plan, const void* const* param_src,
                           void* const* shard_dst);
+
+/* One copy of a prefetch, by offsets: `bytes` bytes of shard (group,
+ * shard) from src_offset to dst_offset of the copy's target. */
+typedef struct {
+  int32_t group;
+  int32_t shard;
+  int64_t dst_offset;  /* bytes from the start of the target (slot or staging) */
+  int64_t src_offset;  /* bytes from the start of the host shard, or (a
+                          gather) from the start of the staging buffer */
+  int64_t bytes;
+} dlo_copy_piece;
+
+typedef enum {
+  DLO_PIECES_SLOT_FROM_SHARDS = 0,   /* DMA / copy kernel: host shards -> slot */
+  DLO_PIECES_STAGING_FROM_SHARDS = 1,/* staged phase 1: host shards -> staging */
+  DLO_PIECES_SLOT_FROM_STAGING = 2   /* staged phase 2: staging -> slot */
+} dlo_pieces_phase;
+
+/* Checks one prefetch's copies against the plan: the layout of [B2] §2
+ * (shard r of group g holds the group's flat elements [r*S_g, (r+1)*S_g))
+ * placed as all_gather_into_tensor places it (shard r at base_g +
+ * r*shard_bytes_g of the slot; in staging at stage_base_g +
+ * r*shard_alloc_bytes_g).  Every piece must
+ *   - name a valid (group, shard) and move at least one byte;
+ *   - read inside its shard: bytes [x, x+bytes) with 0 <= x and x+bytes <=
+ *     shard_bytes (into a slot) or shard_alloc_bytes (into staging), where
+ *     x = src_offset, or for a gather src_offset minus the shard's staging
+ *     offset;
+ *   - write exactly where those bytes belong in the target, and inside its
+ *     target_bytes;
+ * no two pieces may write the same byte, and every byte [0, shard_bytes) of
+ * every shard must be copied.
+ * bad (optional) receives the first failing piece's index, or -1 (a shard
+ * not fully copied, or no failure).
+ * Errors: DLO_ERR_INVALID on null pointers or an unknown phase;
+ * DLO_ERR_STATE when a rule fails (dlo_last_error names the piece and the
+ * rule). */
+dlo_status dlo_check_pieces(const dlo_plan* plan, int32_t phase, const dlo_copy_piece* pieces,
+                            int32_t n, int64_t target_bytes, int32_t* bad);
 void dlo_plan_destroy(dlo_plan* plan);
 
 /* ------------------------------------------------------------------------
@@ -497,6 +536,17 @@ typedef struct {
                              rather than a plausible stale block.  Costs one
                              device memset of the slot per forward; 0 (the
                              default) = off */
+  int32_t checks;         /* debugging: 1 = every prefetch of a block
+                             registered by shards first lists its copies
+                             without issuing them (DMA pieces, the rows of
+                             2-D copies, copy-kernel segments, staged H2D and
+                             gather) and checks their offsets with
+                             dlo_check_pieces; a prefetch that fails is not
+                             issued and returns DLO_ERR_STATE.  dlo_param_view
+                             also checks that the view lies inside its
+                             group's gathered elements and the slot.  Host
+                             work only (a few microseconds a prefetch);
+                             0 (the default) = off */
 } dlo_engine_desc;
 
 typedef struct {
@@ -643,6 +693,7 @@ typedef struct {
                                   groups, STAGED gathers */
   int64_t log_dropped;         /* schedule-log entries overwritten (full ring) */
   int64_t timed_dropped;       /* timing entries overwritten (full ring) */
+  int64_t checked_pieces;      /* copies checked before issue (desc.checks) */
 } dlo_engine_stats;
 dlo_status dlo_engine_query(dlo_engine* e, dlo_engine_stats* out);
 dlo_status dlo_engine_copy_times(dlo_engine* e, float* copy_ms, int64_t* copy_bytes,

@@ -70,7 +70,7 @@ def build(verbose=False, ptxas_info=False, force=False):
     if (not os.path.exists(LIB) or force
             or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs)):
         tmp = LIB + ".tmp%d" % os.getpid()
-        cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
+        cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-ldl"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed: %s\n%s%s" % (" ".join(cmd), r.stdout, r.stderr))

@@ -29,6 +29,7 @@
 #include <thread>
 
 #include "common.h"
+#include "trace.h"
 
 namespace dlo {
 dlo_status forward_impl(const dlo_dit_cfg* cfg, const dlo_plan* plan, const void* block_base,
@@ -185,6 +186,8 @@ struct dlo_engine {
   int32_t copy_ctas = 0;
   bool timing = false;
   bool poison = false;               // debugging: 0xA5 over each slot after its forward
+  bool checks = false;               // debugging: offsets of every copy checked before issue
+  int64_t checked_pieces = 0;
   std::vector<Block> blocks;
   std::vector<Hook> hooks;
   cudaEvent_t ready[2] = {nullptr, nullptr};
@@ -257,6 +260,24 @@ constexpr int32_t kDefaultLogCapacity = 65536;
 constexpr int kRaceWindows = 4;
 inline int64_t race_start(int32_t n_blocks) { return static_cast<int64_t>(n_blocks) + 2; }
 
+// With desc.checks, a prefetch's copies are first listed here by offsets
+// (into `target`, from each piece's own shard or from staging) instead of
+// issued, and checked against the plan with dlo_check_pieces.
+struct DryRun {
+  std::vector<dlo_copy_piece> pieces;
+  const uint8_t* target = nullptr;
+  void add(int32_t g, int32_t r, const void* dst, const void* src, const void* src_base,
+           int64_t bytes) {
+    dlo_copy_piece q;
+    q.group = g;
+    q.shard = r;
+    q.dst_offset = static_cast<const uint8_t*>(dst) - target;
+    q.src_offset = static_cast<const uint8_t*>(src) - static_cast<const uint8_t*>(src_base);
+    q.bytes = bytes;
+    pieces.push_back(q);
+  }
+};
+
 dlo_status build_segments(const dlo_engine::Block& b, uint8_t* dst, SegmentTable* t) {
   const dlo_plan* p = b.plan;
   const int32_t s = p->n_shards;
@@ -313,7 +334,7 @@ dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, in
                       cudaStream_t stream, int fan, cudaStream_t* aux, cudaEvent_t fork_ev,
                       cudaEvent_t* join_ev, cudaStream_t side = nullptr,
                       cudaEvent_t side_fork = nullptr, cudaEvent_t side_join = nullptr,
-                      int64_t* launches = nullptr) {
+                      int64_t* launches = nullptr, DryRun* dry = nullptr) {
   const dlo_plan* p = b.plan;
   const int32_t s = p->n_shards;
   if (mode == DLO_COPY_KERNEL) {
@@ -321,6 +342,11 @@ dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, in
       DLO_FAIL(DLO_ERR_INVALID, "prefetch: a shard is not device-mapped pinned memory");
     SegmentTable t;
     DLO_TRY(build_segments(b, dst, &t));
+    if (dry) {
+      for (int32_t i = 0; i < t.n; ++i)
+        dry->add(i / s, i % s, t.seg[i].dst, t.seg[i].src, b.dev[i], t.seg[i].bytes);
+      return DLO_OK;
+    }
     if (launches) ++*launches;
     return launch_copy_reassemble(t, ctas, stream);
   }
@@ -337,9 +363,10 @@ dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, in
         sg.src = b.dev[g * s + r];
         sg.dst = dst + grp.base + static_cast<int64_t>(r) * grp.shard_bytes;
         sg.bytes = grp.shard_bytes;
+        if (dry) dry->add(static_cast<int32_t>(g), r, sg.dst, sg.src, b.dev[g * s + r], sg.bytes);
       }
     }
-    if (t.n > 0) {
+    if (t.n > 0 && !dry) {
       DLO_CUDA(cudaEventRecord(side_fork, stream));
       DLO_CUDA(cudaStreamWaitEvent(side, side_fork, 0));
       DLO_TRY(launch_copy_reassemble(t, 1, side));
@@ -353,6 +380,15 @@ dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, in
     const auto& grp = p->groups[g];
     if (by_kernel[g]) continue;
     if (fan <= 1 && !b.pitch.empty() && b.pitch[g] > 0) {
+      if (dry) {
+        // a linear copy (pitch = shard bytes) or a 2-D copy: row r of it
+        for (int32_t r = 0; r < s; ++r)
+          dry->add(static_cast<int32_t>(g), r,
+                   dst + grp.base + static_cast<int64_t>(r) * grp.shard_bytes,
+                   static_cast<const uint8_t*>(b.host[g * s]) + r * b.pitch[g],
+                   b.host[g * s + r], grp.shard_bytes);
+        continue;
+      }
       if (b.pitch[g] == grp.shard_bytes) {
         // the shards are back to back in host memory: one linear copy
         DLO_CUDA(cudaMemcpyAsync(dst + grp.base, b.host[g * s],
@@ -367,10 +403,15 @@ dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, in
       }
       continue;
     }
-    for (int32_t r = 0; r < s; ++r)
+    for (int32_t r = 0; r < s; ++r) {
       pieces.push_back({dst + grp.base + static_cast<int64_t>(r) * grp.shard_bytes,
                         b.host[g * s + r], grp.shard_bytes});
+      if (dry)
+        dry->add(static_cast<int32_t>(g), r, pieces.back().dst, pieces.back().src,
+                 b.host[g * s + r], grp.shard_bytes);
+    }
   }
+  if (dry) return DLO_OK;
   auto join_side = [&]() -> dlo_status {
     for (size_t g = 0; g < by_kernel.size(); ++g)
       if (by_kernel[g]) {
@@ -412,7 +453,8 @@ dlo_status copy_block(const dlo_engine::Block& b, uint8_t* dst, int32_t mode, in
 // stage_base_g + r * shard_alloc_bytes (16-byte aligned).  A group whose
 // host shards sit at a constant stride moves as one 2-D copy (one linear
 // copy when that stride equals the staging stride).
-dlo_status stage_h2d(const dlo_engine::Block& b, uint8_t* staging, cudaStream_t stream) {
+dlo_status stage_h2d(const dlo_engine::Block& b, uint8_t* staging, cudaStream_t stream,
+                     DryRun* dry = nullptr) {
   const dlo_plan* p = b.plan;
   const int32_t s = p->n_shards;
   for (size_t g = 0; g < p->groups.size(); ++g) {
@@ -420,6 +462,15 @@ dlo_status stage_h2d(const dlo_engine::Block& b, uint8_t* staging, cudaStream_t 
     uint8_t* d0 = staging + grp.stage_base;
     const int64_t sp = grp.shard_alloc_bytes;
     const int64_t hp = b.pitch.empty() ? 0 : b.pitch[g];
+    if (dry) {
+      // row r of the linear (hp = sp) or 2-D copy, or the per-shard copy
+      const uint8_t* h0 = static_cast<const uint8_t*>(b.host[g * s]);
+      for (int32_t r = 0; r < s; ++r)
+        dry->add(static_cast<int32_t>(g), r, d0 + r * sp,
+                 hp > 0 ? h0 + r * hp : b.host[g * s + r], b.host[g * s + r],
+                 hp == sp ? sp : grp.shard_bytes);
+      continue;
+    }
     if (hp == sp) {
       DLO_CUDA(cudaMemcpyAsync(d0, b.host[g * s], static_cast<size_t>(sp) * s,
                                cudaMemcpyHostToDevice, stream));
@@ -442,7 +493,7 @@ dlo_status stage_h2d(const dlo_engine::Block& b, uint8_t* staging, cudaStream_t 
 // (group base + r * shard_bytes), i.e. the concatenation in rank order that
 // all_gather_into_tensor produces.
 dlo_status stage_gather(const dlo_plan* p, const uint8_t* staging, uint8_t* dst, int ctas,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, DryRun* dry = nullptr) {
   const int32_t s = p->n_shards;
   SegmentTable t;
   t.n = 0;
@@ -456,8 +507,10 @@ dlo_status stage_gather(const dlo_plan* p, const uint8_t* staging, uint8_t* dst,
       sg.src = staging + grp.stage_base + static_cast<int64_t>(r) * grp.shard_alloc_bytes;
       sg.dst = dst + grp.base + static_cast<int64_t>(r) * grp.shard_bytes;
       sg.bytes = grp.shard_bytes;
+      if (dry) dry->add(static_cast<int32_t>(g), r, sg.dst, sg.src, staging, sg.bytes);
     }
   }
+  if (dry) return DLO_OK;
   return launch_copy_reassemble(t, ctas, stream);
 }
 
@@ -575,7 +628,10 @@ dlo_status prefetch_source(dlo_engine* e, int32_t block, int32_t slot) {
       for (int64_t o = 0; o < s.bytes; o += static_cast<int64_t>(kPiece))
         tasks.push_back({e->host_staging[slot] + s.off + o, s.p + o,
                          static_cast<size_t>(std::min<int64_t>(kPiece, s.bytes - o))});
-    e->pool->run(tasks);
+    {
+      TraceRange pack("pack", block);
+      e->pool->run(tasks);
+    }
     e->pack_ms += std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0)
                       .count();
     DLO_CUDA(cudaStreamWaitEvent(cs, e->freed[slot], 0));
@@ -593,9 +649,39 @@ dlo_status prefetch_source(dlo_engine* e, int32_t block, int32_t slot) {
   return DLO_OK;
 }
 
+// desc.checks: lists the copies a prefetch of `b` into `slot` in `mode`
+// would issue (nothing is issued) and checks their offsets against the
+// plan; the prefetch is refused if one fails.
+dlo_status check_prefetch(dlo_engine* e, const dlo_engine::Block& b, int32_t slot,
+                          int32_t mode) {
+  int32_t bad = -1;
+  if (mode == DLO_COPY_STAGED) {
+    DryRun h2d, gather;
+    h2d.target = e->staging[slot];
+    gather.target = e->slot[slot];
+    DLO_TRY(stage_h2d(b, e->staging[slot], nullptr, &h2d));
+    DLO_TRY(stage_gather(b.plan, e->staging[slot], e->slot[slot], 0, nullptr, &gather));
+    DLO_TRY(dlo_check_pieces(b.plan, DLO_PIECES_STAGING_FROM_SHARDS, h2d.pieces.data(),
+                             static_cast<int32_t>(h2d.pieces.size()), e->staging_bytes, &bad));
+    DLO_TRY(dlo_check_pieces(b.plan, DLO_PIECES_SLOT_FROM_STAGING, gather.pieces.data(),
+                             static_cast<int32_t>(gather.pieces.size()), e->slot_bytes, &bad));
+    e->checked_pieces += static_cast<int64_t>(h2d.pieces.size() + gather.pieces.size());
+    return DLO_OK;
+  }
+  DryRun d;
+  d.target = e->slot[slot];
+  DLO_TRY(copy_block(b, e->slot[slot], mode, e->copy_ctas, nullptr, e->fan, e->aux, e->fork_ev,
+                     e->join_ev, e->side, e->side_fork, e->side_join, nullptr, &d));
+  DLO_TRY(dlo_check_pieces(b.plan, DLO_PIECES_SLOT_FROM_SHARDS, d.pieces.data(),
+                           static_cast<int32_t>(d.pieces.size()), e->slot_bytes, &bad));
+  e->checked_pieces += static_cast<int64_t>(d.pieces.size());
+  return DLO_OK;
+}
+
 // Enqueues the prefetch of `block` into `slot` on the copy stream.
 dlo_status enqueue_prefetch(dlo_engine* e, int32_t block, int32_t slot, int64_t issued_by_k,
                             int32_t* used_mode = nullptr) {
+  TraceRange range(slot ? "prefetch slot 1" : "prefetch slot 0", block);
   const dlo_engine::Block& b = e->blocks[block];
   cudaStream_t cs = e->slot_copy[slot];
   if (b.source) {
@@ -604,6 +690,7 @@ dlo_status enqueue_prefetch(dlo_engine* e, int32_t block, int32_t slot, int64_t 
   }
   const int32_t mode = mode_for(e, issued_by_k, b);
   if (used_mode) *used_mode = mode;
+  if (e->checks) DLO_TRY(check_prefetch(e, b, slot, mode));
   if (mode == DLO_COPY_STAGED) {
     // H2D into staging[slot] once the gather that last read it is done;
     // the gather then waits for the H2D and for the slot's free event
@@ -751,6 +838,7 @@ dlo_status dlo_engine_create(const dlo_engine_desc* d, dlo_engine** out) {
   e->copy_ctas = d->copy_ctas;
   e->timing = d->timing != 0;
   e->poison = d->poison != 0;
+  e->checks = d->checks != 0;
   e->fan = d->dma_streams == 0 ? 1 : d->dma_streams;
   const size_t log_cap = d->log_capacity > 0 ? static_cast<size_t>(d->log_capacity)
                                              : static_cast<size_t>(kDefaultLogCapacity);
@@ -881,6 +969,7 @@ dlo_status dlo_replace_block_shards(dlo_engine* e, int32_t block,
   if (!cur.plan || cur.source)
     DLO_FAIL(DLO_ERR_STATE, "dlo_replace_block_shards: block %d has no registered shards",
              block);
+  TraceRange range("replace_block_shards", block);
   dlo_engine::Block b;
   DLO_TRY(shard_table("dlo_replace_block_shards", cur.plan, shard_ptrs, &b));
   if (e->mode == DLO_COPY_KERNEL && !all_mapped(b))
@@ -964,6 +1053,7 @@ dlo_status dlo_wait(dlo_engine* e, int32_t block) {
 dlo_status dlo_wait_host(dlo_engine* e, int32_t block, int32_t timeout_ms) {
   using namespace dlo;
   DLO_TRY(check_engine(e));
+  TraceRange range("wait_host", block);
   const int32_t s = slot_of(e, block);
   if (s < 0) DLO_FAIL(DLO_ERR_STATE, "dlo_wait_host: block %d is in no slot", block);
   const auto t0 = std::chrono::steady_clock::now();
@@ -992,6 +1082,19 @@ dlo_status dlo_param_view(const dlo_engine* e, int32_t block, int32_t param, voi
     DLO_FAIL(DLO_ERR_INVALID, "dlo_param_view: param %d out of range", param);
   const int32_t s = slot_of(e, block);
   if (s < 0) DLO_FAIL(DLO_ERR_STATE, "dlo_param_view: block %d is in no slot", block);
+  if (e->checks) {
+    // the view's bytes: its elements' place in the flat group, which lies
+    // inside the group's gathered elements and the slot
+    const auto& q = p->params[param];
+    const auto& grp = p->groups[q.group];
+    const int64_t lo = q.slot_offset, hi = lo + q.storage_numel * grp.esize;
+    if (lo != grp.base + q.group_offset * grp.esize || q.group_offset < 0 ||
+        q.group_offset + q.storage_numel > grp.numel || hi > e->slot_bytes)
+      DLO_FAIL(DLO_ERR_STATE, "dlo_param_view: param %d's bytes [%lld, %lld) are not its "
+               "elements [%lld, %lld) of group %d at base %lld", param, (long long)lo,
+               (long long)hi, (long long)q.group_offset,
+               (long long)(q.group_offset + q.storage_numel), q.group, (long long)grp.base);
+  }
   *dev_ptr = e->slot[s] + p->params[param].slot_offset;
   return DLO_OK;
 }
@@ -999,6 +1102,7 @@ dlo_status dlo_param_view(const dlo_engine* e, int32_t block, int32_t param, voi
 dlo_status dlo_pre_forward(dlo_engine* e, int32_t block, int32_t* slot_out) {
   using namespace dlo;
   DLO_TRY(check_engine(e));
+  TraceRange range("pre_forward", block);
   if (e->in_forward)
     DLO_FAIL(DLO_ERR_STATE, "dlo_pre_forward: block %d has no post_forward yet", e->cur_block);
   const int32_t n = e->n_blocks;
@@ -1044,6 +1148,7 @@ dlo_status dlo_pre_forward(dlo_engine* e, int32_t block, int32_t* slot_out) {
 dlo_status dlo_post_forward(dlo_engine* e, int32_t block) {
   using namespace dlo;
   DLO_TRY(check_engine(e));
+  TraceRange range("post_forward", block);
   if (!e->in_forward || block != e->cur_block)
     DLO_FAIL(DLO_ERR_STATE, "dlo_post_forward: block %d is not the block in flight", block);
   if (e->poison)
@@ -1070,6 +1175,7 @@ dlo_status dlo_block_forward(dlo_engine* e, int32_t block, const dlo_dit_cfg* cf
                              void* scratch, size_t scratch_bytes) {
   using namespace dlo;
   DLO_TRY(check_engine(e));
+  TraceRange range("block_forward", block);
   int32_t slot = -1;
   DLO_TRY(dlo_pre_forward(e, block, &slot));
   const dlo_status st = forward_impl(cfg, e->blocks[block].plan, e->slot[slot], x, scratch,
@@ -1110,6 +1216,7 @@ dlo_status dlo_engine_query(dlo_engine* e, dlo_engine_stats* out) {
   out->n_copy_kernel_launches = static_cast<int32_t>(e->n_copy_launches);
   out->log_dropped = e->log.dropped();
   out->timed_dropped = e->timed.dropped();
+  out->checked_pieces = e->checked_pieces;
   return DLO_OK;
 }
 
@@ -1188,6 +1295,7 @@ dlo_status dlo_engine_copy_log(dlo_engine* e, int64_t since, dlo_copy_record* bu
 dlo_status dlo_engine_destroy(dlo_engine* e, int32_t timeout_ms) {
   using namespace dlo;
   if (!e) return DLO_OK;
+  TraceRange range("engine_destroy", e->n_blocks);
   // drain the streams (bounded): mark their current tails and poll
   cudaEvent_t tail[4] = {nullptr, nullptr, nullptr, nullptr};
   cudaStream_t st[4] = {e->copy, e->compute, nullptr, nullptr};
@@ -1237,6 +1345,7 @@ dlo_status dlo_reassemble(const dlo_plan* plan, const void* const* shard_ptrs, v
                           int32_t mode, void* stream) {
   using namespace dlo;
   if (!plan || !shard_ptrs || !dst) DLO_FAIL(DLO_ERR_INVALID, "dlo_reassemble: null argument");
+  TraceRange range("reassemble", plan->slot_bytes);
   if (reinterpret_cast<uintptr_t>(dst) & 255u)
     DLO_FAIL(DLO_ERR_INVALID, "dlo_reassemble: dst must be 256-byte aligned");
   const size_t n = plan->groups.size() * static_cast<size_t>(plan->n_shards);
@@ -1274,6 +1383,7 @@ dlo_status dlo_reassemble_staged(const dlo_plan* plan, const void* const* shard_
   using namespace dlo;
   if (!plan || !shard_ptrs || !staging || !dst)
     DLO_FAIL(DLO_ERR_INVALID, "dlo_reassemble_staged: null argument");
+  TraceRange range("reassemble_staged", plan->slot_bytes);
   if ((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(staging)) & 255u)
     DLO_FAIL(DLO_ERR_INVALID, "dlo_reassemble_staged: dst and staging must be 256-byte aligned");
   if (staging_bytes < plan->staging_bytes)

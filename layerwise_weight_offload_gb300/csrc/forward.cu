@@ -17,6 +17,7 @@
 #include <utility>
 
 #include "common.h"
+#include "trace.h"
 
 namespace dlo {
 namespace {
@@ -275,6 +276,7 @@ dlo_status preload_kernels() {
 dlo_status forward_impl(const dlo_dit_cfg* cfg, const dlo_plan* plan, const void* block_base,
                         float* x, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
   DLO_TRY(check_cfg(cfg));
+  TraceRange range("forward", static_cast<int64_t>(cfg->batch) * cfg->tokens);
   DLO_TRY(check_plan(*cfg, plan));
   const ScratchLayout sl = scratch_layout(*cfg);
   if (!block_base || !x || !scratch) DLO_FAIL(DLO_ERR_INVALID, "forward: null pointer");

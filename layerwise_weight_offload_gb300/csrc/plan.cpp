@@ -18,6 +18,7 @@
 #include <new>
 
 #include "common.h"
+#include "trace.h"
 
 namespace dlo {
 
@@ -35,6 +36,11 @@ void set_error(const char* fmt, ...) {
 }
 
 void clear_error() { g_last_error.clear(); }
+
+nvtxDomainHandle_t trace_domain() {
+  static const nvtxDomainHandle_t d = nvtxDomainCreateA("dlo");
+  return d;
+}
 
 const char* const kRoleNames[R_COUNT] = {
     "norm1.weight", "ada1.shift", "ada1.scale", "ada1.gate",
@@ -77,6 +83,7 @@ const char* dlo_version(void) { return "dlo-gb300 0.1 (sm_103a)"; }
 dlo_status dlo_plan_create(const dlo_param_desc* params, int32_t n_params,
                            int32_t n_shards, dlo_plan** out) {
   using namespace dlo;
+  dlo::TraceRange range("plan_create", n_params);
   if (!params || !out) DLO_FAIL(DLO_ERR_INVALID, "dlo_plan_create: null argument");
   if (n_params < 1) DLO_FAIL(DLO_ERR_INVALID, "dlo_plan_create: n_params must be >= 1");
   if (n_shards < 1) DLO_FAIL(DLO_ERR_INVALID, "dlo_plan_create: n_shards must be >= 1");
@@ -215,6 +222,7 @@ dlo_status dlo_shard_host(const dlo_plan* plan, const void* const* param_src,
                           void* const* shard_dst) {
   if (!plan || !param_src || !shard_dst)
     DLO_FAIL(DLO_ERR_INVALID, "dlo_shard_host: null argument");
+  dlo::TraceRange range("shard_host", static_cast<int64_t>(plan->params.size()));
   const int32_t s = plan->n_shards;
   for (size_t g = 0; g < plan->groups.size(); ++g)
     for (int32_t r = 0; r < s; ++r)
@@ -245,6 +253,84 @@ dlo_status dlo_shard_host(const dlo_plan* plan, const void* const* param_src,
       left -= run;
     }
   }
+  return DLO_OK;
+}
+
+dlo_status dlo_check_pieces(const dlo_plan* plan, int32_t phase, const dlo_copy_piece* pieces,
+                            int32_t n, int64_t target_bytes, int32_t* bad) {
+  if (bad) *bad = -1;
+  if (!plan || n < 0 || (n > 0 && !pieces))
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_check_pieces: null argument or negative count");
+  if (phase < DLO_PIECES_SLOT_FROM_SHARDS || phase > DLO_PIECES_SLOT_FROM_STAGING)
+    DLO_FAIL(DLO_ERR_INVALID, "dlo_check_pieces: unknown phase %d", phase);
+  const int32_t s = plan->n_shards;
+  const int32_t n_groups = static_cast<int32_t>(plan->groups.size());
+  const bool into_staging = phase == DLO_PIECES_STAGING_FROM_SHARDS;
+  // per (group, shard): the byte ranges of the shard that some piece copies
+  std::vector<std::vector<std::pair<int64_t, int64_t>>> covered(
+      static_cast<size_t>(n_groups) * s);
+  std::vector<std::pair<int64_t, int32_t>> by_dst;   // (dst_offset, piece)
+  by_dst.reserve(static_cast<size_t>(n));
+  for (int32_t i = 0; i < n; ++i) {
+    const dlo_copy_piece& q = pieces[i];
+    if (q.group < 0 || q.group >= n_groups || q.shard < 0 || q.shard >= s || q.bytes <= 0) {
+      if (bad) *bad = i;
+      DLO_FAIL(DLO_ERR_STATE, "dlo_check_pieces: piece %d names group %d / shard %d with %lld "
+               "bytes (the plan has %d groups of %d shards)", i, q.group, q.shard,
+               (long long)q.bytes, n_groups, s);
+    }
+    const auto& grp = plan->groups[q.group];
+    const int64_t r = q.shard;
+    const int64_t staged_at = grp.stage_base + r * grp.shard_alloc_bytes;
+    const int64_t x = phase == DLO_PIECES_SLOT_FROM_STAGING ? q.src_offset - staged_at
+                                                            : q.src_offset;
+    const int64_t limit = into_staging ? grp.shard_alloc_bytes : grp.shard_bytes;
+    if (x < 0 || x + q.bytes > limit) {
+      if (bad) *bad = i;
+      DLO_FAIL(DLO_ERR_STATE, "dlo_check_pieces: piece %d (group %d, shard %d) reads shard bytes "
+               "[%lld, %lld) of %lld", i, q.group, q.shard, (long long)x,
+               (long long)(x + q.bytes), (long long)limit);
+    }
+    const int64_t want = into_staging ? staged_at + x : grp.base + r * grp.shard_bytes + x;
+    if (q.dst_offset != want) {
+      if (bad) *bad = i;
+      DLO_FAIL(DLO_ERR_STATE, "dlo_check_pieces: piece %d (group %d, shard %d) writes at byte "
+               "%lld; those shard bytes belong at %lld", i, q.group, q.shard,
+               (long long)q.dst_offset, (long long)want);
+    }
+    if (q.dst_offset < 0 || q.dst_offset + q.bytes > target_bytes) {
+      if (bad) *bad = i;
+      DLO_FAIL(DLO_ERR_STATE, "dlo_check_pieces: piece %d writes [%lld, %lld), past the "
+               "target's %lld bytes", i, (long long)q.dst_offset,
+               (long long)(q.dst_offset + q.bytes), (long long)target_bytes);
+    }
+    covered[static_cast<size_t>(q.group) * s + q.shard].push_back(
+        {x, std::min(x + q.bytes, grp.shard_bytes)});
+    by_dst.push_back({q.dst_offset, i});
+  }
+  std::sort(by_dst.begin(), by_dst.end());
+  for (size_t j = 1; j < by_dst.size(); ++j) {
+    const dlo_copy_piece& a = pieces[by_dst[j - 1].second];
+    if (a.dst_offset + a.bytes > by_dst[j].first) {
+      if (bad) *bad = by_dst[j].second;
+      DLO_FAIL(DLO_ERR_STATE, "dlo_check_pieces: pieces %d and %d both write byte %lld",
+               by_dst[j - 1].second, by_dst[j].second, (long long)by_dst[j].first);
+    }
+  }
+  for (int32_t g = 0; g < n_groups; ++g)
+    for (int32_t r = 0; r < s; ++r) {
+      auto& iv = covered[static_cast<size_t>(g) * s + r];
+      std::sort(iv.begin(), iv.end());
+      int64_t end = 0;
+      for (const auto& v : iv) {
+        if (v.first > end) break;
+        end = std::max(end, v.second);
+      }
+      if (end < plan->groups[g].shard_bytes)
+        DLO_FAIL(DLO_ERR_STATE, "dlo_check_pieces: group %d shard %d: bytes from %lld of %lld "
+                 "are not copied", g, r, (long long)end,
+                 (long long)plan->groups[g].shard_bytes);
+    }
   return DLO_OK;
 }
 

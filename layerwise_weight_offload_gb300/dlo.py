@@ -67,7 +67,7 @@ class EngineDesc(ctypes.Structure):
                 ("staging", c_vp * 2), ("staging_bytes", c_i64), ("gather_stream", c_vp),
                 ("host_staging", c_vp * 2), ("host_staging_bytes", c_i64),
                 ("pack_threads", c_i32), ("two_copy_streams", c_i32),
-                ("log_capacity", c_i32), ("poison", c_i32)]
+                ("log_capacity", c_i32), ("poison", c_i32), ("checks", c_i32)]
 
 
 class SchedEvent(ctypes.Structure):
@@ -86,7 +86,15 @@ class EngineStats(ctypes.Structure):
                 ("race_kernel_us", ctypes.c_double), ("n_direct_prefetches", c_i32),
                 ("n_packed_prefetches", c_i32), ("pack_ms", ctypes.c_double),
                 ("n_copy_kernel_launches", c_i32), ("log_dropped", c_i64),
-                ("timed_dropped", c_i64)]
+                ("timed_dropped", c_i64), ("checked_pieces", c_i64)]
+
+
+class CopyPiece(ctypes.Structure):
+    _fields_ = [("group", c_i32), ("shard", c_i32), ("dst_offset", c_i64),
+                ("src_offset", c_i64), ("bytes", c_i64)]
+
+
+PIECES_SLOT_FROM_SHARDS, PIECES_STAGING_FROM_SHARDS, PIECES_SLOT_FROM_STAGING = 0, 1, 2
 
 
 _P = ctypes.POINTER
@@ -96,6 +104,7 @@ _SIGS = {
     "dlo_plan_group": (c_i32, [c_vp, c_i32, _P(GroupInfo)]),
     "dlo_plan_param": (c_i32, [c_vp, c_i32, _P(ParamInfo)]),
     "dlo_shard_host": (c_i32, [c_vp, _P(c_vp), _P(c_vp)]),
+    "dlo_check_pieces": (c_i32, [c_vp, c_i32, _P(CopyPiece), c_i32, c_i64, _P(c_i32)]),
     "dlo_plan_destroy": (None, [c_vp]),
     "dlo_reassemble": (c_i32, [c_vp, _P(c_vp), c_vp, c_i32, c_vp]),
     "dlo_reassemble_staged": (c_i32, [c_vp, _P(c_vp), c_vp, c_i64, c_vp, c_vp, c_vp]),
@@ -271,6 +280,24 @@ def plan_create(descs, n_shards):
     return Plan(descs, n_shards)
 
 
+def check_pieces(plan, phase, pieces, target_bytes):
+    """Checks one prefetch's copies, given as (group, shard, dst_offset,
+    src_offset, bytes) tuples, against the plan.  Returns None if they pass;
+    otherwise (index of the first failing piece or -1, message)."""
+    arr = (CopyPiece * max(1, len(pieces)))()
+    for i, q in enumerate(pieces):
+        arr[i] = CopyPiece(*[int(v) for v in q])
+    bad = c_i32(-2)
+    st = lib().dlo_check_pieces(plan.handle, int(phase), arr, len(pieces), int(target_bytes),
+                                ctypes.byref(bad))
+    if st == OK:
+        assert bad.value == -1
+        return None
+    if st != ERR_STATE:
+        _check(st, "dlo_check_pieces")
+    return bad.value, last_error()
+
+
 def reassemble(plan, shard_ptrs, dst, mode=COPY_DMA, stream=None):
     _check(lib().dlo_reassemble(plan.handle, _ptrs(shard_ptrs), _ptr(dst), int(mode),
                                 _stream(stream)), "dlo_reassemble")
@@ -420,7 +447,7 @@ class Engine:
                  copy_mode=COPY_AUTO, copy_ctas=0, timing=False, dma_streams=0,
                  staging=None, staging_bytes=0, gather_stream=None, host_staging=None,
                  host_staging_bytes=0, pack_threads=0, two_copy_streams=False,
-                 log_capacity=0, poison=False):
+                 log_capacity=0, poison=False, checks=False):
         """staging: two device buffers (and gather_stream) for COPY_STAGED;
         host_staging: two page-locked host buffers for rank-local source
         blocks whose parameters are pageable."""
@@ -448,6 +475,7 @@ class Engine:
         d.two_copy_streams = 1 if two_copy_streams else 0
         d.log_capacity = int(log_capacity)
         d.poison = 1 if poison else 0
+        d.checks = 1 if checks else 0
         h = c_vp()
         _check(lib().dlo_engine_create(ctypes.byref(d), ctypes.byref(h)), "dlo_engine_create")
         self.handle = h.value

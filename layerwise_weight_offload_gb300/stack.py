@@ -585,11 +585,13 @@ class StreamedStack:
 
     def __init__(self, host: HostBlocks, copy_mode=dlo.COPY_AUTO, copy_ctas=0, timing=False,
                  device="cuda", two_copy_streams=False, log_capacity=0, heal=False,
-                 poison=False):
+                 poison=False, checks=False):
         """heal: watch every prefetch's copy time (the engine times each
         one) and, between steps, move host blocks whose copies have turned
         slow to fresh host ranges (CopyHealer, HostBlocks.relocate_block,
-        dlo_replace_block_shards)."""
+        dlo_replace_block_shards).  poison, checks: the engine's debugging
+        options (slots overwritten after each forward; every copy's offsets
+        checked against the plan before it is issued)."""
         w = host.w
         timing = timing or heal
         self.w, self.host, self.plan = w, host, host.plan
@@ -610,7 +612,7 @@ class StreamedStack:
                                  self.compute, self.copy, copy_mode, copy_ctas, timing,
                                  staging=self.staging, staging_bytes=staging_bytes,
                                  gather_stream=self.gather, two_copy_streams=two_copy_streams,
-                                 log_capacity=log_capacity, poison=poison)
+                                 log_capacity=log_capacity, poison=poison, checks=checks)
         for i in range(w.n_blocks):
             self.engine.register_block(i, self.plan, host.shard_ptrs(i % w.distinct))
         self.cfg = dlo.dit_cfg(w.batch, w.tokens, w.hidden, w.heads, w.mlp, w.eps,
