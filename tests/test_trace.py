@@ -59,8 +59,7 @@ torch.cuda.synchronize()
 for _ in range(2):
     st.step(x)
 torch.cuda.synchronize()
-log = [(e.k, e.block, e.read_slot, e.prefetch_block, e.prefetch_slot)
-       for e in st.engine.schedule_log()]
+log = [list(e[:5]) for e in st.engine.schedule_log()]   # k, block, read, prefetch block/slot
 st.engine.wait_host(0, 10000)
 st.close()
 host.close()
