@@ -4,7 +4,9 @@ an fp8 weight with an e8m0 block scale, each contiguous or a transposed
 view, packed in physical order; "Validation coverage": heterogeneous-block
 regression tests).  Every slot the compute stream reads holds the oracle's
 image of its block byte for byte, the schedule is the oracle's, and a
-transposed view rebuilt over the slot equals the original tensor."""
+transposed view rebuilt over the slot equals the original tensor.  The
+engine runs with its `checks` option: every prefetch's copies pass the
+offset checks against their block's plan before they are issued."""
 import numpy as np
 import pytest
 import torch
@@ -82,7 +84,8 @@ def test_heterogeneous_blocks_stream_exact(mode, shards):
         staging = [torch.empty(staging_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
         gather = torch.cuda.Stream()
     e = dlo.Engine(n_blocks, slots[0], slots[1], slot_bytes, compute, copy, mode,
-                   staging=staging, staging_bytes=staging_bytes, gather_stream=gather)
+                   staging=staging, staging_bytes=staging_bytes, gather_stream=gather,
+                   checks=True)
     for b in range(n_blocks):
         e.register_block(b, plans[b], ptrs[b])
     e.prefetch(0, 0)
@@ -96,6 +99,10 @@ def test_heterogeneous_blocks_stream_exact(mode, shards):
         snaps.append((i, snap))
         e.post_forward(i)
     torch.cuda.synchronize()
+    fetched = [0] + [(k + 1) % n_blocks for k in range(n_blocks * steps)]
+    per_phase = 2 if mode == dlo.COPY_STAGED else 1
+    assert e.query().checked_pieces == per_phase * shards * sum(
+        plans[b].info().n_groups for b in fetched)
     log = e.schedule_log()
     ref = oracle.schedule(n_blocks, steps)
     assert [tuple(x[:6]) for x in log] == [tuple(int(v) for v in r[:6]) for r in ref]
