@@ -460,7 +460,8 @@ def run_ours(args, ws, rank, local):
     B.build()
     from layerwise_weight_offload_gb300 import dlo, workloads as W
     apply_gemm_pair(dlo, args)
-    from layerwise_weight_offload_gb300.stack import HostBlocks, StreamedStack, ResidentStack
+    from layerwise_weight_offload_gb300.stack import (HostBlocks, StreamedStack, ResidentStack,
+                                                      PinnedIO)
 
     torch.cuda.set_device(local)
     w = W.CONFIGS[args.config]
@@ -654,14 +655,23 @@ def run_ours(args, ws, rank, local):
         # the weight stream's copy queue (between the block copies, rather
         # than beside them on a second host-to-device queue); the result
         # returns on a data stream (the other direction of the link).
-        xh = torch.empty_like(x0, device="cpu").pin_memory()
+        # the step's input and its two result buffers in the library's
+        # huge-page pinned memory, each copy direction checked (PinnedIO)
+        xb = x0.numel() * x0.element_size()
+        io = PinnedIO(xb, 3)
+        io_rates = io.verify(0.5 * ceiling)
+        xh = io.tensor(0, x0.shape, x0.dtype)
         xh.copy_(x0.cpu())
-        yh = [torch.empty_like(xh).pin_memory() for _ in range(2)]
+        yh = [io.tensor(1 + i, x0.shape, x0.dtype) for i in range(2)]
         xd = [torch.empty_like(x) for _ in range(2)]
         data = torch.cuda.Stream()
         h2d_ev = [torch.cuda.Event() for _ in range(2)]
         done_ev = [torch.cuda.Event() for _ in range(2)]
         rb_ev = [torch.cuda.Event() for _ in range(2)]
+        # timing events around every input copy and result read-back
+        io_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                 for _ in range(args.steps)]
+        step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
         in_q = st.copy if hasattr(st, "copy") else data
         # untimed: one step on each device buffer, so that the forward's cached
         # CUDA graphs for these buffers exist before the timed region
@@ -673,18 +683,28 @@ def run_ours(args, ws, rank, local):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         barrier(ws)
+        clocks_e = ClockSampler(local)
+        if not args.no_clocks:
+            clocks_e.start()
         e0.record(in_q)
         with torch.cuda.stream(in_q):
+            io_ev[0][0].record(in_q)
             xd[0].copy_(xh, non_blocking=True)
+            io_ev[0][1].record(in_q)
         h2d_ev[0].record(in_q)
         for s in range(args.steps):
             b = s & 1
             st.compute.wait_event(h2d_ev[b])
+            if s == 0:
+                step_ev[0].record(st.compute)
             st.step(xd[b])
             done_ev[b].record(st.compute)
+            step_ev[s + 1].record(st.compute)
             with torch.cuda.stream(data):
                 data.wait_event(done_ev[b])
+                io_ev[s][2].record(data)
                 yh[b].copy_(xd[b], non_blocking=True)
+                io_ev[s][3].record(data)
                 rb_ev[b].record(data)
             if s + 1 < args.steps:
                 # the other buffer's last reader was step s-1: its result
@@ -692,19 +712,39 @@ def run_ours(args, ws, rank, local):
                 with torch.cuda.stream(in_q):
                     if s >= 1:
                         in_q.wait_event(rb_ev[b ^ 1])
+                    io_ev[s + 1][0].record(in_q)
                     xd[b ^ 1].copy_(xh, non_blocking=True)
+                    io_ev[s + 1][1].record(in_q)
                     h2d_ev[b ^ 1].record(in_q)
         data.wait_stream(in_q)
         e1.record(data)
         torch.cuda.synchronize()
+        clk_e2e = clocks_e.stop()
         e_ms = max_over_ranks(e0.elapsed_time(e1), ws)
-        xb = x.numel() * x.element_size()
+        x_in_ms = sorted(ev[0].elapsed_time(ev[1]) for ev in io_ev)
+        y_out_ms = sorted(ev[2].elapsed_time(ev[3]) for ev in io_ev)
+        # compute-stream time of each step (from the end of the previous one,
+        # so a step that waited for its input counts the wait)
+        e_step_ms = sorted(step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps))
         e2e = {"value": ws * n_fwd / (e_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": xb + w.n_blocks * bytes_per_block,
                "d2h_bytes_per_step": xb,
+               "clocks": clk_e2e,
+               "x_in_ms": {"p50": x_in_ms[len(x_in_ms) // 2], "max": x_in_ms[-1]},
+               "result_out_ms": {"p50": y_out_ms[len(y_out_ms) // 2], "max": y_out_ms[-1]},
+               "step_ms": {"p50": e_step_ms[len(e_step_ms) // 2], "max": e_step_ms[-1],
+                           "min": e_step_ms[0]},
+               "io_buffers": {"kind": "PinnedIO: huge-page pinned host memory, surveyed, each "
+                                      "copy direction verified",
+                              "h2d_gbs": [round(a, 1) for a, _ in io_rates],
+                              "d2h_gbs": [round(b, 1) for _, b in io_rates],
+                              "relocated": io.relocated, "failed": io.failed},
                "note": "h2d counts x plus every streamed weight shard of the step; x in and "
                        "the result out are double-buffered; x goes through the weight copy "
-                       "stream, the result returns on a data stream"}
+                       "stream, the result returns on a data stream; run after the value, "
+                       "timed-copy and resident passes (clocks: sampled during this pass)"}
+        del xh, yh
+        io.close()
 
     status = dlo.kernel_status()
     if status != 0:

@@ -54,11 +54,12 @@ class PinnedBuffer:
 
     SMALL = 256 << 20     # below this the footprint is too small to matter
 
-    def __init__(self, nbytes, spare=0.25, tries=3, defer=False, extra_ranges=0):
+    def __init__(self, nbytes, spare=0.25, tries=3, defer=False, extra_ranges=0, huge=None):
         """extra_ranges: 512 MiB ranges reserved beyond the spare room for
-        relocate() (address space only until used)."""
+        relocate() (address space only until used).  huge: True to use
+        huge-page ranges whatever the size (None: only from SMALL up)."""
         self.nbytes = int(nbytes)
-        self.small = self.nbytes < self.SMALL
+        self.small = self.nbytes < self.SMALL if huge is None else not huge
         n_ranges = max(1, -(-self.nbytes // _HUGE))
         self.capacity = (_round_up(self.nbytes, 1 << 16) if self.small
                          else (n_ranges + int(n_ranges * spare) + 2 + extra_ranges) * _HUGE)
@@ -408,6 +409,83 @@ class PinnedBuffer:
             self.close()
         except Exception:
             pass
+
+
+class PinnedIO:
+    """Page-locked host buffers for what a step moves besides the weights,
+    its input copied in and its result read back, placed like the weight
+    shards: in huge-page ranges that streamed at the link rate in a survey
+    (PinnedBuffer.place_surveyed), then verify() times every buffer's
+    host->device and device->host copy and moves a slow buffer to fresh
+    ranges (PinnedBuffer.relocate).  Take views with tensor() after
+    verify(): a move changes the buffer's address.
+
+    Why: the host ranges that stall weight copies stall these as well, and
+    buffers of a few hundred MB from torch's pinned allocator sit in base
+    pages: on one GB300 host a 201 MB input copied at 7.5 GB/s (27 ms, the
+    link rate gives 1 ms), and every step waited for it."""
+
+    def __init__(self, nbytes, count, device="cuda"):
+        self.nbytes, self.count, self.device = int(nbytes), int(count), device
+        per = _round_up(self.nbytes, 256)
+        k = -(-per // _HUGE)                  # 512 MiB ranges one moved buffer takes
+        # room for two moves of every buffer (address space until used)
+        self.buf = PinnedBuffer(per * self.count, defer=True, huge=True,
+                                extra_ranges=2 * self.count * k + 1)
+        self.offs = self.buf.place_surveyed([self.nbytes] * self.count)
+        self.relocated, self.failed, self.rates_gbs = [], [], None
+
+    def tensor(self, i, shape, dtype):
+        """Buffer i as a tensor of `shape` and `dtype` (nbytes in all)."""
+        t = self.buf.view(self.offs[i], self.nbytes).view(dtype)
+        return t.view(shape)
+
+    def rates(self, passes=2):
+        """(host->device, device->host) GB/s of each buffer, timed on the
+        last of `passes` round trips (the contents are kept)."""
+        dev = torch.empty(self.nbytes, dtype=torch.uint8, device=self.device)
+        s = torch.cuda.Stream(device=self.device)
+        out = []
+        for o in self.offs:
+            h = self.buf.view(o, self.nbytes)
+            for _ in range(passes):
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                with torch.cuda.stream(s):
+                    ev[0].record(s)
+                    dev.copy_(h, non_blocking=True)
+                    ev[1].record(s)
+                    h.copy_(dev, non_blocking=True)
+                    ev[2].record(s)
+                s.synchronize()
+            out.append((self.nbytes / (ev[0].elapsed_time(ev[1]) * 1e6),
+                        self.nbytes / (ev[1].elapsed_time(ev[2]) * 1e6)))
+        del dev
+        return out
+
+    def verify(self, min_gbs, rounds=2):
+        """Moves every buffer whose copy in either direction is below
+        min_gbs to fresh huge-page ranges (its contents move with it), up to
+        `rounds` times; returns the last measured rates."""
+        for _ in range(rounds):
+            rates = self.rates()
+            slow = [i for i, (a, b) in enumerate(rates) if min(a, b) < min_gbs]
+            if not slow:
+                break
+            for i in slow:
+                new = self.buf.relocate([(self.offs[i], self.nbytes)], min_gbs,
+                                        device=self.device)
+                if new is None:
+                    self.failed.append(i)
+                else:
+                    self.offs[i] = new[0]
+                    self.relocated.append(i)
+        else:
+            rates = self.rates()
+        self.rates_gbs = rates
+        return rates
+
+    def close(self):
+        self.buf.close()
 
 
 class HostBlocks:

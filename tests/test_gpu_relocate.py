@@ -6,7 +6,11 @@ host ranges that turn slow for the GPU to read):
   shards, then later prefetches read the new ones;
 - a host block moved by HostBlocks.relocate_block between two steps, and by
   the stack's healer, streams the same bytes: slot images equal the
-  oracle's, and the streamed output stays bit-identical to the resident one.
+  oracle's, and the streamed output stays bit-identical to the resident one;
+- PinnedIO (a step's input and result buffers in huge-page pinned memory):
+  its buffers round-trip through the device, a move that fails its rate
+  check leaves a buffer where it was, and a move that passes keeps the
+  contents.
 """
 import numpy as np
 import pytest
@@ -15,7 +19,8 @@ import torch
 import oracle
 from tests._util import build_lib, raw_bytes
 from layerwise_weight_offload_gb300 import dlo, workloads as W
-from layerwise_weight_offload_gb300.stack import HostBlocks, StreamedStack, ResidentStack
+from layerwise_weight_offload_gb300.stack import (HostBlocks, StreamedStack, ResidentStack,
+                                                  PinnedIO)
 
 pytestmark = pytest.mark.gpu
 
@@ -133,3 +138,33 @@ def test_relocated_blocks_stream_the_same_bytes(how):
     assert dlo.kernel_status() == 0
     st.close()
     host.close()
+
+
+def test_pinned_io_buffers_round_trip_and_move():
+    shape = (1000, 777)                       # fp32: 3,108,000 bytes, not a multiple of 256
+    nbytes = 1000 * 777 * 4
+    io = PinnedIO(nbytes, 3)
+    assert io.buf.good_fraction() == 1.0      # huge-page ranges although the buffers are small
+    rates = io.verify(1.0)
+    assert len(rates) == 3 and all(a > 1.0 and b > 1.0 for a, b in rates)
+    assert io.relocated == [] and io.failed == []
+    x = torch.randn(shape, generator=torch.Generator().manual_seed(3))
+    xh = io.tensor(0, shape, torch.float32)
+    xh.copy_(x)
+    d = xh.cuda()
+    yh = io.tensor(1, shape, torch.float32)
+    yh.copy_(d, non_blocking=True)
+    torch.cuda.synchronize()
+    assert torch.equal(yh, x)
+    # a move whose new place misses the rate: refused, buffer unchanged
+    off0 = io.offs[0]
+    del xh, yh
+    io.verify(1e12, rounds=1)
+    assert io.failed == [0, 1, 2] and io.relocated == [] and io.offs[0] == off0
+    assert torch.equal(io.tensor(0, shape, torch.float32), x)
+    # a move that passes: a new address, the same contents
+    new = io.buf.relocate([(io.offs[0], nbytes)], 1.0)
+    assert new is not None and new[0] != off0
+    io.offs[0] = new[0]
+    assert torch.equal(io.tensor(0, shape, torch.float32), x)
+    io.close()
