@@ -10,15 +10,19 @@ Prints one JSON line:
               the timed region, the engine as it runs in use; the K timed
               steps run as 5 regions (each bracketed by a device
               synchronisation) and value is the median region's rate;
-  e2e         the same, with x copied from pinned host memory and the result
-              read back every step inside the timed region;
+  e2e         the same, with x copied from pinned host memory (PinnedIO
+              buffers) and the result read back every step inside the timed
+              region;
   h2d_gbs     bytes moved host->device / copy-stream busy time, from a
               second pass of the same steps with an event pair around every
               prefetch (the copy statistics come from that pass);
   exposed_transfer_ms_per_step  streamed minus all-resident step time;
-  roofline    the dominant operation (the host->device copy) against the
-              measured pinned cudaMemcpyAsync ceiling of this box;
-  roofline_compute  the largest linear against the measured bf16 peak;
+  roofline    the dominant operation: where the link bounds the block, the
+              host->device copy against the measured pinned cudaMemcpyAsync
+              ceiling of this machine; where compute does, fc2 (the largest
+              linear, on CTA pairs) timed alone against the measured bf16
+              peak;
+  roofline_h2d, roofline_compute  both of these, always;
   cpu_baseline the CPU oracle on a bounded sample of the same workload.
 
 --impl reference times the CPU oracle (the reference arm of this build):
