@@ -729,15 +729,33 @@ def run_ours(args, ws, rank, local):
         y_out_ms = sorted(ev[2].elapsed_time(ev[3]) for ev in io_ev)
         # compute-stream time of each step (from the end of the previous one,
         # so a step that waited for its input counts the wait)
-        e_step_ms = sorted(step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps))
-        e2e = {"value": ws * n_fwd / (e_ms / 1e3), "unit": UNIT,
+        e_steps = [step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps)]
+        e_step_ms = sorted(e_steps)
+        # the value pass's regions over the same steps: the first from before
+        # step 0's input copy, the last to the end of the last read-back, so
+        # that the regions add up to the whole pass
+        bounds = [0]
+        for k in sizes:
+            bounds.append(bounds[-1] + k)
+        marks = [e0] + [step_ev[b] for b in bounds[1:-1]] + [e1]
+        e_region_ms = [max_over_ranks(marks[i].elapsed_time(marks[i + 1]), ws)
+                       for i in range(len(sizes))]
+        e_rates = [ws * w.n_blocks * k / (ms / 1e3) for k, ms in zip(sizes, e_region_ms)]
+        emed = median_region(sizes, e_region_ms)
+        e2e = {"value": e_rates[emed], "unit": UNIT,
+               "whole_pass_value": ws * n_fwd / (e_ms / 1e3),
+               "block_fwd_per_s_per_region": e_rates,
+               "timing": "median of the value pass's regions over the same steps (the first "
+                         "from before step 0's input copy, the last to the end of the last "
+                         "read-back: together the whole pass, whole_pass_value)",
                "h2d_bytes_per_step": xb + w.n_blocks * bytes_per_block,
                "d2h_bytes_per_step": xb,
                "clocks": clk_e2e,
                "x_in_ms": {"p50": x_in_ms[len(x_in_ms) // 2], "max": x_in_ms[-1]},
                "result_out_ms": {"p50": y_out_ms[len(y_out_ms) // 2], "max": y_out_ms[-1]},
                "step_ms": {"p50": e_step_ms[len(e_step_ms) // 2], "max": e_step_ms[-1],
-                           "min": e_step_ms[0]},
+                           "min": e_step_ms[0], "first": e_steps[:3],
+                           "before_first": e0.elapsed_time(step_ev[0])},
                "io_buffers": {"kind": "PinnedIO: huge-page pinned host memory, surveyed, each "
                                       "copy direction verified",
                               "h2d_gbs": [round(a, 1) for a, _ in io_rates],
