@@ -37,6 +37,13 @@
  *   - The library never allocates device memory or pins host memory: the
  *     caller owns slots, activations, scratch, shard buffers and streams.
  *     The library owns plans, engines, their CUDA events and logs.
+ *   - Tracing: the plan, shard, hook, prefetch, forward, reassembly and
+ *     teardown calls push NVTX ranges in the domain "dlo" (payload: the
+ *     block index for hooks and prefetches, the number of rows for a
+ *     forward, the number of parameters for plan_create and shard_host, the
+ *     slot bytes for a one-shot reassembly).  Without an NVTX tool attached
+ *     (nsys, ncu --nvtx, or a library named by NVTX_INJECTION64_PATH) they
+ *     cost a load and a branch each.
  */
 #ifndef DLO_H_
 #define DLO_H_
