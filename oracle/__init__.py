@@ -57,6 +57,9 @@ def lib():
         L.oracle_block_forward_rows.restype = None
         L.oracle_block_forward_rows.argtypes = [vp, i64, i64, i64, i64, i64, dbl, vp, vp, i64,
                                                 vp, i32]
+        L.oracle_block_forward_ex_rows.restype = None
+        L.oracle_block_forward_ex_rows.argtypes = [vp, i64, i64, i64, i64, i64, dbl, vp, vp, vp,
+                                                   vp, vp, vp, vp, dbl, vp, i64, vp, i32]
         _lib = L
     return _lib
 
@@ -252,12 +255,22 @@ def block_forward(x, params, batch, tokens, d, heads, f, eps=1e-6, threads=None,
     return out
 
 
-def block_forward_rows(x, params, rows, batch, tokens, d, heads, f, eps=1e-6, threads=None):
-    """Block output for the listed query rows only (K and V from all tokens)."""
+def block_forward_rows(x, params, rows, batch, tokens, d, heads, f, eps=1e-6, threads=None,
+                       rope_base=0.0):
+    """Block output for the listed query rows only (K and V from all tokens);
+    the checkpoint-shaped additions as in block_forward."""
     x = np.ascontiguousarray(x, dtype=np.float32).reshape(batch * tokens, d)
     arrs = [np.ascontiguousarray(params[n], dtype=np.float32) for n in PARAM_ORDER]
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     out = np.zeros((len(rows), d), dtype=np.float64)
+    extras = [np.ascontiguousarray(params[n], dtype=np.float32) if n in params else None
+              for n in EXTRA_ORDER]
+    if any(e is not None for e in extras) or rope_base > 0:
+        ptrs = [e.ctypes.data if e is not None else None for e in extras]
+        lib().oracle_block_forward_ex_rows(_ptr(x), batch, tokens, d, heads, f, eps,
+                                           _ptr_array(arrs), *ptrs, float(rope_base), _ptr(rows),
+                                           len(rows), _ptr(out), threads or default_threads())
+        return out
     lib().oracle_block_forward_rows(_ptr(x), batch, tokens, d, heads, f, eps, _ptr_array(arrs),
                                     _ptr(rows), len(rows), _ptr(out),
                                     threads or default_threads())

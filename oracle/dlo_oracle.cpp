@@ -235,6 +235,28 @@ static void run_rows(int64_t rows, int32_t threads,
   for (auto& th : pool) th.join();
 }
 
+// One head's hd values v <- v / sqrt(mean(v^2) + eps) * g (the per-head
+// q/k RMSNorm of the checkpoint-shaped block).
+static void qk_norm_head(double* v, int64_t hd, const float* g, double eps) {
+  double ss = 0.0;
+  for (int64_t c = 0; c < hd; ++c) ss += v[c] * v[c];
+  const double inv = 1.0 / std::sqrt(ss / static_cast<double>(hd) + eps);
+  for (int64_t c = 0; c < hd; ++c) v[c] = v[c] * inv * static_cast<double>(g[c]);
+}
+
+// One head's values at position pos rotated pair by pair: pair (2i, 2i+1)
+// by the angle pos * base^(-2i/hd) (RoFormer's rotary embedding).
+static void rope_head(double* v, int64_t hd, double pos, double base) {
+  for (int64_t i = 0; i < hd / 2; ++i) {
+    const double ang = pos * std::pow(base, -2.0 * static_cast<double>(i) /
+                                                static_cast<double>(hd));
+    const double c = std::cos(ang), s = std::sin(ang);
+    const double a0 = v[2 * i], b0 = v[2 * i + 1];
+    v[2 * i] = a0 * c - b0 * s;
+    v[2 * i + 1] = a0 * s + b0 * c;
+  }
+}
+
 extern "C" {
 
 double oracle_gelu_tanh(double z) {
@@ -324,16 +346,9 @@ void oracle_qk_norm(double* qkv, int64_t rows, int64_t d, int64_t heads, const f
                     const float* gk, double eps) {
   const int64_t hd = d / heads;
   for (int64_t t = 0; t < rows; ++t)
-    for (int64_t part = 0; part < 2; ++part) {
-      const float* g = part == 0 ? gq : gk;
-      for (int64_t j = 0; j < heads; ++j) {
-        double* v = qkv + t * 3 * d + part * d + j * hd;
-        double ss = 0.0;
-        for (int64_t c = 0; c < hd; ++c) ss += v[c] * v[c];
-        const double inv = 1.0 / std::sqrt(ss / static_cast<double>(hd) + eps);
-        for (int64_t c = 0; c < hd; ++c) v[c] = v[c] * inv * static_cast<double>(g[c]);
-      }
-    }
+    for (int64_t part = 0; part < 2; ++part)
+      for (int64_t j = 0; j < heads; ++j)
+        qk_norm_head(qkv + t * 3 * d + part * d + j * hd, hd, part == 0 ? gq : gk, eps);
 }
 
 // Rotary position embedding of q and k (the checkpoint-shaped block), in the
@@ -348,17 +363,7 @@ void oracle_rope(double* qkv, int64_t batch, int64_t tokens, int64_t d, int64_t 
   for (int64_t r = 0; r < batch * tokens; ++r) {
     const double pos = static_cast<double>(r % tokens);
     for (int64_t part = 0; part < 2; ++part)
-      for (int64_t j = 0; j < heads; ++j) {
-        double* v = qkv + r * 3 * d + part * d + j * hd;
-        for (int64_t i = 0; i < hd / 2; ++i) {
-          const double ang = pos * std::pow(base, -2.0 * static_cast<double>(i) /
-                                                      static_cast<double>(hd));
-          const double c = std::cos(ang), s = std::sin(ang);
-          const double a0 = v[2 * i], b0 = v[2 * i + 1];
-          v[2 * i] = a0 * c - b0 * s;
-          v[2 * i + 1] = a0 * s + b0 * c;
-        }
-      }
+      for (int64_t j = 0; j < heads; ++j) rope_head(qkv + r * 3 * d + part * d + j * hd, hd, pos, base);
   }
 }
 
@@ -497,6 +502,100 @@ void oracle_block_forward_rows(const float* x_in, int64_t batch, int64_t tokens,
   oracle_linear(hs.data(), n_rows, d, p[10], f, u.data(), threads);
   for (int64_t e = 0; e < n_rows * f; ++e) u[e] = oracle_gelu_tanh(u[e]);
   oracle_linear(u.data(), n_rows, f, p[11], d, y.data(), threads);
+  for (int64_t i = 0; i < n_rows; ++i)
+    for (int64_t c = 0; c < d; ++c) xs[i * d + c] += static_cast<double>(p[9][c]) * y[i * d + c];
+  std::memcpy(x_out, xs.data(), sizeof(double) * n_rows * d);
+}
+
+// oracle_block_forward_ex evaluated only for the listed query rows (as
+// oracle_block_forward_rows does for the plain block): every token's K and V
+// get their bias, k-norm and rotation, the listed rows' Q likewise, and the
+// out-projection, residuals and MLP run for the listed rows only.  Each value
+// of a listed row is formed by the same operations, in the same order, as in
+// oracle_block_forward_ex.
+void oracle_block_forward_ex_rows(const float* x_in, int64_t batch, int64_t tokens, int64_t d,
+                                  int64_t heads, int64_t f, double eps, const float* const* p,
+                                  const float* bqkv, const float* bo, const float* b1,
+                                  const float* b2, const float* gq, const float* gk,
+                                  double rope_base, const int64_t* rows, int64_t n_rows,
+                                  double* x_out, int32_t threads) {
+  const int64_t M = batch * tokens;
+  const int64_t hd = d / heads;
+  const double scale = 1.0 / std::sqrt(static_cast<double>(hd));
+  const bool qk_norm = gq && gk;
+  std::vector<double> x(M * d), h(M * d), kv(M * 2 * d);
+  for (int64_t e = 0; e < M * d; ++e) x[e] = static_cast<double>(x_in[e]);
+  oracle_rmsnorm_mod(x.data(), M, d, p[0], p[1], p[2], eps, h.data());
+  // K and V of every token: rows d..3d of Wqkv, their bias, then k's norm
+  // and rotation
+  oracle_linear(h.data(), M, d, p[4] + d * d, 2 * d, kv.data(), threads);
+  for (int64_t t = 0; t < M; ++t) {
+    double* r = kv.data() + t * 2 * d;
+    if (bqkv)
+      for (int64_t c = 0; c < 2 * d; ++c) r[c] += static_cast<double>(bqkv[d + c]);
+    for (int64_t j = 0; j < heads; ++j) {
+      if (qk_norm) qk_norm_head(r + j * hd, hd, gk, eps);
+      if (rope_base > 0.0)
+        rope_head(r + j * hd, hd, static_cast<double>(t % tokens), rope_base);
+    }
+  }
+  std::vector<double> xs(n_rows * d), hs(n_rows * d), q(n_rows * d), o(n_rows * d),
+      y(n_rows * d), u(n_rows * f);
+  for (int64_t i = 0; i < n_rows; ++i)
+    for (int64_t c = 0; c < d; ++c) {
+      xs[i * d + c] = x[rows[i] * d + c];
+      hs[i * d + c] = h[rows[i] * d + c];
+    }
+  oracle_linear(hs.data(), n_rows, d, p[4], d, q.data(), threads);   // Q rows 0..d
+  for (int64_t i = 0; i < n_rows; ++i) {
+    double* r = q.data() + i * d;
+    if (bqkv)
+      for (int64_t c = 0; c < d; ++c) r[c] += static_cast<double>(bqkv[c]);
+    for (int64_t j = 0; j < heads; ++j) {
+      if (qk_norm) qk_norm_head(r + j * hd, hd, gq, eps);
+      if (rope_base > 0.0)
+        rope_head(r + j * hd, hd, static_cast<double>(rows[i] % tokens), rope_base);
+    }
+  }
+  run_rows(n_rows * heads, threads, [&](int64_t lo, int64_t hi) {
+    std::vector<double> s(tokens);
+    for (int64_t job = lo; job < hi; ++job) {
+      const int64_t i = job / heads, j = job % heads;
+      const int64_t b = rows[i] / tokens;
+      const double* qr = q.data() + i * d + j * hd;
+      double m = -INFINITY;
+      for (int64_t t = 0; t < tokens; ++t) {
+        const double* kk = kv.data() + (b * tokens + t) * 2 * d + j * hd;
+        double dot = 0.0;
+        for (int64_t c = 0; c < hd; ++c) dot += qr[c] * kk[c];
+        s[t] = dot * scale;
+        m = std::max(m, s[t]);
+      }
+      double denom = 0.0;
+      for (int64_t t = 0; t < tokens; ++t) { s[t] = std::exp(s[t] - m); denom += s[t]; }
+      for (int64_t c = 0; c < hd; ++c) {
+        double acc = 0.0;
+        for (int64_t t = 0; t < tokens; ++t)
+          acc += s[t] * kv[(b * tokens + t) * 2 * d + d + j * hd + c];
+        o[i * d + j * hd + c] = acc / denom;
+      }
+    }
+  });
+  auto add_bias = [](double* v, int64_t n_r, int64_t n, const float* bias) {
+    if (!bias) return;
+    for (int64_t t = 0; t < n_r; ++t)
+      for (int64_t c = 0; c < n; ++c) v[t * n + c] += static_cast<double>(bias[c]);
+  };
+  oracle_linear(o.data(), n_rows, d, p[5], d, y.data(), threads);
+  add_bias(y.data(), n_rows, d, bo);
+  for (int64_t i = 0; i < n_rows; ++i)
+    for (int64_t c = 0; c < d; ++c) xs[i * d + c] += static_cast<double>(p[3][c]) * y[i * d + c];
+  oracle_rmsnorm_mod(xs.data(), n_rows, d, p[6], p[7], p[8], eps, hs.data());
+  oracle_linear(hs.data(), n_rows, d, p[10], f, u.data(), threads);
+  add_bias(u.data(), n_rows, f, b1);
+  for (int64_t e = 0; e < n_rows * f; ++e) u[e] = oracle_gelu_tanh(u[e]);
+  oracle_linear(u.data(), n_rows, f, p[11], d, y.data(), threads);
+  add_bias(y.data(), n_rows, d, b2);
   for (int64_t i = 0; i < n_rows; ++i)
     for (int64_t c = 0; c < d; ++c) xs[i * d + c] += static_cast<double>(p[9][c]) * y[i * d + c];
   std::memcpy(x_out, xs.data(), sizeof(double) * n_rows * d);

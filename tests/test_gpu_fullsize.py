@@ -1,7 +1,9 @@
 """Full-size checks at the shapes of the Nano workload (hidden 3840, 30
-heads, MLP 15360, 4096 tokens, 4 shards), the Super workload (hidden 6144,
-48 heads, MLP 24576, 8192 tokens, 2 shards) and the longest-sequence sweep
-cell (hidden 1664, 13 heads, MLP 6656, 16384 tokens, 2 shards), in the
+heads, MLP 15360, 4096 tokens, 4 shards), its checkpoint-shaped variant
+(biases, per-head q/k RMSNorm, rotary embedding), the Super workload
+(hidden 6144, 48 heads, MLP 24576, 8192 tokens, 2 shards) and the
+longest-sequence sweep cell (hidden 1664, 13 heads, MLP 6656, 16384 tokens,
+2 shards), in the
 launch configuration bench.py times (two-slot engine, AUTO copy mode,
 CUDA-graph forwards):
 - every prefetched slot equals the oracle's reassembled block, byte for byte;
@@ -25,6 +27,7 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("name,rows", [
     ("nano", [0, 1, 777, 2048, 4095]),
+    ("nano-full", [0, 1, 1234, 3000, 4095]),
     ("super", [0, 1, 3333, 4096, 8191]),
     ("sweep-d1664-t16384-s2", [0, 1, 5000, 12345, 16383]),
 ])
@@ -79,7 +82,8 @@ def test_full_shapes_streamed_resident_and_sampled_oracle(name, rows):
     # sampled rows of block 0 against the oracle (K and V over all tokens)
     p = params_f32(host.params[0])
     ref = oracle.block_forward_rows(x_in_block0.cpu().numpy(), p, rows, w.batch, w.tokens,
-                                    w.hidden, w.heads, w.mlp, w.eps)
+                                    w.hidden, w.heads, w.mlp, w.eps,
+                                    rope_base=W.oracle_rope_base(w))
     got = x_out_block0.cpu().numpy()[rows]
     assert_oracle_close(got, ref, name + " rows")
     xin = x_in_block0.cpu().numpy()[rows]

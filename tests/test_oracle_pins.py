@@ -685,3 +685,32 @@ def test_full_block_without_extras_equals_plain_block():
     oracle.lib().oracle_block_forward_ex(x.ctypes.data, 1, t, d, 4, f, 1e-6, ptrs, None, None,
                                          None, None, None, None, 0.0, out.ctypes.data, 2)
     assert np.array_equal(out, oracle.block_forward(x, p, 1, t, d, 4, f))
+
+
+@pytest.mark.parametrize("keep", [
+    ("attn.qkv.bias", "attn.out.bias", "mlp.fc1.bias", "mlp.fc2.bias", "attn.q_norm.weight",
+     "attn.k_norm.weight"),
+    ("attn.qkv.bias", "mlp.fc2.bias"),
+    ("attn.q_norm.weight", "attn.k_norm.weight"),
+    (),
+])
+@pytest.mark.parametrize("rope", [10000.0, 0.0])
+def test_full_block_rows_equals_full_block_on_listed_rows(keep, rope):
+    # the checkpoint-shaped block's sampled-rows form reproduces the full
+    # forward's rows exactly, with any subset of the additions; two batch
+    # items, so the rotation's positions restart (rows 9 and 17 are tokens 0
+    # and 8 of the second item)
+    if not keep and rope == 0.0:
+        pytest.skip("the plain block: test_block_rows_equals_full_block_on_listed_rows")
+    rng = np.random.default_rng(29)
+    d, f, t, heads = 16, 64, 9, 4
+    p = _params(rng, d, f)
+    p.update({k: v for k, v in _extras(rng, d, f, d // heads).items() if k in keep})
+    x = rng.standard_normal((2 * t, d)).astype(np.float32)
+    full = oracle.block_forward(x, p, 2, t, d, heads, f, threads=3, rope_base=rope)
+    rows = [0, 5, 8, 9, 17]
+    part = oracle.block_forward_rows(x, p, rows, 2, t, d, heads, f, threads=3, rope_base=rope)
+    assert np.array_equal(part, full[rows])
+    # the additions matter at these values: the plain block differs
+    plain = {k: v for k, v in p.items() if k not in keep}
+    assert not np.allclose(oracle.block_forward(x, plain, 2, t, d, heads, f), full, atol=1e-6)
