@@ -687,21 +687,22 @@ def test_full_block_without_extras_equals_plain_block():
     assert np.array_equal(out, oracle.block_forward(x, p, 1, t, d, 4, f))
 
 
-@pytest.mark.parametrize("keep", [
-    ("attn.qkv.bias", "attn.out.bias", "mlp.fc1.bias", "mlp.fc2.bias", "attn.q_norm.weight",
-     "attn.k_norm.weight"),
-    ("attn.qkv.bias", "mlp.fc2.bias"),
-    ("attn.q_norm.weight", "attn.k_norm.weight"),
-    (),
+_ALL_EXTRAS = ("attn.qkv.bias", "attn.out.bias", "mlp.fc1.bias", "mlp.fc2.bias",
+               "attn.q_norm.weight", "attn.k_norm.weight")
+
+
+@pytest.mark.parametrize("keep,rope", [
+    (_ALL_EXTRAS, 10000.0), (_ALL_EXTRAS, 0.0),
+    (("attn.qkv.bias", "mlp.fc2.bias"), 10000.0), (("attn.qkv.bias", "mlp.fc2.bias"), 0.0),
+    (("attn.q_norm.weight", "attn.k_norm.weight"), 10000.0),
+    (("attn.q_norm.weight", "attn.k_norm.weight"), 0.0),
+    ((), 10000.0),
 ])
-@pytest.mark.parametrize("rope", [10000.0, 0.0])
 def test_full_block_rows_equals_full_block_on_listed_rows(keep, rope):
     # the checkpoint-shaped block's sampled-rows form reproduces the full
     # forward's rows exactly, with any subset of the additions; two batch
     # items, so the rotation's positions restart (rows 9 and 17 are tokens 0
     # and 8 of the second item)
-    if not keep and rope == 0.0:
-        pytest.skip("the plain block: test_block_rows_equals_full_block_on_listed_rows")
     rng = np.random.default_rng(29)
     d, f, t, heads = 16, 64, 9, 4
     p = _params(rng, d, f)
@@ -714,3 +715,5 @@ def test_full_block_rows_equals_full_block_on_listed_rows(keep, rope):
     # the additions matter at these values: the plain block differs
     plain = {k: v for k, v in p.items() if k not in keep}
     assert not np.allclose(oracle.block_forward(x, plain, 2, t, d, heads, f), full, atol=1e-6)
+    assert np.array_equal(part, oracle.block_forward_rows(x, p, rows, 2, t, d, heads, f,
+                                                          threads=1, rope_base=rope))
