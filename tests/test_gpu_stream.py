@@ -212,6 +212,23 @@ def test_odd_streamed_vs_resident_vs_oracle():
     host.close()
 
 
+def test_odd_full_streamed_vs_resident_vs_oracle():
+    # the checkpoint-shaped block at the odd workload's shape (biases, q/k
+    # norm, rotary embedding; 9 blocks, 3 misaligned shards, head dim 64)
+    w = W.CONFIGS["odd-full"]
+    host = HostBlocks(w, seed=0, keep_params=True)
+    x0 = W.gen_x(w, seed=0)
+    res, per_block = _run_resident(host, x0, w.steps)
+    for mode in (dlo.COPY_AUTO, dlo.COPY_KERNEL):
+        stm = _run_streamed(host, x0, w.steps, mode)
+        for a, b in zip(res, stm):
+            assert torch.equal(a, b)
+    n = w.n_blocks
+    _check_against_oracle(host, per_block, [0, 1, n - 1, (w.steps - 1) * n])
+    assert dlo.kernel_status() == 0
+    host.close()
+
+
 @pytest.mark.parametrize("cfg", [
     dict(n_blocks=3, hidden=320, heads=5, mlp=1280, tokens=200, shards=3),   # ragged tiles
     dict(n_blocks=2, hidden=256, heads=2, mlp=1024, tokens=1, shards=2),     # one token
