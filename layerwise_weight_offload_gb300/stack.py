@@ -619,13 +619,17 @@ class CopyHealer:
     engine's copy log: a copy is slow when its rate is below the median rate
     of the recent copies divided by `factor` and it took at least
     `min_extra_ms` longer than a copy at that rate would; a host block is
-    named once `strikes` of its copies since it last moved were slow.  A
-    block that keeps turning slow is named at most `max_moves` times."""
+    named once `strikes` of its copies since it last moved were slow, or at
+    once after a copy below the median rate divided by `severe` (each copy
+    from a slow place stalls the stream, and a second one costs as much as
+    the move).  A block that keeps turning slow is named at most `max_moves`
+    times."""
 
     def __init__(self, distinct, factor=2.0, min_extra_ms=1.0, strikes=2, window=512,
-                 max_moves=3):
+                 max_moves=3, severe=4.0):
         self.distinct = distinct
         self.factor, self.min_extra_ms, self.strikes = factor, min_extra_ms, strikes
+        self.severe = severe
         self.window, self.max_moves = window, max_moves
         self.rates = []
         self.count = {}
@@ -647,7 +651,8 @@ class CopyHealer:
             expect = nbytes / med
             if ms * med < nbytes * self.factor or ms - expect < self.min_extra_ms:
                 continue
-            self.count[hb] = self.count.get(hb, 0) + 1
+            hit = self.strikes if ms * med >= nbytes * self.severe else 1
+            self.count[hb] = self.count.get(hb, 0) + hit
             if (self.count[hb] >= self.strikes and self.moves.get(hb, 0) < self.max_moves
                     and hb not in out):
                 out.append(hb)

@@ -86,8 +86,9 @@ def test_healer_names_a_block_after_two_slow_copies_only():
     h = CopyHealer(distinct=32)
     fast = [(b, 4.29 + 0.01 * (b % 3)) for b in range(128)]
     assert h.observe(_records(0, fast)) == []
-    # host block 3 (engine blocks 3, 35, 67, 99) turns slow: 30x longer
-    step = [(b, 120.0 if b % 32 == 3 else ms) for b, ms in fast]
+    # host block 3 (engine blocks 3, 35, 67, 99) turns slow: 3x longer (below
+    # the severe factor, so two strikes are needed)
+    step = [(b, 13.0 if b % 32 == 3 else ms) for b, ms in fast]
     assert h.observe(_records(128, step[:40])) == [3]         # blocks 3 and 35: two strikes
     h.moved(3)
     assert h.observe(_records(168, step[40:70])) == []        # block 67: one strike since
@@ -99,9 +100,9 @@ def test_healer_ignores_one_off_and_small_excess():
     h = CopyHealer(distinct=8, min_extra_ms=1.0)
     base = [(b, 4.3) for b in range(64)]
     assert h.observe(_records(0, base)) == []
-    # a single slow copy of host block 5: not named; 2.5x of a 0.1 ms copy:
-    # below the absolute margin, not named either
-    assert h.observe(_records(64, [(5, 40.0)] + base[1:8])) == []
+    # a single slow copy of host block 5 (3x): not named; 2.5x of a 0.1 ms
+    # copy: below the absolute margin, not named either
+    assert h.observe(_records(64, [(5, 13.0)] + base[1:8])) == []
     tiny = [(6, 0.25)] * 4
     assert h.observe(_records(72, [(b, 0.1) for b in range(64)] + tiny, nbytes=1_000_000)) == []
 
@@ -118,3 +119,20 @@ def test_healer_stops_after_max_moves():
             named += 1
             h.moved(1)
     assert named == 2
+
+
+def test_healer_names_a_block_after_one_severely_slow_copy():
+    from layerwise_weight_offload_gb300.stack import CopyHealer
+    h = CopyHealer(distinct=8)
+    base = [(b, 4.3) for b in range(64)]
+    assert h.observe(_records(0, base)) == []
+    assert h.observe(_records(64, [(2, 17.0)])) == []        # 3.95x: one strike of two
+    assert h.observe(_records(65, [(5, 17.5)])) == [5]       # 4.07x: named at once
+    h.moved(5)
+    assert h.observe(_records(66, [(2, 16.0)])) == [2]       # block 2's second strike
+    # a severe copy of a block already moved max_moves times is not named again
+    h2 = CopyHealer(distinct=8, max_moves=1)
+    h2.observe(_records(0, base))
+    assert h2.observe(_records(64, [(1, 90.0)])) == [1]
+    h2.moved(1)
+    assert h2.observe(_records(65, [(1, 90.0)])) == []
