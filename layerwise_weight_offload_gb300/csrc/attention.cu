@@ -17,6 +17,8 @@
 //              into one NS-stage ring (NS = 5 for hd 128, 12 for hd 64);
 //              warp 9: TMEM allocation (512 columns) and the tcgen05.mma
 //              issue.
+// WG2 gives up registers to the softmax warpgroups (setmaxnreg), which hold
+// a whole row of scores.
 // TMEM: S_t at column 128 t (fp32, 128 keys); P_t (bf16, two per column)
 // overwrites the first 64 columns of S_t; O_t at column 256 + hd t.
 // MMA order: S_0(0) S_1(0), then per KV tile j
@@ -27,10 +29,16 @@
 // While softmax t turns S_t(j+1) into P_t(j+1) the tensor pipe runs the
 // other tile's PV and S.  The commit that signals S_t(j+1) also covers
 // PV_t(j), so softmax t may then rescale O_t and overwrite P_t.
-// Softmax per tile: tcgen05.ld of the 128 scores, row maximum (a tile's
-// first KV tile fixes m; later ones keep it unless a row's scaled maximum
-// exceeds m by more than kGrowLimit, which moves m up and rescales O_t, l
-// and the P chunks already written), P =
+// The MMA thread keeps its own synchronisation to one wait, one fence and
+// one commit per query tile and KV tile (each costs tensor-pipe time, the
+// issue queue being shallow): it waits only for P_t(j); the softmax warps
+// check that V_j and K_{j+1} have landed before they signal P, and the last
+// query tile's softmax releases the ring stages (its S commit covers every
+// earlier product).
+// Softmax per tile: the 128 scores of the row with one TMEM load wait; the
+// first KV tile fixes m (its row maximum); later ones keep it unless a row's
+// sum of P over the tile reaches kGrowSum, which moves m up to the row's
+// maximum, rescales O_t and l and recomputes the tile's P; P =
 // 2^(s*scale - m) as bf16 into TMEM with tcgen05.st, row sum l.  At the end
 // o = O_t / l.  Keys past the end are -inf in S and zero in V (TMA zero
 // fill).  All waits are bounded; a wait that runs out records a code in the
@@ -48,10 +56,10 @@ namespace {
 constexpr int BQ = 128, BKV = 128, ATT_THREADS = 384;
 constexpr uint32_t ATT_TMEM_COLS = 512;
 // A query tile keeps the row maximum m of its first KV tile until a row's
-// scaled scores exceed it by more than this (log2 units): P then stays below
-// 2^64, far from the fp32 and bf16 range limits (without loss of relative
-// precision), and O needs no rescaling in the common case.
-constexpr float kGrowLimit = 64.f;
+// sum of P over one KV tile reaches this (2^64): every P of a kept tile is
+// then below 2^64, far from the fp32 and bf16 range limits (without loss of
+// relative precision), and O needs no rescaling in the common case.
+constexpr float kGrowSum = 18446744073709551616.f;
 
 template <int HD>
 struct AttLayout {
@@ -65,6 +73,22 @@ struct AttLayout {
   static constexpr int OFF_BAR = OFF_KV + NS * KV_BYTES;
   static constexpr int SMEM = OFF_BAR + 512 + 1024;    // barriers + alignment slack
 };
+
+// Register budget per thread after the split (setmaxnreg): the issue
+// warpgroup gives up what the two softmax warpgroups take, so the total stays
+// the launch's 384 x 168.
+constexpr int kRegsLaunch = 168, kRegsIssue = 120, kRegsSoftmax = 192;
+static_assert(kRegsIssue * 128 + kRegsSoftmax * 256 == kRegsLaunch * ATT_THREADS,
+              "register split must add up to the launch's registers");
+
+template <int N>
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 __device__ __forceinline__ void att_fail(int* err, volatile int* abort, int code) {
   atomicCAS(err, 0, *abort ? static_cast<int>(DEV_ABORTED) : code);
@@ -105,19 +129,58 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
 
-// Maximum of the first n (clamped to 0..32) of 32 fp32 scores; -inf if none.
-__device__ __forceinline__ float masked_max(const uint32_t (&sr)[32], int n) {
-  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+// The 128 fp32 scores of this thread's row (TMEM lane) from taddr: four
+// loads, one wait.  Scores of keys at or past `valid` become -inf.
+__device__ __forceinline__ void load_row(uint32_t taddr, int valid, uint32_t (&sr)[BKV]) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i)
-    if (i < n) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(sr[i]));
+  for (int c = 0; c < BKV / 32; ++c)
+    tmem_ld_32x32b_x32(taddr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c]));
+  tmem_ld_wait();
+  if (valid < BKV) {
+#pragma unroll
+    for (int i = 0; i < BKV; ++i)
+      if (i >= valid) sr[i] = __float_as_uint(-INFINITY);
+  }
+}
+
+// Maximum of a row's 128 scores (-inf if all are).
+__device__ __forceinline__ float row_max(const uint32_t (&sr)[BKV]) {
+  float mx[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) mx[e] = __uint_as_float(sr[e]);
+#pragma unroll
+  for (int i = 4; i < BKV; i += 8)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      mx[e] = fmax3(mx[e], __uint_as_float(sr[i + e]),
+                    i + 4 + e < BKV ? __uint_as_float(sr[i + 4 + e]) : -INFINITY);
   return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+// P = 2^(s * scale - m) for a row's 128 scores, as 64 bf16 pairs written
+// over sr[0..63] (pair h from scores 2h, 2h+1, which no later pair reads);
+// returns the row sum of P (fp32, before the bf16 rounding), accumulated in
+// four packed pairs of partial sums.
+__device__ __forceinline__ float exp_row(uint32_t (&sr)[BKV], float m, float scale_log2) {
+  const uint64_t sc2 = f2(scale_log2, scale_log2), nm2 = f2(-m, -m);
+  uint64_t ls[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int h = 0; h < BKV / 2; ++h) {
+    const uint64_t x = f2_fma(f2(__uint_as_float(sr[2 * h]), __uint_as_float(sr[2 * h + 1])),
+                              sc2, nm2);
+    const uint64_t pp = f2(ex2_approx(f2_lo(x)), ex2_approx(f2_hi(x)));
+    ls[h & 3] = f2_add(ls[h & 3], pp);
+    sr[h] = pack_bf16(f2_lo(pp), f2_hi(pp));
+  }
+  const uint64_t l2 = f2_add(f2_add(ls[0], ls[1]), f2_add(ls[2], ls[3]));
+  return f2_lo(l2) + f2_hi(l2);
 }
 
 // Multiplies this warp's 32 lanes x (32 * CHUNKS) fp32 columns from taddr by
@@ -135,18 +198,41 @@ __device__ __forceinline__ void rescale_tmem_f32(uint32_t taddr, float corr) {
   }
 }
 
-// Multiplies 16 columns of bf16 pairs from taddr by each lane's corr.
-__device__ __forceinline__ void rescale_tmem_bf16x2(uint32_t taddr, float corr) {
-  uint32_t r[32];
-  tmem_ld_32x32b_x32(taddr, r);              // columns taddr..taddr+31; the
-  tmem_ld_wait();                            // first 16 are the P chunk
-  uint32_t q[16];
-#pragma unroll
-  for (int h = 0; h < 16; ++h) {
-    const float lo = __uint_as_float(r[h] << 16), hi = __uint_as_float(r[h] & 0xFFFF0000u);
-    q[h] = pack_bf16(lo * corr, hi * corr);
-  }
-  tmem_st_32x32b_x16(taddr, q);
+// Four back-to-back kind::f16 products into one accumulator, both operands
+// in shared memory (descriptors a[i], b[i]); the first accumulates only if
+// acc != 0, the other three always.  One asm block, so that no other
+// instruction of the issuing thread sits between the products: the tensor
+// pipe's issue queue is shallow, and each instruction between two products
+// is tensor time lost.
+__device__ __forceinline__ void umma_ss_x4(uint32_t d, const uint64_t (&a)[4],
+                                           const uint64_t (&b)[4], uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %9, 0;\n\t"
+      "setp.eq.b32 q, %9, %9;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %10, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %10, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %10, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %10, q;\n\t}" ::"r"(d),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]),
+      "r"(acc), "r"(idesc)
+      : "memory");
+}
+
+// The same with the A operands in tensor memory (column addresses ta[i]).
+__device__ __forceinline__ void umma_ts_x4(uint32_t d, const uint32_t (&ta)[4],
+                                           const uint64_t (&b)[4], uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.b32 p, %9, 0;\n\t"
+      "setp.eq.b32 q, %9, %9;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %10, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %10, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %10, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %10, q;\n\t}" ::"r"(d),
+      "r"(ta[0]), "r"(ta[1]), "r"(ta[2]), "r"(ta[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]),
+      "r"(acc), "r"(idesc)
+      : "memory");
 }
 
 template <int HD>
@@ -223,6 +309,9 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
   const uint32_t tO = tmem + 256;       // O_t at column 256 + HD t
 
   if (wg == 2) {
+    // the loader and MMA issuer need few registers; the softmax warpgroups
+    // take them (launch 384 x 168 = 128 x 120 + 256 x 192)
+    reg_dealloc<kRegsIssue>();
     if (warp == 8 && lane == 0) {
       // load i = 2j is K_j, i = 2j+1 is V_j; stage i % NS, use i / NS
       mbar_arrive_expect_tx(q_full, nt * L::Q_TILE);
@@ -273,25 +362,35 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
       auto wait_load = [&](int i) {
         return mbar_wait_spin(&full[i % NS], static_cast<uint32_t>((i / NS) & 1), abort);
       };
-      // S_t = Q_t K^T with K in stage s
+      // S_t = Q_t K^T with K in stage s, in groups of four products
       auto mma_s = [&](int t, int s) {
         const uint64_t a = dq + static_cast<uint64_t>((t * L::Q_TILE) >> 4);
         const uint64_t b = dkv + static_cast<uint64_t>((s * L::KV_BYTES) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16(tS + t * BKV, a + (((kk >> 2) * (BQ * 128) + (kk & 3) * 32) >> 4),
-                    b + (((kk >> 2) * L::K_CHUNK + (kk & 3) * 32) >> 4), idesc_s,
-                    kk > 0 ? 1u : 0u);
+        for (int g = 0; g < HD / 64; ++g) {
+          uint64_t ad[4], bd[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            ad[e] = a + static_cast<uint64_t>((g * (BQ * 128) + e * 32) >> 4);
+            bd[e] = b + static_cast<uint64_t>((g * L::K_CHUNK + e * 32) >> 4);
+          }
+          umma_ss_x4(tS + t * BKV, ad, bd, idesc_s, g > 0 ? 1u : 0u);
+        }
       };
       // O_t += P_t V with V^T in stage s
       auto mma_pv = [&](int t, int s, bool acc) {
         const uint64_t b = dkv + static_cast<uint64_t>((s * L::KV_BYTES) >> 4);
-        const uint32_t first = acc ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk)
-          umma_bf16_tmem_a(tO + t * HD, tS + t * BKV + kk * 8,
-                           b + (((kk >> 2) * L::V_CHUNK + (kk & 3) * 32) >> 4), idesc_o,
-                           kk > 0 ? 1u : first);
+        for (int g = 0; g < BKV / 64; ++g) {
+          uint32_t ta[4];
+          uint64_t bd[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            ta[e] = tS + t * BKV + (4 * g + e) * 8;
+            bd[e] = b + static_cast<uint64_t>((g * L::V_CHUNK + e * 32) >> 4);
+          }
+          umma_ts_x4(tO + t * HD, ta, bd, idesc_o, g > 0 || acc ? 1u : 0u);
+        }
       };
       bool ok = mbar_wait_bounded(q_full, 0, abort) && wait_load(0);
       if (ok) {
@@ -302,77 +401,45 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
           mma_s(1, 0);
           umma_commit(&s_full[1]);
         }
-        umma_commit(&empty[0]);
       }
-      // The barriers a group needs are tested (non-blocking) while the
-      // previous group's MMAs issue and the result is used after them, so
-      // the shared-memory reads overlap MMA issue; only a barrier found not
-      // ready is waited on.  pre0 / pre1: PV_0 / PV_1's inputs known ready.
-      auto test_load = [&](int i) {
-        return mbar_test(&full[i % NS], static_cast<uint32_t>((i / NS) & 1));
-      };
-      // pre0 also covers K_{j+1}; without it, the loads (almost always
-      // ready) are checked before the wait for P, so that only that one
-      // barrier read stands between the softmax finishing and the PV issue.
-      auto next_ready = [&](int ik_next) {
-        return test_load(ik_next - 1) && (ik_next >= 2 * n_kv || test_load(ik_next));
-      };
-      bool pre0 = false, pre1 = false;
+      // The MMA thread's own barrier reads, fences and commits cost
+      // tensor-pipe time (the issue queue is shallow), so it keeps one of
+      // each per query tile and KV tile: it waits only for P_t(j), whose
+      // softmax warps have first checked that V_j and K_{j+1} landed, and
+      // commits only the S_t(j+1) (or final O_t) signal; the softmax of the
+      // last query tile releases the K/V stages.
+      int sv = 1 % NS, sk = 2 % NS;              // stages of V_j and K_{j+1}
       for (int j = 0; ok && j < n_kv; ++j) {
         const uint32_t par = static_cast<uint32_t>(j & 1);
-        const int iv = 2 * j + 1, ik = 2 * j + 2;
         const bool more = j + 1 < n_kv;
-        bool k_ready = more;
-        if (!pre0) {
-          if (!wait_load(iv)) {
-            ok = false;
-            break;
-          }
-          k_ready = more && test_load(ik);
-          if (!mbar_wait_spin(&p_full[0], par, abort)) {
-            ok = false;
-            break;
-          }
-        }
-        tc_fence_after();
-        mma_pv(0, iv % NS, j > 0);
-        if (nt == 1) umma_commit(&empty[iv % NS]);
-        if (more) {
-          if (!k_ready && !wait_load(ik)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const bool nxt = nt == 2 ? mbar_test(&p_full[1], par)
-                                   : mbar_test(&p_full[0], par ^ 1u) && next_ready(ik + 2);
-          mma_s(0, ik % NS);
-          umma_commit(&s_full[0]);
-          if (nt == 1) {
-            umma_commit(&empty[ik % NS]);
-            pre0 = nxt;
-            continue;
-          }
-          pre1 = nxt;
-        } else {
-          umma_commit(&o_done[0]);
-          if (nt == 1) continue;
-          pre1 = false;
-        }
-        if (!pre1 && !mbar_wait_spin(&p_full[1], par, abort)) {
+        if (!mbar_wait_spin(&p_full[0], par, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        mma_pv(1, iv % NS, j > 0);
-        umma_commit(&empty[iv % NS]);
+        mma_pv(0, sv, j > 0);
         if (more) {
-          pre0 = mbar_test(&p_full[0], par ^ 1u) && next_ready(ik + 2);
-          mma_s(1, ik % NS);
-          umma_commit(&empty[ik % NS]);
-          umma_commit(&s_full[1]);
+          mma_s(0, sk);
+          umma_commit(&s_full[0]);
         } else {
-          umma_commit(&o_done[1]);
+          umma_commit(&o_done[0]);
         }
+        if (nt == 2) {
+          if (!mbar_wait_spin(&p_full[1], par, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_pv(1, sv, j > 0);
+          if (more) {
+            mma_s(1, sk);
+            umma_commit(&s_full[1]);
+          } else {
+            umma_commit(&o_done[1]);
+          }
+        }
+        sv = sv + 2 >= NS ? sv + 2 - NS : sv + 2;
+        sk = sk + 2 >= NS ? sk + 2 - NS : sk + 2;
       }
       if (!ok) {
         att_fail(err, abort, DEV_TIMEOUT_MMA_FULL);
@@ -382,6 +449,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
       }
     }
   } else if (wg < nt) {
+    reg_alloc<kRegsSoftmax>();
     const int t = wg;                          // query tile of this warpgroup
     const int quad = warp & 3;
     const int row = quad * 32 + lane;          // query row in the tile == TMEM lane
@@ -397,74 +465,75 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm_qk,
         break;
       }
       tc_fence_after();
-      const int valid = tokens - (kv_base + j) * BKV;   // keys of this tile that exist
-      if (j == 0) {
-        // the first KV tile fixes m: its row maximum, read chunk by chunk
-        float mx = -INFINITY;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sr[32];
-          tmem_ld_32x32b_x32(tSt + c * 32, sr);
-          tmem_ld_wait();
-          mx = fmaxf(mx, masked_max(sr, valid - c * 32));
-        }
-        m = mx * scale_log2;
+      // S_t(j) complete: for the last query tile this commit also covers
+      // PV(j-1) and S(j) of every tile, so the stages of V_{j-1} and K_j are
+      // free for the loader
+      if (t == nt - 1 && quad == 0 && lane == 0) {
+        if (j > 0) mbar_arrive(&empty[(2 * j - 1) % NS]);
+        mbar_arrive(&empty[(2 * j) % NS]);
       }
-      // P = exp2(s * scale - m) as bf16 pairs over the first 64 columns of
-      // S_t, 32 scores at a time (chunk c of P lands on columns 16c..16c+15,
-      // which chunk c/2 of S, already read, occupied); the row sum in four
-      // packed pairs of partial sums
-      uint64_t ls[4] = {0, 0, 0, 0};
-      const uint64_t sc2 = f2(scale_log2, scale_log2);
+      // PV_t(j) reads V_j and S_t(j+1) reads K_{j+1}: one thread of the
+      // warpgroup sees both loads complete before the warpgroup signals P
+      // (tested now, waited for only if not yet complete at the end)
+      const int iv = 2 * j + 1, ik = 2 * j + 2;
+      const bool more = j + 1 < n_kv;
+      const bool chk = quad == 0 && lane == 0;
+      bool loads_ok = true;
+      if (chk) {
+        const bool v_ok = mbar_test(&full[iv % NS], static_cast<uint32_t>((iv / NS) & 1));
+        const bool k_ok = !more || mbar_test(&full[ik % NS], static_cast<uint32_t>((ik / NS) & 1));
+        loads_ok = v_ok && k_ok;
+      }
+      const int valid = tokens - (kv_base + j) * BKV;   // keys of this tile that exist
+      // the whole row of S_t at once: one TMEM load wait per KV tile
+      uint32_t sr[BKV];
+      load_row(tSt, valid, sr);
+      if (j == 0) m = row_max(sr) * scale_log2;   // the first KV tile fixes m
+      // P = exp2(s * scale - m) as bf16 pairs, then its row sum
+      float lt = exp_row(sr, m, scale_log2);
+      // A row whose scores outgrew m (its P sum reached kGrowSum, or is not
+      // finite) moves m up to its maximum and redoes the tile: O_t (PV_t(j-1)
+      // has completed: it precedes S_t(j) in issue order) and l are scaled
+      // by 2^(m_old - m_new) and P is recomputed from S_t, still in TMEM.
+      if (__any_sync(0xffffffffu, !(lt < kGrowSum))) {
+        const bool need = !(lt < kGrowSum);
+        float cm = -INFINITY;                 // the row maximum, 32 scores at a time
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32];
-        tmem_ld_32x32b_x32(tSt + c * 32, sr);
-        tmem_ld_wait();
-        const int vc = valid - c * 32;
-        if (vc < 32) {
+        for (int c = 0; c < BKV / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tSt + c * 32, r);
+          tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (i >= vc) sr[i] = __float_as_uint(-INFINITY);
+            if (32 * c + i < valid) cm = fmaxf(cm, __uint_as_float(r[i]));
         }
-        if (j > 0) {
-          // a row whose scores outgrow m by more than kGrowLimit moves m up:
-          // O_t (PV_t(j-1) has completed: it precedes S_t(j) in issue
-          // order), l, this tile's partial sums and its P chunks so far are
-          // scaled by 2^(m_old - m_new)
-          const float cm = masked_max(sr, 32) * scale_log2;
-          const bool need = cm > m + kGrowLimit;
-          if (__any_sync(0xffffffffu, need)) {
-            tmem_st_wait();                    // P chunks so far are in TMEM
-            const float corr = need ? ex2_approx(m - cm) : 1.f;
-            if (need) m = cm;
-            l *= corr;
-            const uint64_t corr2 = f2(corr, corr);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) ls[e] = f2_mul(ls[e], corr2);
-            rescale_tmem_f32<HD / 32>(tOt, corr);
-#pragma unroll 1
-            for (int pc = 0; pc < c; ++pc) rescale_tmem_bf16x2(tSt + pc * 16, corr);
-            tmem_st_wait();
-          }
+        cm *= scale_log2;
+        float corr = 1.f;
+        if (need && cm > m) {
+          corr = ex2_approx(m - cm);
+          m = cm;
         }
-        const uint64_t nm2 = f2(-m, -m);
-        uint32_t pk[16];
-#pragma unroll
-        for (int h = 0; h < 16; ++h) {
-          const uint64_t x = f2_fma(f2(__uint_as_float(sr[2 * h]), __uint_as_float(sr[2 * h + 1])),
-                                    sc2, nm2);
-          const uint64_t pp = f2(ex2_approx(f2_lo(x)), ex2_approx(f2_hi(x)));
-          ls[h & 3] = f2_add(ls[h & 3], pp);
-          pk[h] = pack_bf16(f2_lo(pp), f2_hi(pp));
-        }
-        tmem_st_32x32b_x16(tSt + c * 16, pk);
+        l *= corr;
+        rescale_tmem_f32<HD / 32>(tOt, corr);
+        load_row(tSt, valid, sr);
+        lt = exp_row(sr, m, scale_log2);
       }
-      const uint64_t l2 = f2_add(f2_add(ls[0], ls[1]), f2_add(ls[2], ls[3]));
-      l += f2_lo(l2) + f2_hi(l2);
+      // P over the first 64 columns of S_t
+      tmem_st_32x32b_x32(tSt, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
+      tmem_st_32x32b_x32(tSt + 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[32]));
+      l += lt;
+      if (chk && !loads_ok) {
+        loads_ok = mbar_wait_bounded(&full[iv % NS], static_cast<uint32_t>((iv / NS) & 1), abort) &&
+                   (!more ||
+                    mbar_wait_bounded(&full[ik % NS], static_cast<uint32_t>((ik / NS) & 1), abort));
+        if (!loads_ok) att_fail(err, abort, DEV_TIMEOUT_ATTN);
+      }
       tmem_st_wait();
       tc_fence_before();
-      __syncwarp();
+      if (!__all_sync(0xffffffffu, loads_ok)) {
+        ok = false;
+        break;
+      }
       if (lane == 0) mbar_arrive(&p_full[t]);
     }
     if (ok && !__all_sync(0xffffffffu, mbar_wait_bounded(&o_done[t], 0, abort))) {
@@ -591,6 +660,7 @@ transpose_v_kernel(const uint16_t* __restrict__ qkv, int tokens, int d, uint16_t
 }
 
 cudaError_t g_att_err = cudaSuccess;
+int g_att_regs[2] = {0, 0};          // registers per thread of <64>, <128>
 std::once_flag g_att_once;
 
 void set_att_attrs() {
@@ -601,16 +671,33 @@ void set_att_attrs() {
     cudaError_t e1 = cudaFuncSetAttribute(attention_tc_kernel<128>,
                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           AttLayout<128>::SMEM);
-    g_att_err = e0 != cudaSuccess ? e0 : e1;
+    cudaFuncAttributes a64{}, a128{};
+    cudaError_t e2 = cudaFuncGetAttributes(&a64, attention_tc_kernel<64>);
+    cudaError_t e3 = cudaFuncGetAttributes(&a128, attention_tc_kernel<128>);
+    g_att_regs[0] = a64.numRegs;
+    g_att_regs[1] = a128.numRegs;
+    g_att_err = e0 != cudaSuccess ? e0 : e1 != cudaSuccess ? e1 : e2 != cudaSuccess ? e2 : e3;
   });
+}
+
+// The register split inside the kernel (setmaxnreg) redistributes exactly
+// the registers the CTA is launched with; a build that gave the kernel any
+// other count would leave the softmax warpgroups waiting for registers that
+// do not exist, so it is refused before launch.
+dlo_status check_att_attrs() {
+  set_att_attrs();
+  DLO_CUDA(g_att_err);
+  if (g_att_regs[0] != kRegsLaunch || g_att_regs[1] != kRegsLaunch)
+    DLO_FAIL(DLO_ERR_CUDA, "attention: kernel built with %d / %d registers per thread, the "
+             "register split needs %d", g_att_regs[0], g_att_regs[1], kRegsLaunch);
+  return DLO_OK;
 }
 
 template <int HD>
 dlo_status launch_hd(const CUtensorMap& tm_qk, const CUtensorMap& tm_vt, const AttPlan& pl,
                      int64_t tokens, int64_t d, int64_t heads, uint16_t* o, float* ws, int* err,
                      cudaStream_t stream) {
-  set_att_attrs();
-  DLO_CUDA(g_att_err);
+  DLO_TRY(check_att_attrs());
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
   const int n_split = static_cast<int>(pl.items - pl.n_main);
   DLO_CUDA(launch_kernel(attention_tc_kernel<HD>, dim3(static_cast<unsigned>(pl.units)),
@@ -665,11 +752,7 @@ AttPlan attention_plan(int64_t batch, int64_t tokens, int64_t d, int64_t heads) 
   return p;
 }
 
-dlo_status attention_preload() {
-  set_att_attrs();
-  DLO_CUDA(g_att_err);
-  return DLO_OK;
-}
+dlo_status attention_preload() { return check_att_attrs(); }
 
 dlo_status launch_attention_vt(const uint16_t* qkv, const uint16_t* vt, int64_t vt_ld,
                                int64_t batch, int64_t tokens, int64_t d, int64_t heads,
