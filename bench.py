@@ -465,7 +465,7 @@ def run_ours(args, ws, rank, local):
     from layerwise_weight_offload_gb300 import dlo, workloads as W
     apply_gemm_pair(dlo, args)
     from layerwise_weight_offload_gb300.stack import (HostBlocks, StreamedStack, ResidentStack,
-                                                      PinnedIO)
+                                                      PinnedIO, IOHealer)
 
     torch.cuda.set_device(local)
     w = W.CONFIGS[args.config]
@@ -677,16 +677,12 @@ def run_ours(args, ws, rank, local):
                  for _ in range(args.steps)]
         step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
         in_q = st.copy if hasattr(st, "copy") else data
-        # Host ranges can turn slow after the check above, during the pass;
+        # Host ranges can turn slow after the check above, during the pass:
         # the input and result copies that have completed are read after each
-        # step is queued (no wait on the GPU), and a buffer whose copy took
-        # over 4x the link time (and 2 ms) moves to fresh huge-page ranges
-        # (PinnedBuffer.relocate keeps the old place intact, so the copies
-        # already queued from or into it stay valid); later copies use the
-        # new place.  At most two moves per buffer.
-        link_ms = xb / (ceiling * 1e6)
-        slow_ms = max(2.0, 4.0 * link_ms)
-        io_moves, io_moved = [], [0, 0, 0]
+        # step is queued (no wait on the GPU), and a buffer whose copy ran
+        # over 4x the link time moves to fresh huge-page ranges (IOHealer);
+        # the copies queued after the move use the new place.
+        io_healer = IOHealer(io, ceiling)
         io_checked = 0
 
         def io_heal(upto):
@@ -694,17 +690,11 @@ def run_ours(args, ws, rank, local):
             while io_checked < upto and io_ev[io_checked][3].query():
                 k = io_checked
                 io_checked += 1
-                times = ((0, io_ev[k][0].elapsed_time(io_ev[k][1])),
-                         (1 + (k & 1), io_ev[k][2].elapsed_time(io_ev[k][3])))
-                for i, ms in times:
-                    if ms <= slow_ms or io_moved[i] >= 2:
+                times = [(0, io_ev[k][0].elapsed_time(io_ev[k][1])),
+                         (1 + (k & 1), io_ev[k][2].elapsed_time(io_ev[k][3]))]
+                for i in io_healer.observe(times):
+                    if not io_healer.move(k, i, dict(times)[i], 0.25 * ceiling):
                         continue
-                    io_moved[i] += 1
-                    new = io.buf.relocate([(io.offs[i], xb)], 0.25 * ceiling)
-                    io_moves.append([k, i, round(ms, 2), new is not None])
-                    if new is None:
-                        continue
-                    io.offs[i] = new[0]
                     if i == 0:
                         xh = io.tensor(0, x0.shape, x0.dtype)
                     else:
@@ -794,7 +784,7 @@ def run_ours(args, ws, rank, local):
                               "h2d_gbs": [round(a, 1) for a, _ in io_rates],
                               "d2h_gbs": [round(b, 1) for _, b in io_rates],
                               "relocated": io.relocated, "failed": io.failed,
-                              "moved_during_pass": io_moves,
+                              "moved_during_pass": io_healer.log,
                               "moved_note": "(step, buffer 0 = input / 1, 2 = results, copy ms, "
                                             "new place fast)"},
                "note": "h2d counts x plus every streamed weight shard of the step; x in and "

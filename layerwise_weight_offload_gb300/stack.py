@@ -614,6 +614,46 @@ class HostBlocks:
         self.buf.close()
 
 
+class IOHealer:
+    """Watches the copies of a step's input and result buffers (PinnedIO)
+    while a pass runs.  Host ranges can turn slow after PinnedIO.verify,
+    during the pass: a buffer whose copy took over `factor` times the link
+    time for its bytes (and at least `min_ms`) is named for a move, at most
+    `max_moves` times per buffer.  PinnedBuffer.relocate keeps the old place
+    intact, so the copies already queued from or into it stay valid and only
+    the copies queued after the move use the new place."""
+
+    def __init__(self, io, link_gbs, factor=4.0, min_ms=2.0, max_moves=2):
+        self.io = io
+        self.slow_ms = max(min_ms, factor * io.nbytes / (link_gbs * 1e6))
+        self.max_moves = max_moves
+        self.moved = [0] * io.count
+        self.log = []
+
+    def observe(self, times):
+        """times: [(buffer index, copy ms)] of one completed step; returns
+        the buffers to move, in order (slow, each named once, and moved
+        fewer than max_moves times so far)."""
+        out = []
+        for i, ms in times:
+            if ms > self.slow_ms and self.moved[i] < self.max_moves and i not in out:
+                out.append(i)
+        return out
+
+    def move(self, step, i, ms, min_gbs):
+        """Moves buffer i to fresh huge-page ranges (contents kept); True if
+        the new place streams at min_gbs.  Logged as (step, buffer, copy ms,
+        new place fast)."""
+        self.moved[i] += 1
+        new = self.io.buf.relocate([(self.io.offs[i], self.io.nbytes)], min_gbs,
+                                   device=self.io.device)
+        self.log.append([step, i, round(ms, 2), new is not None])
+        if new is None:
+            return False
+        self.io.offs[i] = new[0]
+        return True
+
+
 class CopyHealer:
     """Names the host blocks whose prefetches have turned slow, from the
     engine's copy log: a copy is slow when its rate is below the median rate

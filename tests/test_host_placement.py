@@ -136,3 +136,54 @@ def test_healer_names_a_block_after_one_severely_slow_copy():
     assert h2.observe(_records(64, [(1, 90.0)])) == [1]
     h2.moved(1)
     assert h2.observe(_records(65, [(1, 90.0)])) == []
+
+
+class _FakeIOBuf:
+    """PinnedBuffer.relocate stand-in: hands out the next offsets, or fails."""
+
+    def __init__(self, fail=()):
+        self.calls, self.fail, self.next = [], set(fail), 1 << 40
+
+    def relocate(self, pieces, min_gbs, device="cuda"):
+        self.calls.append((pieces, min_gbs))
+        if len(self.calls) in self.fail:
+            return None
+        self.next += 1 << 30
+        return [self.next]
+
+
+class _FakeIO:
+    def __init__(self, fail=()):
+        self.nbytes, self.count, self.device = 201_326_592, 3, "cuda"
+        self.offs = [0, 1 << 29, 2 << 29]
+        self.buf = _FakeIOBuf(fail)
+
+
+def test_io_healer_names_slow_copies_and_moves_each_buffer_at_most_twice():
+    from layerwise_weight_offload_gb300.stack import IOHealer
+    io = _FakeIO()
+    h = IOHealer(io, link_gbs=211.0)
+    # a 201 MB copy takes 0.954 ms at 211 GB/s: the limit is 4x that (over
+    # the 2 ms floor)
+    assert abs(h.slow_ms - 4.0 * io.nbytes / 211e6) < 1e-9
+    assert h.observe([(0, 0.96), (1, 1.19)]) == []
+    assert h.observe([(0, 3.8), (2, 2.5)]) == []             # under the limit: not slow
+    assert h.observe([(0, 39.1), (2, 53.6)]) == [0, 2]
+    assert h.move(3, 0, 39.1, 50.0) and h.move(3, 2, 53.6, 50.0)
+    assert io.offs[0] == (1 << 40) + (1 << 30) and io.offs[2] == (1 << 40) + (2 << 30)
+    assert io.buf.calls[0] == ([(0, io.nbytes)], 50.0)
+    assert h.observe([(0, 40.0)]) == [0]
+    h.move(4, 0, 40.0, 50.0)
+    assert h.observe([(0, 40.0), (1, 30.0)]) == [1]          # buffer 0 moved twice already
+    assert h.log == [[3, 0, 39.1, True], [3, 2, 53.6, True], [4, 0, 40.0, True]]
+
+
+def test_io_healer_keeps_the_old_place_when_the_new_one_is_slow():
+    from layerwise_weight_offload_gb300.stack import IOHealer
+    io = _FakeIO(fail={1})
+    h = IOHealer(io, link_gbs=211.0, factor=4.0, min_ms=5.0)
+    assert h.slow_ms == 5.0                                   # the floor, over 4x the link time
+    assert not h.move(0, 1, 9.0, 50.0)
+    assert io.offs[1] == 1 << 29                              # unchanged
+    assert h.log == [[0, 1, 9.0, False]]
+    assert h.observe([(1, 9.0)]) == [1]                       # one move of two used
