@@ -70,10 +70,23 @@ __device__ __forceinline__ void record_failure(int* err, volatile int* abort, in
   *abort = 1;
 }
 
+// GELU in its tanh form, 0.5 z (1 + tanh(u)) with u = sqrt(2/pi) (z + 0.044715
+// z^3), computed through the identity 0.5 (1 + tanh(u)) = 1 / (1 + e^(-2u)):
+// z / (1 + 2^(-2u log2 e)) with the hardware exp2 and reciprocal
+// approximations (a few ulp relative, on both tails: the result goes to 0
+// for large negative z and to z for large positive z).  The full-precision
+// tanhf costs dozens of instructions per element, and four epilogue warps
+// doing that saturate the SM sub-partitions that the loader and the MMA
+// issuer share with them.
 __device__ __forceinline__ float gelu_tanh(float z) {
   const float k0 = 0.7978845608028654f;   // sqrt(2/pi)
   const float k1 = 0.044715f;
-  return 0.5f * z * (1.f + tanhf(k0 * (z + k1 * z * z * z)));
+  const float m2log2e = -2.8853900817779268f;   // -2 log2(e)
+  const float u = k0 * fmaf(k1 * z * z, z, z);
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(u * m2log2e));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+  return z * r;
 }
 
 // r[i] (fp32 bits) += bias[n0 + i] for the columns below N (N a multiple of 8).
