@@ -50,7 +50,7 @@ DEFAULT_CONFIG = "super"
 # shape (M, K, N, on CTA pairs): python bench.py --only fc2 --config super
 # --reps 3, then ncu --set full --clock-control none -k regex:gemm_pair -s 2
 # -c 1 on the same command (4.343 GB read, 0.194 GB written)
-FC2_DRAM_BYTES = {(8192, 24576, 6144, True): 4_343_431_000 + 194_273_024}
+FC2_DRAM_BYTES = {(8192, 24576, 6144, True): 3_064_119_000 + 189_118_720}
 REGIONS = 5          # timed regions per pass; value is the median region
 
 
